@@ -1,0 +1,297 @@
+"""fp64 CPU oracle: gated causal softmax attention, prefill forward/backward and paged
+fp8 decode (test infrastructure only).
+
+Sources (page title, section):
+  [FLA] fla-org/flash-linear-attention issue #1322, "[Perf] Gluon attention backend with
+        large head dimensions": Description (the causal attention contract: dense and
+        packed variable-length inputs, MHA/GQA/MQA, unequal query/key and value dims,
+        logarithmic gates, sliding windows, sink bias, gradients); comment of Oct 3
+        (sink gradient from the backward probabilities, in fp32, not from rounded O).
+  [AIT] ROCm/aiter PR #6660 (gfx1250 unified attention): commit messages and "Technical
+        details" (per-token K/V scales laid out [num_blocks, num_kv_heads, block_size];
+        K scales multiply QK columns, V scales multiply P columns after the row sum,
+        slots past seq_len get scale 0; split-K over context segments with an
+        LSE-weighted reduce where empty partials, M = -inf, weigh 0).
+
+Readings where the pages leave a step open (each is also listed in the design notes):
+  * score s_ij = scale * q_i.k_j + G_i - G_j, G = per-sequence inclusive cumsum of the
+    per-token, per-query-head log gates; the gate is not multiplied by the scale.
+  * window W > 0 keeps key j for query i iff 0 <= i - j < W; W = 0 means no window.
+  * the sink is one logit per query head, present only in the softmax denominator.
+  * LSE includes the sink term; the sink gradient is summed over every token of every
+    sequence in the batch.
+  * decode: query row t of a request with q_len rows sits at position L - q_len + t and
+    sees keys 0..L - q_len + t (bottom-right causal alignment).
+
+Everything runs in float64 with dense per-(sequence, head) matrices; no blocking, no
+online softmax, no fusion.  Inputs are float64 arrays (bf16 / fp32 inputs widened
+exactly) and uint8 e4m3 codes for the cache.
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional
+
+import numpy as np
+
+from .formats import e4m3_decode
+
+
+def _seq_bounds(cu_seqlens):
+    cu = [int(x) for x in np.asarray(cu_seqlens).tolist()]
+    return [(cu[i], cu[i + 1]) for i in range(len(cu) - 1)]
+
+
+def gate_cumsum(log_gate: np.ndarray, cu_seqlens) -> np.ndarray:
+    """G_t = sum of g_u over u = start(seq) .. t, per sequence and head ([FLA] Description,
+    "logarithmic gates"; inclusive cumsum restarted at every sequence start)."""
+    g = np.asarray(log_gate, dtype=np.float64)
+    G = np.zeros_like(g)
+    for a, b in _seq_bounds(cu_seqlens):
+        G[a:b] = np.cumsum(g[a:b], axis=0)
+    return G
+
+
+def _allowed(T: int, window: int) -> np.ndarray:
+    """Mask of visible (i, j) pairs inside one sequence: causal j <= i, and i - j < W."""
+    i = np.arange(T)[:, None]
+    j = np.arange(T)[None, :]
+    m = j <= i
+    if window > 0:
+        m &= (i - j) < window
+    return m
+
+
+def _scores(qh, kh, scale, Gh, allowed):
+    S = scale * (qh @ kh.T)
+    if Gh is not None:
+        S = S + (Gh[:, None] - Gh[None, :])
+    return np.where(allowed, S, -np.inf)
+
+
+def _softmax_with_sink(S, sink_h):
+    """P_ij = e^{s_ij} / Z_i and p_sink,i = e^{sigma} / Z_i with
+    Z_i = sum_j e^{s_ij} (+ e^{sigma}); returns P, p_sink (or None), ln Z."""
+    m = S.max(axis=1)
+    if sink_h is not None:
+        m = np.maximum(m, sink_h)
+    E = np.exp(S - m[:, None])
+    Z = E.sum(axis=1)
+    ps = None
+    if sink_h is not None:
+        es = np.exp(sink_h - m)
+        Z = Z + es
+        ps = es / Z
+    P = E / Z[:, None]
+    return P, ps, m + np.log(Z)
+
+
+def prefill_forward(q, k, v, cu_seqlens, scale, log_gate=None, sink=None, window=0):
+    """Causal softmax attention forward ([FLA] Description).
+
+    q [tot, hq, dqk], k [tot, hkv, dqk], v [tot, hkv, dv]; query head h reads kv head
+    h // (hq // hkv).  Returns o [tot, hq, dv] and lse [hq, tot] (natural log, sink
+    included).
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    tot, hq, _ = q.shape
+    hkv, dv = k.shape[1], v.shape[2]
+    group = hq // hkv
+    G = gate_cumsum(log_gate, cu_seqlens) if log_gate is not None else None
+    sink = None if sink is None else np.asarray(sink, np.float64)
+    o = np.zeros((tot, hq, dv))
+    lse = np.zeros((hq, tot))
+    for a, b in _seq_bounds(cu_seqlens):
+        if b == a:
+            continue
+        allowed = _allowed(b - a, window)
+        for h in range(hq):
+            kvh = h // group
+            S = _scores(q[a:b, h], k[a:b, kvh], scale, None if G is None else G[a:b, h], allowed)
+            P, _, L = _softmax_with_sink(S, None if sink is None else sink[h])
+            o[a:b, h] = P @ v[a:b, kvh]
+            lse[h, a:b] = L
+    return o, lse
+
+
+def prefill_backward(q, k, v, do, cu_seqlens, scale, log_gate=None, sink=None, window=0):
+    """Analytic gradients of L = sum(O * dO) ([FLA] Description "gradients"; Oct 3 comment
+    for the sink).
+
+      dP_ij = dO_i . v_j,   D_i = sum_j P_ij dP_ij,   dS_ij = P_ij (dP_ij - D_i)
+      dq_i = scale sum_j dS_ij k_j;   dk_j, dv_j summed over the query heads of the group
+      dG_t = sum_j dS_tj - sum_i dS_it,   dg_t = sum_{u >= t, same sequence} dG_u
+      dsigma_h = - sum over all sequences and rows of p_sink,i * D_i
+
+    Returns dq, dk, dv, dg (or None), dsink (or None).
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    do = np.asarray(do, np.float64)
+    tot, hq, dqk = q.shape
+    hkv, dv_ = k.shape[1], v.shape[2]
+    group = hq // hkv
+    G = gate_cumsum(log_gate, cu_seqlens) if log_gate is not None else None
+    sink = None if sink is None else np.asarray(sink, np.float64)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    dg = np.zeros((tot, hq)) if G is not None else None
+    dsink = np.zeros(hq) if sink is not None else None
+    for a, b in _seq_bounds(cu_seqlens):
+        if b == a:
+            continue
+        allowed = _allowed(b - a, window)
+        for h in range(hq):
+            kvh = h // group
+            S = _scores(q[a:b, h], k[a:b, kvh], scale, None if G is None else G[a:b, h], allowed)
+            P, ps, _ = _softmax_with_sink(S, None if sink is None else sink[h])
+            dP = do[a:b, h] @ v[a:b, kvh].T
+            D = (P * dP).sum(axis=1)
+            dS = P * (dP - D[:, None])
+            dq[a:b, h] = scale * (dS @ k[a:b, kvh])
+            dk[a:b, kvh] += scale * (dS.T @ q[a:b, h])
+            dv[a:b, kvh] += P.T @ do[a:b, h]
+            if dg is not None:
+                dG = dS.sum(axis=1) - dS.sum(axis=0)
+                dg[a:b, h] = np.cumsum(dG[::-1])[::-1]
+            if dsink is not None:
+                dsink[h] -= float((ps * D).sum())
+    return dq, dk, dv, dg, dsink
+
+
+# ----------------------------------------------------------------------------- decode
+def gather_kv(cache_codes, scales, block_table_row, L, kv_head):
+    """Dequantized keys (or values) 0..L-1 of one request and kv head: e4m3 value times
+    the per-token scale ([AIT] Technical details, layout [num_blocks, num_kv_heads,
+    block_size]).  Slots at or past L are never read."""
+    bs = cache_codes.shape[2]
+    npages = (L + bs - 1) // bs
+    blocks = np.asarray(block_table_row[:npages], dtype=np.int64)
+    codes = np.asarray(cache_codes[blocks, kv_head])  # [npages, bs, d]
+    sc = np.asarray(scales[blocks, kv_head], dtype=np.float64)  # [npages, bs]
+    vals = e4m3_decode(codes.reshape(npages * bs, -1)[:L])
+    return vals * sc.reshape(-1)[:L, None]
+
+
+def decode_paged(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu_q, scale):
+    """Paged decode / short-query attention over the dequantized fp8 cache, unsplit.
+
+    q [nq, hq, d] (rows of request r are cu_q[r]..cu_q[r+1]); row t of request r sits at
+    position L - q_len + t and attends to keys 0..L - q_len + t.  Returns [nq, hq, d].
+    """
+    q = np.asarray(q, np.float64)
+    nq, hq, d = q.shape
+    hkv = k_cache.shape[1]
+    group = hq // hkv
+    seq_lens = np.asarray(seq_lens).tolist()
+    cu_q = np.asarray(cu_q).tolist()
+    out = np.zeros((nq, hq, d))
+    for r, L in enumerate(seq_lens):
+        q0, q1 = cu_q[r], cu_q[r + 1]
+        ql = q1 - q0
+        for kvh in range(hkv):
+            K = gather_kv(k_cache, k_scale, block_table[r], L, kvh)
+            V = gather_kv(v_cache, v_scale, block_table[r], L, kvh)
+            for t in range(ql):
+                pos = L - ql + t
+                for h in range(kvh * group, (kvh + 1) * group):
+                    s = scale * (K[: pos + 1] @ q[q0 + t, h])
+                    p = np.exp(s - s.max())
+                    out[q0 + t, h] = (p @ V[: pos + 1]) / p.sum()
+    return out
+
+
+def decode_partials(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu_q, scale, segment_len):
+    """Split-K partials in the pages' order ([AIT] commits and Technical details).
+
+    For each (request, kv head, segment [segment_len*s, segment_len*(s+1)) of the
+    context) and each query row: s_j = scale * kscale_j * (q . k8_j); the running max m
+    and row sum l use the unscaled probabilities p_j = e^{s_j - m}; the V scales multiply
+    the P columns after the row sum: acc = sum_j (p_j vscale_j) v8_j.  A row with no
+    visible key in the segment stores (acc, m, l) = (0, -inf, 0).
+
+    Returns a list of dicts {r, kvh, seg, acc [ql, group, d], m [ql, group], l [ql, group]}.
+    """
+    q = np.asarray(q, np.float64)
+    nq, hq, d = q.shape
+    hkv = k_cache.shape[1]
+    bs = k_cache.shape[2]
+    group = hq // hkv
+    seq_lens = np.asarray(seq_lens).tolist()
+    cu_q = np.asarray(cu_q).tolist()
+    parts = []
+    for r, L in enumerate(seq_lens):
+        q0, q1 = cu_q[r], cu_q[r + 1]
+        ql = q1 - q0
+        nseg = (L + segment_len - 1) // segment_len
+        npages = (L + bs - 1) // bs
+        blocks = np.asarray(block_table[r][:npages], dtype=np.int64)
+        for kvh in range(hkv):
+            k8 = e4m3_decode(np.asarray(k_cache[blocks, kvh]).reshape(npages * bs, d)[:L])
+            v8 = e4m3_decode(np.asarray(v_cache[blocks, kvh]).reshape(npages * bs, d)[:L])
+            ks = np.asarray(k_scale[blocks, kvh], np.float64).reshape(-1)[:L]
+            vs = np.asarray(v_scale[blocks, kvh], np.float64).reshape(-1)[:L]
+            for sg in range(nseg):
+                j0, j1 = sg * segment_len, min((sg + 1) * segment_len, L)
+                acc = np.zeros((ql, group, d))
+                m = np.full((ql, group), -np.inf)
+                l = np.zeros((ql, group))
+                for t in range(ql):
+                    last = L - ql + t  # last visible key
+                    hi = min(j1, last + 1)
+                    if hi <= j0:
+                        continue  # empty partial
+                    qq = q[q0 + t, kvh * group : (kvh + 1) * group]  # [group, d]
+                    s = scale * (qq @ k8[j0:hi].T) * ks[j0:hi][None, :]
+                    mm = s.max(axis=1)
+                    p = np.exp(s - mm[:, None])
+                    m[t] = mm
+                    l[t] = p.sum(axis=1)
+                    acc[t] = (p * vs[j0:hi][None, :]) @ v8[j0:hi]
+                parts.append(dict(r=r, kvh=kvh, seg=sg, acc=acc, m=m, l=l))
+    return parts
+
+
+def decode_combine(parts, nq, hq, d, cu_q, hkv):
+    """LSE-weighted reduce ([AIT] commit 3 / Technical details): M* = max_s m_s,
+    w_s = 0 for an empty partial (m_s = -inf) else e^{m_s - M*}, O = sum w_s acc_s /
+    sum w_s l_s.  A row whose partials are all empty gets 0."""
+    group = hq // hkv
+    cu_q = np.asarray(cu_q).tolist()
+    by_key = {}
+    for p in parts:
+        by_key.setdefault((p["r"], p["kvh"]), []).append(p)
+    out = np.zeros((nq, hq, d))
+    for (r, kvh), plist in by_key.items():
+        q0 = cu_q[r]
+        M = np.max(np.stack([p["m"] for p in plist]), axis=0)  # [ql, group]
+        num = np.zeros_like(plist[0]["acc"])
+        den = np.zeros_like(plist[0]["l"])
+        for p in plist:
+            w = np.where(np.isneginf(p["m"]), 0.0, np.exp(np.where(np.isneginf(M), 0.0, p["m"] - M)))
+            num += w[:, :, None] * p["acc"]
+            den += w * p["l"]
+        res = np.where(den[:, :, None] > 0, num / np.where(den > 0, den, 1.0)[:, :, None], 0.0)
+        ql = res.shape[0]
+        out[q0 : q0 + ql, kvh * group : (kvh + 1) * group] = res
+    return out
+
+
+def decode_paged_splitk(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu_q, scale, segment_len):
+    """Split-K decode: partials per context segment, then the LSE-weighted reduce."""
+    q = np.asarray(q)
+    parts = decode_partials(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu_q, scale, segment_len)
+    return decode_combine(parts, q.shape[0], q.shape[1], q.shape[2], cu_q, k_cache.shape[1])
+
+
+def rel_rms(x, ref) -> float:
+    """||x - ref||_2 / ||ref||_2 over the whole tensor (the pages' "relative RMS error")."""
+    x = np.asarray(x, np.float64)
+    ref = np.asarray(ref, np.float64)
+    den = math.sqrt(float((ref * ref).sum()))
+    num = math.sqrt(float(((x - ref) ** 2).sum()))
+    return num / den if den > 0 else num

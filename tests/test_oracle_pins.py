@@ -1,0 +1,345 @@
+"""Pins of the fp64 oracle to things other than itself: library routines (fp64 SDPA,
+torch.autograd, torch fp8/bf16 conversions), closed forms, hand-derived values, finite
+differences and invariants.  Each test is chosen so that a dropped term, a sign error, a
+wrong index or a transposed operand in the oracle fails at least one of them."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from synth import make_prefill, make_decode
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def f64(t):
+    return None if t is None else t.double().numpy()
+
+
+def run_fwd(c, **over):
+    kw = dict(log_gate=f64(c.log_gate), sink=f64(c.sink), window=c.window)
+    kw.update(over)
+    return oracle.prefill_forward(f64(c.q), f64(c.k), f64(c.v), c.cu_seqlens.numpy(), c.scale, **kw)
+
+
+def run_bwd(c, **over):
+    kw = dict(log_gate=f64(c.log_gate), sink=f64(c.sink), window=c.window)
+    kw.update(over)
+    return oracle.prefill_backward(f64(c.q), f64(c.k), f64(c.v), f64(c.do), c.cu_seqlens.numpy(), c.scale, **kw)
+
+
+def sdpa_reference(c, use_gate=True, use_sink=True, requires_grad=False):
+    """fp64 torch SDPA per sequence; gate as an additive float mask, sink as an extra key
+    with zero key/value vectors whose mask entry is sigma; GQA by repeating K/V."""
+    group = c.hq // c.hkv
+    q = c.q.double().clone().requires_grad_(requires_grad)
+    k = c.k.double().clone().requires_grad_(requires_grad)
+    v = c.v.double().clone().requires_grad_(requires_grad)
+    g = None
+    if use_gate and c.log_gate is not None:
+        g = c.log_gate.double().clone().requires_grad_(requires_grad)
+    s = None
+    if use_sink and c.sink is not None:
+        s = c.sink.double().clone().requires_grad_(requires_grad)
+    outs = []
+    cu = c.cu_seqlens.tolist()
+    for a, b in zip(cu[:-1], cu[1:]):
+        T = b - a
+        qs = q[a:b].transpose(0, 1)  # [hq, T, d]
+        ks = k[a:b].transpose(0, 1).repeat_interleave(group, 0)
+        vs = v[a:b].transpose(0, 1).repeat_interleave(group, 0)
+        i = torch.arange(T)[:, None]
+        j = torch.arange(T)[None, :]
+        allowed = j <= i
+        if c.window > 0:
+            allowed = allowed & ((i - j) < c.window)
+        mask = torch.zeros(c.hq, T, T, dtype=torch.float64)
+        if g is not None:
+            G = torch.cumsum(g[a:b], 0).transpose(0, 1)  # [hq, T]
+            mask = mask + G[:, :, None] - G[:, None, :]
+        mask = mask.masked_fill(~allowed, float("-inf"))
+        if s is not None:
+            ks = torch.cat([ks, torch.zeros(c.hq, 1, c.dqk, dtype=torch.float64)], 1)
+            vs = torch.cat([vs, torch.zeros(c.hq, 1, c.dv, dtype=torch.float64)], 1)
+            mask = torch.cat([mask, s[:, None, None].expand(c.hq, T, 1)], 2)
+        o = F.scaled_dot_product_attention(qs, ks, vs, attn_mask=mask, scale=c.scale)
+        outs.append(o.transpose(0, 1))
+    o = torch.cat(outs, 0)
+    return o, dict(q=q, k=k, v=v, g=g, s=s)
+
+
+# ---------------------------------------------------------------------------- forward
+def test_forward_plain_matches_fp64_sdpa_causal():
+    c = make_prefill([37, 64], hq=4, hkv=4, dqk=16, dv=8, seed=11)
+    o, _ = run_fwd(c)
+    cu = c.cu_seqlens.tolist()
+    for a, b in zip(cu[:-1], cu[1:]):
+        ref = F.scaled_dot_product_attention(
+            c.q[a:b].double().transpose(0, 1), c.k[a:b].double().transpose(0, 1),
+            c.v[a:b].double().transpose(0, 1), is_causal=True, scale=c.scale).transpose(0, 1)
+        np.testing.assert_allclose(o[a:b], ref.numpy(), rtol=0, atol=1e-12)
+
+
+def test_forward_gate_window_sink_match_sdpa_with_mask():
+    c = make_prefill([19, 33], hq=4, hkv=2, dqk=8, dv=12, seed=12, gate=True, sink=True, window=7)
+    o, _ = run_fwd(c)
+    ref, _ = sdpa_reference(c)
+    np.testing.assert_allclose(o, ref.numpy(), rtol=0, atol=1e-12)
+
+
+def test_zero_gates_equal_plain_softmax():
+    c = make_prefill([40], hq=2, hkv=1, dqk=8, dv=8, seed=13)
+    o0, l0 = run_fwd(c)
+    o1, l1 = run_fwd(c, log_gate=np.zeros((c.total, c.hq)))
+    np.testing.assert_array_equal(o0, o1)
+    np.testing.assert_array_equal(l0, l1)
+
+
+def test_constant_gate_is_alibi_bias():
+    c = make_prefill([30], hq=1, hkv=1, dqk=4, dv=4, seed=14)
+    cst = -0.3
+    o, _ = run_fwd(c, log_gate=np.full((c.total, 1), cst))
+    T = c.total
+    i = torch.arange(T)[:, None]
+    j = torch.arange(T)[None, :]
+    bias = ((i - j).double() * cst).masked_fill(j > i, float("-inf"))
+    ref = F.scaled_dot_product_attention(c.q.double().transpose(0, 1), c.k.double().transpose(0, 1),
+                                         c.v.double().transpose(0, 1), attn_mask=bias, scale=c.scale)
+    np.testing.assert_allclose(o, ref.transpose(0, 1).numpy(), atol=1e-12)
+
+
+def test_sink_closed_form():
+    c = make_prefill([25, 9], hq=3, hkv=1, dqk=8, dv=5, seed=15, gate=True, sink=True)
+    o_s, l_s = run_fwd(c)
+    o_n, l_n = run_fwd(c, sink=None)
+    sig = f64(c.sink)
+    # O_sink = O_nosink * sigmoid(LSE_nosink - sigma); LSE_sink = logaddexp(LSE_nosink, sigma)
+    factor = 1.0 / (1.0 + np.exp(sig[:, None] - l_n))  # [hq, tot]
+    np.testing.assert_allclose(o_s, o_n * factor.T[:, :, None], atol=1e-13)
+    np.testing.assert_allclose(l_s, np.logaddexp(l_n, sig[:, None]), atol=1e-13)
+
+
+def test_probabilities_plus_sink_sum_to_one():
+    c = make_prefill([31, 17], hq=2, hkv=2, dqk=4, dv=1, seed=16, gate=True, sink=True, window=5)
+    ones = np.ones((c.total, c.hkv, 1))
+    o, lse = oracle.prefill_forward(f64(c.q), f64(c.k), ones, c.cu_seqlens.numpy(), c.scale,
+                                    log_gate=f64(c.log_gate), sink=f64(c.sink), window=c.window)
+    p_sink = np.exp(f64(c.sink)[:, None] - lse)  # [hq, tot]
+    np.testing.assert_allclose(o[:, :, 0] + p_sink.T, 1.0, atol=1e-14)
+
+
+def test_window_at_least_T_equals_full_causal_and_window_one_closed_form():
+    c = make_prefill([20, 12], hq=2, hkv=1, dqk=4, dv=3, seed=17, gate=True, sink=True)
+    o_full, l_full = run_fwd(c, window=0)
+    o_big, l_big = run_fwd(c, window=20)
+    np.testing.assert_array_equal(o_full, o_big)
+    np.testing.assert_array_equal(l_full, l_big)
+    o1, l1 = run_fwd(c, window=1)
+    p_sink = np.exp(f64(c.sink)[:, None] - l1).T  # [tot, hq]
+    v = f64(c.v)
+    group = c.hq // c.hkv
+    v_rep = np.repeat(v, group, axis=1)
+    np.testing.assert_allclose(o1, v_rep * (1.0 - p_sink)[:, :, None], atol=1e-14)
+    o2, _ = run_fwd(c, window=2)
+    assert not np.allclose(o2, o1)
+
+
+def test_gqa_equals_mha_on_repeated_kv():
+    c = make_prefill([23, 10], hq=6, hkv=2, dqk=8, dv=4, seed=18, gate=True, sink=True, window=9)
+    o, lse = run_fwd(c)
+    dq, dk, dv, dg, ds = run_bwd(c)
+    rep = lambda x: np.repeat(f64(x), 3, axis=1)
+    o2, lse2 = oracle.prefill_forward(f64(c.q), rep(c.k), rep(c.v), c.cu_seqlens.numpy(), c.scale,
+                                      log_gate=f64(c.log_gate), sink=f64(c.sink), window=c.window)
+    dq2, dk2, dv2, dg2, ds2 = oracle.prefill_backward(f64(c.q), rep(c.k), rep(c.v), f64(c.do),
+                                                      c.cu_seqlens.numpy(), c.scale, log_gate=f64(c.log_gate),
+                                                      sink=f64(c.sink), window=c.window)
+    np.testing.assert_allclose(o, o2, atol=1e-14)
+    np.testing.assert_allclose(dq, dq2, atol=1e-13)
+    np.testing.assert_allclose(dk, dk2.reshape(c.total, 2, 3, -1).sum(2), atol=1e-13)
+    np.testing.assert_allclose(dv, dv2.reshape(c.total, 2, 3, -1).sum(2), atol=1e-13)
+    np.testing.assert_allclose(dg, dg2, atol=1e-13)
+    np.testing.assert_allclose(ds, ds2, atol=1e-13)
+
+
+def test_varlen_equals_concatenated_dense():
+    c = make_prefill([13, 1, 22, 7], hq=2, hkv=1, dqk=4, dv=6, seed=19, gate=True, sink=True, window=6)
+    o, lse = run_fwd(c)
+    dq, dk, dv, dg, ds = run_bwd(c)
+    cu = c.cu_seqlens.tolist()
+    ds_sum = np.zeros_like(ds)
+    for a, b in zip(cu[:-1], cu[1:]):
+        sl = slice(a, b)
+        args = (f64(c.q)[sl], f64(c.k)[sl], f64(c.v)[sl])
+        kw = dict(log_gate=f64(c.log_gate)[sl], sink=f64(c.sink), window=c.window)
+        o1, l1 = oracle.prefill_forward(*args, np.array([0, b - a]), c.scale, **kw)
+        g1 = oracle.prefill_backward(*args, f64(c.do)[sl], np.array([0, b - a]), c.scale, **kw)
+        np.testing.assert_array_equal(o[sl], o1)
+        np.testing.assert_array_equal(lse[:, sl], l1)
+        for full, part in zip((dq, dk, dv, dg), g1[:4]):
+            np.testing.assert_allclose(full[sl], part, atol=1e-15)
+        ds_sum += g1[4]
+    np.testing.assert_allclose(ds, ds_sum, atol=1e-13)
+
+
+def test_hand_derived_two_token_case():
+    with open(os.path.join(HERE, "golden", "tiny_gate_sink.json")) as f:
+        fx = json.load(f)
+    i, e = fx["inputs"], fx["expected"]
+    arr = lambda x: np.array(x, dtype=np.float64)
+    cu = np.array(i["cu_seqlens"])
+    o, lse = oracle.prefill_forward(arr(i["q"]), arr(i["k"]), arr(i["v"]), cu, i["scale"],
+                                    log_gate=arr(i["log_gate"]), sink=arr(i["sink"]))
+    dq, dk, dv, dg, ds = oracle.prefill_backward(arr(i["q"]), arr(i["k"]), arr(i["v"]), arr(i["do"]), cu,
+                                                 i["scale"], log_gate=arr(i["log_gate"]), sink=arr(i["sink"]))
+    for name, got in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv), ("dg", dg), ("dsink", ds)):
+        np.testing.assert_allclose(got, arr(e[name]), rtol=0, atol=1e-14, err_msg=name)
+
+
+# ---------------------------------------------------------------------------- backward
+def _loss(c, q, k, v, g, s):
+    o, _ = oracle.prefill_forward(q, k, v, c.cu_seqlens.numpy(), c.scale, log_gate=g, sink=s, window=c.window)
+    return float((o * f64(c.do)).sum())
+
+
+def test_backward_central_finite_differences():
+    c = make_prefill([5, 3], hq=2, hkv=1, dqk=3, dv=2, seed=20, gate=True, sink=True, window=3)
+    dq, dk, dv, dg, ds = run_bwd(c)
+    base = dict(q=f64(c.q), k=f64(c.k), v=f64(c.v), g=f64(c.log_gate), s=f64(c.sink))
+    grads = dict(q=dq, k=dk, v=dv, g=dg, s=ds)
+    eps = 1e-6
+    for name, x in base.items():
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp = {kk: vv.copy() for kk, vv in base.items()}
+            xm = {kk: vv.copy() for kk, vv in base.items()}
+            xp[name][idx] += eps
+            xm[name][idx] -= eps
+            num[idx] = (_loss(c, **xp) - _loss(c, **xm)) / (2 * eps)
+        np.testing.assert_allclose(grads[name], num, rtol=1e-6, atol=1e-8, err_msg=name)
+
+
+def test_backward_matches_torch_autograd_on_sdpa():
+    c = make_prefill([11, 6, 15], hq=4, hkv=2, dqk=8, dv=4, seed=21, gate=True, sink=True, window=5)
+    dq, dk, dv, dg, ds = run_bwd(c)
+    o, leaves = sdpa_reference(c, requires_grad=True)
+    (o * c.do.double()).sum().backward()
+    np.testing.assert_allclose(dq, leaves["q"].grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dk, leaves["k"].grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dv, leaves["v"].grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dg, leaves["g"].grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(ds, leaves["s"].grad.numpy(), atol=1e-12)
+
+
+def test_sink_gradient_closed_form_and_first_token_gate_gradient():
+    c = make_prefill([26, 14, 3], hq=3, hkv=1, dqk=8, dv=6, seed=22, gate=True, sink=True)
+    o, lse = run_fwd(c)
+    dq, dk, dv, dg, ds = run_bwd(c)
+    # dsigma_h = -sum_i p_sink,i (dO_i . O_i): uses the forward output, not P and dP
+    p_sink = np.exp(f64(c.sink)[:, None] - lse)  # [hq, tot]
+    dot = (f64(c.do) * o).sum(-1).T  # [hq, tot]
+    np.testing.assert_allclose(ds, -(p_sink * dot).sum(1), atol=1e-13)
+    # each dS entry enters dG once as a row term and once as a column term: the gate of
+    # the first token of every sequence never changes a score
+    for a in c.cu_seqlens.tolist()[:-1]:
+        np.testing.assert_allclose(dg[a], 0.0, atol=1e-13)
+
+
+# ---------------------------------------------------------------------------- formats
+def test_e4m3_table_matches_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_decode(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    np.testing.assert_array_equal(np.isnan(ours), np.isnan(ref))
+    np.testing.assert_array_equal(ours[~np.isnan(ours)], ref[~np.isnan(ref)])
+    assert np.nanmax(ours) == 448.0 and np.isnan(ours[0x7F]) and np.isnan(ours[0xFF])
+
+
+def test_bf16_round_matches_torch():
+    rng = np.random.default_rng(0)
+    x = np.concatenate([rng.standard_normal(10000), rng.standard_normal(1000) * 1e-30,
+                        rng.standard_normal(1000) * 1e30]).astype(np.float32).astype(np.float64)
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).double().numpy()
+    np.testing.assert_array_equal(oracle.bf16_round(x), ref)
+
+
+# ---------------------------------------------------------------------------- decode
+def _decode_args(dc):
+    return (f64(dc.q), dc.k_cache.numpy(), dc.v_cache.numpy(), dc.k_scale.numpy(), dc.v_scale.numpy(),
+            dc.block_table.numpy(), dc.seq_lens.numpy(), dc.cu_q.numpy(), dc.scale)
+
+
+@pytest.mark.parametrize("reading", ["A", "B"])
+def test_splitk_combine_equals_unsplit_with_empty_segments(reading):
+    dc = make_decode([1, 17, 40, 70, 33], [1, 2, 4, 3, 4], hq=8, hkv=2, d=16, seed=30, scale_reading=reading,
+                     segment_len=2048)
+    ref = oracle.decode_paged(*_decode_args(dc))
+    for seg in (2048, 32, 16, 3, 2):
+        parts = oracle.decode_partials(*_decode_args(dc), seg)
+        if seg == 2:
+            # a query row that ends before a segment stores an empty partial
+            assert any(np.isneginf(p["m"]).any() for p in parts)
+        out = oracle.decode_combine(parts, dc.q.shape[0], dc.hq, dc.d, dc.cu_q.numpy(), dc.hkv)
+        np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
+        assert np.isfinite(out).all()
+
+
+def test_decode_q1_equals_last_prefill_row_on_dequantized_cache():
+    dc = make_decode([45, 16, 1], [1, 1, 1], hq=4, hkv=2, d=8, seed=31)
+    out = oracle.decode_paged(*_decode_args(dc))
+    for r, L in enumerate(dc.seq_lens.tolist()):
+        K = np.stack([oracle.gather_kv(dc.k_cache.numpy(), dc.k_scale.numpy(), dc.block_table[r].numpy(), L, h)
+                      for h in range(dc.hkv)], 1)
+        V = np.stack([oracle.gather_kv(dc.v_cache.numpy(), dc.v_scale.numpy(), dc.block_table[r].numpy(), L, h)
+                      for h in range(dc.hkv)], 1)
+        q = np.zeros((L, dc.hq, dc.d))
+        q[L - 1] = f64(dc.q)[r]
+        o, _ = oracle.prefill_forward(q, K, V, np.array([0, L]), dc.scale)
+        np.testing.assert_allclose(out[r], o[L - 1], atol=1e-12)
+        # and the same row through torch fp64 SDPA with repeated kv heads
+        rep = lambda x: torch.from_numpy(np.repeat(x, dc.hq // dc.hkv, 1)).transpose(0, 1)
+        ref = F.scaled_dot_product_attention(torch.from_numpy(f64(dc.q)[r][:, None]), rep(K), rep(V),
+                                             scale=dc.scale)
+        np.testing.assert_allclose(out[r], ref[:, 0].numpy(), atol=1e-12)
+
+
+def test_decode_per_token_scales_matter_and_gather_is_exact():
+    dc = make_decode([50, 77], [1, 2], hq=4, hkv=1, d=8, seed=32)
+    args = list(_decode_args(dc))
+    # a dominant key at one chosen slot makes the output equal that slot's dequantized V
+    r, slot = 1, 37
+    L = int(dc.seq_lens[r])
+    blk = int(dc.block_table[r, slot // 16])
+    kc = args[1].copy()
+    ks = args[3].copy()
+    qv = args[0]
+    row = int(dc.cu_q[r + 1]) - 1  # last row sees every key
+    qv = qv.copy()
+    qv[row] = 0.0
+    qv[row, :, 0] = 1.0
+    kc[:, :, :, :] = 0  # code 0 = +0.0
+    kc[blk, 0, slot % 16, 0] = 0x7E  # 448
+    ks[blk, 0, slot % 16] = 1.0
+    args[0], args[1], args[3] = qv, kc, ks
+    args[8] = 1.0
+    out = oracle.decode_paged(*args)
+    vexp = oracle.e4m3_decode(dc.v_cache[blk, 0, slot % 16].numpy()) * float(dc.v_scale[blk, 0, slot % 16])
+    np.testing.assert_allclose(out[row], np.broadcast_to(vexp, out[row].shape), rtol=0, atol=1e-12)
+    # per-token scales change the answer (reading only element 0 would be wrong)
+    args2 = list(_decode_args(dc))
+    vs = args2[4].copy()
+    vs[:] = vs.reshape(-1)[0]
+    assert not np.allclose(oracle.decode_paged(*args2[:4], vs, *args2[5:]), oracle.decode_paged(*_decode_args(dc)))
+
+
+def test_decode_never_reads_unused_slots():
+    dc = make_decode([19, 3], [1, 3], hq=4, hkv=2, d=8, seed=33)
+    out = oracle.decode_paged(*_decode_args(dc))
+    assert np.isfinite(out).all()
+    # unused slots and spare pages are NaN-poisoned by the generator
+    assert np.isnan(dc.k_scale.numpy()).any() and (dc.v_cache.numpy() == 0x7F).any()
