@@ -1,0 +1,318 @@
+"""Python binding of libgcs_attn (GB300 / sm_103a gated causal softmax attention).
+
+Argument marshalling only: every step of the computation runs in the library's CUDA
+kernels.  PyTorch provides device memory (outputs and workspace are allocated here with
+the caching allocator) and the current stream.  There is no CPU or PyTorch fallback: if
+the library cannot be built or loaded, every call raises.
+
+Entry points (same names as the C ABI in include/gcs_attn.h):
+    attn_fwd(q, k, v, cu_seqlens, ...)           -> (o, lse)
+    attn_bwd(q, k, v, o, lse, dout, cu_seqlens, ...) -> (dq, dk, dv, dlog_gate, dsink)
+    attn_decode_paged(q, k_cache, v_cache, ...)  -> out
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+import torch
+
+__all__ = [
+    "load",
+    "lib",
+    "attn_fwd",
+    "attn_bwd",
+    "attn_decode_paged",
+    "PrefillArgs",
+    "DecodeArgs",
+    "GcsError",
+    "get_device_status",
+    "STATUS",
+]
+
+STATUS = {
+    0: "GCS_OK",
+    1: "GCS_ERR_INVALID_ARG",
+    2: "GCS_ERR_UNSUPPORTED",
+    3: "GCS_ERR_WORKSPACE",
+    4: "GCS_ERR_CUDA",
+    5: "GCS_ERR_DEVICE_TIMEOUT",
+}
+
+_c_int, _c_float, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_void_p
+
+
+class PrefillArgs(ctypes.Structure):
+    _fields_ = [
+        ("num_seqs", _c_int),
+        ("cu_seqlens", _vp),
+        ("total_tokens", _c_int),
+        ("max_seqlen", _c_int),
+        ("hq", _c_int),
+        ("hkv", _c_int),
+        ("dqk", _c_int),
+        ("dv", _c_int),
+        ("scale", _c_float),
+        ("window", _c_int),
+        ("q", _vp),
+        ("k", _vp),
+        ("v", _vp),
+        ("log_gate", _vp),
+        ("sink", _vp),
+    ]
+
+
+class DecodeArgs(ctypes.Structure):
+    _fields_ = [
+        ("num_reqs", _c_int),
+        ("cu_q", _vp),
+        ("total_q", _c_int),
+        ("max_q_len", _c_int),
+        ("seq_lens", _vp),
+        ("max_seq_len", _c_int),
+        ("block_table", _vp),
+        ("max_blocks_per_req", _c_int),
+        ("k_cache", _vp),
+        ("v_cache", _vp),
+        ("k_scale", _vp),
+        ("v_scale", _vp),
+        ("num_blocks", _c_int),
+        ("block_size", _c_int),
+        ("hq", _c_int),
+        ("hkv", _c_int),
+        ("d", _c_int),
+        ("scale", _c_float),
+        ("segment_len", _c_int),
+        ("q", _vp),
+    ]
+
+
+class GcsError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)}")
+
+
+_LIB: Optional[ctypes.CDLL] = None
+
+
+def _declare(lib: ctypes.CDLL) -> None:
+    P = ctypes.POINTER
+    lib.gcs_status_str.argtypes = [_c_int]
+    lib.gcs_status_str.restype = ctypes.c_char_p
+    lib.gcs_version.argtypes = []
+    lib.gcs_version.restype = ctypes.c_char_p
+    lib.attn_fwd_workspace.argtypes = [P(PrefillArgs)]
+    lib.attn_fwd_workspace.restype = ctypes.c_size_t
+    lib.attn_bwd_workspace.argtypes = [P(PrefillArgs)]
+    lib.attn_bwd_workspace.restype = ctypes.c_size_t
+    lib.attn_decode_workspace.argtypes = [P(DecodeArgs)]
+    lib.attn_decode_workspace.restype = ctypes.c_size_t
+    lib.attn_fwd.argtypes = [P(PrefillArgs), _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    lib.attn_fwd.restype = _c_int
+    lib.attn_bwd.argtypes = [P(PrefillArgs), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]
+    lib.attn_bwd.restype = _c_int
+    lib.attn_decode_paged.argtypes = [P(DecodeArgs), _vp, _vp, ctypes.c_size_t, _vp]
+    lib.attn_decode_paged.restype = _c_int
+    lib.gcs_get_device_status.argtypes = [P(_c_int), _c_int]
+    lib.gcs_get_device_status.restype = _c_int
+
+
+def load(build_if_needed: bool = True) -> ctypes.CDLL:
+    """Load (building first if the library is missing or stale) libgcs_attn.so."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    from . import build as _build
+
+    path = _build.LIB
+    if build_if_needed:
+        path = _build.build()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libgcs_attn.so not found at {path}; run gated_causal_softmax_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    _declare(lib)
+    _LIB = lib
+    return lib
+
+
+def lib() -> ctypes.CDLL:
+    return load()
+
+
+def _check(status: int, what: str) -> None:
+    if status == 0:
+        return
+    if status == 2:
+        raise NotImplementedError(f"{what}: {STATUS[2]}")
+    raise GcsError(status, what)
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream() -> int:
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _need(t: torch.Tensor, dtype, name: str) -> torch.Tensor:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def get_device_status(clear: bool = True) -> int:
+    """Per-device status word written by kernels that gave up on a bounded wait."""
+    st = _c_int(0)
+    _check(load().gcs_get_device_status(ctypes.byref(st), 1 if clear else 0), "gcs_get_device_status")
+    return st.value
+
+
+def prefill_args(q, k, v, cu_seqlens, max_seqlen, scale, window, log_gate, sink) -> PrefillArgs:
+    _need(q, torch.bfloat16, "q")
+    _need(k, torch.bfloat16, "k")
+    _need(v, torch.bfloat16, "v")
+    _need(cu_seqlens, torch.int32, "cu_seqlens")
+    if log_gate is not None:
+        _need(log_gate, torch.float32, "log_gate")
+    if sink is not None:
+        _need(sink, torch.float32, "sink")
+    tot, hq, dqk = q.shape
+    hkv, dv = k.shape[1], v.shape[2]
+    if max_seqlen is None:
+        max_seqlen = int((cu_seqlens[1:] - cu_seqlens[:-1]).max())
+    if scale is None:
+        scale = 1.0 / math.sqrt(dqk)
+    return PrefillArgs(
+        num_seqs=cu_seqlens.numel() - 1,
+        cu_seqlens=cu_seqlens.data_ptr(),
+        total_tokens=tot,
+        max_seqlen=int(max_seqlen),
+        hq=hq,
+        hkv=hkv,
+        dqk=dqk,
+        dv=dv,
+        scale=float(scale),
+        window=int(window),
+        q=q.data_ptr(),
+        k=k.data_ptr(),
+        v=v.data_ptr(),
+        log_gate=_ptr(log_gate),
+        sink=_ptr(sink),
+    )
+
+
+def attn_fwd(q, k, v, cu_seqlens, max_seqlen=None, scale=None, window=0, log_gate=None, sink=None, out=None,
+             lse=None, workspace=None):
+    """Prefill forward.  q [tot, hq, dqk], k [tot, hkv, dqk], v [tot, hkv, dv] bf16;
+    cu_seqlens int32 [num_seqs + 1]; log_gate fp32 [tot, hq] or None; sink fp32 [hq] or None.
+    Returns o bf16 [tot, hq, dv] and lse fp32 [hq, tot]."""
+    L = load()
+    a = prefill_args(q, k, v, cu_seqlens, max_seqlen, scale, window, log_gate, sink)
+    tot, hq, _ = q.shape
+    if out is None:
+        out = torch.empty((tot, hq, v.shape[2]), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((hq, tot), dtype=torch.float32, device=q.device)
+    ws_bytes = L.attn_fwd_workspace(ctypes.byref(a))
+    if workspace is None and ws_bytes:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    st = L.attn_fwd(ctypes.byref(a), out.data_ptr(), lse.data_ptr(), _ptr(workspace),
+                    workspace.numel() if workspace is not None else 0, _stream())
+    _check(st, "attn_fwd")
+    return out, lse
+
+
+def attn_bwd(q, k, v, o, lse, dout, cu_seqlens, max_seqlen=None, scale=None, window=0, log_gate=None, sink=None,
+             workspace=None, dq=None, dk=None, dv=None, dlog_gate=None, dsink=None):
+    """Prefill backward of sum(O * dO).  Returns dq, dk, dv (bf16), dlog_gate fp32 [tot, hq]
+    (None without gates) and dsink fp32 [hq] (None without sink)."""
+    L = load()
+    a = prefill_args(q, k, v, cu_seqlens, max_seqlen, scale, window, log_gate, sink)
+    _need(o, torch.bfloat16, "o")
+    _need(dout, torch.bfloat16, "dout")
+    _need(lse, torch.float32, "lse")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if log_gate is not None and dlog_gate is None:
+        dlog_gate = torch.empty_like(log_gate)
+    if sink is not None and dsink is None:
+        dsink = torch.empty_like(sink)
+    ws_bytes = L.attn_bwd_workspace(ctypes.byref(a))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
+    st = L.attn_bwd(ctypes.byref(a), o.data_ptr(), lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                    dv.data_ptr(), _ptr(dlog_gate), _ptr(dsink), workspace.data_ptr(), workspace.numel(), _stream())
+    _check(st, "attn_bwd")
+    return dq, dk, dv, dlog_gate, dsink
+
+
+def decode_args(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu_q, max_q_len, max_seq_len, scale,
+                segment_len) -> DecodeArgs:
+    _need(q, torch.bfloat16, "q")
+    if k_cache.dtype == torch.float8_e4m3fn:
+        k_cache = k_cache.view(torch.uint8)
+    if v_cache.dtype == torch.float8_e4m3fn:
+        v_cache = v_cache.view(torch.uint8)
+    _need(k_cache, torch.uint8, "k_cache")
+    _need(v_cache, torch.uint8, "v_cache")
+    _need(k_scale, torch.float32, "k_scale")
+    _need(v_scale, torch.float32, "v_scale")
+    _need(block_table, torch.int32, "block_table")
+    _need(seq_lens, torch.int32, "seq_lens")
+    _need(cu_q, torch.int32, "cu_q")
+    nb, hkv, bs, d = k_cache.shape
+    if tuple(k_scale.shape) != (nb, hkv, bs) or tuple(v_scale.shape) != (nb, hkv, bs):
+        raise NotImplementedError("per-token scales must have the page shape [num_blocks, num_kv_heads, block_size]")
+    if tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("k_cache and v_cache shapes differ")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    return DecodeArgs(
+        num_reqs=seq_lens.numel(),
+        cu_q=cu_q.data_ptr(),
+        total_q=q.shape[0],
+        max_q_len=int(max_q_len),
+        seq_lens=seq_lens.data_ptr(),
+        max_seq_len=int(max_seq_len),
+        block_table=block_table.data_ptr(),
+        max_blocks_per_req=block_table.shape[1],
+        k_cache=k_cache.data_ptr(),
+        v_cache=v_cache.data_ptr(),
+        k_scale=k_scale.data_ptr(),
+        v_scale=v_scale.data_ptr(),
+        num_blocks=nb,
+        block_size=bs,
+        hq=q.shape[1],
+        hkv=hkv,
+        d=d,
+        scale=float(scale),
+        segment_len=int(segment_len),
+        q=q.data_ptr(),
+    )
+
+
+def attn_decode_paged(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu_q, max_q_len, max_seq_len,
+                      scale=None, segment_len=2048, out=None, workspace=None):
+    """Paged fp8 decode.  q bf16 [total_q, hq, d]; caches fp8 e4m3 (uint8 or float8_e4m3fn)
+    [num_blocks, hkv, block_size, d]; scales fp32 [num_blocks, hkv, block_size];
+    block_table int32 [R, max_blocks]; seq_lens int32 [R]; cu_q int32 [R + 1]."""
+    L = load()
+    a = decode_args(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu_q, max_q_len, max_seq_len,
+                    scale, segment_len)
+    if out is None:
+        out = torch.empty_like(q)
+    ws_bytes = L.attn_decode_workspace(ctypes.byref(a))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
+    st = L.attn_decode_paged(ctypes.byref(a), out.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream())
+    _check(st, "attn_decode_paged")
+    return out

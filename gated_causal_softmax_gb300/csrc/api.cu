@@ -1,0 +1,344 @@
+// C ABI: host-side validation, workspace carving, TMA descriptor encoding and launches.
+// Nothing here allocates device memory or synchronises (except gcs_get_device_status,
+// which is a synchronous query by design).
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/gcs_attn.h"
+#include "kernels.h"
+
+namespace gcs {
+
+__device__ int g_device_status = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+int* g_status_ptr[kMaxDevices] = {nullptr};
+std::mutex g_mu;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+// 2-D bf16 view [rows, width] with a 64 x box_rows box and 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t width, uint64_t rows, uint32_t box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {width, rows};
+  cuuint64_t strides[1] = {width * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round_up(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Carves consecutive 256-B aligned regions out of a workspace.
+struct Carver {
+  uint8_t* base;
+  size_t off = 0;
+  template <typename T>
+  T* take(size_t count) {
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += round_up(count * sizeof(T));
+    return p;
+  }
+};
+
+bool supported_dims(int dqk, int dv) {
+  return (dqk == 64 && dv == 64) || (dqk == 128 && dv == 128) || (dqk == 256 && dv == 256) ||
+         (dqk == 256 && dv == 512) || (dqk == 512 && dv == 512);
+}
+
+bool bwd_supported_dims(int dqk, int dv) { return (dqk == 64 && dv == 64) || (dqk == 128 && dv == 128); }
+
+int check_prefill(const gcs_prefill_args* a) {
+  if (!a) return GCS_ERR_INVALID_ARG;
+  if (a->num_seqs < 1 || a->total_tokens < 1 || a->max_seqlen < 1 || a->hq < 1 || a->hkv < 1)
+    return GCS_ERR_INVALID_ARG;
+  if (a->hq % a->hkv != 0) return GCS_ERR_INVALID_ARG;
+  if (a->window < 0) return GCS_ERR_INVALID_ARG;
+  if (!std::isfinite(a->scale)) return GCS_ERR_INVALID_ARG;
+  if (!a->cu_seqlens || !a->q || !a->k || !a->v) return GCS_ERR_INVALID_ARG;
+  if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v)) return GCS_ERR_INVALID_ARG;
+  if ((a->log_gate && !aligned16(a->log_gate)) || (a->sink && (reinterpret_cast<uintptr_t>(a->sink) & 3u)))
+    return GCS_ERR_INVALID_ARG;
+  if (!supported_dims(a->dqk, a->dv)) return GCS_ERR_UNSUPPORTED;
+  // TMA coordinates and element offsets are 32-bit; keep every tensor below 2^31 elements
+  const double big = 2147483647.0;
+  if ((double)a->total_tokens * a->hq * (a->dqk > a->dv ? a->dqk : a->dv) > big) return GCS_ERR_UNSUPPORTED;
+  return GCS_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? GCS_OK : GCS_ERR_CUDA; }
+
+int* status_ptr_for_current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+size_t fwd_ws(const gcs_prefill_args* a) {
+  Carver c{nullptr};
+  if (a->log_gate) c.take<float>((size_t)a->hq * a->total_tokens);
+  return c.off;
+}
+
+size_t bwd_ws(const gcs_prefill_args* a) {
+  Carver c{nullptr};
+  const size_t ht = (size_t)a->hq * a->total_tokens;
+  if (a->log_gate) c.take<float>(ht);                         // G^T
+  c.take<float>(ht);                                           // delta
+  c.take<float>((size_t)a->total_tokens * a->hq * a->dqk);     // dQ accumulator
+  if (a->log_gate || a->sink) c.take<float>(ht);               // row sums of dS
+  if (a->log_gate) c.take<float>(ht);                          // column sums of dS
+  return c.off;
+}
+
+}  // namespace
+
+int* device_status_ptr() { return status_ptr_for_current_device(); }
+
+}  // namespace gcs
+
+using namespace gcs;
+
+extern "C" {
+
+const char* gcs_status_str(int s) {
+  switch (s) {
+    case GCS_OK: return "ok";
+    case GCS_ERR_INVALID_ARG: return "invalid argument";
+    case GCS_ERR_UNSUPPORTED: return "unsupported shape, dtype or layout";
+    case GCS_ERR_WORKSPACE: return "workspace missing or too small";
+    case GCS_ERR_CUDA: return "CUDA error";
+    case GCS_ERR_DEVICE_TIMEOUT: return "a kernel gave up on a bounded wait";
+    default: return "unknown status";
+  }
+}
+
+const char* gcs_version(void) { return "gcs_attn 0.1 (sm_103a)"; }
+
+size_t attn_fwd_workspace(const gcs_prefill_args* a) { return (a && check_prefill(a) == GCS_OK) ? fwd_ws(a) : 0; }
+
+size_t attn_bwd_workspace(const gcs_prefill_args* a) { return (a && check_prefill(a) == GCS_OK) ? bwd_ws(a) : 0; }
+
+int attn_fwd(const gcs_prefill_args* a, void* o, float* lse, void* workspace, size_t workspace_bytes,
+             gcs_stream_t stream) {
+  int st = check_prefill(a);
+  if (st != GCS_OK) return st;
+  if (!o || !lse || !aligned16(o) || !aligned16(lse)) return GCS_ERR_INVALID_ARG;
+  const size_t need = fwd_ws(a);
+  if (need > 0 && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+    return GCS_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int* status = device_status_ptr();
+  if (!status) return GCS_ERR_CUDA;
+
+  Carver c{static_cast<uint8_t*>(workspace)};
+  float* gT = a->log_gate ? c.take<float>((size_t)a->hq * a->total_tokens) : nullptr;
+
+  FwdMaps maps;
+  if (!make_map(&maps.q, a->q, (uint64_t)a->hq * a->dqk, a->total_tokens, 128) ||
+      !make_map(&maps.k, a->k, (uint64_t)a->hkv * a->dqk, a->total_tokens, 128) ||
+      !make_map(&maps.v, a->v, (uint64_t)a->hkv * a->dv, a->total_tokens, 128))
+    return GCS_ERR_CUDA;
+
+  if (gT) {
+    st = cuda_status(launch_gate_cumsum(a->log_gate, a->cu_seqlens, a->num_seqs, a->total_tokens, a->hq, gT, s));
+    if (st != GCS_OK) return st;
+  }
+  FwdParams p;
+  p.cu_seqlens = a->cu_seqlens;
+  p.num_seqs = a->num_seqs;
+  p.total = a->total_tokens;
+  p.hq = a->hq;
+  p.hkv = a->hkv;
+  p.dqk = a->dqk;
+  p.dv = a->dv;
+  p.dv_chunk = a->dv > 256 ? 256 : a->dv;
+  p.scale_log2 = a->scale * 1.4426950408889634f;
+  p.window = a->window;
+  p.gT = gT;
+  p.sink = a->sink;
+  p.o = static_cast<uint16_t*>(o);
+  p.lse = lse;
+  p.status = status;
+  const int num_tiles = (a->total_tokens + 127) / 128 + a->num_seqs;
+  return cuda_status(launch_prefill_fwd(p, maps, num_tiles, s));
+}
+
+int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const void* dout, void* dq, void* dk, void* dv,
+             float* dlog_gate, float* dsink, void* workspace, size_t workspace_bytes, gcs_stream_t stream) {
+  int st = check_prefill(a);
+  if (st != GCS_OK) return st;
+  if (!o || !lse || !dout || !dq || !dk || !dv) return GCS_ERR_INVALID_ARG;
+  if (!aligned16(o) || !aligned16(lse) || !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return GCS_ERR_INVALID_ARG;
+  if ((dlog_gate == nullptr) != (a->log_gate == nullptr)) return GCS_ERR_INVALID_ARG;
+  if ((dsink == nullptr) != (a->sink == nullptr)) return GCS_ERR_INVALID_ARG;
+  if (!bwd_supported_dims(a->dqk, a->dv)) return GCS_ERR_UNSUPPORTED;
+  const size_t need = bwd_ws(a);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return GCS_ERR_WORKSPACE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int* status = device_status_ptr();
+  if (!status) return GCS_ERR_CUDA;
+
+  const size_t ht = (size_t)a->hq * a->total_tokens;
+  Carver c{static_cast<uint8_t*>(workspace)};
+  float* gT = a->log_gate ? c.take<float>(ht) : nullptr;
+  float* delta = c.take<float>(ht);
+  float* dq_acc = c.take<float>((size_t)a->total_tokens * a->hq * a->dqk);
+  float* dg_row = (a->log_gate || a->sink) ? c.take<float>(ht) : nullptr;
+  float* dg_col = a->log_gate ? c.take<float>(ht) : nullptr;
+
+  BwdMaps maps;
+  if (!make_map(&maps.q, a->q, (uint64_t)a->hq * a->dqk, a->total_tokens, 64) ||
+      !make_map(&maps.k, a->k, (uint64_t)a->hkv * a->dqk, a->total_tokens, 128) ||
+      !make_map(&maps.v, a->v, (uint64_t)a->hkv * a->dv, a->total_tokens, 128) ||
+      !make_map(&maps.dout, dout, (uint64_t)a->hq * a->dv, a->total_tokens, 64))
+    return GCS_ERR_CUDA;
+
+  if (gT) {
+    st = cuda_status(launch_gate_cumsum(a->log_gate, a->cu_seqlens, a->num_seqs, a->total_tokens, a->hq, gT, s));
+    if (st != GCS_OK) return st;
+  }
+  st = cuda_status(launch_bwd_pre(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout),
+                                  a->total_tokens, a->hq, a->dv, a->dqk, delta, dq_acc, dg_row, dsink, s));
+  if (st != GCS_OK) return st;
+
+  BwdParams p;
+  p.cu_seqlens = a->cu_seqlens;
+  p.num_seqs = a->num_seqs;
+  p.total = a->total_tokens;
+  p.hq = a->hq;
+  p.hkv = a->hkv;
+  p.dqk = a->dqk;
+  p.dv = a->dv;
+  p.scale = a->scale;
+  p.scale_log2 = a->scale * 1.4426950408889634f;
+  p.window = a->window;
+  p.gT = gT;
+  p.lse = lse;
+  p.delta = delta;
+  p.grad_k = static_cast<uint16_t*>(dk);
+  p.grad_v = static_cast<uint16_t*>(dv);
+  p.dq_acc = dq_acc;
+  p.dg_row = dg_row;
+  p.dg_col = dg_col;
+  p.status = status;
+  const int num_tiles = (a->total_tokens + 127) / 128 + a->num_seqs;
+  st = cuda_status(launch_prefill_bwd(p, maps, num_tiles, s));
+  if (st != GCS_OK) return st;
+  return cuda_status(launch_bwd_post(dq_acc, static_cast<uint16_t*>(dq), a->total_tokens, a->hq, a->dqk,
+                                     a->cu_seqlens, a->num_seqs, dg_row, dg_col, dlog_gate, lse, delta, a->sink,
+                                     dsink, s));
+}
+
+static int check_decode(const gcs_decode_args* a) {
+  if (!a) return GCS_ERR_INVALID_ARG;
+  if (a->num_reqs < 1 || a->total_q < 1 || a->max_q_len < 1 || a->max_seq_len < 1 || a->max_blocks_per_req < 1 ||
+      a->num_blocks < 1 || a->hq < 1 || a->hkv < 1 || a->segment_len < 1)
+    return GCS_ERR_INVALID_ARG;
+  if (!a->cu_q || !a->seq_lens || !a->block_table || !a->k_cache || !a->v_cache || !a->k_scale || !a->v_scale ||
+      !a->q)
+    return GCS_ERR_INVALID_ARG;
+  if (!std::isfinite(a->scale)) return GCS_ERR_INVALID_ARG;
+  // per-token scales are only read on decode / short-query shapes (a prefill shape is rejected)
+  if (a->max_q_len > 4) return GCS_ERR_UNSUPPORTED;
+  if (a->d != 128 || a->block_size != 16 || a->hq != 16 * a->hkv) return GCS_ERR_UNSUPPORTED;
+  if (a->segment_len % a->block_size != 0) return GCS_ERR_UNSUPPORTED;
+  if (a->max_blocks_per_req * a->block_size < a->max_seq_len) return GCS_ERR_INVALID_ARG;
+  if (!aligned16(a->k_cache) || !aligned16(a->v_cache) || !aligned16(a->k_scale) || !aligned16(a->v_scale) ||
+      !aligned16(a->q))
+    return GCS_ERR_INVALID_ARG;
+  if ((double)a->num_blocks * a->hkv * a->block_size * a->d > 9.0e15) return GCS_ERR_UNSUPPORTED;
+  return GCS_OK;
+}
+
+static size_t decode_ws(const gcs_decode_args* a, int* max_segs_out) {
+  const int max_segs = (a->max_seq_len + a->segment_len - 1) / a->segment_len;
+  if (max_segs_out) *max_segs_out = max_segs;
+  const size_t units = (size_t)a->num_reqs * max_segs * a->hkv;
+  const size_t rows = (size_t)a->max_q_len * 16;
+  return round_up(units * rows * 128 * sizeof(float)) + round_up(units * rows * 2 * sizeof(float));
+}
+
+size_t attn_decode_workspace(const gcs_decode_args* a) {
+  return (a && check_decode(a) == GCS_OK) ? decode_ws(a, nullptr) : 0;
+}
+
+int attn_decode_paged(const gcs_decode_args* a, void* out, void* workspace, size_t workspace_bytes,
+                      gcs_stream_t stream) {
+  int st = check_decode(a);
+  if (st != GCS_OK) return st;
+  if (!out || !aligned16(out)) return GCS_ERR_INVALID_ARG;
+  int max_segs = 0;
+  const size_t need = decode_ws(a, &max_segs);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return GCS_ERR_WORKSPACE;
+  int* status = device_status_ptr();
+  if (!status) return GCS_ERR_CUDA;
+  const size_t units = (size_t)a->num_reqs * max_segs * a->hkv;
+  const size_t rows = (size_t)a->max_q_len * 16;
+  DecodeParams p;
+  p.cu_q = a->cu_q;
+  p.seq_lens = a->seq_lens;
+  p.block_table = a->block_table;
+  p.max_blocks = a->max_blocks_per_req;
+  p.k_cache = a->k_cache;
+  p.v_cache = a->v_cache;
+  p.k_scale = a->k_scale;
+  p.v_scale = a->v_scale;
+  p.num_reqs = a->num_reqs;
+  p.hq = a->hq;
+  p.hkv = a->hkv;
+  p.max_q_len = a->max_q_len;
+  p.max_segs = max_segs;
+  p.seg_pages = a->segment_len / a->block_size;
+  p.scale = a->scale;
+  p.q = static_cast<const uint16_t*>(a->q);
+  p.out = static_cast<uint16_t*>(out);
+  p.part_acc = static_cast<float*>(workspace);
+  p.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + round_up(units * rows * 128 * sizeof(float)));
+  p.status = status;
+  return cuda_status(launch_decode(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int gcs_get_device_status(int* status, int clear) {
+  if (!status) return GCS_ERR_INVALID_ARG;
+  int* d = device_status_ptr();
+  if (!d) return GCS_ERR_CUDA;
+  if (cudaMemcpy(status, d, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return GCS_ERR_CUDA;
+  if (clear && cudaMemset(d, 0, sizeof(int)) != cudaSuccess) return GCS_ERR_CUDA;
+  return GCS_OK;
+}
+
+}  // extern "C"

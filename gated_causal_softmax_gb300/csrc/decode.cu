@@ -1,0 +1,397 @@
+// Paged decode / short-query attention over an fp8 e4m3 KV cache with per-token scales.
+//
+// ROCm/aiter PR #6660 (gfx1250 unified attention), commit messages and "Technical
+// details": one fp32 K and V scale per cached token and KV head, laid out [num_blocks,
+// num_kv_heads, block_size]; each tile is one page; K scales multiply the QK columns; V
+// scales multiply the P columns after the row sum; slots past seq_len get scale 0; the
+// context is split into segments (split-K) whose partials are merged by an LSE-weighted
+// reduce in which an empty partial (M = -inf) weighs 0.
+//
+// decode_split_kernel: one CTA per (segment, kv head, request).  Warp 0 streams pages
+// (K 2 KB, V 2 KB, 16 K scales, 16 V scales) into an 8-stage shared-memory ring with
+// cp.async.bulk.  Warps 1..4 each own one query position (16 query heads of the GQA
+// group = one m16 MMA tile) and a share of the pages; fp8 -> f16 conversion is exact,
+// QK^T and PV run on mma.sync m16n8k16 with fp32 accumulation, softmax in fp32 (log2
+// units).  P * vscale is scaled by 2^8 before the f16 rounding (round-to-nearest, no
+// truncation bias) and the factor is removed in fp32 afterwards.
+// decode_combine_kernel: LSE-weighted merge of the segments of each (query row, head).
+#include "kernels.h"
+#include "sm103_ptx.cuh"
+
+namespace gcs {
+namespace {
+
+constexpr int kPage = 16;
+constexpr int kD = 128;
+constexpr int kGroup = 16;
+constexpr int kStage = 4352;  // K 2048 | V 2048 | kscale 64 | vscale 64 | pad
+constexpr int kNST = 8;
+constexpr int kThreads = 160;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kPScale = 256.f;
+constexpr float kInvPScale = 1.f / 256.f;
+
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
+
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
+
+// two e4m3 bytes (low byte = first element) -> f16x2 (low half = first element)
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t x, uint32_t& lo, uint32_t& hi) {
+  asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n"
+      " cvt.rn.f16x2.e4m3x2 %0, a;\n cvt.rn.f16x2.e4m3x2 %1, b;\n}\n"
+      : "=r"(lo), "=r"(hi)
+      : "r"(x));
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+__device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t bf16pair_to_f16x2(uint32_t w) {
+  const float lo = __uint_as_float(w << 16);
+  const float hi = __uint_as_float(w & 0xffff0000u);
+  return pack_f16x2(lo, hi);
+}
+
+__global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodeParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ uint64_t full[kNST], empty[kNST];
+  __shared__ int abort_flag_s;
+  const int seg = blockIdx.x, kvh = blockIdx.y, r = blockIdx.z;
+  const int L = __ldg(p.seq_lens + r);
+  const int q_begin = __ldg(p.cu_q + r);
+  const int ql = __ldg(p.cu_q + r + 1) - q_begin;
+  const int npages = (L + kPage - 1) / kPage;
+  const int pb = seg * p.seg_pages;
+  if (pb >= npages || ql < 1 || ql > 4) return;
+  const int np = min(pb + p.seg_pages, npages) - pb;
+  const int ng = 4 / ql;  // page groups
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kNST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], ql);
+    }
+    abort_flag_s = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const Abort ab{&abort_flag_s, p.status};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ page producer
+    const int32_t* trow = p.block_table + (size_t)r * p.max_blocks + pb;
+    bool ok = true;
+    for (int base = 0; base < np && ok; base += 32) {
+      const int blk_l = (base + lane < np) ? __ldg(trow + base + lane) : 0;
+      const int cnt = min(32, np - base);
+      for (int ii = 0; ii < cnt; ++ii) {
+        const int blk = __shfl_sync(0xffffffffu, blk_l, ii);
+        if (lane == 0 && ok) {
+          const int i = base + ii;
+          const int stage = i % kNST;
+          const uint32_t par = ((i / kNST) & 1) ^ 1;
+          ok = wait_bar(&empty[stage], par, ab);
+          if (ok) {
+            uint8_t* st = smem + stage * kStage;
+            const size_t slot0 = ((size_t)blk * p.hkv + kvh) * kPage;
+            mbar_expect_tx(&full[stage], 2 * kPage * kD + 2 * kPage * 4);
+            bulk_load(st, p.k_cache + slot0 * kD, kPage * kD, &full[stage]);
+            bulk_load(st + 2048, p.v_cache + slot0 * kD, kPage * kD, &full[stage]);
+            bulk_load(st + 4096, p.k_scale + slot0, kPage * 4, &full[stage]);
+            bulk_load(st + 4160, p.v_scale + slot0, kPage * 4, &full[stage]);
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int cw = warp - 1;
+  const int mt = cw % ql, grp = cw / ql;
+  const bool active = grp < ng;
+  const int g = lane >> 2, tq = lane & 3;
+  const int lastk = L - ql + mt;  // last key visible to this query position
+  const float sl2 = p.scale * kLog2e;
+  float o[16][4];
+#pragma unroll
+  for (int u = 0; u < 16; ++u) o[u][0] = o[u][1] = o[u][2] = o[u][3] = 0.f;
+  float m0 = neg_inf(), m1 = neg_inf(), l0 = 0.f, l1 = 0.f;
+  bool ok = true;
+
+  if (active) {
+    uint32_t qa[8][4];
+    {
+      const uint16_t* q0p = p.q + ((size_t)(q_begin + mt) * p.hq + kvh * kGroup + g) * kD + 32 * tq;
+      const uint16_t* q1p = q0p + 8 * kD;
+      uint32_t w0[16], w1[16];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 a = __ldg(reinterpret_cast<const uint4*>(q0p) + j);
+        const uint4 b = __ldg(reinterpret_cast<const uint4*>(q1p) + j);
+        w0[4 * j] = a.x; w0[4 * j + 1] = a.y; w0[4 * j + 2] = a.z; w0[4 * j + 3] = a.w;
+        w1[4 * j] = b.x; w1[4 * j + 1] = b.y; w1[4 * j + 2] = b.z; w1[4 * j + 3] = b.w;
+      }
+      // k-step s covers physical dims 32tq + 4s .. 32tq + 4s + 3 of this thread
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        qa[s][0] = bf16pair_to_f16x2(w0[2 * s]);
+        qa[s][1] = bf16pair_to_f16x2(w1[2 * s]);
+        qa[s][2] = bf16pair_to_f16x2(w0[2 * s + 1]);
+        qa[s][3] = bf16pair_to_f16x2(w1[2 * s + 1]);
+      }
+    }
+    for (int i = grp; i < np; i += ng) {
+      const int stage = i % kNST;
+      ok = wait_bar(&full[stage], (i / kNST) & 1, ab);
+      if (!ok) break;
+      const uint8_t* st = smem + stage * kStage;
+      const uint4 ka0 = lds128(st + g * kD + 32 * tq);
+      const uint4 ka1 = lds128(st + g * kD + 32 * tq + 16);
+      const uint4 kb0 = lds128(st + (8 + g) * kD + 32 * tq);
+      const uint4 kb1 = lds128(st + (8 + g) * kD + 32 * tq + 16);
+      uint4 v0 = lds128(st + 2048 + (2 * tq) * kD + 16 * g);
+      uint4 v1 = lds128(st + 2048 + (2 * tq + 1) * kD + 16 * g);
+      uint4 v2 = lds128(st + 2048 + (2 * tq + 8) * kD + 16 * g);
+      uint4 v3 = lds128(st + 2048 + (2 * tq + 9) * kD + 16 * g);
+      const float2 ksA = *reinterpret_cast<const float2*>(st + 4096 + 8 * tq);
+      const float2 ksB = *reinterpret_cast<const float2*>(st + 4096 + 32 + 8 * tq);
+      const float2 vsA = *reinterpret_cast<const float2*>(st + 4160 + 8 * tq);
+      const float2 vsB = *reinterpret_cast<const float2*>(st + 4160 + 32 + 8 * tq);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
+
+      // S = q . k8 over the page: n-tile 0 = slots 0..7, n-tile 1 = slots 8..15
+      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint32_t kw0[8] = {ka0.x, ka0.y, ka0.z, ka0.w, ka1.x, ka1.y, ka1.z, ka1.w};
+      const uint32_t kw1[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        uint32_t b0, b1;
+        e4m3x4_to_f16x2x2(kw0[s], b0, b1);
+        mma_f16(s0, qa[s], b0, b1);
+        e4m3x4_to_f16x2x2(kw1[s], b0, b1);
+        mma_f16(s1, qa[s], b0, b1);
+      }
+      // this thread's columns: slots 2tq, 2tq+1 (n-tile 0) and 8+2tq, 9+2tq (n-tile 1)
+      const int tok0 = (pb + i) * kPage + 2 * tq;
+      const int tk[4] = {tok0, tok0 + 1, tok0 + 8, tok0 + 9};
+      const float ks[4] = {ksA.x, ksA.y, ksB.x, ksB.y};
+      float x[2][4];  // [row g / g+8][column]
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const bool vis = tk[c] <= lastk;
+        const float sa = (c < 2) ? s0[c] : s1[c - 2];
+        const float sb = (c < 2) ? s0[c + 2] : s1[c];
+        x[0][c] = vis ? sa * sl2 * ks[c] : neg_inf();
+        x[1][c] = vis ? sb * sl2 * ks[c] : neg_inf();
+      }
+      float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[0][2], x[0][3]));
+      float mx1 = fmaxf(fmaxf(x[1][0], x[1][1]), fmaxf(x[1][2], x[1][3]));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+      const float a0 = (n0 == neg_inf()) ? 1.f : ex2(m0 - n0);
+      const float a1 = (n1 == neg_inf()) ? 1.f : ex2(m1 - n1);
+      const float u0 = (n0 == neg_inf()) ? 0.f : n0;
+      const float u1 = (n1 == neg_inf()) ? 0.f : n1;
+      m0 = n0;
+      m1 = n1;
+      float pr[2][4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        pr[0][c] = ex2(x[0][c] - u0);
+        pr[1][c] = ex2(x[1][c] - u1);
+      }
+      l0 = l0 * a0 + (pr[0][0] + pr[0][1]) + (pr[0][2] + pr[0][3]);
+      l1 = l1 * a1 + (pr[1][0] + pr[1][1]) + (pr[1][2] + pr[1][3]);
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        o[u][0] *= a0;
+        o[u][1] *= a0;
+        o[u][2] *= a1;
+        o[u][3] *= a1;
+      }
+      // V scales multiply the probabilities after the row sum; slots >= L get scale 0
+      float vs[4] = {vsA.x, vsA.y, vsB.x, vsB.y};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) vs[c] = (tk[c] < L) ? vs[c] * kPScale : 0.f;
+      uint32_t pa[4];
+      pa[0] = pack_f16x2(pr[0][0] * vs[0], pr[0][1] * vs[1]);
+      pa[1] = pack_f16x2(pr[1][0] * vs[0], pr[1][1] * vs[1]);
+      pa[2] = pack_f16x2(pr[0][2] * vs[2], pr[0][3] * vs[3]);
+      pa[3] = pack_f16x2(pr[1][2] * vs[2], pr[1][3] * vs[3]);
+      // value bytes of slots past seq_len are never multiplied (NaN codes allowed there)
+      if (tk[0] >= L) v0 = make_uint4(0, 0, 0, 0);
+      if (tk[1] >= L) v1 = make_uint4(0, 0, 0, 0);
+      if (tk[2] >= L) v2 = make_uint4(0, 0, 0, 0);
+      if (tk[3] >= L) v3 = make_uint4(0, 0, 0, 0);
+      const uint32_t va[4] = {v0.x, v0.y, v0.z, v0.w}, vb[4] = {v1.x, v1.y, v1.z, v1.w};
+      const uint32_t vc[4] = {v2.x, v2.y, v2.z, v2.w}, vd[4] = {v3.x, v3.y, v3.z, v3.w};
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        uint32_t lo01, hi01, lo23, hi23;
+        // bytes (4w, 4w+1) of slots (2tq, 2tq+1) interleaved, then bytes (4w+2, 4w+3)
+        const uint32_t ab01 = prmt(va[w], vb[w], 0x5140);
+        const uint32_t ab23 = prmt(va[w], vb[w], 0x7362);
+        const uint32_t cd01 = prmt(vc[w], vd[w], 0x5140);
+        const uint32_t cd23 = prmt(vc[w], vd[w], 0x7362);
+        uint32_t b0, b1;
+        e4m3x4_to_f16x2x2(ab01, lo01, hi01);
+        e4m3x4_to_f16x2x2(cd01, b0, b1);
+        mma_f16(o[4 * w + 0], pa, lo01, b0);
+        mma_f16(o[4 * w + 1], pa, hi01, b1);
+        e4m3x4_to_f16x2x2(ab23, lo23, hi23);
+        e4m3x4_to_f16x2x2(cd23, b0, b1);
+        mma_f16(o[4 * w + 2], pa, lo23, b0);
+        mma_f16(o[4 * w + 3], pa, hi23, b1);
+      }
+    }
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  }
+
+  // ------------------------------------------------ merge page groups, write the partial
+  // thread (g, tq) holds dims 32tq + u (o[u][0], o[u][2]) and 32tq + 16 + u (o[u][1], o[u][3])
+  float* red = reinterpret_cast<float*>(smem);  // reuses the ring: [4 warps][16 rows][130]
+  if (ng > 1) {
+    named_bar_sync(1, 128);  // every consumer is done with the ring
+    if (active) {
+      float* mine = red + cw * (16 * 130);
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        mine[g * 130 + 32 * tq + u] = o[u][0];
+        mine[g * 130 + 32 * tq + 16 + u] = o[u][1];
+        mine[(g + 8) * 130 + 32 * tq + u] = o[u][2];
+        mine[(g + 8) * 130 + 32 * tq + 16 + u] = o[u][3];
+      }
+      if (tq == 0) {
+        mine[g * 130 + 128] = m0;
+        mine[g * 130 + 129] = l0;
+        mine[(g + 8) * 130 + 128] = m1;
+        mine[(g + 8) * 130 + 129] = l1;
+      }
+    }
+    named_bar_sync(1, 128);
+    if (active && grp == 0) {
+      for (int gg = 1; gg < ng; ++gg) {
+        const float* other = red + (gg * ql + mt) * (16 * 130);
+        const float om0 = other[g * 130 + 128], ol0 = other[g * 130 + 129];
+        const float om1 = other[(g + 8) * 130 + 128], ol1 = other[(g + 8) * 130 + 129];
+        const float n0 = fmaxf(m0, om0), n1 = fmaxf(m1, om1);
+        const float wa0 = (m0 == neg_inf()) ? 0.f : ex2(m0 - n0);
+        const float wb0 = (om0 == neg_inf()) ? 0.f : ex2(om0 - n0);
+        const float wa1 = (m1 == neg_inf()) ? 0.f : ex2(m1 - n1);
+        const float wb1 = (om1 == neg_inf()) ? 0.f : ex2(om1 - n1);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          o[u][0] = o[u][0] * wa0 + other[g * 130 + 32 * tq + u] * wb0;
+          o[u][1] = o[u][1] * wa0 + other[g * 130 + 32 * tq + 16 + u] * wb0;
+          o[u][2] = o[u][2] * wa1 + other[(g + 8) * 130 + 32 * tq + u] * wb1;
+          o[u][3] = o[u][3] * wa1 + other[(g + 8) * 130 + 32 * tq + 16 + u] * wb1;
+        }
+        l0 = l0 * wa0 + ol0 * wb0;
+        l1 = l1 * wa1 + ol1 * wb1;
+        m0 = n0;
+        m1 = n1;
+      }
+    }
+  }
+  if (active && grp == 0) {
+    const size_t unit = ((size_t)r * p.max_segs + seg) * p.hkv + kvh;
+    const int rows = p.max_q_len * kGroup;
+    const size_t row0 = unit * rows + mt * kGroup + g;
+    float4* d0 = reinterpret_cast<float4*>(p.part_acc + row0 * kD + 32 * tq);
+    float4* d1 = reinterpret_cast<float4*>(p.part_acc + (row0 + 8) * kD + 32 * tq);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      d0[k] = make_float4(o[4 * k][0] * kInvPScale, o[4 * k + 1][0] * kInvPScale, o[4 * k + 2][0] * kInvPScale,
+                          o[4 * k + 3][0] * kInvPScale);
+      d0[4 + k] = make_float4(o[4 * k][1] * kInvPScale, o[4 * k + 1][1] * kInvPScale, o[4 * k + 2][1] * kInvPScale,
+                              o[4 * k + 3][1] * kInvPScale);
+      d1[k] = make_float4(o[4 * k][2] * kInvPScale, o[4 * k + 1][2] * kInvPScale, o[4 * k + 2][2] * kInvPScale,
+                          o[4 * k + 3][2] * kInvPScale);
+      d1[4 + k] = make_float4(o[4 * k][3] * kInvPScale, o[4 * k + 1][3] * kInvPScale,
+                              o[4 * k + 2][3] * kInvPScale, o[4 * k + 3][3] * kInvPScale);
+    }
+    if (tq == 0) {
+      reinterpret_cast<float2*>(p.part_ml)[row0] = make_float2(m0, l0);
+      reinterpret_cast<float2*>(p.part_ml)[row0 + 8] = make_float2(m1, l1);
+    }
+  }
+}
+
+// One CTA per (request, query position) x kv head; 256 threads = 16 heads x 16 threads,
+// 8 value dims per thread.
+__global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams p) {
+  const int r = blockIdx.x / p.max_q_len, t = blockIdx.x % p.max_q_len;
+  const int kvh = blockIdx.y;
+  const int q_begin = __ldg(p.cu_q + r);
+  const int ql = __ldg(p.cu_q + r + 1) - q_begin;
+  if (t >= ql) return;
+  const int L = __ldg(p.seq_lens + r);
+  const int npages = (L + kPage - 1) / kPage;
+  const int nseg = (npages + p.seg_pages - 1) / p.seg_pages;
+  const int hh = threadIdx.x >> 4, d0 = (threadIdx.x & 15) * 8;
+  const int rows = p.max_q_len * kGroup;
+  const int row = t * kGroup + hh;
+  auto unit_row = [&](int s) { return ((((size_t)r * p.max_segs + s) * p.hkv + kvh) * rows + row); };
+  const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
+  float M = neg_inf();
+  for (int s = 0; s < nseg; ++s) M = fmaxf(M, ml[unit_row(s)].x);
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  float den = 0.f;
+  for (int s = 0; s < nseg; ++s) {
+    const float2 v = ml[unit_row(s)];
+    const float w = (v.x == neg_inf()) ? 0.f : ex2(v.x - M);  // empty partial weighs 0
+    den += w * v.y;
+    const float4* a = reinterpret_cast<const float4*>(p.part_acc + unit_row(s) * kD + d0);
+    const float4 x0 = a[0], x1 = a[1];
+    acc[0] += w * x0.x; acc[1] += w * x0.y; acc[2] += w * x0.z; acc[3] += w * x0.w;
+    acc[4] += w * x1.x; acc[5] += w * x1.y; acc[6] += w * x1.z; acc[7] += w * x1.w;
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  uint4 outv;
+  outv.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+  outv.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+  outv.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+  outv.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+  *reinterpret_cast<uint4*>(p.out + ((size_t)(q_begin + t) * p.hq + kvh * kGroup + hh) * kD + d0) = outv;
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s) {
+  const int smem = kNST * kStage;
+  dim3 g1(p.max_segs, p.hkv, p.num_reqs);
+  decode_split_kernel<<<g1, kThreads, smem, s>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  dim3 g2(p.num_reqs * p.max_q_len, p.hkv);
+  decode_combine_kernel<<<g2, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace gcs

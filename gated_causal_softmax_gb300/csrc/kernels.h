@@ -1,0 +1,91 @@
+// Internal launch interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace gcs {
+
+// Per-device status word (GCS_OK / GCS_ERR_DEVICE_TIMEOUT), written by kernels.
+int* device_status_ptr();
+
+struct FwdParams {
+  const int32_t* cu_seqlens;
+  int num_seqs;
+  int total;
+  int hq, hkv, dqk, dv;
+  int dv_chunk;          // value columns handled by one CTA
+  float scale_log2;      // scale * log2(e)
+  int window;            // 0 = none
+  const float* gT;       // G^T [hq, total] in log2 units (gate cumsum * log2 e), or null
+  const float* sink;     // [hq] natural-log sink logits, or null
+  uint16_t* o;           // bf16 [total, hq, dv]
+  float* lse;            // [hq, total]
+  int* status;
+};
+
+struct FwdMaps {
+  CUtensorMap q, k, v;  // 2-D bf16 maps, box 64 x 128, 128-B swizzle
+};
+
+cudaError_t launch_prefill_fwd(const FwdParams& p, const FwdMaps& maps, int num_tiles, cudaStream_t s);
+
+struct BwdParams {
+  const int32_t* cu_seqlens;
+  int num_seqs;
+  int total;
+  int hq, hkv, dqk, dv;
+  float scale;           // softmax scale
+  float scale_log2;      // scale * log2(e)
+  int window;
+  const float* gT;       // G^T [hq, total] (log2 units) or null
+  const float* lse;      // [hq, total] natural log
+  const float* delta;    // [hq, total] rowsum(dO * O)
+  uint16_t* grad_k;      // bf16 [total, hkv, dqk]
+  uint16_t* grad_v;      // bf16 [total, hkv, dv]
+  float* dq_acc;         // fp32 [total, hq, dqk] (zeroed)
+  float* dg_row;         // fp32 [hq, total] sum_j dS_ij (zeroed); null if not needed
+  float* dg_col;         // fp32 [hq, total] sum_i dS_ij; null if no gate
+  int* status;
+};
+
+struct BwdMaps {
+  CUtensorMap q, k, v, dout;  // 2-D bf16 maps, 128-B swizzle
+};
+
+cudaError_t launch_prefill_bwd(const BwdParams& p, const BwdMaps& maps, int num_kv_tiles, cudaStream_t s);
+
+// Small HBM-bound helpers.
+cudaError_t launch_gate_cumsum(const float* g, const int32_t* cu, int num_seqs, int total, int hq, float* gT,
+                               cudaStream_t s);
+cudaError_t launch_bwd_pre(const uint16_t* o, const uint16_t* dout, int total, int hq, int dv, int dqk,
+                           float* delta, float* dq_acc, float* dg_row, float* dsink, cudaStream_t s);
+cudaError_t launch_bwd_post(const float* dq_acc, uint16_t* dq, int total, int hq, int dqk, const int32_t* cu,
+                            int num_seqs, const float* dg_row, const float* dg_col, float* dlog_gate,
+                            const float* lse, const float* delta, const float* sink, float* dsink, cudaStream_t s);
+
+struct DecodeParams {
+  const int32_t* cu_q;
+  const int32_t* seq_lens;
+  const int32_t* block_table;
+  int max_blocks;
+  const uint8_t* k_cache;
+  const uint8_t* v_cache;
+  const float* k_scale;
+  const float* v_scale;
+  int num_reqs, hq, hkv;
+  int max_q_len;
+  int max_segs;          // segments per request slot in the partial buffers
+  int seg_pages;         // pages per segment
+  float scale;
+  const uint16_t* q;     // bf16 [total_q, hq, 128]
+  uint16_t* out;         // bf16 [total_q, hq, 128]
+  float* part_acc;       // [units, 4*16, 128]
+  float* part_ml;        // [units, 4*16, 2]
+  int* status;
+};
+
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s);
+
+}  // namespace gcs

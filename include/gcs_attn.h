@@ -1,0 +1,168 @@
+/*
+ * gcs_attn.h -- C ABI of the GB300 (sm_103a) gated causal softmax attention library.
+ *
+ * Three calls make up the hot path:
+ *   attn_fwd           prefill forward  (O, LSE)
+ *   attn_bwd           prefill backward (dQ, dK, dV, d log_gate, d sink)
+ *   attn_decode_paged  paged single-query / short-query decode over an fp8 e4m3 KV cache
+ *
+ * Sources for what each call computes (page title, section):
+ *   [FLA] fla-org/flash-linear-attention issue #1322 "[Perf] Gluon attention backend with
+ *         large head dimensions" -- Description: the causal attention contract (dense and
+ *         packed variable-length inputs, MHA/GQA/MQA, unequal query/key and value head
+ *         dims up to 512, logarithmic gates, sliding windows, sink bias, gradients);
+ *         comment of Oct 3: the sink gradient is accumulated in fp32 from the backward
+ *         probabilities, not from the rounded output; comment of Oct 5: dQ partials
+ *         accumulate into a zero-initialised fp32 buffer and are converted afterwards.
+ *   [AIT] ROCm/aiter PR #6660 (gfx1250 unified attention) -- commit messages and
+ *         "Technical details": per-token fp32 K/V scales laid out [num_blocks,
+ *         num_kv_heads, block_size]; K scales multiply QK columns; V scales multiply P
+ *         columns after the row sum; slots past seq_len get scale 0; split-K over context
+ *         segments with an LSE-weighted reduce in which an empty partial (M = -inf)
+ *         weighs 0; per-token scales on a prefill shape are rejected.
+ *
+ * Conventions for every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller (inputs, outputs and
+ *     workspace).  The library never allocates, frees or synchronises.
+ *   - Every call is asynchronous on the given stream.  Arguments are validated on the
+ *     host first; on any error the call returns a nonzero gcs_status and launches
+ *     nothing, so outputs are untouched.
+ *   - Tensors are contiguous, row-major, last dimension fastest; base addresses are
+ *     16-byte aligned.
+ *   - bf16 = bfloat16 stored as uint16; fp8 = OCP e4m3 ("fn") stored as uint8.
+ *   - Device-side contents (cu_seqlens monotone and ending at total_tokens, page-table
+ *     entries in [0, num_blocks), seq_lens >= q_len) are preconditions; they are not
+ *     checked on the host because reading them would synchronise.
+ *   - Every wait inside a kernel is bounded (2 s).  A kernel that gives up records
+ *     GCS_ERR_DEVICE_TIMEOUT in a per-device status word, releases its resources and
+ *     returns; read it with gcs_get_device_status().
+ */
+#ifndef GCS_ATTN_H_
+#define GCS_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* gcs_stream_t; /* same type as cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  GCS_OK = 0,
+  GCS_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned base, inconsistent shape */
+  GCS_ERR_UNSUPPORTED = 2,   /* a shape / dtype / layout this library does not implement   */
+  GCS_ERR_WORKSPACE = 3,     /* workspace pointer NULL or smaller than the *_workspace size */
+  GCS_ERR_CUDA = 4,          /* a CUDA launch or runtime call failed                       */
+  GCS_ERR_DEVICE_TIMEOUT = 5 /* a kernel gave up on a bounded wait (device status word)    */
+} gcs_status;
+
+const char* gcs_status_str(int status);
+
+/* ------------------------------------------------------------------ prefill
+ * Causal softmax attention over packed sequences ([FLA] Description).
+ * Sequence s occupies tokens cu_seqlens[s] .. cu_seqlens[s+1]-1 of the packed tensors;
+ * dense [B, T] inputs are the special case cu_seqlens = {0, T, 2T, ..., B*T}.
+ * Query head h reads kv head h / (hq / hkv) (MHA: hq == hkv; MQA: hkv == 1).
+ * Score of query token i and key token j of the same sequence:
+ *     s_ij = scale * (q_i . k_j) + G_i - G_j,   G = per-sequence inclusive cumsum of log_gate
+ * visible iff j <= i and (window == 0 or i - j < window).  The per-head sink logit sigma_h
+ * joins the softmax denominator only:  P_ij = e^{s_ij} / (sum_j e^{s_ij} + e^{sigma_h}).
+ * Supported (dqk, dv): (64, 64), (128, 128), (256, 256), (256, 512), (512, 512).
+ */
+typedef struct {
+  int num_seqs;               /* >= 1                                                    */
+  const int32_t* cu_seqlens;  /* device int32 [num_seqs + 1]                            */
+  int total_tokens;           /* host copy of cu_seqlens[num_seqs]; >= 1                */
+  int max_seqlen;             /* host upper bound on any sequence length                */
+  int hq, hkv;                /* query heads, kv heads; hq % hkv == 0                    */
+  int dqk, dv;                /* head dims of q/k and of v                               */
+  float scale;                /* softmax scale (usually 1/sqrt(dqk))                     */
+  int window;                 /* 0 = none, else number of visible keys including self    */
+  const void* q;              /* bf16 [total_tokens, hq, dqk]                            */
+  const void* k;              /* bf16 [total_tokens, hkv, dqk]                           */
+  const void* v;              /* bf16 [total_tokens, hkv, dv]                            */
+  const float* log_gate;      /* fp32 [total_tokens, hq] per-token log forget gates, or NULL */
+  const float* sink;          /* fp32 [hq] sink logits, or NULL                          */
+} gcs_prefill_args;
+
+/* Workspace bytes attn_fwd needs (0 when there is no gate). */
+size_t attn_fwd_workspace(const gcs_prefill_args* a);
+
+/* Forward.  o: bf16 [total_tokens, hq, dv]; lse: fp32 [hq, total_tokens], natural-log
+ * logsumexp of each row's scores including the sink term (needed by attn_bwd). */
+int attn_fwd(const gcs_prefill_args* a, void* o, float* lse, void* workspace, size_t workspace_bytes,
+             gcs_stream_t stream);
+
+/* Workspace bytes attn_bwd needs. */
+size_t attn_bwd_workspace(const gcs_prefill_args* a);
+
+/* Backward of L = sum(O * dO) ([FLA] Description "gradients"; Oct 3 / Oct 5 comments).
+ * o, lse: the forward's outputs; dout: bf16 [total_tokens, hq, dv].
+ * Outputs: dq bf16 [total_tokens, hq, dqk], dk bf16 [total_tokens, hkv, dqk],
+ * dv bf16 [total_tokens, hkv, dv], dlog_gate fp32 [total_tokens, hq] (must be NULL iff
+ * log_gate is NULL), dsink fp32 [hq] (must be NULL iff sink is NULL).
+ * The sink gradient is -sum_i p_sink,i * sum_j P_ij (dO_i . v_j), accumulated in fp32.
+ * fp32 reduce-adds make low bits of dq, dlog_gate and dsink vary from run to run. */
+int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const void* dout, void* dq, void* dk,
+             void* dv, float* dlog_gate, float* dsink, void* workspace, size_t workspace_bytes,
+             gcs_stream_t stream);
+
+/* ------------------------------------------------------------------ paged decode
+ * Decode / short-query attention over a paged fp8 e4m3 KV cache with per-token fp32 scales
+ * ([AIT] commits 1-3, Technical details).  Request r has q_len = cu_q[r+1] - cu_q[r] query
+ * rows (1..4) and seq_len = seq_lens[r] cached tokens (the query tokens are the last
+ * q_len of them); query row t sits at position seq_len - q_len + t and sees keys
+ * 0 .. seq_len - q_len + t.  Key j of request r lives in block block_table[r][j / block_size],
+ * slot j % block_size.  Dequantised key = e4m3(k) * k_scale[block][kv_head][slot], same for
+ * values.  s_j = scale * k_scale_j * (q . k8_j); the row sum uses the unscaled e^{s_j - m};
+ * the V scales multiply the probabilities after the row sum.  Slots at or past seq_len are
+ * never used (scale 0, probability 0), whatever their bytes or scales hold (NaN allowed).
+ * The context is split into segments of segment_len tokens; each (request, kv head,
+ * segment) yields a partial (acc, M, L) and a combine kernel merges them with weights
+ * e^{M_s - max M}; a partial with no visible key (M = -inf) weighs 0.
+ * Supported: d == 128, block_size == 16, hq / hkv == 16, 1 <= q_len <= 4,
+ * segment_len a positive multiple of block_size.
+ */
+typedef struct {
+  int num_reqs;                /* >= 1                                                   */
+  const int32_t* cu_q;         /* device int32 [num_reqs + 1]                           */
+  int total_q;                 /* host copy of cu_q[num_reqs]                           */
+  int max_q_len;               /* host upper bound on q_len, 1..4                        */
+  const int32_t* seq_lens;     /* device int32 [num_reqs], each >= its q_len             */
+  int max_seq_len;             /* host upper bound on seq_lens                           */
+  const int32_t* block_table;  /* device int32 [num_reqs, max_blocks_per_req]           */
+  int max_blocks_per_req;      /* row stride of block_table                             */
+  const uint8_t* k_cache;      /* fp8 e4m3 [num_blocks, hkv, block_size, d]             */
+  const uint8_t* v_cache;      /* fp8 e4m3 [num_blocks, hkv, block_size, d]             */
+  const float* k_scale;        /* fp32 [num_blocks, hkv, block_size]                    */
+  const float* v_scale;        /* fp32 [num_blocks, hkv, block_size]                    */
+  int num_blocks, block_size;  /* cache blocks, tokens per block                        */
+  int hq, hkv, d;              /* query heads, kv heads, head dim                       */
+  float scale;                 /* softmax scale                                         */
+  int segment_len;             /* split-K segment length in tokens                      */
+  const void* q;               /* bf16 [total_q, hq, d]                                 */
+} gcs_decode_args;
+
+/* Workspace bytes attn_decode_paged needs (split-K partials). */
+size_t attn_decode_workspace(const gcs_decode_args* a);
+
+/* out: bf16 [total_q, hq, d]. */
+int attn_decode_paged(const gcs_decode_args* a, void* out, void* workspace, size_t workspace_bytes,
+                      gcs_stream_t stream);
+
+/* ------------------------------------------------------------------ status
+ * Per-device status word written by kernels that gave up on a bounded wait.
+ * Copies the word for the current device into *status (synchronous) and, if clear != 0,
+ * resets it to GCS_OK.  Returns GCS_OK or GCS_ERR_CUDA. */
+int gcs_get_device_status(int* status, int clear);
+
+/* Library version string. */
+const char* gcs_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GCS_ATTN_H_ */

@@ -1,0 +1,108 @@
+"""Host-side tests of the C ABI (no GPU needed): the library builds for sm_103a, loads,
+exports every function include/gcs_attn.h declares, and rejects bad arguments on the host
+before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gcs_attn.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w]*\s*\*?\s*([A-Za-z_]\w*)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "while")))
+
+
+@pytest.fixture(scope="module")
+def L():
+    import gated_causal_softmax_gb300 as gcs
+
+    return gcs.load()
+
+
+def test_header_declares_the_three_calls():
+    names = declared_functions()
+    for n in ("attn_fwd", "attn_bwd", "attn_decode_paged", "attn_fwd_workspace", "attn_bwd_workspace",
+              "attn_decode_workspace", "gcs_get_device_status", "gcs_status_str", "gcs_version"):
+        assert n in names, n
+
+
+def test_library_exports_every_declared_symbol(L):
+    for n in declared_functions():
+        assert hasattr(L, n), f"missing export {n}"
+    assert L.gcs_version().startswith(b"gcs_attn")
+    assert L.gcs_status_str(2) == b"unsupported shape, dtype or layout"
+
+
+FAKE = 0x10000  # 16-B aligned, never dereferenced by host validation
+
+
+def prefill(**over):
+    import gated_causal_softmax_gb300 as gcs
+
+    kw = dict(num_seqs=1, cu_seqlens=FAKE, total_tokens=256, max_seqlen=256, hq=4, hkv=2, dqk=128, dv=128,
+              scale=0.088, window=0, q=FAKE, k=FAKE, v=FAKE, log_gate=None, sink=None)
+    kw.update(over)
+    return gcs.PrefillArgs(**kw)
+
+
+def decode(**over):
+    import gated_causal_softmax_gb300 as gcs
+
+    kw = dict(num_reqs=2, cu_q=FAKE, total_q=2, max_q_len=1, seq_lens=FAKE, max_seq_len=4096, block_table=FAKE,
+              max_blocks_per_req=256, k_cache=FAKE, v_cache=FAKE, k_scale=FAKE, v_scale=FAKE, num_blocks=600,
+              block_size=16, hq=64, hkv=4, d=128, scale=0.088, segment_len=2048, q=FAKE)
+    kw.update(over)
+    return gcs.DecodeArgs(**kw)
+
+
+def test_prefill_validation_on_host(L):
+    b = ctypes.byref
+    fwd = lambda a: L.attn_fwd(b(a), FAKE, FAKE, FAKE, 1 << 30, None)
+    assert fwd(prefill(hq=3, hkv=2)) == 1  # hq % hkv
+    assert fwd(prefill(q=None)) == 1
+    assert fwd(prefill(q=FAKE + 2)) == 1  # misaligned
+    assert fwd(prefill(window=-1)) == 1
+    assert fwd(prefill(scale=float("nan"))) == 1
+    assert fwd(prefill(dqk=96, dv=96)) == 2  # not a compiled head dim
+    assert fwd(prefill(dqk=128, dv=256)) == 2
+    assert L.attn_fwd(b(prefill()), None, FAKE, FAKE, 0, None) == 1  # no output
+    # gated forward needs a workspace
+    assert L.attn_fwd(b(prefill(log_gate=FAKE)), FAKE, FAKE, None, 0, None) == 3
+    bwd = lambda a, **k: L.attn_bwd(b(a), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, k.get("dg"), k.get("ds"), FAKE,
+                                    1 << 40, None)
+    assert bwd(prefill(log_gate=FAKE)) == 1  # dlog_gate must be given iff log_gate is
+    assert bwd(prefill(sink=FAKE)) == 1
+    assert bwd(prefill(), dg=FAKE) == 1
+
+
+def test_workspace_sizes_on_host(L):
+    b = ctypes.byref
+    assert L.attn_fwd_workspace(b(prefill())) == 0
+    assert L.attn_fwd_workspace(b(prefill(log_gate=FAKE))) == 4 * 4 * 256
+    ws = L.attn_bwd_workspace(b(prefill(log_gate=FAKE, sink=FAKE)))
+    # G^T, delta, dQ accumulator, dS row sums, dS column sums
+    assert ws == 4 * (4 * 256) * 4 + 4 * 256 * 4 * 128
+    units, rows = 2 * 2 * 4, 16
+    assert L.attn_decode_workspace(b(decode())) == units * rows * 128 * 4 + units * rows * 2 * 4
+    assert L.attn_decode_workspace(b(decode(max_q_len=5))) == 0
+
+
+def test_decode_validation_on_host(L):
+    b = ctypes.byref
+    dec = lambda a: L.attn_decode_paged(b(a), FAKE, FAKE, 1 << 40, None)
+    # per-token scales on a prefill shape are rejected
+    assert dec(decode(max_q_len=5)) == 2
+    assert dec(decode(block_size=32)) == 2
+    assert dec(decode(d=64)) == 2
+    assert dec(decode(hq=32)) == 2  # GQA group must be 16
+    assert dec(decode(segment_len=2040)) == 2
+    assert dec(decode(k_scale=None)) == 1
+    assert dec(decode(max_blocks_per_req=10)) == 1  # table too short for max_seq_len
+    assert L.attn_decode_paged(b(decode()), FAKE, None, 0, None) == 3
+    assert L.attn_decode_paged(b(decode()), FAKE + 8, FAKE, 1 << 40, None) == 1

@@ -1,0 +1,125 @@
+"""Device parity: paged fp8 decode through the C ABI against the fp64 oracle on the
+dequantised cache (unused slots NaN-poisoned), relative RMS <= 1e-2 and |bias| <= 1e-3."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synth import decode_config, make_decode
+from helpers import DECODE_BIAS, DECODE_RTOL, assert_close, bias, decode_dev, f64, oracle_decode, run_decode
+
+pytestmark = pytest.mark.gpu
+
+
+CASES = {
+    # name: (seq_lens, q_lens, hq, hkv, reading, segment_len)
+    "q1_page_edges": ([1, 15, 16, 17, 100, 2047, 2048, 2049, 5000], [1] * 9, 16, 1, "A", 2048),
+    "q1_gqa16_hkv4": ([3000, 33, 700, 4097], [1] * 4, 64, 4, "A", 2048),
+    "short_query_tails": ([4, 17, 18, 20, 2049, 4100], [4, 4, 3, 2, 4, 3], 32, 2, "B", 2048),
+    "short_query_context_65537": ([65537, 300], [4, 2], 16, 1, "B", 2048),
+    "tiny_segments_empty_partials": ([40, 70, 5], [4, 3, 4], 16, 1, "A", 16),
+    "mixed_q_lens_reading_A": ([1000, 1001, 1003, 64], [1, 2, 4, 3], 32, 2, "A", 256),
+}
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_decode_parity(gcs_lib, name):
+    sl, ql, hq, hkv, reading, seg = CASES[name]
+    dc = make_decode(sl, ql, hq, hkv, 128, seed=200 + len(name), scale_reading=reading, segment_len=seg)
+    out = run_decode(gcs_lib, dc)
+    ref = oracle_decode(dc)
+    assert_close("out", out, ref, DECODE_RTOL)
+    assert abs(bias(out, ref)) <= DECODE_BIAS
+
+
+def test_decode_rejects_prefill_shapes(gcs_lib):
+    dc = make_decode([40], [5], 16, 1, 128, seed=3)
+    with pytest.raises(NotImplementedError):
+        run_decode(gcs_lib, dc)
+
+
+def test_decode_per_token_scales_matter(gcs_lib):
+    """Reading only the first scale of the cache (the bug the per-token path fixed) would be
+    far off: the scales span 20x."""
+    dc = make_decode([500, 1200], [1, 1], 16, 1, 128, seed=9)
+    out = run_decode(gcs_lib, dc)
+    ref = oracle_decode(dc)
+    vs = dc.v_scale.clone()
+    flat = vs.view(-1)
+    flat[:] = flat[torch.isfinite(flat)][0]
+    ks = dc.k_scale.clone()
+    fk = ks.view(-1)
+    fk[:] = fk[torch.isfinite(fk)][0]
+    wrong = oracle.decode_paged(f64(dc.q), dc.k_cache.numpy(), dc.v_cache.numpy(), ks.numpy(), vs.numpy(),
+                                dc.block_table.numpy(), dc.seq_lens.numpy(), dc.cu_q.numpy(), dc.scale)
+    assert oracle.rel_rms(wrong, ref) > 0.2
+    assert oracle.rel_rms(f64(out), ref) < DECODE_RTOL
+
+
+def test_decode_gather_order_is_exact(gcs_lib):
+    """One dominant key per (request, kv head) at a chosen slot; its value page holds the code
+    for the page id, so the output identifies the gathered (block, slot) exactly."""
+    sl = [37, 2050, 700]
+    dc = make_decode(sl, [1, 1, 1], 16, 1, 128, seed=11)
+    kc = dc.k_cache.clone()
+    vc = dc.v_cache.clone()
+    ks = dc.k_scale.clone()
+    vs = dc.v_scale.clone()
+    q = torch.zeros_like(dc.q)
+    q[:, :, 0] = 1.0
+    kc.zero_()  # code 0 = +0
+    picks = [5, 2049, 333]
+    for r, slot in enumerate(picks):
+        blk = int(dc.block_table[r, slot // 16])
+        kc[blk, 0, slot % 16, 0] = 0x7E  # 448
+        ks[blk, 0, slot % 16] = 1.0
+        # integer page identity in e4m3: codes for blk % 8 and (blk // 8) % 8 on dims 0 and 1
+        vc[blk, 0, slot % 16, 0] = int(torch.tensor(float(blk % 8)).to(torch.float8_e4m3fn).view(torch.uint8))
+        vc[blk, 0, slot % 16, 1] = int(torch.tensor(float((blk // 8) % 8)).to(torch.float8_e4m3fn).view(torch.uint8))
+        vs[blk, 0, slot % 16] = 1.0
+    dc.k_cache, dc.v_cache, dc.k_scale, dc.v_scale, dc.q = kc, vc, ks, vs, q
+    dc.scale = 1.0
+    out = run_decode(gcs_lib, dc).float().cpu()
+    for r, slot in enumerate(picks):
+        blk = int(dc.block_table[r, slot // 16])
+        assert out[r, :, 0].eq(float(blk % 8)).all(), (r, out[r, :, 0])
+        assert out[r, :, 1].eq(float((blk // 8) % 8)).all()
+
+
+def test_decode_full_size_64x1_sampled(gcs_lib):
+    dc = decode_config("paged_fp8_decode_64x1")
+    out = run_decode(gcs_lib, dc)
+    pick = [0, 7, 21, 40, 63]
+    sub = make_sub(dc, pick)
+    ref = oracle_decode(sub)
+    got = f64(out)[[int(dc.cu_q[r]) for r in pick]]
+    assert_close("out", got, ref, DECODE_RTOL)
+    assert abs(bias(got, ref)) <= DECODE_BIAS
+
+
+def test_decode_full_size_verify_3x4_227k(gcs_lib):
+    dc = decode_config("paged_fp8_verify_3x4_227k")
+    out = run_decode(gcs_lib, dc)
+    sub = make_sub(dc, [1])
+    ref = oracle_decode(sub)
+    got = f64(out)[int(dc.cu_q[1]) : int(dc.cu_q[2])]
+    assert_close("out", got, ref, DECODE_RTOL)
+    assert abs(bias(got, ref)) <= DECODE_BIAS
+
+
+def make_sub(dc, reqs):
+    """Same cache, only the chosen requests (the oracle is per request)."""
+    import copy
+
+    sub = copy.copy(dc)
+    rows = []
+    cu = [0]
+    for r in reqs:
+        a, b = int(dc.cu_q[r]), int(dc.cu_q[r + 1])
+        rows.extend(range(a, b))
+        cu.append(cu[-1] + b - a)
+    sub.q = dc.q[rows]
+    sub.cu_q = torch.tensor(cu, dtype=torch.int32)
+    sub.seq_lens = dc.seq_lens[reqs]
+    sub.block_table = dc.block_table[reqs]
+    return sub

@@ -1,0 +1,145 @@
+"""Device parity: prefill forward and backward through the C ABI against the fp64 oracle on
+the same seeded inputs.  Sizes span several 128-row tiles with ragged tails; full-size
+configurations are checked on sampled (sequence, kv-head group) blocks."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synth import make_prefill, prefill_config
+from helpers import PREFILL_RTOL, assert_close, f64, oracle_prefill, run_prefill
+
+pytestmark = pytest.mark.gpu
+
+CASES = {
+    # name: (seqlens, hq, hkv, dqk, dv, gate, sink, window, backward)
+    "dense_mha_t128_d64": ([128], 2, 2, 64, 64, False, False, 0, True),
+    "varlen_ragged_gqa_d128_gate_sink": ([1, 100, 128, 129, 300], 8, 2, 128, 128, True, True, 0, True),
+    "mqa_d64_window_gate_sink": ([200, 513], 4, 1, 64, 64, True, True, 70, True),
+    "mha_d128_window_only": ([385, 64], 2, 2, 128, 128, False, False, 129, True),
+    "gqa_d128_sink_only": ([257, 33], 4, 2, 128, 128, False, True, 0, True),
+    "gqa_d64_gate_only": ([190, 2, 66], 6, 3, 64, 64, True, False, 0, True),
+    "d256_d256": ([190, 130], 2, 2, 256, 256, True, True, 0, False),
+    "d256_d512_window": ([300, 140], 4, 2, 256, 512, True, True, 100, False),
+    "d512_d512": ([260, 77], 2, 1, 512, 512, True, True, 0, False),
+}
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_prefill_parity(gcs_lib, name):
+    lens, hq, hkv, dqk, dv, gate, sink, window, bwd = CASES[name]
+    case = make_prefill(lens, hq, hkv, dqk, dv, seed=100 + len(name), gate=gate, sink=sink, window=window)
+    o, lse, grads = run_prefill(gcs_lib, case, backward=bwd)
+    ro, rlse, rg = oracle_prefill(case, backward=bwd)
+    assert_close("o", o, ro, PREFILL_RTOL)
+    np.testing.assert_allclose(f64(lse), rlse, rtol=0, atol=2e-3)
+    if bwd:
+        dq, dk, dv_, dg, ds = grads
+        rdq, rdk, rdv, rdg, rds = rg
+        assert_close("dq", dq, rdq, PREFILL_RTOL)
+        assert_close("dk", dk, rdk, PREFILL_RTOL)
+        assert_close("dv", dv_, rdv, PREFILL_RTOL)
+        if gate:
+            assert_close("dlog_gate", dg, rdg, PREFILL_RTOL)
+            # the gate of the first token of a sequence never changes a score
+            first = case.cu_seqlens.tolist()[:-1]
+            assert np.abs(f64(dg)[first]).max() <= 1e-3 * np.abs(rdg).max()
+        else:
+            assert dg is None
+        if sink:
+            assert_close("dsink", ds, rds, PREFILL_RTOL)
+        else:
+            assert ds is None
+
+
+def test_backward_large_head_dims_not_yet_supported(gcs_lib):
+    case = make_prefill([64], 2, 2, 256, 512, seed=1)
+    with pytest.raises(NotImplementedError):
+        run_prefill(gcs_lib, case, backward=True)
+
+
+def test_prefill_gather_order_is_exact(gcs_lib):
+    """Keys equal to the queries with a huge diagonal score: every row attends to itself only,
+    so O_i must be exactly V_i (integer token ids, bf16-exact), across sequence boundaries."""
+    lens = [130, 7, 200]
+    tot = sum(lens)
+    hq = hkv = 2
+    d = 64
+    idx = torch.arange(tot)
+    q = torch.zeros(tot, hq, d)
+    # one-hot on dim (token % 64): q_i . k_j = 900 for j = i and 0 for the other 63 keys of
+    # a 64-key window, so P_ii = 1 and every other probability underflows to 0
+    q[idx, :, idx % d] = 30.0
+    k = q.clone()
+    v = torch.zeros(tot, hkv, d)
+    v[:, :, 0] = (idx % 256).float()[:, None]
+    v[:, :, 1] = (idx // 256).float()[:, None]
+    cu = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32)
+    dev = torch.device("cuda:0")
+    o, _ = gcs_lib.attn_fwd(q.bfloat16().to(dev), k.bfloat16().to(dev), v.bfloat16().to(dev), cu.to(dev),
+                            max(lens), 1.0, 64)
+    torch.cuda.synchronize()
+    got = o.float().cpu()
+    np.testing.assert_array_equal(got[:, :, 0].numpy(), (idx % 256).float()[:, None].expand(tot, hq).numpy())
+    np.testing.assert_array_equal(got[:, :, 1].numpy(), (idx // 256).float()[:, None].expand(tot, hq).numpy())
+
+
+def _sampled_full_size(gcs_lib, name, kv_group=1, backward=True, seqs=None):
+    case = prefill_config(name)
+    o, lse, grads = run_prefill(gcs_lib, case, backward=backward)
+    hq, hkv = case.hq, case.hkv
+    group = hq // hkv
+    heads = list(range(kv_group * group, (kv_group + 1) * group))
+    cu = case.cu_seqlens.tolist()
+    seq_ids = seqs if seqs is not None else range(len(cu) - 1)
+    for s in seq_ids:
+        a, b = cu[s], cu[s + 1]
+        sub = dict(q=f64(case.q)[a:b][:, heads], k=f64(case.k)[a:b][:, [kv_group]],
+                   v=f64(case.v)[a:b][:, [kv_group]])
+        kw = dict(log_gate=None if case.log_gate is None else f64(case.log_gate)[a:b][:, heads],
+                  sink=None if case.sink is None else f64(case.sink)[heads], window=case.window)
+        ro, rl = oracle.prefill_forward(sub["q"], sub["k"], sub["v"], np.array([0, b - a]), case.scale, **kw)
+        assert_close(f"o[seq {s}]", f64(o)[a:b][:, heads], ro, PREFILL_RTOL)
+        np.testing.assert_allclose(f64(lse)[heads][:, a:b], rl, rtol=0, atol=2e-3)
+        if backward:
+            rdq, rdk, rdv, rdg, _ = oracle.prefill_backward(sub["q"], sub["k"], sub["v"],
+                                                            f64(case.do)[a:b][:, heads], np.array([0, b - a]),
+                                                            case.scale, **kw)
+            dq, dk, dv_, dg, _ = grads
+            assert_close(f"dq[seq {s}]", f64(dq)[a:b][:, heads], rdq, PREFILL_RTOL)
+            assert_close(f"dk[seq {s}]", f64(dk)[a:b][:, [kv_group]], rdk, PREFILL_RTOL)
+            assert_close(f"dv[seq {s}]", f64(dv_)[a:b][:, [kv_group]], rdv, PREFILL_RTOL)
+            if rdg is not None:
+                assert_close(f"dg[seq {s}]", f64(dg)[a:b][:, heads], rdg, PREFILL_RTOL)
+    return case, grads
+
+
+def test_full_size_varlen_gqa_d128_sampled(gcs_lib):
+    """Packed 1000/3000/4192, Hq=32, Hkv=8, D=128, gate + sink: every sequence of kv-head
+    group 5 against the oracle; the sink gradient of those heads over the whole batch."""
+    case, grads = _sampled_full_size(gcs_lib, "varlen_gqa_8192_d128", kv_group=5)
+    heads = list(range(20, 24))
+    cu = case.cu_seqlens.numpy()
+    _, _, _, _, rds = oracle.prefill_backward(
+        f64(case.q)[:, heads], f64(case.k)[:, [5]], f64(case.v)[:, [5]], f64(case.do)[:, heads], cu, case.scale,
+        log_gate=f64(case.log_gate)[:, heads], sink=f64(case.sink)[heads])
+    assert_close("dsink", f64(grads[4])[heads], rds, PREFILL_RTOL)
+
+
+def test_full_size_dense_mha_t128_d64(gcs_lib):
+    case = prefill_config("dense_mha_t128_d64")
+    o, lse, grads = run_prefill(gcs_lib, case)
+    ro, rl, rg = oracle_prefill(case)
+    assert_close("o", o, ro, PREFILL_RTOL)
+    for n, got, ref in zip(("dq", "dk", "dv"), grads[:3], rg[:3]):
+        assert_close(n, got, ref, PREFILL_RTOL)
+
+
+def test_full_size_window_dqk256_dv512_forward_sampled(gcs_lib):
+    _sampled_full_size(gcs_lib, "window_b2_t4096_dqk256_dv512", kv_group=3, backward=False, seqs=[1])
+
+
+def test_full_size_varlen_d512_forward_sampled(gcs_lib):
+    case = prefill_config("varlen_16384_d512")
+    shortest = int(np.argmin(case.seqlens))
+    _sampled_full_size(gcs_lib, "varlen_16384_d512", kv_group=2, backward=False, seqs=[shortest])
