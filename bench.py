@@ -1,0 +1,450 @@
+#!/usr/bin/env python
+"""Benchmark of the gated causal softmax attention hot path on GB300.
+
+One step = prefill forward + backward of the packed variable-length GQA workload
+(3 sequences of 1000 / 3000 / 4192 tokens = 8192, Hq=32, Hkv=8, D=128, bf16, per-token
+log gates, per-head sink, full causal) through the library's C ABI.  `value` is causal
+TFLOP/s over visible (query, key, head) pairs: 2(Dqk+Dv) forward + 2(3Dqk+2Dv) backward
+flops per pair.  The same run also times the paged fp8 decode (64 requests x 1 query,
+context uniform in [1, 32768], Hq=64, Hkv=4, D=128, page 16, split-K segments of 2048)
+and reports it under "decode" in GB/s of algorithmic bytes.
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+Under torchrun each rank runs an independent replica on its own GPU (no collective on
+the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "prefill fwd+bwd causal TFLOP/s (% bf16 peak); paged decode GB/s (% HBM peak)"
+PREFILL_WORKLOAD = "varlen_gqa_8192_d128"
+DECODE_WORKLOAD = "paged_fp8_decode_64x1"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# my kernels per prefill step with gates and sink: fwd (gate cumsum, attention) and bwd
+# (gate cumsum, delta, attention, dQ convert, d gate scan, d sink reduce)
+LAUNCHES_PER_PREFILL_STEP = 8
+LAUNCHES_PER_DECODE = 2
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def prefill_pairs(seqlens, hq, window=0):
+    pairs = 0
+    for T in seqlens:
+        if window > 0:
+            w = min(window, T)
+            pairs += w * (w + 1) // 2 + (T - w) * w
+        else:
+            pairs += T * (T + 1) // 2
+    return pairs * hq
+
+
+def prefill_flops(seqlens, hq, dqk, dv, window=0):
+    p = prefill_pairs(seqlens, hq, window)
+    return 2 * (dqk + dv) * p, 2 * (3 * dqk + 2 * dv) * p
+
+
+def decode_bytes(seq_lens, q_lens, hq, hkv, d, block_size):
+    """K and V bytes (1 B/elem) + K and V scales (4 B) per (token, kv head), q and out
+    (bf16), page-table entries and seq_lens."""
+    kv = sum(seq_lens) * hkv * (2 * d + 2 * 4)
+    qo = 2 * sum(q_lens) * hq * d * 2
+    table = 4 * sum((L + block_size - 1) // block_size for L in seq_lens)
+    return kv + qo + table + 4 * len(seq_lens)
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100", "-i",
+                 str(self.dev)], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "", 1).isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "", 1).isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup(n_gpus):
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(world, x):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- native arm
+def run_native(args):
+    import torch
+
+    import gated_causal_softmax_gb300 as gcs
+    from synth import decode_config, prefill_config
+
+    world, rank, local = dist_setup(args.gpus)
+    gcs.load()
+    dev = torch.device("cuda", local if world > 1 else 0)
+    pk, pk_kind = peaks()
+
+    # ------------------------------------------------------------ prefill inputs
+    case = prefill_config(PREFILL_WORKLOAD)
+    ms = max(case.seqlens)
+    q, k, v, do = (t.to(dev) for t in (case.q, case.k, case.v, case.do))
+    g, s, cu = case.log_gate.to(dev), case.sink.to(dev), case.cu_seqlens.to(dev)
+    fwd_fl, bwd_fl = prefill_flops(case.seqlens, case.hq, case.dqk, case.dv, case.window)
+    step_fl = fwd_fl + bwd_fl
+
+    def step(ev=None):
+        if ev is not None:
+            gcs.set_kernel_events(ev[0], ev[1])
+        o, lse = gcs.attn_fwd(q, k, v, cu, ms, case.scale, case.window, g, s)
+        if ev is not None:
+            gcs.set_kernel_events(ev[2], ev[3])
+        return gcs.attn_bwd(q, k, v, o, lse, do, cu, ms, case.scale, case.window, g, s)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if gcs.get_device_status() != 0:
+        raise RuntimeError("a kernel timed out during warm-up")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    for e4 in evs:
+        for e in e4:
+            e.record()  # create the handles
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local if world > 1 else 0)
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0.record()
+    for i in range(K):
+        step(evs[i])
+    t1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    ms_total = max_over_ranks(world, t0.elapsed_time(t1))
+    ms_step = ms_total / K
+    fwd_k = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    bwd_k = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    value = step_fl * world / (ms_total / K * 1e-3) / 1e12
+    if gcs.get_device_status() != 0:
+        raise RuntimeError("a kernel timed out during the timed region")
+
+    # dominant kernel: the fused backward attention kernel
+    sustained = pk.get("bf16_tflops_sustained", pk.get("bf16_tflops"))
+    dom = "prefill_bwd_kernel<128,128>" if bwd_k >= fwd_k else "prefill_fwd_kernel<128,128>"
+    dom_fl, dom_ms = (bwd_fl, bwd_k) if bwd_k >= fwd_k else (fwd_fl, fwd_k)
+    achieved = dom_fl / (dom_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": sustained,
+                "unit": "TFLOP/s", "frac": round(achieved / sustained, 4), "traffic": args.traffic,
+                "peak_source": f"{pk_kind} bf16_tflops_sustained", "algorithmic_flops_per_launch": dom_fl,
+                "fwd_kernel_ms": round(fwd_k, 4), "bwd_kernel_ms": round(bwd_k, 4),
+                "fwd_kernel_tflops": round(fwd_fl / (fwd_k * 1e-3) / 1e12, 1),
+                "bwd_kernel_tflops": round(bwd_fl / (bwd_k * 1e-3) / 1e12, 1)}
+
+    # ------------------------------------------------------------ end to end (host buffers)
+    host = {n: t.pin_memory() for n, t in (("q", case.q), ("k", case.k), ("v", case.v), ("do", case.do),
+                                           ("g", case.log_gate), ("s", case.sink), ("cu", case.cu_seqlens))}
+    outs = {n: torch.empty(shape, dtype=dt).pin_memory() for n, shape, dt in (
+        ("dq", case.q.shape, torch.bfloat16), ("dk", case.k.shape, torch.bfloat16),
+        ("dv", case.v.shape, torch.bfloat16), ("dg", case.log_gate.shape, torch.float32),
+        ("ds", case.sink.shape, torch.float32))}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs.values())
+
+    def e2e_step():
+        d = {n: t.to(dev, non_blocking=True) for n, t in host.items()}
+        o, lse = gcs.attn_fwd(d["q"], d["k"], d["v"], d["cu"], ms, case.scale, case.window, d["g"], d["s"])
+        dq, dk, dv_, dg, ds = gcs.attn_bwd(d["q"], d["k"], d["v"], o, lse, d["do"], d["cu"], ms, case.scale,
+                                           case.window, d["g"], d["s"])
+        for n, t in (("dq", dq), ("dk", dk), ("dv", dv_), ("dg", dg), ("ds", ds)):
+            outs[n].copy_(t, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(world, e0.elapsed_time(e1)) / K
+    e2e = {"value": round(step_fl * world / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
+    del q, k, v, do, g, s, cu
+    torch.cuda.empty_cache()
+
+    # ------------------------------------------------------------ paged fp8 decode
+    dc = decode_config(DECODE_WORKLOAD)
+    dd = dict(q=dc.q.to(dev), kc=dc.k_cache.to(dev), vc=dc.v_cache.to(dev), ks=dc.k_scale.to(dev),
+              vs=dc.v_scale.to(dev), bt=dc.block_table.to(dev), sl=dc.seq_lens.to(dev), cq=dc.cu_q.to(dev))
+    maxl = int(dc.seq_lens.max())
+    out = torch.empty_like(dd["q"])
+
+    def dstep(ev=None):
+        if ev is not None:
+            gcs.set_kernel_events(ev[0], ev[1])
+        gcs.attn_decode_paged(dd["q"], dd["kc"], dd["vc"], dd["ks"], dd["vs"], dd["bt"], dd["sl"], dd["cq"], 1, maxl,
+                              dc.scale, dc.segment_len, out=out)
+
+    for _ in range(args.warmup):
+        dstep()
+    torch.cuda.synchronize()
+    DK = max(K, 10)
+    devs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(DK)]
+    for e2 in devs:
+        for e in e2:
+            e.record()
+    barrier(world)
+    torch.cuda.synchronize()
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    d0.record()
+    for i in range(DK):
+        dstep(devs[i])
+    d1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    dec_ms = max_over_ranks(world, d0.elapsed_time(d1)) / DK
+    split_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in devs)
+    dbytes = decode_bytes(dc.seq_lens.tolist(), dc.q_lens, dc.hq, dc.hkv, dc.d, dc.block_size)
+    hbm = pk.get("hbm_gbs")
+    dec_gbs = dbytes * world / (dec_ms * 1e-3) / 1e9
+    split_gbs = dbytes / (split_ms * 1e-3) / 1e9
+    decode = {"workload": DECODE_WORKLOAD, "value": round(dec_gbs, 1), "unit": "GB/s",
+              "frac_of_hbm": round(dec_gbs / world / hbm, 4), "ms_per_call": round(dec_ms, 4),
+              "bytes_per_call": dbytes, "launches_per_call": LAUNCHES_PER_DECODE,
+              "roofline": {"bound": "hbm", "kernel": "decode_split_kernel", "achieved": round(split_gbs, 1),
+                           "peak": hbm, "unit": "GB/s", "frac": round(split_gbs / hbm, 4),
+                           "traffic": args.decode_traffic, "peak_source": f"{pk_kind} hbm_gbs",
+                           "kernel_ms": round(split_ms, 4)}}
+    if gcs.get_device_status() != 0:
+        raise RuntimeError("a decode kernel timed out")
+
+    # ------------------------------------------------------------ CPU oracle baseline
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(case, min_seconds=10.0)
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "pct_of_peak": round(value / world / sustained, 4),
+        "config": {"workload": PREFILL_WORKLOAD, "seqlens": case.seqlens, "hq": case.hq, "hkv": case.hkv,
+                   "dqk": case.dqk, "dv": case.dv, "gate": True, "sink": True, "window": case.window,
+                   "flops_per_step": step_fl, "fwd_flops": fwd_fl, "bwd_flops": bwd_fl,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs and fp32 dQ buffer (~0.5 GB) larger than L2; no flush"},
+        "roofline": roofline,
+        "decode": decode,
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": K * LAUNCHES_PER_PREFILL_STEP,
+        "gpu_launches_note": "prefill timed region; decode region adds 2 per call",
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def _oracle_sample(case, seq=1, kv_group=0):
+    """Sequence `seq` (3000 tokens) of the workload for the query heads of one kv group."""
+    import numpy as np
+
+    group = case.hq // case.hkv
+    heads = list(range(kv_group * group, (kv_group + 1) * group))
+    cu = case.cu_seqlens.tolist()
+    a, b = cu[seq], cu[seq + 1]
+    f = lambda t: t.double().numpy()
+    arrs = dict(q=f(case.q)[a:b][:, heads], k=f(case.k)[a:b][:, [kv_group]], v=f(case.v)[a:b][:, [kv_group]],
+                do=f(case.do)[a:b][:, heads], g=f(case.log_gate)[a:b][:, heads], s=f(case.sink)[heads])
+    fl = sum(prefill_flops([b - a], len(heads), case.dqk, case.dv, case.window))
+    desc = (f"oracle fwd+bwd (numpy fp64) of sequence {seq} ({b - a} tokens) for the {len(heads)} query heads of "
+            f"kv head {kv_group}: {fl / 1e9:.2f} GFLOP of the {sum(prefill_flops(case.seqlens, case.hq, case.dqk, case.dv)) / 1e9:.1f} "
+            f"GFLOP step")
+    return arrs, fl, desc, (a, b)
+
+
+def _run_oracle(case, arrs, a, b):
+    import numpy as np
+
+    import oracle  # CPU baseline leg only
+
+    cu = np.array([0, b - a])
+    kw = dict(log_gate=arrs["g"], sink=arrs["s"], window=case.window)
+    oracle.prefill_forward(arrs["q"], arrs["k"], arrs["v"], cu, case.scale, **kw)
+    oracle.prefill_backward(arrs["q"], arrs["k"], arrs["v"], arrs["do"], cu, case.scale, **kw)
+
+
+def cpu_baseline(case, min_seconds=10.0):
+    arrs, fl, desc, (a, b) = _oracle_sample(case)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        _run_oracle(case, arrs, a, b)
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds:
+            break
+    return {"value": round(fl * n / dt / 1e12, 6), "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle", "sample": f"{desc}; repeated {n}x over {dt:.1f} s"}
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from synth import prefill_config
+
+    case = prefill_config(PREFILL_WORKLOAD)
+    arrs, fl, desc, (a, b) = _oracle_sample(case)
+    for _ in range(args.warmup):
+        _run_oracle(case, arrs, a, b)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _run_oracle(case, arrs, a, b)
+    dt = time.perf_counter() - t0
+    value = fl / (dt / args.steps) / 1e12
+    cores = len(os.sched_getaffinity(0))
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 6),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": PREFILL_WORKLOAD, "sample": desc},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per launch of the dominant kernel from an ncu capture")
+    ap.add_argument("--decode-traffic", type=float, default=None)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

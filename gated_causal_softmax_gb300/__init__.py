@@ -29,6 +29,7 @@ __all__ = [
     "DecodeArgs",
     "GcsError",
     "get_device_status",
+    "set_kernel_events",
     "STATUS",
 ]
 
@@ -118,6 +119,8 @@ def _declare(lib: ctypes.CDLL) -> None:
     lib.attn_decode_paged.restype = _c_int
     lib.gcs_get_device_status.argtypes = [P(_c_int), _c_int]
     lib.gcs_get_device_status.restype = _c_int
+    lib.gcs_set_kernel_events.argtypes = [_vp, _vp]
+    lib.gcs_set_kernel_events.restype = _c_int
 
 
 def load(build_if_needed: bool = True) -> ctypes.CDLL:
@@ -166,6 +169,12 @@ def _need(t: torch.Tensor, dtype, name: str) -> torch.Tensor:
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     return t
+
+
+def set_kernel_events(before: Optional[torch.cuda.Event], after: Optional[torch.cuda.Event]) -> None:
+    """Arm two recorded-once torch CUDA events around the main kernel of the next call."""
+    h = lambda e: None if e is None else e.cuda_event
+    _check(load().gcs_set_kernel_events(h(before), h(after)), "gcs_set_kernel_events")
 
 
 def get_device_status(clear: bool = True) -> int:

@@ -22,6 +22,23 @@ int* g_status_ptr[kMaxDevices] = {nullptr};
 std::mutex g_mu;
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// events armed by gcs_set_kernel_events for the next call of this thread
+thread_local cudaEvent_t t_ev_before = nullptr, t_ev_after = nullptr;
+
+struct KernelTimer {
+  cudaStream_t s;
+  cudaEvent_t b, a;
+  explicit KernelTimer(cudaStream_t st) : s(st), b(t_ev_before), a(t_ev_after) {
+    t_ev_before = t_ev_after = nullptr;
+  }
+  void before() const {
+    if (b) cudaEventRecord(b, s);
+  }
+  void after() const {
+    if (a) cudaEventRecord(a, s);
+  }
+};
 std::once_flag g_encode_once;
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -191,7 +208,11 @@ int attn_fwd(const gcs_prefill_args* a, void* o, float* lse, void* workspace, si
   p.lse = lse;
   p.status = status;
   const int num_tiles = (a->total_tokens + 127) / 128 + a->num_seqs;
-  return cuda_status(launch_prefill_fwd(p, maps, num_tiles, s));
+  KernelTimer timer(s);
+  timer.before();
+  st = cuda_status(launch_prefill_fwd(p, maps, num_tiles, s));
+  timer.after();
+  return st;
 }
 
 int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const void* dout, void* dq, void* dk, void* dv,
@@ -231,7 +252,7 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
     if (st != GCS_OK) return st;
   }
   st = cuda_status(launch_bwd_pre(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout),
-                                  a->total_tokens, a->hq, a->dv, a->dqk, delta, dq_acc, dg_row, dsink, s));
+                                  a->total_tokens, a->hq, a->dv, a->dqk, delta, dq_acc, dg_row, dg_col, s));
   if (st != GCS_OK) return st;
 
   BwdParams p;
@@ -255,7 +276,10 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
   p.dg_col = dg_col;
   p.status = status;
   const int num_tiles = (a->total_tokens + 127) / 128 + a->num_seqs;
+  KernelTimer timer(s);
+  timer.before();
   st = cuda_status(launch_prefill_bwd(p, maps, num_tiles, s));
+  timer.after();
   if (st != GCS_OK) return st;
   return cuda_status(launch_bwd_post(dq_acc, static_cast<uint16_t*>(dq), a->total_tokens, a->hq, a->dqk,
                                      a->cu_seqlens, a->num_seqs, dg_row, dg_col, dlog_gate, lse, delta, a->sink,
@@ -329,7 +353,14 @@ int attn_decode_paged(const gcs_decode_args* a, void* out, void* workspace, size
   p.part_acc = static_cast<float*>(workspace);
   p.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + round_up(units * rows * 128 * sizeof(float)));
   p.status = status;
-  return cuda_status(launch_decode(p, reinterpret_cast<cudaStream_t>(stream)));
+  KernelTimer timer(reinterpret_cast<cudaStream_t>(stream));
+  return cuda_status(launch_decode(p, reinterpret_cast<cudaStream_t>(stream), &timer.b, &timer.a));
+}
+
+int gcs_set_kernel_events(void* before, void* after) {
+  t_ev_before = static_cast<cudaEvent_t>(before);
+  t_ev_after = static_cast<cudaEvent_t>(after);
+  return GCS_OK;
 }
 
 int gcs_get_device_status(int* status, int clear) {

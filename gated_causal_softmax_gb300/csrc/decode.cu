@@ -25,7 +25,7 @@ constexpr int kPage = 16;
 constexpr int kD = 128;
 constexpr int kGroup = 16;
 constexpr int kStage = 4352;  // K 2048 | V 2048 | kscale 64 | vscale 64 | pad
-constexpr int kNST = 8;
+constexpr int kNST = 12;
 constexpr int kThreads = 160;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kPScale = 256.f;
@@ -67,7 +67,7 @@ __device__ __forceinline__ uint32_t bf16pair_to_f16x2(uint32_t w) {
   return pack_f16x2(lo, hi);
 }
 
-__global__ void __launch_bounds__(kThreads) decode_split_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint64_t full[kNST], empty[kNST];
   __shared__ int abort_flag_s;
@@ -383,11 +383,16 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
 
 }  // namespace
 
-cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s) {
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, const cudaEvent_t* ev_before,
+                          const cudaEvent_t* ev_after) {
   const int smem = kNST * kStage;
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
   dim3 g1(p.max_segs, p.hkv, p.num_reqs);
+  if (ev_before && *ev_before) cudaEventRecord(*ev_before, s);
   decode_split_kernel<<<g1, kThreads, smem, s>>>(p);
-  cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
+  if (ev_after && *ev_after) cudaEventRecord(*ev_after, s);
   if (e != cudaSuccess) return e;
   dim3 g2(p.num_reqs * p.max_q_len, p.hkv);
   decode_combine_kernel<<<g2, 256, 0, s>>>(p);

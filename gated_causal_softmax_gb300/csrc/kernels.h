@@ -46,7 +46,7 @@ struct BwdParams {
   uint16_t* grad_v;      // bf16 [total, hkv, dv]
   float* dq_acc;         // fp32 [total, hq, dqk] (zeroed)
   float* dg_row;         // fp32 [hq, total] sum_j dS_ij (zeroed); null if not needed
-  float* dg_col;         // fp32 [hq, total] sum_i dS_ij; null if no gate
+  float* dg_col;         // fp32 [hq, total] sum_i dS_ij (zeroed); null if no gate
   int* status;
 };
 
@@ -60,7 +60,7 @@ cudaError_t launch_prefill_bwd(const BwdParams& p, const BwdMaps& maps, int num_
 cudaError_t launch_gate_cumsum(const float* g, const int32_t* cu, int num_seqs, int total, int hq, float* gT,
                                cudaStream_t s);
 cudaError_t launch_bwd_pre(const uint16_t* o, const uint16_t* dout, int total, int hq, int dv, int dqk,
-                           float* delta, float* dq_acc, float* dg_row, float* dsink, cudaStream_t s);
+                           float* delta, float* dq_acc, float* dg_row, float* dg_col, cudaStream_t s);
 cudaError_t launch_bwd_post(const float* dq_acc, uint16_t* dq, int total, int hq, int dqk, const int32_t* cu,
                             int num_seqs, const float* dg_row, const float* dg_col, float* dlog_gate,
                             const float* lse, const float* delta, const float* sink, float* dsink, cudaStream_t s);
@@ -86,6 +86,8 @@ struct DecodeParams {
   int* status;
 };
 
-cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s);
+// ev_before / ev_after (may point to null events) are recorded around the split-K kernel.
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, const cudaEvent_t* ev_before,
+                          const cudaEvent_t* ev_after);
 
 }  // namespace gcs

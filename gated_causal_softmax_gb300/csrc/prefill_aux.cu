@@ -4,7 +4,8 @@
 //                 query head; written transposed [hq, total] and pre-multiplied by
 //                 log2(e) for the exp2-based softmax.  (fla-org/flash-linear-attention
 //                 #1322, Description: logarithmic gates.)
-//   bwd_pre       delta_i = sum_d dO_id * O_id in fp32 from the stored bf16 output.
+//   bwd_pre       delta_i = sum_d dO_id * O_id in fp32 from the stored bf16 output;
+//                 zeroes the fp32 dQ accumulator and the dS row / column sums.
 //   bwd_post      dQ = bf16(dQ_acc) (Oct 5 comment: fp32 buffer converted after the
 //                 kernel); d log_gate = reverse cumsum of (rowsum dS - colsum dS);
 //                 d sink_h = -sum_i p_sink,i * sum_j P_ij dP_ij (Oct 3 comment), where the
@@ -174,8 +175,7 @@ cudaError_t launch_gate_cumsum(const float* g, const int32_t* cu, int num_seqs, 
 }
 
 cudaError_t launch_bwd_pre(const uint16_t* o, const uint16_t* dout, int total, int hq, int dv, int dqk, float* delta,
-                           float* dq_acc, float* dg_row, float* dsink, cudaStream_t s) {
-  (void)dsink;
+                           float* dq_acc, float* dg_row, float* dg_col, cudaStream_t s) {
   const int rows = total * hq;
   bwd_pre_kernel<<<(rows + 7) / 8, 256, 0, s>>>(o, dout, total, hq, dv, delta);
   cudaError_t e = cudaGetLastError();
@@ -183,6 +183,8 @@ cudaError_t launch_bwd_pre(const uint16_t* o, const uint16_t* dout, int total, i
   e = cudaMemsetAsync(dq_acc, 0, (size_t)total * hq * dqk * sizeof(float), s);
   if (e != cudaSuccess) return e;
   if (dg_row) e = cudaMemsetAsync(dg_row, 0, (size_t)total * hq * sizeof(float), s);
+  if (e != cudaSuccess) return e;
+  if (dg_col) e = cudaMemsetAsync(dg_col, 0, (size_t)total * hq * sizeof(float), s);
   return e;
 }
 

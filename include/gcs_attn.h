@@ -158,6 +158,15 @@ int attn_decode_paged(const gcs_decode_args* a, void* out, void* workspace, size
  * resets it to GCS_OK.  Returns GCS_OK or GCS_ERR_CUDA. */
 int gcs_get_device_status(int* status, int clear);
 
+/* ------------------------------------------------------------------ instrumentation
+ * Arms two caller-created CUDA events (cudaEvent_t, passed as void*) for the next attn_fwd,
+ * attn_bwd or attn_decode_paged call made by this host thread: `before` is recorded on the
+ * call's stream immediately before its main attention kernel (prefill forward kernel,
+ * fused backward kernel, or split-K decode kernel) and `after` immediately after it, so
+ * cudaEventElapsedTime(before, after) is that kernel's device time.  The events are
+ * disarmed once used; passing NULL, NULL disarms them.  Returns GCS_OK. */
+int gcs_set_kernel_events(void* before, void* after);
+
 /* Library version string. */
 const char* gcs_version(void);
 
