@@ -25,6 +25,7 @@ __all__ = [
     "attn_fwd",
     "attn_bwd",
     "attn_decode_paged",
+    "attn_decode_paged_noalloc",
     "PrefillArgs",
     "DecodeArgs",
     "GcsError",
@@ -117,6 +118,8 @@ def _declare(lib: ctypes.CDLL) -> None:
     lib.attn_bwd.restype = _c_int
     lib.attn_decode_paged.argtypes = [P(DecodeArgs), _vp, _vp, ctypes.c_size_t, _vp]
     lib.attn_decode_paged.restype = _c_int
+    lib.attn_decode_paged_noalloc.argtypes = [P(DecodeArgs), _vp, _vp]
+    lib.attn_decode_paged_noalloc.restype = _c_int
     lib.gcs_get_device_status.argtypes = [P(_c_int), _c_int]
     lib.gcs_get_device_status.restype = _c_int
     lib.gcs_set_kernel_events.argtypes = [_vp, _vp]
@@ -325,3 +328,18 @@ def attn_decode_paged(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_le
     st = L.attn_decode_paged(ctypes.byref(a), out.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream())
     _check(st, "attn_decode_paged")
     return out
+
+
+def attn_decode_paged_noalloc(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu_q, max_q_len,
+                              max_seq_len, scale=None, segment_len=2048, out=None):
+    """attn_decode_paged without a workspace: the library keeps the split-K partials in
+    its own fixed 64 MiB device scratch (for callers that cannot allocate device memory).
+    Calls share that scratch, so calls must not overlap on the GPU."""
+    L = load()
+    a = decode_args(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu_q, max_q_len, max_seq_len,
+                    scale, segment_len)
+    if out is None:
+        out = torch.empty_like(q)
+    _check(L.attn_decode_paged_noalloc(ctypes.byref(a), out.data_ptr(), _stream()), "attn_decode_paged_noalloc")
+    return out
+

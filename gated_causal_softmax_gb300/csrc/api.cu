@@ -357,6 +357,16 @@ int attn_decode_paged(const gcs_decode_args* a, void* out, void* workspace, size
   return cuda_status(launch_decode(p, reinterpret_cast<cudaStream_t>(stream), &timer.b, &timer.a));
 }
 
+int attn_decode_paged_noalloc(const gcs_decode_args* a, void* out, gcs_stream_t stream) {
+  int st = check_decode(a);
+  if (st != GCS_OK) return st;
+  // the split-K partials must fit the library's fixed scratch
+  if (decode_ws(a, nullptr) > kNoAllocScratchBytes) return GCS_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  if (decode_noalloc_scratch(&scratch) != cudaSuccess) return GCS_ERR_CUDA;
+  return attn_decode_paged(a, out, scratch, kNoAllocScratchBytes, stream);
+}
+
 int gcs_set_kernel_events(void* before, void* after) {
   t_ev_before = static_cast<cudaEvent_t>(before);
   t_ev_after = static_cast<cudaEvent_t>(after);

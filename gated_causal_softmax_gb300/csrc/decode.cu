@@ -15,11 +15,21 @@
 // units).  P * vscale is scaled by 2^8 before the f16 rounding (round-to-nearest, no
 // truncation bias) and the factor is removed in fp32 afterwards.
 // decode_combine_kernel: LSE-weighted merge of the segments of each (query row, head).
+#include <mutex>
+
 #include "kernels.h"
 #include "sm103_ptx.cuh"
 
 namespace gcs {
 namespace {
+
+// Fixed scratch for the allocation-free decode entry point: the split-K partials live
+// here instead of in a caller-provided workspace.  Every GPU that loads the library
+// holds this array until the process exits.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+constexpr int kMaxScratchDevices = 64;
+void* g_noalloc_ptr[kMaxScratchDevices] = {nullptr};
+std::mutex g_noalloc_mu;
 
 constexpr int kPage = 16;
 constexpr int kD = 128;
@@ -397,6 +407,25 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, const cudaEvent
   dim3 g2(p.num_reqs * p.max_q_len, p.hkv);
   decode_combine_kernel<<<g2, 256, 0, s>>>(p);
   return cudaGetLastError();
+}
+
+// Device address of the static scratch on the current device.  The first call on a
+// device looks the address up (cudaGetSymbolAddress, with that device current); later
+// calls reuse it.
+cudaError_t decode_noalloc_scratch(void** ptr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxScratchDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = p;
+  }
+  *ptr = g_noalloc_ptr[dev];
+  return cudaSuccess;
 }
 
 }  // namespace gcs

@@ -90,4 +90,10 @@ struct DecodeParams {
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, const cudaEvent_t* ev_before,
                           const cudaEvent_t* ev_after);
 
+// Size of the static scratch behind attn_decode_paged_noalloc (64 MiB).
+constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;
+
+// Device address of that scratch on the current device (set up on first use per device).
+cudaError_t decode_noalloc_scratch(void** ptr);
+
 }  // namespace gcs

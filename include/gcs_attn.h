@@ -152,6 +152,25 @@ size_t attn_decode_workspace(const gcs_decode_args* a);
 int attn_decode_paged(const gcs_decode_args* a, void* out, void* workspace, size_t workspace_bytes,
                       gcs_stream_t stream);
 
+/* Allocation-free variant of attn_decode_paged (no counterpart in the pages: this is a
+ * library convenience).  Some callers cannot allocate device memory for a workspace: a
+ * host runtime with a fixed, pre-planned memory budget, a C program without a device
+ * allocator of its own, or a latency-critical decode loop in which a cudaMalloc (which
+ * may synchronise the device) is not acceptable.  This entry point takes the same
+ * arguments minus the workspace and keeps the split-K partials in a fixed scratch array
+ * compiled into the library (64 MiB, held on every GPU that loads the library until the
+ * process exits).  It calls no allocator.
+ *   - Sizes whose partials exceed the scratch (attn_decode_workspace(a) > 64 MiB) are
+ *     rejected with GCS_ERR_WORKSPACE before anything is launched.
+ *   - The first call on a device looks up the scratch's device address (with that device
+ *     current); make that first call before any stream capture on that device.
+ *   - All calls share the one scratch array and it keeps the previous call's contents;
+ *     nothing needs clearing because every partial a call reads it first writes.  Calls
+ *     that overlap on the GPU (e.g. on two concurrent streams) race on the scratch and
+ *     give wrong results: serialise them.
+ * out: bf16 [total_q, hq, d]; returns the same statuses as attn_decode_paged. */
+int attn_decode_paged_noalloc(const gcs_decode_args* a, void* out, gcs_stream_t stream);
+
 /* ------------------------------------------------------------------ status
  * Per-device status word written by kernels that gave up on a bounded wait.
  * Copies the word for the current device into *status (synchronous) and, if clear != 0,
