@@ -87,8 +87,6 @@ bool supported_dims(int dqk, int dv) {
          (dqk == 256 && dv == 512) || (dqk == 512 && dv == 512);
 }
 
-bool bwd_supported_dims(int dqk, int dv) { return (dqk == 64 && dv == 64) || (dqk == 128 && dv == 128); }
-
 int check_prefill(const gcs_prefill_args* a) {
   if (!a) return GCS_ERR_INVALID_ARG;
   if (a->num_seqs < 1 || a->total_tokens < 1 || a->max_seqlen < 1 || a->hq < 1 || a->hkv < 1)
@@ -224,7 +222,6 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
     return GCS_ERR_INVALID_ARG;
   if ((dlog_gate == nullptr) != (a->log_gate == nullptr)) return GCS_ERR_INVALID_ARG;
   if ((dsink == nullptr) != (a->sink == nullptr)) return GCS_ERR_INVALID_ARG;
-  if (!bwd_supported_dims(a->dqk, a->dv)) return GCS_ERR_UNSUPPORTED;
   const size_t need = bwd_ws(a);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return GCS_ERR_WORKSPACE;
@@ -278,7 +275,8 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
   const int num_tiles = (a->total_tokens + 127) / 128 + a->num_seqs;
   KernelTimer timer(s);
   timer.before();
-  st = cuda_status(launch_prefill_bwd(p, maps, num_tiles, s));
+  st = cuda_status(a->dqk <= 128 && a->dv <= 128 ? launch_prefill_bwd(p, maps, num_tiles, s)
+                                                 : launch_prefill_bwd_wide(p, maps, num_tiles, s));
   timer.after();
   if (st != GCS_OK) return st;
   return cuda_status(launch_bwd_post(dq_acc, static_cast<uint16_t*>(dq), a->total_tokens, a->hq, a->dqk,

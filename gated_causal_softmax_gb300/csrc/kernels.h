@@ -55,6 +55,8 @@ struct BwdMaps {
 };
 
 cudaError_t launch_prefill_bwd(const BwdParams& p, const BwdMaps& maps, int num_kv_tiles, cudaStream_t s);
+// Head dims above 128: output-column roles (dV chunks; dK + dQ chunks), two launches.
+cudaError_t launch_prefill_bwd_wide(const BwdParams& p, const BwdMaps& maps, int num_kv_tiles, cudaStream_t s);
 
 // Small HBM-bound helpers.
 cudaError_t launch_gate_cumsum(const float* g, const int32_t* cu, int num_seqs, int total, int hq, float* gT,

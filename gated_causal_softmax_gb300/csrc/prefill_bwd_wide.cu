@@ -1,0 +1,493 @@
+// Prefill backward for head dims above 128 (fla-org/flash-linear-attention #1322
+// "Gluon attention backend with large head dimensions": Description, head dims through
+// 512; Oct 3 / Oct 5 comments for the fp32 sink / gate reductions and the fp32 dQ buffer).
+//
+// At 128 key rows per tile the fp32 dK and dV accumulators of a 256/512-wide head need
+// 768-1024 TMEM columns (512 exist), and the K / V tiles alone exceed shared memory.  The
+// work of one (128-key tile, kv head) is therefore split over CTAs by output columns:
+//   role V   (kind 0):  dV[:, v0 : v0+256)                 needs P  -> recomputes S
+//   role KQ  (kind 1):  dK[:, k0 : k0+256), dQ[:, k0 : k0+256)  needs dS -> recomputes S, dP
+// Every role recomputes the full-width contractions it needs; the extra work is the price
+// of fitting the accumulators in TMEM.  Operands stream through a ring of 16 KB stages
+// (128 x 64 or 64 x 64 bf16 chunks, 128-B swizzle); the K columns a role keeps using
+// (its own 256 dims) stay resident.  One softmax warpgroup, one thread per key row.
+// Per 64-row query step (s = step, b = none; the pipeline is sequential per step):
+//     S^T = K Q^T (TMEM)   [dP^T = V dO^T (TMEM)]   P^T / dS^T in fp32, bf16 operands
+//     role V:  dV  += P^T dO[:, v0..]
+//     role KQ: dK  += dS^T Q[:, k0..];  dQ^T[k0..] = K[:, k0..]^T dS^T -> fp32 reduce-adds
+// Row / column sums of dS (gate and sink gradients) are taken by the KQ role with k0 = 0.
+#include "kernels.h"
+#include "sm103_ptx.cuh"
+
+namespace gcs {
+namespace {
+
+constexpr int kBN = 128;
+constexpr int kBM = 64;
+constexpr int kThreads = 192;
+constexpr int kStage = 16384;
+constexpr int kW = 256;  // output columns per role
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
+
+__device__ __forceinline__ void red_add_f32(float* addr, float v) {
+  asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+}
+
+template <int DQK, int DV, int KIND>
+struct WideCfg {
+  static constexpr int KCH = DQK / 64, VCH = DV / 64, WCH = kW / 64;
+  static constexpr int NRES = (KIND == 1 ? kW : (DQK < kW ? DQK : kW)) / 64;  // resident K chunks
+  static constexpr int NST = 8;
+  static constexpr int OFF_KRES = 0;
+  static constexpr int OFF_RING = OFF_KRES + NRES * kStage;
+  static constexpr int OFF_DS = OFF_RING + NST * kStage;
+  static constexpr int OFF_VEC = OFF_DS + (KIND == 1 ? kStage : 0);  // [2][2][64] floats
+  static constexpr int OFF_BAR = OFF_VEC + 2 * 2 * kBM * 4;
+  static constexpr int OFF_MISC = OFF_BAR + (2 * NST + 16) * 8;
+  static constexpr int SMEM = OFF_MISC + 16 + 1024;
+  static_assert(SMEM <= 227 * 1024, "shared memory budget");
+  // TMEM: S^T 0..63, dP^T 64..127, accumulator (dV or dK) 128..383, dQ^T halves 384..511
+  static constexpr int T_S = 0, T_DP = 64, T_ACC = 128, T_DQ = 384;
+};
+
+__device__ __forceinline__ bool find_kv_tile(const int32_t* cu, int num_seqs, int t, int& start, int& len, int& jt) {
+  for (int s = 0; s < num_seqs; ++s) {
+    const int a = __ldg(cu + s), b = __ldg(cu + s + 1);
+    const int n = (b - a + kBN - 1) / kBN;
+    if (t < n) {
+      start = a;
+      len = b - a;
+      jt = t;
+      return true;
+    }
+    t -= n;
+  }
+  return false;
+}
+
+template <int DQK, int DV, int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                            const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                            const BwdParams p) {
+  using C = WideCfg<DQK, DV, KIND>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  int seq_start, len, jt;
+  if (!find_kv_tile(p.cu_seqlens, p.num_seqs, blockIdx.x, seq_start, len, jt)) return;
+  const int kvh = blockIdx.y;
+  const int w0 = blockIdx.z * kW;         // v0 (role V) or k0 (role KQ)
+  const int res0 = (KIND == 1) ? w0 / 64 : 0;  // first resident K chunk
+  const int group = p.hq / p.hkv;
+  const int j0 = jt * kBN;
+  const int it_lo = j0 / kBM;
+  int i_hi = len - 1;
+  if (p.window > 0) i_hi = min(i_hi, j0 + kBN - 1 + p.window - 1);
+  const int n_it = i_hi / kBM - it_lo + 1;
+  const int nsteps = n_it * group;
+  const bool sums = (KIND == 1) && (w0 == 0);  // this role takes the dS row / column sums
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* full = bars;                 // [NST]
+  uint64_t* empty = bars + C::NST;       // [NST]
+  uint64_t* kv_full = bars + 2 * C::NST;
+  uint64_t* vec_full = kv_full + 1;      // [2]
+  uint64_t* vec_empty = kv_full + 3;     // [2]
+  uint64_t* s_full = kv_full + 5;
+  uint64_t* p_full = kv_full + 6;
+  uint64_t* mma_done = kv_full + 7;
+  uint64_t* dq_free = kv_full + 8;
+  uint64_t* drain = kv_full + 9;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  const Abort ab{abort_flag, p.status};
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::NST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(kv_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&vec_full[b], 1);
+      mbar_init(&vec_empty[b], 4);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 4);
+    mbar_init(mma_done, 1);
+    mbar_init(dq_free, 4);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    bool ok = true;
+    uint32_t stage = 0, phase = 0;
+    auto issue = [&](const CUtensorMap* m, int x, int y, uint32_t bytes) -> bool {
+      if (!wait_bar(&empty[stage], phase ^ 1, ab)) return false;
+      mbar_expect_tx(&full[stage], bytes);
+      tma_load_2d(smem + C::OFF_RING + stage * kStage, m, &full[stage], x, y);
+      if (++stage == C::NST) {
+        stage = 0;
+        phase ^= 1;
+      }
+      return true;
+    };
+    if (lane == 0) {
+      mbar_expect_tx(kv_full, C::NRES * kStage);
+      for (int c = 0; c < C::NRES; ++c)
+        tma_load_2d(smem + C::OFF_KRES + c * kStage, &tmK, kv_full, kvh * DQK + (res0 + c) * 64, seq_start + j0);
+    }
+    for (int s = 0; s < nsteps && ok; ++s) {
+      const int h = kvh * group + s / n_it;
+      const int i0 = (it_lo + s % n_it) * kBM;
+      const int yq = seq_start + i0, yk = seq_start + j0;
+      if (lane == 0) {
+        for (int c = 0; c < C::KCH && ok; ++c) {
+          if (c < res0 || c >= res0 + C::NRES) ok = issue(&tmK, kvh * DQK + c * 64, yk, kStage);
+          if (ok) ok = issue(&tmQ, h * DQK + c * 64, yq, kStage / 2);
+        }
+        if (KIND == 1) {
+          for (int c = 0; c < C::VCH && ok; ++c) {
+            ok = issue(&tmV, kvh * DV + c * 64, yk, kStage);
+            if (ok) ok = issue(&tmDO, h * DV + c * 64, yq, kStage / 2);
+          }
+          for (int c = 0; c < C::WCH && ok; ++c) ok = issue(&tmQ, h * DQK + w0 + c * 64, yq, kStage / 2);
+        } else {
+          for (int c = 0; c < C::WCH && ok; ++c) ok = issue(&tmDO, h * DV + w0 + c * 64, yq, kStage / 2);
+        }
+        if (ok) ok = wait_bar(&vec_empty[s & 1], ((s >> 1) & 1) ^ 1, ab);
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      float* vec = reinterpret_cast<float*>(smem + C::OFF_VEC) + (s & 1) * 2 * kBM;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int c = lane * 2 + u;
+        const int i = i0 + c;
+        float colterm = 0.f, dl = 0.f;
+        if (i < len) {
+          const size_t idx = (size_t)h * p.total + seq_start + i;
+          colterm = -__ldg(p.lse + idx) * kLog2e;
+          if (p.gT) colterm += __ldg(p.gT + idx);
+          dl = __ldg(p.delta + idx);
+        }
+        vec[c] = colterm;
+        vec[kBM + c] = dl;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&vec_full[s & 1]);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idS = idesc_bf16(128, kBM, false, false);  // S^T, dP^T
+      const uint32_t idAcc = idesc_bf16(128, 64, false, true);  // dV / dK, one 64-column chunk
+      const uint32_t idDQ = idesc_bf16(128, kBM, true, true);   // dQ^T half
+      const uint32_t sRes = smem_u32(smem + C::OFF_KRES), sRing = smem_u32(smem + C::OFF_RING);
+      const uint32_t sDS = smem_u32(smem + C::OFF_DS);
+      uint32_t stage = 0, phase = 0;
+      auto take = [&](uint32_t& addr) -> bool {  // wait for the current ring stage
+        if (!wait_bar(&full[stage], phase, ab)) return false;
+        tc_fence_after();
+        addr = sRing + stage * kStage;
+        return true;
+      };
+      auto advance = [&]() {
+        if (++stage == C::NST) {
+          stage = 0;
+          phase ^= 1;
+        }
+      };
+      auto give = [&]() {  // release the current stage once the MMAs issued so far retire
+        mma_commit(&empty[stage]);
+        advance();
+      };
+      bool ok = wait_bar(kv_full, 0, ab);
+      for (int s = 0; s < nsteps && ok; ++s) {
+        // S^T = K Q^T over all of DQK (K chunk resident or streamed, Q chunk streamed)
+        for (int c = 0; c < C::KCH && ok; ++c) {
+          uint32_t a = 0, bq = 0;
+          int kst = -1;
+          if (c >= res0 && c < res0 + C::NRES) {
+            a = sRes + (c - res0) * kStage;
+          } else {
+            ok = take(a);
+            if (!ok) break;
+            kst = stage;
+            advance();
+          }
+          ok = take(bq);
+          if (!ok) break;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ss(tmem + C::T_S, sdesc_sw128(a + k * 32, 16, 1024), sdesc_sw128(bq + k * 32, 16, 1024), idS,
+                   (c | k) != 0);
+          if (kst >= 0) mma_commit(&empty[kst]);
+          give();
+        }
+        if (!ok) break;
+        if (KIND == 1) {
+          // dP^T = V dO^T over all of DV
+          for (int c = 0; c < C::VCH && ok; ++c) {
+            uint32_t a = 0, bq = 0;
+            ok = take(a);
+            if (!ok) break;
+            const int vst = stage;
+            advance();
+            ok = take(bq);
+            if (!ok) break;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_ss(tmem + C::T_DP, sdesc_sw128(a + k * 32, 16, 1024), sdesc_sw128(bq + k * 32, 16, 1024), idS,
+                     (c | k) != 0);
+            mma_commit(&empty[vst]);
+            give();
+          }
+          if (!ok) break;
+        }
+        mma_commit(s_full);
+        ok = wait_bar(p_full, s & 1, ab);
+        if (!ok) break;
+        tc_fence_after();
+        // accumulator += (P^T or dS^T) x (dO or Q) chunk by chunk (N = 64 each)
+        const uint32_t aT = tmem + (KIND == 1 ? C::T_DP : C::T_S);
+        for (int c = 0; c < C::WCH && ok; ++c) {
+          uint32_t bq = 0;
+          ok = take(bq);
+          if (!ok) break;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ts(tmem + C::T_ACC + c * 64, aT + k * 8, sdesc_sw128(bq + k * 2048, kStage, 1024), idAcc,
+                   (s > 0 || k > 0) ? 1u : 0u);
+          give();
+        }
+        if (!ok) break;
+        if (KIND == 1) {
+          if (s > 0) {
+            ok = wait_bar(dq_free, (s - 1) & 1, ab);
+            if (!ok) break;
+            tc_fence_after();
+          }
+          // dQ^T for dims w0 .. w0+255: two M=128 halves from the resident K chunks
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              mma_ss(tmem + C::T_DQ + hf * 64, sdesc_sw128(sRes + 2 * hf * kStage + k * 2048, kStage, 1024),
+                     sdesc_sw128(sDS + k * 2048, kStage, 1024), idDQ, k > 0);
+        }
+        mma_commit(mma_done);
+      }
+      if (!ok) {
+        mma_commit(drain);
+        mbar_wait(drain, 0, nullptr);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ key rows
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_off + C::T_S, tDP = tmem + lane_off + C::T_DP;
+    const int jl = j0 + r;
+    const bool has_gate = p.gT != nullptr;
+    const bool want_row = sums && p.dg_row != nullptr;
+    uint8_t* sDS = smem + C::OFF_DS;
+    float dgcol = 0.f, rowterm = 0.f;
+    int cur_h = -1;
+    bool ok = true;
+    for (int s = 0; s < nsteps; ++s) {
+      const int h = kvh * group + s / n_it;
+      const int i0 = (it_lo + s % n_it) * kBM;
+      if (h != cur_h) {
+        if (sums && cur_h >= 0 && has_gate && jl < len)
+          red_add_f32(p.dg_col + (size_t)cur_h * p.total + seq_start + jl, dgcol);
+        dgcol = 0.f;
+        cur_h = h;
+        rowterm = (has_gate && jl < len) ? -__ldg(p.gT + (size_t)h * p.total + seq_start + jl) : 0.f;
+      }
+      ok = wait_bar(&vec_full[s & 1], (s >> 1) & 1, ab);
+      if (!ok) break;
+      ok = wait_bar(s_full, s & 1, ab);
+      if (!ok) break;
+      tc_fence_after();
+      const float* vec = reinterpret_cast<const float*>(smem + C::OFF_VEC) + (s & 1) * 2 * kBM;
+      const bool need_mask = (i0 < j0 + kBN - 1) || (p.window > 0 && i0 + kBM - 1 - j0 >= p.window) ||
+                             (i0 + kBM > len);
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        uint32_t sv[32], dp[32];
+        tmem_ld32(tS + 32 * ch, sv);
+        if (KIND == 1) tmem_ld32(tDP + 32 * ch, dp);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int col = 32 * ch + c;
+          float t = fmaf(__uint_as_float(sv[c]), p.scale_log2, vec[col]) + rowterm;
+          if (need_mask) {
+            const int i = i0 + col;
+            const bool vis = (i < len) && (jl <= i) && (p.window == 0 || i - jl < p.window);
+            t = vis ? t : neg_inf();
+          }
+          const float pr = ex2(t);
+          sv[c] = __float_as_uint(pr);
+          if (KIND == 1) dp[c] = __float_as_uint(pr * (__uint_as_float(dp[c]) - vec[kBM + col]));
+        }
+        uint32_t pk[16];
+        if (KIND == 0) {
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            pk[c] = pack_bf16x2(__uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1]));
+          tmem_st16(tS + 16 * ch, pk);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            pk[c] = pack_bf16x2(__uint_as_float(dp[2 * c]), __uint_as_float(dp[2 * c + 1]));
+          tmem_st16(tDP + 16 * ch, pk);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(sDS + sw128_offset(r, 4 * ch + q)) =
+                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          if (sums && has_gate) {
+            float acc = 0.f;
+#pragma unroll
+            for (int c = 0; c < 32; ++c) acc += __uint_as_float(dp[c]);
+            dgcol += acc;
+          }
+          if (want_row) {
+            float v[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) v[c] = __uint_as_float(dp[c]);
+#pragma unroll
+            for (int half = 16; half >= 1; half >>= 1) {
+              const bool upper = (lane & half) != 0;
+#pragma unroll
+              for (int c = 0; c < half; ++c) {
+                const float send = upper ? v[c] : v[c + half];
+                const float keep = upper ? v[c + half] : v[c];
+                v[c] = keep + __shfl_xor_sync(0xffffffffu, send, half);
+              }
+            }
+            const int i = i0 + 32 * ch + lane;
+            if (i < len) red_add_f32(p.dg_row + (size_t)h * p.total + seq_start + i, v[0]);
+          }
+        }
+      }
+      tmem_st_wait();
+      if (KIND == 1) fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&vec_empty[s & 1]);
+        mbar_arrive(p_full);
+      }
+      ok = wait_bar(mma_done, s & 1, ab);
+      if (!ok) break;
+      if (KIND == 1) {
+        // dQ^T halves: lane r holds dims w0 + r (half 0) and w0 + 128 + r (half 1)
+        tc_fence_after();
+        uint32_t dq[64];
+#pragma unroll 1
+        for (int hf = 0; hf < 2; ++hf) {
+          tmem_ld32(tmem + lane_off + C::T_DQ + hf * 64, dq);
+          tmem_ld32(tmem + lane_off + C::T_DQ + hf * 64 + 32, dq + 32);
+          tmem_ld_wait();
+          if (hf == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(dq_free);
+          }
+          const int nrows = min(kBM, len - i0);
+          float* base = p.dq_acc + ((size_t)(seq_start + i0) * p.hq + h) * DQK + w0 + hf * 128 + r;
+          const size_t row_stride = (size_t)p.hq * DQK;
+#pragma unroll
+          for (int c = 0; c < kBM; ++c)
+            if (c < nrows) red_add_f32(base + c * row_stride, __uint_as_float(dq[c]) * p.scale);
+        }
+      }
+    }
+    if (ok && sums && cur_h >= 0 && has_gate && jl < len)
+      red_add_f32(p.dg_col + (size_t)cur_h * p.total + seq_start + jl, dgcol);
+    // ---- epilogue: dV (role V) or scale * dK (role KQ), columns w0 .. w0+255
+    if (ok && nsteps > 0) {
+      tc_fence_after();
+      const bool row_ok = jl < len;
+      uint16_t* dst = (KIND == 1)
+                          ? p.grad_k + ((size_t)(seq_start + (row_ok ? jl : 0)) * p.hkv + kvh) * DQK + w0
+                          : p.grad_v + ((size_t)(seq_start + (row_ok ? jl : 0)) * p.hkv + kvh) * DV + w0;
+      const float sc = (KIND == 1) ? p.scale : 1.f;
+#pragma unroll 1
+      for (int c = 0; c < kW / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_off + C::T_ACC + c * 32, v);
+        tmem_ld_wait();
+        if (row_ok) {
+          uint4* d = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            d[q] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * q]) * sc, __uint_as_float(v[8 * q + 1]) * sc),
+                              pack_bf16x2(__uint_as_float(v[8 * q + 2]) * sc, __uint_as_float(v[8 * q + 3]) * sc),
+                              pack_bf16x2(__uint_as_float(v[8 * q + 4]) * sc, __uint_as_float(v[8 * q + 5]) * sc),
+                              pack_bf16x2(__uint_as_float(v[8 * q + 6]) * sc, __uint_as_float(v[8 * q + 7]) * sc));
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    const unsigned long long t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 1000000ull) {
+    }
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int DQK, int DV, int KIND>
+cudaError_t launch_t(const BwdParams& p, const BwdMaps& maps, int num_tiles, cudaStream_t s) {
+  using C = WideCfg<DQK, DV, KIND>;
+  auto kern = prefill_bwd_wide_kernel<DQK, DV, KIND>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  const int roles = (KIND == 1 ? DQK : DV) / kW;
+  kern<<<dim3(num_tiles, p.hkv, roles), kThreads, C::SMEM, s>>>(maps.q, maps.k, maps.v, maps.dout, p);
+  return cudaGetLastError();
+}
+
+template <int DQK, int DV>
+cudaError_t launch_both(const BwdParams& p, const BwdMaps& maps, int num_tiles, cudaStream_t s) {
+  cudaError_t e = launch_t<DQK, DV, 1>(p, maps, num_tiles, s);
+  if (e != cudaSuccess) return e;
+  return launch_t<DQK, DV, 0>(p, maps, num_tiles, s);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_bwd_wide(const BwdParams& p, const BwdMaps& maps, int num_kv_tiles, cudaStream_t s) {
+  if (p.dqk == 256 && p.dv == 256) return launch_both<256, 256>(p, maps, num_kv_tiles, s);
+  if (p.dqk == 256 && p.dv == 512) return launch_both<256, 512>(p, maps, num_kv_tiles, s);
+  if (p.dqk == 512 && p.dv == 512) return launch_both<512, 512>(p, maps, num_kv_tiles, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace gcs

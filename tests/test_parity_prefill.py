@@ -19,9 +19,10 @@ CASES = {
     "mha_d128_window_only": ([385, 64], 2, 2, 128, 128, False, False, 129, True),
     "gqa_d128_sink_only": ([257, 33], 4, 2, 128, 128, False, True, 0, True),
     "gqa_d64_gate_only": ([190, 2, 66], 6, 3, 64, 64, True, False, 0, True),
-    "d256_d256": ([190, 130], 2, 2, 256, 256, True, True, 0, False),
-    "d256_d512_window": ([300, 140], 4, 2, 256, 512, True, True, 100, False),
-    "d512_d512": ([260, 77], 2, 1, 512, 512, True, True, 0, False),
+    "d256_d256": ([190, 130], 2, 2, 256, 256, True, True, 0, True),
+    "d256_d512_window": ([300, 140], 4, 2, 256, 512, True, True, 100, True),
+    "d512_d512": ([260, 77], 2, 1, 512, 512, True, True, 0, True),
+    "d512_d512_window_no_gate": ([200, 129], 4, 2, 512, 512, False, True, 65, True),
 }
 
 
@@ -52,10 +53,10 @@ def test_prefill_parity(gcs_lib, name):
             assert ds is None
 
 
-def test_backward_large_head_dims_not_yet_supported(gcs_lib):
-    case = make_prefill([64], 2, 2, 256, 512, seed=1)
+def test_unsupported_head_dims_raise(gcs_lib):
+    case = make_prefill([64], 2, 2, 96, 96, seed=1)
     with pytest.raises(NotImplementedError):
-        run_prefill(gcs_lib, case, backward=True)
+        run_prefill(gcs_lib, case, backward=False)
 
 
 def test_prefill_gather_order_is_exact(gcs_lib):
@@ -135,11 +136,11 @@ def test_full_size_dense_mha_t128_d64(gcs_lib):
         assert_close(n, got, ref, PREFILL_RTOL)
 
 
-def test_full_size_window_dqk256_dv512_forward_sampled(gcs_lib):
-    _sampled_full_size(gcs_lib, "window_b2_t4096_dqk256_dv512", kv_group=3, backward=False, seqs=[1])
+def test_full_size_window_dqk256_dv512_sampled(gcs_lib):
+    _sampled_full_size(gcs_lib, "window_b2_t4096_dqk256_dv512", kv_group=3, backward=True, seqs=[1])
 
 
-def test_full_size_varlen_d512_forward_sampled(gcs_lib):
+def test_full_size_varlen_d512_sampled(gcs_lib):
     case = prefill_config("varlen_16384_d512")
     shortest = int(np.argmin(case.seqlens))
-    _sampled_full_size(gcs_lib, "varlen_16384_d512", kv_group=2, backward=False, seqs=[shortest])
+    _sampled_full_size(gcs_lib, "varlen_16384_d512", kv_group=2, backward=True, seqs=[shortest])
