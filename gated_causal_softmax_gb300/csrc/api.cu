@@ -133,6 +133,7 @@ size_t bwd_ws(const gcs_prefill_args* a) {
   c.take<float>((size_t)a->total_tokens * a->hq * a->dqk);     // dQ accumulator
   if (a->log_gate || a->sink) c.take<float>(ht);               // row sums of dS
   if (a->log_gate) c.take<float>(ht);                          // column sums of dS
+  c.take<float>((size_t)a->hq * ((a->total_tokens + 63) / 64 + a->num_seqs) * 128);  // packed vectors
   return c.off;
 }
 
@@ -236,6 +237,8 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
   float* dq_acc = c.take<float>((size_t)a->total_tokens * a->hq * a->dqk);
   float* dg_row = (a->log_gate || a->sink) ? c.take<float>(ht) : nullptr;
   float* dg_col = a->log_gate ? c.take<float>(ht) : nullptr;
+  const int n_qtiles = (a->total_tokens + 63) / 64 + a->num_seqs;
+  float* vecp = c.take<float>((size_t)a->hq * n_qtiles * 128);
 
   BwdMaps maps;
   if (!make_map(&maps.q, a->q, (uint64_t)a->hq * a->dqk, a->total_tokens, 64) ||
@@ -250,6 +253,10 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
   }
   st = cuda_status(launch_bwd_pre(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout),
                                   a->total_tokens, a->hq, a->dv, a->dqk, delta, dq_acc, dg_row, dg_col, s));
+  if (st != GCS_OK) return st;
+
+  st = cuda_status(launch_bwd_pack(a->cu_seqlens, a->num_seqs, a->total_tokens, a->hq, n_qtiles, lse, gT, delta,
+                                   vecp, s));
   if (st != GCS_OK) return st;
 
   BwdParams p;
@@ -271,6 +278,8 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
   p.dq_acc = dq_acc;
   p.dg_row = dg_row;
   p.dg_col = dg_col;
+  p.vecp = vecp;
+  p.n_qtiles = n_qtiles;
   p.status = status;
   const int num_tiles = (a->total_tokens + 127) / 128 + a->num_seqs;
   KernelTimer timer(s);

@@ -47,6 +47,8 @@ struct BwdParams {
   float* dq_acc;         // fp32 [total, hq, dqk] (zeroed)
   float* dg_row;         // fp32 [hq, total] sum_j dS_ij (zeroed); null if not needed
   float* dg_col;         // fp32 [hq, total] sum_i dS_ij (zeroed); null if no gate
+  const float* vecp;     // packed per-(head, 64-row query tile) vectors (see launch_bwd_pack)
+  int n_qtiles;          // query tiles per head in vecp
   int* status;
 };
 
@@ -63,6 +65,10 @@ cudaError_t launch_gate_cumsum(const float* g, const int32_t* cu, int num_seqs, 
                                cudaStream_t s);
 cudaError_t launch_bwd_pre(const uint16_t* o, const uint16_t* dout, int total, int hq, int dv, int dqk,
                            float* delta, float* dq_acc, float* dg_row, float* dg_col, cudaStream_t s);
+// Packs (G_i - LSE_i) * log2 e and delta_i per (head, 64-row query tile): vecp
+// [hq][n_qtiles][128] with n_qtiles = ceil(total / 64) + num_seqs.
+cudaError_t launch_bwd_pack(const int32_t* cu, int num_seqs, int total, int hq, int n_qtiles, const float* lse,
+                            const float* gT, const float* delta, float* vecp, cudaStream_t s);
 cudaError_t launch_bwd_post(const float* dq_acc, uint16_t* dq, int total, int hq, int dqk, const int32_t* cu,
                             int num_seqs, const float* dg_row, const float* dg_col, float* dlog_gate,
                             const float* lse, const float* delta, const float* sink, float* dsink, cudaStream_t s);

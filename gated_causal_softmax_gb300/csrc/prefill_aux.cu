@@ -166,7 +166,47 @@ __global__ void __launch_bounds__(256) dsink_kernel(const float* __restrict__ ro
   }
 }
 
+// grid (query tiles of 64 rows over all sequences, hq), 64 threads: packs the per-column
+// vectors the fused backward reads per step, [h][tile][0..63] = (G_i - LSE_i) * log2 e,
+// [64..127] = delta_i, so one aligned 512-B bulk copy fetches them.
+__global__ void __launch_bounds__(64) bwd_pack_kernel(const int32_t* __restrict__ cu, int num_seqs, int total,
+                                                      const float* __restrict__ lse, const float* __restrict__ gT,
+                                                      const float* __restrict__ delta, float* __restrict__ vecp) {
+  int t = blockIdx.x;
+  int start = -1, len = 0, local = 0;
+  for (int s = 0; s < num_seqs; ++s) {
+    const int a = __ldg(cu + s), b = __ldg(cu + s + 1);
+    const int n = (b - a + 63) / 64;
+    if (t < n) {
+      start = a;
+      len = b - a;
+      local = t;
+      break;
+    }
+    t -= n;
+  }
+  if (start < 0) return;
+  const int h = blockIdx.y;
+  const int i = local * 64 + threadIdx.x;
+  float colterm = 0.f, dl = 0.f;
+  if (i < len) {
+    const size_t idx = (size_t)h * total + start + i;
+    colterm = -__ldg(lse + idx) * kLog2e;
+    if (gT) colterm += __ldg(gT + idx);
+    dl = __ldg(delta + idx);
+  }
+  float* dst = vecp + ((size_t)h * gridDim.x + blockIdx.x) * 128;
+  dst[threadIdx.x] = colterm;
+  dst[64 + threadIdx.x] = dl;
+}
+
 }  // namespace
+
+cudaError_t launch_bwd_pack(const int32_t* cu, int num_seqs, int total, int hq, int n_qtiles, const float* lse,
+                            const float* gT, const float* delta, float* vecp, cudaStream_t s) {
+  bwd_pack_kernel<<<dim3(n_qtiles, hq), 64, 0, s>>>(cu, num_seqs, total, lse, gT, delta, vecp);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_gate_cumsum(const float* g, const int32_t* cu, int num_seqs, int total, int hq, float* gT,
                                cudaStream_t s) {

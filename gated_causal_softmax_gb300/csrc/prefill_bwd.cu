@@ -10,18 +10,22 @@
 //     dP^T = V dO^T           (TMEM, fp32)        dS^T = P^T o (dP^T - delta_i)
 //     dV  += P^T dO           (A operand = P^T, bf16, written over the consumed S^T)
 //     dK  += dS^T Q           (A operand = dS^T, bf16, written over the consumed dP^T)
-//     dQ^T = K^T dS^T         (dS^T staged in shared memory; result written over S^T)
+//     dQ^T = K^T dS^T         (dS^T staged in shared memory; result written over dP^T)
 //     dQ  += scale * dQ^T     (coalesced fp32 reduce-adds straight from TMEM)
 // plus fp32 row / column sums of dS for the gate and sink gradients.
 //
-// Warp roles (320 threads): warp 0 TMA producer (K/V once; Q, dO and the per-column
-// LSE / delta / gate vectors in three rotating buffers), warp 1 tcgen05 issuer, warps
-// 2..5 and 6..9 two ping-pong softmax warpgroups: warpgroup w owns TMEM score buffer w
-// and handles the steps s with s % 2 == w, so one warpgroup's exponentials overlap the
-// other warpgroup's MMAs.  tcgen05.mma operations issued by one thread execute in issue
-// order, so an MMA may overwrite TMEM columns that an earlier MMA reads as its A operand.
+// Warp roles (320 threads): warp 0 TMA producer (K/V once; Q, dO and the packed
+// per-column LSE / delta / gate vectors in three rotating buffers), warp 1 tcgen05
+// issuer, warps 2..5 and 6..9 two ping-pong softmax warpgroups: warpgroup w owns TMEM
+// buffers S^T[w], dP^T[w] and handles the steps s with s % 2 == w, so one warpgroup's
+// exponentials overlap the other warpgroup's MMAs.  P^T and dS^T are signalled
+// separately (dV starts as soon as P^T is in TMEM), and because dQ^T lands in the dP^T
+// buffer the next step's S^T is issued without waiting for the dQ drain.  tcgen05.mma
+// operations issued by one thread execute in issue order, so an MMA may overwrite TMEM
+// columns that an earlier MMA reads as its A operand.
 #include "kernels.h"
 #include "sm103_ptx.cuh"
+#include "tiles.cuh"
 
 namespace gcs {
 namespace {
@@ -56,21 +60,6 @@ struct BwdCfg {
   static_assert(T_DK + DQK <= 512, "TMEM budget");
 };
 
-__device__ __forceinline__ bool find_kv_tile(const int32_t* cu, int num_seqs, int t, int& start, int& len, int& jt) {
-  for (int s = 0; s < num_seqs; ++s) {
-    const int a = __ldg(cu + s), b = __ldg(cu + s + 1);
-    const int n = (b - a + kBN - 1) / kBN;
-    if (t < n) {
-      start = a;
-      len = b - a;
-      jt = t;  // early key tiles see the most queries: hand them out first
-      return true;
-    }
-    t -= n;
-  }
-  return false;
-}
-
 __device__ __forceinline__ void red_add_f32(float* addr, float v) {
   asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
 }
@@ -84,9 +73,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-  int seq_start, len, jt;
-  if (!find_kv_tile(p.cu_seqlens, p.num_seqs, blockIdx.x, seq_start, len, jt)) return;
-  const int kvh = blockIdx.y;
+  // heaviest key tiles (most query tiles after them) first
+  TileRef tr;
+  if (!lpt_tile(p.cu_seqlens, p.num_seqs, kBN, blockIdx.y, tr)) return;
+  const int seq_start = tr.start, len = tr.len, jt = tr.n - 1 - tr.u;
+  int qoff = 0;  // first 64-row query tile of this sequence in the packed vectors
+  for (int q = 0; q < tr.seq; ++q) qoff += (__ldg(p.cu_seqlens + q + 1) - __ldg(p.cu_seqlens + q) + kBM - 1) / kBM;
+  const int kvh = blockIdx.x;
   const int group = p.hq / p.hkv;
   const int j0 = jt * kBN;
   // query tiles that see any key of this tile: i >= j0 (causal), i < j0 + 127 + W (window)
@@ -101,11 +94,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* kv_full = bars + 0;
   uint64_t* q_full = bars + 1;     // [kNQB]
   uint64_t* q_empty = bars + 4;    // [kNQB]
-  uint64_t* s_full = bars + 7;     // [2]
-  uint64_t* p_full = bars + 9;     // [2]
-  uint64_t* mma_done = bars + 11;  // [2]
-  uint64_t* dq_free = bars + 13;   // [2]
-  uint64_t* drain = bars + 15;
+  uint64_t* s_full = bars + 7;     // [2] S^T[b] written
+  uint64_t* dp_full = bars + 9;    // [2] dP^T[b] written
+  uint64_t* pv_ready = bars + 11;  // [2] P^T[b] stored (A operand of dV)
+  uint64_t* ds_ready = bars + 13;  // [2] dS^T[b] stored in TMEM and shared memory
+  uint64_t* mma_done = bars + 15;  // [2] dV, dK, dQ^T of the step retired
+  uint64_t* dq_free = bars + 17;   // [2] dQ^T drained from dP^T[b]
+  uint64_t* drain = bars + 19;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   const Abort ab{abort_flag, p.status};
@@ -114,12 +109,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
     for (int b = 0; b < kNQB; ++b) {
-      mbar_init(&q_full[b], 2);
+      mbar_init(&q_full[b], 1);
       mbar_init(&q_empty[b], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
-      mbar_init(&p_full[b], 4);
+      mbar_init(&dp_full[b], 1);
+      mbar_init(&pv_ready[b], 4);
+      mbar_init(&ds_ready[b], 4);
       mbar_init(&mma_done[b], 1);
       mbar_init(&dq_free[b], 4);
     }
@@ -151,43 +148,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(smem + C::OFF_V + c * kKVChunk, &tmV, kv_full, kvh * DV + c * 64, seq_start + j0);
     }
     const uint64_t pol = l2_policy_evict_last();
-    for (int s = 0; s < nsteps && ok; ++s) {
-      const int qb = s % kNQB;
-      const int h = kvh * group + s / n_it;
-      const int i0 = (it_lo + s % n_it) * kBM;
-      if (lane == 0) {
+    if (lane == 0) {
+      for (int s = 0; s < nsteps && ok; ++s) {
+        const int qb = s % kNQB;
+        const int h = kvh * group + s / n_it;
+        const int it = it_lo + s % n_it;
         ok = wait_bar(&q_empty[qb], ((s / kNQB) & 1) ^ 1, ab);
-        if (ok) {
-          mbar_expect_tx(&q_full[qb], (C::KCH + C::VCH) * kQChunk);
-          for (int c = 0; c < C::KCH; ++c)
-            tma_load_2d_hint(smem + C::OFF_Q + (qb * C::KCH + c) * kQChunk, &tmQ, &q_full[qb], h * DQK + c * 64,
-                             seq_start + i0, pol);
-          for (int c = 0; c < C::VCH; ++c)
-            tma_load_2d_hint(smem + C::OFF_DO + (qb * C::VCH + c) * kQChunk, &tmDO, &q_full[qb], h * DV + c * 64,
-                             seq_start + i0, pol);
-        }
+        if (!ok) break;
+        mbar_expect_tx(&q_full[qb], (C::KCH + C::VCH) * kQChunk + 2 * kBM * 4);
+        for (int c = 0; c < C::KCH; ++c)
+          tma_load_2d_hint(smem + C::OFF_Q + (qb * C::KCH + c) * kQChunk, &tmQ, &q_full[qb], h * DQK + c * 64,
+                           seq_start + it * kBM, pol);
+        for (int c = 0; c < C::VCH; ++c)
+          tma_load_2d_hint(smem + C::OFF_DO + (qb * C::VCH + c) * kQChunk, &tmDO, &q_full[qb], h * DV + c * 64,
+                           seq_start + it * kBM, pol);
+        // per-column vectors: [0..63] (G_i - LSE_i) log2 e, [64..127] delta_i
+        bulk_load(smem + C::OFF_VEC + qb * 2 * kBM * 4, p.vecp + ((size_t)h * p.n_qtiles + qoff + it) * 2 * kBM,
+                  2 * kBM * 4, &q_full[qb]);
       }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (!ok) break;
-      // per-column vectors: [0] G_i - LSE_i (log2 units), [1] delta_i, for i0 .. i0+63
-      float* vec = reinterpret_cast<float*>(smem + C::OFF_VEC) + qb * 2 * kBM;
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int c = lane * 2 + u;
-        const int i = i0 + c;
-        float colterm = 0.f, dl = 0.f;
-        if (i < len) {
-          const size_t idx = (size_t)h * p.total + seq_start + i;
-          colterm = -__ldg(p.lse + idx) * kLog2e;
-          if (p.gT) colterm += __ldg(p.gT + idx);
-          dl = __ldg(p.delta + idx);
-        }
-        vec[c] = colterm;
-        vec[kBM + c] = dl;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&q_full[qb]);
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -201,52 +181,67 @@ __global__ void __launch_bounds__(kThreads, 1)
       // rows 64..127 of K^T for DQK = 64 read the V tile (results ignored)
       const uint32_t lboK = (DQK >= 128) ? kKVChunk : (C::OFF_V - C::OFF_K);
       bool ok = wait_bar(kv_full, 0, ab);
-      auto issue_scores = [&](int t) -> bool {
+      auto issue_s = [&](int t) -> bool {  // S^T(t) = K Q(t)^T -> S^T[t & 1]
         const int qb = t % kNQB, b = t & 1;
         if (!wait_bar(&q_full[qb], (t / kNQB) & 1, ab)) return false;
         tc_fence_after();
-        const uint32_t qa = sQ + qb * C::KCH * kQChunk, da = sDO + qb * C::VCH * kQChunk;
+        const uint32_t qa = sQ + qb * C::KCH * kQChunk;
         for (int c = 0; c < C::KCH; ++c)
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             mma_ss(tmem + C::T_S + 64 * b, sdesc_sw128(sK + c * kKVChunk + k * 32, 16, 1024),
                    sdesc_sw128(qa + c * kQChunk + k * 32, 16, 1024), idS, (c | k) != 0);
+        mma_commit(&s_full[b]);
+        return true;
+      };
+      auto issue_dp = [&](int t) {  // dP^T(t) = V dO(t)^T -> dP^T[t & 1] (Q/dO(t) already landed)
+        const int qb = t % kNQB, b = t & 1;
+        const uint32_t da = sDO + qb * C::VCH * kQChunk;
         for (int c = 0; c < C::VCH; ++c)
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             mma_ss(tmem + C::T_DP + 64 * b, sdesc_sw128(sV + c * kKVChunk + k * 32, 16, 1024),
                    sdesc_sw128(da + c * kQChunk + k * 32, 16, 1024), idS, (c | k) != 0);
-        mma_commit(&s_full[b]);
-        return true;
+        mma_commit(&dp_full[b]);
       };
-      if (ok && nsteps > 0) ok = issue_scores(0);
-      if (ok && nsteps > 1) ok = issue_scores(1);
+      for (int t = 0; t < 2 && t < nsteps && ok; ++t) {
+        ok = issue_s(t);
+        if (ok) issue_dp(t);
+      }
       for (int s = 0; s < nsteps && ok; ++s) {
         const int b = s & 1, qb = s % kNQB;
-        ok = wait_bar(&p_full[b], (s >> 1) & 1, ab);
+        const uint32_t qa = sQ + qb * C::KCH * kQChunk, da = sDO + qb * C::VCH * kQChunk;
+        ok = wait_bar(&pv_ready[b], (s >> 1) & 1, ab);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t qa = sQ + qb * C::KCH * kQChunk, da = sDO + qb * C::VCH * kQChunk;
         // K dimension = 64 query rows = 4 steps of 16 rows (2048 B in the MN-major views)
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           mma_ts(tmem + C::T_DV, tmem + C::T_S + 64 * b + k * 8, sdesc_sw128(da + k * 2048, kQChunk, 1024), idDV,
                  (s > 0 || k > 0) ? 1u : 0u);
+        // dP^T of the other buffer's next step as soon as its dQ^T has been drained, so the
+        // other warpgroup's dS phase overlaps this warpgroup's
+        if (s + 1 < nsteps && s + 1 >= 2) {
+          ok = wait_bar(&dq_free[b ^ 1], ((s - 1) >> 1) & 1, ab);
+          if (!ok) break;
+          issue_dp(s + 1);
+        }
+        ok = wait_bar(&ds_ready[b], (s >> 1) & 1, ab);
+        if (!ok) break;
+        tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           mma_ts(tmem + C::T_DK, tmem + C::T_DP + 64 * b + k * 8, sdesc_sw128(qa + k * 2048, kQChunk, 1024), idDK,
                  (s > 0 || k > 0) ? 1u : 0u);
-        // dQ^T over the score buffer b (its P^T was read by the dV MMAs above)
+        // dQ^T over the dP^T buffer b (its dS^T was read by the dK MMAs above)
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          mma_ss(tmem + C::T_S + 64 * b, sdesc_sw128(sK + k * 2048, lboK, 1024),
+          mma_ss(tmem + C::T_DP + 64 * b, sdesc_sw128(sK + k * 2048, lboK, 1024),
                  sdesc_sw128(sDS + b * kKVChunk + k * 2048, kKVChunk, 1024), idDQ, k > 0);
         mma_commit(&mma_done[b]);
         mma_commit(&q_empty[qb]);
-        if (s + 2 < nsteps) {
-          ok = wait_bar(&dq_free[b], (s >> 1) & 1, ab);
-          if (ok) ok = issue_scores(s + 2);
-        }
+        // next scores of this buffer (P^T was read by dV above)
+        if (s + 2 < nsteps) ok = issue_s(s + 2);
       }
       if (!ok) {
         mma_commit(drain);
@@ -283,55 +278,92 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ok = wait_bar(&q_full[qb], (s / kNQB) & 1, ab);
       if (!ok) break;
+      const float4* vec4 = reinterpret_cast<const float4*>(smem + C::OFF_VEC + qb * 2 * kBM * 4);
+      const bool need_mask = (i0 < j0 + kBN - 1) || (p.window > 0 && i0 + kBM - 1 - j0 >= p.window) ||
+                             (i0 + kBM > len);
+      // ---- P = 2^(S scale log2e + G_i - LSE_i - G_j) in fp32, P^T (bf16) over S^T
       ok = wait_bar(&s_full[wg], (s >> 1) & 1, ab);
       if (!ok) break;
       tc_fence_after();
-      const float* vec = reinterpret_cast<const float*>(smem + C::OFF_VEC) + qb * 2 * kBM;
-      const bool need_mask = (i0 < j0 + kBN - 1) || (p.window > 0 && i0 + kBM - 1 - j0 >= p.window) ||
-                             (i0 + kBM > len);
+      float pr[64];
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
-        uint32_t sv[32], dp[32];
+        uint32_t sv[32];
         tmem_ld32(tS + 32 * ch, sv);
-        tmem_ld32(tDP + 32 * ch, dp);
         tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int col = 32 * ch + c;
-          float t = fmaf(__uint_as_float(sv[c]), p.scale_log2, vec[col]) + rowterm;
-          if (need_mask) {
-            const int i = i0 + col;
-            const bool vis = (i < len) && (jl <= i) && (p.window == 0 || i - jl < p.window);
-            t = vis ? t : neg_inf();
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 ct = vec4[8 * ch + c4];
+          const float cts[4] = {ct.x, ct.y, ct.z, ct.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = 4 * c4 + e, col = 32 * ch + c;
+            float t = fmaf(__uint_as_float(sv[c]), p.scale_log2, cts[e]) + rowterm;
+            if (need_mask) {
+              const int i = i0 + col;
+              const bool vis = (i < len) && (jl <= i) && (p.window == 0 || i - jl < p.window);
+              t = vis ? t : neg_inf();
+            }
+            pr[col] = ex2(t);
           }
-          const float pr = ex2(t);
-          sv[c] = __float_as_uint(pr);
-          dp[c] = __float_as_uint(pr * (__uint_as_float(dp[c]) - vec[kBM + col]));
         }
         uint32_t pk[16];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(__uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1]));
-        tmem_st16(tS + 16 * ch, pk);  // P^T over S^T columns already loaded
+        for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(pr[32 * ch + 2 * c], pr[32 * ch + 2 * c + 1]);
+        tmem_st16(tS + 16 * ch, pk);  // over S^T columns already loaded
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pv_ready[wg]);
+      // ---- dS = P (dP - delta_i) in fp32, dS^T (bf16) over dP^T and into shared memory
+      ok = wait_bar(&dp_full[wg], (s >> 1) & 1, ab);
+      if (!ok) break;
+      tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(__uint_as_float(dp[2 * c]), __uint_as_float(dp[2 * c + 1]));
+      for (int ch = 0; ch < 2; ++ch) {
+        uint32_t dp[32];
+        tmem_ld32(tDP + 32 * ch, dp);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 dl = vec4[16 + 8 * ch + c4];
+          const float dls[4] = {dl.x, dl.y, dl.z, dl.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = 4 * c4 + e, col = 32 * ch + c;
+            pr[col] = pr[col] * (__uint_as_float(dp[c]) - dls[e]);
+          }
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(pr[32 * ch + 2 * c], pr[32 * ch + 2 * c + 1]);
         tmem_st16(tDP + 16 * ch, pk);
         // dS^T row r, query columns 32ch .. 32ch+31 = 16-B pieces 4ch .. 4ch+3 of the swizzled row
 #pragma unroll
         for (int q = 0; q < 4; ++q)
           *reinterpret_cast<uint4*>(sDS + sw128_offset(r, 4 * ch + q)) =
               make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-        if (has_gate) {
-          float acc = 0.f;
+      }
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ds_ready[wg]);
+      // ---- fp32 sums of dS: over this row's query columns (column sum for key j) and over
+      // the warp's 32 key rows for each query column (transpose-reduce; lane l ends with
+      // column 32ch + l)
+      if (has_gate) {
+        float acc = 0.f;
 #pragma unroll
-          for (int c = 0; c < 32; ++c) acc += __uint_as_float(dp[c]);
-          dgcol += acc;
-        }
-        if (want_row) {
-          // sum of dS over this warp's 32 key rows for each of the 32 columns:
-          // transpose-reduce, lane l ends with column 32ch + l
-          float v[32];
+        for (int c = 0; c < 64; ++c) acc += pr[c];
+        dgcol += acc;
+      }
+      if (want_row) {
+        // in place on pr (the column sum above was its last other use)
 #pragma unroll
-          for (int c = 0; c < 32; ++c) v[c] = __uint_as_float(dp[c]);
+        for (int ch = 0; ch < 2; ++ch) {
+          float* v = pr + 32 * ch;
 #pragma unroll
           for (int half = 16; half >= 1; half >>= 1) {
             const bool upper = (lane & half) != 0;
@@ -346,18 +378,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (i < len) red_add_f32(p.dg_row + (size_t)h * p.total + seq_start + i, v[0]);
         }
       }
-      tmem_st_wait();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[wg]);
-      // ---- dQ^T of this step: TMEM -> registers -> coalesced fp32 reduce-adds into dQ
+      // ---- dQ^T of this step: TMEM (dP^T buffer) -> registers -> fp32 reduce-adds into dQ
       ok = wait_bar(&mma_done[wg], (s >> 1) & 1, ab);
       if (!ok) break;
       tc_fence_after();
       uint32_t dq[64];
-      tmem_ld32(tS, dq);
-      tmem_ld32(tS + 32, dq + 32);
+      tmem_ld32(tDP, dq);
+      tmem_ld32(tDP + 32, dq + 32);
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
@@ -425,7 +452,7 @@ cudaError_t launch_t(const BwdParams& p, const BwdMaps& maps, int num_tiles, cud
   auto kern = prefill_bwd_kernel<DQK, DV>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<dim3(num_tiles, p.hkv), kThreads, C::SMEM, s>>>(maps.q, maps.k, maps.v, maps.dout, p);
+  kern<<<dim3(p.hkv, num_tiles), kThreads, C::SMEM, s>>>(maps.q, maps.k, maps.v, maps.dout, p);
   return cudaGetLastError();
 }
 

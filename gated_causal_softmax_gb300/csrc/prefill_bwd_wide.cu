@@ -18,6 +18,7 @@
 // Row / column sums of dS (gate and sink gradients) are taken by the KQ role with k0 = 0.
 #include "kernels.h"
 #include "sm103_ptx.cuh"
+#include "tiles.cuh"
 
 namespace gcs {
 namespace {
@@ -52,21 +53,6 @@ struct WideCfg {
   static constexpr int T_S = 0, T_DP = 64, T_ACC = 128, T_DQ = 384;
 };
 
-__device__ __forceinline__ bool find_kv_tile(const int32_t* cu, int num_seqs, int t, int& start, int& len, int& jt) {
-  for (int s = 0; s < num_seqs; ++s) {
-    const int a = __ldg(cu + s), b = __ldg(cu + s + 1);
-    const int n = (b - a + kBN - 1) / kBN;
-    if (t < n) {
-      start = a;
-      len = b - a;
-      jt = t;
-      return true;
-    }
-    t -= n;
-  }
-  return false;
-}
-
 template <int DQK, int DV, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -76,9 +62,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-  int seq_start, len, jt;
-  if (!find_kv_tile(p.cu_seqlens, p.num_seqs, blockIdx.x, seq_start, len, jt)) return;
-  const int kvh = blockIdx.y;
+  TileRef tr;
+  if (!lpt_tile(p.cu_seqlens, p.num_seqs, kBN, blockIdx.y, tr)) return;
+  const int seq_start = tr.start, len = tr.len, jt = tr.n - 1 - tr.u;
+  const int kvh = blockIdx.x;
   const int w0 = blockIdx.z * kW;         // v0 (role V) or k0 (role KQ)
   const int res0 = (KIND == 1) ? w0 / 64 : 0;  // first resident K chunk
   const int group = p.hq / p.hkv;
@@ -470,7 +457,7 @@ cudaError_t launch_t(const BwdParams& p, const BwdMaps& maps, int num_tiles, cud
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const int roles = (KIND == 1 ? DQK : DV) / kW;
-  kern<<<dim3(num_tiles, p.hkv, roles), kThreads, C::SMEM, s>>>(maps.q, maps.k, maps.v, maps.dout, p);
+  kern<<<dim3(p.hkv, num_tiles, roles), kThreads, C::SMEM, s>>>(maps.q, maps.k, maps.v, maps.dout, p);
   return cudaGetLastError();
 }
 

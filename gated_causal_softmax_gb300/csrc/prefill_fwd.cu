@@ -19,6 +19,7 @@
 // scores come first, so the running max rarely moves and O is rarely rescaled.
 #include "kernels.h"
 #include "sm103_ptx.cuh"
+#include "tiles.cuh"
 
 namespace gcs {
 namespace {
@@ -50,23 +51,6 @@ struct FwdCfg {
   static_assert(256 + DVC <= 512, "TMEM budget");
 };
 
-// Maps a linear tile index to (sequence start, length, query tile); tiles of each
-// sequence are handed out last-tile-first (the diagonal-heavy ones first).
-__device__ __forceinline__ bool find_tile(const int32_t* cu, int num_seqs, int t, int& start, int& len, int& qt) {
-  for (int s = 0; s < num_seqs; ++s) {
-    const int a = __ldg(cu + s), b = __ldg(cu + s + 1);
-    const int n = (b - a + kBM - 1) / kBM;
-    if (t < n) {
-      start = a;
-      len = b - a;
-      qt = n - 1 - t;
-      return true;
-    }
-    t -= n;
-  }
-  return false;
-}
-
 template <int DQK, int DVC>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -75,9 +59,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-  int seq_start, len, qt;
-  if (!find_tile(p.cu_seqlens, p.num_seqs, blockIdx.x, seq_start, len, qt)) return;
-  const int h = blockIdx.y;
+  // heaviest query tiles (most key tiles to visit) first
+  TileRef tr;
+  if (!lpt_tile(p.cu_seqlens, p.num_seqs, kBM, blockIdx.y, tr)) return;
+  const int seq_start = tr.start, len = tr.len, qt = tr.u;
+  const int h = blockIdx.x;
   const int kvh = h / (p.hq / p.hkv);
   const int dv0 = blockIdx.z * DVC;
   const int q0 = qt * kBM;
@@ -372,7 +358,7 @@ cudaError_t launch_t(const FwdParams& p, const FwdMaps& maps, int num_tiles, cud
   auto kern = prefill_fwd_kernel<DQK, DVC>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  dim3 grid(num_tiles, p.hq, p.dv / DVC);
+  dim3 grid(p.hq, num_tiles, p.dv / DVC);  // heads fastest, so every head's heavy tiles go first
   kern<<<grid, kThreads, C::SMEM, s>>>(maps.q, maps.k, maps.v, p);
   return cudaGetLastError();
 }
