@@ -34,8 +34,8 @@ PREFILL_WORKLOAD = "varlen_gqa_8192_d128"
 DECODE_WORKLOAD = "paged_fp8_decode_64x1"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # my kernels per prefill step with gates and sink: fwd (gate cumsum, attention) and bwd
-# (gate cumsum, delta, attention, dQ convert, d gate scan, d sink reduce)
-LAUNCHES_PER_PREFILL_STEP = 8
+# (gate cumsum, delta, vector pack, dQ pass, dK/dV pass, d gate scan, d sink reduce)
+LAUNCHES_PER_PREFILL_STEP = 9
 LAUNCHES_PER_DECODE = 2
 
 
@@ -215,7 +215,8 @@ def run_native(args):
 
     # dominant kernel: the fused backward attention kernel
     sustained = pk.get("bf16_tflops_sustained", pk.get("bf16_tflops"))
-    dom = "prefill_bwd_kernel<128,128>" if bwd_k >= fwd_k else "prefill_fwd_kernel<128,128>"
+    dom = ("prefill_bwd_dq_kernel<128> + prefill_bwd_kernel<128,128> (two-pass backward)" if bwd_k >= fwd_k
+           else "prefill_fwd_kernel<128,128>")
     dom_fl, dom_ms = (bwd_fl, bwd_k) if bwd_k >= fwd_k else (fwd_fl, fwd_k)
     achieved = dom_fl / (dom_ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": sustained,

@@ -125,12 +125,16 @@ size_t fwd_ws(const gcs_prefill_args* a) {
   return c.off;
 }
 
+// Head dims <= 128 take the two-pass backward (dQ pass + dK/dV pass, no fp32 dQ buffer);
+// wider heads take the output-column roles with an fp32 dQ accumulator.
+bool two_pass(const gcs_prefill_args* a) { return a->dqk <= 128 && a->dv <= 128; }
+
 size_t bwd_ws(const gcs_prefill_args* a) {
   Carver c{nullptr};
   const size_t ht = (size_t)a->hq * a->total_tokens;
   if (a->log_gate) c.take<float>(ht);                         // G^T
   c.take<float>(ht);                                           // delta
-  c.take<float>((size_t)a->total_tokens * a->hq * a->dqk);     // dQ accumulator
+  if (!two_pass(a)) c.take<float>((size_t)a->total_tokens * a->hq * a->dqk);  // dQ accumulator
   if (a->log_gate || a->sink) c.take<float>(ht);               // row sums of dS
   if (a->log_gate) c.take<float>(ht);                          // column sums of dS
   c.take<float>((size_t)a->hq * ((a->total_tokens + 63) / 64 + a->num_seqs) * 128);  // packed vectors
@@ -234,7 +238,8 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
   Carver c{static_cast<uint8_t*>(workspace)};
   float* gT = a->log_gate ? c.take<float>(ht) : nullptr;
   float* delta = c.take<float>(ht);
-  float* dq_acc = c.take<float>((size_t)a->total_tokens * a->hq * a->dqk);
+  const bool tp = two_pass(a);
+  float* dq_acc = tp ? nullptr : c.take<float>((size_t)a->total_tokens * a->hq * a->dqk);
   float* dg_row = (a->log_gate || a->sink) ? c.take<float>(ht) : nullptr;
   float* dg_col = a->log_gate ? c.take<float>(ht) : nullptr;
   const int n_qtiles = (a->total_tokens + 63) / 64 + a->num_seqs;
@@ -244,7 +249,9 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
   if (!make_map(&maps.q, a->q, (uint64_t)a->hq * a->dqk, a->total_tokens, 64) ||
       !make_map(&maps.k, a->k, (uint64_t)a->hkv * a->dqk, a->total_tokens, 128) ||
       !make_map(&maps.v, a->v, (uint64_t)a->hkv * a->dv, a->total_tokens, 128) ||
-      !make_map(&maps.dout, dout, (uint64_t)a->hq * a->dv, a->total_tokens, 64))
+      !make_map(&maps.dout, dout, (uint64_t)a->hq * a->dv, a->total_tokens, 64) ||
+      !make_map(&maps.q128, a->q, (uint64_t)a->hq * a->dqk, a->total_tokens, 128) ||
+      !make_map(&maps.dout128, dout, (uint64_t)a->hq * a->dv, a->total_tokens, 128))
     return GCS_ERR_CUDA;
 
   if (gT) {
@@ -273,6 +280,7 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
   p.gT = gT;
   p.lse = lse;
   p.delta = delta;
+  p.grad_q = static_cast<uint16_t*>(dq);
   p.grad_k = static_cast<uint16_t*>(dk);
   p.grad_v = static_cast<uint16_t*>(dv);
   p.dq_acc = dq_acc;
@@ -283,10 +291,21 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
   p.status = status;
   const int num_tiles = (a->total_tokens + 127) / 128 + a->num_seqs;
   KernelTimer timer(s);
-  timer.before();
-  st = cuda_status(a->dqk <= 128 && a->dv <= 128 ? launch_prefill_bwd(p, maps, num_tiles, s)
-                                                 : launch_prefill_bwd_wide(p, maps, num_tiles, s));
-  timer.after();
+  if (tp) {
+    // dQ pass (query tiles of 128 rows), then the dK/dV pass; the timer brackets both
+    BwdMaps dqmaps = maps;
+    dqmaps.q = maps.q128;
+    dqmaps.dout = maps.dout128;
+    timer.before();
+    st = cuda_status(launch_prefill_bwd_dq(p, dqmaps, num_tiles, s));
+    if (st != GCS_OK) return st;
+    st = cuda_status(launch_prefill_bwd(p, maps, num_tiles, s));
+    timer.after();
+  } else {
+    timer.before();
+    st = cuda_status(launch_prefill_bwd_wide(p, maps, num_tiles, s));
+    timer.after();
+  }
   if (st != GCS_OK) return st;
   return cuda_status(launch_bwd_post(dq_acc, static_cast<uint16_t*>(dq), a->total_tokens, a->hq, a->dqk,
                                      a->cu_seqlens, a->num_seqs, dg_row, dg_col, dlog_gate, lse, delta, a->sink,

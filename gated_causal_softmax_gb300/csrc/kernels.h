@@ -42,10 +42,11 @@ struct BwdParams {
   const float* gT;       // G^T [hq, total] (log2 units) or null
   const float* lse;      // [hq, total] natural log
   const float* delta;    // [hq, total] rowsum(dO * O)
+  uint16_t* grad_q;      // bf16 [total, hq, dqk] (written directly by the dQ pass)
   uint16_t* grad_k;      // bf16 [total, hkv, dqk]
   uint16_t* grad_v;      // bf16 [total, hkv, dv]
-  float* dq_acc;         // fp32 [total, hq, dqk] (zeroed)
-  float* dg_row;         // fp32 [hq, total] sum_j dS_ij (zeroed); null if not needed
+  float* dq_acc;         // fp32 [total, hq, dqk] (zeroed; wide head dims only)
+  float* dg_row;         // fp32 [hq, total] sum_j dS_ij; null if not needed
   float* dg_col;         // fp32 [hq, total] sum_i dS_ij (zeroed); null if no gate
   const float* vecp;     // packed per-(head, 64-row query tile) vectors (see launch_bwd_pack)
   int n_qtiles;          // query tiles per head in vecp
@@ -53,10 +54,13 @@ struct BwdParams {
 };
 
 struct BwdMaps {
-  CUtensorMap q, k, v, dout;  // 2-D bf16 maps, 128-B swizzle
+  CUtensorMap q, k, v, dout;   // 2-D bf16 maps, 128-B swizzle (q, dout: 64-row boxes)
+  CUtensorMap q128, dout128;   // q, dout with 128-row boxes (dQ pass)
 };
 
 cudaError_t launch_prefill_bwd(const BwdParams& p, const BwdMaps& maps, int num_kv_tiles, cudaStream_t s);
+// dQ pass of the two-pass backward (head dims <= 128): writes dQ (bf16) and dS row sums.
+cudaError_t launch_prefill_bwd_dq(const BwdParams& p, const BwdMaps& maps, int num_q_tiles, cudaStream_t s);
 // Head dims above 128: output-column roles (dV chunks; dK + dQ chunks), two launches.
 cudaError_t launch_prefill_bwd_wide(const BwdParams& p, const BwdMaps& maps, int num_kv_tiles, cudaStream_t s);
 

@@ -220,7 +220,7 @@ cudaError_t launch_bwd_pre(const uint16_t* o, const uint16_t* dout, int total, i
   bwd_pre_kernel<<<(rows + 7) / 8, 256, 0, s>>>(o, dout, total, hq, dv, delta);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = cudaMemsetAsync(dq_acc, 0, (size_t)total * hq * dqk * sizeof(float), s);
+  if (dq_acc) e = cudaMemsetAsync(dq_acc, 0, (size_t)total * hq * dqk * sizeof(float), s);
   if (e != cudaSuccess) return e;
   if (dg_row) e = cudaMemsetAsync(dg_row, 0, (size_t)total * hq * sizeof(float), s);
   if (e != cudaSuccess) return e;
@@ -231,12 +231,15 @@ cudaError_t launch_bwd_pre(const uint16_t* o, const uint16_t* dout, int total, i
 cudaError_t launch_bwd_post(const float* dq_acc, uint16_t* dq, int total, int hq, int dqk, const int32_t* cu,
                             int num_seqs, const float* dg_row, const float* dg_col, float* dlog_gate,
                             const float* lse, const float* delta, const float* sink, float* dsink, cudaStream_t s) {
-  const size_t n4 = (size_t)total * hq * dqk / 4;
-  const int blocks = (int)((n4 + 255) / 256 < 152 * 16 ? (n4 + 255) / 256 : 152 * 16);
-  dq_convert_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(dq_acc), reinterpret_cast<uint2*>(dq),
-                                           n4);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
+  if (dq_acc) {
+    const size_t n4 = (size_t)total * hq * dqk / 4;
+    const int blocks = (int)((n4 + 255) / 256 < 152 * 16 ? (n4 + 255) / 256 : 152 * 16);
+    dq_convert_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(dq_acc), reinterpret_cast<uint2*>(dq),
+                                             n4);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   if (dlog_gate) {
     dgate_kernel<<<dim3(num_seqs, hq), kScanThreads, 0, s>>>(dg_row, dg_col, cu, total, hq, dlog_gate);
     e = cudaGetLastError();

@@ -1,8 +1,8 @@
-// Prefill backward, single pass: dQ is folded into the dK/dV pass
-// (fla-org/flash-linear-attention #1322 "Gluon attention backend with large head
-// dimensions": Oct 5 comment -- each score and dP tile is computed once, dQ partials
-// accumulate into a zero-initialised fp32 buffer that is converted afterwards, gate and
-// sink partials use fp32 reductions; Oct 3 comment -- probabilities recomputed in fp32).
+// Prefill backward, dK / dV pass of the two-pass backward (fla-org/flash-linear-attention
+// #1322 "Gluon attention backend with large head dimensions": Oct 5 comment keeps the
+// two-pass route beside the fused-dQ experiment; Oct 3 comment -- probabilities
+// recomputed in fp32).  dQ and the row sums of dS come from the dQ pass
+// (prefill_bwd_dq.cu), so this kernel has no reduce-adds on its hot path.
 //
 // One CTA per (128-key tile, kv head); it loops over the query heads of its GQA group and
 // over 64-row query tiles in the causal / window range ("steps").  Per step:
@@ -10,19 +10,16 @@
 //     dP^T = V dO^T           (TMEM, fp32)        dS^T = P^T o (dP^T - delta_i)
 //     dV  += P^T dO           (A operand = P^T, bf16, written over the consumed S^T)
 //     dK  += dS^T Q           (A operand = dS^T, bf16, written over the consumed dP^T)
-//     dQ^T = K^T dS^T         (dS^T staged in shared memory; result written over dP^T)
-//     dQ  += scale * dQ^T     (coalesced fp32 reduce-adds straight from TMEM)
-// plus fp32 row / column sums of dS for the gate and sink gradients.
+// plus the fp32 column sums of dS (gate gradient), one thread per key row.
 //
 // Warp roles (320 threads): warp 0 TMA producer (K/V once; Q, dO and the packed
-// per-column LSE / delta / gate vectors in three rotating buffers), warp 1 tcgen05
-// issuer, warps 2..5 and 6..9 two ping-pong softmax warpgroups: warpgroup w owns TMEM
-// buffers S^T[w], dP^T[w] and handles the steps s with s % 2 == w, so one warpgroup's
+// per-column LSE / delta / gate vectors in rotating buffers), warp 1 tcgen05 issuer,
+// warps 2..5 and 6..9 two ping-pong softmax warpgroups: warpgroup w owns TMEM buffers
+// S^T[w], dP^T[w] and handles the steps s with s % 2 == w, so one warpgroup's
 // exponentials overlap the other warpgroup's MMAs.  P^T and dS^T are signalled
-// separately (dV starts as soon as P^T is in TMEM), and because dQ^T lands in the dP^T
-// buffer the next step's S^T is issued without waiting for the dQ drain.  tcgen05.mma
-// operations issued by one thread execute in issue order, so an MMA may overwrite TMEM
-// columns that an earlier MMA reads as its A operand.
+// separately (dV starts as soon as P^T is in TMEM).  tcgen05.mma operations issued by
+// one thread execute in issue order, so an MMA may overwrite TMEM columns that an
+// earlier MMA reads as its A operand.
 #include "kernels.h"
 #include "sm103_ptx.cuh"
 #include "tiles.cuh"
@@ -33,7 +30,7 @@ namespace {
 constexpr int kBN = 128;  // keys per CTA (TMEM lanes)
 constexpr int kBM = 64;   // query rows per step
 constexpr int kThreads = 320;
-constexpr int kNQB = 3;   // query-side buffers
+constexpr int kNQB = 4;   // query-side buffers
 constexpr int kKVChunk = 128 * 128;  // 128 rows x 64 bf16
 constexpr int kQChunk = 64 * 128;    // 64 rows x 64 bf16
 constexpr float kLog2e = 1.4426950408889634f;
@@ -48,8 +45,7 @@ struct BwdCfg {
   static constexpr int OFF_V = OFF_K + KCH * kKVChunk;
   static constexpr int OFF_Q = OFF_V + VCH * kKVChunk;            // [kNQB][KCH] chunks
   static constexpr int OFF_DO = OFF_Q + kNQB * KCH * kQChunk;     // [kNQB][VCH] chunks
-  static constexpr int OFF_DS = OFF_DO + kNQB * VCH * kQChunk;    // [2] 128 rows x 64 bf16
-  static constexpr int OFF_VEC = OFF_DS + 2 * kKVChunk;           // [kNQB][2][64] floats
+  static constexpr int OFF_VEC = OFF_DO + kNQB * VCH * kQChunk;   // [kNQB][2][64] floats
   static constexpr int OFF_BAR = OFF_VEC + kNQB * 2 * kBM * 4;
   static constexpr int NBAR = 24;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
@@ -62,6 +58,25 @@ struct BwdCfg {
 
 __device__ __forceinline__ void red_add_f32(float* addr, float v) {
   asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+}
+
+// P for 32 query columns of a key row: pr = 2^(S scale log2e + colterm_i + rowterm),
+// MASK keeps columns cmin..cmax (compile-time variant: unmasked steps carry no mask work).
+template <bool MASK>
+__device__ __forceinline__ void p_chunk(float* pr, const uint32_t* sv, const float4* ct4, float rowterm,
+                                        float scale_log2, int cb, int cmin, int cmax) {
+#pragma unroll
+  for (int c4 = 0; c4 < 8; ++c4) {
+    const float4 ct = ct4[c4];
+    const float cts[4] = {ct.x + rowterm, ct.y + rowterm, ct.z + rowterm, ct.w + rowterm};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int c = 4 * c4 + e;
+      float t = fmaf(__uint_as_float(sv[c]), scale_log2, cts[e]);
+      if (MASK) t = (cb + c >= cmin && cb + c <= cmax) ? t : neg_inf();
+      pr[c] = ex2(t);
+    }
+  }
 }
 
 template <int DQK, int DV>
@@ -93,14 +108,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* kv_full = bars + 0;
   uint64_t* q_full = bars + 1;     // [kNQB]
-  uint64_t* q_empty = bars + 4;    // [kNQB]
-  uint64_t* s_full = bars + 7;     // [2] S^T[b] written
-  uint64_t* dp_full = bars + 9;    // [2] dP^T[b] written
-  uint64_t* pv_ready = bars + 11;  // [2] P^T[b] stored (A operand of dV)
-  uint64_t* ds_ready = bars + 13;  // [2] dS^T[b] stored in TMEM and shared memory
-  uint64_t* mma_done = bars + 15;  // [2] dV, dK, dQ^T of the step retired
-  uint64_t* dq_free = bars + 17;   // [2] dQ^T drained from dP^T[b]
+  uint64_t* q_empty = bars + 5;    // [kNQB]
+  uint64_t* s_full = bars + 9;     // [2] S^T[b] written
+  uint64_t* dp_full = bars + 11;   // [2] dP^T[b] written
+  uint64_t* pv_ready = bars + 13;  // [2] P^T[b] stored (A operand of dV)
+  uint64_t* ds_ready = bars + 15;  // [2] dS^T[b] stored (A operand of dK)
   uint64_t* drain = bars + 19;
+  uint64_t* all_done = bars + 20;  // every MMA of the CTA retired (epilogue)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   const Abort ab{abort_flag, p.status};
@@ -117,10 +131,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&dp_full[b], 1);
       mbar_init(&pv_ready[b], 4);
       mbar_init(&ds_ready[b], 4);
-      mbar_init(&mma_done[b], 1);
-      mbar_init(&dq_free[b], 4);
     }
     mbar_init(drain, 1);
+    mbar_init(all_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -174,12 +187,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idS = idesc_bf16(128, kBM, false, false);   // S^T, dP^T
       const uint32_t idDV = idesc_bf16(128, DV, false, true);    // dV += P^T dO
       const uint32_t idDK = idesc_bf16(128, DQK, false, true);   // dK += dS^T Q
-      const uint32_t idDQ = idesc_bf16(128, kBM, true, true);    // dQ^T = K^T dS^T
       const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
       const uint32_t sQ = smem_u32(smem + C::OFF_Q), sDO = smem_u32(smem + C::OFF_DO);
-      const uint32_t sDS = smem_u32(smem + C::OFF_DS);
-      // rows 64..127 of K^T for DQK = 64 read the V tile (results ignored)
-      const uint32_t lboK = (DQK >= 128) ? kKVChunk : (C::OFF_V - C::OFF_K);
       bool ok = wait_bar(kv_full, 0, ab);
       auto issue_s = [&](int t) -> bool {  // S^T(t) = K Q(t)^T -> S^T[t & 1]
         const int qb = t % kNQB, b = t & 1;
@@ -219,13 +228,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < 4; ++k)
           mma_ts(tmem + C::T_DV, tmem + C::T_S + 64 * b + k * 8, sdesc_sw128(da + k * 2048, kQChunk, 1024), idDV,
                  (s > 0 || k > 0) ? 1u : 0u);
-        // dP^T of the other buffer's next step as soon as its dQ^T has been drained, so the
-        // other warpgroup's dS phase overlaps this warpgroup's
-        if (s + 1 < nsteps && s + 1 >= 2) {
-          ok = wait_bar(&dq_free[b ^ 1], ((s - 1) >> 1) & 1, ab);
-          if (!ok) break;
-          issue_dp(s + 1);
-        }
         ok = wait_bar(&ds_ready[b], (s >> 1) & 1, ab);
         if (!ok) break;
         tc_fence_after();
@@ -233,16 +235,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < 4; ++k)
           mma_ts(tmem + C::T_DK, tmem + C::T_DP + 64 * b + k * 8, sdesc_sw128(qa + k * 2048, kQChunk, 1024), idDK,
                  (s > 0 || k > 0) ? 1u : 0u);
-        // dQ^T over the dP^T buffer b (its dS^T was read by the dK MMAs above)
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_ss(tmem + C::T_DP + 64 * b, sdesc_sw128(sK + k * 2048, lboK, 1024),
-                 sdesc_sw128(sDS + b * kKVChunk + k * 2048, kKVChunk, 1024), idDQ, k > 0);
-        mma_commit(&mma_done[b]);
         mma_commit(&q_empty[qb]);
-        // next scores of this buffer (P^T was read by dV above)
-        if (s + 2 < nsteps) ok = issue_s(s + 2);
+        // next scores of this buffer pair (P^T / dS^T were read by the MMAs above)
+        if (s + 2 < nsteps) {
+          ok = issue_s(s + 2);
+          if (ok) issue_dp(s + 2);
+        }
       }
+      if (ok) mma_commit(all_done);
       if (!ok) {
         mma_commit(drain);
         mbar_wait(drain, 0, nullptr);
@@ -259,8 +259,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tDP = tmem + lane_off + C::T_DP + 64 * wg;
     const int jl = j0 + r;
     const bool has_gate = p.gT != nullptr;
-    const bool want_row = p.dg_row != nullptr;
-    uint8_t* sDS = smem + C::OFF_DS + wg * kKVChunk;
     float dgcol = 0.f;
     int cur_h = -1;
     float rowterm = 0.f;
@@ -285,28 +283,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = wait_bar(&s_full[wg], (s >> 1) & 1, ab);
       if (!ok) break;
       tc_fence_after();
+      // visible query columns of this key row: causal i >= j, window i - j < W, i < len
+      const int cmin = jl - i0;
+      const int cmax = min(p.window > 0 ? jl + p.window - 1 - i0 : (1 << 30), len - 1 - i0);
       float pr[64];
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         uint32_t sv[32];
         tmem_ld32(tS + 32 * ch, sv);
         tmem_ld_wait();
-#pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
-          const float4 ct = vec4[8 * ch + c4];
-          const float cts[4] = {ct.x, ct.y, ct.z, ct.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int c = 4 * c4 + e, col = 32 * ch + c;
-            float t = fmaf(__uint_as_float(sv[c]), p.scale_log2, cts[e]) + rowterm;
-            if (need_mask) {
-              const int i = i0 + col;
-              const bool vis = (i < len) && (jl <= i) && (p.window == 0 || i - jl < p.window);
-              t = vis ? t : neg_inf();
-            }
-            pr[col] = ex2(t);
-          }
-        }
+        if (need_mask)
+          p_chunk<true>(pr + 32 * ch, sv, vec4 + 8 * ch, rowterm, p.scale_log2, 32 * ch, cmin, cmax);
+        else
+          p_chunk<false>(pr + 32 * ch, sv, vec4 + 8 * ch, rowterm, p.scale_log2, 32 * ch, cmin, cmax);
         uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(pr[32 * ch + 2 * c], pr[32 * ch + 2 * c + 1]);
@@ -316,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&pv_ready[wg]);
-      // ---- dS = P (dP - delta_i) in fp32, dS^T (bf16) over dP^T and into shared memory
+      // ---- dS = P (dP - delta_i) in fp32, dS^T (bf16) over dP^T
       ok = wait_bar(&dp_full[wg], (s >> 1) & 1, ab);
       if (!ok) break;
       tc_fence_after();
@@ -339,63 +328,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(pr[32 * ch + 2 * c], pr[32 * ch + 2 * c + 1]);
         tmem_st16(tDP + 16 * ch, pk);
-        // dS^T row r, query columns 32ch .. 32ch+31 = 16-B pieces 4ch .. 4ch+3 of the swizzled row
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          *reinterpret_cast<uint4*>(sDS + sw128_offset(r, 4 * ch + q)) =
-              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
       }
       tmem_st_wait();
-      fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ds_ready[wg]);
-      // ---- fp32 sums of dS: over this row's query columns (column sum for key j) and over
-      // the warp's 32 key rows for each query column (transpose-reduce; lane l ends with
-      // column 32ch + l)
+      // fp32 column sum of dS for this key row (gate gradient)
       if (has_gate) {
         float acc = 0.f;
 #pragma unroll
         for (int c = 0; c < 64; ++c) acc += pr[c];
         dgcol += acc;
-      }
-      if (want_row) {
-        // in place on pr (the column sum above was its last other use)
-#pragma unroll
-        for (int ch = 0; ch < 2; ++ch) {
-          float* v = pr + 32 * ch;
-#pragma unroll
-          for (int half = 16; half >= 1; half >>= 1) {
-            const bool upper = (lane & half) != 0;
-#pragma unroll
-            for (int c = 0; c < half; ++c) {
-              const float send = upper ? v[c] : v[c + half];
-              const float keep = upper ? v[c + half] : v[c];
-              v[c] = keep + __shfl_xor_sync(0xffffffffu, send, half);
-            }
-          }
-          const int i = i0 + 32 * ch + lane;
-          if (i < len) red_add_f32(p.dg_row + (size_t)h * p.total + seq_start + i, v[0]);
-        }
-      }
-      // ---- dQ^T of this step: TMEM (dP^T buffer) -> registers -> fp32 reduce-adds into dQ
-      ok = wait_bar(&mma_done[wg], (s >> 1) & 1, ab);
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t dq[64];
-      tmem_ld32(tDP, dq);
-      tmem_ld32(tDP + 32, dq + 32);
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&dq_free[wg]);
-      if (r < DQK) {
-        const int nrows = min(kBM, len - i0);
-        float* base = p.dq_acc + ((size_t)(seq_start + i0) * p.hq + h) * DQK + r;
-        const size_t row_stride = (size_t)p.hq * DQK;
-#pragma unroll
-        for (int c = 0; c < kBM; ++c)
-          if (c < nrows) red_add_f32(base + c * row_stride, __uint_as_float(dq[c]) * p.scale);
       }
     }
     if (ok && cur_h >= 0 && has_gate && jl < len)
@@ -403,9 +346,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- epilogue (warpgroup 0): dV and scale * dK for this key row.  TMEM loads are
     // warp-collective; only the stores depend on the row being inside the sequence.
     if (ok && wg == 0 && nsteps > 0) {
-      // every MMA has retired once the last step's mma_done completed
-      const int last = nsteps - 1;
-      ok = wait_bar(&mma_done[last & 1], (last >> 1) & 1, ab);
+      // a single-use barrier: the per-buffer mma_done barriers may be more than one phase
+      // ahead of this warpgroup, where a parity wait could alias
+      ok = wait_bar(all_done, 0, ab);
       if (ok) {
         tc_fence_after();
         const bool row_ok = jl < len;

@@ -228,6 +228,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m = p.sink ? __ldg(p.sink + h) * kLog2e : neg_inf();
     float l = p.sink ? 1.f : 0.f;
     bool ok = true;
+    if (!has_gate) {
+      // no gate: the G_j buffers stay zero
+      for (int u = lane; u < 2 * kBN; u += 32) sG[quarter * 2 * kBN + u] = 0.f;
+      __syncwarp();
+    }
     for (int n = 0; n < nt; ++n) {
       const int jt = hi_t - n;
       const int j0 = jt * kBN;
@@ -251,23 +256,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(tmem + lane_off + b * 128 + 96, sv + 96);
       tmem_ld_wait();
       const bool need_mask = (jt == hi_t) || (p.window > 0 && j0 < q0 + kBM - p.window);
+      // visible key columns of this row within the tile: causal j <= i, window i - j < W
+      const int jmax = il - j0;
+      const int jmin = p.window > 0 ? il - p.window + 1 - j0 : -(1 << 30);
       float mx = neg_inf();
       if (need_mask) {
 #pragma unroll
         for (int j = 0; j < 128; ++j) {
-          float t = fmaf(__uint_as_float(sv[j]), p.scale_log2, gi);
-          if (has_gate) t += gj[j];
-          const int jl = j0 + j;
-          const bool vis = (jl <= il) && (p.window == 0 || il - jl < p.window);
-          t = vis ? t : neg_inf();
+          float t = fmaf(__uint_as_float(sv[j]), p.scale_log2, gi) + gj[j];
+          t = (j >= jmin && j <= jmax) ? t : neg_inf();
           sv[j] = __float_as_uint(t);
           mx = fmaxf(mx, t);
         }
       } else {
 #pragma unroll
         for (int j = 0; j < 128; ++j) {
-          float t = fmaf(__uint_as_float(sv[j]), p.scale_log2, gi);
-          if (has_gate) t += gj[j];
+          const float t = fmaf(__uint_as_float(sv[j]), p.scale_log2, gi) + gj[j];
           sv[j] = __float_as_uint(t);
           mx = fmaxf(mx, t);
         }

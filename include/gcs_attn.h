@@ -180,9 +180,10 @@ int gcs_get_device_status(int* status, int clear);
 /* ------------------------------------------------------------------ instrumentation
  * Arms two caller-created CUDA events (cudaEvent_t, passed as void*) for the next attn_fwd,
  * attn_bwd or attn_decode_paged call made by this host thread: `before` is recorded on the
- * call's stream immediately before its main attention kernel (prefill forward kernel,
- * fused backward kernel, or split-K decode kernel) and `after` immediately after it, so
- * cudaEventElapsedTime(before, after) is that kernel's device time.  The events are
+ * call's stream immediately before its main attention kernels (the prefill forward
+ * kernel; the backward's attention kernels -- dQ pass + dK/dV pass, or the wide-head role
+ * kernels; the split-K decode kernel) and `after` immediately after them, so
+ * cudaEventElapsedTime(before, after) is their device time.  The events are
  * disarmed once used; passing NULL, NULL disarms them.  Returns GCS_OK. */
 int gcs_set_kernel_events(void* before, void* after);
 

@@ -86,9 +86,12 @@ def test_workspace_sizes_on_host(L):
     assert L.attn_fwd_workspace(b(prefill())) == 0
     assert L.attn_fwd_workspace(b(prefill(log_gate=FAKE))) == 4 * 4 * 256
     ws = L.attn_bwd_workspace(b(prefill(log_gate=FAKE, sink=FAKE)))
-    # G^T, delta, dQ accumulator, dS row sums, dS column sums, packed per-tile vectors
+    # head dims <= 128 (two-pass backward): G^T, delta, dS row sums, dS column sums,
+    # packed per-tile vectors; wider heads add the fp32 dQ accumulator
     n_qtiles = 256 // 64 + 1
-    assert ws == 4 * (4 * 256) * 4 + 4 * 256 * 4 * 128 + 4 * n_qtiles * 128 * 4
+    assert ws == 4 * (4 * 256) * 4 + 4 * n_qtiles * 128 * 4
+    ws_wide = L.attn_bwd_workspace(b(prefill(log_gate=FAKE, sink=FAKE, dqk=256, dv=512)))
+    assert ws_wide == 4 * (4 * 256) * 4 + 256 * 4 * 256 * 4 + 4 * n_qtiles * 128 * 4
     units, rows = 2 * 2 * 4, 16
     assert L.attn_decode_workspace(b(decode())) == units * rows * 128 * 4 + units * rows * 2 * 4
     assert L.attn_decode_workspace(b(decode(max_q_len=5))) == 0
