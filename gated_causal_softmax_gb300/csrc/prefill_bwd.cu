@@ -335,10 +335,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&ds_ready[wg]);
       // fp32 column sum of dS for this key row (gate gradient)
       if (has_gate) {
-        float acc = 0.f;
+        float acc[8];
 #pragma unroll
-        for (int c = 0; c < 64; ++c) acc += pr[c];
-        dgcol += acc;
+        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) acc[c & 7] += pr[c];
+        dgcol += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
       }
     }
     if (ok && cur_h >= 0 && has_gate && jl < len)

@@ -49,16 +49,16 @@ struct DqCfg {
 template <bool MASK>
 __device__ __forceinline__ float dq_chunk(uint32_t* sv, const uint32_t* dp, const float* gj, int jb, float rowterm,
                                           float scale_log2, float dl, int jmin, int jmax) {
-  float acc = 0.f;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial sums (latency)
 #pragma unroll
   for (int c = 0; c < 32; ++c) {
     float t = fmaf(__uint_as_float(sv[c]), scale_log2, rowterm) + gj[jb + c];
     if (MASK) t = (jb + c >= jmin && jb + c <= jmax) ? t : neg_inf();
     const float ds = ex2(t) * (__uint_as_float(dp[c]) - dl);
-    acc += ds;
+    acc[c & 3] += ds;
     sv[c] = __float_as_uint(ds);
   }
-  return acc;
+  return (acc[0] + acc[1]) + (acc[2] + acc[3]);
 }
 
 template <int D>

@@ -259,23 +259,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       // visible key columns of this row within the tile: causal j <= i, window i - j < W
       const int jmax = il - j0;
       const int jmin = p.window > 0 ? il - p.window + 1 - j0 : -(1 << 30);
-      float mx = neg_inf();
+      // row max with 8 independent partial maxima (a single 128-long chain is latency-bound)
+      float mxp[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) mxp[e] = neg_inf();
       if (need_mask) {
 #pragma unroll
         for (int j = 0; j < 128; ++j) {
           float t = fmaf(__uint_as_float(sv[j]), p.scale_log2, gi) + gj[j];
           t = (j >= jmin && j <= jmax) ? t : neg_inf();
           sv[j] = __float_as_uint(t);
-          mx = fmaxf(mx, t);
+          mxp[j & 7] = fmaxf(mxp[j & 7], t);
         }
       } else {
 #pragma unroll
         for (int j = 0; j < 128; ++j) {
           const float t = fmaf(__uint_as_float(sv[j]), p.scale_log2, gi) + gj[j];
           sv[j] = __float_as_uint(t);
-          mx = fmaxf(mx, t);
+          mxp[j & 7] = fmaxf(mxp[j & 7], t);
         }
       }
+      const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                             fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
       const float m_new = fmaxf(m, mx);
       const bool need = m_new > m + kRescale;
       if (__any_sync(0xffffffffu, need)) {
@@ -299,7 +304,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (need) m = m_new;
       }
       const float mu = (m == neg_inf()) ? 0.f : m;
-      float lsum = 0.f;
+      float lsp[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) lsp[e] = 0.f;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t pk[32];
@@ -307,12 +314,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int jj = 0; jj < 32; ++jj) {
           const float p0 = ex2(__uint_as_float(sv[half * 64 + 2 * jj]) - mu);
           const float p1 = ex2(__uint_as_float(sv[half * 64 + 2 * jj + 1]) - mu);
-          lsum += p0 + p1;
+          lsp[jj & 7] += p0 + p1;
           pk[jj] = pack_bf16x2(p0, p1);
         }
         tmem_st32(tmem + lane_off + b * 128 + half * 32, pk);
       }
-      l += lsum;
+      l += ((lsp[0] + lsp[1]) + (lsp[2] + lsp[3])) + ((lsp[4] + lsp[5]) + (lsp[6] + lsp[7]));
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
