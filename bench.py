@@ -37,6 +37,14 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # (gate cumsum, delta, vector pack, dQ pass, dK/dV pass, d gate scan, d sink reduce)
 LAUNCHES_PER_PREFILL_STEP = 9
 LAUNCHES_PER_DECODE = 2
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the ncu captures
+# summarised in profiles/ (prefill_kernels_varlen_gqa_8192_d128.md,
+# decode_kernels_paged_fp8_decode_64x1.md); set back to None whenever the kernel changes.
+NCU_TRAFFIC = {
+    "bwd": 218.3e6 + 273.2e6,  # prefill_bwd_dq_kernel<128> + prefill_bwd_kernel<128,128>
+    "fwd": 120.3e6,            # prefill_fwd_kernel<128,128>
+    "decode_split": 1188.2e6,  # decode_split_kernel
+}
 
 
 def peaks():
@@ -219,8 +227,9 @@ def run_native(args):
            else "prefill_fwd_kernel<128,128>")
     dom_fl, dom_ms = (bwd_fl, bwd_k) if bwd_k >= fwd_k else (fwd_fl, fwd_k)
     achieved = dom_fl / (dom_ms * 1e-3) / 1e12
+    traffic = args.traffic if args.traffic is not None else NCU_TRAFFIC["bwd" if bwd_k >= fwd_k else "fwd"]
     roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": sustained,
-                "unit": "TFLOP/s", "frac": round(achieved / sustained, 4), "traffic": args.traffic,
+                "unit": "TFLOP/s", "frac": round(achieved / sustained, 4), "traffic": traffic,
                 "peak_source": f"{pk_kind} bf16_tflops_sustained", "algorithmic_flops_per_launch": dom_fl,
                 "fwd_kernel_ms": round(fwd_k, 4), "bwd_kernel_ms": round(bwd_k, 4),
                 "fwd_kernel_tflops": round(fwd_fl / (fwd_k * 1e-3) / 1e12, 1),
@@ -302,7 +311,9 @@ def run_native(args):
               "bytes_per_call": dbytes, "launches_per_call": LAUNCHES_PER_DECODE,
               "roofline": {"bound": "hbm", "kernel": "decode_split_kernel", "achieved": round(split_gbs, 1),
                            "peak": hbm, "unit": "GB/s", "frac": round(split_gbs / hbm, 4),
-                           "traffic": args.decode_traffic, "peak_source": f"{pk_kind} hbm_gbs",
+                           "traffic": (args.decode_traffic if args.decode_traffic is not None
+                                       else NCU_TRAFFIC["decode_split"]),
+                           "peak_source": f"{pk_kind} hbm_gbs",
                            "kernel_ms": round(split_ms, 4)}}
     if gcs.get_device_status() != 0:
         raise RuntimeError("a decode kernel timed out")
