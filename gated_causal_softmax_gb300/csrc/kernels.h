@@ -30,6 +30,8 @@ struct FwdMaps {
 };
 
 cudaError_t launch_prefill_fwd(const FwdParams& p, const FwdMaps& maps, int num_tiles, cudaStream_t s);
+// Head dims 64 / 128: two 128-row query tiles per CTA (num_pairs = 256-row query tiles).
+cudaError_t launch_prefill_fwd2(const FwdParams& p, const FwdMaps& maps, int num_pairs, cudaStream_t s);
 
 struct BwdParams {
   const int32_t* cu_seqlens;

@@ -1,0 +1,394 @@
+// Prefill forward for head dims <= 128: two 128-row query tiles per CTA (fla-org/
+// flash-linear-attention #1322 "Gluon attention backend with large head dimensions",
+// Description: causal attention with log gates, sliding windows and a sink bias).
+//
+// Same arithmetic as prefill_fwd.cu; the difference is the schedule.  One CTA takes 256
+// query rows of one head as tiles A (rows q0..q0+127) and B (q0+128..q0+255).  Each tile has
+// its own TMEM score buffer and accumulator (S_A, S_B, O_A, O_B: 4 x 128 columns) and its
+// own softmax warpgroup, and the MMA issuer interleaves them
+//     PV_A(n), S_A(n+1), PV_B(n), S_B(n+1), ...
+// so one warpgroup's exponentials overlap the other tile's MMAs, and both tiles share every
+// K / V tile loaded into shared memory.
+//
+// Warp roles (384 threads): warp 0 TMA producer (Q_A, Q_B once; K and V chunks through a
+// ring), warp 1 tcgen05 issuer, warps 2-3 idle; warps 4-7 softmax of tile A, warps 8-11
+// softmax of tile B (one thread per row).  setmaxnreg moves registers from the first
+// warpgroup to the softmax warpgroups, which keep a 128-column score row in registers.
+#include "kernels.h"
+#include "sm103_ptx.cuh"
+#include "tiles.cuh"
+
+namespace gcs {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBN = 128;
+constexpr int kChunk = 128 * 128;
+constexpr int kThreads = 384;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescale = 8.0f;
+
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
+
+template <int D>
+struct Fwd2Cfg {
+  static constexpr int CH = D / 64;
+  static constexpr int NST = 8;
+  static constexpr int OFF_Q = 0;                           // [2 tiles][CH] chunks
+  static constexpr int OFF_RING = 2 * CH * kChunk;
+  static constexpr int OFF_G = OFF_RING + NST * kChunk;     // [2 tiles][4 warps][2][128] floats
+  static constexpr int OFF_BAR = OFF_G + 2 * 4 * 2 * kBN * 4;
+  static constexpr int OFF_MISC = OFF_BAR + (2 * NST + 16) * 8;
+  static constexpr int SMEM = OFF_MISC + 16 + 1024;
+  static_assert(SMEM <= 227 * 1024, "shared memory budget");
+};
+
+// Register split (per thread): warpgroup 0 (producer, MMA, 2 idle warps) 72, the two softmax
+// warpgroups 216 each: 128 x 72 + 256 x 216 = 64512 = 384 threads x 168 at launch.
+__device__ __forceinline__ void reg_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 72;\n" ::: "memory"); }
+__device__ __forceinline__ void reg_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 216;\n" ::: "memory"); }
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  using C = Fwd2Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  // heaviest 256-row query pairs first
+  TileRef tr;
+  if (!lpt_tile(p.cu_seqlens, p.num_seqs, 2 * kBM, blockIdx.y, tr)) return;
+  const int seq_start = tr.start, len = tr.len;
+  const int h = blockIdx.x;
+  const int kvh = h / (p.hq / p.hkv);
+  const int q0 = tr.u * 2 * kBM;
+  const int qt[2] = {q0 / kBM, q0 / kBM + 1};
+  const bool valid_b = q0 + kBM < len;
+  int lo[2];
+  for (int x = 0; x < 2; ++x) {
+    const int lo_j = qt[x] * kBM - p.window + 1;
+    lo[x] = (p.window > 0 && lo_j > 0) ? lo_j / kBN : 0;
+  }
+  const int hi_t = valid_b ? qt[1] : qt[0];
+  const int lo_t = lo[0];
+  const int nt = hi_t - lo_t + 1;
+  // tile x takes part in key tile n (jt = hi_t - n) when jt lies in [lo[x], qt[x]]
+  auto part = [&](int x, int n) -> bool {
+    const int jt = hi_t - n;
+    return (x == 0 || valid_b) && jt <= qt[x] && jt >= lo[x];
+  };
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* full = bars;              // [NST]
+  uint64_t* empty = bars + C::NST;    // [NST]
+  uint64_t* q_full = bars + 2 * C::NST;
+  uint64_t* s_full = q_full + 1;      // [2 tiles]
+  uint64_t* p_full = q_full + 3;      // [2 tiles]
+  uint64_t* pv_done = q_full + 5;     // [2 tiles]
+  uint64_t* drain = q_full + 7;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  const Abort ab{abort_flag, p.status};
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::NST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(q_full, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&s_full[x], 1);
+      mbar_init(&p_full[x], 4);
+      mbar_init(&pv_done[x], 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp < 4) {
+    reg_dec();
+    if (warp == 0 && lane == 0) {
+      // ---------------------------------------------------------- TMA producer
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      const uint64_t pol_kv = l2_policy_evict_last();
+      const uint64_t pol_q = l2_policy_evict_first();
+      mbar_expect_tx(q_full, 2 * C::CH * kChunk);
+      for (int x = 0; x < 2; ++x)
+        for (int c = 0; c < C::CH; ++c)
+          tma_load_2d_hint(smem + C::OFF_Q + (x * C::CH + c) * kChunk, &tmQ, q_full, h * D + c * 64,
+                           seq_start + q0 + x * kBM, pol_q);
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int n = 0; n < nt && ok; ++n) {
+        const int y = seq_start + (hi_t - n) * kBN;
+        for (int kv = 0; kv < 2 && ok; ++kv)
+          for (int c = 0; c < C::CH && ok; ++c) {
+            ok = wait_bar(&empty[stage], phase ^ 1, ab);
+            if (!ok) break;
+            mbar_expect_tx(&full[stage], kChunk);
+            tma_load_2d_hint(smem + C::OFF_RING + stage * kChunk, kv ? &tmV : &tmK, &full[stage], kvh * D + c * 64,
+                             y, pol_kv);
+            if (++stage == C::NST) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+      }
+    } else if (warp == 1 && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      const uint32_t idS = idesc_bf16(128, kBN, false, false);
+      const uint32_t idPV = idesc_bf16(128, 64, false, true);
+      const uint32_t sQ = smem_u32(smem + C::OFF_Q), sRing = smem_u32(smem + C::OFF_RING);
+      uint32_t stage = 0, phase = 0;
+      // ring chunks of key tile n: K at positions kpos..kpos+CH-1, V after them
+      auto take = [&](uint32_t& pos_out) -> bool {  // wait for the next CH chunks
+        pos_out = stage;
+        for (int c = 0; c < C::CH; ++c) {
+          if (!wait_bar(&full[stage], phase, ab)) return false;
+          if (++stage == C::NST) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        tc_fence_after();
+        return true;
+      };
+      auto release = [&](uint32_t pos) {
+        for (int c = 0; c < C::CH; ++c) mma_commit(&empty[(pos + c) % C::NST]);
+      };
+      auto issue_s = [&](int x, uint32_t kpos) {
+        for (int c = 0; c < C::CH; ++c)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ss(tmem + 128 * x, sdesc_sw128(sQ + (x * C::CH + c) * kChunk + k * 32, 16, 1024),
+                   sdesc_sw128(sRing + ((kpos + c) % C::NST) * kChunk + k * 32, 16, 1024), idS, (c | k) != 0);
+        mma_commit(&s_full[x]);
+      };
+      int kp[2] = {0, 0};  // PV issued per tile (accumulate flag and p_full parity)
+      bool ok = wait_bar(q_full, 0, ab);
+      uint32_t kpos = 0, vpos = 0;
+      if (ok) ok = take(kpos);
+      if (ok) {
+        for (int x = 0; x < 2; ++x)
+          if (part(x, 0)) issue_s(x, kpos);
+        release(kpos);
+      }
+      for (int n = 0; n < nt && ok; ++n) {
+        ok = take(vpos);
+        if (!ok) break;
+        uint32_t knext = 0;
+        if (n + 1 < nt) {
+          ok = take(knext);
+          if (!ok) break;
+        }
+        for (int x = 0; x < 2 && ok; ++x) {
+          if (part(x, n)) {
+            ok = wait_bar(&p_full[x], kp[x] & 1, ab);
+            if (!ok) break;
+            tc_fence_after();
+            for (int c = 0; c < C::CH; ++c)
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                mma_ts(tmem + 256 + 128 * x + c * 64, tmem + 128 * x + k * 8,
+                       sdesc_sw128(sRing + ((vpos + c) % C::NST) * kChunk + k * 2048, kChunk, 1024), idPV,
+                       (kp[x] > 0 || k > 0) ? 1u : 0u);
+            mma_commit(&pv_done[x]);
+            ++kp[x];
+          }
+          // next scores of this tile over its buffer (P was read by the PV above)
+          if (n + 1 < nt && part(x, n + 1)) issue_s(x, knext);
+        }
+        if (!ok) break;
+        release(vpos);
+        if (n + 1 < nt) release(knext);
+      }
+      if (!ok) {
+        mma_commit(drain);
+        mbar_wait(drain, 0, nullptr);
+      }
+    }
+    __syncwarp();
+  } else {
+    reg_inc();
+    // ------------------------------------------------------------ softmax, tile x
+    const int x = (warp - 4) >> 2;
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_off + 128 * x, tO = tmem + lane_off + 256 + 128 * x;
+    const int xq0 = q0 + x * kBM;
+    const int il = xq0 + r;
+    const bool row_valid = il < len;
+    const int tok = seq_start + (row_valid ? il : len - 1);
+    const bool has_gate = p.gT != nullptr;
+    const float gi = has_gate ? __ldg(p.gT + (size_t)h * p.total + tok) : 0.f;
+    float m = p.sink ? __ldg(p.sink + h) * kLog2e : neg_inf();
+    float l = p.sink ? 1.f : 0.f;
+    float* sG = reinterpret_cast<float*>(smem + C::OFF_G) + (x * 4 + quarter) * 2 * kBN;
+    if (!has_gate) {
+      for (int u = lane; u < 2 * kBN; u += 32) sG[u] = 0.f;
+      __syncwarp();
+    }
+    bool ok = true;
+    int kx = 0;  // key tiles processed by this tile
+    for (int n = 0; n < nt; ++n) {
+      if (!part(x, n)) continue;
+      const int jt = hi_t - n, j0 = jt * kBN;
+      float* gj = sG + (kx & 1) * kBN;  // this warp's copy of -G_j for the key tile
+      if (has_gate) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int jl = j0 + lane * 4 + u;
+          gj[lane * 4 + u] = (jl < len) ? -__ldg(p.gT + (size_t)h * p.total + seq_start + jl) : 0.f;
+        }
+        __syncwarp();
+      }
+      ok = wait_bar(&s_full[x], kx & 1, ab);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sv[128];
+      tmem_ld32(tS + 0, sv);
+      tmem_ld32(tS + 32, sv + 32);
+      tmem_ld32(tS + 64, sv + 64);
+      tmem_ld32(tS + 96, sv + 96);
+      tmem_ld_wait();
+      const bool need_mask = (jt == qt[x]) || (p.window > 0 && j0 < xq0 + kBM - p.window);
+      const int jmax = il - j0;
+      const int jmin = p.window > 0 ? il - p.window + 1 - j0 : -(1 << 30);
+      float mxp[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) mxp[e] = neg_inf();
+      if (need_mask) {
+#pragma unroll
+        for (int j = 0; j < 128; ++j) {
+          float t = fmaf(__uint_as_float(sv[j]), p.scale_log2, gi) + gj[j];
+          t = (j >= jmin && j <= jmax) ? t : neg_inf();
+          sv[j] = __float_as_uint(t);
+          mxp[j & 7] = fmaxf(mxp[j & 7], t);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 128; ++j) {
+          const float t = fmaf(__uint_as_float(sv[j]), p.scale_log2, gi) + gj[j];
+          sv[j] = __float_as_uint(t);
+          mxp[j & 7] = fmaxf(mxp[j & 7], t);
+        }
+      }
+      const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                             fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
+      const float m_new = fmaxf(m, mx);
+      const bool need = m_new > m + kRescale;
+      if (__any_sync(0xffffffffu, need)) {
+        const float alpha = need ? ex2(m - m_new) : 1.f;
+        if (kx > 0) {
+          // O holds the previous key tiles: wait for their PV before scaling it
+          ok = wait_bar(&pv_done[x], (kx - 1) & 1, ab);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(tO + c * 32, ov);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
+            tmem_st32(tO + c * 32, ov);
+          }
+          tmem_st_wait();
+        }
+        l *= alpha;
+        if (need) m = m_new;
+      }
+      const float mu = (m == neg_inf()) ? 0.f : m;
+      float lsp[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) lsp[e] = 0.f;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          const float p0 = ex2(__uint_as_float(sv[half * 64 + 2 * jj]) - mu);
+          const float p1 = ex2(__uint_as_float(sv[half * 64 + 2 * jj + 1]) - mu);
+          lsp[jj & 7] += p0 + p1;
+          pk[jj] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(tS + half * 32, pk);
+      }
+      l += ((lsp[0] + lsp[1]) + (lsp[2] + lsp[3])) + ((lsp[4] + lsp[5]) + (lsp[6] + lsp[7]));
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[x]);
+      ++kx;
+    }
+    if (ok && kx > 0) ok = wait_bar(&pv_done[x], (kx - 1) & 1, ab);
+    if (ok && kx > 0) {
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      uint16_t* orow = p.o + ((size_t)(seq_start + (row_valid ? il : 0)) * p.hq + h) * p.dv;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t ov[32];
+        tmem_ld32(tO + c * 32, ov);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          pk[j] = pack_bf16x2(__uint_as_float(ov[2 * j]) * inv_l, __uint_as_float(ov[2 * j + 1]) * inv_l);
+        if (row_valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+        }
+      }
+      if (row_valid) p.lse[(size_t)h * p.total + seq_start + il] = (m + log2f(l)) * kLn2;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    const unsigned long long t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 1000000ull) {
+    }
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch_t(const FwdParams& p, const FwdMaps& maps, int num_pairs, cudaStream_t s) {
+  using C = Fwd2Cfg<D>;
+  auto kern = prefill_fwd2_kernel<D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  kern<<<dim3(p.hq, num_pairs), kThreads, C::SMEM, s>>>(maps.q, maps.k, maps.v, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_fwd2(const FwdParams& p, const FwdMaps& maps, int num_pairs, cudaStream_t s) {
+  if (p.dqk == 64 && p.dv == 64) return launch_t<64>(p, maps, num_pairs, s);
+  if (p.dqk == 128 && p.dv == 128) return launch_t<128>(p, maps, num_pairs, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace gcs
