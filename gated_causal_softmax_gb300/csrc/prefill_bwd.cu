@@ -187,30 +187,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idS = idesc_bf16(128, kBM, false, false);   // S^T, dP^T
       const uint32_t idDV = idesc_bf16(128, DV, false, true);    // dV += P^T dO
       const uint32_t idDK = idesc_bf16(128, DQK, false, true);   // dK += dS^T Q
-      const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
-      const uint32_t sQ = smem_u32(smem + C::OFF_Q), sDO = smem_u32(smem + C::OFF_DO);
+      // descriptors built once; offsets are added to the address field (shared-memory
+      // addresses stay below 2^18, so the 14-bit field never carries)
+      const uint64_t dK0 = sdesc_sw128(smem_u32(smem + C::OFF_K), 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(smem_u32(smem + C::OFF_V), 16, 1024);
+      const uint64_t dQ0 = sdesc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024);
+      const uint64_t dDO0 = sdesc_sw128(smem_u32(smem + C::OFF_DO), 16, 1024);
+      const uint64_t dQmn0 = sdesc_sw128(smem_u32(smem + C::OFF_Q), kQChunk, 1024);
+      const uint64_t dDOmn0 = sdesc_sw128(smem_u32(smem + C::OFF_DO), kQChunk, 1024);
+      constexpr uint32_t kKV16 = kKVChunk >> 4, kQ16 = kQChunk >> 4;
       bool ok = wait_bar(kv_full, 0, ab);
       auto issue_s = [&](int t) -> bool {  // S^T(t) = K Q(t)^T -> S^T[t & 1]
         const int qb = t % kNQB, b = t & 1;
         if (!wait_bar(&q_full[qb], (t / kNQB) & 1, ab)) return false;
         tc_fence_after();
-        const uint32_t qa = sQ + qb * C::KCH * kQChunk;
-        for (int c = 0; c < C::KCH; ++c)
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + C::T_S + 64 * b, sdesc_sw128(sK + c * kKVChunk + k * 32, 16, 1024),
-                   sdesc_sw128(qa + c * kQChunk + k * 32, 16, 1024), idS, (c | k) != 0);
+        for (int c = 0; c < C::KCH; ++c) {
+          const uint64_t a = dK0 + c * kKV16, bq = dQ0 + (qb * C::KCH + c) * kQ16;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) mma_ss(tmem + C::T_S + 64 * b, a + 2 * k, bq + 2 * k, idS, (c | k) != 0);
+        }
         mma_commit(&s_full[b]);
         return true;
       };
       auto issue_dp = [&](int t) {  // dP^T(t) = V dO(t)^T -> dP^T[t & 1] (Q/dO(t) already landed)
         const int qb = t % kNQB, b = t & 1;
-        const uint32_t da = sDO + qb * C::VCH * kQChunk;
-        for (int c = 0; c < C::VCH; ++c)
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + C::T_DP + 64 * b, sdesc_sw128(sV + c * kKVChunk + k * 32, 16, 1024),
-                   sdesc_sw128(da + c * kQChunk + k * 32, 16, 1024), idS, (c | k) != 0);
+        for (int c = 0; c < C::VCH; ++c) {
+          const uint64_t a = dV0 + c * kKV16, bd = dDO0 + (qb * C::VCH + c) * kQ16;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) mma_ss(tmem + C::T_DP + 64 * b, a + 2 * k, bd + 2 * k, idS, (c | k) != 0);
+        }
         mma_commit(&dp_full[b]);
       };
       for (int t = 0; t < 2 && t < nsteps && ok; ++t) {
@@ -219,22 +226,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int s = 0; s < nsteps && ok; ++s) {
         const int b = s & 1, qb = s % kNQB;
-        const uint32_t qa = sQ + qb * C::KCH * kQChunk, da = sDO + qb * C::VCH * kQChunk;
+        const uint64_t qa = dQmn0 + qb * C::KCH * kQ16, da = dDOmn0 + qb * C::VCH * kQ16;
         ok = wait_bar(&pv_ready[b], (s >> 1) & 1, ab);
         if (!ok) break;
         tc_fence_after();
         // K dimension = 64 query rows = 4 steps of 16 rows (2048 B in the MN-major views)
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_ts(tmem + C::T_DV, tmem + C::T_S + 64 * b + k * 8, sdesc_sw128(da + k * 2048, kQChunk, 1024), idDV,
-                 (s > 0 || k > 0) ? 1u : 0u);
+          mma_ts(tmem + C::T_DV, tmem + C::T_S + 64 * b + k * 8, da + 128 * k, idDV, (s > 0 || k > 0) ? 1u : 0u);
         ok = wait_bar(&ds_ready[b], (s >> 1) & 1, ab);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          mma_ts(tmem + C::T_DK, tmem + C::T_DP + 64 * b + k * 8, sdesc_sw128(qa + k * 2048, kQChunk, 1024), idDK,
-                 (s > 0 || k > 0) ? 1u : 0u);
+          mma_ts(tmem + C::T_DK, tmem + C::T_DP + 64 * b + k * 8, qa + 128 * k, idDK, (s > 0 || k > 0) ? 1u : 0u);
         mma_commit(&q_empty[qb]);
         // next scores of this buffer pair (P^T / dS^T were read by the MMAs above)
         if (s + 2 < nsteps) {

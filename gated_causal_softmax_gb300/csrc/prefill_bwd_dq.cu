@@ -164,18 +164,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t idSS = idesc_bf16(128, kBN, false, false);  // S, dP
       const uint32_t idDQ = idesc_bf16(128, D, false, true);     // dQ += dS K (K as MN-major B)
-      const uint32_t sQ = smem_u32(smem + C::OFF_Q), sDO = smem_u32(smem + C::OFF_DO);
-      const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
+      // descriptors built once; offsets are added to the address field (shared-memory
+      // addresses stay below 2^18, so the 14-bit field never carries)
+      const uint64_t dQ0 = sdesc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024);
+      const uint64_t dDO0 = sdesc_sw128(smem_u32(smem + C::OFF_DO), 16, 1024);
+      const uint64_t dK0 = sdesc_sw128(smem_u32(smem + C::OFF_K), 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(smem_u32(smem + C::OFF_V), 16, 1024);
+      const uint64_t dKmn0 = sdesc_sw128(smem_u32(smem + C::OFF_K), kChunk, 1024);
+      constexpr uint32_t kChunk16 = kChunk >> 4, kTile16 = C::TILE >> 4;
       bool ok = wait_bar(qd_full, 0, ab);
       auto issue_s = [&](int n) -> bool {
         const int kb = n & 1;
         if (!wait_bar(&k_full[kb], (n >> 1) & 1, ab)) return false;
         tc_fence_after();
-        for (int c = 0; c < C::CH; ++c)
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + C::T_S + 128 * (n & 1), sdesc_sw128(sQ + c * kChunk + k * 32, 16, 1024),
-                   sdesc_sw128(sK + kb * C::TILE + c * kChunk + k * 32, 16, 1024), idSS, (c | k) != 0);
+        for (int c = 0; c < C::CH; ++c) {
+          const uint64_t a = dQ0 + c * kChunk16, b = dK0 + kb * kTile16 + c * kChunk16;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) mma_ss(tmem + C::T_S + 128 * (n & 1), a + 2 * k, b + 2 * k, idSS, (c | k) != 0);
+        }
         mma_commit(&s_full[n & 1]);
         return true;
       };
@@ -183,11 +190,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kb = n & 1;
         if (!wait_bar(&v_full[kb], (n >> 1) & 1, ab)) return false;
         tc_fence_after();
-        for (int c = 0; c < C::CH; ++c)
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + C::T_DP, sdesc_sw128(sDO + c * kChunk + k * 32, 16, 1024),
-                   sdesc_sw128(sV + kb * C::TILE + c * kChunk + k * 32, 16, 1024), idSS, (c | k) != 0);
+        for (int c = 0; c < C::CH; ++c) {
+          const uint64_t a = dDO0 + c * kChunk16, b = dV0 + kb * kTile16 + c * kChunk16;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) mma_ss(tmem + C::T_DP, a + 2 * k, b + 2 * k, idSS, (c | k) != 0);
+        }
         mma_commit(dp_full);
         mma_commit(&v_empty[kb]);
         return true;
@@ -207,8 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          mma_ts(tmem + C::T_DQ, tmem + C::T_S + 128 * b + k * 8,
-                 sdesc_sw128(sK + kb * C::TILE + k * 2048, kChunk, 1024), idDQ, (n > 0 || k > 0) ? 1u : 0u);
+          mma_ts(tmem + C::T_DQ, tmem + C::T_S + 128 * b + k * 8, dKmn0 + kb * kTile16 + 128 * k, idDQ,
+                 (n > 0 || k > 0) ? 1u : 0u);
         mma_commit(&k_empty[kb]);
         // scores of tile n + 2 over buffer b (its dS was read by the dQ MMAs above)
         if (n + 2 < nt) ok = issue_s(n + 2);

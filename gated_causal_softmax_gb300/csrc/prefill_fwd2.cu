@@ -44,10 +44,10 @@ struct Fwd2Cfg {
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
 
-// Register split (per thread): warpgroup 0 (producer, MMA, 2 idle warps) 72, the two softmax
-// warpgroups 216 each: 128 x 72 + 256 x 216 = 64512 = 384 threads x 168 at launch.
-__device__ __forceinline__ void reg_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 72;\n" ::: "memory"); }
-__device__ __forceinline__ void reg_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 216;\n" ::: "memory"); }
+// Register split (per thread): warpgroup 0 (producer, MMA, 2 idle warps) 88, the two softmax
+// warpgroups 208 each: 128 x 88 + 256 x 208 = 64512 = 384 threads x 168 at launch.
+__device__ __forceinline__ void reg_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 88;\n" ::: "memory"); }
+__device__ __forceinline__ void reg_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 208;\n" ::: "memory"); }
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -150,9 +150,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (warp == 1 && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
+      // One MMA with N < 128 takes nearly as long as one with N = 128, so P V is issued with
+      // N = D across the D/64 value chunks of a key tile (adjacent ring stages, LBO = one
+      // chunk).  Descriptors are built once; an operand offset is added to the address field
+      // (shared-memory addresses stay below 2^18, so the 14-bit field never carries).
       const uint32_t idS = idesc_bf16(128, kBN, false, false);
-      const uint32_t idPV = idesc_bf16(128, 64, false, true);
-      const uint32_t sQ = smem_u32(smem + C::OFF_Q), sRing = smem_u32(smem + C::OFF_RING);
+      const uint32_t idPV = idesc_bf16(128, D, false, true);
+      const uint64_t dQ0 = sdesc_sw128(smem_u32(smem + C::OFF_Q), 16, 1024);
+      const uint64_t dK0 = sdesc_sw128(smem_u32(smem + C::OFF_RING), 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(smem_u32(smem + C::OFF_RING), kChunk, 1024);
+      constexpr uint32_t kChunk16 = kChunk >> 4;
+      static_assert(C::NST % C::CH == 0, "a key tile's chunks must be adjacent ring stages");
       uint32_t stage = 0, phase = 0;
       // ring chunks of key tile n: K at positions kpos..kpos+CH-1, V after them
       auto take = [&](uint32_t& pos_out) -> bool {  // wait for the next CH chunks
@@ -171,11 +179,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < C::CH; ++c) mma_commit(&empty[(pos + c) % C::NST]);
       };
       auto issue_s = [&](int x, uint32_t kpos) {
-        for (int c = 0; c < C::CH; ++c)
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + 128 * x, sdesc_sw128(sQ + (x * C::CH + c) * kChunk + k * 32, 16, 1024),
-                   sdesc_sw128(sRing + ((kpos + c) % C::NST) * kChunk + k * 32, 16, 1024), idS, (c | k) != 0);
+        for (int c = 0; c < C::CH; ++c) {
+          const uint64_t a = dQ0 + (x * C::CH + c) * kChunk16, b = dK0 + (kpos + c) * kChunk16;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) mma_ss(tmem + 128 * x, a + 2 * k, b + 2 * k, idS, (c | k) != 0);
+        }
         mma_commit(&s_full[x]);
       };
       int kp[2] = {0, 0};  // PV issued per tile (accumulate flag and p_full parity)
@@ -200,12 +209,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = wait_bar(&p_full[x], kp[x] & 1, ab);
             if (!ok) break;
             tc_fence_after();
-            for (int c = 0; c < C::CH; ++c)
+            const uint64_t b = dV0 + vpos * kChunk16;
 #pragma unroll
-              for (int k = 0; k < 8; ++k)
-                mma_ts(tmem + 256 + 128 * x + c * 64, tmem + 128 * x + k * 8,
-                       sdesc_sw128(sRing + ((vpos + c) % C::NST) * kChunk + k * 2048, kChunk, 1024), idPV,
-                       (kp[x] > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < 8; ++k)
+              mma_ts(tmem + 256 + 128 * x, tmem + 128 * x + k * 8, b + 128 * k, idPV, (kp[x] > 0 || k > 0) ? 1u : 0u);
             mma_commit(&pv_done[x]);
             ++kp[x];
           }
