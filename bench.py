@@ -41,7 +41,7 @@ LAUNCHES_PER_DECODE = 2
 # summarised in profiles/ (prefill_kernels_varlen_gqa_8192_d128.md,
 # decode_kernels_paged_fp8_decode_64x1.md); set back to None whenever the kernel changes.
 NCU_TRAFFIC = {
-    "bwd": None,               # prefill_bwd_dq_kernel<128> + prefill_bwd_kernel<128,128>: changed since capture
+    "bwd": None,               # prefill_bwd_dq_kernel<128> + prefill_bwd_kernel<128>: changed since capture
     "fwd": None,               # prefill_fwd2_kernel<128>: not captured since it replaced prefill_fwd_kernel
     "decode_split": 1188.2e6,  # decode_split_kernel
 }
@@ -223,7 +223,7 @@ def run_native(args):
 
     # dominant kernel: the fused backward attention kernel
     sustained = pk.get("bf16_tflops_sustained", pk.get("bf16_tflops"))
-    dom = ("prefill_bwd_dq_kernel<128> + prefill_bwd_kernel<128,128> (two-pass backward)" if bwd_k >= fwd_k
+    dom = ("prefill_bwd_dq_kernel<128> + prefill_bwd_kernel<128> (two-pass backward)" if bwd_k >= fwd_k
            else "prefill_fwd2_kernel<128>")
     dom_fl, dom_ms = (bwd_fl, bwd_k) if bwd_k >= fwd_k else (fwd_fl, fwd_k)
     achieved = dom_fl / (dom_ms * 1e-3) / 1e12

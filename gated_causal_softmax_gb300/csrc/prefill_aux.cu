@@ -185,11 +185,11 @@ __global__ void __launch_bounds__(64) bwd_pack_kernel(const int32_t* __restrict_
     }
     t -= n;
   }
-  if (start < 0) return;
+  // tiles past the last sequence are zero-filled: a 128-row consumer step may read one
   const int h = blockIdx.y;
   const int i = local * 64 + threadIdx.x;
   float colterm = 0.f, dl = 0.f;
-  if (i < len) {
+  if (start >= 0 && i < len) {
     const size_t idx = (size_t)h * total + start + i;
     colterm = -__ldg(lse + idx) * kLog2e;
     if (gT) colterm += __ldg(gT + idx);
