@@ -8,22 +8,21 @@
 // over 128-row query tiles in the causal / window range ("steps").  Per step:
 //     S^T  = K Q^T       (TMEM, fp32)     P^T  = 2^(S^T scale log2e + G_i - G_j - LSE_i)
 //     dP^T = V dO^T      (TMEM, fp32)     dS^T = P^T o (dP^T - delta_i)
-//     dV  += P^T dO      (A operand = P^T, bf16, a swizzled shared-memory tile)
+//     dV  += P^T dO      (A operand = P^T, bf16, written over the consumed S^T in TMEM)
 //     dK  += dS^T Q      (A operand = dS^T, bf16, written over the consumed dP^T in TMEM)
 // plus the fp32 column sums of dS (gate gradient), one thread per key row.
 //
 // Every MMA has N = 128: on this part an MMA with N = 64 takes nearly as long as one with
-// N = 128.  TMEM then holds S^T, dP^T, dV and dK (4 x 128 columns at D = 128), so there is
-// one score buffer; P^T goes to shared memory, which frees S^T as soon as the warps have
-// loaded it.  The issue order
-//     S^T(s+1), dV(s), dK(s), dP^T(s+1), S^T(s+2), dV(s+1), ...
-// keeps the tensor pipe busy while the warps work on a step: S^T(s+1) runs under the
-// exponentials of step s, dV(s) / dK(s) / dP^T(s+1) under those of step s + 1.  tcgen05.mma
-// operations issued by one thread execute in issue order, so dP^T(s+1) may overwrite the
-// TMEM columns that dK(s) reads as its A operand.
+// N = 128.  TMEM holds S^T, dP^T, dV and dK (4 x 128 columns at D = 128).  The issue order
+//     dV(s), S^T(s+1), dK(s), dP^T(s+1), dV(s+1), ...
+// runs dV / S^T(s+1) under the dS work of step s and dK(s) / dP^T(s+1) under the
+// exponentials of step s + 1.  tcgen05.mma operations issued by one thread execute in
+// issue order, so S^T(s+1) may overwrite the TMEM columns that dV(s) reads as its A
+// operand, and dP^T(s+1) those that dK(s) reads.  Q tiles rotate through three buffers
+// (S^T(s+1) is issued early in step s), dO tiles and the per-column vectors through two.
 //
 // Warp roles (384 threads): warp 0 TMA producer (K, V once; Q, dO and the packed
-// per-column LSE / delta / gate vectors in two rotating buffers), warp 1 tcgen05 issuer,
+// per-column LSE / delta / gate vectors in rotating buffers), warp 1 tcgen05 issuer,
 // warps 2-3 idle, warps 4-7 and 8-11 the two halves (query columns 0-63, 64-127) of every
 // step.  setmaxnreg moves registers from the first warpgroup to the other two.
 #include "kernels.h"
@@ -39,6 +38,8 @@ constexpr int kThreads = 384;
 constexpr int kChunk = 128 * 128;  // 128 rows x 64 bf16: one swizzled operand chunk
 constexpr int kVecBytes = 2 * kBM * 4;  // per step: two packed 64-row tiles of (colterm, delta)
 constexpr int kSmemOptinMax = 232448;
+constexpr int kNQ = 3;   // Q buffers
+constexpr int kNDO = 2;  // dO + vector buffers
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
@@ -48,12 +49,11 @@ struct BwdCfg {
   static constexpr int TILE = CH * kChunk;          // one 128-row tile of a D-wide operand
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + TILE;
-  static constexpr int OFF_Q = OFF_V + TILE;        // [2] tiles
-  static constexpr int OFF_DO = OFF_Q + 2 * TILE;   // [2] tiles
-  static constexpr int OFF_P = OFF_DO + 2 * TILE;   // P^T: chunk 0 = query columns 0-63, chunk 1 = 64-127
-  static constexpr int OFF_VEC = OFF_P + 2 * kChunk;  // [2] x kVecBytes
-  static constexpr int OFF_BAR = OFF_VEC + 2 * kVecBytes;
-  static constexpr int NBAR = 16;
+  static constexpr int OFF_Q = OFF_V + TILE;        // [kNQ] tiles
+  static constexpr int OFF_DO = OFF_Q + kNQ * TILE;  // [kNDO] tiles
+  static constexpr int OFF_VEC = OFF_DO + kNDO * TILE;  // [kNDO] x kVecBytes (travel with dO)
+  static constexpr int OFF_BAR = OFF_VEC + kNDO * kVecBytes;
+  static constexpr int NBAR = 18;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   // The operand tiles need 1024-B alignment; the dynamic shared window starts aligned when
   // the kernel has no static shared memory, which the kernel checks (no slack is left).
@@ -124,16 +124,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* kv_full = bars + 0;
-  uint64_t* q_full = bars + 1;     // [2] Q, dO and vectors of a step landed
-  uint64_t* q_empty = bars + 3;    // [2] dV and dK of a step retired
-  uint64_t* s_full = bars + 5;     // S^T written
-  uint64_t* s_free = bars + 6;     // S^T loaded by all 8 warps
-  uint64_t* dp_full = bars + 7;    // dP^T written
-  uint64_t* p_ready = bars + 8;    // P^T stored in shared memory (8 warps)
-  uint64_t* p_free = bars + 9;     // dV MMA retired (P^T may be overwritten)
-  uint64_t* ds_ready = bars + 10;  // dS^T stored in TMEM (8 warps)
-  uint64_t* all_done = bars + 11;  // every MMA of the CTA retired (epilogue)
-  uint64_t* drain = bars + 12;
+  uint64_t* q_full = bars + 1;     // [kNQ] Q tile landed
+  uint64_t* q_empty = bars + 4;    // [kNQ] dK of its step retired
+  uint64_t* do_full = bars + 7;    // [kNDO] dO tile and vectors landed
+  uint64_t* do_empty = bars + 9;   // [kNDO] dK of its step retired (vectors are read until then)
+  uint64_t* s_full = bars + 11;    // S^T written
+  uint64_t* dp_full = bars + 12;   // dP^T written
+  uint64_t* p_ready = bars + 13;   // P^T stored in TMEM (8 warps)
+  uint64_t* ds_ready = bars + 14;  // dS^T stored in TMEM (8 warps)
+  uint64_t* all_done = bars + 15;  // every MMA of the CTA retired (epilogue)
+  uint64_t* drain = bars + 16;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   const Abort ab{abort_flag, p.status};
@@ -141,15 +141,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kNQ; ++b) {
       mbar_init(&q_full[b], 1);
       mbar_init(&q_empty[b], 1);
     }
+    for (int b = 0; b < kNDO; ++b) {
+      mbar_init(&do_full[b], 1);
+      mbar_init(&do_empty[b], 1);
+    }
     mbar_init(s_full, 1);
-    mbar_init(s_free, 8);
     mbar_init(dp_full, 1);
     mbar_init(p_ready, 8);
-    mbar_init(p_free, 1);
     mbar_init(ds_ready, 8);
     mbar_init(all_done, 1);
     mbar_init(drain, 1);
@@ -180,20 +182,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d(smem + C::OFF_V + c * kChunk, &tmV, kv_full, kvh * D + c * 64, seq_start + j0);
       const uint64_t pol = l2_policy_evict_last();
       for (int s = 0; s < nsteps; ++s) {
-        const int qb = s & 1;
+        const int qb = s % kNQ, db = s % kNDO;
         const int h = kvh * group + s / n_it;
         const int it = it_lo + s % n_it;
-        if (!wait_bar(&q_empty[qb], ((s >> 1) & 1) ^ 1, ab)) break;
-        mbar_expect_tx(&q_full[qb], 2 * C::TILE + kVecBytes);
+        if (!wait_bar(&q_empty[qb], ((s / kNQ) & 1) ^ 1, ab)) break;
+        mbar_expect_tx(&q_full[qb], C::TILE);
         for (int c = 0; c < C::CH; ++c)
           tma_load_2d_hint(smem + C::OFF_Q + qb * C::TILE + c * kChunk, &tmQ, &q_full[qb], h * D + c * 64,
                            seq_start + it * kBM, pol);
+        if (!wait_bar(&do_empty[db], ((s / kNDO) & 1) ^ 1, ab)) break;
+        mbar_expect_tx(&do_full[db], C::TILE + kVecBytes);
         for (int c = 0; c < C::CH; ++c)
-          tma_load_2d_hint(smem + C::OFF_DO + qb * C::TILE + c * kChunk, &tmDO, &q_full[qb], h * D + c * 64,
+          tma_load_2d_hint(smem + C::OFF_DO + db * C::TILE + c * kChunk, &tmDO, &do_full[db], h * D + c * 64,
                            seq_start + it * kBM, pol);
         // per-column vectors of the two 64-row tiles: [(G_i - LSE_i) log2 e x 64, delta_i x 64] x 2
-        bulk_load(smem + C::OFF_VEC + qb * kVecBytes, p.vecp + ((size_t)h * p.n_qtiles + qoff + 2 * it) * 128,
-                  kVecBytes, &q_full[qb]);
+        bulk_load(smem + C::OFF_VEC + db * kVecBytes, p.vecp + ((size_t)h * p.n_qtiles + qoff + 2 * it) * 128,
+                  kVecBytes, &do_full[db]);
       }
     } else if (warp == 1 && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
@@ -207,12 +211,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dDO0 = sdesc_sw128(smem_u32(smem + C::OFF_DO), 16, 1024);
       const uint64_t dQmn0 = sdesc_sw128(smem_u32(smem + C::OFF_Q), kChunk, 1024);
       const uint64_t dDOmn0 = sdesc_sw128(smem_u32(smem + C::OFF_DO), kChunk, 1024);
-      const uint64_t dP0 = sdesc_sw128(smem_u32(smem + C::OFF_P), 16, 1024);
       constexpr uint32_t kChunk16 = kChunk >> 4, kTile16 = C::TILE >> 4;
-      auto issue_s = [&](int t) -> bool {  // S^T(t) = K Q(t)^T
-        const int qb = t & 1;
-        if (!wait_bar(&q_full[qb], (t >> 1) & 1, ab)) return false;
-        tc_fence_after();
+      // Waits are batched: the tensor pipe has almost no issue queue, so every stall of this
+      // thread on a barrier (a shared-memory access that the operand reads of running MMAs
+      // slow down) leaves the pipe idle.  Per step: one combined wait, then dV(s) and S^T(s+1)
+      // back to back; a second one, then dK(s) and dP^T(s+1).
+      auto mma_s = [&](int t) {  // S^T(t) = K Q(t)^T (Q(t) landed)
+        const int qb = t % kNQ;
 #pragma unroll
         for (int c = 0; c < C::CH; ++c) {
           const uint64_t a = dK0 + c * kChunk16, b = dQ0 + qb * kTile16 + c * kChunk16;
@@ -220,49 +225,52 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < 4; ++k) mma_ss(tmem + C::T_S, a + 2 * k, b + 2 * k, idS, (c | k) != 0);
         }
         mma_commit(s_full);
-        return true;
       };
-      auto issue_dp = [&](int t) {  // dP^T(t) = V dO(t)^T (Q / dO(t) already landed)
-        const int qb = t & 1;
+      auto mma_dp = [&](int t) {  // dP^T(t) = V dO(t)^T (dO(t) landed)
+        const int db = t % kNDO;
 #pragma unroll
         for (int c = 0; c < C::CH; ++c) {
-          const uint64_t a = dV0 + c * kChunk16, b = dDO0 + qb * kTile16 + c * kChunk16;
+          const uint64_t a = dV0 + c * kChunk16, b = dDO0 + db * kTile16 + c * kChunk16;
 #pragma unroll
           for (int k = 0; k < 4; ++k) mma_ss(tmem + C::T_DP, a + 2 * k, b + 2 * k, idS, (c | k) != 0);
         }
         mma_commit(dp_full);
       };
-      bool ok = wait_bar(kv_full, 0, ab);
-      if (ok) ok = issue_s(0);
-      if (ok) issue_dp(0);
+      bool ok = wait_bars(ab, kv_full, 0, &q_full[0], 0, &do_full[0], 0);
+      if (ok) {
+        tc_fence_after();
+        mma_s(0);
+        mma_dp(0);
+      }
       for (int s = 0; s < nsteps && ok; ++s) {
-        const int qb = s & 1;
-        if (s + 1 < nsteps) {
-          // next scores into the single S^T buffer once all warps have loaded S^T(s)
-          ok = wait_bar(s_free, s & 1, ab);
-          if (!ok) break;
-          ok = issue_s(s + 1);
-          if (!ok) break;
-        }
-        ok = wait_bar(p_ready, s & 1, ab);
+        const int qb = s % kNQ, db = s % kNDO;
+        const bool more = s + 1 < nsteps;
+        // P^T(s) stored, Q(s+1) landed
+        ok = more ? wait_bars(ab, p_ready, s & 1, &q_full[(s + 1) % kNQ], ((s + 1) / kNQ) & 1)
+                  : wait_bars(ab, p_ready, s & 1);
         if (!ok) break;
         tc_fence_after();
-        // dV += P^T dO: K = 128 query rows, 8 steps of 16 (P^T chunk k / 4, 32 B per step)
+        // dV += P^T dO: K = 128 query rows, 8 steps of 16; P^T of query columns 0-63 at
+        // T_S + 0..31, of 64-127 at T_S + 64..95 (each warpgroup packs over its own half)
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          mma_ss(tmem + C::T_DV, dP0 + (k >> 2) * kChunk16 + 2 * (k & 3), dDOmn0 + qb * kTile16 + 128 * k, idAcc,
+          mma_ts(tmem + C::T_DV, tmem + C::T_S + (k >> 2) * 64 + 8 * (k & 3), dDOmn0 + db * kTile16 + 128 * k, idAcc,
                  (s > 0 || k > 0) ? 1u : 0u);
-        mma_commit(p_free);
-        ok = wait_bar(ds_ready, s & 1, ab);
+        // next scores over the S^T columns (dV above reads P^T first: in-order execution)
+        if (more) mma_s(s + 1);
+        // dS^T(s) stored, dO(s+1) landed
+        ok = more ? wait_bars(ab, ds_ready, s & 1, &do_full[(s + 1) % kNDO], ((s + 1) / kNDO) & 1)
+                  : wait_bars(ab, ds_ready, s & 1);
         if (!ok) break;
         tc_fence_after();
-        // dK += dS^T Q: dS^T of query columns 0-63 at T_DP + 0..31, of 64-127 at T_DP + 64..95
+        // dK += dS^T Q, dS^T laid out over dP^T like P^T over S^T
 #pragma unroll
         for (int k = 0; k < 8; ++k)
           mma_ts(tmem + C::T_DK, tmem + C::T_DP + (k >> 2) * 64 + 8 * (k & 3), dQmn0 + qb * kTile16 + 128 * k, idAcc,
                  (s > 0 || k > 0) ? 1u : 0u);
         mma_commit(&q_empty[qb]);
-        if (s + 1 < nsteps) issue_dp(s + 1);
+        mma_commit(&do_empty[db]);
+        if (more) mma_dp(s + 1);
       }
       if (ok) mma_commit(all_done);
       if (!ok) {
@@ -280,8 +288,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_off + C::T_S + 64 * wg;
     const uint32_t tDP = tmem + lane_off + C::T_DP + 64 * wg;
-    uint8_t* prow = smem + C::OFF_P + wg * kChunk + r * 128;  // this key row of P^T chunk wg
-    const uint32_t rsw = static_cast<uint32_t>(r & 7);
     const int jl = j0 + r;
     const bool has_gate = p.gT != nullptr;
     float dgcol = 0.f;
@@ -289,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float rowterm = 0.f;
     bool ok = true;
     for (int s = 0; s < nsteps; ++s) {
-      const int qb = s & 1;
+      const int db = s % kNDO;
       const int h = kvh * group + s / n_it;
       const int i0 = (it_lo + s % n_it) * kBM;
       if (h != cur_h) {
@@ -301,9 +307,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         cur_h = h;
         rowterm = (has_gate && jl < len) ? -__ldg(p.gT + (size_t)h * p.total + seq_start + jl) : 0.f;
       }
-      ok = wait_bar(&q_full[qb], (s >> 1) & 1, ab);
+      ok = wait_bar(&do_full[db], (s / kNDO) & 1, ab);
       if (!ok) break;
-      const float4* vec4 = reinterpret_cast<const float4*>(smem + C::OFF_VEC + qb * kVecBytes + wg * (kVecBytes / 2));
+      const float4* vec4 = reinterpret_cast<const float4*>(smem + C::OFF_VEC + db * kVecBytes + wg * (kVecBytes / 2));
       const bool need_mask = (i0 < j0 + kBN - 1) || (p.window > 0 && i0 + kBM - 1 - j0 >= p.window) ||
                              (i0 + kBM > len);
       // visible query columns of this key row (relative to this warpgroup's first column):
@@ -311,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int cb = i0 + 64 * wg;
       const int cmin = jl - cb;
       const int cmax = min(p.window > 0 ? jl + p.window - 1 - cb : (1 << 30), len - 1 - cb);
-      // ---- S^T -> registers, then release the score buffer for the next step
+      // ---- P = 2^(S scale log2e + G_i - LSE_i - G_j) in fp32, P^T (bf16) over S^T
       ok = wait_bar(s_full, s & 1, ab);
       if (!ok) break;
       tc_fence_after();
@@ -321,26 +327,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tS, sv);
         tmem_ld32(tS + 32, sv + 32);
         tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(s_free);
-        // ---- P = 2^(S scale log2e + G_i - LSE_i - G_j) in fp32
         if (need_mask)
           p_row<true>(pr, sv, vec4, rowterm, p.scale_log2, cmin, cmax);
         else
           p_row<false>(pr, sv, vec4, rowterm, p.scale_log2, cmin, cmax);
       }
-      // ---- P^T (bf16) into the swizzled K-major tile, once dV of the previous step is done
-      if (s > 0) {
-        ok = wait_bar(p_free, (s - 1) & 1, ab);
-        if (!ok) break;
-      }
 #pragma unroll
-      for (int c16 = 0; c16 < 8; ++c16)
-        *reinterpret_cast<uint4*>(prow + ((c16 ^ rsw) << 4)) =
-            make_uint4(pack_bf16x2(pr[8 * c16], pr[8 * c16 + 1]), pack_bf16x2(pr[8 * c16 + 2], pr[8 * c16 + 3]),
-                       pack_bf16x2(pr[8 * c16 + 4], pr[8 * c16 + 5]), pack_bf16x2(pr[8 * c16 + 6], pr[8 * c16 + 7]));
-      fence_proxy_async_smem();
+      for (int ch = 0; ch < 2; ++ch) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) pk[c] = pack_bf16x2(pr[32 * ch + 2 * c], pr[32 * ch + 2 * c + 1]);
+        tmem_st16(tS + 16 * ch, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_ready);
       // ---- dS = P (dP - delta_i) in fp32, dS^T (bf16) over this warpgroup's dP^T columns

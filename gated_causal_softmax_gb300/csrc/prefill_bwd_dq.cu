@@ -50,13 +50,21 @@ template <bool MASK>
 __device__ __forceinline__ float dq_chunk(uint32_t* sv, const uint32_t* dp, const float* gj, int jb, float rowterm,
                                           float scale_log2, float dl, int jmin, int jmax) {
   float acc[4] = {0.f, 0.f, 0.f, 0.f};  // independent partial sums (latency)
+  // -G_j as 16-B broadcast loads: shared-memory loads compete with running MMAs' operand reads
+  const float4* gj4 = reinterpret_cast<const float4*>(gj + jb);
 #pragma unroll
-  for (int c = 0; c < 32; ++c) {
-    float t = fmaf(__uint_as_float(sv[c]), scale_log2, rowterm) + gj[jb + c];
-    if (MASK) t = (jb + c >= jmin && jb + c <= jmax) ? t : neg_inf();
-    const float ds = ex2(t) * (__uint_as_float(dp[c]) - dl);
-    acc[c & 3] += ds;
-    sv[c] = __float_as_uint(ds);
+  for (int c4 = 0; c4 < 8; ++c4) {
+    const float4 g4 = gj4[c4];
+    const float gs[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int c = 4 * c4 + e;
+      float t = fmaf(__uint_as_float(sv[c]), scale_log2, rowterm) + gs[e];
+      if (MASK) t = (jb + c >= jmin && jb + c <= jmax) ? t : neg_inf();
+      const float ds = ex2(t) * (__uint_as_float(dp[c]) - dl);
+      acc[c & 3] += ds;
+      sv[c] = __float_as_uint(ds);
+    }
   }
   return (acc[0] + acc[1]) + (acc[2] + acc[3]);
 }
@@ -172,11 +180,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dV0 = sdesc_sw128(smem_u32(smem + C::OFF_V), 16, 1024);
       const uint64_t dKmn0 = sdesc_sw128(smem_u32(smem + C::OFF_K), kChunk, 1024);
       constexpr uint32_t kChunk16 = kChunk >> 4, kTile16 = C::TILE >> 4;
-      bool ok = wait_bar(qd_full, 0, ab);
-      auto issue_s = [&](int n) -> bool {
+      // Waits are batched ahead of runs of back-to-back MMAs: the tensor pipe has almost no
+      // issue queue, so each stall of this thread on a barrier leaves it idle.
+      auto mma_s = [&](int n) {  // S(n) = Q K(n)^T into S[n & 1] (K(n) landed)
         const int kb = n & 1;
-        if (!wait_bar(&k_full[kb], (n >> 1) & 1, ab)) return false;
-        tc_fence_after();
 #pragma unroll
         for (int c = 0; c < C::CH; ++c) {
           const uint64_t a = dQ0 + c * kChunk16, b = dK0 + kb * kTile16 + c * kChunk16;
@@ -184,12 +191,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < 4; ++k) mma_ss(tmem + C::T_S + 128 * (n & 1), a + 2 * k, b + 2 * k, idSS, (c | k) != 0);
         }
         mma_commit(&s_full[n & 1]);
-        return true;
       };
-      auto issue_dp = [&](int n) -> bool {
+      auto mma_dp = [&](int n) {  // dP(n) = dO V(n)^T (V(n) landed)
         const int kb = n & 1;
-        if (!wait_bar(&v_full[kb], (n >> 1) & 1, ab)) return false;
-        tc_fence_after();
 #pragma unroll
         for (int c = 0; c < C::CH; ++c) {
           const uint64_t a = dDO0 + c * kChunk16, b = dV0 + kb * kTile16 + c * kChunk16;
@@ -198,28 +202,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(dp_full);
         mma_commit(&v_empty[kb]);
-        return true;
       };
-      if (ok) ok = issue_s(0);
-      if (ok) ok = issue_dp(0);
-      if (ok && nt > 1) ok = issue_s(1);
+      bool ok = wait_bars(ab, qd_full, 0, &k_full[0], 0, &v_full[0], 0);
+      if (ok) {
+        tc_fence_after();
+        mma_s(0);
+        mma_dp(0);
+      }
+      if (ok && nt > 1) {
+        ok = wait_bars(ab, &k_full[1], 0);
+        if (ok) {
+          tc_fence_after();
+          mma_s(1);
+        }
+      }
       for (int n = 0; n < nt && ok; ++n) {
         const int b = n & 1, kb = n & 1;
-        ok = wait_bar(ds_ready, n & 1, ab);
+        const bool more = n + 1 < nt;
+        // dS(n) stored (the warps consumed dP(n) before signalling), V(n+1) landed
+        ok = more ? wait_bars(ab, ds_ready, n & 1, &v_full[(n + 1) & 1], ((n + 1) >> 1) & 1)
+                  : wait_bars(ab, ds_ready, n & 1);
         if (!ok) break;
         tc_fence_after();
-        // dP of the next tile first (the warps consumed dP before signalling), then dQ
-        if (n + 1 < nt) {
-          ok = issue_dp(n + 1);
-          if (!ok) break;
-        }
+        if (more) mma_dp(n + 1);
 #pragma unroll
         for (int k = 0; k < 8; ++k)
           mma_ts(tmem + C::T_DQ, tmem + C::T_S + 128 * b + k * 8, dKmn0 + kb * kTile16 + 128 * k, idDQ,
                  (n > 0 || k > 0) ? 1u : 0u);
         mma_commit(&k_empty[kb]);
-        // scores of tile n + 2 over buffer b (its dS was read by the dQ MMAs above)
-        if (n + 2 < nt) ok = issue_s(n + 2);
+        // scores of tile n + 2 over buffer b (its dS was read by the dQ MMAs above); its K
+        // stage was freed by those MMAs, so this wait covers the load
+        if (n + 2 < nt) {
+          ok = wait_bars(ab, &k_full[kb], ((n + 2) >> 1) & 1);
+          if (!ok) break;
+          tc_fence_after();
+          mma_s(n + 2);
+        }
       }
       if (ok) mma_commit(dq_done);
       if (!ok) {

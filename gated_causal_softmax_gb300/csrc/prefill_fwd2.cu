@@ -34,10 +34,11 @@ __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); 
 template <int D>
 struct Fwd2Cfg {
   static constexpr int CH = D / 64;
-  static constexpr int NST = 8;
+  static constexpr int TILE = CH * kChunk;                 // one K or V tile (128 keys)
+  static constexpr int NST = 8 / CH;                       // ring stages, one tile each
   static constexpr int OFF_Q = 0;                           // [2 tiles][CH] chunks
   static constexpr int OFF_RING = 2 * CH * kChunk;
-  static constexpr int OFF_G = OFF_RING + NST * kChunk;     // [2 tiles][4 warps][2][128] floats
+  static constexpr int OFF_G = OFF_RING + NST * TILE;      // [2 tiles][4 warps][2][128] floats
   static constexpr int OFF_BAR = OFF_G + 2 * 4 * 2 * kBN * 4;
   static constexpr int OFF_MISC = OFF_BAR + (2 * NST + 16) * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;
@@ -74,11 +75,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int hi_t = valid_b ? qt[1] : qt[0];
   const int lo_t = lo[0];
   const int nt = hi_t - lo_t + 1;
-  // tile x takes part in key tile n (jt = hi_t - n) when jt lies in [lo[x], qt[x]]
-  auto part = [&](int x, int n) -> bool {
-    const int jt = hi_t - n;
-    return (x == 0 || valid_b) && jt <= qt[x] && jt >= lo[x];
-  };
+  // tile x takes part in key tile n (jt = hi_t - n) when jt lies in [lo[x], qt[x]], i.e. when
+  // n lies in [hi_t - qt[x], hi_t - lo[x]] (an empty range for an invalid tile B)
+  const int n_first[2] = {hi_t - qt[0], valid_b ? hi_t - qt[1] : nt};
+  const int n_last[2] = {hi_t - lo[0], valid_b ? hi_t - lo[1] : -1};
+  auto part = [&](int x, int n) -> bool { return n >= n_first[x] && n <= n_last[x]; };
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* full = bars;              // [NST]
@@ -135,24 +136,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int n = 0; n < nt && ok; ++n) {
         const int y = seq_start + (hi_t - n) * kBN;
-        for (int kv = 0; kv < 2 && ok; ++kv)
-          for (int c = 0; c < C::CH && ok; ++c) {
-            ok = wait_bar(&empty[stage], phase ^ 1, ab);
-            if (!ok) break;
-            mbar_expect_tx(&full[stage], kChunk);
-            tma_load_2d_hint(smem + C::OFF_RING + stage * kChunk, kv ? &tmV : &tmK, &full[stage], kvh * D + c * 64,
-                             y, pol_kv);
-            if (++stage == C::NST) {
-              stage = 0;
-              phase ^= 1;
-            }
+        for (int kv = 0; kv < 2 && ok; ++kv) {
+          ok = wait_bar(&empty[stage], phase ^ 1, ab);
+          if (!ok) break;
+          mbar_expect_tx(&full[stage], C::TILE);
+          for (int c = 0; c < C::CH; ++c)
+            tma_load_2d_hint(smem + C::OFF_RING + stage * C::TILE + c * kChunk, kv ? &tmV : &tmK, &full[stage],
+                             kvh * D + c * 64, y, pol_kv);
+          if (++stage == C::NST) {
+            stage = 0;
+            phase ^= 1;
           }
+        }
       }
     } else if (warp == 1 && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
       // One MMA with N < 128 takes nearly as long as one with N = 128, so P V is issued with
-      // N = D across the D/64 value chunks of a key tile (adjacent ring stages, LBO = one
-      // chunk).  Descriptors are built once; an operand offset is added to the address field
+      // N = D across the D/64 value chunks of a ring stage (LBO = one chunk).  Descriptors are built once; an operand offset is added to the address field
       // (shared-memory addresses stay below 2^18, so the 14-bit field never carries).
       const uint32_t idS = idesc_bf16(128, kBN, false, false);
       const uint32_t idPV = idesc_bf16(128, D, false, true);
@@ -160,56 +160,60 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dK0 = sdesc_sw128(smem_u32(smem + C::OFF_RING), 16, 1024);
       const uint64_t dV0 = sdesc_sw128(smem_u32(smem + C::OFF_RING), kChunk, 1024);
       constexpr uint32_t kChunk16 = kChunk >> 4;
-      static_assert(C::NST % C::CH == 0, "a key tile's chunks must be adjacent ring stages");
-      uint32_t stage = 0, phase = 0;
-      // ring chunks of key tile n: K at positions kpos..kpos+CH-1, V after them
-      auto take = [&](uint32_t& pos_out) -> bool {  // wait for the next CH chunks
-        pos_out = stage;
-        for (int c = 0; c < C::CH; ++c) {
-          if (!wait_bar(&full[stage], phase, ab)) return false;
-          if (++stage == C::NST) {
-            stage = 0;
-            phase ^= 1;
-          }
+      constexpr uint32_t kTile16 = C::TILE >> 4;
+      // Waits are batched ahead of runs of back-to-back MMAs: the tensor pipe has almost no
+      // issue queue, so each stall of this thread on a barrier leaves it idle.
+      uint32_t stage = 0, phase = 0;  // ring position of the next tile (K, V, K, V, ...)
+      auto next = [&](uint32_t& st, uint32_t& ph) {
+        st = stage;
+        ph = phase;
+        if (++stage == C::NST) {
+          stage = 0;
+          phase ^= 1;
         }
-        tc_fence_after();
-        return true;
       };
-      auto release = [&](uint32_t pos) {
-        for (int c = 0; c < C::CH; ++c) mma_commit(&empty[(pos + c) % C::NST]);
-      };
-      auto issue_s = [&](int x, uint32_t kpos) {
+      auto mma_s = [&](int x, uint32_t st) {  // S_x = Q_x K^T over ring stage st
 #pragma unroll
         for (int c = 0; c < C::CH; ++c) {
-          const uint64_t a = dQ0 + (x * C::CH + c) * kChunk16, b = dK0 + (kpos + c) * kChunk16;
+          const uint64_t a = dQ0 + (x * C::CH + c) * kChunk16, b = dK0 + st * kTile16 + c * kChunk16;
 #pragma unroll
           for (int k = 0; k < 4; ++k) mma_ss(tmem + 128 * x, a + 2 * k, b + 2 * k, idS, (c | k) != 0);
         }
         mma_commit(&s_full[x]);
       };
       int kp[2] = {0, 0};  // PV issued per tile (accumulate flag and p_full parity)
-      bool ok = wait_bar(q_full, 0, ab);
-      uint32_t kpos = 0, vpos = 0;
-      if (ok) ok = take(kpos);
+      uint32_t sk = 0, pk = 0;
+      next(sk, pk);  // K of key tile 0
+      bool ok = wait_bars(ab, q_full, 0, &full[sk], pk);
       if (ok) {
+        tc_fence_after();
+#pragma unroll
         for (int x = 0; x < 2; ++x)
-          if (part(x, 0)) issue_s(x, kpos);
-        release(kpos);
+          if (part(x, 0)) mma_s(x, sk);
+        mma_commit(&empty[sk]);
       }
       for (int n = 0; n < nt && ok; ++n) {
-        ok = take(vpos);
-        if (!ok) break;
-        uint32_t knext = 0;
-        if (n + 1 < nt) {
-          ok = take(knext);
+        const bool more = n + 1 < nt;
+        uint32_t sv, pv, sk1 = 0, pk1 = 0;
+        next(sv, pv);  // V of key tile n
+        if (more) next(sk1, pk1);  // K of key tile n + 1
+        bool first = true;
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
           if (!ok) break;
-        }
-        for (int x = 0; x < 2 && ok; ++x) {
-          if (part(x, n)) {
-            ok = wait_bar(&p_full[x], kp[x] & 1, ab);
-            if (!ok) break;
-            tc_fence_after();
-            const uint64_t b = dV0 + vpos * kChunk16;
+          const bool do_pv = part(x, n), do_s = more && part(x, n + 1);
+          if (!do_pv && !do_s) continue;
+          // the first batch also waits for this key tile's V and the next one's K
+          if (first)
+            ok = wait_bars(ab, &full[sv], pv, more ? &full[sk1] : nullptr, pk1, do_pv ? &p_full[x] : nullptr,
+                           kp[x] & 1);
+          else if (do_pv)
+            ok = wait_bars(ab, &p_full[x], kp[x] & 1);
+          first = false;
+          if (!ok) break;
+          tc_fence_after();
+          if (do_pv) {
+            const uint64_t b = dV0 + sv * kTile16;
 #pragma unroll
             for (int k = 0; k < 8; ++k)
               mma_ts(tmem + 256 + 128 * x, tmem + 128 * x + k * 8, b + 128 * k, idPV, (kp[x] > 0 || k > 0) ? 1u : 0u);
@@ -217,11 +221,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++kp[x];
           }
           // next scores of this tile over its buffer (P was read by the PV above)
-          if (n + 1 < nt && part(x, n + 1)) issue_s(x, knext);
+          if (do_s) mma_s(x, sk1);
         }
         if (!ok) break;
-        release(vpos);
-        if (n + 1 < nt) release(knext);
+        mma_commit(&empty[sv]);
+        if (more) mma_commit(&empty[sk1]);
       }
       if (!ok) {
         mma_commit(drain);
@@ -233,6 +237,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     reg_inc();
     // ------------------------------------------------------------ softmax, tile x
     const int x = (warp - 4) >> 2;
+    const int my_first = x ? n_first[1] : n_first[0], my_last = x ? n_last[1] : n_last[0];
+    const int my_qt = x ? qt[1] : qt[0];
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
@@ -253,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int kx = 0;  // key tiles processed by this tile
     for (int n = 0; n < nt; ++n) {
-      if (!part(x, n)) continue;
+      if (n < my_first || n > my_last) continue;
       const int jt = hi_t - n, j0 = jt * kBN;
       float* gj = sG + (kx & 1) * kBN;  // this warp's copy of -G_j for the key tile
       if (has_gate) {
@@ -273,26 +279,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(tS + 64, sv + 64);
       tmem_ld32(tS + 96, sv + 96);
       tmem_ld_wait();
-      const bool need_mask = (jt == qt[x]) || (p.window > 0 && j0 < xq0 + kBM - p.window);
+      const bool need_mask = (jt == my_qt) || (p.window > 0 && j0 < xq0 + kBM - p.window);
       const int jmax = il - j0;
       const int jmin = p.window > 0 ? il - p.window + 1 - j0 : -(1 << 30);
       float mxp[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) mxp[e] = neg_inf();
+      // -G_j read as 16-B broadcast loads: shared-memory loads compete with the operand reads
+      // of running MMAs, so fewer, wider ones
+      const float4* gj4 = reinterpret_cast<const float4*>(gj);
       if (need_mask) {
 #pragma unroll
-        for (int j = 0; j < 128; ++j) {
-          float t = fmaf(__uint_as_float(sv[j]), p.scale_log2, gi) + gj[j];
-          t = (j >= jmin && j <= jmax) ? t : neg_inf();
-          sv[j] = __float_as_uint(t);
-          mxp[j & 7] = fmaxf(mxp[j & 7], t);
+        for (int j4 = 0; j4 < 32; ++j4) {
+          const float4 g4 = gj4[j4];
+          const float gs[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int j = 4 * j4 + e;
+            float t = fmaf(__uint_as_float(sv[j]), p.scale_log2, gi) + gs[e];
+            t = (j >= jmin && j <= jmax) ? t : neg_inf();
+            sv[j] = __float_as_uint(t);
+            mxp[j & 7] = fmaxf(mxp[j & 7], t);
+          }
         }
       } else {
 #pragma unroll
-        for (int j = 0; j < 128; ++j) {
-          const float t = fmaf(__uint_as_float(sv[j]), p.scale_log2, gi) + gj[j];
-          sv[j] = __float_as_uint(t);
-          mxp[j & 7] = fmaxf(mxp[j & 7], t);
+        for (int j4 = 0; j4 < 32; ++j4) {
+          const float4 g4 = gj4[j4];
+          const float gs[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int j = 4 * j4 + e;
+            const float t = fmaf(__uint_as_float(sv[j]), p.scale_log2, gi) + gs[e];
+            sv[j] = __float_as_uint(t);
+            mxp[j & 7] = fmaxf(mxp[j & 7], t);
+          }
         }
       }
       const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),

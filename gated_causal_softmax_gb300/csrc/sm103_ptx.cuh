@@ -110,6 +110,37 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const A
   }
 }
 
+// Tests three barrier phases with the tests issued back to back, so their shared-memory
+// round trips overlap (pass the same barrier twice for fewer).
+__device__ __forceinline__ bool mbar_test3(uint32_t a0, uint32_t p0, uint32_t a1, uint32_t p1, uint32_t a2,
+                                           uint32_t p2) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred q0, q1, q2;\n"
+      " mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 q0, [%1], %2;\n"
+      " mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 q1, [%3], %4;\n"
+      " mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 q2, [%5], %6;\n"
+      " and.pred q0, q0, q1;\n and.pred q0, q0, q2;\n selp.u32 %0, 1, 0, q0;\n}\n"
+      : "=r"(ok)
+      : "r"(a0), "r"(p0), "r"(a1), "r"(p1), "r"(a2), "r"(p2)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for up to three barrier phases (nullptr = unused).  The MMA issuer waits
+// once per batch of MMAs: the tensor pipe drains while its thread stalls on a shared-memory
+// access, so one combined test costs one pipe bubble instead of three.
+__device__ __forceinline__ bool wait_bars(const Abort& ab, uint64_t* b0, uint32_t p0, uint64_t* b1 = nullptr,
+                                          uint32_t p1 = 0, uint64_t* b2 = nullptr, uint32_t p2 = 0) {
+  const uint32_t a0 = smem_u32(b0);
+  const uint32_t a1 = b1 ? smem_u32(b1) : a0, a2 = b2 ? smem_u32(b2) : a0;
+  if (mbar_test3(a0, p0, a1, b1 ? p1 : p0, a2, b2 ? p2 : p0)) return true;
+  if (!wait_bar(b0, p0, ab)) return false;
+  if (b1 && !wait_bar(b1, p1, ab)) return false;
+  if (b2 && !wait_bar(b2, p2, ab)) return false;
+  return true;
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
