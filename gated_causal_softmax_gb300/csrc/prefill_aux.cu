@@ -11,6 +11,8 @@
 //                 d sink_h = -sum_i p_sink,i * sum_j P_ij dP_ij (Oct 3 comment), where the
 //                 fp32 row sum sum_j P_ij dP_ij is recovered exactly from the fp32 row sum
 //                 of dS:  sum_j P_ij dP_ij = sum_j dS_ij + delta_i * (1 - p_sink,i).
+#include <algorithm>
+
 #include "kernels.h"
 #include "sm103_ptx.cuh"
 
@@ -72,30 +74,46 @@ __global__ void __launch_bounds__(kScanThreads) gate_cumsum_kernel(const float* 
   }
 }
 
-// one warp per (token, head) row
+// L = min(32, dv / 8) lanes per (token, head) row, 8 elements (16 B of O and of dO) per lane
+// and chunk; rows are handed out grid-stride.
+// L = min(32, dv / 8) lanes per (token, head) row, 8 elements (16 B of O and of dO) per lane
+// and chunk; each warp takes 32 / L consecutive rows at a time, grid-stride.  The loop is
+// uniform across the warp (rows past the end load nothing), so the shuffles see every lane.
+template <int L>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict__ o,
                                                       const uint16_t* __restrict__ dout, int total, int hq, int dv,
                                                       float* __restrict__ delta) {
-  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= total * hq) return;
-  const uint4* po = reinterpret_cast<const uint4*>(o + (size_t)row * dv);
-  const uint4* pd = reinterpret_cast<const uint4*>(dout + (size_t)row * dv);
-  float acc = 0.f;
-  for (int c = lane; c < dv / 8; c += 32) {
-    const uint4 a = __ldg(po + c), b = __ldg(pd + c);
-    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+  constexpr int kRowsPerWarp = 32 / L;
+  const int lane = threadIdx.x & (L - 1);
+  const int group = (threadIdx.x & 31) / L;
+  const int rows = total * hq;
+  const int chunks = dv / (8 * L);
+  const int warps = gridDim.x * (blockDim.x >> 5);
+  for (int row0 = (blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * kRowsPerWarp; row0 < rows;
+       row0 += warps * kRowsPerWarp) {
+    const int row = row0 + group;
+    const bool valid = row < rows;
+    float acc0 = 0.f, acc1 = 0.f;
+    if (valid) {
+      const uint4* po = reinterpret_cast<const uint4*>(o + (size_t)row * dv);
+      const uint4* pd = reinterpret_cast<const uint4*>(dout + (size_t)row * dv);
+      for (int c = 0; c < chunks; ++c) {
+        const uint4 a = __ldg(po + c * L + lane), b = __ldg(pd + c * L + lane);
+        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      acc = fmaf(__uint_as_float(aw[k] << 16), __uint_as_float(bw[k] << 16), acc);
-      acc = fmaf(__uint_as_float(aw[k] & 0xffff0000u), __uint_as_float(bw[k] & 0xffff0000u), acc);
+        for (int k = 0; k < 4; ++k) {
+          acc0 = fmaf(__uint_as_float(aw[k] << 16), __uint_as_float(bw[k] << 16), acc0);
+          acc1 = fmaf(__uint_as_float(aw[k] & 0xffff0000u), __uint_as_float(bw[k] & 0xffff0000u), acc1);
+        }
+      }
     }
-  }
+    float acc = acc0 + acc1;
 #pragma unroll
-  for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) {
-    const int t = row / hq, h = row % hq;
-    delta[(size_t)h * total + t] = acc;
+    for (int off = L / 2; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, L);
+    if (valid && lane == 0) {
+      const int t = row / hq, h = row % hq;
+      delta[(size_t)h * total + t] = acc;
+    }
   }
 }
 
@@ -142,27 +160,39 @@ __global__ void __launch_bounds__(kScanThreads) dgate_kernel(const float* __rest
   }
 }
 
-// grid (hq): dsink_h = -sum_i p_i (rowsum_i + delta_i (1 - p_i)), p_i = e^{sigma_h - lse_i}
-__global__ void __launch_bounds__(256) dsink_kernel(const float* __restrict__ row, const float* __restrict__ lse,
-                                                    const float* __restrict__ delta, const float* __restrict__ sink,
-                                                    int total, float* __restrict__ dsink) {
-  __shared__ float red[8];
+// grid (hq), 1024 threads: dsink_h = -sum_i p_i (rowsum_i + delta_i (1 - p_i)), p_i = e^{sigma_h - lse_i};
+// four independent rows per thread and iteration keep loads in flight.  One block per head
+// sums in a fixed order, so the result does not depend on scheduling.
+__global__ void __launch_bounds__(1024) dsink_kernel(const float* __restrict__ row, const float* __restrict__ lse,
+                                                     const float* __restrict__ delta, const float* __restrict__ sink,
+                                                     int total, float* __restrict__ dsink) {
+  __shared__ float red[32];
   const int h = blockIdx.x;
   const float sig = __ldg(sink + h);
-  float acc = 0.f;
-  for (int t = threadIdx.x; t < total; t += blockDim.x) {
-    const size_t i = (size_t)h * total + t;
-    const float ps = __expf(sig - lse[i]);
-    acc += ps * (row[i] + delta[i] * (1.f - ps));
-  }
+  const float* rr = row + (size_t)h * total;
+  const float* ll = lse + (size_t)h * total;
+  const float* dd = delta + (size_t)h * total;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int base = 0; base < total; base += 4 * 1024) {
 #pragma unroll
-  for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+    for (int u = 0; u < 4; ++u) {
+      const int t = base + u * 1024 + threadIdx.x;
+      if (t < total) {
+        const float ps = __expf(sig - __ldg(ll + t));
+        acc[u] += ps * (__ldg(rr + t) + __ldg(dd + t) * (1.f - ps));
+      }
+    }
+  }
+  float a = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+#pragma unroll
+  for (int off = 16; off; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    float s = 0.f;
-    for (int w = 0; w < 8; ++w) s += red[w];
-    dsink[h] = -s;
+  if (threadIdx.x < 32) {
+    a = red[threadIdx.x];
+#pragma unroll
+    for (int off = 16; off; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
+    if (threadIdx.x == 0) dsink[h] = -a;
   }
 }
 
@@ -216,8 +246,13 @@ cudaError_t launch_gate_cumsum(const float* g, const int32_t* cu, int num_seqs, 
 
 cudaError_t launch_bwd_pre(const uint16_t* o, const uint16_t* dout, int total, int hq, int dv, int dqk, float* delta,
                            float* dq_acc, float* dg_row, float* dg_col, cudaStream_t s) {
-  const int rows = total * hq;
-  bwd_pre_kernel<<<(rows + 7) / 8, 256, 0, s>>>(o, dout, total, hq, dv, delta);
+  // enough blocks to fill the GPU several times over; rows are grid-stride
+  const int L = dv >= 256 ? 32 : dv / 8;
+  const long long lanes = (long long)total * hq * L;
+  const int blocks = (int)std::min<long long>((lanes + 255) / 256, 152 * 16);
+  if (L == 8) bwd_pre_kernel<8><<<blocks, 256, 0, s>>>(o, dout, total, hq, dv, delta);
+  else if (L == 16) bwd_pre_kernel<16><<<blocks, 256, 0, s>>>(o, dout, total, hq, dv, delta);
+  else bwd_pre_kernel<32><<<blocks, 256, 0, s>>>(o, dout, total, hq, dv, delta);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (dq_acc) e = cudaMemsetAsync(dq_acc, 0, (size_t)total * hq * dqk * sizeof(float), s);
@@ -246,7 +281,7 @@ cudaError_t launch_bwd_post(const float* dq_acc, uint16_t* dq, int total, int hq
     if (e != cudaSuccess) return e;
   }
   if (dsink) {
-    dsink_kernel<<<hq, 256, 0, s>>>(dg_row, lse, delta, sink, total, dsink);
+    dsink_kernel<<<hq, 1024, 0, s>>>(dg_row, lse, delta, sink, total, dsink);
     e = cudaGetLastError();
   }
   return e;
