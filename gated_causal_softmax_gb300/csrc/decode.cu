@@ -8,8 +8,10 @@
 // reduce in which an empty partial (M = -inf) weighs 0.
 //
 // decode_split_kernel: one CTA per (segment, kv head, request).  Warp 0 streams pages
-// (K 2 KB, V 2 KB, 16 K scales, 16 V scales) into an 8-stage shared-memory ring with
-// cp.async.bulk.  Warps 1..4 each own one query position (16 query heads of the GQA
+// (K 2 KB, V 2 KB, 16 K scales, 16 V scales) into a 16-stage shared-memory ring with
+// cp.async.bulk, eight pages per round: each of its 32 lanes issues one of the round's 32
+// copies (a bulk copy is a per-thread instruction, and one lane issuing them all serially
+// was the bottleneck).  Warps 1..4 each own one query position (16 query heads of the GQA
 // group = one m16 MMA tile) and a share of the pages; fp8 -> f16 conversion is exact,
 // QK^T and PV run on mma.sync m16n8k16 with fp32 accumulation, softmax in fp32 (log2
 // units).  P * vscale is scaled by 2^8 before the f16 rounding (round-to-nearest, no
@@ -35,7 +37,8 @@ constexpr int kPage = 16;
 constexpr int kD = 128;
 constexpr int kGroup = 16;
 constexpr int kStage = 4352;  // K 2048 | V 2048 | kscale 64 | vscale 64 | pad
-constexpr int kNST = 12;
+constexpr int kNST = 16;
+constexpr int kBatch = 8;  // pages the producer warp issues per round (4 copies each, one per lane)
 constexpr int kThreads = 160;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kPScale = 256.f;
@@ -105,30 +108,27 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
 
   if (warp == 0) {
     // ------------------------------------------------------------ page producer
+    // lane = 8 * kind + page within the round; kind 0: K, 1: V, 2: K scales, 3: V scales
     const int32_t* trow = p.block_table + (size_t)r * p.max_blocks + pb;
-    bool ok = true;
-    for (int base = 0; base < np && ok; base += 32) {
-      const int blk_l = (base + lane < np) ? __ldg(trow + base + lane) : 0;
-      const int cnt = min(32, np - base);
-      for (int ii = 0; ii < cnt; ++ii) {
-        const int blk = __shfl_sync(0xffffffffu, blk_l, ii);
-        if (lane == 0 && ok) {
-          const int i = base + ii;
-          const int stage = i % kNST;
-          const uint32_t par = ((i / kNST) & 1) ^ 1;
-          ok = wait_bar(&empty[stage], par, ab);
-          if (ok) {
-            uint8_t* st = smem + stage * kStage;
-            const size_t slot0 = ((size_t)blk * p.hkv + kvh) * kPage;
-            mbar_expect_tx(&full[stage], 2 * kPage * kD + 2 * kPage * 4);
-            bulk_load(st, p.k_cache + slot0 * kD, kPage * kD, &full[stage]);
-            bulk_load(st + 2048, p.v_cache + slot0 * kD, kPage * kD, &full[stage]);
-            bulk_load(st + 4096, p.k_scale + slot0, kPage * 4, &full[stage]);
-            bulk_load(st + 4160, p.v_scale + slot0, kPage * 4, &full[stage]);
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
+    const int pl = lane & (kBatch - 1), kind = lane / kBatch;
+    const uint32_t bytes = kind < 2 ? kPage * kD : kPage * 4;
+    const uint32_t dst_off = kind < 2 ? kind * 2048 : 4096 + (kind - 2) * 64;
+    for (int base = 0; base < np; base += kBatch) {
+      const int i = base + pl;
+      const bool act = i < np;
+      const int stage = i % kNST;
+      bool okl = true;
+      if (act) okl = wait_bar(&empty[stage], ((i / kNST) & 1) ^ 1, ab);
+      if (!__all_sync(0xffffffffu, okl)) break;
+      if (act && kind == 0) mbar_expect_tx(&full[stage], 2 * kPage * kD + 2 * kPage * 4);
+      __syncwarp();
+      if (act) {
+        const size_t slot0 = ((size_t)__ldg(trow + i) * p.hkv + kvh) * kPage;
+        const void* src = kind == 0   ? static_cast<const void*>(p.k_cache + slot0 * kD)
+                          : kind == 1 ? static_cast<const void*>(p.v_cache + slot0 * kD)
+                          : kind == 2 ? static_cast<const void*>(p.k_scale + slot0)
+                                      : static_cast<const void*>(p.v_scale + slot0);
+        bulk_load(smem + stage * kStage + dst_off, src, bytes, &full[stage]);
       }
     }
     return;
