@@ -41,9 +41,9 @@ LAUNCHES_PER_DECODE = 2
 # summarised in profiles/ (prefill_kernels_varlen_gqa_8192_d128.md,
 # decode_kernels_paged_fp8_decode_64x1.md); set back to None whenever the kernel changes.
 NCU_TRAFFIC = {
-    "bwd": None,               # prefill_bwd_dq_kernel<128> + prefill_bwd_kernel<128>: changed since capture
-    "fwd": None,               # prefill_fwd2_kernel<128>: not captured since it replaced prefill_fwd_kernel
-    "decode_split": 1188.2e6,  # decode_split_kernel
+    "bwd": 217.9e6 + 277.0e6,  # prefill_bwd_dq_kernel<128> + prefill_bwd_kernel<128>
+    "fwd": 119.8e6,            # prefill_fwd2_kernel<128>
+    "decode_split": 1188.9e6,  # decode_split_kernel
 }
 
 
