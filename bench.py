@@ -151,15 +151,21 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(world, x):
+def max_over_ranks(world, x, device="cuda"):
+    """Maximum of a per-rank host value over all ranks (the timed region of the slowest rank)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
 
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_rate(units_per_rank, world, seconds_max):
+    """Whole-job throughput of `world` independent replicas: every rank's units over the slowest rank's time."""
+    return units_per_rank * world / seconds_max
 
 
 # ----------------------------------------------------------------------------- native arm
@@ -217,7 +223,7 @@ def run_native(args):
     ms_step = ms_total / K
     fwd_k = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     bwd_k = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
-    value = step_fl * world / (ms_total / K * 1e-3) / 1e12
+    value = whole_job_rate(step_fl, world, ms_total / K * 1e-3) / 1e12
     if gcs.get_device_status() != 0:
         raise RuntimeError("a kernel timed out during the timed region")
 
@@ -265,7 +271,7 @@ def run_native(args):
     torch.cuda.synchronize()
     barrier(world)
     e2e_ms = max_over_ranks(world, e0.elapsed_time(e1)) / K
-    e2e = {"value": round(step_fl * world / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+    e2e = {"value": round(whole_job_rate(step_fl, world, e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
     del q, k, v, do, g, s, cu
     torch.cuda.empty_cache()
