@@ -164,17 +164,38 @@ def prefill_backward(q, k, v, do, cu_seqlens, scale, log_gate=None, sink=None, w
 
 
 # ----------------------------------------------------------------------------- decode
-def gather_kv(cache_codes, scales, block_table_row, L, kv_head):
-    """Dequantized keys (or values) 0..L-1 of one request and kv head: e4m3 value times
-    the per-token scale ([AIT] Technical details, layout [num_blocks, num_kv_heads,
-    block_size]).  Slots at or past L are never read."""
-    bs = cache_codes.shape[2]
+def _token_values(cache, scales, blocks, kv_head, L):
+    """Stored values and scales of tokens 0..L-1 of one request and kv head, before scaling:
+    an e4m3 cache (uint8 codes) with one fp32 scale per token ([AIT] Technical details,
+    layout [num_blocks, num_kv_heads, block_size]) or one per tensor (the older path the
+    same section keeps: "Per-tensor scales use the same code as before"); or a bf16 cache
+    ([AIT] commit 3, the bf16-KV route) with no scales.  Slots at or past L are never read.
+    Returns (values [L, d], scales [L]) in float64."""
+    bs = cache.shape[2]
+    npages = len(blocks)
+    raw = np.asarray(cache[blocks, kv_head])  # [npages, bs, d]
+    if raw.dtype == np.uint8:
+        vals = e4m3_decode(raw.reshape(npages * bs, -1)[:L])
+        sc = np.asarray(scales, dtype=np.float64)
+        if sc.size == 1:
+            sc = np.full(L, float(sc.reshape(-1)[0]))
+        else:
+            sc = sc[blocks, kv_head].reshape(-1)[:L]
+    else:
+        assert scales is None, "a bf16 cache has no scales"
+        vals = raw.astype(np.float64).reshape(npages * bs, -1)[:L]
+        sc = np.ones(L)
+    return vals, sc
+
+
+def gather_kv(cache, scales, block_table_row, L, kv_head):
+    """Dequantized keys (or values) 0..L-1 of one request and kv head: stored value times
+    its scale (see _token_values)."""
+    bs = cache.shape[2]
     npages = (L + bs - 1) // bs
     blocks = np.asarray(block_table_row[:npages], dtype=np.int64)
-    codes = np.asarray(cache_codes[blocks, kv_head])  # [npages, bs, d]
-    sc = np.asarray(scales[blocks, kv_head], dtype=np.float64)  # [npages, bs]
-    vals = e4m3_decode(codes.reshape(npages * bs, -1)[:L])
-    return vals * sc.reshape(-1)[:L, None]
+    vals, sc = _token_values(cache, scales, blocks, kv_head, L)
+    return vals * sc[:, None]
 
 
 def decode_paged(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu_q, scale):
@@ -231,10 +252,8 @@ def decode_partials(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens
         npages = (L + bs - 1) // bs
         blocks = np.asarray(block_table[r][:npages], dtype=np.int64)
         for kvh in range(hkv):
-            k8 = e4m3_decode(np.asarray(k_cache[blocks, kvh]).reshape(npages * bs, d)[:L])
-            v8 = e4m3_decode(np.asarray(v_cache[blocks, kvh]).reshape(npages * bs, d)[:L])
-            ks = np.asarray(k_scale[blocks, kvh], np.float64).reshape(-1)[:L]
-            vs = np.asarray(v_scale[blocks, kvh], np.float64).reshape(-1)[:L]
+            k8, ks = _token_values(k_cache, k_scale, blocks, kvh, L)
+            v8, vs = _token_values(v_cache, v_scale, blocks, kvh, L)
             for sg in range(nseg):
                 j0, j1 = sg * segment_len, min((sg + 1) * segment_len, L)
                 acc = np.zeros((ql, group, d))

@@ -165,12 +165,14 @@ class DecodeCase:
     cu_q: torch.Tensor  # int32 [R + 1]
     seq_lens: torch.Tensor  # int32 [R]
     block_table: torch.Tensor  # int32 [R, max_blocks]
-    k_cache: torch.Tensor  # uint8 (fp8 e4m3 codes) [num_blocks, hkv, block_size, d]
-    v_cache: torch.Tensor  # uint8 [num_blocks, hkv, block_size, d]
-    k_scale: torch.Tensor  # fp32 [num_blocks, hkv, block_size]
-    v_scale: torch.Tensor  # fp32 [num_blocks, hkv, block_size]
+    k_cache: torch.Tensor  # uint8 (fp8 e4m3 codes) or bf16 [num_blocks, hkv, block_size, d]
+    v_cache: torch.Tensor  # same
+    k_scale: Optional[torch.Tensor]  # fp32 [num_blocks, hkv, block_size] (per token) or [1] (per tensor); None for bf16
+    v_scale: Optional[torch.Tensor]
     scale: float
     segment_len: int
+    kv_format: str = "fp8"  # "fp8" (e4m3 codes and scales) or "bf16" (values, no scales)
+    scale_mode: str = "per_token"  # "per_token" or "per_tensor" (fp8 only)
 
     @property
     def num_reqs(self) -> int:
@@ -212,6 +214,8 @@ def make_decode(
     scale: Optional[float] = None,
     segment_len: int = 2048,
     name: str = "decode",
+    kv_format: str = "fp8",
+    scale_mode: str = "per_token",
 ) -> DecodeCase:
     """Draw order: q N(0,1) -> bf16; a random permutation of the physical blocks (the page
     table); then per request: K scales, V scales (log-uniform over a 20x range), K normals,
@@ -222,7 +226,14 @@ def make_decode(
     magnitudes differ up to 20x between tokens).  Unused slots of used pages and every
     slot of unreferenced pages hold NaN scales and the NaN code 0x7F; unused page-table
     entries point at spare (all-NaN) blocks.
+
+    kv_format "bf16": the cache holds bf16 values z ~ N(0,1) and no scales (NaN in unused
+    slots).  scale_mode "per_tensor" (fp8): one K and one V scale for the whole cache, drawn
+    once from logU[1/64, 20/64] after the page table, codes e4m3(z / scale).  Both draw
+    orders are otherwise those above, so the default cases are unchanged.
     """
+    assert kv_format in ("fp8", "bf16") and scale_mode in ("per_token", "per_tensor")
+    assert not (kv_format == "bf16" and scale_mode != "per_token")
     rng = np.random.Generator(np.random.PCG64(seed))
     seq_lens = [int(x) for x in seq_lens]
     q_lens = [int(x) for x in q_lens]
@@ -248,6 +259,9 @@ def make_decode(
         table[r, pages[r] :] = fill
         pos += pages[r]
 
+    if kv_format == "bf16" or scale_mode == "per_tensor":
+        return _make_decode_variant(rng, seq_lens, q_lens, cu_q, q, table, pages, num_blocks, hkv, d, block_size,
+                                    scale, segment_len, name, kv_format, scale_mode)
     k_cache = np.full((num_blocks, hkv, block_size, d), E4M3_NAN_CODE, dtype=np.uint8)
     v_cache = np.full((num_blocks, hkv, block_size, d), E4M3_NAN_CODE, dtype=np.uint8)
     k_sc = np.full((num_blocks, hkv, block_size), np.nan, dtype=np.float32)
@@ -290,6 +304,51 @@ def make_decode(
     )
 
 
+def _make_decode_variant(rng, seq_lens, q_lens, cu_q, q, table, pages, num_blocks, hkv, d, block_size, scale,
+                         segment_len, name, kv_format, scale_mode) -> DecodeCase:
+    """bf16 cache, or fp8 codes with one K and one V scale (see make_decode)."""
+    R = len(seq_lens)
+    if kv_format == "bf16":
+        k_cache = np.full((num_blocks, hkv, block_size, d), np.nan, dtype=np.float32)
+        v_cache = np.full((num_blocks, hkv, block_size, d), np.nan, dtype=np.float32)
+        k_sc = v_sc = None
+    else:
+        k_cache = np.full((num_blocks, hkv, block_size, d), E4M3_NAN_CODE, dtype=np.uint8)
+        v_cache = np.full((num_blocks, hkv, block_size, d), E4M3_NAN_CODE, dtype=np.uint8)
+        lo, hi = 1.0 / 64, 20.0 / 64
+        k_sc = np.exp(rng.uniform(math.log(lo), math.log(hi), size=1)).astype(np.float32)
+        v_sc = np.exp(rng.uniform(math.log(lo), math.log(hi), size=1)).astype(np.float32)
+    for r in range(R):
+        L, P = seq_lens[r], pages[r]
+        blocks = table[r, :P]
+        for cache, sc in ((k_cache, k_sc), (v_cache, v_sc)):
+            z = rng.standard_normal((L, hkv, d), dtype=np.float32)
+            pad = P * block_size - L
+            if kv_format == "bf16":
+                vals = _bf16(z).float().numpy()
+                vals = np.concatenate([vals, np.full((pad, hkv, d), np.nan, np.float32)], axis=0)
+            else:
+                vals = _e4m3_codes(z / sc[0]).numpy()
+                vals = np.concatenate([vals, np.full((pad, hkv, d), E4M3_NAN_CODE, np.uint8)], axis=0)
+            cache[blocks] = vals.reshape(P, block_size, hkv, d).transpose(0, 2, 1, 3)
+    as_cache = (lambda a: torch.from_numpy(a).to(torch.bfloat16)) if kv_format == "bf16" else torch.from_numpy
+    return DecodeCase(
+        name=name,
+        q=q,
+        cu_q=torch.from_numpy(cu_q),
+        seq_lens=torch.tensor(seq_lens, dtype=torch.int32),
+        block_table=torch.from_numpy(table),
+        k_cache=as_cache(k_cache),
+        v_cache=as_cache(v_cache),
+        k_scale=None if k_sc is None else torch.from_numpy(k_sc),
+        v_scale=None if v_sc is None else torch.from_numpy(v_sc),
+        scale=float(scale if scale is not None else 1.0 / math.sqrt(d)),
+        segment_len=int(segment_len),
+        kv_format=kv_format,
+        scale_mode=scale_mode,
+    )
+
+
 def _c5a_lengths(seed: int, n: int = 64, max_len: int = 32768) -> list[int]:
     rng = np.random.Generator(np.random.PCG64(seed))
     return [int(x) for x in rng.integers(1, max_len + 1, size=n)]
@@ -307,8 +366,9 @@ DECODE_CONFIGS = {
 }
 
 
-def decode_config(name: str, scale_reading: str = "A") -> DecodeCase:
+def decode_config(name: str, scale_reading: str = "A", kv_format: str = "fp8",
+                  scale_mode: str = "per_token") -> DecodeCase:
     cfg = dict(DECODE_CONFIGS[name])
     if cfg["seq_lens"] is None:
         cfg["seq_lens"] = _c5a_lengths(cfg["seed"] + 1000)
-    return make_decode(name=name, scale_reading=scale_reading, **cfg)
+    return make_decode(name=name, scale_reading=scale_reading, kv_format=kv_format, scale_mode=scale_mode, **cfg)

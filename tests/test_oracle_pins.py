@@ -343,3 +343,68 @@ def test_decode_never_reads_unused_slots():
     assert np.isfinite(out).all()
     # unused slots and spare pages are NaN-poisoned by the generator
     assert np.isnan(dc.k_scale.numpy()).any() and (dc.v_cache.numpy() == 0x7F).any()
+
+
+# ------------------------------------------------------------- decode variants (bf16 KV, per-tensor scales)
+def _variant_args(dc):
+    kc = dc.k_cache.float().numpy() if dc.kv_format == "bf16" else dc.k_cache.numpy()
+    vc = dc.v_cache.float().numpy() if dc.kv_format == "bf16" else dc.v_cache.numpy()
+    ks = None if dc.k_scale is None else dc.k_scale.numpy()
+    vs = None if dc.v_scale is None else dc.v_scale.numpy()
+    return (f64(dc.q), kc, vc, ks, vs, dc.block_table.numpy(), dc.seq_lens.numpy(), dc.cu_q.numpy(), dc.scale)
+
+
+def _sdpa_decode(dc):
+    """Independent reference: gather each request's pages by indexing the table, dequantize
+    with torch's own float8_e4m3fn (or take the bf16 values), and run fp64 SDPA with the
+    bottom-right causal mask of a short query (row t of q_len sits at L - q_len + t)."""
+    out = torch.zeros(dc.q.shape, dtype=torch.float64)
+    group = dc.hq // dc.hkv
+    for r, L in enumerate(dc.seq_lens.tolist()):
+        q0, q1 = int(dc.cu_q[r]), int(dc.cu_q[r + 1])
+        ql = q1 - q0
+        npg = (L + dc.block_size - 1) // dc.block_size
+        blocks = dc.block_table[r, :npg].long()
+
+        def dequant(cache, sc):
+            x = cache[blocks]  # [npg, hkv, bs, d]
+            if dc.kv_format == "bf16":
+                v = x.double()
+            else:
+                v = x.view(torch.float8_e4m3fn).double() * float(sc.reshape(-1)[0])
+            return v.permute(1, 0, 2, 3).reshape(dc.hkv, npg * dc.block_size, dc.d)[:, :L]
+
+        K, V = dequant(dc.k_cache, dc.k_scale), dequant(dc.v_cache, dc.v_scale)
+        K, V = K.repeat_interleave(group, 0), V.repeat_interleave(group, 0)  # [hq, L, d]
+        q = dc.q[q0:q1].double().transpose(0, 1)  # [hq, ql, d]
+        mask = torch.arange(L)[None, :] <= (L - ql + torch.arange(ql))[:, None]
+        out[q0:q1] = F.scaled_dot_product_attention(q, K, V, attn_mask=mask, scale=dc.scale).transpose(0, 1)
+    return out.numpy()
+
+
+@pytest.mark.parametrize("fmt", [("bf16", "per_token"), ("fp8", "per_tensor")])
+def test_decode_variants_equal_sdpa_and_splitk(fmt):
+    kv_format, scale_mode = fmt
+    dc = make_decode([1, 17, 40, 70, 33], [1, 2, 4, 3, 4], hq=8, hkv=2, d=16, seed=34, kv_format=kv_format,
+                     scale_mode=scale_mode)
+    args = _variant_args(dc)
+    out = oracle.decode_paged(*args)
+    assert np.isfinite(out).all()  # NaN-poisoned unused slots are never read
+    np.testing.assert_allclose(out, _sdpa_decode(dc), rtol=0, atol=1e-12)
+    for seg in (2048, 16, 3):
+        parts = oracle.decode_partials(*args, seg)
+        res = oracle.decode_combine(parts, dc.q.shape[0], dc.hq, dc.d, dc.cu_q.numpy(), dc.hkv)
+        np.testing.assert_allclose(res, out, rtol=0, atol=1e-12)
+
+
+def test_decode_per_tensor_scale_is_one_scale_for_every_token():
+    # scaling every code by the one K scale: doubling it doubles every score (one scale, not per token)
+    dc = make_decode([33, 50], [1, 2], hq=4, hkv=2, d=8, seed=35, scale_mode="per_tensor")
+    a = list(_variant_args(dc))
+    b = list(a)
+    b[3] = a[3] * 2.0
+    b[8] = a[8] / 2.0
+    np.testing.assert_allclose(oracle.decode_paged(*a), oracle.decode_paged(*b), rtol=0, atol=1e-12)
+    c = list(a)
+    c[4] = a[4] * 4.0  # the V scale multiplies the output linearly (a power of two keeps the fp32 scale exact)
+    np.testing.assert_allclose(oracle.decode_paged(*c), 4.0 * oracle.decode_paged(*a), rtol=1e-12, atol=1e-12)
