@@ -88,7 +88,13 @@ class DecodeArgs(ctypes.Structure):
         ("scale", _c_float),
         ("segment_len", _c_int),
         ("q", _vp),
+        ("kv_format", _c_int),
+        ("scale_mode", _c_int),
     ]
+
+
+KV_FP8_E4M3, KV_BF16 = 0, 1
+SCALE_PER_TOKEN, SCALE_PER_TENSOR = 0, 1
 
 
 class GcsError(RuntimeError):
@@ -165,6 +171,8 @@ def _stream() -> int:
 
 
 def _need(t: torch.Tensor, dtype, name: str) -> torch.Tensor:
+    if t is None:
+        raise ValueError(f"{name} is required")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
     if t.dtype != dtype:
@@ -269,23 +277,39 @@ def attn_bwd(q, k, v, o, lse, dout, cu_seqlens, max_seqlen=None, scale=None, win
 
 def decode_args(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu_q, max_q_len, max_seq_len, scale,
                 segment_len) -> DecodeArgs:
+    """Marshals the decode arguments.  The cache format follows the cache dtype (fp8 e4m3 as
+    uint8 or float8_e4m3fn, or bf16); fp8 scales are per token when they have the page shape
+    [num_blocks, num_kv_heads, block_size] and per tensor when they hold one value; a bf16
+    cache takes no scales.  Any other scale shape raises NotImplementedError."""
     _need(q, torch.bfloat16, "q")
     if k_cache.dtype == torch.float8_e4m3fn:
         k_cache = k_cache.view(torch.uint8)
     if v_cache.dtype == torch.float8_e4m3fn:
         v_cache = v_cache.view(torch.uint8)
-    _need(k_cache, torch.uint8, "k_cache")
-    _need(v_cache, torch.uint8, "v_cache")
-    _need(k_scale, torch.float32, "k_scale")
-    _need(v_scale, torch.float32, "v_scale")
     _need(block_table, torch.int32, "block_table")
     _need(seq_lens, torch.int32, "seq_lens")
     _need(cu_q, torch.int32, "cu_q")
-    nb, hkv, bs, d = k_cache.shape
-    if tuple(k_scale.shape) != (nb, hkv, bs) or tuple(v_scale.shape) != (nb, hkv, bs):
-        raise NotImplementedError("per-token scales must have the page shape [num_blocks, num_kv_heads, block_size]")
     if tuple(v_cache.shape) != tuple(k_cache.shape):
         raise ValueError("k_cache and v_cache shapes differ")
+    nb, hkv, bs, d = k_cache.shape
+    if k_cache.dtype == torch.bfloat16:
+        _need(v_cache, torch.bfloat16, "v_cache")
+        if k_scale is not None or v_scale is not None:
+            raise ValueError("a bf16 KV cache takes no scales")
+        kv_format, scale_mode, ks_ptr, vs_ptr = KV_BF16, SCALE_PER_TOKEN, None, None
+    else:
+        _need(k_cache, torch.uint8, "k_cache")
+        _need(v_cache, torch.uint8, "v_cache")
+        _need(k_scale, torch.float32, "k_scale")
+        _need(v_scale, torch.float32, "v_scale")
+        if tuple(k_scale.shape) == (nb, hkv, bs) and tuple(v_scale.shape) == (nb, hkv, bs):
+            scale_mode = SCALE_PER_TOKEN
+        elif k_scale.numel() == 1 and v_scale.numel() == 1:
+            scale_mode = SCALE_PER_TENSOR
+        else:
+            raise NotImplementedError("fp8 scales must have the page shape [num_blocks, num_kv_heads, block_size] "
+                                      "(per token) or hold one value (per tensor)")
+        kv_format, ks_ptr, vs_ptr = KV_FP8_E4M3, k_scale.data_ptr(), v_scale.data_ptr()
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     return DecodeArgs(
@@ -299,8 +323,8 @@ def decode_args(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu
         max_blocks_per_req=block_table.shape[1],
         k_cache=k_cache.data_ptr(),
         v_cache=v_cache.data_ptr(),
-        k_scale=k_scale.data_ptr(),
-        v_scale=v_scale.data_ptr(),
+        k_scale=ks_ptr,
+        v_scale=vs_ptr,
         num_blocks=nb,
         block_size=bs,
         hq=q.shape[1],
@@ -309,6 +333,8 @@ def decode_args(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu
         scale=float(scale),
         segment_len=int(segment_len),
         q=q.data_ptr(),
+        kv_format=kv_format,
+        scale_mode=scale_mode,
     )
 
 

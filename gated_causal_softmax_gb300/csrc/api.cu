@@ -322,18 +322,31 @@ static int check_decode(const gcs_decode_args* a) {
   if (a->num_reqs < 1 || a->total_q < 1 || a->max_q_len < 1 || a->max_seq_len < 1 || a->max_blocks_per_req < 1 ||
       a->num_blocks < 1 || a->hq < 1 || a->hkv < 1 || a->segment_len < 1)
     return GCS_ERR_INVALID_ARG;
-  if (!a->cu_q || !a->seq_lens || !a->block_table || !a->k_cache || !a->v_cache || !a->k_scale || !a->v_scale ||
-      !a->q)
+  if (!a->cu_q || !a->seq_lens || !a->block_table || !a->k_cache || !a->v_cache || !a->q)
     return GCS_ERR_INVALID_ARG;
   if (!std::isfinite(a->scale)) return GCS_ERR_INVALID_ARG;
+  if (a->kv_format == GCS_KV_BF16) {
+    // a bf16 cache carries no scales
+    if (a->k_scale || a->v_scale || a->scale_mode != GCS_SCALE_PER_TOKEN) return GCS_ERR_INVALID_ARG;
+  } else if (a->kv_format == GCS_KV_FP8_E4M3) {
+    if (!a->k_scale || !a->v_scale) return GCS_ERR_INVALID_ARG;
+    if (a->scale_mode == GCS_SCALE_PER_TOKEN) {
+      if (!aligned16(a->k_scale) || !aligned16(a->v_scale)) return GCS_ERR_INVALID_ARG;
+    } else if (a->scale_mode == GCS_SCALE_PER_TENSOR) {
+      if ((reinterpret_cast<uintptr_t>(a->k_scale) | reinterpret_cast<uintptr_t>(a->v_scale)) & 3u)
+        return GCS_ERR_INVALID_ARG;
+    } else {
+      return GCS_ERR_INVALID_ARG;
+    }
+  } else {
+    return GCS_ERR_INVALID_ARG;
+  }
   // per-token scales are only read on decode / short-query shapes (a prefill shape is rejected)
   if (a->max_q_len > 4) return GCS_ERR_UNSUPPORTED;
   if (a->d != 128 || a->block_size != 16 || a->hq != 16 * a->hkv) return GCS_ERR_UNSUPPORTED;
   if (a->segment_len % a->block_size != 0) return GCS_ERR_UNSUPPORTED;
   if (a->max_blocks_per_req * a->block_size < a->max_seq_len) return GCS_ERR_INVALID_ARG;
-  if (!aligned16(a->k_cache) || !aligned16(a->v_cache) || !aligned16(a->k_scale) || !aligned16(a->v_scale) ||
-      !aligned16(a->q))
-    return GCS_ERR_INVALID_ARG;
+  if (!aligned16(a->k_cache) || !aligned16(a->v_cache) || !aligned16(a->q)) return GCS_ERR_INVALID_ARG;
   if ((double)a->num_blocks * a->hkv * a->block_size * a->d > 9.0e15) return GCS_ERR_UNSUPPORTED;
   return GCS_OK;
 }
@@ -368,10 +381,12 @@ int attn_decode_paged(const gcs_decode_args* a, void* out, void* workspace, size
   p.seq_lens = a->seq_lens;
   p.block_table = a->block_table;
   p.max_blocks = a->max_blocks_per_req;
-  p.k_cache = a->k_cache;
-  p.v_cache = a->v_cache;
+  p.k_cache = static_cast<const uint8_t*>(a->k_cache);
+  p.v_cache = static_cast<const uint8_t*>(a->v_cache);
   p.k_scale = a->k_scale;
   p.v_scale = a->v_scale;
+  p.kv_format = a->kv_format;
+  p.scale_mode = a->scale_mode;
   p.num_reqs = a->num_reqs;
   p.hq = a->hq;
   p.hkv = a->hkv;

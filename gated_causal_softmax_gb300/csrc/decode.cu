@@ -36,9 +36,16 @@ std::mutex g_noalloc_mu;
 constexpr int kPage = 16;
 constexpr int kD = 128;
 constexpr int kGroup = 16;
-constexpr int kStage = 4352;  // K 2048 | V 2048 | kscale 64 | vscale 64 | pad
-constexpr int kNST = 16;
-constexpr int kBatch = 8;  // pages the producer warp issues per round (4 copies each, one per lane)
+// Ring layout per cache format.  fp8: stage = K 2048 | V 2048 | K scales 64 | V scales 64 | pad,
+// 16 stages, 8 pages per producer round.  bf16: stage = K 4096 | V 4096, 8 stages, 4 pages per
+// round (three CTAs per SM either way).
+template <int KVF>
+struct DecCfg {
+  static constexpr int KB = KVF == 0 ? 2048 : 4096;  // bytes of one page of K (or V) for one kv head
+  static constexpr int STAGE = KVF == 0 ? 4352 : 8192;
+  static constexpr int NST = KVF == 0 ? 16 : 8;
+  static constexpr int BATCH = KVF == 0 ? 8 : 4;
+};
 constexpr int kThreads = 160;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kPScale = 256.f;
@@ -74,13 +81,26 @@ __device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], u
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 __device__ __forceinline__ uint32_t bf16pair_to_f16x2(uint32_t w) {
   const float lo = __uint_as_float(w << 16);
   const float hi = __uint_as_float(w & 0xffff0000u);
   return pack_f16x2(lo, hi);
 }
 
+// KVF: 0 fp8 e4m3 codes, 1 bf16 values.  PT: one K and one V scale for the whole cache (fp8).
+template <int KVF, bool PT>
 __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeParams p) {
+  using C = DecCfg<KVF>;
+  constexpr int kNST = C::NST, kStage = C::STAGE, kBatch = C::BATCH;
+  constexpr int kKinds = (KVF == 0 && !PT) ? 4 : 2;  // copies per page: K, V (, K scales, V scales)
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint64_t full[kNST], empty[kNST];
   __shared__ int abort_flag_s;
@@ -108,24 +128,25 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
 
   if (warp == 0) {
     // ------------------------------------------------------------ page producer
-    // lane = 8 * kind + page within the round; kind 0: K, 1: V, 2: K scales, 3: V scales
+    // lane = kBatch * kind + page within the round; kind 0: K, 1: V, 2: K scales, 3: V scales
     const int32_t* trow = p.block_table + (size_t)r * p.max_blocks + pb;
     const int pl = lane & (kBatch - 1), kind = lane / kBatch;
-    const uint32_t bytes = kind < 2 ? kPage * kD : kPage * 4;
-    const uint32_t dst_off = kind < 2 ? kind * 2048 : 4096 + (kind - 2) * 64;
+    const uint32_t bytes = kind < 2 ? C::KB : kPage * 4;
+    const uint32_t dst_off = kind < 2 ? kind * C::KB : 2 * C::KB + (kind - 2) * 64;
+    constexpr uint32_t kTx = 2 * C::KB + (kKinds == 4 ? 2 * kPage * 4 : 0);
     for (int base = 0; base < np; base += kBatch) {
       const int i = base + pl;
-      const bool act = i < np;
+      const bool act = i < np && kind < kKinds;
       const int stage = i % kNST;
       bool okl = true;
       if (act) okl = wait_bar(&empty[stage], ((i / kNST) & 1) ^ 1, ab);
       if (!__all_sync(0xffffffffu, okl)) break;
-      if (act && kind == 0) mbar_expect_tx(&full[stage], 2 * kPage * kD + 2 * kPage * 4);
+      if (act && kind == 0) mbar_expect_tx(&full[stage], kTx);
       __syncwarp();
       if (act) {
         const size_t slot0 = ((size_t)__ldg(trow + i) * p.hkv + kvh) * kPage;
-        const void* src = kind == 0   ? static_cast<const void*>(p.k_cache + slot0 * kD)
-                          : kind == 1 ? static_cast<const void*>(p.v_cache + slot0 * kD)
+        const void* src = kind == 0   ? static_cast<const void*>(p.k_cache + slot0 * (C::KB / kPage))
+                          : kind == 1 ? static_cast<const void*>(p.v_cache + slot0 * (C::KB / kPage))
                           : kind == 2 ? static_cast<const void*>(p.k_scale + slot0)
                                       : static_cast<const void*>(p.v_scale + slot0);
         bulk_load(smem + stage * kStage + dst_off, src, bytes, &full[stage]);
@@ -160,51 +181,83 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
         w0[4 * j] = a.x; w0[4 * j + 1] = a.y; w0[4 * j + 2] = a.z; w0[4 * j + 3] = a.w;
         w1[4 * j] = b.x; w1[4 * j + 1] = b.y; w1[4 * j + 2] = b.z; w1[4 * j + 3] = b.w;
       }
-      // k-step s covers physical dims 32tq + 4s .. 32tq + 4s + 3 of this thread
+      // k-step s covers physical dims 32tq + 4s .. 32tq + 4s + 3 of this thread; the fp8
+      // path multiplies in f16 (exact e4m3 -> f16), the bf16 path in bf16
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
-        qa[s][0] = bf16pair_to_f16x2(w0[2 * s]);
-        qa[s][1] = bf16pair_to_f16x2(w1[2 * s]);
-        qa[s][2] = bf16pair_to_f16x2(w0[2 * s + 1]);
-        qa[s][3] = bf16pair_to_f16x2(w1[2 * s + 1]);
+        qa[s][0] = KVF == 0 ? bf16pair_to_f16x2(w0[2 * s]) : w0[2 * s];
+        qa[s][1] = KVF == 0 ? bf16pair_to_f16x2(w1[2 * s]) : w1[2 * s];
+        qa[s][2] = KVF == 0 ? bf16pair_to_f16x2(w0[2 * s + 1]) : w0[2 * s + 1];
+        qa[s][3] = KVF == 0 ? bf16pair_to_f16x2(w1[2 * s + 1]) : w1[2 * s + 1];
       }
+    }
+    // one K and one V scale for the whole cache (fp8 per-tensor)
+    const float kst = PT ? __ldg(p.k_scale) : 1.f, vst = PT ? __ldg(p.v_scale) : 1.f;
+    {
     }
     for (int i = grp; i < np; i += ng) {
       const int stage = i % kNST;
       ok = wait_bar(&full[stage], (i / kNST) & 1, ab);
       if (!ok) break;
       const uint8_t* st = smem + stage * kStage;
-      const uint4 ka0 = lds128(st + g * kD + 32 * tq);
-      const uint4 ka1 = lds128(st + g * kD + 32 * tq + 16);
-      const uint4 kb0 = lds128(st + (8 + g) * kD + 32 * tq);
-      const uint4 kb1 = lds128(st + (8 + g) * kD + 32 * tq + 16);
-      uint4 v0 = lds128(st + 2048 + (2 * tq) * kD + 16 * g);
-      uint4 v1 = lds128(st + 2048 + (2 * tq + 1) * kD + 16 * g);
-      uint4 v2 = lds128(st + 2048 + (2 * tq + 8) * kD + 16 * g);
-      uint4 v3 = lds128(st + 2048 + (2 * tq + 9) * kD + 16 * g);
-      const float2 ksA = *reinterpret_cast<const float2*>(st + 4096 + 8 * tq);
-      const float2 ksB = *reinterpret_cast<const float2*>(st + 4096 + 32 + 8 * tq);
-      const float2 vsA = *reinterpret_cast<const float2*>(st + 4160 + 8 * tq);
-      const float2 vsB = *reinterpret_cast<const float2*>(st + 4160 + 32 + 8 * tq);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[stage]);
-
-      // S = q . k8 over the page: n-tile 0 = slots 0..7, n-tile 1 = slots 8..15
       float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-      const uint32_t kw0[8] = {ka0.x, ka0.y, ka0.z, ka0.w, ka1.x, ka1.y, ka1.z, ka1.w};
-      const uint32_t kw1[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
+      float ks[4], vs[4];  // K / V scale of this thread's four columns
+      uint4 vr[4];         // fp8 value fragments: rows 2tq, 2tq+1, 2tq+8, 2tq+9 (bf16 reads values later)
+      if constexpr (KVF == 0) {
+        const uint4 ka0 = lds128(st + g * kD + 32 * tq);
+        const uint4 ka1 = lds128(st + g * kD + 32 * tq + 16);
+        const uint4 kb0 = lds128(st + (8 + g) * kD + 32 * tq);
+        const uint4 kb1 = lds128(st + (8 + g) * kD + 32 * tq + 16);
+        vr[0] = lds128(st + 2048 + (2 * tq) * kD + 16 * g);
+        vr[1] = lds128(st + 2048 + (2 * tq + 1) * kD + 16 * g);
+        vr[2] = lds128(st + 2048 + (2 * tq + 8) * kD + 16 * g);
+        vr[3] = lds128(st + 2048 + (2 * tq + 9) * kD + 16 * g);
+        if constexpr (PT) {
+          ks[0] = ks[1] = ks[2] = ks[3] = kst;
+          vs[0] = vs[1] = vs[2] = vs[3] = vst;
+        } else {
+          const float2 ksA = *reinterpret_cast<const float2*>(st + 4096 + 8 * tq);
+          const float2 ksB = *reinterpret_cast<const float2*>(st + 4096 + 32 + 8 * tq);
+          const float2 vsA = *reinterpret_cast<const float2*>(st + 4160 + 8 * tq);
+          const float2 vsB = *reinterpret_cast<const float2*>(st + 4160 + 32 + 8 * tq);
+          ks[0] = ksA.x; ks[1] = ksA.y; ks[2] = ksB.x; ks[3] = ksB.y;
+          vs[0] = vsA.x; vs[1] = vsA.y; vs[2] = vsB.x; vs[3] = vsB.y;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[stage]);
+        // S = q . k8 over the page: n-tile 0 = slots 0..7, n-tile 1 = slots 8..15
+        const uint32_t kw0[8] = {ka0.x, ka0.y, ka0.z, ka0.w, ka1.x, ka1.y, ka1.z, ka1.w};
+        const uint32_t kw1[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
 #pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        uint32_t b0, b1;
-        e4m3x4_to_f16x2x2(kw0[s], b0, b1);
-        mma_f16(s0, qa[s], b0, b1);
-        e4m3x4_to_f16x2x2(kw1[s], b0, b1);
-        mma_f16(s1, qa[s], b0, b1);
+        for (int s = 0; s < 8; ++s) {
+          uint32_t b0, b1;
+          e4m3x4_to_f16x2x2(kw0[s], b0, b1);
+          mma_f16(s0, qa[s], b0, b1);
+          e4m3x4_to_f16x2x2(kw1[s], b0, b1);
+          mma_f16(s1, qa[s], b0, b1);
+        }
+      } else {
+        // bf16 page: 16 keys x 256 B; this thread's 32 dims of keys g and g + 8 (64 B each)
+        uint32_t kw0[16], kw1[16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 a = lds128(st + g * 256 + 64 * tq + 16 * c);
+          const uint4 b = lds128(st + (8 + g) * 256 + 64 * tq + 16 * c);
+          kw0[4 * c] = a.x; kw0[4 * c + 1] = a.y; kw0[4 * c + 2] = a.z; kw0[4 * c + 3] = a.w;
+          kw1[4 * c] = b.x; kw1[4 * c + 1] = b.y; kw1[4 * c + 2] = b.z; kw1[4 * c + 3] = b.w;
+        }
+        ks[0] = ks[1] = ks[2] = ks[3] = 1.f;
+        vs[0] = vs[1] = vs[2] = vs[3] = 1.f;
+        // (values are read after the softmax and the stage is released then: fewer live registers)
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          mma_bf16(s0, qa[s], kw0[2 * s], kw0[2 * s + 1]);
+          mma_bf16(s1, qa[s], kw1[2 * s], kw1[2 * s + 1]);
+        }
       }
       // this thread's columns: slots 2tq, 2tq+1 (n-tile 0) and 8+2tq, 9+2tq (n-tile 1)
       const int tok0 = (pb + i) * kPage + 2 * tq;
       const int tk[4] = {tok0, tok0 + 1, tok0 + 8, tok0 + 9};
-      const float ks[4] = {ksA.x, ksA.y, ksB.x, ksB.y};
       float x[2][4];  // [row g / g+8][column]
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -242,39 +295,65 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
         o[u][2] *= a1;
         o[u][3] *= a1;
       }
-      // V scales multiply the probabilities after the row sum; slots >= L get scale 0
-      float vs[4] = {vsA.x, vsA.y, vsB.x, vsB.y};
+      // V scales multiply the probabilities after the row sum; slots >= L get scale 0, and
+      // their value bytes are never multiplied (NaN allowed there)
 #pragma unroll
-      for (int c = 0; c < 4; ++c) vs[c] = (tk[c] < L) ? vs[c] * kPScale : 0.f;
-      uint32_t pa[4];
-      pa[0] = pack_f16x2(pr[0][0] * vs[0], pr[0][1] * vs[1]);
-      pa[1] = pack_f16x2(pr[1][0] * vs[0], pr[1][1] * vs[1]);
-      pa[2] = pack_f16x2(pr[0][2] * vs[2], pr[0][3] * vs[3]);
-      pa[3] = pack_f16x2(pr[1][2] * vs[2], pr[1][3] * vs[3]);
-      // value bytes of slots past seq_len are never multiplied (NaN codes allowed there)
-      if (tk[0] >= L) v0 = make_uint4(0, 0, 0, 0);
-      if (tk[1] >= L) v1 = make_uint4(0, 0, 0, 0);
-      if (tk[2] >= L) v2 = make_uint4(0, 0, 0, 0);
-      if (tk[3] >= L) v3 = make_uint4(0, 0, 0, 0);
-      const uint32_t va[4] = {v0.x, v0.y, v0.z, v0.w}, vb[4] = {v1.x, v1.y, v1.z, v1.w};
-      const uint32_t vc[4] = {v2.x, v2.y, v2.z, v2.w}, vd[4] = {v3.x, v3.y, v3.z, v3.w};
+      for (int c = 0; c < 4; ++c) vs[c] = (tk[c] < L) ? vs[c] * (KVF == 0 ? kPScale : 1.f) : 0.f;
+      if constexpr (KVF == 0) {
+        uint32_t pa[4];
+        pa[0] = pack_f16x2(pr[0][0] * vs[0], pr[0][1] * vs[1]);
+        pa[1] = pack_f16x2(pr[1][0] * vs[0], pr[1][1] * vs[1]);
+        pa[2] = pack_f16x2(pr[0][2] * vs[2], pr[0][3] * vs[3]);
+        pa[3] = pack_f16x2(pr[1][2] * vs[2], pr[1][3] * vs[3]);
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        uint32_t lo01, hi01, lo23, hi23;
-        // bytes (4w, 4w+1) of slots (2tq, 2tq+1) interleaved, then bytes (4w+2, 4w+3)
-        const uint32_t ab01 = prmt(va[w], vb[w], 0x5140);
-        const uint32_t ab23 = prmt(va[w], vb[w], 0x7362);
-        const uint32_t cd01 = prmt(vc[w], vd[w], 0x5140);
-        const uint32_t cd23 = prmt(vc[w], vd[w], 0x7362);
-        uint32_t b0, b1;
-        e4m3x4_to_f16x2x2(ab01, lo01, hi01);
-        e4m3x4_to_f16x2x2(cd01, b0, b1);
-        mma_f16(o[4 * w + 0], pa, lo01, b0);
-        mma_f16(o[4 * w + 1], pa, hi01, b1);
-        e4m3x4_to_f16x2x2(ab23, lo23, hi23);
-        e4m3x4_to_f16x2x2(cd23, b0, b1);
-        mma_f16(o[4 * w + 2], pa, lo23, b0);
-        mma_f16(o[4 * w + 3], pa, hi23, b1);
+        for (int c = 0; c < 4; ++c)
+          if (tk[c] >= L) vr[c] = make_uint4(0, 0, 0, 0);
+        const uint32_t va[4] = {vr[0].x, vr[0].y, vr[0].z, vr[0].w}, vb[4] = {vr[1].x, vr[1].y, vr[1].z, vr[1].w};
+        const uint32_t vc[4] = {vr[2].x, vr[2].y, vr[2].z, vr[2].w}, vd[4] = {vr[3].x, vr[3].y, vr[3].z, vr[3].w};
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          uint32_t lo01, hi01, lo23, hi23;
+          // bytes (4w, 4w+1) of slots (2tq, 2tq+1) interleaved, then bytes (4w+2, 4w+3)
+          const uint32_t ab01 = prmt(va[w], vb[w], 0x5140);
+          const uint32_t ab23 = prmt(va[w], vb[w], 0x7362);
+          const uint32_t cd01 = prmt(vc[w], vd[w], 0x5140);
+          const uint32_t cd23 = prmt(vc[w], vd[w], 0x7362);
+          uint32_t b0, b1;
+          e4m3x4_to_f16x2x2(ab01, lo01, hi01);
+          e4m3x4_to_f16x2x2(cd01, b0, b1);
+          mma_f16(o[4 * w + 0], pa, lo01, b0);
+          mma_f16(o[4 * w + 1], pa, hi01, b1);
+          e4m3x4_to_f16x2x2(ab23, lo23, hi23);
+          e4m3x4_to_f16x2x2(cd23, b0, b1);
+          mma_f16(o[4 * w + 2], pa, lo23, b0);
+          mma_f16(o[4 * w + 3], pa, hi23, b1);
+        }
+      } else {
+        uint32_t pa[4];
+        pa[0] = pack_bf16x2(pr[0][0] * vs[0], pr[0][1] * vs[1]);
+        pa[1] = pack_bf16x2(pr[1][0] * vs[0], pr[1][1] * vs[1]);
+        pa[2] = pack_bf16x2(pr[0][2] * vs[2], pr[0][3] * vs[3]);
+        pa[3] = pack_bf16x2(pr[1][2] * vs[2], pr[1][3] * vs[3]);
+        // values of rows 2tq, 2tq+1, 2tq+8, 2tq+9 (tk[0..3]), dims 16g .. 16g + 15 (32 B each);
+        // rows at or past seq_len are zero (NaN allowed in their bytes)
+        uint32_t rw[4][8];
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+          const int row = 2 * tq + (rr & 1) + 8 * (rr >> 1);
+          uint4 a = lds128(st + 4096 + row * 256 + 32 * g), b = lds128(st + 4096 + row * 256 + 32 * g + 16);
+          if (tk[rr] >= L) a = b = make_uint4(0, 0, 0, 0);
+          rw[rr][0] = a.x; rw[rr][1] = a.y; rw[rr][2] = a.z; rw[rr][3] = a.w;
+          rw[rr][4] = b.x; rw[rr][5] = b.y; rw[rr][6] = b.z; rw[rr][7] = b.w;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[stage]);
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const uint32_t sel = (u & 1) ? 0x7632 : 0x5410;
+          const uint32_t b0 = prmt(rw[0][u >> 1], rw[1][u >> 1], sel);  // keys 2tq, 2tq + 1
+          const uint32_t b1 = prmt(rw[2][u >> 1], rw[3][u >> 1], sel);  // keys 2tq + 8, 2tq + 9
+          mma_bf16(o[u], pa, b0, b1);
+        }
       }
     }
     l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
@@ -330,6 +409,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
     }
   }
   if (active && grp == 0) {
+    constexpr float kOut = KVF == 0 ? kInvPScale : 1.f;  // the fp8 path carries P scaled by 2^8
     const size_t unit = ((size_t)r * p.max_segs + seg) * p.hkv + kvh;
     const int rows = p.max_q_len * kGroup;
     const size_t row0 = unit * rows + mt * kGroup + g;
@@ -337,14 +417,14 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
     float4* d1 = reinterpret_cast<float4*>(p.part_acc + (row0 + 8) * kD + 32 * tq);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      d0[k] = make_float4(o[4 * k][0] * kInvPScale, o[4 * k + 1][0] * kInvPScale, o[4 * k + 2][0] * kInvPScale,
-                          o[4 * k + 3][0] * kInvPScale);
-      d0[4 + k] = make_float4(o[4 * k][1] * kInvPScale, o[4 * k + 1][1] * kInvPScale, o[4 * k + 2][1] * kInvPScale,
-                              o[4 * k + 3][1] * kInvPScale);
-      d1[k] = make_float4(o[4 * k][2] * kInvPScale, o[4 * k + 1][2] * kInvPScale, o[4 * k + 2][2] * kInvPScale,
-                          o[4 * k + 3][2] * kInvPScale);
-      d1[4 + k] = make_float4(o[4 * k][3] * kInvPScale, o[4 * k + 1][3] * kInvPScale,
-                              o[4 * k + 2][3] * kInvPScale, o[4 * k + 3][3] * kInvPScale);
+      d0[k] = make_float4(o[4 * k][0] * kOut, o[4 * k + 1][0] * kOut, o[4 * k + 2][0] * kOut,
+                          o[4 * k + 3][0] * kOut);
+      d0[4 + k] = make_float4(o[4 * k][1] * kOut, o[4 * k + 1][1] * kOut, o[4 * k + 2][1] * kOut,
+                              o[4 * k + 3][1] * kOut);
+      d1[k] = make_float4(o[4 * k][2] * kOut, o[4 * k + 1][2] * kOut, o[4 * k + 2][2] * kOut,
+                          o[4 * k + 3][2] * kOut);
+      d1[4 + k] = make_float4(o[4 * k][3] * kOut, o[4 * k + 1][3] * kOut,
+                              o[4 * k + 2][3] * kOut, o[4 * k + 3][3] * kOut);
     }
     if (tq == 0) {
       reinterpret_cast<float2*>(p.part_ml)[row0] = make_float2(m0, l0);
@@ -395,13 +475,21 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
 
 cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, const cudaEvent_t* ev_before,
                           const cudaEvent_t* ev_after) {
-  const int smem = kNST * kStage;
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
   dim3 g1(p.max_segs, p.hkv, p.num_reqs);
-  if (ev_before && *ev_before) cudaEventRecord(*ev_before, s);
-  decode_split_kernel<<<g1, kThreads, smem, s>>>(p);
-  e = cudaGetLastError();
+  auto run = [&](auto kern, int smem) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    if (ev_before && *ev_before) cudaEventRecord(*ev_before, s);
+    kern<<<g1, kThreads, smem, s>>>(p);
+    return cudaGetLastError();
+  };
+  cudaError_t e;
+  if (p.kv_format == 1)
+    e = run(decode_split_kernel<1, false>, DecCfg<1>::NST * DecCfg<1>::STAGE);
+  else if (p.scale_mode == 1)
+    e = run(decode_split_kernel<0, true>, DecCfg<0>::NST * DecCfg<0>::STAGE);
+  else
+    e = run(decode_split_kernel<0, false>, DecCfg<0>::NST * DecCfg<0>::STAGE);
   if (ev_after && *ev_after) cudaEventRecord(*ev_after, s);
   if (e != cudaSuccess) return e;
   dim3 g2(p.num_reqs * p.max_q_len, p.hkv);

@@ -84,10 +84,12 @@ struct DecodeParams {
   const int32_t* seq_lens;
   const int32_t* block_table;
   int max_blocks;
-  const uint8_t* k_cache;
+  const uint8_t* k_cache;  // fp8 e4m3 codes or bf16 values (kv_format)
   const uint8_t* v_cache;
-  const float* k_scale;
+  const float* k_scale;    // per token [num_blocks, hkv, 16], per tensor [1], or null (bf16)
   const float* v_scale;
+  int kv_format;           // 0: fp8 e4m3, 1: bf16
+  int scale_mode;          // 0: per token, 1: per tensor
   int num_reqs, hq, hkv;
   int max_q_len;
   int max_segs;          // segments per request slot in the partial buffers

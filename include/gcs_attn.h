@@ -110,8 +110,10 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
              gcs_stream_t stream);
 
 /* ------------------------------------------------------------------ paged decode
- * Decode / short-query attention over a paged fp8 e4m3 KV cache with per-token fp32 scales
- * ([AIT] commits 1-3, Technical details).  Request r has q_len = cu_q[r+1] - cu_q[r] query
+ * Decode / short-query attention over a paged KV cache ([AIT] commits 1-3, Technical
+ * details): fp8 e4m3 with per-token fp32 scales (the default), fp8 e4m3 with one K and one
+ * V scale for the whole cache (per-tensor; "Per-tensor scales use the same code as
+ * before"), or bf16 with no scales (the bf16-KV route of commit 3).  Request r has q_len = cu_q[r+1] - cu_q[r] query
  * rows (1..4) and seq_len = seq_lens[r] cached tokens (the query tokens are the last
  * q_len of them); query row t sits at position seq_len - q_len + t and sees keys
  * 0 .. seq_len - q_len + t.  Key j of request r lives in block block_table[r][j / block_size],
@@ -122,9 +124,13 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
  * The context is split into segments of segment_len tokens; each (request, kv head,
  * segment) yields a partial (acc, M, L) and a combine kernel merges them with weights
  * e^{M_s - max M}; a partial with no visible key (M = -inf) weighs 0.
+ * With per-tensor scales, k_scale and v_scale each point to one fp32 used for every token;
+ * with a bf16 cache, k_cache / v_cache hold bf16 values and k_scale, v_scale must be NULL.
  * Supported: d == 128, block_size == 16, hq / hkv == 16, 1 <= q_len <= 4,
  * segment_len a positive multiple of block_size.
  */
+enum { GCS_KV_FP8_E4M3 = 0, GCS_KV_BF16 = 1 };
+enum { GCS_SCALE_PER_TOKEN = 0, GCS_SCALE_PER_TENSOR = 1 };
 typedef struct {
   int num_reqs;                /* >= 1                                                   */
   const int32_t* cu_q;         /* device int32 [num_reqs + 1]                           */
@@ -134,15 +140,17 @@ typedef struct {
   int max_seq_len;             /* host upper bound on seq_lens                           */
   const int32_t* block_table;  /* device int32 [num_reqs, max_blocks_per_req]           */
   int max_blocks_per_req;      /* row stride of block_table                             */
-  const uint8_t* k_cache;      /* fp8 e4m3 [num_blocks, hkv, block_size, d]             */
-  const uint8_t* v_cache;      /* fp8 e4m3 [num_blocks, hkv, block_size, d]             */
-  const float* k_scale;        /* fp32 [num_blocks, hkv, block_size]                    */
-  const float* v_scale;        /* fp32 [num_blocks, hkv, block_size]                    */
+  const void* k_cache;         /* fp8 e4m3 or bf16 [num_blocks, hkv, block_size, d]     */
+  const void* v_cache;         /* same format as k_cache                                 */
+  const float* k_scale;        /* fp32 [num_blocks, hkv, block_size], or [1], or NULL   */
+  const float* v_scale;        /* same layout as k_scale                                 */
   int num_blocks, block_size;  /* cache blocks, tokens per block                        */
   int hq, hkv, d;              /* query heads, kv heads, head dim                       */
   float scale;                 /* softmax scale                                         */
   int segment_len;             /* split-K segment length in tokens                      */
   const void* q;               /* bf16 [total_q, hq, d]                                 */
+  int kv_format;               /* GCS_KV_FP8_E4M3 or GCS_KV_BF16                         */
+  int scale_mode;              /* GCS_SCALE_PER_TOKEN or GCS_SCALE_PER_TENSOR (fp8 only) */
 } gcs_decode_args;
 
 /* Workspace bytes attn_decode_paged needs (split-K partials). */

@@ -64,8 +64,9 @@ def bias(got, ref):
 
 def decode_dev(dc):
     dev = torch.device("cuda:0")
-    return dict(q=dc.q.to(dev), kc=dc.k_cache.to(dev), vc=dc.v_cache.to(dev), ks=dc.k_scale.to(dev),
-                vs=dc.v_scale.to(dev), bt=dc.block_table.to(dev), sl=dc.seq_lens.to(dev), cq=dc.cu_q.to(dev))
+    opt = lambda t: None if t is None else t.to(dev)
+    return dict(q=dc.q.to(dev), kc=dc.k_cache.to(dev), vc=dc.v_cache.to(dev), ks=opt(dc.k_scale),
+                vs=opt(dc.v_scale), bt=dc.block_table.to(dev), sl=dc.seq_lens.to(dev), cq=dc.cu_q.to(dev))
 
 
 def run_decode(gcs, dc, d=None):
@@ -78,6 +79,7 @@ def run_decode(gcs, dc, d=None):
 
 
 def oracle_decode(dc, rows=None):
-    return oracle.decode_paged(f64(dc.q), dc.k_cache.numpy(), dc.v_cache.numpy(), dc.k_scale.numpy(),
-                               dc.v_scale.numpy(), dc.block_table.numpy(), dc.seq_lens.numpy(), dc.cu_q.numpy(),
-                               dc.scale)
+    cache = lambda t: t.float().numpy() if t.dtype == torch.bfloat16 else t.numpy()
+    opt = lambda t: None if t is None else t.numpy()
+    return oracle.decode_paged(f64(dc.q), cache(dc.k_cache), cache(dc.v_cache), opt(dc.k_scale), opt(dc.v_scale),
+                               dc.block_table.numpy(), dc.seq_lens.numpy(), dc.cu_q.numpy(), dc.scale)

@@ -110,3 +110,12 @@ def test_decode_validation_on_host(L):
     assert dec(decode(max_blocks_per_req=10)) == 1  # table too short for max_seq_len
     assert L.attn_decode_paged(b(decode()), FAKE, None, 0, None) == 3
     assert L.attn_decode_paged(b(decode()), FAKE + 8, FAKE, 1 << 40, None) == 1
+    # cache formats and scale modes: a bf16 cache takes no scales; per-tensor scales need
+    # 4-byte alignment; unknown formats or modes are invalid
+    assert dec(decode(kv_format=1)) == 1
+    assert dec(decode(kv_format=1, k_scale=None, v_scale=None, scale_mode=1)) == 1
+    assert L.attn_decode_workspace(b(decode(kv_format=1, k_scale=None, v_scale=None))) > 0
+    assert dec(decode(scale_mode=1, k_scale=FAKE + 2)) == 1
+    assert L.attn_decode_workspace(b(decode(scale_mode=1, k_scale=FAKE + 4, v_scale=FAKE + 8))) > 0
+    assert dec(decode(scale_mode=2)) == 1
+    assert dec(decode(kv_format=2)) == 1

@@ -123,3 +123,62 @@ def make_sub(dc, reqs):
     sub.seq_lens = dc.seq_lens[reqs]
     sub.block_table = dc.block_table[reqs]
     return sub
+
+
+# ------------------------------------------------- bf16 KV cache and per-tensor fp8 scales
+VARIANTS = [("bf16", "per_token"), ("fp8", "per_tensor")]
+VARIANT_CASES = {
+    # name: (seq_lens, q_lens, hq, hkv, segment_len)
+    "page_edges_q1": ([1, 15, 16, 17, 2047, 2048, 2049, 5000], [1] * 8, 16, 1, 2048),
+    "short_query_tails_gqa": ([4, 18, 20, 2049, 4100, 65537], [4, 3, 2, 4, 3, 4], 32, 2, 2048),
+    "tiny_segments_empty_partials": ([40, 70, 5], [4, 3, 4], 16, 1, 16),
+}
+
+
+@pytest.mark.parametrize("fmt", VARIANTS)
+@pytest.mark.parametrize("name", list(VARIANT_CASES))
+def test_decode_variant_parity(gcs_lib, fmt, name):
+    sl, ql, hq, hkv, seg = VARIANT_CASES[name]
+    dc = make_decode(sl, ql, hq, hkv, 128, seed=300 + len(name), segment_len=seg, kv_format=fmt[0],
+                     scale_mode=fmt[1])
+    out = run_decode(gcs_lib, dc)
+    ref = oracle_decode(dc)
+    assert np.isfinite(f64(out)).all()
+    assert_close("out", out, ref, DECODE_RTOL)
+    assert abs(bias(out, ref)) <= DECODE_BIAS
+
+
+@pytest.mark.parametrize("fmt", VARIANTS)
+def test_decode_variant_full_size_64x1_sampled(gcs_lib, fmt):
+    dc = decode_config("paged_fp8_decode_64x1", kv_format=fmt[0], scale_mode=fmt[1])
+    out = run_decode(gcs_lib, dc)
+    pick = [0, 7, 21, 40, 63]
+    sub = make_sub(dc, pick)
+    ref = oracle_decode(sub)
+    got = f64(out)[[int(dc.cu_q[r]) for r in pick]]
+    assert_close("out", got, ref, DECODE_RTOL)
+    assert abs(bias(got, ref)) <= DECODE_BIAS
+
+
+def test_decode_bf16_gather_order_is_exact(gcs_lib):
+    """bf16 cache: one dominant key per request at a chosen slot whose value row holds the page
+    id (exact in bf16), so the output identifies the gathered (block, slot) exactly."""
+    sl = [37, 2050, 700]
+    dc = make_decode(sl, [1, 1, 1], 16, 1, 128, seed=12, kv_format="bf16")
+    kc = torch.zeros_like(dc.k_cache)
+    vc = dc.v_cache.clone()
+    q = torch.zeros_like(dc.q)
+    q[:, :, 0] = 1.0
+    picks = [5, 2049, 333]
+    for r, slot in enumerate(picks):
+        blk = int(dc.block_table[r, slot // 16])
+        kc[blk, 0, slot % 16, 0] = 1000.0
+        vc[blk, 0, slot % 16, 0] = float(blk % 64)
+        vc[blk, 0, slot % 16, 1] = float(blk // 64)
+    dc.k_cache, dc.v_cache, dc.q = kc, vc, q
+    dc.scale = 1.0
+    out = run_decode(gcs_lib, dc).float().cpu()
+    for r, slot in enumerate(picks):
+        blk = int(dc.block_table[r, slot // 16])
+        assert out[r, :, 0].eq(float(blk % 64)).all(), (r, out[r, :, 0])
+        assert out[r, :, 1].eq(float(blk // 64)).all()
