@@ -22,6 +22,10 @@ Readings where the pages leave a step open (each is also listed in the design no
     sequence in the batch.
   * decode: query row t of a request with q_len rows sits at position L - q_len + t and
     sees keys 0..L - q_len + t (bottom-right causal alignment).
+  * decode with gates keeps the cumulative log gates G of the cached tokens paged like the
+    scales, per query head: g_cache [num_blocks, hq, block_size] (natural-log units); a
+    query row's own G is the entry at its position.  The window and the sink follow the
+    prefill rules; in split-K the sink enters once, in the combine's denominator.
 
 Everything runs in float64 with dense per-(sequence, head) matrices; no blocking, no
 online softmax, no fusion.  Inputs are float64 arrays (bf16 / fp32 inputs widened
@@ -198,11 +202,33 @@ def gather_kv(cache, scales, block_table_row, L, kv_head):
     return vals * sc[:, None]
 
 
-def decode_paged(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu_q, scale):
-    """Paged decode / short-query attention over the dequantized fp8 cache, unsplit.
+def _gate_of(g_cache, block_table_row, L, h):
+    """G_j, j = 0..L-1, of one request and query head from the paged fp32 array
+    [num_blocks, hq, block_size] (reading: the cumulative log gates of the cached tokens are
+    kept paged like the scales, per query head)."""
+    bs = g_cache.shape[2]
+    npages = (L + bs - 1) // bs
+    blocks = np.asarray(block_table_row[:npages], dtype=np.int64)
+    return np.asarray(g_cache[blocks, h], dtype=np.float64).reshape(-1)[:L]
+
+
+def _visible(pos, window, lo=0, hi=None):
+    """Keys visible to a query at position pos: j <= pos (causal) and pos - j < W (window),
+    intersected with [lo, hi)."""
+    a = max(lo, pos - window + 1) if window > 0 else lo
+    b = pos + 1 if hi is None else min(hi, pos + 1)
+    return a, b
+
+
+def decode_paged(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu_q, scale, *, g_cache=None,
+                 sink=None, window=0):
+    """Paged decode / short-query attention over the dequantized cache, unsplit.
 
     q [nq, hq, d] (rows of request r are cu_q[r]..cu_q[r+1]); row t of request r sits at
-    position L - q_len + t and attends to keys 0..L - q_len + t.  Returns [nq, hq, d].
+    position L - q_len + t and attends to keys 0..L - q_len + t.  With the decoding
+    features of [FLA] Description: s_j = scale q.k_j + G_i - G_j (G from g_cache, the query's
+    own G at its position), the window keeps pos - j < W, and the sink adds e^sigma_h to the
+    denominator only.  Returns [nq, hq, d].
     """
     q = np.asarray(q, np.float64)
     nq, hq, d = q.shape
@@ -217,23 +243,31 @@ def decode_paged(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, c
         for kvh in range(hkv):
             K = gather_kv(k_cache, k_scale, block_table[r], L, kvh)
             V = gather_kv(v_cache, v_scale, block_table[r], L, kvh)
-            for t in range(ql):
-                pos = L - ql + t
-                for h in range(kvh * group, (kvh + 1) * group):
-                    s = scale * (K[: pos + 1] @ q[q0 + t, h])
-                    p = np.exp(s - s.max())
-                    out[q0 + t, h] = (p @ V[: pos + 1]) / p.sum()
+            for h in range(kvh * group, (kvh + 1) * group):
+                G = None if g_cache is None else _gate_of(g_cache, block_table[r], L, h)
+                for t in range(ql):
+                    pos = L - ql + t
+                    a, b = _visible(pos, window)
+                    s = scale * (K[a:b] @ q[q0 + t, h])
+                    if G is not None:
+                        s = s + (G[pos] - G[a:b])
+                    m = s.max() if sink is None else max(s.max(), float(sink[h]))
+                    p = np.exp(s - m)
+                    den = p.sum() + (0.0 if sink is None else math.exp(float(sink[h]) - m))
+                    out[q0 + t, h] = (p @ V[a:b]) / den
     return out
 
 
-def decode_partials(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu_q, scale, segment_len):
+def decode_partials(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu_q, scale, segment_len, *,
+                    g_cache=None, window=0):
     """Split-K partials in the pages' order ([AIT] commits and Technical details).
 
     For each (request, kv head, segment [segment_len*s, segment_len*(s+1)) of the
-    context) and each query row: s_j = scale * kscale_j * (q . k8_j); the running max m
-    and row sum l use the unscaled probabilities p_j = e^{s_j - m}; the V scales multiply
-    the P columns after the row sum: acc = sum_j (p_j vscale_j) v8_j.  A row with no
-    visible key in the segment stores (acc, m, l) = (0, -inf, 0).
+    context) and each query row: s_j = scale * kscale_j * (q . k8_j) (+ G_i - G_j with
+    gates); the running max m and row sum l use the unscaled probabilities p_j = e^{s_j - m};
+    the V scales multiply the P columns after the row sum: acc = sum_j (p_j vscale_j) v8_j.
+    A row with no visible key in the segment (past its position, or before its window)
+    stores (acc, m, l) = (0, -inf, 0).  The sink is not part of any partial.
 
     Returns a list of dicts {r, kvh, seg, acc [ql, group, d], m [ql, group], l [ql, group]}.
     """
@@ -254,31 +288,36 @@ def decode_partials(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens
         for kvh in range(hkv):
             k8, ks = _token_values(k_cache, k_scale, blocks, kvh, L)
             v8, vs = _token_values(v_cache, v_scale, blocks, kvh, L)
+            Gs = None if g_cache is None else [_gate_of(g_cache, block_table[r], L, h)
+                                               for h in range(kvh * group, (kvh + 1) * group)]
             for sg in range(nseg):
                 j0, j1 = sg * segment_len, min((sg + 1) * segment_len, L)
                 acc = np.zeros((ql, group, d))
                 m = np.full((ql, group), -np.inf)
                 l = np.zeros((ql, group))
                 for t in range(ql):
-                    last = L - ql + t  # last visible key
-                    hi = min(j1, last + 1)
-                    if hi <= j0:
+                    pos = L - ql + t
+                    a, b = _visible(pos, window, j0, j1)
+                    if b <= a:
                         continue  # empty partial
                     qq = q[q0 + t, kvh * group : (kvh + 1) * group]  # [group, d]
-                    s = scale * (qq @ k8[j0:hi].T) * ks[j0:hi][None, :]
+                    s = scale * (qq @ k8[a:b].T) * ks[a:b][None, :]
+                    if Gs is not None:
+                        s = s + np.stack([G[pos] - G[a:b] for G in Gs])
                     mm = s.max(axis=1)
                     p = np.exp(s - mm[:, None])
                     m[t] = mm
                     l[t] = p.sum(axis=1)
-                    acc[t] = (p * vs[j0:hi][None, :]) @ v8[j0:hi]
+                    acc[t] = (p * vs[a:b][None, :]) @ v8[a:b]
                 parts.append(dict(r=r, kvh=kvh, seg=sg, acc=acc, m=m, l=l))
     return parts
 
 
-def decode_combine(parts, nq, hq, d, cu_q, hkv):
-    """LSE-weighted reduce ([AIT] commit 3 / Technical details): M* = max_s m_s,
-    w_s = 0 for an empty partial (m_s = -inf) else e^{m_s - M*}, O = sum w_s acc_s /
-    sum w_s l_s.  A row whose partials are all empty gets 0."""
+def decode_combine(parts, nq, hq, d, cu_q, hkv, *, sink=None):
+    """LSE-weighted reduce ([AIT] commit 3 / Technical details): M* = max_s m_s (and the
+    sink logit when there is one), w_s = 0 for an empty partial (m_s = -inf) else
+    e^{m_s - M*}, O = sum w_s acc_s / (sum w_s l_s + e^{sigma - M*}).  A row whose partials
+    are all empty gets 0."""
     group = hq // hkv
     cu_q = np.asarray(cu_q).tolist()
     by_key = {}
@@ -288,23 +327,30 @@ def decode_combine(parts, nq, hq, d, cu_q, hkv):
     for (r, kvh), plist in by_key.items():
         q0 = cu_q[r]
         M = np.max(np.stack([p["m"] for p in plist]), axis=0)  # [ql, group]
+        if sink is not None:
+            sg = np.asarray(sink, np.float64)[kvh * group : (kvh + 1) * group][None, :]
+            M = np.maximum(M, sg)
         num = np.zeros_like(plist[0]["acc"])
         den = np.zeros_like(plist[0]["l"])
         for p in plist:
             w = np.where(np.isneginf(p["m"]), 0.0, np.exp(np.where(np.isneginf(M), 0.0, p["m"] - M)))
             num += w[:, :, None] * p["acc"]
             den += w * p["l"]
+        if sink is not None:
+            den = den + np.exp(sg - M)
         res = np.where(den[:, :, None] > 0, num / np.where(den > 0, den, 1.0)[:, :, None], 0.0)
         ql = res.shape[0]
         out[q0 : q0 + ql, kvh * group : (kvh + 1) * group] = res
     return out
 
 
-def decode_paged_splitk(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu_q, scale, segment_len):
+def decode_paged_splitk(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu_q, scale, segment_len, *,
+                        g_cache=None, sink=None, window=0):
     """Split-K decode: partials per context segment, then the LSE-weighted reduce."""
     q = np.asarray(q)
-    parts = decode_partials(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu_q, scale, segment_len)
-    return decode_combine(parts, q.shape[0], q.shape[1], q.shape[2], cu_q, k_cache.shape[1])
+    parts = decode_partials(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu_q, scale, segment_len,
+                            g_cache=g_cache, window=window)
+    return decode_combine(parts, q.shape[0], q.shape[1], q.shape[2], cu_q, k_cache.shape[1], sink=sink)
 
 
 def rel_rms(x, ref) -> float:

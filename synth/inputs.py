@@ -173,6 +173,9 @@ class DecodeCase:
     segment_len: int
     kv_format: str = "fp8"  # "fp8" (e4m3 codes and scales) or "bf16" (values, no scales)
     scale_mode: str = "per_token"  # "per_token" or "per_tensor" (fp8 only)
+    g_cache: Optional[torch.Tensor] = None  # fp32 [num_blocks, hq, block_size]: cumulative log gates G
+    sink: Optional[torch.Tensor] = None  # fp32 [hq]
+    window: int = 0
 
     @property
     def num_reqs(self) -> int:
@@ -216,6 +219,8 @@ def make_decode(
     name: str = "decode",
     kv_format: str = "fp8",
     scale_mode: str = "per_token",
+    features: bool = False,
+    window: int = 0,
 ) -> DecodeCase:
     """Draw order: q N(0,1) -> bf16; a random permutation of the physical blocks (the page
     table); then per request: K scales, V scales (log-uniform over a 20x range), K normals,
@@ -231,6 +236,11 @@ def make_decode(
     slots).  scale_mode "per_tensor" (fp8): one K and one V scale for the whole cache, drawn
     once from logU[1/64, 20/64] after the page table, codes e4m3(z / scale).  Both draw
     orders are otherwise those above, so the default cases are unchanged.
+
+    features: after every draw above, per request the log gates g ~ logsigmoid(N(3, 1)) per
+    (token, query head), G = their cumulative sum from the request's first token, stored
+    in g_cache [num_blocks, hq, block_size] (NaN in unused slots); then sink ~ N(0, 1) [hq].
+    window: the sliding window W (0 = none).
     """
     assert kv_format in ("fp8", "bf16") and scale_mode in ("per_token", "per_tensor")
     assert not (kv_format == "bf16" and scale_mode != "per_token")
@@ -260,8 +270,9 @@ def make_decode(
         pos += pages[r]
 
     if kv_format == "bf16" or scale_mode == "per_tensor":
-        return _make_decode_variant(rng, seq_lens, q_lens, cu_q, q, table, pages, num_blocks, hkv, d, block_size,
+        case = _make_decode_variant(rng, seq_lens, q_lens, cu_q, q, table, pages, num_blocks, hkv, d, block_size,
                                     scale, segment_len, name, kv_format, scale_mode)
+        return _add_decode_features(rng, case, features, window)
     k_cache = np.full((num_blocks, hkv, block_size, d), E4M3_NAN_CODE, dtype=np.uint8)
     v_cache = np.full((num_blocks, hkv, block_size, d), E4M3_NAN_CODE, dtype=np.uint8)
     k_sc = np.full((num_blocks, hkv, block_size), np.nan, dtype=np.float32)
@@ -289,7 +300,7 @@ def make_decode(
             scp = np.concatenate([sc, np.full((pad, hkv), np.nan, np.float32)], axis=0)
             cache[blocks] = codes.reshape(P, block_size, hkv, d).transpose(0, 2, 1, 3)
             scache[blocks] = scp.reshape(P, block_size, hkv).transpose(0, 2, 1)
-    return DecodeCase(
+    case = DecodeCase(
         name=name,
         q=q,
         cu_q=torch.from_numpy(cu_q),
@@ -302,6 +313,28 @@ def make_decode(
         scale=float(scale if scale is not None else 1.0 / math.sqrt(d)),
         segment_len=int(segment_len),
     )
+    return _add_decode_features(rng, case, features, window)
+
+
+def _add_decode_features(rng, case: DecodeCase, features: bool, window: int) -> DecodeCase:
+    """Gates (paged cumulative G) and sink, drawn after everything else; see make_decode."""
+    case.window = int(window)
+    if not features:
+        return case
+    num_blocks, _, bs, _ = case.k_cache.shape
+    hq = case.hq
+    g_cache = np.full((num_blocks, hq, bs), np.nan, dtype=np.float32)
+    table = case.block_table.numpy()
+    for r, L in enumerate(case.seq_lens.tolist()):
+        P = (L + bs - 1) // bs
+        z = rng.normal(3.0, 1.0, size=(L, hq))
+        g = -np.logaddexp(0.0, -z)  # logsigmoid
+        G = np.cumsum(g, axis=0).astype(np.float32)  # [L, hq]
+        Gp = np.concatenate([G, np.full((P * bs - L, hq), np.nan, np.float32)], axis=0)
+        g_cache[table[r, :P]] = Gp.reshape(P, bs, hq).transpose(0, 2, 1)
+    case.g_cache = torch.from_numpy(g_cache)
+    case.sink = torch.from_numpy(rng.standard_normal(hq).astype(np.float32))
+    return case
 
 
 def _make_decode_variant(rng, seq_lens, q_lens, cu_q, q, table, pages, num_blocks, hkv, d, block_size, scale,
@@ -367,8 +400,9 @@ DECODE_CONFIGS = {
 
 
 def decode_config(name: str, scale_reading: str = "A", kv_format: str = "fp8",
-                  scale_mode: str = "per_token") -> DecodeCase:
+                  scale_mode: str = "per_token", features: bool = False, window: int = 0) -> DecodeCase:
     cfg = dict(DECODE_CONFIGS[name])
     if cfg["seq_lens"] is None:
         cfg["seq_lens"] = _c5a_lengths(cfg["seed"] + 1000)
-    return make_decode(name=name, scale_reading=scale_reading, kv_format=kv_format, scale_mode=scale_mode, **cfg)
+    return make_decode(name=name, scale_reading=scale_reading, kv_format=kv_format, scale_mode=scale_mode,
+                       features=features, window=window, **cfg)

@@ -408,3 +408,62 @@ def test_decode_per_tensor_scale_is_one_scale_for_every_token():
     c = list(a)
     c[4] = a[4] * 4.0  # the V scale multiplies the output linearly (a power of two keeps the fp32 scale exact)
     np.testing.assert_allclose(oracle.decode_paged(*c), 4.0 * oracle.decode_paged(*a), rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------- decode with gate, window and sink
+def _feature_kwargs(dc):
+    return dict(g_cache=dc.g_cache.numpy(), sink=dc.sink.double().numpy(), window=dc.window)
+
+
+@pytest.mark.parametrize("window", [0, 5, 23])
+def test_decode_features_equal_prefill_rows(window):
+    """Decode with gates, window and sink equals the last q_len rows of the prefill oracle
+    (itself pinned to fp64 SDPA) over the same dequantized keys and values, with the
+    per-token log gates recovered as differences of the cumulative G."""
+    dc = make_decode([45, 16, 1, 33], [1, 2, 1, 4], hq=4, hkv=2, d=8, seed=36, features=True, window=window)
+    out = oracle.decode_paged(*_decode_args(dc), **_feature_kwargs(dc))
+    assert np.isfinite(out).all()
+    for r, L in enumerate(dc.seq_lens.tolist()):
+        q0, q1 = int(dc.cu_q[r]), int(dc.cu_q[r + 1])
+        ql = q1 - q0
+        K = np.stack([oracle.gather_kv(dc.k_cache.numpy(), dc.k_scale.numpy(), dc.block_table[r].numpy(), L, h)
+                      for h in range(dc.hkv)], 1)
+        V = np.stack([oracle.gather_kv(dc.v_cache.numpy(), dc.v_scale.numpy(), dc.block_table[r].numpy(), L, h)
+                      for h in range(dc.hkv)], 1)
+        npg = (L + 15) // 16
+        G = dc.g_cache[dc.block_table[r, :npg].long()].double().permute(0, 2, 1).reshape(npg * 16, dc.hq)[:L]
+        g = torch.diff(G, dim=0, prepend=torch.zeros(1, dc.hq, dtype=torch.float64)).numpy()
+        q = np.zeros((L, dc.hq, dc.d))
+        q[L - ql :] = f64(dc.q)[q0:q1]
+        o, _ = oracle.prefill_forward(q, K, V, np.array([0, L]), dc.scale, log_gate=g, sink=dc.sink.double().numpy(),
+                                      window=window)
+        np.testing.assert_allclose(out[q0:q1], o[L - ql :], rtol=1e-10, atol=1e-12)
+
+
+def test_decode_features_splitk_equals_unsplit():
+    dc = make_decode([1, 17, 40, 70, 33], [1, 2, 4, 3, 4], hq=8, hkv=2, d=16, seed=37, features=True, window=9)
+    ref = oracle.decode_paged(*_decode_args(dc), **_feature_kwargs(dc))
+    for seg in (2048, 16, 3):
+        parts = oracle.decode_partials(*_decode_args(dc), seg, g_cache=dc.g_cache.numpy(), window=dc.window)
+        if seg == 3:
+            assert any(np.isneginf(p["m"]).any() for p in parts)  # windows and short queries leave empty partials
+        out = oracle.decode_combine(parts, dc.q.shape[0], dc.hq, dc.d, dc.cu_q.numpy(), dc.hkv,
+                                    sink=dc.sink.double().numpy())
+        np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
+
+
+def test_decode_window_one_with_sink_closed_form():
+    """W = 1: each query sees only its own key, whose gate difference is 0, so
+    O = v_pos * e^s / (e^s + e^sigma)."""
+    dc = make_decode([20, 9], [1, 3], hq=4, hkv=1, d=8, seed=38, features=True, window=1)
+    out = oracle.decode_paged(*_decode_args(dc), **_feature_kwargs(dc))
+    for r, L in enumerate(dc.seq_lens.tolist()):
+        K = oracle.gather_kv(dc.k_cache.numpy(), dc.k_scale.numpy(), dc.block_table[r].numpy(), L, 0)
+        V = oracle.gather_kv(dc.v_cache.numpy(), dc.v_scale.numpy(), dc.block_table[r].numpy(), L, 0)
+        q0, q1 = int(dc.cu_q[r]), int(dc.cu_q[r + 1])
+        for t in range(q1 - q0):
+            pos = L - (q1 - q0) + t
+            for h in range(dc.hq):
+                s = dc.scale * float(K[pos] @ f64(dc.q)[q0 + t, h])
+                w = 1.0 / (1.0 + math.exp(float(dc.sink[h]) - s))
+                np.testing.assert_allclose(out[q0 + t, h], V[pos] * w, rtol=1e-12, atol=1e-14)
