@@ -72,11 +72,14 @@ def prefill_flops(seqlens, hq, dqk, dv, window=0):
     return 2 * (dqk + dv) * p, 2 * (3 * dqk + 2 * dv) * p
 
 
-def decode_bytes(seq_lens, q_lens, hq, hkv, d, block_size, kv_format="fp8", scale_mode="per_token"):
+def decode_bytes(seq_lens, q_lens, hq, hkv, d, block_size, kv_format="fp8", scale_mode="per_token", gates=False):
     """K and V bytes (1 B/elem fp8, 2 B/elem bf16) + K and V scales (4 B each, per-token fp8
-    only) per (token, kv head), q and out (bf16), page-table entries and seq_lens."""
+    only) + the cumulative gates of the group's query heads (4 B each, with gates) per (token,
+    kv head), q and out (bf16), page-table entries and seq_lens."""
     per_tok = (2 * d + 2 * 4) if kv_format == "fp8" and scale_mode == "per_token" else \
         (2 * d if kv_format == "fp8" else 2 * 2 * d)
+    if gates:
+        per_tok += 4 * (hq // hkv)
     kv = sum(seq_lens) * hkv * per_tok
     qo = 2 * sum(q_lens) * hq * d * 2
     table = 4 * sum((L + block_size - 1) // block_size for L in seq_lens)
@@ -330,16 +333,20 @@ def run_native(args):
 
     # ------------------------------------------------ decode variants: bf16 KV, per-tensor fp8
     variants = {}
-    for key, fmt, smode in (("bf16_kv", "bf16", "per_token"), ("fp8_per_tensor", "fp8", "per_tensor")):
-        vc = decode_config(DECODE_WORKLOAD, kv_format=fmt, scale_mode=smode)
+    for key, fmt, smode, feat in (("bf16_kv", "bf16", "per_token", False),
+                                  ("fp8_per_tensor", "fp8", "per_tensor", False),
+                                  ("fp8_gates_sink", "fp8", "per_token", True)):
+        vc = decode_config(DECODE_WORKLOAD, kv_format=fmt, scale_mode=smode, features=feat)
         opt = lambda t: None if t is None else t.to(dev)
         vd = dict(q=vc.q.to(dev), kc=vc.k_cache.to(dev), vc=vc.v_cache.to(dev), ks=opt(vc.k_scale),
-                  vs=opt(vc.v_scale), bt=vc.block_table.to(dev), sl=vc.seq_lens.to(dev), cq=vc.cu_q.to(dev))
+                  vs=opt(vc.v_scale), bt=vc.block_table.to(dev), sl=vc.seq_lens.to(dev), cq=vc.cu_q.to(dev),
+                  g=opt(vc.g_cache), sink=opt(vc.sink))
         vout = torch.empty_like(vd["q"])
 
         def vstep(vd=vd, vc=vc, vout=vout):
             gcs.attn_decode_paged(vd["q"], vd["kc"], vd["vc"], vd["ks"], vd["vs"], vd["bt"], vd["sl"], vd["cq"], 1,
-                                  int(vc.seq_lens.max()), vc.scale, vc.segment_len, out=vout)
+                                  int(vc.seq_lens.max()), vc.scale, vc.segment_len, out=vout, g_cache=vd["g"],
+                                  sink=vd["sink"], window=vc.window)
 
         for _ in range(args.warmup):
             vstep()
@@ -353,7 +360,7 @@ def run_native(args):
         torch.cuda.synchronize()
         barrier(world)
         v_ms = max_over_ranks(world, v0.elapsed_time(v1)) / DK
-        vbytes = decode_bytes(vc.seq_lens.tolist(), vc.q_lens, vc.hq, vc.hkv, vc.d, vc.block_size, fmt, smode)
+        vbytes = decode_bytes(vc.seq_lens.tolist(), vc.q_lens, vc.hq, vc.hkv, vc.d, vc.block_size, fmt, smode, feat)
         vgbs = vbytes * world / (v_ms * 1e-3) / 1e9
         variants[key] = {"value": round(vgbs, 1), "unit": "GB/s", "frac_of_hbm": round(vgbs / world / hbm, 4),
                          "ms_per_call": round(v_ms, 4), "bytes_per_call": vbytes}

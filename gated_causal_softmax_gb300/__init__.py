@@ -90,6 +90,9 @@ class DecodeArgs(ctypes.Structure):
         ("q", _vp),
         ("kv_format", _c_int),
         ("scale_mode", _c_int),
+        ("g_cache", _vp),
+        ("sink", _vp),
+        ("window", _c_int),
     ]
 
 
@@ -276,7 +279,7 @@ def attn_bwd(q, k, v, o, lse, dout, cu_seqlens, max_seqlen=None, scale=None, win
 
 
 def decode_args(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu_q, max_q_len, max_seq_len, scale,
-                segment_len) -> DecodeArgs:
+                segment_len, g_cache=None, sink=None, window=0) -> DecodeArgs:
     """Marshals the decode arguments.  The cache format follows the cache dtype (fp8 e4m3 as
     uint8 or float8_e4m3fn, or bf16); fp8 scales are per token when they have the page shape
     [num_blocks, num_kv_heads, block_size] and per tensor when they hold one value; a bf16
@@ -310,6 +313,12 @@ def decode_args(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu
             raise NotImplementedError("fp8 scales must have the page shape [num_blocks, num_kv_heads, block_size] "
                                       "(per token) or hold one value (per tensor)")
         kv_format, ks_ptr, vs_ptr = KV_FP8_E4M3, k_scale.data_ptr(), v_scale.data_ptr()
+    if g_cache is not None:
+        _need(g_cache, torch.float32, "g_cache")
+        if tuple(g_cache.shape) != (nb, q.shape[1], bs):
+            raise ValueError("g_cache must be [num_blocks, num_q_heads, block_size]")
+    if sink is not None:
+        _need(sink, torch.float32, "sink")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     return DecodeArgs(
@@ -335,17 +344,22 @@ def decode_args(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu
         q=q.data_ptr(),
         kv_format=kv_format,
         scale_mode=scale_mode,
+        g_cache=None if g_cache is None else g_cache.data_ptr(),
+        sink=None if sink is None else sink.data_ptr(),
+        window=int(window),
     )
 
 
 def attn_decode_paged(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu_q, max_q_len, max_seq_len,
-                      scale=None, segment_len=2048, out=None, workspace=None):
-    """Paged fp8 decode.  q bf16 [total_q, hq, d]; caches fp8 e4m3 (uint8 or float8_e4m3fn)
-    [num_blocks, hkv, block_size, d]; scales fp32 [num_blocks, hkv, block_size];
-    block_table int32 [R, max_blocks]; seq_lens int32 [R]; cu_q int32 [R + 1]."""
+                      scale=None, segment_len=2048, out=None, workspace=None, g_cache=None, sink=None, window=0):
+    """Paged decode.  q bf16 [total_q, hq, d]; caches fp8 e4m3 (uint8 or float8_e4m3fn) or bf16
+    [num_blocks, hkv, block_size, d]; fp8 scales fp32 [num_blocks, hkv, block_size] (per token)
+    or one value each (per tensor), None for bf16; block_table int32 [R, max_blocks]; seq_lens
+    int32 [R]; cu_q int32 [R + 1].  Optional decoding features: g_cache fp32 [num_blocks, hq,
+    block_size] cumulative log gates, sink fp32 [hq], window (0 = none)."""
     L = load()
     a = decode_args(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu_q, max_q_len, max_seq_len,
-                    scale, segment_len)
+                    scale, segment_len, g_cache, sink, window)
     if out is None:
         out = torch.empty_like(q)
     ws_bytes = L.attn_decode_workspace(ctypes.byref(a))
@@ -357,13 +371,13 @@ def attn_decode_paged(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_le
 
 
 def attn_decode_paged_noalloc(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu_q, max_q_len,
-                              max_seq_len, scale=None, segment_len=2048, out=None):
+                              max_seq_len, scale=None, segment_len=2048, out=None, g_cache=None, sink=None, window=0):
     """attn_decode_paged without a workspace: the library keeps the split-K partials in
     its own fixed 64 MiB device scratch (for callers that cannot allocate device memory).
     Calls share that scratch, so calls must not overlap on the GPU."""
     L = load()
     a = decode_args(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu_q, max_q_len, max_seq_len,
-                    scale, segment_len)
+                    scale, segment_len, g_cache, sink, window)
     if out is None:
         out = torch.empty_like(q)
     _check(L.attn_decode_paged_noalloc(ctypes.byref(a), out.data_ptr(), _stream()), "attn_decode_paged_noalloc")

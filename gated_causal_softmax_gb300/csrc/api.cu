@@ -347,6 +347,9 @@ static int check_decode(const gcs_decode_args* a) {
   if (a->segment_len % a->block_size != 0) return GCS_ERR_UNSUPPORTED;
   if (a->max_blocks_per_req * a->block_size < a->max_seq_len) return GCS_ERR_INVALID_ARG;
   if (!aligned16(a->k_cache) || !aligned16(a->v_cache) || !aligned16(a->q)) return GCS_ERR_INVALID_ARG;
+  if (a->window < 0) return GCS_ERR_INVALID_ARG;
+  if (a->g_cache && !aligned16(a->g_cache)) return GCS_ERR_INVALID_ARG;
+  if (a->sink && (reinterpret_cast<uintptr_t>(a->sink) & 3u)) return GCS_ERR_INVALID_ARG;
   if ((double)a->num_blocks * a->hkv * a->block_size * a->d > 9.0e15) return GCS_ERR_UNSUPPORTED;
   return GCS_OK;
 }
@@ -387,6 +390,9 @@ int attn_decode_paged(const gcs_decode_args* a, void* out, void* workspace, size
   p.v_scale = a->v_scale;
   p.kv_format = a->kv_format;
   p.scale_mode = a->scale_mode;
+  p.g_cache = a->g_cache;
+  p.sink = a->sink;
+  p.window = a->window;
   p.num_reqs = a->num_reqs;
   p.hq = a->hq;
   p.hkv = a->hkv;

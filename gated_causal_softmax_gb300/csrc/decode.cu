@@ -36,15 +36,26 @@ std::mutex g_noalloc_mu;
 constexpr int kPage = 16;
 constexpr int kD = 128;
 constexpr int kGroup = 16;
-// Ring layout per cache format.  fp8: stage = K 2048 | V 2048 | K scales 64 | V scales 64 | pad,
-// 16 stages, 8 pages per producer round.  bf16: stage = K 4096 | V 4096, 8 stages, 4 pages per
-// round (three CTAs per SM either way).
-template <int KVF>
+// Ring layout.  fp8: stage = K 2048 | V 2048 | K scales 64 | V scales 64 | pad (4352 B).  bf16:
+// stage = K 4096 | V 4096.  With the decoding features the page's cumulative gates of the
+// group's 16 query heads (16 x 16 fp32 = 1 KB) follow.  Stages fill ~72 KB (three CTAs per
+// SM); the producer issues BATCH pages per round, one copy per lane.
+template <int KVF, bool PT, bool FEAT>
 struct DecCfg {
   static constexpr int KB = KVF == 0 ? 2048 : 4096;  // bytes of one page of K (or V) for one kv head
-  static constexpr int STAGE = KVF == 0 ? 4352 : 8192;
-  static constexpr int NST = KVF == 0 ? 16 : 8;
-  static constexpr int BATCH = KVF == 0 ? 8 : 4;
+  static constexpr bool SCALES = KVF == 0 && !PT;    // per-token scale copies
+  static constexpr int G_OFF = KVF == 0 ? 4352 : 8192;
+  static constexpr int STAGE = G_OFF + (FEAT ? 1024 : 0);
+  // NST is a multiple of 4: the page groups of a CTA are 4 / q_len warps (4, 2 or 1), so the
+  // previous page of every stage belongs to the warp that waits for the stage's next page.
+  // That warp has therefore seen the previous phase complete, and a full-barrier parity wait
+  // cannot match the phase before it (which a stage consumed by another warp could, while the
+  // previous page's copy is still in flight).
+  static constexpr int NST = ((72 * 1024 / STAGE) < 16 ? (72 * 1024 / STAGE) : 16) & ~3;
+  static constexpr int KINDS = 2 + (SCALES ? 2 : 0) + (FEAT ? 1 : 0);  // K, V (, K/V scales) (, gates)
+  static constexpr int BATCH = (KINDS * 8 <= 32 && NST >= 16) ? 8 : 4;
+  static_assert(NST % 4 == 0, "stages per page-group warp");
+  static_assert(KINDS * BATCH <= 32 && NST >= 2 * BATCH, "producer round");
 };
 constexpr int kThreads = 160;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -96,11 +107,13 @@ __device__ __forceinline__ uint32_t bf16pair_to_f16x2(uint32_t w) {
 }
 
 // KVF: 0 fp8 e4m3 codes, 1 bf16 values.  PT: one K and one V scale for the whole cache (fp8).
-template <int KVF, bool PT>
+// FEAT: the decoding features (gates from g_cache when given, the window; the sink is the
+// combine's).
+template <int KVF, bool PT, bool FEAT>
 __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeParams p) {
-  using C = DecCfg<KVF>;
+  using C = DecCfg<KVF, PT, FEAT>;
   constexpr int kNST = C::NST, kStage = C::STAGE, kBatch = C::BATCH;
-  constexpr int kKinds = (KVF == 0 && !PT) ? 4 : 2;  // copies per page: K, V (, K scales, V scales)
+  constexpr int kKinds = C::KINDS;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ uint64_t full[kNST], empty[kNST];
   __shared__ int abort_flag_s;
@@ -109,9 +122,18 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
   const int q_begin = __ldg(p.cu_q + r);
   const int ql = __ldg(p.cu_q + r + 1) - q_begin;
   const int npages = (L + kPage - 1) / kPage;
-  const int pb = seg * p.seg_pages;
+  int pb = seg * p.seg_pages;
   if (pb >= npages || ql < 1 || ql > 4) return;
-  const int np = min(pb + p.seg_pages, npages) - pb;
+  const int pend = min(pb + p.seg_pages, npages);
+  if (FEAT && p.window > 0) {
+    // pages before the earliest key any query row of the request sees are skipped; a segment
+    // that lies wholly before them writes nothing (the combine starts after it)
+    const int first_page = max(0, L - ql - p.window + 1) / kPage;
+    if (pend <= first_page) return;
+    pb = max(pb, first_page);
+  }
+  const int np = pend - pb;
+  const bool has_gate = FEAT && p.g_cache != nullptr;
   const int ng = 4 / ql;  // page groups
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -128,25 +150,30 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
 
   if (warp == 0) {
     // ------------------------------------------------------------ page producer
-    // lane = kBatch * kind + page within the round; kind 0: K, 1: V, 2: K scales, 3: V scales
+    // lane = kBatch * kind + page within the round; kind 0: K, 1: V, then (per-token fp8)
+    // 2: K scales, 3: V scales, then (features) the gates of the group's query heads
     const int32_t* trow = p.block_table + (size_t)r * p.max_blocks + pb;
     const int pl = lane & (kBatch - 1), kind = lane / kBatch;
-    const uint32_t bytes = kind < 2 ? C::KB : kPage * 4;
-    const uint32_t dst_off = kind < 2 ? kind * C::KB : 2 * C::KB + (kind - 2) * 64;
-    constexpr uint32_t kTx = 2 * C::KB + (kKinds == 4 ? 2 * kPage * 4 : 0);
+    const int g_kind = C::SCALES ? 4 : 2;
+    const bool is_g = FEAT && kind == g_kind;
+    const uint32_t bytes = kind < 2 ? C::KB : is_g ? 1024 : kPage * 4;
+    const uint32_t dst_off = kind < 2 ? kind * C::KB : is_g ? C::G_OFF : 2 * C::KB + (kind - 2) * 64;
+    const uint32_t tx = 2 * C::KB + (C::SCALES ? 2 * kPage * 4 : 0) + (has_gate ? 1024 : 0);
     for (int base = 0; base < np; base += kBatch) {
       const int i = base + pl;
-      const bool act = i < np && kind < kKinds;
+      const bool act = i < np && kind < kKinds && (!is_g || has_gate);
       const int stage = i % kNST;
       bool okl = true;
       if (act) okl = wait_bar(&empty[stage], ((i / kNST) & 1) ^ 1, ab);
       if (!__all_sync(0xffffffffu, okl)) break;
-      if (act && kind == 0) mbar_expect_tx(&full[stage], kTx);
+      if (act && kind == 0) mbar_expect_tx(&full[stage], tx);
       __syncwarp();
       if (act) {
-        const size_t slot0 = ((size_t)__ldg(trow + i) * p.hkv + kvh) * kPage;
+        const int blk = __ldg(trow + i);
+        const size_t slot0 = ((size_t)blk * p.hkv + kvh) * kPage;
         const void* src = kind == 0   ? static_cast<const void*>(p.k_cache + slot0 * (C::KB / kPage))
                           : kind == 1 ? static_cast<const void*>(p.v_cache + slot0 * (C::KB / kPage))
+                          : is_g      ? static_cast<const void*>(p.g_cache + ((size_t)blk * p.hq + kvh * kGroup) * kPage)
                           : kind == 2 ? static_cast<const void*>(p.k_scale + slot0)
                                       : static_cast<const void*>(p.v_scale + slot0);
         bulk_load(smem + stage * kStage + dst_off, src, bytes, &full[stage]);
@@ -193,13 +220,30 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
     }
     // one K and one V scale for the whole cache (fp8 per-tensor)
     const float kst = PT ? __ldg(p.k_scale) : 1.f, vst = PT ? __ldg(p.v_scale) : 1.f;
-    {
+    // the query row's own cumulative gate (log2 units) for heads g and g + 8 of the group
+    float gq0 = 0.f, gq1 = 0.f;
+    if (has_gate) {
+      const int blk = __ldg(p.block_table + (size_t)r * p.max_blocks + lastk / kPage);
+      const float* gp = p.g_cache + ((size_t)blk * p.hq + kvh * kGroup) * kPage + lastk % kPage;
+      gq0 = __ldg(gp + g * kPage) * kLog2e;
+      gq1 = __ldg(gp + (g + 8) * kPage) * kLog2e;
     }
     for (int i = grp; i < np; i += ng) {
       const int stage = i % kNST;
       ok = wait_bar(&full[stage], (i / kNST) & 1, ab);
       if (!ok) break;
       const uint8_t* st = smem + stage * kStage;
+      // gates of this thread's four keys for heads g and g + 8 (read before the stage is freed)
+      float gk[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      if (has_gate) {
+        const float* gs = reinterpret_cast<const float*>(st + C::G_OFF);
+#pragma unroll
+        for (int rw2 = 0; rw2 < 2; ++rw2) {
+          const float2 a = *reinterpret_cast<const float2*>(gs + (g + 8 * rw2) * kPage + 2 * tq);
+          const float2 b = *reinterpret_cast<const float2*>(gs + (g + 8 * rw2) * kPage + 8 + 2 * tq);
+          gk[rw2][0] = a.x; gk[rw2][1] = a.y; gk[rw2][2] = b.x; gk[rw2][3] = b.y;
+        }
+      }
       float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
       float ks[4], vs[4];  // K / V scale of this thread's four columns
       uint4 vr[4];         // fp8 value fragments: rows 2tq, 2tq+1, 2tq+8, 2tq+9 (bf16 reads values later)
@@ -261,11 +305,17 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
       float x[2][4];  // [row g / g+8][column]
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const bool vis = tk[c] <= lastk;
+        bool vis = tk[c] <= lastk;
+        if (FEAT && p.window > 0) vis = vis && tk[c] > lastk - p.window;
         const float sa = (c < 2) ? s0[c] : s1[c - 2];
         const float sb = (c < 2) ? s0[c + 2] : s1[c];
-        x[0][c] = vis ? sa * sl2 * ks[c] : neg_inf();
-        x[1][c] = vis ? sb * sl2 * ks[c] : neg_inf();
+        if (FEAT) {  // + G_i - G_j
+          x[0][c] = vis ? fmaf(sa, sl2 * ks[c], fmaf(-gk[0][c], kLog2e, gq0)) : neg_inf();
+          x[1][c] = vis ? fmaf(sb, sl2 * ks[c], fmaf(-gk[1][c], kLog2e, gq1)) : neg_inf();
+        } else {
+          x[0][c] = vis ? sa * sl2 * ks[c] : neg_inf();
+          x[1][c] = vis ? sb * sl2 * ks[c] : neg_inf();
+        }
       }
       float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[0][2], x[0][3]));
       float mx1 = fmaxf(fmaxf(x[1][0], x[1][1]), fmaxf(x[1][2], x[1][3]));
@@ -449,11 +499,16 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
   const int row = t * kGroup + hh;
   auto unit_row = [&](int s) { return ((((size_t)r * p.max_segs + s) * p.hkv + kvh) * rows + row); };
   const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
+  // segments wholly before every window of the request were not written (see the split kernel)
+  const int s_begin = p.window > 0 ? (max(0, L - ql - p.window + 1) / kPage) / p.seg_pages : 0;
   float M = neg_inf();
-  for (int s = 0; s < nseg; ++s) M = fmaxf(M, ml[unit_row(s)].x);
+  for (int s = s_begin; s < nseg; ++s) M = fmaxf(M, ml[unit_row(s)].x);
+  // the sink logit (log2 units) joins the max and, once, the denominator
+  const float sg = p.sink ? __ldg(p.sink + kvh * kGroup + hh) * kLog2e : neg_inf();
+  M = fmaxf(M, sg);
   float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  float den = 0.f;
-  for (int s = 0; s < nseg; ++s) {
+  float den = p.sink ? ex2(sg - M) : 0.f;
+  for (int s = s_begin; s < nseg; ++s) {
     const float2 v = ml[unit_row(s)];
     const float w = (v.x == neg_inf()) ? 0.f : ex2(v.x - M);  // empty partial weighs 0
     den += w * v.y;
@@ -484,12 +539,16 @@ cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, const cudaEvent
     return cudaGetLastError();
   };
   cudaError_t e;
+  // the sink alone needs no change in the split kernel (it is the combine's)
+  const bool feat = p.g_cache != nullptr || p.window > 0;
+#define GCS_RUN(KVF, PT, F) run(decode_split_kernel<KVF, PT, F>, DecCfg<KVF, PT, F>::NST * DecCfg<KVF, PT, F>::STAGE)
   if (p.kv_format == 1)
-    e = run(decode_split_kernel<1, false>, DecCfg<1>::NST * DecCfg<1>::STAGE);
+    e = feat ? GCS_RUN(1, false, true) : GCS_RUN(1, false, false);
   else if (p.scale_mode == 1)
-    e = run(decode_split_kernel<0, true>, DecCfg<0>::NST * DecCfg<0>::STAGE);
+    e = feat ? GCS_RUN(0, true, true) : GCS_RUN(0, true, false);
   else
-    e = run(decode_split_kernel<0, false>, DecCfg<0>::NST * DecCfg<0>::STAGE);
+    e = feat ? GCS_RUN(0, false, true) : GCS_RUN(0, false, false);
+#undef GCS_RUN
   if (ev_after && *ev_after) cudaEventRecord(*ev_after, s);
   if (e != cudaSuccess) return e;
   dim3 g2(p.num_reqs * p.max_q_len, p.hkv);

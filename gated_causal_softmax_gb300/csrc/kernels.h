@@ -90,6 +90,9 @@ struct DecodeParams {
   const float* v_scale;
   int kv_format;           // 0: fp8 e4m3, 1: bf16
   int scale_mode;          // 0: per token, 1: per tensor
+  const float* g_cache;    // cumulative log gates [num_blocks, hq, 16] (natural log), or null
+  const float* sink;       // [hq] sink logits, or null
+  int window;              // 0 = none
   int num_reqs, hq, hkv;
   int max_q_len;
   int max_segs;          // segments per request slot in the partial buffers

@@ -126,6 +126,12 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
  * e^{M_s - max M}; a partial with no visible key (M = -inf) weighs 0.
  * With per-tensor scales, k_scale and v_scale each point to one fp32 used for every token;
  * with a bf16 cache, k_cache / v_cache hold bf16 values and k_scale, v_scale must be NULL.
+ * Decoding features ([FLA] Description: "the corresponding packed single-query decoding
+ * features"), each optional: g_cache holds the cumulative log gates G of the cached tokens,
+ * paged like the scales but per query head, fp32 [num_blocks, hq, block_size] (natural-log
+ * units); the score becomes scale*q.k_j + G_i - G_j with G_i the entry at the query row's
+ * own position.  window W > 0 keeps keys with position_i - j < W.  sink fp32 [hq] adds
+ * e^sink_h to the softmax denominator (once, in the combine).
  * Supported: d == 128, block_size == 16, hq / hkv == 16, 1 <= q_len <= 4,
  * segment_len a positive multiple of block_size.
  */
@@ -151,6 +157,9 @@ typedef struct {
   const void* q;               /* bf16 [total_q, hq, d]                                 */
   int kv_format;               /* GCS_KV_FP8_E4M3 or GCS_KV_BF16                         */
   int scale_mode;              /* GCS_SCALE_PER_TOKEN or GCS_SCALE_PER_TENSOR (fp8 only) */
+  const float* g_cache;        /* fp32 [num_blocks, hq, block_size] cumulative log gates, or NULL */
+  const float* sink;           /* fp32 [hq] sink logits, or NULL                          */
+  int window;                  /* sliding window in keys, 0 = none                        */
 } gcs_decode_args;
 
 /* Workspace bytes attn_decode_paged needs (split-K partials). */

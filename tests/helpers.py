@@ -66,13 +66,15 @@ def decode_dev(dc):
     dev = torch.device("cuda:0")
     opt = lambda t: None if t is None else t.to(dev)
     return dict(q=dc.q.to(dev), kc=dc.k_cache.to(dev), vc=dc.v_cache.to(dev), ks=opt(dc.k_scale),
-                vs=opt(dc.v_scale), bt=dc.block_table.to(dev), sl=dc.seq_lens.to(dev), cq=dc.cu_q.to(dev))
+                vs=opt(dc.v_scale), bt=dc.block_table.to(dev), sl=dc.seq_lens.to(dev), cq=dc.cu_q.to(dev),
+                g=opt(dc.g_cache), sink=opt(dc.sink))
 
 
 def run_decode(gcs, dc, d=None):
     d = d or decode_dev(dc)
     out = gcs.attn_decode_paged(d["q"], d["kc"], d["vc"], d["ks"], d["vs"], d["bt"], d["sl"], d["cq"],
-                                max(dc.q_lens), int(dc.seq_lens.max()), dc.scale, dc.segment_len)
+                                max(dc.q_lens), int(dc.seq_lens.max()), dc.scale, dc.segment_len,
+                                g_cache=d["g"], sink=d["sink"], window=dc.window)
     torch.cuda.synchronize()
     assert gcs.get_device_status() == 0
     return out
@@ -82,4 +84,6 @@ def oracle_decode(dc, rows=None):
     cache = lambda t: t.float().numpy() if t.dtype == torch.bfloat16 else t.numpy()
     opt = lambda t: None if t is None else t.numpy()
     return oracle.decode_paged(f64(dc.q), cache(dc.k_cache), cache(dc.v_cache), opt(dc.k_scale), opt(dc.v_scale),
-                               dc.block_table.numpy(), dc.seq_lens.numpy(), dc.cu_q.numpy(), dc.scale)
+                               dc.block_table.numpy(), dc.seq_lens.numpy(), dc.cu_q.numpy(), dc.scale,
+                               g_cache=opt(dc.g_cache), sink=None if dc.sink is None else f64(dc.sink),
+                               window=dc.window)

@@ -119,3 +119,8 @@ def test_decode_validation_on_host(L):
     assert L.attn_decode_workspace(b(decode(scale_mode=1, k_scale=FAKE + 4, v_scale=FAKE + 8))) > 0
     assert dec(decode(scale_mode=2)) == 1
     assert dec(decode(kv_format=2)) == 1
+    # decoding features: a negative window, a misaligned gate array or sink are invalid
+    assert dec(decode(window=-1)) == 1
+    assert dec(decode(g_cache=FAKE + 4)) == 1
+    assert dec(decode(sink=FAKE + 2)) == 1
+    assert L.attn_decode_workspace(b(decode(g_cache=FAKE, sink=FAKE + 4, window=1024))) > 0

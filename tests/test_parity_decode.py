@@ -182,3 +182,40 @@ def test_decode_bf16_gather_order_is_exact(gcs_lib):
         blk = int(dc.block_table[r, slot // 16])
         assert out[r, :, 0].eq(float(blk % 64)).all(), (r, out[r, :, 0])
         assert out[r, :, 1].eq(float(blk // 64)).all()
+
+
+# ------------------------------------------------------- decode with gates, window and sink
+FEATURE_CASES = {
+    # name: (seq_lens, q_lens, hq, hkv, segment_len, window, kv_format, scale_mode)
+    "gates_sink_no_window": ([1, 17, 700, 2049, 5000], [1, 1, 4, 2, 3], 32, 2, 2048, 0, "fp8", "per_token"),
+    "window_skips_segments": ([5000, 4100, 300, 64], [1, 4, 2, 3], 16, 1, 2048, 1000, "fp8", "per_token"),
+    "window_inside_page": ([40, 70, 17], [4, 3, 1], 16, 1, 16, 7, "fp8", "per_token"),
+    "per_tensor_features": ([3000, 33, 2049], [1, 4, 2], 32, 2, 2048, 500, "fp8", "per_tensor"),
+    "bf16_features": ([3000, 33, 2049], [1, 4, 2], 32, 2, 2048, 500, "bf16", "per_token"),
+}
+
+
+@pytest.mark.parametrize("name", list(FEATURE_CASES))
+def test_decode_features_parity(gcs_lib, name):
+    sl, ql, hq, hkv, seg, win, fmt, smode = FEATURE_CASES[name]
+    dc = make_decode(sl, ql, hq, hkv, 128, seed=400 + len(name), segment_len=seg, kv_format=fmt, scale_mode=smode,
+                     features=True, window=win)
+    out = run_decode(gcs_lib, dc)
+    ref = oracle_decode(dc)
+    assert np.isfinite(f64(out)).all()
+    assert_close("out", out, ref, DECODE_RTOL)
+    assert abs(bias(out, ref)) <= DECODE_BIAS
+
+
+def test_decode_sink_only_and_window_only(gcs_lib):
+    """Each feature on its own: the sink alone (split kernel unchanged, combine adds it) and a
+    window alone (no gates)."""
+    for win, keep_sink in ((0, True), (300, False)):
+        dc = make_decode([1000, 2500, 70], [1, 3, 2], 16, 1, 128, seed=41 + win, features=True, window=win)
+        dc.g_cache = None
+        if not keep_sink:
+            dc.sink = None
+        out = run_decode(gcs_lib, dc)
+        ref = oracle_decode(dc)
+        assert_close("out", out, ref, DECODE_RTOL)
+        assert abs(bias(out, ref)) <= DECODE_BIAS
