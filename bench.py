@@ -43,7 +43,7 @@ LAUNCHES_PER_DECODE = 2
 NCU_TRAFFIC = {
     "bwd": 217.9e6 + 277.0e6,  # prefill_bwd_dq_kernel<128> + prefill_bwd_kernel<128>
     "fwd": 119.8e6,            # prefill_fwd2_kernel<128>
-    "decode_split": 1188.9e6,  # decode_split_kernel
+    "decode_split": None,  # decode_split_kernel (changed since its last capture)
 }
 
 

@@ -66,6 +66,20 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t width, uint64_t rows, u
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D byte view [rows, 128] of a paged fp8 cache, one page (16 rows x 128 B) per box, 128-byte
+// swizzle.
+bool make_page_map_u8(CUtensorMap* m, const void* base, uint64_t rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {128, rows};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {128, 16};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 size_t round_up(size_t x) { return (x + 255) & ~size_t(255); }
@@ -351,6 +365,9 @@ static int check_decode(const gcs_decode_args* a) {
   if (a->g_cache && !aligned16(a->g_cache)) return GCS_ERR_INVALID_ARG;
   if (a->sink && (reinterpret_cast<uintptr_t>(a->sink) & 3u)) return GCS_ERR_INVALID_ARG;
   if ((double)a->num_blocks * a->hkv * a->block_size * a->d > 9.0e15) return GCS_ERR_UNSUPPORTED;
+  // the fp8 pages are fetched by tensor copies whose row coordinate is a 32-bit integer
+  if (a->kv_format == GCS_KV_FP8_E4M3 && (double)a->num_blocks * a->hkv * a->block_size > 2147483647.0)
+    return GCS_ERR_UNSUPPORTED;
   return GCS_OK;
 }
 
@@ -405,8 +422,15 @@ int attn_decode_paged(const gcs_decode_args* a, void* out, void* workspace, size
   p.part_acc = static_cast<float*>(workspace);
   p.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + round_up(units * rows * 128 * sizeof(float)));
   p.status = status;
+  DecodeMaps maps;
+  std::memset(&maps, 0, sizeof(maps));
+  if (a->kv_format == GCS_KV_FP8_E4M3) {
+    const uint64_t rows = (uint64_t)a->num_blocks * a->hkv * a->block_size;
+    if (!make_page_map_u8(&maps.k, a->k_cache, rows) || !make_page_map_u8(&maps.v, a->v_cache, rows))
+      return GCS_ERR_CUDA;
+  }
   KernelTimer timer(reinterpret_cast<cudaStream_t>(stream));
-  return cuda_status(launch_decode(p, reinterpret_cast<cudaStream_t>(stream), &timer.b, &timer.a));
+  return cuda_status(launch_decode(p, maps, reinterpret_cast<cudaStream_t>(stream), &timer.b, &timer.a));
 }
 
 int attn_decode_paged_noalloc(const gcs_decode_args* a, void* out, gcs_stream_t stream) {

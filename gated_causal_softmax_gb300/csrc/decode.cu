@@ -8,10 +8,12 @@
 // reduce in which an empty partial (M = -inf) weighs 0.
 //
 // decode_split_kernel: one CTA per (segment, kv head, request).  Warp 0 streams pages
-// (K 2 KB, V 2 KB, 16 K scales, 16 V scales) into a 16-stage shared-memory ring with
-// cp.async.bulk, eight pages per round: each of its 32 lanes issues one of the round's 32
-// copies (a bulk copy is a per-thread instruction, and one lane issuing them all serially
-// was the bottleneck).  Warps 1..4 each own one query position (16 query heads of the GQA
+// (K 2 KB, V 2 KB, 16 K scales, 16 V scales) into a 16-stage shared-memory ring, eight pages
+// per round: each of its 32 lanes issues one of the round's 32 copies (a copy is a
+// per-thread instruction, and one lane issuing them all serially was the bottleneck).  The
+// fp8 K and V pages come by tensor copy with the 128-byte swizzle, so the consumers' 16-B
+// reads of four rows at one column, or of two columns of two rows, hit eight different bank
+// groups; the scales (and gates) come by plain bulk copy.  Warps 1..4 each own one query position (16 query heads of the GQA
 // group = one m16 MMA tile) and a share of the pages; fp8 -> f16 conversion is exact,
 // QK^T and PV run on mma.sync m16n8k16 with fp32 accumulation, softmax in fp32 (log2
 // units).  P * vscale is scaled by 2^8 before the f16 rounding (round-to-nearest, no
@@ -36,22 +38,27 @@ std::mutex g_noalloc_mu;
 constexpr int kPage = 16;
 constexpr int kD = 128;
 constexpr int kGroup = 16;
-// Ring layout.  fp8: stage = K 2048 | V 2048 | K scales 64 | V scales 64 | pad (4352 B).  bf16:
-// stage = K 4096 | V 4096.  With the decoding features the page's cumulative gates of the
-// group's 16 query heads (16 x 16 fp32 = 1 KB) follow.  Stages fill ~72 KB (three CTAs per
-// SM); the producer issues BATCH pages per round, one copy per lane.
+// Ring layout: a K | V ring of NST pages (fp8: 2 KB + 2 KB, rows of 128 B stored with the
+// 128-byte swizzle of the tensor copy; bf16: 4 KB + 4 KB, linear) and, beside it, a ring of
+// the pages' small vectors: K and V scales (per-token fp8, 64 B each) and, with the decoding
+// features, the cumulative gates of the group's 16 query heads (16 x 16 fp32 = 1 KB).
+// Stages fill ~72 KB (three CTAs per SM); the producer issues BATCH pages per round, one
+// copy per lane.
 template <int KVF, bool PT, bool FEAT>
 struct DecCfg {
   static constexpr int KB = KVF == 0 ? 2048 : 4096;  // bytes of one page of K (or V) for one kv head
   static constexpr bool SCALES = KVF == 0 && !PT;    // per-token scale copies
-  static constexpr int G_OFF = KVF == 0 ? 4352 : 8192;
-  static constexpr int STAGE = G_OFF + (FEAT ? 1024 : 0);
+  static constexpr int KV = 2 * KB;                  // K | V of one page (a multiple of 1 KB)
+  static constexpr int G_OFF = SCALES ? 128 : 0;     // gates inside a small-vector stage
+  static constexpr int AUX = G_OFF + (FEAT ? 1024 : 0);
   // NST is a multiple of 4: the page groups of a CTA are 4 / q_len warps (4, 2 or 1), so the
   // previous page of every stage belongs to the warp that waits for the stage's next page.
   // That warp has therefore seen the previous phase complete, and a full-barrier parity wait
   // cannot match the phase before it (which a stage consumed by another warp could, while the
   // previous page's copy is still in flight).
-  static constexpr int NST = ((72 * 1024 / STAGE) < 16 ? (72 * 1024 / STAGE) : 16) & ~3;
+  static constexpr int NST = ((72 * 1024 / (KV + AUX)) < 16 ? (72 * 1024 / (KV + AUX)) : 16) & ~3;
+  static constexpr int OFF_AUX = NST * KV;
+  static constexpr int SMEM = OFF_AUX + NST * AUX + 1024;  // + alignment of the base to 1 KB
   static constexpr int KINDS = 2 + (SCALES ? 2 : 0) + (FEAT ? 1 : 0);  // K, V (, K/V scales) (, gates)
   static constexpr int BATCH = (KINDS * 8 <= 32 && NST >= 16) ? 8 : 4;
   static_assert(NST % 4 == 0, "stages per page-group warp");
@@ -110,11 +117,16 @@ __device__ __forceinline__ uint32_t bf16pair_to_f16x2(uint32_t w) {
 // FEAT: the decoding features (gates from g_cache when given, the window; the sink is the
 // combine's).
 template <int KVF, bool PT, bool FEAT>
-__global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, 3)
+    decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                        const DecodeParams p) {
   using C = DecCfg<KVF, PT, FEAT>;
-  constexpr int kNST = C::NST, kStage = C::STAGE, kBatch = C::BATCH;
+  constexpr int kNST = C::NST, kBatch = C::BATCH;
   constexpr int kKinds = C::KINDS;
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  // the swizzled tensor copies want 1 KB-aligned pages
+  uint8_t* kv = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* aux = kv + C::OFF_AUX;
   __shared__ uint64_t full[kNST], empty[kNST];
   __shared__ int abort_flag_s;
   const int seg = blockIdx.x, kvh = blockIdx.y, r = blockIdx.z;
@@ -157,7 +169,11 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
     const int g_kind = C::SCALES ? 4 : 2;
     const bool is_g = FEAT && kind == g_kind;
     const uint32_t bytes = kind < 2 ? C::KB : is_g ? 1024 : kPage * 4;
-    const uint32_t dst_off = kind < 2 ? kind * C::KB : is_g ? C::G_OFF : 2 * C::KB + (kind - 2) * 64;
+    const uint32_t dst_off = kind < 2 ? kind * C::KB : is_g ? C::G_OFF : (kind - 2) * 64;
+    if (KVF == 0 && lane == 0) {
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+    }
     const uint32_t tx = 2 * C::KB + (C::SCALES ? 2 * kPage * 4 : 0) + (has_gate ? 1024 : 0);
     for (int base = 0; base < np; base += kBatch) {
       const int i = base + pl;
@@ -171,12 +187,17 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
       if (act) {
         const int blk = __ldg(trow + i);
         const size_t slot0 = ((size_t)blk * p.hkv + kvh) * kPage;
-        const void* src = kind == 0   ? static_cast<const void*>(p.k_cache + slot0 * (C::KB / kPage))
-                          : kind == 1 ? static_cast<const void*>(p.v_cache + slot0 * (C::KB / kPage))
-                          : is_g      ? static_cast<const void*>(p.g_cache + ((size_t)blk * p.hq + kvh * kGroup) * kPage)
-                          : kind == 2 ? static_cast<const void*>(p.k_scale + slot0)
-                                      : static_cast<const void*>(p.v_scale + slot0);
-        bulk_load(smem + stage * kStage + dst_off, src, bytes, &full[stage]);
+        if (KVF == 0 && kind < 2) {
+          // fp8 K or V page: one 16-row x 128-B box of the cache viewed as [rows, 128 B]
+          tma_load_2d(kv + stage * C::KV + dst_off, kind ? &tmV : &tmK, &full[stage], 0, static_cast<int>(slot0));
+        } else {
+          const void* src = kind == 0   ? static_cast<const void*>(p.k_cache + slot0 * (C::KB / kPage))
+                            : kind == 1 ? static_cast<const void*>(p.v_cache + slot0 * (C::KB / kPage))
+                            : is_g ? static_cast<const void*>(p.g_cache + ((size_t)blk * p.hq + kvh * kGroup) * kPage)
+                            : kind == 2 ? static_cast<const void*>(p.k_scale + slot0)
+                                        : static_cast<const void*>(p.v_scale + slot0);
+          bulk_load((kind < 2 ? kv + stage * C::KV : aux + stage * C::AUX) + dst_off, src, bytes, &full[stage]);
+        }
       }
     }
     return;
@@ -232,11 +253,12 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
       const int stage = i % kNST;
       ok = wait_bar(&full[stage], (i / kNST) & 1, ab);
       if (!ok) break;
-      const uint8_t* st = smem + stage * kStage;
+      const uint8_t* st = kv + stage * C::KV;    // K page | V page
+      const uint8_t* sa = aux + stage * C::AUX;  // K scales | V scales | gates
       // gates of this thread's four keys for heads g and g + 8 (read before the stage is freed)
       float gk[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
       if (has_gate) {
-        const float* gs = reinterpret_cast<const float*>(st + C::G_OFF);
+        const float* gs = reinterpret_cast<const float*>(sa + C::G_OFF);
 #pragma unroll
         for (int rw2 = 0; rw2 < 2; ++rw2) {
           const float2 a = *reinterpret_cast<const float2*>(gs + (g + 8 * rw2) * kPage + 2 * tq);
@@ -246,29 +268,26 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
       }
       float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
       float ks[4], vs[4];  // K / V scale of this thread's four columns
-      uint4 vr[4];         // fp8 value fragments: rows 2tq, 2tq+1, 2tq+8, 2tq+9 (bf16 reads values later)
       if constexpr (KVF == 0) {
-        const uint4 ka0 = lds128(st + g * kD + 32 * tq);
-        const uint4 ka1 = lds128(st + g * kD + 32 * tq + 16);
-        const uint4 kb0 = lds128(st + (8 + g) * kD + 32 * tq);
-        const uint4 kb1 = lds128(st + (8 + g) * kD + 32 * tq + 16);
-        vr[0] = lds128(st + 2048 + (2 * tq) * kD + 16 * g);
-        vr[1] = lds128(st + 2048 + (2 * tq + 1) * kD + 16 * g);
-        vr[2] = lds128(st + 2048 + (2 * tq + 8) * kD + 16 * g);
-        vr[3] = lds128(st + 2048 + (2 * tq + 9) * kD + 16 * g);
+        // dims 32tq .. 32tq + 31 of keys g and g + 8: 16-B units 2tq and 2tq + 1 of those rows,
+        // at unit ^ (row & 7) in the swizzled page (conflict-free across each quarter warp)
+        const uint32_t u0 = ((2 * tq) ^ (g & 7)) << 4, u1 = ((2 * tq + 1) ^ (g & 7)) << 4;
+        const uint4 ka0 = lds128(st + g * kD + u0);
+        const uint4 ka1 = lds128(st + g * kD + u1);
+        const uint4 kb0 = lds128(st + (8 + g) * kD + u0);
+        const uint4 kb1 = lds128(st + (8 + g) * kD + u1);
         if constexpr (PT) {
           ks[0] = ks[1] = ks[2] = ks[3] = kst;
           vs[0] = vs[1] = vs[2] = vs[3] = vst;
         } else {
-          const float2 ksA = *reinterpret_cast<const float2*>(st + 4096 + 8 * tq);
-          const float2 ksB = *reinterpret_cast<const float2*>(st + 4096 + 32 + 8 * tq);
-          const float2 vsA = *reinterpret_cast<const float2*>(st + 4160 + 8 * tq);
-          const float2 vsB = *reinterpret_cast<const float2*>(st + 4160 + 32 + 8 * tq);
+          const float2 ksA = *reinterpret_cast<const float2*>(sa + 8 * tq);
+          const float2 ksB = *reinterpret_cast<const float2*>(sa + 32 + 8 * tq);
+          const float2 vsA = *reinterpret_cast<const float2*>(sa + 64 + 8 * tq);
+          const float2 vsB = *reinterpret_cast<const float2*>(sa + 64 + 32 + 8 * tq);
           ks[0] = ksA.x; ks[1] = ksA.y; ks[2] = ksB.x; ks[3] = ksB.y;
           vs[0] = vsA.x; vs[1] = vsA.y; vs[2] = vsB.x; vs[3] = vsB.y;
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[stage]);
+        // (values are read after the softmax and the stage is released then: fewer live registers)
         // S = q . k8 over the page: n-tile 0 = slots 0..7, n-tile 1 = slots 8..15
         const uint32_t kw0[8] = {ka0.x, ka0.y, ka0.z, ka0.w, ka1.x, ka1.y, ka1.z, ka1.w};
         const uint32_t kw1[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
@@ -355,9 +374,17 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
         pa[1] = pack_f16x2(pr[1][0] * vs[0], pr[1][1] * vs[1]);
         pa[2] = pack_f16x2(pr[0][2] * vs[2], pr[0][3] * vs[3]);
         pa[3] = pack_f16x2(pr[1][2] * vs[2], pr[1][3] * vs[3]);
+        // value fragments: dims 16g .. 16g + 15 (16-B unit g) of slots 2tq, 2tq+1, 2tq+8, 2tq+9;
+        // slots at or past seq_len are zero (NaN allowed in their bytes)
+        uint4 vr[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < 4; ++c) {
+          const int row = 2 * tq + (c & 1) + 8 * (c >> 1);
+          vr[c] = lds128(st + C::KB + row * kD + ((g ^ (row & 7)) << 4));
           if (tk[c] >= L) vr[c] = make_uint4(0, 0, 0, 0);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[stage]);
         const uint32_t va[4] = {vr[0].x, vr[0].y, vr[0].z, vr[0].w}, vb[4] = {vr[1].x, vr[1].y, vr[1].z, vr[1].w};
         const uint32_t vc[4] = {vr[2].x, vr[2].y, vr[2].z, vr[2].w}, vd[4] = {vr[3].x, vr[3].y, vr[3].z, vr[3].w};
 #pragma unroll
@@ -390,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr) {
           const int row = 2 * tq + (rr & 1) + 8 * (rr >> 1);
-          uint4 a = lds128(st + 4096 + row * 256 + 32 * g), b = lds128(st + 4096 + row * 256 + 32 * g + 16);
+          uint4 a = lds128(st + C::KB + row * 256 + 32 * g), b = lds128(st + C::KB + row * 256 + 32 * g + 16);
           if (tk[rr] >= L) a = b = make_uint4(0, 0, 0, 0);
           rw[rr][0] = a.x; rw[rr][1] = a.y; rw[rr][2] = a.z; rw[rr][3] = a.w;
           rw[rr][4] = b.x; rw[rr][5] = b.y; rw[rr][6] = b.z; rw[rr][7] = b.w;
@@ -414,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_split_kernel(const DecodeP
 
   // ------------------------------------------------ merge page groups, write the partial
   // thread (g, tq) holds dims 32tq + u (o[u][0], o[u][2]) and 32tq + 16 + u (o[u][1], o[u][3])
-  float* red = reinterpret_cast<float*>(smem);  // reuses the ring: [4 warps][16 rows][130]
+  float* red = reinterpret_cast<float*>(kv);  // reuses the ring: [4 warps][16 rows][130]
   if (ng > 1) {
     named_bar_sync(1, 128);  // every consumer is done with the ring
     if (active) {
@@ -528,20 +555,20 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
 
 }  // namespace
 
-cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, const cudaEvent_t* ev_before,
-                          const cudaEvent_t* ev_after) {
+cudaError_t launch_decode(const DecodeParams& p, const DecodeMaps& maps, cudaStream_t s,
+                          const cudaEvent_t* ev_before, const cudaEvent_t* ev_after) {
   dim3 g1(p.max_segs, p.hkv, p.num_reqs);
   auto run = [&](auto kern, int smem) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     if (ev_before && *ev_before) cudaEventRecord(*ev_before, s);
-    kern<<<g1, kThreads, smem, s>>>(p);
+    kern<<<g1, kThreads, smem, s>>>(maps.k, maps.v, p);
     return cudaGetLastError();
   };
   cudaError_t e;
   // the sink alone needs no change in the split kernel (it is the combine's)
   const bool feat = p.g_cache != nullptr || p.window > 0;
-#define GCS_RUN(KVF, PT, F) run(decode_split_kernel<KVF, PT, F>, DecCfg<KVF, PT, F>::NST * DecCfg<KVF, PT, F>::STAGE)
+#define GCS_RUN(KVF, PT, F) run(decode_split_kernel<KVF, PT, F>, DecCfg<KVF, PT, F>::SMEM)
   if (p.kv_format == 1)
     e = feat ? GCS_RUN(1, false, true) : GCS_RUN(1, false, false);
   else if (p.scale_mode == 1)

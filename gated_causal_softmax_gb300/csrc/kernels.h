@@ -105,9 +105,15 @@ struct DecodeParams {
   int* status;
 };
 
+// fp8 K and V caches viewed as 2-D [num_blocks * hkv * 16 rows, 128 B], box 128 B x 16 rows
+// (one page), 128-byte swizzle; unused for a bf16 cache.
+struct DecodeMaps {
+  CUtensorMap k, v;
+};
+
 // ev_before / ev_after (may point to null events) are recorded around the split-K kernel.
-cudaError_t launch_decode(const DecodeParams& p, cudaStream_t s, const cudaEvent_t* ev_before,
-                          const cudaEvent_t* ev_after);
+cudaError_t launch_decode(const DecodeParams& p, const DecodeMaps& maps, cudaStream_t s,
+                          const cudaEvent_t* ev_before, const cudaEvent_t* ev_after);
 
 // Size of the static scratch behind attn_decode_paged_noalloc (64 MiB).
 constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;
