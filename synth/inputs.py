@@ -396,6 +396,10 @@ DECODE_CONFIGS = {
     # Short-query (speculative verify) case: 3 requests x 4 tokens at 227K context.
     "paged_fp8_verify_3x4_227k": dict(seq_lens=[CTX_227K + 1, CTX_227K + 2, CTX_227K + 4], q_lens=[4, 4, 4], hq=64,
                                       hkv=4, d=128, seed=5),
+    # Chunked prefill (a batch that is not all-decode): 4 requests, each a 1024-token chunk at
+    # the end of its cached context (8K, 16K, 24K, 32K tokens), Hq=64, Hkv=4, D=128, page 16.
+    "paged_fp8_chunked_prefill_4x1024": dict(seq_lens=[8192, 16384, 24576, 32768], q_lens=[1024] * 4, hq=64,
+                                             hkv=4, d=128, seed=6),
 }
 
 

@@ -467,3 +467,55 @@ def test_decode_window_one_with_sink_closed_form():
                 s = dc.scale * float(K[pos] @ f64(dc.q)[q0 + t, h])
                 w = 1.0 / (1.0 + math.exp(float(dc.sink[h]) - s))
                 np.testing.assert_allclose(out[q0 + t, h], V[pos] * w, rtol=1e-12, atol=1e-14)
+
+
+@pytest.mark.parametrize("window", [0, 7, 40])
+def test_paged_chunks_equal_prefill_rows(window):
+    """Query chunks longer than a decode (q_len 5 .. seq_len, the chunked-prefill shape) over
+    the paged cache equal the last q_len rows of the prefill oracle (pinned to fp64 SDPA) on
+    the dequantized keys and values; a chunk with q_len == seq_len is a whole prefill."""
+    dc = make_decode([45, 37, 70, 20], [45, 9, 33, 17], hq=4, hkv=2, d=8, seed=39, features=True, window=window)
+    out = oracle.decode_paged(*_decode_args(dc), **_feature_kwargs(dc))
+    assert np.isfinite(out).all()
+    for r, L in enumerate(dc.seq_lens.tolist()):
+        q0, q1 = int(dc.cu_q[r]), int(dc.cu_q[r + 1])
+        ql = q1 - q0
+        K = np.stack([oracle.gather_kv(dc.k_cache.numpy(), dc.k_scale.numpy(), dc.block_table[r].numpy(), L, h)
+                      for h in range(dc.hkv)], 1)
+        V = np.stack([oracle.gather_kv(dc.v_cache.numpy(), dc.v_scale.numpy(), dc.block_table[r].numpy(), L, h)
+                      for h in range(dc.hkv)], 1)
+        npg = (L + 15) // 16
+        G = dc.g_cache[dc.block_table[r, :npg].long()].double().permute(0, 2, 1).reshape(npg * 16, dc.hq)[:L]
+        g = torch.diff(G, dim=0, prepend=torch.zeros(1, dc.hq, dtype=torch.float64)).numpy()
+        q = np.zeros((L, dc.hq, dc.d))
+        q[L - ql :] = f64(dc.q)[q0:q1]
+        o, _ = oracle.prefill_forward(q, K, V, np.array([0, L]), dc.scale, log_gate=g, sink=dc.sink.double().numpy(),
+                                      window=window)
+        np.testing.assert_allclose(out[q0:q1], o[L - ql :], rtol=1e-10, atol=1e-12)
+
+
+def test_paged_chunk_splitk_equals_unsplit_and_rows_are_single_queries():
+    """Long chunks in split-K (segments of 16 and 48 tokens leave rows with no visible key in
+    a segment: weight 0) equal the unsplit result, and each row equals the single-query
+    request that ends at its own position."""
+    dc = make_decode([70, 33, 50], [40, 33, 6], hq=8, hkv=2, d=16, seed=40, features=True, window=21)
+    ref = oracle.decode_paged(*_decode_args(dc), **_feature_kwargs(dc))
+    for seg in (16, 48):
+        parts = oracle.decode_partials(*_decode_args(dc), seg, g_cache=dc.g_cache.numpy(), window=dc.window)
+        assert any(np.isneginf(p["m"]).any() for p in parts)
+        out = oracle.decode_combine(parts, dc.q.shape[0], dc.hq, dc.d, dc.cu_q.numpy(), dc.hkv,
+                                    sink=dc.sink.double().numpy())
+        np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
+    # row t of request r == a one-row request whose context ends at position L - q_len + t
+    seq, cu = [], [0]
+    bt = []
+    for r, L in enumerate(dc.seq_lens.tolist()):
+        ql = int(dc.cu_q[r + 1] - dc.cu_q[r])
+        for t in range(ql):
+            seq.append(L - ql + t + 1)
+            cu.append(cu[-1] + 1)
+            bt.append(dc.block_table[r].numpy())
+    one = oracle.decode_paged(f64(dc.q), dc.k_cache.numpy(), dc.v_cache.numpy(), dc.k_scale.numpy(),
+                              dc.v_scale.numpy(), np.stack(bt), np.array(seq), np.array(cu), dc.scale,
+                              **_feature_kwargs(dc))
+    np.testing.assert_allclose(one, ref, rtol=0, atol=1e-12)
