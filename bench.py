@@ -32,6 +32,7 @@ if ROOT not in sys.path:
 METRIC = "prefill fwd+bwd causal TFLOP/s (% bf16 peak); paged decode GB/s (% HBM peak)"
 PREFILL_WORKLOAD = "varlen_gqa_8192_d128"
 DECODE_WORKLOAD = "paged_fp8_decode_64x1"
+CHUNK_WORKLOAD = "paged_fp8_chunked_prefill_4x1024"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # my kernels per prefill step with gates and sink: fwd (gate cumsum, attention) and bwd
 # (gate cumsum, delta, vector pack, dQ pass, dK/dV pass, d gate scan, d sink reduce)
@@ -70,6 +71,17 @@ def prefill_pairs(seqlens, hq, window=0):
 def prefill_flops(seqlens, hq, dqk, dv, window=0):
     p = prefill_pairs(seqlens, hq, window)
     return 2 * (dqk + dv) * p, 2 * (3 * dqk + 2 * dv) * p
+
+
+def paged_chunk_flops(seq_lens, q_lens, hq, d, window=0):
+    """Algorithmic FLOPs of paged attention over query chunks: 4 d per visible (query row,
+    key, query head) pair (QK^T and PV), row t of a chunk of q_len at position L - q_len + t."""
+    pairs = 0
+    for L, ql in zip(seq_lens, q_lens):
+        for t in range(ql):
+            pos = L - ql + t
+            pairs += min(pos + 1, window) if window > 0 else pos + 1
+    return 4 * d * pairs * hq
 
 
 def decode_bytes(seq_lens, q_lens, hq, hkv, d, block_size, kv_format="fp8", scale_mode="per_token", gates=False):
@@ -370,6 +382,53 @@ def run_native(args):
     if gcs.get_device_status() != 0:
         raise RuntimeError("a decode kernel timed out")
 
+    # ------------------------------------------------ paged chunked prefill (fp8 cache)
+    pc = decode_config(CHUNK_WORKLOAD)
+    pd = dict(q=pc.q.to(dev), kc=pc.k_cache.to(dev), vc=pc.v_cache.to(dev), ks=pc.k_scale.to(dev),
+              vs=pc.v_scale.to(dev), bt=pc.block_table.to(dev), sl=pc.seq_lens.to(dev), cq=pc.cu_q.to(dev))
+    pout = torch.empty_like(pd["q"])
+    pmaxq, pmaxl = max(pc.q_lens), int(pc.seq_lens.max())
+
+    def pstep(ev=None):
+        if ev is not None:
+            gcs.set_kernel_events(ev[0], ev[1])
+        gcs.attn_prefill_paged(pd["q"], pd["kc"], pd["vc"], pd["ks"], pd["vs"], pd["bt"], pd["sl"], pd["cq"], pmaxq,
+                               pmaxl, pc.scale, 0, out=pout)
+
+    for _ in range(args.warmup):
+        pstep()
+    torch.cuda.synchronize()
+    pevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(DK)]
+    for e2 in pevs:
+        for e in e2:
+            e.record()
+    barrier(world)
+    torch.cuda.synchronize()
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record()
+    for i in range(DK):
+        pstep(pevs[i])
+    c1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    if gcs.get_device_status() != 0:
+        raise RuntimeError("a paged prefill kernel timed out")
+    p_ms = max_over_ranks(world, c0.elapsed_time(c1)) / DK
+    pk_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in pevs)
+    p_fl = paged_chunk_flops(pc.seq_lens.tolist(), pc.q_lens, pc.hq, pc.d)
+    p_tf = p_fl * world / (p_ms * 1e-3) / 1e12
+    pk_tf = p_fl / (pk_ms * 1e-3) / 1e12
+    chunked = {"workload": CHUNK_WORKLOAD, "value": round(p_tf, 1), "unit": "TFLOP/s",
+               "pct_of_peak": round(p_tf / world / sustained, 4), "ms_per_call": round(p_ms, 4),
+               "flops_per_call": p_fl,
+               "roofline": {"bound": "tensor", "kernel": "prefill_paged_kernel", "achieved": round(pk_tf, 1),
+                            "peak": sustained, "unit": "TFLOP/s", "frac": round(pk_tf / sustained, 4),
+                            "traffic": NCU_TRAFFIC.get("prefill_paged"),
+                            "peak_source": f"{pk_kind} bf16_tflops_sustained (f16 runs at the bf16 rate)",
+                            "kernel_ms": round(pk_ms, 4)}}
+    del pd, pout
+    torch.cuda.empty_cache()
+
     # ------------------------------------------------------------ CPU oracle baseline
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -396,6 +455,7 @@ def run_native(args):
                    "l2": "inputs and fp32 dQ buffer (~0.5 GB) larger than L2; no flush"},
         "roofline": roofline,
         "decode": decode,
+        "chunked_prefill": chunked,
         "cpu_baseline": cpu,
         "clocks": clocks,
         "e2e": e2e,

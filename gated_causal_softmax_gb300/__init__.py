@@ -26,6 +26,7 @@ __all__ = [
     "attn_bwd",
     "attn_decode_paged",
     "attn_decode_paged_noalloc",
+    "attn_prefill_paged",
     "PrefillArgs",
     "DecodeArgs",
     "GcsError",
@@ -129,6 +130,10 @@ def _declare(lib: ctypes.CDLL) -> None:
     lib.attn_decode_paged.restype = _c_int
     lib.attn_decode_paged_noalloc.argtypes = [P(DecodeArgs), _vp, _vp]
     lib.attn_decode_paged_noalloc.restype = _c_int
+    lib.attn_prefill_paged_workspace.argtypes = [P(DecodeArgs)]
+    lib.attn_prefill_paged_workspace.restype = ctypes.c_size_t
+    lib.attn_prefill_paged.argtypes = [P(DecodeArgs), _vp, _vp, ctypes.c_size_t, _vp]
+    lib.attn_prefill_paged.restype = _c_int
     lib.gcs_get_device_status.argtypes = [P(_c_int), _c_int]
     lib.gcs_get_device_status.restype = _c_int
     lib.gcs_set_kernel_events.argtypes = [_vp, _vp]
@@ -367,6 +372,25 @@ def attn_decode_paged(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_le
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
     st = L.attn_decode_paged(ctypes.byref(a), out.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream())
     _check(st, "attn_decode_paged")
+    return out
+
+
+def attn_prefill_paged(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu_q, max_q_len, max_seq_len,
+                       scale=None, segment_len=0, out=None, workspace=None, g_cache=None, sink=None, window=0):
+    """Paged chunked prefill: like attn_decode_paged, but a request's q_len may be anything
+    from 1 to its seq_len (its query rows are the last q_len cached positions).  fp8 e4m3
+    cache with per-token or per-tensor scales.  segment_len 0 lets the library choose the
+    split of the context (no workspace when it needs none); otherwise a multiple of 128."""
+    L = load()
+    a = decode_args(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu_q, max_q_len, max_seq_len,
+                    scale, segment_len, g_cache, sink, window)
+    if out is None:
+        out = torch.empty_like(q)
+    ws_bytes = L.attn_prefill_paged_workspace(ctypes.byref(a))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
+    st = L.attn_prefill_paged(ctypes.byref(a), out.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream())
+    _check(st, "attn_prefill_paged")
     return out
 
 

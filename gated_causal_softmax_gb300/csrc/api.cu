@@ -371,6 +371,35 @@ static int check_decode(const gcs_decode_args* a) {
   return GCS_OK;
 }
 
+// Kernel parameters common to the paged calls (segments and partial buffers set by the caller).
+static void fill_paged_params(const gcs_decode_args* a, void* out, int* status, DecodeParams& p) {
+  p.cu_q = a->cu_q;
+  p.seq_lens = a->seq_lens;
+  p.block_table = a->block_table;
+  p.max_blocks = a->max_blocks_per_req;
+  p.k_cache = static_cast<const uint8_t*>(a->k_cache);
+  p.v_cache = static_cast<const uint8_t*>(a->v_cache);
+  p.k_scale = a->k_scale;
+  p.v_scale = a->v_scale;
+  p.kv_format = a->kv_format;
+  p.scale_mode = a->scale_mode;
+  p.g_cache = a->g_cache;
+  p.sink = a->sink;
+  p.window = a->window;
+  p.num_reqs = a->num_reqs;
+  p.hq = a->hq;
+  p.hkv = a->hkv;
+  p.max_q_len = a->max_q_len;
+  p.max_segs = 1;
+  p.seg_pages = 0;
+  p.scale = a->scale;
+  p.q = static_cast<const uint16_t*>(a->q);
+  p.out = static_cast<uint16_t*>(out);
+  p.part_acc = nullptr;
+  p.part_ml = nullptr;
+  p.status = status;
+}
+
 static size_t decode_ws(const gcs_decode_args* a, int* max_segs_out) {
   const int max_segs = (a->max_seq_len + a->segment_len - 1) / a->segment_len;
   if (max_segs_out) *max_segs_out = max_segs;
@@ -397,36 +426,16 @@ int attn_decode_paged(const gcs_decode_args* a, void* out, void* workspace, size
   const size_t units = (size_t)a->num_reqs * max_segs * a->hkv;
   const size_t rows = (size_t)a->max_q_len * 16;
   DecodeParams p;
-  p.cu_q = a->cu_q;
-  p.seq_lens = a->seq_lens;
-  p.block_table = a->block_table;
-  p.max_blocks = a->max_blocks_per_req;
-  p.k_cache = static_cast<const uint8_t*>(a->k_cache);
-  p.v_cache = static_cast<const uint8_t*>(a->v_cache);
-  p.k_scale = a->k_scale;
-  p.v_scale = a->v_scale;
-  p.kv_format = a->kv_format;
-  p.scale_mode = a->scale_mode;
-  p.g_cache = a->g_cache;
-  p.sink = a->sink;
-  p.window = a->window;
-  p.num_reqs = a->num_reqs;
-  p.hq = a->hq;
-  p.hkv = a->hkv;
-  p.max_q_len = a->max_q_len;
+  fill_paged_params(a, out, status, p);
   p.max_segs = max_segs;
   p.seg_pages = a->segment_len / a->block_size;
-  p.scale = a->scale;
-  p.q = static_cast<const uint16_t*>(a->q);
-  p.out = static_cast<uint16_t*>(out);
   p.part_acc = static_cast<float*>(workspace);
   p.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + round_up(units * rows * 128 * sizeof(float)));
-  p.status = status;
   DecodeMaps maps;
   std::memset(&maps, 0, sizeof(maps));
   if (a->kv_format == GCS_KV_FP8_E4M3) {
-    const uint64_t rows = (uint64_t)a->num_blocks * a->hkv * a->block_size;
-    if (!make_page_map_u8(&maps.k, a->k_cache, rows) || !make_page_map_u8(&maps.v, a->v_cache, rows))
+    const uint64_t cache_rows = (uint64_t)a->num_blocks * a->hkv * a->block_size;
+    if (!make_page_map_u8(&maps.k, a->k_cache, cache_rows) || !make_page_map_u8(&maps.v, a->v_cache, cache_rows))
       return GCS_ERR_CUDA;
   }
   KernelTimer timer(reinterpret_cast<cudaStream_t>(stream));
@@ -441,6 +450,88 @@ int attn_decode_paged_noalloc(const gcs_decode_args* a, void* out, gcs_stream_t 
   void* scratch = nullptr;
   if (decode_noalloc_scratch(&scratch) != cudaSuccess) return GCS_ERR_CUDA;
   return attn_decode_paged(a, out, scratch, kNoAllocScratchBytes, stream);
+}
+
+// Paged chunked prefill: the decode checks with the q_len limit lifted, fp8 only, and
+// segment_len 0 (automatic) or a multiple of 128 tokens (one key tile of 8 pages).
+static int check_prefill_paged(const gcs_decode_args* a) {
+  if (!a) return GCS_ERR_INVALID_ARG;
+  if (a->max_q_len < 1 || a->segment_len < 0) return GCS_ERR_INVALID_ARG;
+  gcs_decode_args b = *a;
+  b.max_q_len = a->max_q_len < 4 ? a->max_q_len : 4;
+  b.segment_len = a->segment_len > 0 ? a->segment_len : 128;
+  const int st = check_decode(&b);
+  if (st != GCS_OK) return st;
+  if (a->kv_format != GCS_KV_FP8_E4M3) return GCS_ERR_UNSUPPORTED;
+  if (a->segment_len % 128 != 0) return GCS_ERR_UNSUPPORTED;
+  if (a->max_q_len > a->max_seq_len) return GCS_ERR_INVALID_ARG;
+  return GCS_OK;
+}
+
+struct PagedPlan {
+  int seg_pages = 0, max_segs = 1;
+  size_t ws = 0;  // 0: one segment per request, the kernel writes out directly
+};
+
+// Segments of the paged prefill: the caller's, or (segment_len 0) the fewest that give
+// about two CTAs per SM with the query blocks of 16 positions x kv heads x requests.
+static bool plan_prefill_paged(const gcs_decode_args* a, PagedPlan* pl) {
+  const int max_pages = (a->max_seq_len + 15) / 16;
+  int sp;
+  if (a->segment_len > 0) {
+    sp = a->segment_len / 16;
+  } else {
+    int dev = 0, nsm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return false;
+    const long long ctas = (long long)((a->max_q_len + 15) / 16) * a->hkv * a->num_reqs;
+    long long want = (2LL * nsm + ctas - 1) / ctas;
+    if (want < 1) want = 1;
+    sp = (int)((max_pages + want - 1) / want);
+    sp = ((sp + 7) / 8) * 8;
+  }
+  pl->seg_pages = sp;
+  pl->max_segs = (max_pages + sp - 1) / sp;
+  pl->ws = 0;
+  if (pl->max_segs > 1) {
+    const size_t units = (size_t)a->num_reqs * pl->max_segs * a->hkv;
+    const size_t rows = (size_t)a->max_q_len * 16;
+    pl->ws = round_up(units * rows * 128 * sizeof(float)) + round_up(units * rows * 2 * sizeof(float));
+  }
+  return true;
+}
+
+size_t attn_prefill_paged_workspace(const gcs_decode_args* a) {
+  PagedPlan pl;
+  if (!a || check_prefill_paged(a) != GCS_OK || !plan_prefill_paged(a, &pl)) return 0;
+  return pl.ws;
+}
+
+int attn_prefill_paged(const gcs_decode_args* a, void* out, void* workspace, size_t workspace_bytes,
+                       gcs_stream_t stream) {
+  int st = check_prefill_paged(a);
+  if (st != GCS_OK) return st;
+  if (!out || !aligned16(out)) return GCS_ERR_INVALID_ARG;
+  PagedPlan pl;
+  if (!plan_prefill_paged(a, &pl)) return GCS_ERR_CUDA;
+  if (pl.ws > 0 && (!workspace || workspace_bytes < pl.ws || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
+    return GCS_ERR_WORKSPACE;
+  int* status = device_status_ptr();
+  if (!status) return GCS_ERR_CUDA;
+  DecodeParams p;
+  fill_paged_params(a, out, status, p);
+  p.max_segs = pl.max_segs;
+  p.seg_pages = pl.seg_pages;
+  if (pl.ws > 0) {
+    const size_t units = (size_t)a->num_reqs * pl.max_segs * a->hkv;
+    const size_t rows = (size_t)a->max_q_len * 16;
+    p.part_acc = static_cast<float*>(workspace);
+    p.part_ml =
+        reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + round_up(units * rows * 128 * sizeof(float)));
+  }
+  KernelTimer timer(reinterpret_cast<cudaStream_t>(stream));
+  return cuda_status(launch_prefill_paged(p, reinterpret_cast<cudaStream_t>(stream), &timer.b, &timer.a));
 }
 
 int gcs_set_kernel_events(void* before, void* after) {

@@ -578,6 +578,10 @@ cudaError_t launch_decode(const DecodeParams& p, const DecodeMaps& maps, cudaStr
 #undef GCS_RUN
   if (ev_after && *ev_after) cudaEventRecord(*ev_after, s);
   if (e != cudaSuccess) return e;
+  return launch_decode_combine(p, s);
+}
+
+cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t s) {
   dim3 g2(p.num_reqs * p.max_q_len, p.hkv);
   decode_combine_kernel<<<g2, 256, 0, s>>>(p);
   return cudaGetLastError();

@@ -5,6 +5,7 @@
  *   attn_fwd           prefill forward  (O, LSE)
  *   attn_bwd           prefill backward (dQ, dK, dV, d log_gate, d sink)
  *   attn_decode_paged  paged single-query / short-query decode over an fp8 e4m3 KV cache
+ *   attn_prefill_paged paged chunked prefill (query chunks of any length) over the same cache
  *
  * Sources for what each call computes (page title, section):
  *   [FLA] fla-org/flash-linear-attention issue #1322 "[Perf] Gluon attention backend with
@@ -188,6 +189,29 @@ int attn_decode_paged(const gcs_decode_args* a, void* out, void* workspace, size
  * out: bf16 [total_q, hq, d]; returns the same statuses as attn_decode_paged. */
 int attn_decode_paged_noalloc(const gcs_decode_args* a, void* out, gcs_stream_t stream);
 
+/* ------------------------------------------------------------------ paged chunked prefill
+ * Attention of query chunks of any length over the same paged fp8 KV cache ([AIT] commit
+ * messages: a batch that is not all-decode takes the "2d" unified-attention route, one
+ * program per (kv head, query block)).  Arguments and semantics are those of
+ * attn_decode_paged (gcs_decode_args, the decoding features included), except:
+ *   - q_len = cu_q[r+1] - cu_q[r] may be any value in 1 .. seq_lens[r]; max_q_len >= 1 is
+ *     its host upper bound.  Query row t of request r still sits at position
+ *     seq_len - q_len + t and sees keys 0 .. seq_len - q_len + t (and the window).
+ *   - fp8 e4m3 with per-token or per-tensor scales; a bf16 cache is GCS_ERR_UNSUPPORTED.
+ *     (The pages' 2d route rejects per-token scales; here they are applied as in decode.)
+ *   - segment_len == 0 lets the library split the context: one segment per request when
+ *     the query blocks alone give about two CTAs per SM (the kernel then writes out
+ *     directly and needs no workspace), otherwise segments sized for that many CTAs whose
+ *     split-K partials the decode combine merges.  A positive segment_len must be a
+ *     multiple of 128 tokens.  attn_prefill_paged_workspace(a) gives the bytes needed
+ *     (0 when nothing is split; the choice depends on the current device's SM count).
+ *   - The tensor cores see Q rounded from bf16 to f16 (|q| < 65504), K and V as exact f16
+ *     from e4m3, and P * vscale rounded to f16 (vscale < 255), with fp32 accumulation.
+ * out: bf16 [total_q, hq, d].  Preconditions: q_len <= seq_len per request. */
+size_t attn_prefill_paged_workspace(const gcs_decode_args* a);
+int attn_prefill_paged(const gcs_decode_args* a, void* out, void* workspace, size_t workspace_bytes,
+                       gcs_stream_t stream);
+
 /* ------------------------------------------------------------------ status
  * Per-device status word written by kernels that gave up on a bounded wait.
  * Copies the word for the current device into *status (synchronous) and, if clear != 0,
@@ -196,10 +220,11 @@ int gcs_get_device_status(int* status, int clear);
 
 /* ------------------------------------------------------------------ instrumentation
  * Arms two caller-created CUDA events (cudaEvent_t, passed as void*) for the next attn_fwd,
- * attn_bwd or attn_decode_paged call made by this host thread: `before` is recorded on the
- * call's stream immediately before its main attention kernels (the prefill forward
- * kernel; the backward's attention kernels -- dQ pass + dK/dV pass, or the wide-head role
- * kernels; the split-K decode kernel) and `after` immediately after them, so
+ * attn_bwd, attn_decode_paged or attn_prefill_paged call made by this host thread: `before`
+ * is recorded on the call's stream immediately before its main attention kernels (the
+ * prefill forward kernel; the backward's attention kernels -- dQ pass + dK/dV pass, or the
+ * wide-head role kernels; the split-K decode kernel; the paged prefill kernel) and `after`
+ * immediately after them, so
  * cudaEventElapsedTime(before, after) is their device time.  The events are
  * disarmed once used; passing NULL, NULL disarms them.  Returns GCS_OK. */
 int gcs_set_kernel_events(void* before, void* after);

@@ -124,3 +124,22 @@ def test_decode_validation_on_host(L):
     assert dec(decode(g_cache=FAKE + 4)) == 1
     assert dec(decode(sink=FAKE + 2)) == 1
     assert L.attn_decode_workspace(b(decode(g_cache=FAKE, sink=FAKE + 4, window=1024))) > 0
+
+
+def test_prefill_paged_validation_and_workspace_on_host(L):
+    b = ctypes.byref
+    pp = lambda a, ws=1 << 40: L.attn_prefill_paged(b(a), FAKE, FAKE, ws, None)
+    # any q_len is accepted; the workspace holds the split-K partials of the chosen segments
+    a = decode(max_q_len=64, segment_len=256)
+    units, rows = 2 * (4096 // 256) * 4, 64 * 16
+    assert L.attn_prefill_paged_workspace(b(a)) == units * rows * 128 * 4 + units * rows * 2 * 4
+    # one segment per request: the kernel writes the output itself and needs no workspace
+    assert L.attn_prefill_paged_workspace(b(decode(max_q_len=64, segment_len=4096))) == 0
+    assert pp(a, ws=0) == 3
+    assert pp(decode(max_q_len=64, segment_len=200)) == 2  # not a whole number of 128-key tiles
+    assert pp(decode(max_q_len=64, kv_format=1, k_scale=None, v_scale=None)) == 2  # fp8 only
+    assert pp(decode(max_q_len=5000)) == 1  # more query rows than cached tokens
+    assert pp(decode(max_q_len=64, window=-1)) == 1
+    assert pp(decode(max_q_len=64, hq=32)) == 2
+    assert pp(decode(max_q_len=64, segment_len=-128)) == 1
+    assert L.attn_prefill_paged(b(decode(max_q_len=64)), FAKE + 8, FAKE, 1 << 40, None) == 1
