@@ -14,7 +14,9 @@
 // fp8 K and V pages come by tensor copy with the 128-byte swizzle, so the consumers' 16-B
 // reads of four rows at one column, or of two columns of two rows, hit eight different bank
 // groups; the scales (and gates) come by plain bulk copy.  Warps 1..4 each own one query position (16 query heads of the GQA
-// group = one m16 MMA tile) and a share of the pages; fp8 -> f16 conversion is exact,
+// group = one m16 MMA tile) and a share of the pages (the query's MMA fragments are kept in
+// shared memory, one copy per query position, so the loop runs without register spills);
+// fp8 -> f16 conversion is exact,
 // QK^T and PV run on mma.sync m16n8k16 with fp32 accumulation, softmax in fp32 (log2
 // units).  P * vscale is scaled by 2^8 before the f16 rounding (round-to-nearest, no
 // truncation bias) and the factor is removed in fp32 afterwards.
@@ -216,7 +218,9 @@ __global__ void __launch_bounds__(kThreads, 3)
   float m0 = neg_inf(), m1 = neg_inf(), l0 = 0.f, l1 = 0.f;
   bool ok = true;
 
-  if (active) {
+  // query fragments in shared memory, one copy per query position: [8 k-steps][32 lanes]
+  uint4* qf = reinterpret_cast<uint4*>(aux + C::NST * C::AUX) + mt * (8 * 32);
+  if (active && grp == 0) {
     uint32_t qa[8][4];
     {
       const uint16_t* q0p = p.q + ((size_t)(q_begin + mt) * p.hq + kvh * kGroup + g) * kD + 32 * tq;
@@ -239,6 +243,11 @@ __global__ void __launch_bounds__(kThreads, 3)
         qa[s][3] = KVF == 0 ? bf16pair_to_f16x2(w1[2 * s + 1]) : w1[2 * s + 1];
       }
     }
+#pragma unroll
+    for (int s = 0; s < 8; ++s) qf[s * 32 + lane] = make_uint4(qa[s][0], qa[s][1], qa[s][2], qa[s][3]);
+  }
+  named_bar_sync(1, 128);
+  if (active) {
     // one K and one V scale for the whole cache (fp8 per-tensor)
     const float kst = PT ? __ldg(p.k_scale) : 1.f, vst = PT ? __ldg(p.v_scale) : 1.f;
     // the query row's own cumulative gate (log2 units) for heads g and g + 8 of the group
@@ -294,10 +303,12 @@ __global__ void __launch_bounds__(kThreads, 3)
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
           uint32_t b0, b1;
+          const uint4 qv = qf[s * 32 + lane];
+          const uint32_t qa[4] = {qv.x, qv.y, qv.z, qv.w};
           e4m3x4_to_f16x2x2(kw0[s], b0, b1);
-          mma_f16(s0, qa[s], b0, b1);
+          mma_f16(s0, qa, b0, b1);
           e4m3x4_to_f16x2x2(kw1[s], b0, b1);
-          mma_f16(s1, qa[s], b0, b1);
+          mma_f16(s1, qa, b0, b1);
         }
       } else {
         // bf16 page: 16 keys x 256 B; this thread's 32 dims of keys g and g + 8 (64 B each)
@@ -314,8 +325,10 @@ __global__ void __launch_bounds__(kThreads, 3)
         // (values are read after the softmax and the stage is released then: fewer live registers)
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
-          mma_bf16(s0, qa[s], kw0[2 * s], kw0[2 * s + 1]);
-          mma_bf16(s1, qa[s], kw1[2 * s], kw1[2 * s + 1]);
+          const uint4 qv = qf[s * 32 + lane];
+          const uint32_t qa[4] = {qv.x, qv.y, qv.z, qv.w};
+          mma_bf16(s0, qa, kw0[2 * s], kw0[2 * s + 1]);
+          mma_bf16(s1, qa, kw1[2 * s], kw1[2 * s + 1]);
         }
       }
       // this thread's columns: slots 2tq, 2tq+1 (n-tile 0) and 8+2tq, 9+2tq (n-tile 1)
@@ -559,10 +572,11 @@ cudaError_t launch_decode(const DecodeParams& p, const DecodeMaps& maps, cudaStr
                           const cudaEvent_t* ev_before, const cudaEvent_t* ev_after) {
   dim3 g1(p.max_segs, p.hkv, p.num_reqs);
   auto run = [&](auto kern, int smem) -> cudaError_t {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem + 4096 * 4);
     if (e != cudaSuccess) return e;
     if (ev_before && *ev_before) cudaEventRecord(*ev_before, s);
-    kern<<<g1, kThreads, smem, s>>>(maps.k, maps.v, p);
+    // + the query fragments: 4 KB per query position
+    kern<<<g1, kThreads, smem + 4096 * p.max_q_len, s>>>(maps.k, maps.v, p);
     return cudaGetLastError();
   };
   cudaError_t e;
