@@ -530,8 +530,12 @@ int attn_prefill_paged(const gcs_decode_args* a, void* out, void* workspace, siz
     p.part_ml =
         reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + round_up(units * rows * 128 * sizeof(float)));
   }
+  DecodeMaps maps;
+  const uint64_t cache_rows = (uint64_t)a->num_blocks * a->hkv * a->block_size;
+  if (!make_page_map_u8(&maps.k, a->k_cache, cache_rows) || !make_page_map_u8(&maps.v, a->v_cache, cache_rows))
+    return GCS_ERR_CUDA;
   KernelTimer timer(reinterpret_cast<cudaStream_t>(stream));
-  return cuda_status(launch_prefill_paged(p, reinterpret_cast<cudaStream_t>(stream), &timer.b, &timer.a));
+  return cuda_status(launch_prefill_paged(p, maps, reinterpret_cast<cudaStream_t>(stream), &timer.b, &timer.a));
 }
 
 int gcs_set_kernel_events(void* before, void* after) {

@@ -120,8 +120,8 @@ cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t s);
 
 // Paged chunked prefill (any q_len) over an fp8 cache.  p.part_acc == nullptr: one segment
 // per request, the kernel writes p.out; otherwise split-K partials and the combine.
-cudaError_t launch_prefill_paged(const DecodeParams& p, cudaStream_t s, const cudaEvent_t* ev_before,
-                                 const cudaEvent_t* ev_after);
+cudaError_t launch_prefill_paged(const DecodeParams& p, const DecodeMaps& maps, cudaStream_t s,
+                                 const cudaEvent_t* ev_before, const cudaEvent_t* ev_after);
 
 // Size of the static scratch behind attn_decode_paged_noalloc (64 MiB).
 constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;

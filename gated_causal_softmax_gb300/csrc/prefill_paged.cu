@@ -14,9 +14,9 @@
 // accumulator, running max in log2 units and row sum) that the decode combine merges.
 //
 // Warp roles (384 threads):
-//   warp 0      producer: per 128-key tile, the 8 pages' K (2 KB each) with their K and V
-//               scales (64 B each) and the group's gates (1 KB), then the 8 V pages, by
-//               cp.async.bulk, one copy per lane
+//   warp 0      producer: per 128-key tile, the 8 pages' K (2 KB each, tensor copy with the
+//               128-byte swizzle) with their K and V scales (64 B each) and the group's gates
+//               (1 KB) by plain bulk copy, then the 8 V pages (swizzled), one copy per lane
 //   warp 1      tcgen05 issuer: S_x = Q_x K^T (both operands in shared memory) and
 //               O_x += P_x V (P in TMEM), interleaved PV_A(n), S_A(n+1), PV_B(n), S_B(n+1)
 //   warps 2-3   converters: e4m3 -> f16 (exact) into 128-byte-swizzled operand stages, slots
@@ -83,7 +83,9 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
 }
 
 template <bool FEAT>
-__global__ void __launch_bounds__(kThreads, 1) prefill_paged_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_paged_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                         const DecodeParams p) {
   using C = PpCfg<FEAT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -218,6 +220,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_paged_kernel(const Decode
       const bool per_token = p.scale_mode == 0;
       const bool has_gate = FEAT && p.g_cache != nullptr;
       const int pl = lane & 7, kind = lane >> 3;  // 0: K page, 1: K scales, 2: V scales, 3: gates
+      if (lane == 0) {
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+      }
       for (int n = 0; n < nt; ++n) {
         const int pg0 = pb + (hi_t - n) * 8;
         const int nv = min(8, pend - pg0);  // pages of the tile that exist
@@ -231,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_paged_kernel(const Decode
         const size_t slot0 = ((size_t)blk * p.hkv + kvh) * kPage;
         if (pl < nv) {
           if (kind == 0)
-            bulk_load(kraw + pl * 2048, p.k_cache + slot0 * kD, 2048, kr_full);
+            tma_load_2d(kraw + pl * 2048, &tmK, kr_full, 0, static_cast<int>(slot0));
           else if (kind == 1 && per_token)
             bulk_load(kraw + C::KR_KS + pl * 64, p.k_scale + slot0, 64, kr_full);
           else if (kind == 2 && per_token)
@@ -244,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_paged_kernel(const Decode
         if (!__all_sync(0xffffffffu, okl)) break;
         if (lane == 0) mbar_expect_tx(vr_full, nv * 2048);
         __syncwarp();
-        if (kind == 0 && pl < nv) bulk_load(vraw + pl * 2048, p.v_cache + slot0 * kD, 2048, vr_full);
+        if (kind == 0 && pl < nv) tma_load_2d(vraw + pl * 2048, &tmV, vr_full, 0, static_cast<int>(slot0));
       }
     } else if (warp == 1) {
       if (lane == 0) {
@@ -371,35 +377,37 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_paged_kernel(const Decode
           phase ^= 1;
         }
       };
-      // 8 pages of fp8 rows (128 B) -> f16 operand rows.  Item = (key, 16-byte group q of 16
-      // dims); a quarter warp takes one key's 8 groups, and the two 16-B halves of each result
-      // go to units (u, u + 1) of a 128-B-swizzled row in an order that keeps the eight stores
-      // of a quarter warp in eight different bank groups.
+      // 8 pages of fp8 rows (128 B, 128-byte swizzled) -> f16 operand rows.  Thread c takes the
+      // keys 8 i + (c & 7), i = 0..15, and the 16-dim group q = c / 8 of each: a quarter warp
+      // reads one group of eight consecutive keys and writes the two 16-B halves of each result
+      // to units (2 (q & 3), 2 (q & 3) + 1) of their swizzled rows, all in different bank groups.
       //   K (is_v false): stage sa holds dims 0..63, sb dims 64..127; row = key (K-major).
       //   V (is_v true):  stage sa holds keys 0..63, sb keys 64..127; inside a stage, dims
       //                   0..63 then 64..127 (8 KB apart), row = key (MN-major).
+      const int cq = c >> 3, ck = c & 7;
+      const uint32_t su0 = ((2 * (cq & 3)) ^ ck) << 4, su1 = ((2 * (cq & 3) + 1) ^ ck) << 4;
       auto convert = [&](const uint8_t* raw, int key0, bool is_v, uint32_t sa, uint32_t sb) {
+        const uint8_t* src = raw + ck * 128 + ((cq ^ ck) << 4);
+        uint8_t* dst_a;
+        uint8_t* dst_b;
+        if (!is_v) {
+          dst_a = dst_b = ring + ((cq >> 2) ? sb : sa) * kStage + ck * 128;
+        } else {
+          dst_a = ring + sa * kStage + (cq >> 2) * (kStage / 2) + ck * 128;
+          dst_b = ring + sb * kStage + (cq >> 2) * (kStage / 2) + ck * 128;
+        }
 #pragma unroll 4
         for (int i = 0; i < 16; ++i) {
-          const int it = 64 * i + c;
-          const int key = it >> 3, q = it & 7;
           uint4 xv = make_uint4(0u, 0u, 0u, 0u);
-          if (key0 + key < L) xv = lds128(raw + key * 128 + q * 16);
+          if (key0 + 8 * i + ck < L) xv = lds128(src + i * 1024);
           uint32_t w[8];
           e4m3x4_to_f16(xv.x, w[0], w[1]);
           e4m3x4_to_f16(xv.y, w[2], w[3]);
           e4m3x4_to_f16(xv.z, w[4], w[5]);
           e4m3x4_to_f16(xv.w, w[6], w[7]);
-          uint8_t* row;
-          if (!is_v)
-            row = ring + ((q >> 2) ? sb : sa) * kStage + key * 128;
-          else
-            row = ring + ((key >> 6) ? sb : sa) * kStage + (q >> 2) * (kStage / 2) + (key & 63) * 128;
-          const uint32_t u0 = 2 * (q & 3), sw = key & 7;
-          const bool swap = (q & 4) != 0;
-          const uint4 lo = make_uint4(w[0], w[1], w[2], w[3]), hi = make_uint4(w[4], w[5], w[6], w[7]);
-          sts128(row + (((swap ? u0 + 1 : u0) ^ sw) << 4), swap ? hi : lo);
-          sts128(row + (((swap ? u0 : u0 + 1) ^ sw) << 4), swap ? lo : hi);
+          uint8_t* row = !is_v ? dst_a + i * 1024 : (i < 8 ? dst_a + i * 1024 : dst_b + (i - 8) * 1024);
+          sts128(row + su0, make_uint4(w[0], w[1], w[2], w[3]));
+          sts128(row + su1, make_uint4(w[4], w[5], w[6], w[7]));
         }
       };
       for (int n = 0; n < nt; ++n) {
@@ -665,23 +673,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_paged_kernel(const Decode
 }
 
 template <bool FEAT>
-cudaError_t launch_t(const DecodeParams& p, int qpairs, cudaStream_t s) {
+cudaError_t launch_t(const DecodeParams& p, const DecodeMaps& maps, int qpairs, cudaStream_t s) {
   using C = PpCfg<FEAT>;
   auto kern = prefill_paged_kernel<FEAT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<dim3(qpairs * p.max_segs, p.hkv, p.num_reqs), kThreads, C::SMEM, s>>>(p);
+  kern<<<dim3(qpairs * p.max_segs, p.hkv, p.num_reqs), kThreads, C::SMEM, s>>>(maps.k, maps.v, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_prefill_paged(const DecodeParams& p, cudaStream_t s, const cudaEvent_t* ev_before,
-                                 const cudaEvent_t* ev_after) {
+cudaError_t launch_prefill_paged(const DecodeParams& p, const DecodeMaps& maps, cudaStream_t s,
+                                 const cudaEvent_t* ev_before, const cudaEvent_t* ev_after) {
   const int qpairs = (p.max_q_len + 2 * kPosPerTile - 1) / (2 * kPosPerTile);
   if (ev_before && *ev_before) cudaEventRecord(*ev_before, s);
   const bool feat = p.g_cache != nullptr || p.window > 0;
-  cudaError_t e = feat ? launch_t<true>(p, qpairs, s) : launch_t<false>(p, qpairs, s);
+  cudaError_t e = feat ? launch_t<true>(p, maps, qpairs, s) : launch_t<false>(p, maps, qpairs, s);
   if (ev_after && *ev_after) cudaEventRecord(*ev_after, s);
   if (e != cudaSuccess) return e;
   if (p.part_acc == nullptr) return cudaSuccess;
