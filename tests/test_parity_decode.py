@@ -219,3 +219,18 @@ def test_decode_sink_only_and_window_only(gcs_lib):
         ref = oracle_decode(dc)
         assert_close("out", out, ref, DECODE_RTOL)
         assert abs(bias(out, ref)) <= DECODE_BIAS
+
+
+@pytest.mark.parametrize("reading", ["A", "B"])
+def test_decode_rn_bias_is_far_below_the_limit(gcs_lib, reading):
+    """P * vscale is rounded to nearest (not truncated): at full size the relative signed bias
+    stays an order of magnitude inside the 1e-3 limit, in both scale readings (32 of the 64
+    requests, every query head)."""
+    dc = decode_config("paged_fp8_decode_64x1", scale_reading=reading)
+    out = run_decode(gcs_lib, dc)
+    pick = list(range(0, 64, 2))
+    sub = make_sub(dc, pick)
+    ref = oracle_decode(sub)
+    got = f64(out)[[int(dc.cu_q[r]) for r in pick]]
+    assert_close("out", got, ref, DECODE_RTOL)
+    assert abs(bias(got, ref)) <= 2e-4
