@@ -40,11 +40,13 @@ LAUNCHES_PER_PREFILL_STEP = 9
 LAUNCHES_PER_DECODE = 2
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the ncu captures
 # summarised in profiles/ (prefill_kernels_varlen_gqa_8192_d128.md,
-# decode_kernels_paged_fp8_decode_64x1.md); set back to None whenever the kernel changes.
+# decode_kernels_paged_fp8_decode_64x1.md, prefill_paged_kernel_paged_fp8_chunked_prefill_4x1024.md);
+# set back to None whenever the kernel changes.
 NCU_TRAFFIC = {
     "bwd": 217.9e6 + 277.0e6,  # prefill_bwd_dq_kernel<128> + prefill_bwd_kernel<128>
     "fwd": 119.8e6,            # prefill_fwd2_kernel<128>
-    "decode_split": None,  # decode_split_kernel (changed since its last capture)
+    "decode_split": 1155.4e6 + 19.2e6,  # decode_split_kernel<0, 0, 0>
+    "prefill_paged": 153.8e6 + 35.3e6,  # prefill_paged_kernel<0>
 }
 
 
