@@ -64,6 +64,7 @@ class PrefillArgs(ctypes.Structure):
         ("v", _vp),
         ("log_gate", _vp),
         ("sink", _vp),
+        ("deterministic", _c_int),
     ]
 
 
@@ -259,11 +260,13 @@ def attn_fwd(q, k, v, cu_seqlens, max_seqlen=None, scale=None, window=0, log_gat
 
 
 def attn_bwd(q, k, v, o, lse, dout, cu_seqlens, max_seqlen=None, scale=None, window=0, log_gate=None, sink=None,
-             workspace=None, dq=None, dk=None, dv=None, dlog_gate=None, dsink=None):
+             workspace=None, dq=None, dk=None, dv=None, dlog_gate=None, dsink=None, deterministic=False):
     """Prefill backward of sum(O * dO).  Returns dq, dk, dv (bf16), dlog_gate fp32 [tot, hq]
-    (None without gates) and dsink fp32 [hq] (None without sink)."""
+    (None without gates) and dsink fp32 [hq] (None without sink).  deterministic=True makes
+    head dims above 128 take the fixed-order route (dims <= 128 always do)."""
     L = load()
     a = prefill_args(q, k, v, cu_seqlens, max_seqlen, scale, window, log_gate, sink)
+    a.deterministic = 1 if deterministic else 0
     _need(o, torch.bfloat16, "o")
     _need(dout, torch.bfloat16, "dout")
     _need(lse, torch.float32, "lse")

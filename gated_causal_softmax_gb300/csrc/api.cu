@@ -107,6 +107,7 @@ int check_prefill(const gcs_prefill_args* a) {
     return GCS_ERR_INVALID_ARG;
   if (a->hq % a->hkv != 0) return GCS_ERR_INVALID_ARG;
   if (a->window < 0) return GCS_ERR_INVALID_ARG;
+  if (a->deterministic != 0 && a->deterministic != 1) return GCS_ERR_INVALID_ARG;
   if (!std::isfinite(a->scale)) return GCS_ERR_INVALID_ARG;
   if (!a->cu_seqlens || !a->q || !a->k || !a->v) return GCS_ERR_INVALID_ARG;
   if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v)) return GCS_ERR_INVALID_ARG;
@@ -148,7 +149,7 @@ size_t bwd_ws(const gcs_prefill_args* a) {
   const size_t ht = (size_t)a->hq * a->total_tokens;
   if (a->log_gate) c.take<float>(ht);                         // G^T
   c.take<float>(ht);                                           // delta
-  if (!two_pass(a)) c.take<float>((size_t)a->total_tokens * a->hq * a->dqk);  // dQ accumulator
+  if (!two_pass(a) && !a->deterministic) c.take<float>((size_t)a->total_tokens * a->hq * a->dqk);  // dQ accumulator
   if (a->log_gate || a->sink) c.take<float>(ht);               // row sums of dS
   if (a->log_gate) c.take<float>(ht);                          // column sums of dS
   c.take<float>((size_t)a->hq * ((a->total_tokens + 63) / 64 + a->num_seqs) * 128);  // packed vectors
@@ -258,7 +259,9 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
   float* gT = a->log_gate ? c.take<float>(ht) : nullptr;
   float* delta = c.take<float>(ht);
   const bool tp = two_pass(a);
-  float* dq_acc = tp ? nullptr : c.take<float>((size_t)a->total_tokens * a->hq * a->dqk);
+  const bool wide_det = !tp && a->deterministic;
+  // fp32 dQ accumulator: wide heads on the reduce-add route only
+  float* dq_acc = (tp || wide_det) ? nullptr : c.take<float>((size_t)a->total_tokens * a->hq * a->dqk);
   float* dg_row = (a->log_gate || a->sink) ? c.take<float>(ht) : nullptr;
   float* dg_col = a->log_gate ? c.take<float>(ht) : nullptr;
   const int n_qtiles = (a->total_tokens + 63) / 64 + a->num_seqs;
@@ -320,9 +323,16 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
     if (st != GCS_OK) return st;
     st = cuda_status(launch_prefill_bwd(p, maps, num_tiles, s));
     timer.after();
+  } else if (wide_det) {
+    // dQ pass (query tiles of 64 rows), then the dK / dV roles; the timer brackets both
+    timer.before();
+    st = cuda_status(launch_prefill_bwd_wide_dq(p, maps, n_qtiles, s));
+    if (st != GCS_OK) return st;
+    st = cuda_status(launch_prefill_bwd_wide(p, maps, num_tiles, false, s));
+    timer.after();
   } else {
     timer.before();
-    st = cuda_status(launch_prefill_bwd_wide(p, maps, num_tiles, s));
+    st = cuda_status(launch_prefill_bwd_wide(p, maps, num_tiles, true, s));
     timer.after();
   }
   if (st != GCS_OK) return st;

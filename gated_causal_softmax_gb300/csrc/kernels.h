@@ -47,7 +47,7 @@ struct BwdParams {
   uint16_t* grad_q;      // bf16 [total, hq, dqk] (written directly by the dQ pass)
   uint16_t* grad_k;      // bf16 [total, hkv, dqk]
   uint16_t* grad_v;      // bf16 [total, hkv, dv]
-  float* dq_acc;         // fp32 [total, hq, dqk] (zeroed; wide head dims only)
+  float* dq_acc;         // fp32 [total, hq, dqk] (zeroed; wide heads, reduce-add route only)
   float* dg_row;         // fp32 [hq, total] sum_j dS_ij; null if not needed
   float* dg_col;         // fp32 [hq, total] sum_i dS_ij (zeroed); null if no gate
   const float* vecp;     // packed per-(head, 64-row query tile) vectors (see launch_bwd_pack)
@@ -63,8 +63,12 @@ struct BwdMaps {
 cudaError_t launch_prefill_bwd(const BwdParams& p, const BwdMaps& maps, int num_kv_tiles, cudaStream_t s);
 // dQ pass of the two-pass backward (head dims <= 128): writes dQ (bf16) and dS row sums.
 cudaError_t launch_prefill_bwd_dq(const BwdParams& p, const BwdMaps& maps, int num_q_tiles, cudaStream_t s);
-// Head dims above 128: output-column roles (dV chunks; dK + dQ chunks), two launches.
-cudaError_t launch_prefill_bwd_wide(const BwdParams& p, const BwdMaps& maps, int num_kv_tiles, cudaStream_t s);
+// Head dims above 128, key-stationary output-column roles: dV chunks, and dK chunks that
+// also reduce-add dQ and the dS row sums into fp32 buffers (with_dq) or leave them to the
+// query-stationary dQ pass (deterministic route; it writes dQ in bf16 and the row sums).
+cudaError_t launch_prefill_bwd_wide_dq(const BwdParams& p, const BwdMaps& maps, int num_q_tiles, cudaStream_t s);
+cudaError_t launch_prefill_bwd_wide(const BwdParams& p, const BwdMaps& maps, int num_kv_tiles, bool with_dq,
+                                    cudaStream_t s);
 
 // Small HBM-bound helpers.
 cudaError_t launch_gate_cumsum(const float* g, const int32_t* cu, int num_seqs, int total, int hq, float* gT,

@@ -7,6 +7,8 @@
 // work of one (128-key tile, kv head) is therefore split over CTAs by output columns:
 //   role V   (kind 0):  dV[:, v0 : v0+256)                 needs P  -> recomputes S
 //   role KQ  (kind 1):  dK[:, k0 : k0+256), dQ[:, k0 : k0+256)  needs dS -> recomputes S, dP
+//   role K   (kind 2):  dK[:, k0 : k0+256) only, for the deterministic backward, whose dQ and
+//                       dS row sums come from the query-stationary pass (prefill_bwd_wide_dq.cu)
 // Every role recomputes the full-width contractions it needs; the extra work is the price
 // of fitting the accumulators in TMEM.  Operands stream through a ring of 16 KB stages
 // (128 x 64 or 64 x 64 bf16 chunks, 128-B swizzle); the K columns a role keeps using
@@ -15,7 +17,10 @@
 //     S^T = K Q^T (TMEM)   [dP^T = V dO^T (TMEM)]   P^T / dS^T in fp32, bf16 operands
 //     role V:  dV  += P^T dO[:, v0..]
 //     role KQ: dK  += dS^T Q[:, k0..];  dQ^T[k0..] = K[:, k0..]^T dS^T -> fp32 reduce-adds
-// Row / column sums of dS (gate and sink gradients) are taken by the KQ role with k0 = 0.
+//     role K:  dK  += dS^T Q[:, k0..]
+// Row / column sums of dS (gate and sink gradients) are taken by the KQ role with k0 = 0; the
+// K role takes the column sums only (thread-local per key row and head, added once to a
+// zeroed entry, so they do not depend on scheduling).
 #include "kernels.h"
 #include "sm103_ptx.cuh"
 #include "tiles.cuh"
@@ -39,7 +44,7 @@ __device__ __forceinline__ void red_add_f32(float* addr, float v) {
 template <int DQK, int DV, int KIND>
 struct WideCfg {
   static constexpr int KCH = DQK / 64, VCH = DV / 64, WCH = kW / 64;
-  static constexpr int NRES = (KIND == 1 ? kW : (DQK < kW ? DQK : kW)) / 64;  // resident K chunks
+  static constexpr int NRES = (KIND >= 1 ? kW : (DQK < kW ? DQK : kW)) / 64;  // resident K chunks
   static constexpr int NST = 8;
   static constexpr int OFF_KRES = 0;
   static constexpr int OFF_RING = OFF_KRES + NRES * kStage;
@@ -66,8 +71,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!lpt_tile(p.cu_seqlens, p.num_seqs, kBN, blockIdx.y, tr)) return;
   const int seq_start = tr.start, len = tr.len, jt = tr.n - 1 - tr.u;
   const int kvh = blockIdx.x;
-  const int w0 = blockIdx.z * kW;         // v0 (role V) or k0 (role KQ)
-  const int res0 = (KIND == 1) ? w0 / 64 : 0;  // first resident K chunk
+  const int w0 = blockIdx.z * kW;         // v0 (role V) or k0 (roles KQ, K)
+  const int res0 = (KIND >= 1) ? w0 / 64 : 0;  // first resident K chunk
   const int group = p.hq / p.hkv;
   const int j0 = jt * kBN;
   const int it_lo = j0 / kBM;
@@ -75,7 +80,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (p.window > 0) i_hi = min(i_hi, j0 + kBN - 1 + p.window - 1);
   const int n_it = i_hi / kBM - it_lo + 1;
   const int nsteps = n_it * group;
-  const bool sums = (KIND == 1) && (w0 == 0);  // this role takes the dS row / column sums
+  const bool sums = (KIND >= 1) && (w0 == 0);  // this role takes the dS column (and row) sums
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* full = bars;                 // [NST]
@@ -148,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (c < res0 || c >= res0 + C::NRES) ok = issue(&tmK, kvh * DQK + c * 64, yk, kStage);
           if (ok) ok = issue(&tmQ, h * DQK + c * 64, yq, kStage / 2);
         }
-        if (KIND == 1) {
+        if (KIND >= 1) {
           for (int c = 0; c < C::VCH && ok; ++c) {
             ok = issue(&tmV, kvh * DV + c * 64, yk, kStage);
             if (ok) ok = issue(&tmDO, h * DV + c * 64, yq, kStage / 2);
@@ -228,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           give();
         }
         if (!ok) break;
-        if (KIND == 1) {
+        if (KIND >= 1) {
           // dP^T = V dO^T over all of DV
           for (int c = 0; c < C::VCH && ok; ++c) {
             uint32_t a = 0, bq = 0;
@@ -252,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         tc_fence_after();
         // accumulator += (P^T or dS^T) x (dO or Q) chunk by chunk (N = 64 each)
-        const uint32_t aT = tmem + (KIND == 1 ? C::T_DP : C::T_S);
+        const uint32_t aT = tmem + (KIND >= 1 ? C::T_DP : C::T_S);
         for (int c = 0; c < C::WCH && ok; ++c) {
           uint32_t bq = 0;
           ok = take(bq);
@@ -294,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_off + C::T_S, tDP = tmem + lane_off + C::T_DP;
     const int jl = j0 + r;
     const bool has_gate = p.gT != nullptr;
-    const bool want_row = sums && p.dg_row != nullptr;
+    const bool want_row = KIND == 1 && sums && p.dg_row != nullptr;
     uint8_t* sDS = smem + C::OFF_DS;
     float dgcol = 0.f, rowterm = 0.f;
     int cur_h = -1;
@@ -321,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ch = 0; ch < 2; ++ch) {
         uint32_t sv[32], dp[32];
         tmem_ld32(tS + 32 * ch, sv);
-        if (KIND == 1) tmem_ld32(tDP + 32 * ch, dp);
+        if (KIND >= 1) tmem_ld32(tDP + 32 * ch, dp);
         tmem_ld_wait();
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
@@ -334,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const float pr = ex2(t);
           sv[c] = __float_as_uint(pr);
-          if (KIND == 1) dp[c] = __float_as_uint(pr * (__uint_as_float(dp[c]) - vec[kBM + col]));
+          if (KIND >= 1) dp[c] = __float_as_uint(pr * (__uint_as_float(dp[c]) - vec[kBM + col]));
         }
         uint32_t pk[16];
         if (KIND == 0) {
@@ -347,10 +352,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 16; ++c)
             pk[c] = pack_bf16x2(__uint_as_float(dp[2 * c]), __uint_as_float(dp[2 * c + 1]));
           tmem_st16(tDP + 16 * ch, pk);
+          if (KIND == 1) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<uint4*>(sDS + sw128_offset(r, 4 * ch + q)) =
-                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            for (int q = 0; q < 4; ++q)
+              *reinterpret_cast<uint4*>(sDS + sw128_offset(r, 4 * ch + q)) =
+                  make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          }
           if (sums && has_gate) {
             float acc = 0.f;
 #pragma unroll
@@ -415,10 +422,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && nsteps > 0) {
       tc_fence_after();
       const bool row_ok = jl < len;
-      uint16_t* dst = (KIND == 1)
+      uint16_t* dst = (KIND >= 1)
                           ? p.grad_k + ((size_t)(seq_start + (row_ok ? jl : 0)) * p.hkv + kvh) * DQK + w0
                           : p.grad_v + ((size_t)(seq_start + (row_ok ? jl : 0)) * p.hkv + kvh) * DV + w0;
-      const float sc = (KIND == 1) ? p.scale : 1.f;
+      const float sc = (KIND >= 1) ? p.scale : 1.f;
 #pragma unroll 1
       for (int c = 0; c < kW / 32; ++c) {
         uint32_t v[32];
@@ -456,24 +463,25 @@ cudaError_t launch_t(const BwdParams& p, const BwdMaps& maps, int num_tiles, cud
   auto kern = prefill_bwd_wide_kernel<DQK, DV, KIND>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  const int roles = (KIND == 1 ? DQK : DV) / kW;
+  const int roles = (KIND >= 1 ? DQK : DV) / kW;
   kern<<<dim3(p.hkv, num_tiles, roles), kThreads, C::SMEM, s>>>(maps.q, maps.k, maps.v, maps.dout, p);
   return cudaGetLastError();
 }
 
 template <int DQK, int DV>
-cudaError_t launch_both(const BwdParams& p, const BwdMaps& maps, int num_tiles, cudaStream_t s) {
-  cudaError_t e = launch_t<DQK, DV, 1>(p, maps, num_tiles, s);
+cudaError_t launch_both(const BwdParams& p, const BwdMaps& maps, int num_tiles, bool with_dq, cudaStream_t s) {
+  cudaError_t e = with_dq ? launch_t<DQK, DV, 1>(p, maps, num_tiles, s) : launch_t<DQK, DV, 2>(p, maps, num_tiles, s);
   if (e != cudaSuccess) return e;
   return launch_t<DQK, DV, 0>(p, maps, num_tiles, s);
 }
 
 }  // namespace
 
-cudaError_t launch_prefill_bwd_wide(const BwdParams& p, const BwdMaps& maps, int num_kv_tiles, cudaStream_t s) {
-  if (p.dqk == 256 && p.dv == 256) return launch_both<256, 256>(p, maps, num_kv_tiles, s);
-  if (p.dqk == 256 && p.dv == 512) return launch_both<256, 512>(p, maps, num_kv_tiles, s);
-  if (p.dqk == 512 && p.dv == 512) return launch_both<512, 512>(p, maps, num_kv_tiles, s);
+cudaError_t launch_prefill_bwd_wide(const BwdParams& p, const BwdMaps& maps, int num_kv_tiles, bool with_dq,
+                                    cudaStream_t s) {
+  if (p.dqk == 256 && p.dv == 256) return launch_both<256, 256>(p, maps, num_kv_tiles, with_dq, s);
+  if (p.dqk == 256 && p.dv == 512) return launch_both<256, 512>(p, maps, num_kv_tiles, with_dq, s);
+  if (p.dqk == 512 && p.dv == 512) return launch_both<512, 512>(p, maps, num_kv_tiles, with_dq, s);
   return cudaErrorInvalidValue;
 }
 

@@ -23,14 +23,14 @@ def to_dev(case):
                 g=mv(case.log_gate), s=mv(case.sink))
 
 
-def run_prefill(gcs, case, backward=True):
+def run_prefill(gcs, case, backward=True, deterministic=False):
     d = to_dev(case)
     ms = max(case.seqlens)
     o, lse = gcs.attn_fwd(d["q"], d["k"], d["v"], d["cu"], ms, case.scale, case.window, d["g"], d["s"])
     grads = None
     if backward:
         grads = gcs.attn_bwd(d["q"], d["k"], d["v"], o, lse, d["do"], d["cu"], ms, case.scale, case.window, d["g"],
-                             d["s"])
+                             d["s"], deterministic=deterministic)
     torch.cuda.synchronize()
     assert gcs.get_device_status() == 0
     return o, lse, grads

@@ -68,6 +68,7 @@ def test_prefill_validation_on_host(L):
     assert fwd(prefill(q=None)) == 1
     assert fwd(prefill(q=FAKE + 2)) == 1  # misaligned
     assert fwd(prefill(window=-1)) == 1
+    assert fwd(prefill(deterministic=2)) == 1
     assert fwd(prefill(scale=float("nan"))) == 1
     assert fwd(prefill(dqk=96, dv=96)) == 2  # not a compiled head dim
     assert fwd(prefill(dqk=128, dv=256)) == 2
@@ -86,12 +87,15 @@ def test_workspace_sizes_on_host(L):
     assert L.attn_fwd_workspace(b(prefill())) == 0
     assert L.attn_fwd_workspace(b(prefill(log_gate=FAKE))) == 4 * 4 * 256
     ws = L.attn_bwd_workspace(b(prefill(log_gate=FAKE, sink=FAKE)))
-    # head dims <= 128 (two-pass backward): G^T, delta, dS row sums, dS column sums,
-    # packed per-tile vectors; wider heads add the fp32 dQ accumulator
+    # G^T, delta, dS row sums, dS column sums, packed per-tile vectors; wider heads on the
+    # reduce-add route add the fp32 dQ accumulator, the deterministic route does not
     n_qtiles = 256 // 64 + 1
     assert ws == 4 * (4 * 256) * 4 + 4 * n_qtiles * 128 * 4
     ws_wide = L.attn_bwd_workspace(b(prefill(log_gate=FAKE, sink=FAKE, dqk=256, dv=512)))
     assert ws_wide == 4 * (4 * 256) * 4 + 256 * 4 * 256 * 4 + 4 * n_qtiles * 128 * 4
+    ws_det = L.attn_bwd_workspace(b(prefill(log_gate=FAKE, sink=FAKE, dqk=256, dv=512, deterministic=1)))
+    assert ws_det == ws
+    assert L.attn_bwd_workspace(b(prefill(log_gate=FAKE, sink=FAKE, deterministic=1))) == ws
     units, rows = 2 * 2 * 4, 16
     assert L.attn_decode_workspace(b(decode())) == units * rows * 128 * 4 + units * rows * 2 * 4
     assert L.attn_decode_workspace(b(decode(max_q_len=5))) == 0

@@ -7,7 +7,7 @@ import torch
 
 import oracle
 from synth import make_prefill, prefill_config
-from helpers import PREFILL_RTOL, assert_close, f64, oracle_prefill, run_prefill
+from helpers import PREFILL_RTOL, assert_close, f64, oracle_prefill, run_prefill, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -26,11 +26,14 @@ CASES = {
 }
 
 
-@pytest.mark.parametrize("name", list(CASES))
-def test_prefill_parity(gcs_lib, name):
+PARITY_RUNS = [(n, False) for n in CASES] + [(n, True) for n in CASES if CASES[n][3] > 128 or CASES[n][4] > 128]
+
+
+@pytest.mark.parametrize("name,deterministic", PARITY_RUNS)
+def test_prefill_parity(gcs_lib, name, deterministic):
     lens, hq, hkv, dqk, dv, gate, sink, window, bwd = CASES[name]
     case = make_prefill(lens, hq, hkv, dqk, dv, seed=100 + len(name), gate=gate, sink=sink, window=window)
-    o, lse, grads = run_prefill(gcs_lib, case, backward=bwd)
+    o, lse, grads = run_prefill(gcs_lib, case, backward=bwd, deterministic=deterministic)
     ro, rlse, rg = oracle_prefill(case, backward=bwd)
     assert_close("o", o, ro, PREFILL_RTOL)
     np.testing.assert_allclose(f64(lse), rlse, rtol=0, atol=2e-3)
@@ -51,6 +54,27 @@ def test_prefill_parity(gcs_lib, name):
             assert_close("dsink", ds, rds, PREFILL_RTOL)
         else:
             assert ds is None
+
+
+@pytest.mark.parametrize("dims", [(128, 128), (256, 512), (512, 512)])
+def test_backward_is_deterministic(gcs_lib, dims):
+    """Every gradient is written once or summed in a fixed order (head dims <= 128 always;
+    wider heads with deterministic=True): repeated backward calls agree bit for bit."""
+    dqk, dv = dims
+    case = make_prefill([300, 141, 77], 4, 2, dqk, dv, seed=150 + dqk, gate=True, sink=True, window=0)
+    d = to_dev(case)
+    ms = max(case.seqlens)
+    o, lse = gcs_lib.attn_fwd(d["q"], d["k"], d["v"], d["cu"], ms, case.scale, case.window, d["g"], d["s"])
+    runs = []
+    for _ in range(3):
+        g = gcs_lib.attn_bwd(d["q"], d["k"], d["v"], o, lse, d["do"], d["cu"], ms, case.scale, case.window, d["g"],
+                             d["s"], deterministic=True)
+        torch.cuda.synchronize()
+        runs.append([t.clone() for t in g])
+    assert gcs_lib.get_device_status() == 0
+    for other in runs[1:]:
+        for name, a, b in zip(("dq", "dk", "dv", "dlog_gate", "dsink"), runs[0], other):
+            assert torch.equal(a, b), name
 
 
 def test_unsupported_head_dims_raise(gcs_lib):
@@ -85,9 +109,9 @@ def test_prefill_gather_order_is_exact(gcs_lib):
     np.testing.assert_array_equal(got[:, :, 1].numpy(), (idx // 256).float()[:, None].expand(tot, hq).numpy())
 
 
-def _sampled_full_size(gcs_lib, name, kv_group=1, backward=True, seqs=None):
+def _sampled_full_size(gcs_lib, name, kv_group=1, backward=True, seqs=None, deterministic=False):
     case = prefill_config(name)
-    o, lse, grads = run_prefill(gcs_lib, case, backward=backward)
+    o, lse, grads = run_prefill(gcs_lib, case, backward=backward, deterministic=deterministic)
     hq, hkv = case.hq, case.hkv
     group = hq // hkv
     heads = list(range(kv_group * group, (kv_group + 1) * group))
@@ -136,11 +160,15 @@ def test_full_size_dense_mha_t128_d64(gcs_lib):
         assert_close(n, got, ref, PREFILL_RTOL)
 
 
-def test_full_size_window_dqk256_dv512_sampled(gcs_lib):
-    _sampled_full_size(gcs_lib, "window_b2_t4096_dqk256_dv512", kv_group=3, backward=True, seqs=[1])
+@pytest.mark.parametrize("deterministic", [False, True])
+def test_full_size_window_dqk256_dv512_sampled(gcs_lib, deterministic):
+    _sampled_full_size(gcs_lib, "window_b2_t4096_dqk256_dv512", kv_group=3, backward=True, seqs=[1],
+                       deterministic=deterministic)
 
 
-def test_full_size_varlen_d512_sampled(gcs_lib):
+@pytest.mark.parametrize("deterministic", [False, True])
+def test_full_size_varlen_d512_sampled(gcs_lib, deterministic):
     case = prefill_config("varlen_16384_d512")
     shortest = int(np.argmin(case.seqlens))
-    _sampled_full_size(gcs_lib, "varlen_16384_d512", kv_group=2, backward=True, seqs=[shortest])
+    _sampled_full_size(gcs_lib, "varlen_16384_d512", kv_group=2, backward=True, seqs=[shortest],
+                       deterministic=deterministic)
