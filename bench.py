@@ -33,6 +33,7 @@ METRIC = "prefill fwd+bwd causal TFLOP/s (% bf16 peak); paged decode GB/s (% HBM
 PREFILL_WORKLOAD = "varlen_gqa_8192_d128"
 DECODE_WORKLOAD = "paged_fp8_decode_64x1"
 CHUNK_WORKLOAD = "paged_fp8_chunked_prefill_4x1024"
+WIDE_WORKLOAD = "window_b2_t4096_dqk256_dv512"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # my kernels per prefill step with gates and sink: fwd (gate cumsum, attention) and bwd
 # (gate cumsum, delta, vector pack, dQ pass, dK/dV pass, d gate scan, d sink reduce)
@@ -384,6 +385,40 @@ def run_native(args):
     if gcs.get_device_status() != 0:
         raise RuntimeError("a decode kernel timed out")
 
+    # ------------------------------------------------ wide heads: Dqk 256 / Dv 512, window 1024
+    wc = prefill_config(WIDE_WORKLOAD)
+    wq, wk, wv, wdo = (t.to(dev) for t in (wc.q, wc.k, wc.v, wc.do))
+    wg, wsk, wcu = wc.log_gate.to(dev), wc.sink.to(dev), wc.cu_seqlens.to(dev)
+    wms = max(wc.seqlens)
+    wide = {"workload": WIDE_WORKLOAD, "unit": "TFLOP/s"}
+    w_fwd_fl, w_bwd_fl = prefill_flops(wc.seqlens, wc.hq, wc.dqk, wc.dv, wc.window)
+    for mode, det in (("reduce_add", False), ("deterministic", True)):
+        def wstep():
+            o_, l_ = gcs.attn_fwd(wq, wk, wv, wcu, wms, wc.scale, wc.window, log_gate=wg, sink=wsk)
+            gcs.attn_bwd(wq, wk, wv, o_, l_, wdo, wcu, wms, wc.scale, wc.window, log_gate=wg, sink=wsk,
+                         deterministic=det)
+
+        for _ in range(args.warmup):
+            wstep()
+        barrier(world)
+        torch.cuda.synchronize()
+        w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        w0.record()
+        for _ in range(DK):
+            wstep()
+        w1.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        w_ms = max_over_ranks(world, w0.elapsed_time(w1)) / DK
+        w_tf = (w_fwd_fl + w_bwd_fl) * world / (w_ms * 1e-3) / 1e12
+        wide[mode] = {"value": round(w_tf, 1), "pct_of_peak": round(w_tf / world / sustained, 4),
+                      "ms_per_step": round(w_ms, 4)}
+    wide["flops_per_step"] = w_fwd_fl + w_bwd_fl
+    if gcs.get_device_status() != 0:
+        raise RuntimeError("a wide-head kernel timed out")
+    del wq, wk, wv, wdo, wg, wsk, wcu
+    torch.cuda.empty_cache()
+
     # ------------------------------------------------ paged chunked prefill (fp8 cache)
     pc = decode_config(CHUNK_WORKLOAD)
     pd = dict(q=pc.q.to(dev), kc=pc.k_cache.to(dev), vc=pc.v_cache.to(dev), ks=pc.k_scale.to(dev),
@@ -458,6 +493,7 @@ def run_native(args):
         "roofline": roofline,
         "decode": decode,
         "chunked_prefill": chunked,
+        "wide_prefill": wide,
         "cpu_baseline": cpu,
         "clocks": clocks,
         "e2e": e2e,
