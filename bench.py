@@ -542,6 +542,9 @@ def run_native(args):
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(case, min_seconds=10.0)
+        # the same oracle beside the decode and the chunked prefill, each on a bounded sample
+        decode["cpu_baseline"] = cpu_baseline_paged(dc, [(r, 0) for r in range(0, 64, 8)], "GB/s")
+        chunked["cpu_baseline"] = cpu_baseline_paged(pc, [(r, t) for r in range(4) for t in (0, 1023)], "TFLOP/s")
 
     line = {
         "metric": METRIC,
@@ -620,6 +623,47 @@ def cpu_baseline(case, min_seconds=10.0):
             break
     return {"value": round(fl * n / dt / 1e12, 6), "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)),
             "kind": "oracle", "sample": f"{desc}; repeated {n}x over {dt:.1f} s"}
+
+
+def _oracle_paged(dc, rows):
+    """The oracle on single-row requests: row t of request r becomes a request of one query
+    row whose context ends at that row's position (the row's exact result)."""
+    import numpy as np
+
+    import oracle  # CPU baseline legs only
+
+    seq, cu, bt, qi = [], [0], [], []
+    for r, t in rows:
+        L = int(dc.seq_lens[r])
+        ql = int(dc.cu_q[r + 1] - dc.cu_q[r])
+        seq.append(L - ql + t + 1)
+        cu.append(cu[-1] + 1)
+        bt.append(dc.block_table[r].numpy())
+        qi.append(int(dc.cu_q[r]) + t)
+    oracle.decode_paged(dc.q[qi].double().numpy(), dc.k_cache.numpy(), dc.v_cache.numpy(), dc.k_scale.numpy(),
+                        dc.v_scale.numpy(), np.stack(bt), np.array(seq), np.array(cu), dc.scale)
+    return seq
+
+
+def cpu_baseline_paged(dc, rows, unit, min_seconds=5.0):
+    """Oracle time on a bounded sample of a paged workload, in the leg's own unit: GB/s of the
+    decode's algorithmic bytes or TFLOP/s of the chunk's algorithmic flops for the sampled rows."""
+    n, t0 = 0, time.perf_counter()
+    while True:
+        seq = _oracle_paged(dc, rows)
+        n += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds:
+            break
+    if unit == "GB/s":
+        work = decode_bytes(seq, [1] * len(seq), dc.hq, dc.hkv, dc.d, dc.block_size)
+        value = work * n / dt / 1e9
+    else:
+        work = paged_chunk_flops(seq, [1] * len(seq), dc.hq, dc.d)
+        value = work * n / dt / 1e12
+    return {"value": round(value, 6), "unit": unit, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"oracle (numpy fp64) on {len(rows)} query rows of the workload, every query head; "
+                      f"repeated {n}x over {dt:.1f} s"}
 
 
 # ----------------------------------------------------------------------------- reference arm
