@@ -27,6 +27,7 @@ __all__ = [
     "attn_decode_paged",
     "attn_decode_paged_noalloc",
     "attn_prefill_paged",
+    "selftest_bounded_wait",
     "PrefillArgs",
     "DecodeArgs",
     "GcsError",
@@ -137,6 +138,8 @@ def _declare(lib: ctypes.CDLL) -> None:
     lib.attn_prefill_paged.restype = _c_int
     lib.gcs_get_device_status.argtypes = [P(_c_int), _c_int]
     lib.gcs_get_device_status.restype = _c_int
+    lib.gcs_selftest_bounded_wait.argtypes = [_vp]
+    lib.gcs_selftest_bounded_wait.restype = _c_int
     lib.gcs_set_kernel_events.argtypes = [_vp, _vp]
     lib.gcs_set_kernel_events.restype = _c_int
 
@@ -202,6 +205,14 @@ def get_device_status(clear: bool = True) -> int:
     st = _c_int(0)
     _check(load().gcs_get_device_status(ctypes.byref(st), 1 if clear else 0), "gcs_get_device_status")
     return st.value
+
+
+def selftest_bounded_wait() -> int:
+    """Runs the bounded-wait self-test kernel on the current stream, waits for it and returns
+    (and clears) the device status word: GCS_ERR_DEVICE_TIMEOUT (5) when the wait gave up."""
+    _check(load().gcs_selftest_bounded_wait(_stream()), "gcs_selftest_bounded_wait")
+    torch.cuda.synchronize()
+    return get_device_status(clear=True)
 
 
 def prefill_args(q, k, v, cu_seqlens, max_seqlen, scale, window, log_gate, sink) -> PrefillArgs:

@@ -554,6 +554,12 @@ int gcs_set_kernel_events(void* before, void* after) {
   return GCS_OK;
 }
 
+int gcs_selftest_bounded_wait(gcs_stream_t stream) {
+  int* d = device_status_ptr();
+  if (!d) return GCS_ERR_CUDA;
+  return cuda_status(launch_bounded_wait_selftest(d, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int gcs_get_device_status(int* status, int clear) {
   if (!status) return GCS_ERR_INVALID_ARG;
   int* d = device_status_ptr();

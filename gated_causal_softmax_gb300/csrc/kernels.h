@@ -127,6 +127,10 @@ cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_prefill_paged(const DecodeParams& p, const DecodeMaps& maps, cudaStream_t s,
                                  const cudaEvent_t* ev_before, const cudaEvent_t* ev_after);
 
+// One CTA that waits on a barrier phase nothing completes; its bounded wait records a
+// timeout in *status and the kernel exits.
+cudaError_t launch_bounded_wait_selftest(int* status, cudaStream_t s);
+
 // Size of the static scratch behind attn_decode_paged_noalloc (64 MiB).
 constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;
 

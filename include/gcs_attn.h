@@ -226,6 +226,14 @@ int attn_prefill_paged(const gcs_decode_args* a, void* out, void* workspace, siz
  * resets it to GCS_OK.  Returns GCS_OK or GCS_ERR_CUDA. */
 int gcs_get_device_status(int* status, int clear);
 
+/* Self-test of the bounded waits (a library diagnostic with no counterpart in the pages).
+ * Launches one small kernel on the stream that waits, through the same bounded wait every
+ * kernel uses, on a barrier phase that nothing completes.  After the 2 s wait limit it
+ * records GCS_ERR_DEVICE_TIMEOUT in the current device's status word and exits; the context
+ * stays usable.  Read (and clear) the word with gcs_get_device_status.
+ * Returns GCS_OK once the kernel is launched, or GCS_ERR_CUDA. */
+int gcs_selftest_bounded_wait(gcs_stream_t stream);
+
 /* ------------------------------------------------------------------ instrumentation
  * Arms two caller-created CUDA events (cudaEvent_t, passed as void*) for the next attn_fwd,
  * attn_bwd, attn_decode_paged or attn_prefill_paged call made by this host thread: `before`
