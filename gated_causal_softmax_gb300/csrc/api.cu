@@ -144,12 +144,17 @@ size_t fwd_ws(const gcs_prefill_args* a) {
 // wider heads take the output-column roles with an fp32 dQ accumulator.
 bool two_pass(const gcs_prefill_args* a) { return a->dqk <= 128 && a->dv <= 128; }
 
+// Head dims above 128 take the query-stationary dQ pass when asked for a deterministic result,
+// and where it is also the faster route (Dqk = 512, where the reduce-add role's 64-row steps
+// cost more than the dQ pass's recompute); otherwise the dK role reduce-adds dQ in fp32.
+bool wide_two_pass(const gcs_prefill_args* a) { return a->deterministic != 0 || a->dqk == 512; }
+
 size_t bwd_ws(const gcs_prefill_args* a) {
   Carver c{nullptr};
   const size_t ht = (size_t)a->hq * a->total_tokens;
   if (a->log_gate) c.take<float>(ht);                         // G^T
   c.take<float>(ht);                                           // delta
-  if (!two_pass(a) && !a->deterministic) c.take<float>((size_t)a->total_tokens * a->hq * a->dqk);  // dQ accumulator
+  if (!two_pass(a) && !wide_two_pass(a)) c.take<float>((size_t)a->total_tokens * a->hq * a->dqk);  // dQ accumulator
   if (a->log_gate || a->sink) c.take<float>(ht);               // row sums of dS
   if (a->log_gate) c.take<float>(ht);                          // column sums of dS
   c.take<float>((size_t)a->hq * ((a->total_tokens + 63) / 64 + a->num_seqs) * 128);  // packed vectors
@@ -259,7 +264,7 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
   float* gT = a->log_gate ? c.take<float>(ht) : nullptr;
   float* delta = c.take<float>(ht);
   const bool tp = two_pass(a);
-  const bool wide_det = !tp && a->deterministic;
+  const bool wide_det = !tp && wide_two_pass(a);
   // fp32 dQ accumulator: wide heads on the reduce-add route only
   float* dq_acc = (tp || wide_det) ? nullptr : c.take<float>((size_t)a->total_tokens * a->hq * a->dqk);
   float* dg_row = (a->log_gate || a->sink) ? c.take<float>(ht) : nullptr;

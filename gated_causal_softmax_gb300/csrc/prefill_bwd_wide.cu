@@ -13,7 +13,7 @@
 // of fitting the accumulators in TMEM.  Operands stream through a ring of 16 KB stages
 // (128 x 64 or 64 x 64 bf16 chunks, 128-B swizzle); the K columns a role keeps using
 // (its own 256 dims) stay resident.  One softmax warpgroup, one thread per key row.
-// Per 64-row query step (s = step, b = none; the pipeline is sequential per step):
+// Per query step of BM rows (s = step; the pipeline is sequential per step):
 //     S^T = K Q^T (TMEM)   [dP^T = V dO^T (TMEM)]   P^T / dS^T in fp32, bf16 operands
 //     role V:  dV  += P^T dO[:, v0..]
 //     role KQ: dK  += dS^T Q[:, k0..];  dQ^T[k0..] = K[:, k0..]^T dS^T -> fp32 reduce-adds
@@ -29,7 +29,6 @@ namespace gcs {
 namespace {
 
 constexpr int kBN = 128;
-constexpr int kBM = 64;
 constexpr int kThreads = 192;
 constexpr int kStage = 16384;
 constexpr int kW = 256;  // output columns per role
@@ -41,8 +40,12 @@ __device__ __forceinline__ void red_add_f32(float* addr, float v) {
   asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
 }
 
-template <int DQK, int DV, int KIND>
+// BM = query rows per step: 128 for the dV and dK-only roles (N = 128 MMAs), 64 for the
+// dK + dQ role, whose dQ^T halves need the TMEM columns that 128-row steps would take.
+template <int DQK, int DV, int KIND, int BM>
 struct WideCfg {
+  static_assert(BM == 64 || BM == 128, "query step");
+  static_assert(KIND != 1 || BM == 64, "the dQ role keeps 64-row steps");
   static constexpr int KCH = DQK / 64, VCH = DV / 64, WCH = kW / 64;
   static constexpr int NRES = (KIND >= 1 ? kW : (DQK < kW ? DQK : kW)) / 64;  // resident K chunks
   static constexpr int NST = 8;
@@ -50,20 +53,21 @@ struct WideCfg {
   static constexpr int OFF_RING = OFF_KRES + NRES * kStage;
   static constexpr int OFF_DS = OFF_RING + NST * kStage;
   static constexpr int OFF_VEC = OFF_DS + (KIND == 1 ? kStage : 0);  // [2][2][64] floats
-  static constexpr int OFF_BAR = OFF_VEC + 2 * 2 * kBM * 4;
+  static constexpr int OFF_BAR = OFF_VEC + 2 * 2 * BM * 4;
   static constexpr int OFF_MISC = OFF_BAR + (2 * NST + 16) * 8;
   static constexpr int SMEM = OFF_MISC + 16 + 1024;
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
-  // TMEM: S^T 0..63, dP^T 64..127, accumulator (dV or dK) 128..383, dQ^T halves 384..511
-  static constexpr int T_S = 0, T_DP = 64, T_ACC = 128, T_DQ = 384;
+  // TMEM: S^T 0..BM-1, dP^T BM..2BM-1, accumulator (dV or dK) 2BM..2BM+255, dQ^T halves 384..511
+  static constexpr int T_S = 0, T_DP = BM, T_ACC = 2 * BM, T_DQ = 384;
+  static_assert(T_ACC + 256 <= 512, "TMEM columns");
 };
 
-template <int DQK, int DV, int KIND>
+template <int DQK, int DV, int KIND, int BM>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                             const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                             const BwdParams p) {
-  using C = WideCfg<DQK, DV, KIND>;
+  using C = WideCfg<DQK, DV, KIND, BM>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -75,10 +79,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int res0 = (KIND >= 1) ? w0 / 64 : 0;  // first resident K chunk
   const int group = p.hq / p.hkv;
   const int j0 = jt * kBN;
-  const int it_lo = j0 / kBM;
+  const int it_lo = j0 / BM;
   int i_hi = len - 1;
   if (p.window > 0) i_hi = min(i_hi, j0 + kBN - 1 + p.window - 1);
-  const int n_it = i_hi / kBM - it_lo + 1;
+  const int n_it = i_hi / BM - it_lo + 1;
   const int nsteps = n_it * group;
   const bool sums = (KIND >= 1) && (w0 == 0);  // this role takes the dS column (and row) sums
 
@@ -146,30 +150,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < nsteps && ok; ++s) {
       const int h = kvh * group + s / n_it;
-      const int i0 = (it_lo + s % n_it) * kBM;
+      const int i0 = (it_lo + s % n_it) * BM;
       const int yq = seq_start + i0, yk = seq_start + j0;
       if (lane == 0) {
         for (int c = 0; c < C::KCH && ok; ++c) {
           if (c < res0 || c >= res0 + C::NRES) ok = issue(&tmK, kvh * DQK + c * 64, yk, kStage);
-          if (ok) ok = issue(&tmQ, h * DQK + c * 64, yq, kStage / 2);
+          if (ok) ok = issue(&tmQ, h * DQK + c * 64, yq, BM * 128);
         }
         if (KIND >= 1) {
           for (int c = 0; c < C::VCH && ok; ++c) {
             ok = issue(&tmV, kvh * DV + c * 64, yk, kStage);
-            if (ok) ok = issue(&tmDO, h * DV + c * 64, yq, kStage / 2);
+            if (ok) ok = issue(&tmDO, h * DV + c * 64, yq, BM * 128);
           }
-          for (int c = 0; c < C::WCH && ok; ++c) ok = issue(&tmQ, h * DQK + w0 + c * 64, yq, kStage / 2);
+          for (int c = 0; c < C::WCH && ok; ++c) ok = issue(&tmQ, h * DQK + w0 + c * 64, yq, BM * 128);
         } else {
-          for (int c = 0; c < C::WCH && ok; ++c) ok = issue(&tmDO, h * DV + w0 + c * 64, yq, kStage / 2);
+          for (int c = 0; c < C::WCH && ok; ++c) ok = issue(&tmDO, h * DV + w0 + c * 64, yq, BM * 128);
         }
         if (ok) ok = wait_bar(&vec_empty[s & 1], ((s >> 1) & 1) ^ 1, ab);
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
-      float* vec = reinterpret_cast<float*>(smem + C::OFF_VEC) + (s & 1) * 2 * kBM;
+      float* vec = reinterpret_cast<float*>(smem + C::OFF_VEC) + (s & 1) * 2 * BM;
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int c = lane * 2 + u;
+      for (int u = 0; u < BM / 32; ++u) {
+        const int c = lane * (BM / 32) + u;
         const int i = i0 + c;
         float colterm = 0.f, dl = 0.f;
         if (i < len) {
@@ -179,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           dl = __ldg(p.delta + idx);
         }
         vec[c] = colterm;
-        vec[kBM + c] = dl;
+        vec[BM + c] = dl;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&vec_full[s & 1]);
@@ -187,9 +191,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idS = idesc_bf16(128, kBM, false, false);  // S^T, dP^T
+      const uint32_t idS = idesc_bf16(128, BM, false, false);  // S^T, dP^T
       const uint32_t idAcc = idesc_bf16(128, 64, false, true);  // dV / dK, one 64-column chunk
-      const uint32_t idDQ = idesc_bf16(128, kBM, true, true);   // dQ^T half
+      const uint32_t idDQ = idesc_bf16(128, BM, true, true);    // dQ^T half
       const uint32_t sRes = smem_u32(smem + C::OFF_KRES), sRing = smem_u32(smem + C::OFF_RING);
       const uint32_t sDS = smem_u32(smem + C::OFF_DS);
       uint32_t stage = 0, phase = 0;
@@ -263,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = take(bq);
           if (!ok) break;
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
+          for (int k = 0; k < BM / 16; ++k)
             mma_ts(tmem + C::T_ACC + c * 64, aT + k * 8, sdesc_sw128(bq + k * 2048, kStage, 1024), idAcc,
                    (s > 0 || k > 0) ? 1u : 0u);
           give();
@@ -306,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int s = 0; s < nsteps; ++s) {
       const int h = kvh * group + s / n_it;
-      const int i0 = (it_lo + s % n_it) * kBM;
+      const int i0 = (it_lo + s % n_it) * BM;
       if (h != cur_h) {
         if (sums && cur_h >= 0 && has_gate && jl < len)
           red_add_f32(p.dg_col + (size_t)cur_h * p.total + seq_start + jl, dgcol);
@@ -319,11 +323,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = wait_bar(s_full, s & 1, ab);
       if (!ok) break;
       tc_fence_after();
-      const float* vec = reinterpret_cast<const float*>(smem + C::OFF_VEC) + (s & 1) * 2 * kBM;
-      const bool need_mask = (i0 < j0 + kBN - 1) || (p.window > 0 && i0 + kBM - 1 - j0 >= p.window) ||
-                             (i0 + kBM > len);
+      const float* vec = reinterpret_cast<const float*>(smem + C::OFF_VEC) + (s & 1) * 2 * BM;
+      const bool need_mask = (i0 < j0 + kBN - 1) || (p.window > 0 && i0 + BM - 1 - j0 >= p.window) ||
+                             (i0 + BM > len);
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
+      for (int ch = 0; ch < BM / 32; ++ch) {
         uint32_t sv[32], dp[32];
         tmem_ld32(tS + 32 * ch, sv);
         if (KIND >= 1) tmem_ld32(tDP + 32 * ch, dp);
@@ -339,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const float pr = ex2(t);
           sv[c] = __float_as_uint(pr);
-          if (KIND >= 1) dp[c] = __float_as_uint(pr * (__uint_as_float(dp[c]) - vec[kBM + col]));
+          if (KIND >= 1) dp[c] = __float_as_uint(pr * (__uint_as_float(dp[c]) - vec[BM + col]));
         }
         uint32_t pk[16];
         if (KIND == 0) {
@@ -407,11 +411,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(dq_free);
           }
-          const int nrows = min(kBM, len - i0);
+          const int nrows = min(BM, len - i0);
           float* base = p.dq_acc + ((size_t)(seq_start + i0) * p.hq + h) * DQK + w0 + hf * 128 + r;
           const size_t row_stride = (size_t)p.hq * DQK;
 #pragma unroll
-          for (int c = 0; c < kBM; ++c)
+          for (int c = 0; c < BM; ++c)
             if (c < nrows) red_add_f32(base + c * row_stride, __uint_as_float(dq[c]) * p.scale);
         }
       }
@@ -459,12 +463,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int DQK, int DV, int KIND>
 cudaError_t launch_t(const BwdParams& p, const BwdMaps& maps, int num_tiles, cudaStream_t s) {
-  using C = WideCfg<DQK, DV, KIND>;
-  auto kern = prefill_bwd_wide_kernel<DQK, DV, KIND>;
+  constexpr int BM = KIND == 1 ? 64 : 128;
+  using C = WideCfg<DQK, DV, KIND, BM>;
+  auto kern = prefill_bwd_wide_kernel<DQK, DV, KIND, BM>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   const int roles = (KIND >= 1 ? DQK : DV) / kW;
-  kern<<<dim3(p.hkv, num_tiles, roles), kThreads, C::SMEM, s>>>(maps.q, maps.k, maps.v, maps.dout, p);
+  // query and dO boxes of BM rows
+  const CUtensorMap& mq = BM == 128 ? maps.q128 : maps.q;
+  const CUtensorMap& mdo = BM == 128 ? maps.dout128 : maps.dout;
+  kern<<<dim3(p.hkv, num_tiles, roles), kThreads, C::SMEM, s>>>(mq, maps.k, maps.v, mdo, p);
   return cudaGetLastError();
 }
 

@@ -86,10 +86,11 @@ typedef struct {
   const void* v;              /* bf16 [total_tokens, hkv, dv]                            */
   const float* log_gate;      /* fp32 [total_tokens, hq] per-token log forget gates, or NULL */
   const float* sink;          /* fp32 [hq] sink logits, or NULL                          */
-  int deterministic;          /* attn_bwd with dqk or dv > 128: 0 = dQ and the dS row sums by
-                                 fp32 reduce-adds (fastest); 1 = a separate query-stationary
+  int deterministic;          /* attn_bwd with dqk or dv > 128: 1 = a separate query-stationary
                                  dQ pass, every gradient written once or summed in a fixed
-                                 order.  Head dims <= 128 are deterministic either way.   */
+                                 order; 0 = the faster route for the shape: that same pass
+                                 for dqk = 512, fp32 reduce-adds of dQ and the dS row sums
+                                 otherwise.  Head dims <= 128 are deterministic either way. */
 } gcs_prefill_args;
 
 /* Workspace bytes attn_fwd needs (0 when there is no gate). */
@@ -111,9 +112,9 @@ size_t attn_bwd_workspace(const gcs_prefill_args* a);
  * The sink gradient is -sum_i p_sink,i * sum_j P_ij (dO_i . v_j), accumulated in fp32.
  * Head dims <= 128: dQ is accumulated per query tile in a separate pass and every gradient is
  * written once or summed in a fixed order, so repeated calls give the same bits.  Wider heads
- * do the same with a->deterministic = 1; with 0 (the faster route) dQ and d log_gate are
- * accumulated by fp32 reduce-adds into a zero-initialised buffer, and their low bits may vary
- * from run to run. */
+ * do the same with a->deterministic = 1, and with 0 when dqk = 512; otherwise (dqk = 256 with
+ * deterministic = 0) dQ and d log_gate are accumulated by fp32 reduce-adds into a
+ * zero-initialised buffer, and their low bits may vary from run to run. */
 int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const void* dout, void* dq, void* dk,
              void* dv, float* dlog_gate, float* dsink, void* workspace, size_t workspace_bytes,
              gcs_stream_t stream);

@@ -95,6 +95,8 @@ def test_workspace_sizes_on_host(L):
     assert ws_wide == 4 * (4 * 256) * 4 + 256 * 4 * 256 * 4 + 4 * n_qtiles * 128 * 4
     ws_det = L.attn_bwd_workspace(b(prefill(log_gate=FAKE, sink=FAKE, dqk=256, dv=512, deterministic=1)))
     assert ws_det == ws
+    # (512, 512) takes the dQ pass either way: it is the faster route there
+    assert L.attn_bwd_workspace(b(prefill(log_gate=FAKE, sink=FAKE, dqk=512, dv=512))) == ws
     assert L.attn_bwd_workspace(b(prefill(log_gate=FAKE, sink=FAKE, deterministic=1))) == ws
     units, rows = 2 * 2 * 4, 16
     assert L.attn_decode_workspace(b(decode())) == units * rows * 128 * 4 + units * rows * 2 * 4
