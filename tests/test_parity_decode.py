@@ -19,6 +19,8 @@ CASES = {
     "short_query_context_65537": ([65537, 300], [4, 2], 16, 1, "B", 2048),
     "tiny_segments_empty_partials": ([40, 70, 5], [4, 3, 4], 16, 1, "A", 16),
     "mixed_q_lens_reading_A": ([1000, 1001, 1003, 64], [1, 2, 4, 3], 32, 2, "A", 256),
+    # a request with no query rows in the middle of the batch is skipped
+    "empty_request_in_batch": ([700, 50, 2100], [2, 0, 3], 16, 1, "A", 2048),
 }
 
 

@@ -42,6 +42,8 @@ CASES = {
     "window_inside_tile": ([400, 260], [150, 260], 16, 1, True, 9, "per_token"),
     "per_tensor": ([1200, 333, 64], [100, 333, 7], 32, 2, False, 0, "per_tensor"),
     "per_tensor_features": ([900, 2100], [77, 300], 16, 1, True, 500, "per_tensor"),
+    # a request with no query rows in the middle of the batch is skipped
+    "empty_request_in_batch": ([300, 64, 1000], [40, 0, 17], 16, 1, False, 0, "per_token"),
 }
 
 
