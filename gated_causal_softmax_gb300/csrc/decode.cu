@@ -370,12 +370,15 @@ __global__ void __launch_bounds__(kThreads, 3)
       }
       l0 = l0 * a0 + (pr[0][0] + pr[0][1]) + (pr[0][2] + pr[0][3]);
       l1 = l1 * a1 + (pr[1][0] + pr[1][1]) + (pr[1][2] + pr[1][3]);
+      // the accumulators change only where a row's max moved (the factor is 1 elsewhere)
+      if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        o[u][0] *= a0;
-        o[u][1] *= a0;
-        o[u][2] *= a1;
-        o[u][3] *= a1;
+        for (int u = 0; u < 16; ++u) {
+          o[u][0] *= a0;
+          o[u][1] *= a0;
+          o[u][2] *= a1;
+          o[u][3] *= a1;
+        }
       }
       // V scales multiply the probabilities after the row sum; slots >= L get scale 0, and
       // their value bytes are never multiplied (NaN allowed there)
