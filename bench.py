@@ -47,7 +47,7 @@ LAUNCHES_PER_DECODE = 2
 NCU_TRAFFIC = {
     "bwd": 217.9e6 + 277.0e6,  # prefill_bwd_dq_kernel<128> + prefill_bwd_kernel<128>
     "fwd": 119.8e6,            # prefill_fwd2_kernel<128>
-    "decode_split": None,  # decode_split_kernel<0, 0, 0> (changed since its last capture)
+    "decode_split": 1155.5e6 + 19.1e6,  # decode_split_kernel<0, 0, 0>
     "prefill_paged": 153.8e6 + 35.3e6,  # prefill_paged_kernel<0>
 }
 
