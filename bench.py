@@ -356,11 +356,16 @@ def run_native(args):
             e.record()
     barrier(world)
     torch.cuda.synchronize()
+    # whole calls with nothing recorded between their kernels (an event between the split
+    # kernel and the combine would stop the combine's programmatic launch), then the same calls
+    # with events around the split kernel for its own duration
     d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     d0.record()
     for i in range(DK):
-        dstep(devs[i])
+        dstep()
     d1.record()
+    for i in range(DK):
+        dstep(devs[i])
     torch.cuda.synchronize()
     barrier(world)
     dec_ms = max_over_ranks(world, d0.elapsed_time(d1)) / DK
