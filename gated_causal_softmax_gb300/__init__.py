@@ -28,6 +28,10 @@ __all__ = [
     "attn_decode_paged_noalloc",
     "attn_prefill_paged",
     "selftest_bounded_wait",
+    "set_device_checks",
+    "device_checks",
+    "check_prefill_inputs",
+    "check_paged_inputs",
     "PrefillArgs",
     "DecodeArgs",
     "GcsError",
@@ -142,6 +146,14 @@ def _declare(lib: ctypes.CDLL) -> None:
     lib.gcs_selftest_bounded_wait.restype = _c_int
     lib.gcs_set_kernel_events.argtypes = [_vp, _vp]
     lib.gcs_set_kernel_events.restype = _c_int
+    lib.gcs_set_device_checks.argtypes = [_c_int]
+    lib.gcs_set_device_checks.restype = _c_int
+    lib.gcs_get_device_checks.argtypes = []
+    lib.gcs_get_device_checks.restype = _c_int
+    lib.gcs_check_prefill_inputs.argtypes = [P(PrefillArgs), _vp]
+    lib.gcs_check_prefill_inputs.restype = _c_int
+    lib.gcs_check_paged_inputs.argtypes = [P(DecodeArgs), _vp]
+    lib.gcs_check_paged_inputs.restype = _c_int
 
 
 def load(build_if_needed: bool = True) -> ctypes.CDLL:
@@ -201,7 +213,8 @@ def set_kernel_events(before: Optional[torch.cuda.Event], after: Optional[torch.
 
 
 def get_device_status(clear: bool = True) -> int:
-    """Per-device status word written by kernels that gave up on a bounded wait."""
+    """Per-device status word: GCS_ERR_DEVICE_TIMEOUT (5) from a kernel that gave up on a bounded
+    wait, GCS_ERR_INVALID_ARG (1) from a failed device-content check, else 0."""
     st = _c_int(0)
     _check(load().gcs_get_device_status(ctypes.byref(st), 1 if clear else 0), "gcs_get_device_status")
     return st.value
@@ -213,6 +226,34 @@ def selftest_bounded_wait() -> int:
     _check(load().gcs_selftest_bounded_wait(_stream()), "gcs_selftest_bounded_wait")
     torch.cuda.synchronize()
     return get_device_status(clear=True)
+
+
+def set_device_checks(enable: bool) -> None:
+    """Checked mode for every later call of this process: each call first checks its index
+    arrays on the device; a failed check records GCS_ERR_INVALID_ARG (1) in the device status
+    word and the call's kernels see an empty batch."""
+    _check(load().gcs_set_device_checks(1 if enable else 0), "gcs_set_device_checks")
+
+
+def device_checks() -> bool:
+    return bool(load().gcs_get_device_checks())
+
+
+def check_prefill_inputs(q, k, v, cu_seqlens, max_seqlen=None, scale=None, window=0, log_gate=None,
+                         sink=None) -> None:
+    """Launches the device-content checks of a prefill call's cu_seqlens on the current stream
+    (nothing else); read the result with get_device_status()."""
+    a = prefill_args(q, k, v, cu_seqlens, max_seqlen, scale, window, log_gate, sink)
+    _check(load().gcs_check_prefill_inputs(ctypes.byref(a), _stream()), "gcs_check_prefill_inputs")
+
+
+def check_paged_inputs(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu_q, max_q_len, max_seq_len,
+                       scale=None, segment_len=0, g_cache=None, sink=None, window=0) -> None:
+    """Launches the device-content checks of a paged call's cu_q, seq_lens and page table on
+    the current stream (nothing else); read the result with get_device_status()."""
+    a = decode_args(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu_q, max_q_len, max_seq_len,
+                    scale, segment_len, g_cache, sink, window)
+    _check(load().gcs_check_paged_inputs(ctypes.byref(a), _stream()), "gcs_check_paged_inputs")
 
 
 def prefill_args(q, k, v, cu_seqlens, max_seqlen, scale, window, log_gate, sink) -> PrefillArgs:

@@ -3,6 +3,7 @@
 // which is a synchronous query by design).
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -22,6 +23,10 @@ int* g_status_ptr[kMaxDevices] = {nullptr};
 std::mutex g_mu;
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// gcs_set_device_checks: every call first checks its index arrays on the device
+std::atomic<int> g_device_checks{0};
+bool device_checks_on() { return g_device_checks.load(std::memory_order_relaxed) != 0; }
 
 // events armed by gcs_set_kernel_events for the next call of this thread
 thread_local cudaEvent_t t_ev_before = nullptr, t_ev_after = nullptr;
@@ -134,9 +139,11 @@ int* status_ptr_for_current_device() {
   return g_status_ptr[dev];
 }
 
-size_t fwd_ws(const gcs_prefill_args* a) {
+// With device checks on, every workspace ends with the checked copy of cu_seqlens / cu_q.
+size_t fwd_ws(const gcs_prefill_args* a, bool chk) {
   Carver c{nullptr};
   if (a->log_gate) c.take<float>((size_t)a->hq * a->total_tokens);
+  if (chk) c.take<int32_t>((size_t)a->num_seqs + 1);
   return c.off;
 }
 
@@ -149,7 +156,7 @@ bool two_pass(const gcs_prefill_args* a) { return a->dqk <= 128 && a->dv <= 128;
 // cost more than the dQ pass's recompute); otherwise the dK role reduce-adds dQ in fp32.
 bool wide_two_pass(const gcs_prefill_args* a) { return a->deterministic != 0 || a->dqk == 512; }
 
-size_t bwd_ws(const gcs_prefill_args* a) {
+size_t bwd_ws(const gcs_prefill_args* a, bool chk) {
   Carver c{nullptr};
   const size_t ht = (size_t)a->hq * a->total_tokens;
   if (a->log_gate) c.take<float>(ht);                         // G^T
@@ -158,6 +165,7 @@ size_t bwd_ws(const gcs_prefill_args* a) {
   if (a->log_gate || a->sink) c.take<float>(ht);               // row sums of dS
   if (a->log_gate) c.take<float>(ht);                          // column sums of dS
   c.take<float>((size_t)a->hq * ((a->total_tokens + 63) / 64 + a->num_seqs) * 128);  // packed vectors
+  if (chk) c.take<int32_t>((size_t)a->num_seqs + 1);
   return c.off;
 }
 
@@ -185,16 +193,21 @@ const char* gcs_status_str(int s) {
 
 const char* gcs_version(void) { return "gcs_attn 0.1 (sm_103a)"; }
 
-size_t attn_fwd_workspace(const gcs_prefill_args* a) { return (a && check_prefill(a) == GCS_OK) ? fwd_ws(a) : 0; }
+size_t attn_fwd_workspace(const gcs_prefill_args* a) {
+  return (a && check_prefill(a) == GCS_OK) ? fwd_ws(a, device_checks_on()) : 0;
+}
 
-size_t attn_bwd_workspace(const gcs_prefill_args* a) { return (a && check_prefill(a) == GCS_OK) ? bwd_ws(a) : 0; }
+size_t attn_bwd_workspace(const gcs_prefill_args* a) {
+  return (a && check_prefill(a) == GCS_OK) ? bwd_ws(a, device_checks_on()) : 0;
+}
 
 int attn_fwd(const gcs_prefill_args* a, void* o, float* lse, void* workspace, size_t workspace_bytes,
              gcs_stream_t stream) {
   int st = check_prefill(a);
   if (st != GCS_OK) return st;
   if (!o || !lse || !aligned16(o) || !aligned16(lse)) return GCS_ERR_INVALID_ARG;
-  const size_t need = fwd_ws(a);
+  const bool chk = device_checks_on();
+  const size_t need = fwd_ws(a, chk);
   if (need > 0 && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
     return GCS_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -203,6 +216,7 @@ int attn_fwd(const gcs_prefill_args* a, void* o, float* lse, void* workspace, si
 
   Carver c{static_cast<uint8_t*>(workspace)};
   float* gT = a->log_gate ? c.take<float>((size_t)a->hq * a->total_tokens) : nullptr;
+  int32_t* cu_chk = chk ? c.take<int32_t>((size_t)a->num_seqs + 1) : nullptr;
 
   FwdMaps maps;
   if (!make_map(&maps.q, a->q, (uint64_t)a->hq * a->dqk, a->total_tokens, 128) ||
@@ -210,12 +224,19 @@ int attn_fwd(const gcs_prefill_args* a, void* o, float* lse, void* workspace, si
       !make_map(&maps.v, a->v, (uint64_t)a->hkv * a->dv, a->total_tokens, 128))
     return GCS_ERR_CUDA;
 
+  // the kernels read the checked copy of cu_seqlens when device checks are on
+  const int32_t* cu = a->cu_seqlens;
+  if (cu_chk) {
+    st = cuda_status(launch_check_prefill(a->cu_seqlens, a->num_seqs, a->total_tokens, a->max_seqlen, cu_chk, status, s));
+    if (st != GCS_OK) return st;
+    cu = cu_chk;
+  }
   if (gT) {
-    st = cuda_status(launch_gate_cumsum(a->log_gate, a->cu_seqlens, a->num_seqs, a->total_tokens, a->hq, gT, s));
+    st = cuda_status(launch_gate_cumsum(a->log_gate, cu, a->num_seqs, a->total_tokens, a->hq, gT, s));
     if (st != GCS_OK) return st;
   }
   FwdParams p;
-  p.cu_seqlens = a->cu_seqlens;
+  p.cu_seqlens = cu;
   p.num_seqs = a->num_seqs;
   p.total = a->total_tokens;
   p.hq = a->hq;
@@ -252,7 +273,8 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
     return GCS_ERR_INVALID_ARG;
   if ((dlog_gate == nullptr) != (a->log_gate == nullptr)) return GCS_ERR_INVALID_ARG;
   if ((dsink == nullptr) != (a->sink == nullptr)) return GCS_ERR_INVALID_ARG;
-  const size_t need = bwd_ws(a);
+  const bool chk = device_checks_on();
+  const size_t need = bwd_ws(a, chk);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return GCS_ERR_WORKSPACE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -271,6 +293,7 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
   float* dg_col = a->log_gate ? c.take<float>(ht) : nullptr;
   const int n_qtiles = (a->total_tokens + 63) / 64 + a->num_seqs;
   float* vecp = c.take<float>((size_t)a->hq * n_qtiles * 128);
+  int32_t* cu_chk = chk ? c.take<int32_t>((size_t)a->num_seqs + 1) : nullptr;
 
   BwdMaps maps;
   if (!make_map(&maps.q, a->q, (uint64_t)a->hq * a->dqk, a->total_tokens, 64) ||
@@ -281,20 +304,26 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
       !make_map(&maps.dout128, dout, (uint64_t)a->hq * a->dv, a->total_tokens, 128))
     return GCS_ERR_CUDA;
 
+  const int32_t* cu = a->cu_seqlens;
+  if (cu_chk) {
+    st = cuda_status(launch_check_prefill(a->cu_seqlens, a->num_seqs, a->total_tokens, a->max_seqlen, cu_chk, status, s));
+    if (st != GCS_OK) return st;
+    cu = cu_chk;
+  }
   if (gT) {
-    st = cuda_status(launch_gate_cumsum(a->log_gate, a->cu_seqlens, a->num_seqs, a->total_tokens, a->hq, gT, s));
+    st = cuda_status(launch_gate_cumsum(a->log_gate, cu, a->num_seqs, a->total_tokens, a->hq, gT, s));
     if (st != GCS_OK) return st;
   }
   st = cuda_status(launch_bwd_pre(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout),
                                   a->total_tokens, a->hq, a->dv, a->dqk, delta, dq_acc, dg_row, dg_col, s));
   if (st != GCS_OK) return st;
 
-  st = cuda_status(launch_bwd_pack(a->cu_seqlens, a->num_seqs, a->total_tokens, a->hq, n_qtiles, lse, gT, delta,
+  st = cuda_status(launch_bwd_pack(cu, a->num_seqs, a->total_tokens, a->hq, n_qtiles, lse, gT, delta,
                                    vecp, s));
   if (st != GCS_OK) return st;
 
   BwdParams p;
-  p.cu_seqlens = a->cu_seqlens;
+  p.cu_seqlens = cu;
   p.num_seqs = a->num_seqs;
   p.total = a->total_tokens;
   p.hq = a->hq;
@@ -342,7 +371,7 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
   }
   if (st != GCS_OK) return st;
   return cuda_status(launch_bwd_post(dq_acc, static_cast<uint16_t*>(dq), a->total_tokens, a->hq, a->dqk,
-                                     a->cu_seqlens, a->num_seqs, dg_row, dg_col, dlog_gate, lse, delta, a->sink,
+                                     cu, a->num_seqs, dg_row, dg_col, dlog_gate, lse, delta, a->sink,
                                      dsink, s));
 }
 
@@ -415,16 +444,37 @@ static void fill_paged_params(const gcs_decode_args* a, void* out, int* status, 
   p.status = status;
 }
 
-static size_t decode_ws(const gcs_decode_args* a, int* max_segs_out) {
-  const int max_segs = (a->max_seq_len + a->segment_len - 1) / a->segment_len;
-  if (max_segs_out) *max_segs_out = max_segs;
+// Bytes of the split-K partials (acc, then (m, l)) of num_reqs x max_segs x hkv units.
+static size_t partials_ws(const gcs_decode_args* a, int max_segs) {
   const size_t units = (size_t)a->num_reqs * max_segs * a->hkv;
   const size_t rows = (size_t)a->max_q_len * 16;
   return round_up(units * rows * 128 * sizeof(float)) + round_up(units * rows * 2 * sizeof(float));
 }
 
+// Bytes of the checked copy of cu_q that ends the workspace when device checks are on.
+static size_t cu_q_copy_ws(const gcs_decode_args* a, bool chk) {
+  return chk ? round_up(((size_t)a->num_reqs + 1) * sizeof(int32_t)) : 0;
+}
+
+static size_t decode_ws(const gcs_decode_args* a, bool chk, int* max_segs_out) {
+  const int max_segs = (a->max_seq_len + a->segment_len - 1) / a->segment_len;
+  if (max_segs_out) *max_segs_out = max_segs;
+  return partials_ws(a, max_segs) + cu_q_copy_ws(a, chk);
+}
+
+// Runs the device-content checks of a paged call when they are on: p.cu_q then points to the
+// checked copy at byte offset `off` of the workspace.
+static int paged_checks(const gcs_decode_args* a, void* workspace, size_t off, DecodeParams& p, cudaStream_t s) {
+  int32_t* cu_chk = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + off);
+  const int st = cuda_status(launch_check_paged(a->cu_q, a->seq_lens, a->block_table, a->num_reqs, a->total_q,
+                                                a->max_q_len, a->max_seq_len, a->max_blocks_per_req, a->num_blocks,
+                                                a->block_size, a->window, cu_chk, p.status, s));
+  if (st == GCS_OK) p.cu_q = cu_chk;
+  return st;
+}
+
 size_t attn_decode_workspace(const gcs_decode_args* a) {
-  return (a && check_decode(a) == GCS_OK) ? decode_ws(a, nullptr) : 0;
+  return (a && check_decode(a) == GCS_OK) ? decode_ws(a, device_checks_on(), nullptr) : 0;
 }
 
 int attn_decode_paged(const gcs_decode_args* a, void* out, void* workspace, size_t workspace_bytes,
@@ -433,7 +483,8 @@ int attn_decode_paged(const gcs_decode_args* a, void* out, void* workspace, size
   if (st != GCS_OK) return st;
   if (!out || !aligned16(out)) return GCS_ERR_INVALID_ARG;
   int max_segs = 0;
-  const size_t need = decode_ws(a, &max_segs);
+  const bool chk = device_checks_on();
+  const size_t need = decode_ws(a, chk, &max_segs);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
     return GCS_ERR_WORKSPACE;
   int* status = device_status_ptr();
@@ -453,15 +504,20 @@ int attn_decode_paged(const gcs_decode_args* a, void* out, void* workspace, size
     if (!make_page_map_u8(&maps.k, a->k_cache, cache_rows) || !make_page_map_u8(&maps.v, a->v_cache, cache_rows))
       return GCS_ERR_CUDA;
   }
-  KernelTimer timer(reinterpret_cast<cudaStream_t>(stream));
-  return cuda_status(launch_decode(p, maps, reinterpret_cast<cudaStream_t>(stream), &timer.b, &timer.a));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (chk) {
+    const int st2 = paged_checks(a, workspace, partials_ws(a, max_segs), p, s);
+    if (st2 != GCS_OK) return st2;
+  }
+  KernelTimer timer(s);
+  return cuda_status(launch_decode(p, maps, s, &timer.b, &timer.a));
 }
 
 int attn_decode_paged_noalloc(const gcs_decode_args* a, void* out, gcs_stream_t stream) {
   int st = check_decode(a);
   if (st != GCS_OK) return st;
   // the split-K partials must fit the library's fixed scratch
-  if (decode_ws(a, nullptr) > kNoAllocScratchBytes) return GCS_ERR_WORKSPACE;
+  if (decode_ws(a, device_checks_on(), nullptr) > kNoAllocScratchBytes) return GCS_ERR_WORKSPACE;
   void* scratch = nullptr;
   if (decode_noalloc_scratch(&scratch) != cudaSuccess) return GCS_ERR_CUDA;
   return attn_decode_paged(a, out, scratch, kNoAllocScratchBytes, stream);
@@ -484,13 +540,14 @@ static int check_prefill_paged(const gcs_decode_args* a) {
 }
 
 struct PagedPlan {
-  int seg_pages = 0, max_segs = 1;
-  size_t ws = 0;  // 0: one segment per request, the kernel writes out directly
+  int seg_pages = 0, max_segs = 1;  // max_segs 1: one segment per request, the kernel writes out directly
+  size_t part_ws = 0;               // split-K partials (none with one segment)
+  size_t ws = 0;                    // + the checked copy of cu_q with device checks on
 };
 
 // Segments of the paged prefill: the caller's, or (segment_len 0) the fewest that give
 // about two CTAs per SM with the query blocks of 16 positions x kv heads x requests.
-static bool plan_prefill_paged(const gcs_decode_args* a, PagedPlan* pl) {
+static bool plan_prefill_paged(const gcs_decode_args* a, bool chk, PagedPlan* pl) {
   const int max_pages = (a->max_seq_len + 15) / 16;
   int sp;
   if (a->segment_len > 0) {
@@ -508,18 +565,14 @@ static bool plan_prefill_paged(const gcs_decode_args* a, PagedPlan* pl) {
   }
   pl->seg_pages = sp;
   pl->max_segs = (max_pages + sp - 1) / sp;
-  pl->ws = 0;
-  if (pl->max_segs > 1) {
-    const size_t units = (size_t)a->num_reqs * pl->max_segs * a->hkv;
-    const size_t rows = (size_t)a->max_q_len * 16;
-    pl->ws = round_up(units * rows * 128 * sizeof(float)) + round_up(units * rows * 2 * sizeof(float));
-  }
+  pl->part_ws = pl->max_segs > 1 ? partials_ws(a, pl->max_segs) : 0;
+  pl->ws = pl->part_ws + cu_q_copy_ws(a, chk);
   return true;
 }
 
 size_t attn_prefill_paged_workspace(const gcs_decode_args* a) {
   PagedPlan pl;
-  if (!a || check_prefill_paged(a) != GCS_OK || !plan_prefill_paged(a, &pl)) return 0;
+  if (!a || check_prefill_paged(a) != GCS_OK || !plan_prefill_paged(a, device_checks_on(), &pl)) return 0;
   return pl.ws;
 }
 
@@ -529,7 +582,8 @@ int attn_prefill_paged(const gcs_decode_args* a, void* out, void* workspace, siz
   if (st != GCS_OK) return st;
   if (!out || !aligned16(out)) return GCS_ERR_INVALID_ARG;
   PagedPlan pl;
-  if (!plan_prefill_paged(a, &pl)) return GCS_ERR_CUDA;
+  const bool chk = device_checks_on();
+  if (!plan_prefill_paged(a, chk, &pl)) return GCS_ERR_CUDA;
   if (pl.ws > 0 && (!workspace || workspace_bytes < pl.ws || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
     return GCS_ERR_WORKSPACE;
   int* status = device_status_ptr();
@@ -538,7 +592,7 @@ int attn_prefill_paged(const gcs_decode_args* a, void* out, void* workspace, siz
   fill_paged_params(a, out, status, p);
   p.max_segs = pl.max_segs;
   p.seg_pages = pl.seg_pages;
-  if (pl.ws > 0) {
+  if (pl.max_segs > 1) {
     const size_t units = (size_t)a->num_reqs * pl.max_segs * a->hkv;
     const size_t rows = (size_t)a->max_q_len * 16;
     p.part_acc = static_cast<float*>(workspace);
@@ -549,8 +603,43 @@ int attn_prefill_paged(const gcs_decode_args* a, void* out, void* workspace, siz
   const uint64_t cache_rows = (uint64_t)a->num_blocks * a->hkv * a->block_size;
   if (!make_page_map_u8(&maps.k, a->k_cache, cache_rows) || !make_page_map_u8(&maps.v, a->v_cache, cache_rows))
     return GCS_ERR_CUDA;
-  KernelTimer timer(reinterpret_cast<cudaStream_t>(stream));
-  return cuda_status(launch_prefill_paged(p, maps, reinterpret_cast<cudaStream_t>(stream), &timer.b, &timer.a));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (chk) {
+    const int st2 = paged_checks(a, workspace, pl.part_ws, p, s);
+    if (st2 != GCS_OK) return st2;
+  }
+  KernelTimer timer(s);
+  return cuda_status(launch_prefill_paged(p, maps, s, &timer.b, &timer.a));
+}
+
+int gcs_set_device_checks(int enable) {
+  if (enable != 0 && enable != 1) return GCS_ERR_INVALID_ARG;
+  g_device_checks.store(enable, std::memory_order_relaxed);
+  return GCS_OK;
+}
+
+int gcs_get_device_checks(void) { return device_checks_on() ? 1 : 0; }
+
+int gcs_check_prefill_inputs(const gcs_prefill_args* a, gcs_stream_t stream) {
+  const int st = check_prefill(a);
+  if (st != GCS_OK) return st;
+  int* status = device_status_ptr();
+  if (!status) return GCS_ERR_CUDA;
+  return cuda_status(launch_check_prefill(a->cu_seqlens, a->num_seqs, a->total_tokens, a->max_seqlen, nullptr, status,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int gcs_check_paged_inputs(const gcs_decode_args* a, gcs_stream_t stream) {
+  // the arguments of either paged call
+  if (check_decode(a) != GCS_OK) {
+    const int st = check_prefill_paged(a);
+    if (st != GCS_OK) return st;
+  }
+  int* status = device_status_ptr();
+  if (!status) return GCS_ERR_CUDA;
+  return cuda_status(launch_check_paged(a->cu_q, a->seq_lens, a->block_table, a->num_reqs, a->total_q, a->max_q_len,
+                                        a->max_seq_len, a->max_blocks_per_req, a->num_blocks, a->block_size,
+                                        a->window, nullptr, status, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int gcs_set_kernel_events(void* before, void* after) {

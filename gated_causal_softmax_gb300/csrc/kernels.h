@@ -131,6 +131,15 @@ cudaError_t launch_prefill_paged(const DecodeParams& p, const DecodeMaps& maps, 
 // timeout in *status and the kernel exits.
 cudaError_t launch_bounded_wait_selftest(int* status, cudaStream_t s);
 
+// Device-content checks (one CTA, before the call's kernels): record kDevInvalidArg in *status
+// when a precondition on the index arrays fails, and write to cu_out (if not null) a copy of
+// cu_seqlens / cu_q, or all zeros (an empty batch) on a failure.
+cudaError_t launch_check_prefill(const int32_t* cu, int num_seqs, int total, int max_seqlen, int32_t* cu_out,
+                                 int* status, cudaStream_t s);
+cudaError_t launch_check_paged(const int32_t* cu_q, const int32_t* seq_lens, const int32_t* table, int num_reqs,
+                               int total_q, int max_q_len, int max_seq_len, int max_blocks, int num_blocks,
+                               int block_size, int window, int32_t* cu_out, int* status, cudaStream_t s);
+
 // Size of the static scratch behind attn_decode_paged_noalloc (64 MiB).
 constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;
 

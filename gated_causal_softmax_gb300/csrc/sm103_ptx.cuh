@@ -16,6 +16,7 @@ namespace gcs {
 
 // Device status word values (mirrors gcs_status in the public header).
 constexpr int kDevOk = 0;
+constexpr int kDevInvalidArg = 1;   // the device-content checks found a broken precondition
 constexpr int kDevUnsupported = 2;  // a launch-time precondition failed on the device
 constexpr int kDevTimeout = 5;
 

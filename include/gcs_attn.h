@@ -33,7 +33,8 @@
  *   - bf16 = bfloat16 stored as uint16; fp8 = OCP e4m3 ("fn") stored as uint8.
  *   - Device-side contents (cu_seqlens monotone and ending at total_tokens, page-table
  *     entries in [0, num_blocks), seq_lens >= q_len) are preconditions; they are not
- *     checked on the host because reading them would synchronise.
+ *     checked on the host because reading them would synchronise.  gcs_set_device_checks
+ *     makes every call check them on the device first (see "device-content checks").
  *   - Every wait inside a kernel is bounded (2 s).  A kernel that gives up records
  *     GCS_ERR_DEVICE_TIMEOUT in a per-device status word, releases its resources and
  *     returns; read it with gcs_get_device_status().
@@ -234,6 +235,40 @@ int gcs_get_device_status(int* status, int clear);
  * stays usable.  Read (and clear) the word with gcs_get_device_status.
  * Returns GCS_OK once the kernel is launched, or GCS_ERR_CUDA. */
 int gcs_selftest_bounded_wait(gcs_stream_t stream);
+
+/* ------------------------------------------------------------------ device-content checks
+ * A library diagnostic with no counterpart in the pages.  The preconditions checked:
+ *   prefill: cu_seqlens[0] == 0, cu_seqlens[num_seqs] == total_tokens, and every length
+ *            cu_seqlens[s+1] - cu_seqlens[s] in 0 .. max_seqlen;
+ *   paged:   cu_q[0] == 0, cu_q[num_reqs] == total_q; for every request
+ *            0 <= q_len <= max_q_len and q_len <= seq_len <= max_seq_len; and, for a request
+ *            with q_len >= 1, every block_table entry in [0, num_blocks) from the 128-key tile
+ *            that holds the earliest key one of its query rows sees (key 0 without a window)
+ *            up to the page of its last cached token (the pages the paged calls can read).
+ * A failed check records GCS_ERR_INVALID_ARG in the current device's status word (first
+ * writer wins, like a timeout); read it with gcs_get_device_status.
+ *
+ * gcs_set_device_checks(1) turns on checked mode for every later call of this process (0
+ * turns it off; other values return GCS_ERR_INVALID_ARG).  In checked mode each attn_* call
+ * first launches one single-CTA kernel on its stream that checks its arrays and writes a copy
+ * of cu_seqlens (or cu_q) to the end of the call's workspace; the call's kernels read that
+ * copy.  When a check fails the copy is all zeros, an empty batch: no kernel then reads a key,
+ * a query row or a page-table entry, so a broken array cannot send a kernel outside a buffer.
+ * The outputs of such a call are unspecified.  The copy takes ((num_seqs or num_reqs) + 1)
+ * x 4 bytes, rounded up to 256, more workspace: the *_workspace queries include it while
+ * checked mode is on (query them after switching the mode), so attn_fwd and
+ * attn_prefill_paged then need a workspace even where they otherwise take none;
+ * attn_decode_paged_noalloc keeps it in its scratch.  gcs_get_device_checks returns the mode.
+ *
+ * gcs_check_prefill_inputs / gcs_check_paged_inputs run the same checks on their own (no
+ * copy, nothing else launched) on the stream, after the host validation of attn_fwd (or
+ * attn_bwd) and of attn_decode_paged or attn_prefill_paged, whose errors they return.
+ * Return GCS_OK once the kernel is launched, or the host validation's error, or
+ * GCS_ERR_CUDA. */
+int gcs_set_device_checks(int enable);
+int gcs_get_device_checks(void);
+int gcs_check_prefill_inputs(const gcs_prefill_args* a, gcs_stream_t stream);
+int gcs_check_paged_inputs(const gcs_decode_args* a, gcs_stream_t stream);
 
 /* ------------------------------------------------------------------ instrumentation
  * Arms two caller-created CUDA events (cudaEvent_t, passed as void*) for the next attn_fwd,

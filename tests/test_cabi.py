@@ -149,3 +149,38 @@ def test_prefill_paged_validation_and_workspace_on_host(L):
     assert pp(decode(max_q_len=64, hq=32)) == 2
     assert pp(decode(max_q_len=64, segment_len=-128)) == 1
     assert L.attn_prefill_paged(b(decode(max_q_len=64)), FAKE + 8, FAKE, 1 << 40, None) == 1
+
+
+def test_device_checks_mode_and_workspace_on_host(L):
+    """Checked mode: the switch takes 0 or 1, and while it is on every workspace query adds
+    the checked copy of cu_seqlens / cu_q ((n + 1) int32 rounded up to 256 B) at its end.
+    The host validation of the stand-alone checks runs before any CUDA call."""
+    b = ctypes.byref
+    assert L.gcs_set_device_checks(2) == 1
+    assert L.gcs_get_device_checks() == 0
+    base = dict(fwd=L.attn_fwd_workspace(b(prefill())), fwd_g=L.attn_fwd_workspace(b(prefill(log_gate=FAKE))),
+                bwd=L.attn_bwd_workspace(b(prefill(num_seqs=300, log_gate=FAKE))),
+                dec=L.attn_decode_workspace(b(decode())),
+                pp=L.attn_prefill_paged_workspace(b(decode(max_q_len=64, segment_len=256))),
+                pp1=L.attn_prefill_paged_workspace(b(decode(max_q_len=64, segment_len=4096))))
+    assert L.gcs_set_device_checks(1) == 0
+    try:
+        assert L.gcs_get_device_checks() == 1
+        assert L.attn_fwd_workspace(b(prefill())) == base["fwd"] + 256
+        assert L.attn_fwd_workspace(b(prefill(log_gate=FAKE))) == base["fwd_g"] + 256
+        assert L.attn_bwd_workspace(b(prefill(num_seqs=300, log_gate=FAKE))) == base["bwd"] + 1280  # 301 x 4 B
+        assert L.attn_decode_workspace(b(decode())) == base["dec"] + 256
+        assert L.attn_prefill_paged_workspace(b(decode(max_q_len=64, segment_len=256))) == base["pp"] + 256
+        # one segment per request: the copy alone, so the call now needs a workspace
+        assert base["pp1"] == 0
+        assert L.attn_prefill_paged_workspace(b(decode(max_q_len=64, segment_len=4096))) == 256
+        assert L.attn_prefill_paged(b(decode(max_q_len=64, segment_len=4096)), FAKE, None, 0, None) == 3
+        assert L.attn_fwd(b(prefill()), FAKE, FAKE, None, 0, None) == 3
+    finally:
+        assert L.gcs_set_device_checks(0) == 0
+    assert L.attn_fwd_workspace(b(prefill())) == base["fwd"]
+    # the stand-alone checks validate their arguments on the host first
+    assert L.gcs_check_prefill_inputs(b(prefill(hq=3, hkv=2)), None) == 1
+    assert L.gcs_check_prefill_inputs(b(prefill(dqk=96, dv=96)), None) == 2
+    assert L.gcs_check_paged_inputs(b(decode(block_size=32)), None) == 2
+    assert L.gcs_check_paged_inputs(b(decode(cu_q=None)), None) == 1
