@@ -172,6 +172,43 @@ def barrier(world):
         dist.barrier()
 
 
+def time_decode_graph(world, step, nbytes, calls=10, replays=5):
+    """The same decode calls captured once into a CUDA graph (the split kernel and the combine of
+    `calls` back-to-back calls) and replayed: per-call time and GB/s without host launch work.
+    A capture the runtime refuses is reported, not raised (every rank still joins the max)."""
+    import torch
+
+    err, g_ms = None, -1.0
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                step()
+        torch.cuda.current_stream().wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(calls):
+                step()
+        graph.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(replays):
+            graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        g_ms = e0.elapsed_time(e1) / (replays * calls)
+        del graph
+    except Exception as e:  # noqa: BLE001 - reported in the JSON line
+        err = f"{type(e).__name__}: {e}"[:200]
+    g_ms = max_over_ranks(world, g_ms)
+    if err is not None or g_ms <= 0:
+        return {"error": err or "capture failed on another rank"}
+    return {"ms_per_call": round(g_ms, 4), "value": round(nbytes * world / (g_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "calls_per_graph": calls, "replays": replays}
+
+
 def max_over_ranks(world, x, device="cuda"):
     """Maximum of a per-rank host value over all ranks (the timed region of the slowest rank)."""
     if world == 1:
@@ -541,6 +578,22 @@ def run_native(args):
                             "peak_source": f"{pk_kind} bf16_tflops_sustained (f16 runs at the bf16 rate)",
                             "kernel_ms": round(pk_ms, 4)}}
     del pd, pout
+    torch.cuda.empty_cache()
+
+    # ------------------------------------------------ the decode calls replayed from a CUDA graph
+    # (after every other leg, so a capture the runtime refused could not disturb one)
+    gd = dict(q=dc.q.to(dev), kc=dc.k_cache.to(dev), vc=dc.v_cache.to(dev), ks=dc.k_scale.to(dev),
+              vs=dc.v_scale.to(dev), bt=dc.block_table.to(dev), sl=dc.seq_lens.to(dev), cq=dc.cu_q.to(dev))
+    gout = torch.empty_like(gd["q"])
+
+    def gstep():
+        gcs.attn_decode_paged(gd["q"], gd["kc"], gd["vc"], gd["ks"], gd["vs"], gd["bt"], gd["sl"], gd["cq"], 1, maxl,
+                              dc.scale, dc.segment_len, out=gout)
+
+    decode["graph"] = time_decode_graph(world, gstep, dbytes)
+    if "error" not in decode["graph"] and gcs.get_device_status() != 0:
+        raise RuntimeError("a decode kernel timed out")
+    del gd, gout
     torch.cuda.empty_cache()
 
     # ------------------------------------------------------------ CPU oracle baseline
