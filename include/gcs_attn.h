@@ -1,7 +1,7 @@
 /*
  * gcs_attn.h -- C ABI of the GB300 (sm_103a) gated causal softmax attention library.
  *
- * Three calls make up the hot path:
+ * Four calls make up the hot path:
  *   attn_fwd           prefill forward  (O, LSE)
  *   attn_bwd           prefill backward (dQ, dK, dV, d log_gate, d sink)
  *   attn_decode_paged  paged single-query / short-query decode over an fp8 e4m3 KV cache
@@ -105,7 +105,7 @@ int attn_fwd(const gcs_prefill_args* a, void* o, float* lse, void* workspace, si
 /* Workspace bytes attn_bwd needs. */
 size_t attn_bwd_workspace(const gcs_prefill_args* a);
 
-/* Backward of L = sum(O * dO) ([FLA] Description "gradients"; Oct 3 / Oct 5 comments).
+/* Backward of L = sum(O * dO) ([FLA] Description, the gradient list; Oct 3 / Oct 5 comments).
  * o, lse: the forward's outputs; dout: bf16 [total_tokens, hq, dv].
  * Outputs: dq bf16 [total_tokens, hq, dqk], dk bf16 [total_tokens, hkv, dqk],
  * dv bf16 [total_tokens, hkv, dv], dlog_gate fp32 [total_tokens, hq] (must be NULL iff
@@ -123,8 +123,8 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
 /* ------------------------------------------------------------------ paged decode
  * Decode / short-query attention over a paged KV cache ([AIT] commits 1-3, Technical
  * details): fp8 e4m3 with per-token fp32 scales (the default), fp8 e4m3 with one K and one
- * V scale for the whole cache (per-tensor; "Per-tensor scales use the same code as
- * before"), or bf16 with no scales (the bf16-KV route of commit 3).  Request r has q_len = cu_q[r+1] - cu_q[r] query
+ * V scale for the whole cache (per-tensor, which the page leaves on its earlier code path),
+ * or bf16 with no scales (the bf16-KV route of commit 3).  Request r has q_len = cu_q[r+1] - cu_q[r] query
  * rows (1..4) and seq_len = seq_lens[r] cached tokens (the query tokens are the last
  * q_len of them); query row t sits at position seq_len - q_len + t and sees keys
  * 0 .. seq_len - q_len + t.  Key j of request r lives in block block_table[r][j / block_size],
@@ -137,8 +137,8 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
  * e^{M_s - max M}; a partial with no visible key (M = -inf) weighs 0.
  * With per-tensor scales, k_scale and v_scale each point to one fp32 used for every token;
  * with a bf16 cache, k_cache / v_cache hold bf16 values and k_scale, v_scale must be NULL.
- * Decoding features ([FLA] Description: "the corresponding packed single-query decoding
- * features"), each optional: g_cache holds the cumulative log gates G of the cached tokens,
+ * Decoding features (the [FLA] Description asks for the prefill features on the packed
+ * single-query decode too), each optional: g_cache holds the cumulative log gates G of the cached tokens,
  * paged like the scales but per query head, fp32 [num_blocks, hq, block_size] (natural-log
  * units); the score becomes scale*q.k_j + G_i - G_j with G_i the entry at the query row's
  * own position.  window W > 0 keeps keys with position_i - j < W.  sink fp32 [hq] adds
@@ -201,7 +201,7 @@ int attn_decode_paged_noalloc(const gcs_decode_args* a, void* out, gcs_stream_t 
 
 /* ------------------------------------------------------------------ paged chunked prefill
  * Attention of query chunks of any length over the same paged fp8 KV cache ([AIT] commit
- * messages: a batch that is not all-decode takes the "2d" unified-attention route, one
+ * messages: a batch that is not all-decode takes the 2d unified-attention route, one
  * program per (kv head, query block)).  Arguments and semantics are those of
  * attn_decode_paged (gcs_decode_args, the decoding features included), except:
  *   - q_len = cu_q[r+1] - cu_q[r] may be any value in 1 .. seq_lens[r]; max_q_len >= 1 is

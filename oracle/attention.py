@@ -48,7 +48,7 @@ def _seq_bounds(cu_seqlens):
 
 def gate_cumsum(log_gate: np.ndarray, cu_seqlens) -> np.ndarray:
     """G_t = sum of g_u over u = start(seq) .. t, per sequence and head ([FLA] Description,
-    "logarithmic gates"; inclusive cumsum restarted at every sequence start)."""
+    the per-token log gates; inclusive cumsum restarted at every sequence start)."""
     g = np.asarray(log_gate, dtype=np.float64)
     G = np.zeros_like(g)
     for a, b in _seq_bounds(cu_seqlens):
@@ -121,7 +121,7 @@ def prefill_forward(q, k, v, cu_seqlens, scale, log_gate=None, sink=None, window
 
 
 def prefill_backward(q, k, v, do, cu_seqlens, scale, log_gate=None, sink=None, window=0):
-    """Analytic gradients of L = sum(O * dO) ([FLA] Description "gradients"; Oct 3 comment
+    """Analytic gradients of L = sum(O * dO) ([FLA] Description, the gradient list; Oct 3 comment
     for the sink).
 
       dP_ij = dO_i . v_j,   D_i = sum_j P_ij dP_ij,   dS_ij = P_ij (dP_ij - D_i)
@@ -171,8 +171,8 @@ def prefill_backward(q, k, v, do, cu_seqlens, scale, log_gate=None, sink=None, w
 def _token_values(cache, scales, blocks, kv_head, L):
     """Stored values and scales of tokens 0..L-1 of one request and kv head, before scaling:
     an e4m3 cache (uint8 codes) with one fp32 scale per token ([AIT] Technical details,
-    layout [num_blocks, num_kv_heads, block_size]) or one per tensor (the older path the
-    same section keeps: "Per-tensor scales use the same code as before"); or a bf16 cache
+    layout [num_blocks, num_kv_heads, block_size]) or one per tensor (the same section leaves
+    per-tensor scaling on the path that existed before); or a bf16 cache
     ([AIT] commit 3, the bf16-KV route) with no scales.  Slots at or past L are never read.
     Returns (values [L, d], scales [L]) in float64."""
     bs = cache.shape[2]
@@ -354,7 +354,7 @@ def decode_paged_splitk(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_
 
 
 def rel_rms(x, ref) -> float:
-    """||x - ref||_2 / ||ref||_2 over the whole tensor (the pages' "relative RMS error")."""
+    """||x - ref||_2 / ||ref||_2 over the whole tensor (the error measure of the pages' budget)."""
     x = np.asarray(x, np.float64)
     ref = np.asarray(ref, np.float64)
     den = math.sqrt(float((ref * ref).sum()))
