@@ -184,3 +184,39 @@ def test_device_checks_mode_and_workspace_on_host(L):
     assert L.gcs_check_prefill_inputs(b(prefill(dqk=96, dv=96)), None) == 2
     assert L.gcs_check_paged_inputs(b(decode(block_size=32)), None) == 2
     assert L.gcs_check_paged_inputs(b(decode(cu_q=None)), None) == 1
+
+
+def test_size_limits_on_host(L):
+    """Sizes the kernels' 32-bit TMA coordinates and element offsets cannot address are
+    refused before any launch: a prefill tensor of 2^31 or more elements, and an fp8 cache of
+    2^31 or more rows (num_blocks x hkv x block_size); just below both limits is accepted."""
+    b = ctypes.byref
+    fwd = lambda a: L.attn_fwd(b(a), FAKE, FAKE, FAKE, 1 << 40, None)
+    # hq x dqk = 4 x 128 = 512 elements per token: 2^22 tokens reach 2^31 elements
+    assert fwd(prefill(total_tokens=1 << 22, max_seqlen=1 << 22)) == 2
+    assert L.attn_fwd_workspace(b(prefill(total_tokens=(1 << 22) - 1, max_seqlen=1 << 20))) == 0
+    assert L.attn_bwd_workspace(b(prefill(total_tokens=(1 << 22) - 1, max_seqlen=1 << 20))) > 0
+    # the larger of dqk and dv counts: dv = 512 with 2^20 tokens and hq = 4 is 2^31 elements
+    assert fwd(prefill(total_tokens=1 << 20, max_seqlen=1 << 20, dqk=256, dv=512)) == 2
+    dec = lambda a: L.attn_decode_paged(b(a), FAKE, FAKE, 1 << 40, None)
+    # hkv x block_size = 64 rows per block: 2^25 blocks reach 2^31 rows
+    assert dec(decode(num_blocks=1 << 25)) == 2
+    assert L.attn_decode_workspace(b(decode(num_blocks=(1 << 25) - 1))) > 0
+    # a bf16 cache is read with plain 64-bit addressing and has no row limit
+    assert L.attn_decode_workspace(b(decode(num_blocks=1 << 25, kv_format=1, k_scale=None, v_scale=None))) > 0
+
+
+def test_degenerate_shapes_on_host(L):
+    """Zero or negative counts are invalid arguments; one-token and one-request shapes are
+    accepted (their workspace is sized)."""
+    b = ctypes.byref
+    for bad in (dict(num_seqs=0), dict(total_tokens=0), dict(max_seqlen=0), dict(hq=0), dict(hkv=0)):
+        assert L.attn_fwd(b(prefill(**bad)), FAKE, FAKE, FAKE, 1 << 40, None) == 1, bad
+        assert L.attn_fwd_workspace(b(prefill(**bad))) == 0, bad
+    assert L.attn_bwd_workspace(b(prefill(num_seqs=1, total_tokens=1, max_seqlen=1))) > 0
+    for bad in (dict(num_reqs=0), dict(total_q=0), dict(max_q_len=0), dict(max_seq_len=0), dict(num_blocks=0),
+                dict(max_blocks_per_req=0), dict(segment_len=0)):
+        assert L.attn_decode_paged(b(decode(**bad)), FAKE, FAKE, 1 << 40, None) == 1, bad
+    one = decode(num_reqs=1, total_q=1, max_seq_len=1, max_blocks_per_req=1)
+    units, rows = 1 * 1 * 4, 16  # one request, one segment, four kv heads
+    assert L.attn_decode_workspace(b(one)) == units * rows * 128 * 4 + units * rows * 2 * 4
