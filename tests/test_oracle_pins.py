@@ -201,6 +201,25 @@ def test_hand_derived_two_token_case():
         np.testing.assert_allclose(got, arr(e[name]), rtol=0, atol=1e-14, err_msg=name)
 
 
+
+def test_hand_derived_paged_decode_case():
+    """Gather through a permuted page table, K scales on the score columns, V scales after the
+    row sum, bottom-right rows of a short query, NaN slots never read, and split-K with an
+    empty partial, against values derived on paper (tests/golden/tiny_paged_decode.json)."""
+    with open(os.path.join(HERE, "golden", "tiny_paged_decode.json")) as f:
+        fx = json.load(f)
+    i, e = fx["inputs"], fx["expected"]
+    f32 = lambda x: np.array([[[np.nan if v is None else v for v in s] for s in h] for h in x], dtype=np.float32)
+    args = (np.array(i["q"], dtype=np.float64), np.array(i["k_cache"], dtype=np.uint8),
+            np.array(i["v_cache"], dtype=np.uint8), f32(i["k_scale"]), f32(i["v_scale"]),
+            np.array(i["block_table"]), np.array(i["seq_lens"]), np.array(i["cu_q"]), i["scale"])
+    want = np.array(e["out"], dtype=np.float64)
+    np.testing.assert_allclose(oracle.decode_paged(*args), want, rtol=0, atol=1e-14)
+    parts = oracle.decode_partials(*args, i["segment_len"])
+    split = oracle.decode_combine(parts, 2, 1, 1, np.array(i["cu_q"]), 1)
+    np.testing.assert_allclose(split, want, rtol=0, atol=1e-14)
+
+
 # ---------------------------------------------------------------------------- backward
 def _loss(c, q, k, v, g, s):
     o, _ = oracle.prefill_forward(q, k, v, c.cu_seqlens.numpy(), c.scale, log_gate=g, sink=s, window=c.window)
