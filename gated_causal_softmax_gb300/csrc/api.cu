@@ -89,6 +89,29 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 size_t round_up(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Byte range [a, b) of a caller buffer; a null pointer is an empty range.
+struct Span {
+  uintptr_t a, b;
+};
+Span span(const void* p, size_t bytes) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return Span{a, p ? a + bytes : a};
+}
+bool overlap(const Span& x, const Span& y) { return x.a < x.b && y.a < y.b && x.a < y.b && y.a < x.b; }
+
+// True when an output range overlaps an input range or another output range (kernels read
+// their inputs and write their outputs concurrently, so any overlap is a race).
+template <size_t NO, size_t NI>
+bool outputs_overlap(const Span (&outs)[NO], const Span (&ins)[NI]) {
+  for (size_t i = 0; i < NO; ++i) {
+    for (size_t j = 0; j < NI; ++j)
+      if (overlap(outs[i], ins[j])) return true;
+    for (size_t j = i + 1; j < NO; ++j)
+      if (overlap(outs[i], outs[j])) return true;
+  }
+  return false;
+}
+
 // Carves consecutive 256-B aligned regions out of a workspace.
 struct Carver {
   uint8_t* base;
@@ -123,6 +146,17 @@ int check_prefill(const gcs_prefill_args* a) {
   const double big = 2147483647.0;
   if ((double)a->total_tokens * a->hq * (a->dqk > a->dv ? a->dqk : a->dv) > big) return GCS_ERR_UNSUPPORTED;
   return GCS_OK;
+}
+
+// Byte ranges of a prefill call's inputs: q, k, v, log_gate, sink, cu_seqlens.
+struct PrefillSpans {
+  Span q, k, v, g, s, cu;
+};
+PrefillSpans prefill_spans(const gcs_prefill_args* a) {
+  const size_t t = (size_t)a->total_tokens;
+  return PrefillSpans{span(a->q, t * a->hq * a->dqk * 2),     span(a->k, t * a->hkv * a->dqk * 2),
+                      span(a->v, t * a->hkv * a->dv * 2),     span(a->log_gate, t * a->hq * 4),
+                      span(a->sink, (size_t)a->hq * 4),       span(a->cu_seqlens, ((size_t)a->num_seqs + 1) * 4)};
 }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? GCS_OK : GCS_ERR_CUDA; }
@@ -206,6 +240,13 @@ int attn_fwd(const gcs_prefill_args* a, void* o, float* lse, void* workspace, si
   int st = check_prefill(a);
   if (st != GCS_OK) return st;
   if (!o || !lse || !aligned16(o) || !aligned16(lse)) return GCS_ERR_INVALID_ARG;
+  {
+    const size_t t = (size_t)a->total_tokens;
+    const PrefillSpans in = prefill_spans(a);
+    const Span outs[] = {span(o, t * a->hq * a->dv * 2), span(lse, t * a->hq * 4)};
+    const Span ins[] = {in.q, in.k, in.v, in.g, in.s, in.cu};
+    if (outputs_overlap(outs, ins)) return GCS_ERR_INVALID_ARG;
+  }
   const bool chk = device_checks_on();
   const size_t need = fwd_ws(a, chk);
   if (need > 0 && (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)))
@@ -273,6 +314,16 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
     return GCS_ERR_INVALID_ARG;
   if ((dlog_gate == nullptr) != (a->log_gate == nullptr)) return GCS_ERR_INVALID_ARG;
   if ((dsink == nullptr) != (a->sink == nullptr)) return GCS_ERR_INVALID_ARG;
+  {
+    const size_t t = (size_t)a->total_tokens;
+    const PrefillSpans in = prefill_spans(a);
+    const Span outs[] = {span(dq, t * a->hq * a->dqk * 2), span(dk, t * a->hkv * a->dqk * 2),
+                         span(dv, t * a->hkv * a->dv * 2), span(dlog_gate, t * a->hq * 4),
+                         span(dsink, (size_t)a->hq * 4)};
+    const Span ins[] = {in.q,  in.k, in.v, in.g, in.s, in.cu, span(o, t * a->hq * a->dv * 2), span(lse, t * a->hq * 4),
+                        span(dout, t * a->hq * a->dv * 2)};
+    if (outputs_overlap(outs, ins)) return GCS_ERR_INVALID_ARG;
+  }
   const bool chk = device_checks_on();
   const size_t need = bwd_ws(a, chk);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
@@ -415,6 +466,25 @@ static int check_decode(const gcs_decode_args* a) {
   return GCS_OK;
 }
 
+// True when the output of a paged call overlaps one of its inputs.
+static bool paged_out_overlaps(const gcs_decode_args* a, const void* out) {
+  const size_t rows = (size_t)a->num_blocks * a->hkv * a->block_size;
+  const size_t elt = a->kv_format == GCS_KV_BF16 ? 2 : 1;
+  const size_t sc = a->scale_mode == GCS_SCALE_PER_TENSOR ? 4 : rows * 4;
+  const Span outs[] = {span(out, (size_t)a->total_q * a->hq * a->d * 2)};
+  const Span ins[] = {span(a->q, (size_t)a->total_q * a->hq * a->d * 2),
+                      span(a->k_cache, rows * a->d * elt),
+                      span(a->v_cache, rows * a->d * elt),
+                      span(a->k_scale, sc),
+                      span(a->v_scale, sc),
+                      span(a->block_table, (size_t)a->num_reqs * a->max_blocks_per_req * 4),
+                      span(a->seq_lens, (size_t)a->num_reqs * 4),
+                      span(a->cu_q, ((size_t)a->num_reqs + 1) * 4),
+                      span(a->g_cache, (size_t)a->num_blocks * a->hq * a->block_size * 4),
+                      span(a->sink, (size_t)a->hq * 4)};
+  return outputs_overlap(outs, ins);
+}
+
 // Kernel parameters common to the paged calls (segments and partial buffers set by the caller).
 static void fill_paged_params(const gcs_decode_args* a, void* out, int* status, DecodeParams& p) {
   p.cu_q = a->cu_q;
@@ -482,6 +552,7 @@ int attn_decode_paged(const gcs_decode_args* a, void* out, void* workspace, size
   int st = check_decode(a);
   if (st != GCS_OK) return st;
   if (!out || !aligned16(out)) return GCS_ERR_INVALID_ARG;
+  if (paged_out_overlaps(a, out)) return GCS_ERR_INVALID_ARG;
   int max_segs = 0;
   const bool chk = device_checks_on();
   const size_t need = decode_ws(a, chk, &max_segs);
@@ -581,6 +652,7 @@ int attn_prefill_paged(const gcs_decode_args* a, void* out, void* workspace, siz
   int st = check_prefill_paged(a);
   if (st != GCS_OK) return st;
   if (!out || !aligned16(out)) return GCS_ERR_INVALID_ARG;
+  if (paged_out_overlaps(a, out)) return GCS_ERR_INVALID_ARG;
   PagedPlan pl;
   const bool chk = device_checks_on();
   if (!plan_prefill_paged(a, chk, &pl)) return GCS_ERR_CUDA;

@@ -30,6 +30,9 @@
  *     nothing, so outputs are untouched.
  *   - Tensors are contiguous, row-major, last dimension fastest; base addresses are
  *     16-byte aligned.
+ *   - No output may share a byte with an input or with another output (the kernels read
+ *     and write concurrently); such a call returns GCS_ERR_INVALID_ARG.  Inputs may share
+ *     memory with each other.
  *   - bf16 = bfloat16 stored as uint16; fp8 = OCP e4m3 ("fn") stored as uint8.
  *   - Device-side contents (cu_seqlens monotone and ending at total_tokens, page-table
  *     entries in [0, num_blocks), seq_lens >= q_len) are preconditions; they are not

@@ -42,6 +42,14 @@ def test_library_exports_every_declared_symbol(L):
 FAKE = 0x10000  # 16-B aligned, never dereferenced by host validation
 
 
+def at(k):
+    """A fake 16-B aligned address k GiB above 64 GiB: ranges there never meet FAKE's."""
+    return (1 << 36) + k * (1 << 30)
+
+
+OUT, OUT2 = at(0), at(1)  # fake output buffers apart from the inputs
+
+
 def prefill(**over):
     import gated_causal_softmax_gb300 as gcs
 
@@ -74,7 +82,7 @@ def test_prefill_validation_on_host(L):
     assert fwd(prefill(dqk=128, dv=256)) == 2
     assert L.attn_fwd(b(prefill()), None, FAKE, FAKE, 0, None) == 1  # no output
     # gated forward needs a workspace
-    assert L.attn_fwd(b(prefill(log_gate=FAKE)), FAKE, FAKE, None, 0, None) == 3
+    assert L.attn_fwd(b(prefill(log_gate=FAKE)), OUT, OUT2, None, 0, None) == 3
     bwd = lambda a, **k: L.attn_bwd(b(a), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, k.get("dg"), k.get("ds"), FAKE,
                                     1 << 40, None)
     assert bwd(prefill(log_gate=FAKE)) == 1  # dlog_gate must be given iff log_gate is
@@ -114,7 +122,7 @@ def test_decode_validation_on_host(L):
     assert dec(decode(segment_len=2040)) == 2
     assert dec(decode(k_scale=None)) == 1
     assert dec(decode(max_blocks_per_req=10)) == 1  # table too short for max_seq_len
-    assert L.attn_decode_paged(b(decode()), FAKE, None, 0, None) == 3
+    assert L.attn_decode_paged(b(decode()), OUT, None, 0, None) == 3
     assert L.attn_decode_paged(b(decode()), FAKE + 8, FAKE, 1 << 40, None) == 1
     # cache formats and scale modes: a bf16 cache takes no scales; per-tensor scales need
     # 4-byte alignment; unknown formats or modes are invalid
@@ -134,7 +142,7 @@ def test_decode_validation_on_host(L):
 
 def test_prefill_paged_validation_and_workspace_on_host(L):
     b = ctypes.byref
-    pp = lambda a, ws=1 << 40: L.attn_prefill_paged(b(a), FAKE, FAKE, ws, None)
+    pp = lambda a, ws=1 << 40: L.attn_prefill_paged(b(a), OUT, FAKE, ws, None)
     # any q_len is accepted; the workspace holds the split-K partials of the chosen segments
     a = decode(max_q_len=64, segment_len=256)
     units, rows = 2 * (4096 // 256) * 4, 64 * 16
@@ -174,8 +182,8 @@ def test_device_checks_mode_and_workspace_on_host(L):
         # one segment per request: the copy alone, so the call now needs a workspace
         assert base["pp1"] == 0
         assert L.attn_prefill_paged_workspace(b(decode(max_q_len=64, segment_len=4096))) == 256
-        assert L.attn_prefill_paged(b(decode(max_q_len=64, segment_len=4096)), FAKE, None, 0, None) == 3
-        assert L.attn_fwd(b(prefill()), FAKE, FAKE, None, 0, None) == 3
+        assert L.attn_prefill_paged(b(decode(max_q_len=64, segment_len=4096)), OUT, None, 0, None) == 3
+        assert L.attn_fwd(b(prefill()), OUT, OUT2, None, 0, None) == 3
     finally:
         assert L.gcs_set_device_checks(0) == 0
     assert L.attn_fwd_workspace(b(prefill())) == base["fwd"]
@@ -220,3 +228,38 @@ def test_degenerate_shapes_on_host(L):
     one = decode(num_reqs=1, total_q=1, max_seq_len=1, max_blocks_per_req=1)
     units, rows = 1 * 1 * 4, 16  # one request, one segment, four kv heads
     assert L.attn_decode_workspace(b(one)) == units * rows * 128 * 4 + units * rows * 2 * 4
+
+
+def test_outputs_overlapping_inputs_are_rejected_on_host(L):
+    """An output whose byte range meets an input's or another output's is an invalid
+    argument; adjacent ranges are fine.  Accepted calls stop at the missing workspace (3),
+    so nothing is launched either way."""
+    b = ctypes.byref
+    a = prefill(log_gate=FAKE, sink=FAKE)  # inputs may share memory with each other
+    qbytes = 256 * 4 * 128 * 2  # q [256, 4, 128] bf16, the largest input
+    fwd = lambda o, lse: L.attn_fwd(b(a), o, lse, None, 0, None)
+    assert fwd(FAKE, OUT) == 1  # o on q
+    assert fwd(FAKE + qbytes - 16, OUT) == 1  # o's first bytes on q's last
+    assert fwd(FAKE + qbytes, OUT) == 3  # adjacent
+    assert fwd(OUT, OUT + 16) == 1  # lse inside o
+    assert fwd(OUT, OUT + 256 * 4 * 128 * 2) == 3  # lse right after o
+    bwd = lambda dq, dk, dv, dg, ds, dout=at(5): L.attn_bwd(b(a), at(3), at(4), dout, dq, dk, dv, dg, ds, None, 0,
+                                                         None)
+    outs = [at(6), at(7), at(8), at(9), at(10)]
+    assert bwd(*outs) == 3
+    for i in range(5):
+        bad = list(outs)
+        bad[i] = FAKE  # each output on the inputs
+        assert bwd(*bad) == 1, i
+    assert bwd(at(6), at(6) + 64, at(8), at(9), at(10)) == 1  # dk inside dq
+    assert bwd(*outs, dout=at(8) + 1024) == 1  # dv on dout
+    dec = lambda out, **over: L.attn_decode_paged(b(decode(**over)), out, None, 0, None)
+    assert dec(OUT) == 3
+    assert dec(FAKE) == 1  # out on every input
+    assert dec(OUT, block_table=OUT + 32) == 1
+    assert dec(OUT, g_cache=OUT2, sink=OUT + 4096) == 1
+    assert dec(OUT, g_cache=OUT2, sink=OUT2 + 600 * 64 * 16 * 4) == 3  # sink right after g_cache, apart from out
+    pp = lambda out, **over: L.attn_prefill_paged(b(decode(max_q_len=64, segment_len=256, **over)), out, None, 0,
+                                                  None)
+    assert pp(OUT) == 3
+    assert pp(OUT, k_scale=OUT + 512) == 1
