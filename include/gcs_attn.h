@@ -127,10 +127,11 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
  * Decode / short-query attention over a paged KV cache ([AIT] commits 1-3, Technical
  * details): fp8 e4m3 with per-token fp32 scales (the default), fp8 e4m3 with one K and one
  * V scale for the whole cache (per-tensor, which the page leaves on its earlier code path),
- * or bf16 with no scales (the bf16-KV route of commit 3).  Request r has q_len = cu_q[r+1] - cu_q[r] query
- * rows (1..4) and seq_len = seq_lens[r] cached tokens (the query tokens are the last
- * q_len of them); query row t sits at position seq_len - q_len + t and sees keys
- * 0 .. seq_len - q_len + t.  Key j of request r lives in block block_table[r][j / block_size],
+ * or bf16 with no scales (the bf16-KV route of commit 3).  Request r has
+ * q_len = cu_q[r+1] - cu_q[r] query rows (1..4) and seq_len = seq_lens[r] cached tokens (the
+ * query tokens are the last q_len of them); query row t sits at position seq_len - q_len + t
+ * and sees keys 0 .. seq_len - q_len + t.  Key j of request r lives in block
+ * block_table[r][j / block_size],
  * slot j % block_size.  Dequantised key = e4m3(k) * k_scale[block][kv_head][slot], same for
  * values.  s_j = scale * k_scale_j * (q . k8_j); the row sum uses the unscaled e^{s_j - m};
  * the V scales multiply the probabilities after the row sum.  Slots at or past seq_len are
@@ -141,9 +142,9 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
  * With per-tensor scales, k_scale and v_scale each point to one fp32 used for every token;
  * with a bf16 cache, k_cache / v_cache hold bf16 values and k_scale, v_scale must be NULL.
  * Decoding features (the [FLA] Description asks for the prefill features on the packed
- * single-query decode too), each optional: g_cache holds the cumulative log gates G of the cached tokens,
- * paged like the scales but per query head, fp32 [num_blocks, hq, block_size] (natural-log
- * units); the score becomes scale*q.k_j + G_i - G_j with G_i the entry at the query row's
+ * single-query decode too), each optional: g_cache holds the cumulative log gates G of the
+ * cached tokens, paged like the scales but per query head, fp32 [num_blocks, hq, block_size]
+ * (natural-log units); the score becomes scale*q.k_j + G_i - G_j with G_i the entry at the query row's
  * own position.  window W > 0 keeps keys with position_i - j < W.  sink fp32 [hq] adds
  * e^sink_h to the softmax denominator (once, in the combine).
  * Supported: d == 128, block_size == 16, hq / hkv == 16, 1 <= q_len <= 4,
