@@ -187,6 +187,21 @@ def test_varlen_equals_concatenated_dense():
     np.testing.assert_allclose(ds, ds_sum, atol=1e-13)
 
 
+def test_empty_sequences_change_nothing():
+    """cu_seqlens with repeated entries (sequences of length 0, first, inside and last) give
+    the same outputs and gradients as the same tokens without them."""
+    c = make_prefill([9, 6], hq=2, hkv=1, dqk=4, dv=3, seed=23, gate=True, sink=True, window=4)
+    args = (f64(c.q), f64(c.k), f64(c.v))
+    kw = dict(log_gate=f64(c.log_gate), sink=f64(c.sink), window=4)
+    plain, padded = np.array([0, 9, 15]), np.array([0, 0, 9, 9, 15, 15])
+    for a, b in zip(oracle.prefill_forward(*args, plain, c.scale, **kw),
+                    oracle.prefill_forward(*args, padded, c.scale, **kw)):
+        np.testing.assert_array_equal(a, b)
+    for a, b in zip(oracle.prefill_backward(*args, f64(c.do), plain, c.scale, **kw),
+                    oracle.prefill_backward(*args, f64(c.do), padded, c.scale, **kw)):
+        np.testing.assert_array_equal(a, b)
+
+
 def test_hand_derived_two_token_case():
     with open(os.path.join(HERE, "golden", "tiny_gate_sink.json")) as f:
         fx = json.load(f)
