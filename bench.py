@@ -670,6 +670,26 @@ def _run_oracle(case, arrs, a, b):
     oracle.prefill_backward(arrs["q"], arrs["k"], arrs["v"], arrs["do"], cu, case.scale, **kw)
 
 
+def host_cpu():
+    """The host CPU's model as the kernel reports it (x86 "model name"; on Arm the
+    implementer / part codes), for the CPU baseline's record."""
+    import platform
+
+    try:
+        fields = {}
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k, _, v = line.partition(":")
+                fields.setdefault(k.strip(), v.strip())
+        if fields.get("model name"):
+            return fields["model name"]
+        if fields.get("CPU part"):
+            return f"{platform.machine()} implementer {fields.get('CPU implementer', '?')} part {fields['CPU part']}"
+    except OSError:
+        pass
+    return platform.machine() or "unknown"
+
+
 def cpu_baseline(case, min_seconds=10.0):
     arrs, fl, desc, (a, b) = _oracle_sample(case)
     n, t0 = 0, time.perf_counter()
@@ -680,7 +700,7 @@ def cpu_baseline(case, min_seconds=10.0):
         if dt >= min_seconds:
             break
     return {"value": round(fl * n / dt / 1e12, 6), "unit": "TFLOP/s", "cores": len(os.sched_getaffinity(0)),
-            "kind": "oracle", "sample": f"{desc}; repeated {n}x over {dt:.1f} s"}
+            "cpu_model": host_cpu(), "kind": "oracle", "sample": f"{desc}; repeated {n}x over {dt:.1f} s"}
 
 
 def _oracle_paged(dc, rows):
@@ -719,8 +739,8 @@ def cpu_baseline_paged(dc, rows, unit, min_seconds=5.0):
     else:
         work = paged_chunk_flops(seq, [1] * len(seq), dc.hq, dc.d)
         value = work * n / dt / 1e12
-    return {"value": round(value, 6), "unit": unit, "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-            "sample": f"oracle (numpy fp64) on {len(rows)} query rows of the workload, every query head; "
+    return {"value": round(value, 6), "unit": unit, "cores": len(os.sched_getaffinity(0)), "cpu_model": host_cpu(),
+            "kind": "oracle", "sample": f"oracle (numpy fp64) on {len(rows)} query rows of the workload, every query head; "
                       f"repeated {n}x over {dt:.1f} s"}
 
 
@@ -757,8 +777,8 @@ def run_reference(args):
         "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": PREFILL_WORKLOAD, "sample": desc},
-        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": desc},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "cpu_model": host_cpu(),
+                         "kind": "oracle", "sample": desc},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
