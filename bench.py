@@ -279,8 +279,9 @@ def run_native(args):
     clocks = sampler.stop()
     ms_total = max_over_ranks(world, t0.elapsed_time(t1))
     ms_step = ms_total / K
-    fwd_k = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    bwd_k = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    fwd_all = [e[0].elapsed_time(e[1]) for e in evs]
+    bwd_all = [e[2].elapsed_time(e[3]) for e in evs]
+    fwd_k, bwd_k = statistics.mean(fwd_all), statistics.mean(bwd_all)
     value = whole_job_rate(step_fl, world, ms_total / K * 1e-3) / 1e12
     if gcs.get_device_status() != 0:
         raise RuntimeError("a kernel timed out during the timed region")
@@ -296,6 +297,8 @@ def run_native(args):
                 "unit": "TFLOP/s", "frac": round(achieved / sustained, 4), "traffic": traffic,
                 "peak_source": f"{pk_kind} bf16_tflops_sustained", "algorithmic_flops_per_launch": dom_fl,
                 "fwd_kernel_ms": round(fwd_k, 4), "bwd_kernel_ms": round(bwd_k, 4),
+                "kernel_ms_median_min": {"fwd": [round(statistics.median(fwd_all), 4), round(min(fwd_all), 4)],
+                                         "bwd": [round(statistics.median(bwd_all), 4), round(min(bwd_all), 4)]},
                 "fwd_kernel_tflops": round(fwd_fl / (fwd_k * 1e-3) / 1e12, 1),
                 "bwd_kernel_tflops": round(bwd_fl / (bwd_k * 1e-3) / 1e12, 1)}
 
@@ -406,7 +409,8 @@ def run_native(args):
     torch.cuda.synchronize()
     barrier(world)
     dec_ms = max_over_ranks(world, d0.elapsed_time(d1)) / DK
-    split_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in devs)
+    split_all = [e[0].elapsed_time(e[1]) for e in devs]
+    split_ms = statistics.mean(split_all)
     dbytes = decode_bytes(dc.seq_lens.tolist(), dc.q_lens, dc.hq, dc.hkv, dc.d, dc.block_size)
     hbm = pk.get("hbm_gbs")
     dec_gbs = dbytes * world / (dec_ms * 1e-3) / 1e9
@@ -419,7 +423,9 @@ def run_native(args):
                            "traffic": (args.decode_traffic if args.decode_traffic is not None
                                        else NCU_TRAFFIC["decode_split"]),
                            "peak_source": f"{pk_kind} hbm_gbs",
-                           "kernel_ms": round(split_ms, 4)}}
+                           "kernel_ms": round(split_ms, 4),
+                           "kernel_ms_median_min": [round(statistics.median(split_all), 4),
+                                                    round(min(split_all), 4)]}}
     if gcs.get_device_status() != 0:
         raise RuntimeError("a decode kernel timed out")
     del dd
