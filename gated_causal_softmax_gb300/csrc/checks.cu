@@ -7,8 +7,8 @@
 // kernels then read in place of the caller's: a copy when every check holds, and all zeros
 // (an empty batch) when one fails, in which case it records kDevInvalidArg in the device
 // status word.  In an empty batch every prefill tile and every paged request has no rows, so
-// every kernel of the library returns before it reads a key, a query row or a page-table
-// entry.
+// no kernel reads through an index taken from these arrays (the kernels that sweep every
+// token, such as the backward's delta, stay within total_tokens, which the host checked).
 #include "kernels.h"
 #include "sm103_ptx.cuh"
 

@@ -256,8 +256,9 @@ int gcs_selftest_bounded_wait(gcs_stream_t stream);
  * turns it off; other values return GCS_ERR_INVALID_ARG).  In checked mode each attn_* call
  * first launches one single-CTA kernel on its stream that checks its arrays and writes a copy
  * of cu_seqlens (or cu_q) to the end of the call's workspace; the call's kernels read that
- * copy.  When a check fails the copy is all zeros, an empty batch: no kernel then reads a key,
- * a query row or a page-table entry, so a broken array cannot send a kernel outside a buffer.
+ * copy.  When a check fails the copy is all zeros, an empty batch: no kernel then reads
+ * through an index taken from these arrays, so a broken array cannot send a kernel outside a
+ * buffer.
  * The outputs of such a call are unspecified.  The copy takes ((num_seqs or num_reqs) + 1)
  * x 4 bytes, rounded up to 256, more workspace: the *_workspace queries include it while
  * checked mode is on (query them after switching the mode), so attn_fwd and
