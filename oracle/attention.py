@@ -42,6 +42,8 @@ from .formats import e4m3_decode
 
 
 def _seq_bounds(cu_seqlens):
+    """(start, end) token ranges of the packed sequences ([FLA] Description, packed
+    variable-length inputs: sequence s owns tokens cu_seqlens[s] .. cu_seqlens[s+1] - 1)."""
     cu = [int(x) for x in np.asarray(cu_seqlens).tolist()]
     return [(cu[i], cu[i + 1]) for i in range(len(cu) - 1)]
 
@@ -57,7 +59,8 @@ def gate_cumsum(log_gate: np.ndarray, cu_seqlens) -> np.ndarray:
 
 
 def _allowed(T: int, window: int) -> np.ndarray:
-    """Mask of visible (i, j) pairs inside one sequence: causal j <= i, and i - j < W."""
+    """Mask of visible (i, j) pairs inside one sequence ([FLA] Description, causal attention
+    with sliding windows): causal j <= i, and i - j < W when a window W is set."""
     i = np.arange(T)[:, None]
     j = np.arange(T)[None, :]
     m = j <= i
@@ -67,6 +70,8 @@ def _allowed(T: int, window: int) -> np.ndarray:
 
 
 def _scores(qh, kh, scale, Gh, allowed):
+    """s_ij = scale q_i . k_j + G_i - G_j for visible pairs, -inf elsewhere ([FLA] Description,
+    causal attention with logarithmic gates)."""
     S = scale * (qh @ kh.T)
     if Gh is not None:
         S = S + (Gh[:, None] - Gh[None, :])
@@ -75,7 +80,8 @@ def _scores(qh, kh, scale, Gh, allowed):
 
 def _softmax_with_sink(S, sink_h):
     """P_ij = e^{s_ij} / Z_i and p_sink,i = e^{sigma} / Z_i with
-    Z_i = sum_j e^{s_ij} (+ e^{sigma}); returns P, p_sink (or None), ln Z."""
+    Z_i = sum_j e^{s_ij} (+ e^{sigma}); returns P, p_sink (or None), ln Z ([FLA] Description,
+    the sink bias: one logit per head in the softmax denominator only)."""
     m = S.max(axis=1)
     if sink_h is not None:
         m = np.maximum(m, sink_h)
@@ -194,7 +200,8 @@ def _token_values(cache, scales, blocks, kv_head, L):
 
 def gather_kv(cache, scales, block_table_row, L, kv_head):
     """Dequantized keys (or values) 0..L-1 of one request and kv head: stored value times
-    its scale (see _token_values)."""
+    its scale ([AIT] Technical details: key j of a request sits in block table[j / block_size],
+    slot j % block_size; see _token_values)."""
     bs = cache.shape[2]
     npages = (L + bs - 1) // bs
     blocks = np.asarray(block_table_row[:npages], dtype=np.int64)
@@ -204,8 +211,9 @@ def gather_kv(cache, scales, block_table_row, L, kv_head):
 
 def _gate_of(g_cache, block_table_row, L, h):
     """G_j, j = 0..L-1, of one request and query head from the paged fp32 array
-    [num_blocks, hq, block_size] (reading: the cumulative log gates of the cached tokens are
-    kept paged like the scales, per query head)."""
+    [num_blocks, hq, block_size] ([FLA] Description asks for the gates on the decode path and
+    gives no layout; read here as the cumulative log gates of the cached tokens kept paged like
+    the scales, per query head)."""
     bs = g_cache.shape[2]
     npages = (L + bs - 1) // bs
     blocks = np.asarray(block_table_row[:npages], dtype=np.int64)
@@ -214,7 +222,8 @@ def _gate_of(g_cache, block_table_row, L, h):
 
 def _visible(pos, window, lo=0, hi=None):
     """Keys visible to a query at position pos: j <= pos (causal) and pos - j < W (window),
-    intersected with [lo, hi)."""
+    intersected with [lo, hi) ([AIT] commit messages: short queries are the last q_len cached
+    tokens, so a query row sees the keys up to its own position; [FLA] Description, windows)."""
     a = max(lo, pos - window + 1) if window > 0 else lo
     b = pos + 1 if hi is None else min(hi, pos + 1)
     return a, b
@@ -346,7 +355,8 @@ def decode_combine(parts, nq, hq, d, cu_q, hkv, *, sink=None):
 
 def decode_paged_splitk(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu_q, scale, segment_len, *,
                         g_cache=None, sink=None, window=0):
-    """Split-K decode: partials per context segment, then the LSE-weighted reduce."""
+    """Split-K decode ([AIT] commits and Technical details): partials per context segment,
+    then the LSE-weighted reduce."""
     q = np.asarray(q)
     parts = decode_partials(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu_q, scale, segment_len,
                             g_cache=g_cache, window=window)
@@ -354,7 +364,8 @@ def decode_paged_splitk(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_
 
 
 def rel_rms(x, ref) -> float:
-    """||x - ref||_2 / ||ref||_2 over the whole tensor (the error measure of the pages' budget)."""
+    """||x - ref||_2 / ||ref||_2 over the whole tensor (the error measure of the [FLA] issue's
+    accuracy budget)."""
     x = np.asarray(x, np.float64)
     ref = np.asarray(ref, np.float64)
     den = math.sqrt(float((ref * ref).sum()))
