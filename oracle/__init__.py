@@ -7,7 +7,8 @@ it.  It shares no code with the CUDA path.
 Parity pins: every function here is checked in ``tests/test_oracle_pins.py`` against
 library routines (fp64 ``scaled_dot_product_attention``, ``torch.autograd``,
 ``torch.float8_e4m3fn`` / ``torch.bfloat16`` conversions), closed forms, finite
-differences and invariants.  No function is "parity unpinned".
+differences, invariants and hand-derived fixtures (``tests/golden/``), and on random small
+cases in ``tests/test_oracle_properties.py``.  No function is "parity unpinned".
 """
 from .formats import bf16_round, e4m3_decode  # noqa: F401
 from .attention import (  # noqa: F401
