@@ -40,10 +40,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # (gate cumsum, delta, vector pack, dQ pass, dK/dV pass, d gate scan, d sink reduce)
 LAUNCHES_PER_PREFILL_STEP = 9
 LAUNCHES_PER_DECODE = 2
-# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) from the ncu captures
-# summarised in profiles/ (prefill_kernels_varlen_gqa_8192_d128.md,
-# decode_kernels_paged_fp8_decode_64x1.md, prefill_paged_kernel_paged_fp8_chunked_prefill_4x1024.md);
-# set back to None whenever the kernel changes.
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of each kernel on these
+# workloads, from one ncu capture of the kernel as it stands; set back to None whenever the
+# kernel changes.
 NCU_TRAFFIC = {
     "bwd": 217.9e6 + 277.0e6,  # prefill_bwd_dq_kernel<128> + prefill_bwd_kernel<128>
     "fwd": 119.8e6,            # prefill_fwd2_kernel<128>
@@ -396,9 +395,8 @@ def run_native(args):
             e.record()
     barrier(world)
     torch.cuda.synchronize()
-    # whole calls with nothing recorded between their kernels (an event between the split
-    # kernel and the combine would stop the combine's programmatic launch), then the same calls
-    # with events around the split kernel for its own duration
+    # whole calls with nothing recorded between their kernels (the call's own rate), then the
+    # same calls with events around the split kernel for its own duration
     d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     d0.record()
     for i in range(DK):

@@ -454,7 +454,7 @@ static int check_decode(const gcs_decode_args* a) {
   if (a->max_q_len > 4) return GCS_ERR_UNSUPPORTED;
   if (a->d != 128 || a->block_size != 16 || a->hq != 16 * a->hkv) return GCS_ERR_UNSUPPORTED;
   if (a->segment_len % a->block_size != 0) return GCS_ERR_UNSUPPORTED;
-  if (a->max_blocks_per_req * a->block_size < a->max_seq_len) return GCS_ERR_INVALID_ARG;
+  if ((long long)a->max_blocks_per_req * a->block_size < a->max_seq_len) return GCS_ERR_INVALID_ARG;
   if (!aligned16(a->k_cache) || !aligned16(a->v_cache) || !aligned16(a->q)) return GCS_ERR_INVALID_ARG;
   if (a->window < 0) return GCS_ERR_INVALID_ARG;
   if (a->g_cache && !aligned16(a->g_cache)) return GCS_ERR_INVALID_ARG;

@@ -41,6 +41,10 @@
  *   - Every wait inside a kernel is bounded (2 s).  A kernel that gives up records
  *     GCS_ERR_DEVICE_TIMEOUT in a per-device status word, releases its resources and
  *     returns; read it with gcs_get_device_status().
+ *   - The library caches, per device, the device addresses of its own status word and of
+ *     the scratch of attn_decode_paged_noalloc.  cudaDeviceReset unloads the library's
+ *     device code and those addresses go stale: do not call the library on a device after
+ *     cudaDeviceReset of that device in the same process.
  */
 #ifndef GCS_ATTN_H_
 #define GCS_ATTN_H_

@@ -365,7 +365,8 @@ def decode_paged_splitk(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_
 
 def rel_rms(x, ref) -> float:
     """||x - ref||_2 / ||ref||_2 over the whole tensor (the error measure of the [FLA] issue's
-    accuracy budget)."""
+    accuracy budget, comment of Oct 3).  A reference that is all zeros gives the absolute
+    norm ||x||_2 instead; a NaN in x gives NaN, which fails every tolerance comparison."""
     x = np.asarray(x, np.float64)
     ref = np.asarray(ref, np.float64)
     den = math.sqrt(float((ref * ref).sum()))

@@ -212,6 +212,11 @@ def test_size_limits_on_host(L):
     assert L.attn_decode_workspace(b(decode(num_blocks=(1 << 25) - 1))) > 0
     # a bf16 cache is read with plain 64-bit addressing and has no row limit
     assert L.attn_decode_workspace(b(decode(num_blocks=1 << 25, kv_format=1, k_scale=None, v_scale=None))) > 0
+    # the table-length check multiplies in 64 bits: (2^28 + 1) x 16 would wrap a 32-bit int to
+    # 16 tokens, below max_seq_len, and the valid shape would be refused
+    assert L.attn_decode_workspace(b(decode(max_blocks_per_req=(1 << 28) + 1))) > 0
+    assert L.attn_decode_workspace(b(decode(max_blocks_per_req=(1 << 31) - 1))) > 0
+    assert L.attn_decode_workspace(b(decode(max_blocks_per_req=255))) == 0
 
 
 def test_degenerate_shapes_on_host(L):
