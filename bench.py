@@ -34,6 +34,7 @@ PREFILL_WORKLOAD = "varlen_gqa_8192_d128"
 DECODE_WORKLOAD = "paged_fp8_decode_64x1"
 CHUNK_WORKLOAD = "paged_fp8_chunked_prefill_4x1024"
 WIDE_WORKLOAD = "window_b2_t4096_dqk256_dv512"
+LARGE_WORKLOAD = "varlen_16384_d512"
 VERIFY_WORKLOAD = "paged_fp8_verify_3x4_227k"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # my kernels per prefill step with gates and sink: fwd (gate cumsum, attention) and bwd
@@ -286,15 +287,20 @@ def run_native(args):
         raise RuntimeError("a kernel timed out during the timed region")
 
     # dominant kernel: the fused backward attention kernel
-    sustained = pk.get("bf16_tflops_sustained", pk.get("bf16_tflops"))
+    # The prefill kernels run in timed regions of tens of milliseconds at the maximum SM clock
+    # (the clock record shows it), so the burst cuBLAS figure is their peak; the sustained one
+    # was measured seconds into a power-capped loop at a lower clock and is reported beside it.
+    burst = pk["bf16_tflops"]
+    sustained = pk.get("bf16_tflops_sustained", burst)
     dom = ("prefill_bwd_dq_kernel<128> + prefill_bwd_kernel<128> (two-pass backward)" if bwd_k >= fwd_k
            else "prefill_fwd2_kernel<128>")
     dom_fl, dom_ms = (bwd_fl, bwd_k) if bwd_k >= fwd_k else (fwd_fl, fwd_k)
     achieved = dom_fl / (dom_ms * 1e-3) / 1e12
     traffic = args.traffic if args.traffic is not None else NCU_TRAFFIC["bwd" if bwd_k >= fwd_k else "fwd"]
-    roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": sustained,
-                "unit": "TFLOP/s", "frac": round(achieved / sustained, 4), "traffic": traffic,
-                "peak_source": f"{pk_kind} bf16_tflops_sustained", "algorithmic_flops_per_launch": dom_fl,
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": round(achieved, 1), "peak": burst,
+                "unit": "TFLOP/s", "frac": round(achieved / burst, 4), "traffic": traffic,
+                "peak_source": f"{pk_kind} bf16_tflops (burst)", "frac_of_sustained": round(achieved / sustained, 4),
+                "algorithmic_flops_per_launch": dom_fl,
                 "fwd_kernel_ms": round(fwd_k, 4), "bwd_kernel_ms": round(bwd_k, 4),
                 "kernel_ms_median_min": {"fwd": [round(statistics.median(fwd_all), 4), round(min(fwd_all), 4)],
                                          "bwd": [round(statistics.median(bwd_all), 4), round(min(bwd_all), 4)]},
@@ -503,39 +509,56 @@ def run_native(args):
     if gcs.get_device_status() != 0:
         raise RuntimeError("a decode kernel timed out")
 
-    # ------------------------------------------------ wide heads: Dqk 256 / Dv 512, window 1024
-    wc = prefill_config(WIDE_WORKLOAD)
-    wq, wk, wv, wdo = (t.to(dev) for t in (wc.q, wc.k, wc.v, wc.do))
-    wg, wsk, wcu = wc.log_gate.to(dev), wc.sink.to(dev), wc.cu_seqlens.to(dev)
-    wms = max(wc.seqlens)
-    wide = {"workload": WIDE_WORKLOAD, "unit": "TFLOP/s"}
-    w_fwd_fl, w_bwd_fl = prefill_flops(wc.seqlens, wc.hq, wc.dqk, wc.dv, wc.window)
-    for mode, det in (("reduce_add", False), ("deterministic", True)):
-        def wstep():
-            o_, l_ = gcs.attn_fwd(wq, wk, wv, wcu, wms, wc.scale, wc.window, log_gate=wg, sink=wsk)
-            gcs.attn_bwd(wq, wk, wv, o_, l_, wdo, wcu, wms, wc.scale, wc.window, log_gate=wg, sink=wsk,
-                         deterministic=det)
+    # ------------------------------------------------ wide heads: (256, 512) with a window, and D = 512
+    def wide_leg(name):
+        wc = prefill_config(name)
+        wq, wk, wv, wdo = (t.to(dev) for t in (wc.q, wc.k, wc.v, wc.do))
+        wg, wsk, wcu = wc.log_gate.to(dev), wc.sink.to(dev), wc.cu_seqlens.to(dev)
+        wms = max(wc.seqlens)
+        res = {"workload": name, "unit": "TFLOP/s", "seqlens": wc.seqlens}
+        w_fwd_fl, w_bwd_fl = prefill_flops(wc.seqlens, wc.hq, wc.dqk, wc.dv, wc.window)
+        for mode, det in (("reduce_add", False), ("deterministic", True)):
+            def wstep(ev=None):
+                if ev is not None:
+                    gcs.set_kernel_events(ev[0], ev[1])
+                o_, l_ = gcs.attn_fwd(wq, wk, wv, wcu, wms, wc.scale, wc.window, log_gate=wg, sink=wsk)
+                if ev is not None:
+                    gcs.set_kernel_events(ev[2], ev[3])
+                gcs.attn_bwd(wq, wk, wv, o_, l_, wdo, wcu, wms, wc.scale, wc.window, log_gate=wg, sink=wsk,
+                             deterministic=det)
 
-        for _ in range(args.warmup):
-            wstep()
-        barrier(world)
-        torch.cuda.synchronize()
-        w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        w0.record()
-        for _ in range(DK):
-            wstep()
-        w1.record()
-        torch.cuda.synchronize()
-        barrier(world)
-        w_ms = max_over_ranks(world, w0.elapsed_time(w1)) / DK
-        w_tf = (w_fwd_fl + w_bwd_fl) * world / (w_ms * 1e-3) / 1e12
-        wide[mode] = {"value": round(w_tf, 1), "pct_of_peak": round(w_tf / world / sustained, 4),
-                      "ms_per_step": round(w_ms, 4)}
-    wide["flops_per_step"] = w_fwd_fl + w_bwd_fl
-    if gcs.get_device_status() != 0:
-        raise RuntimeError("a wide-head kernel timed out")
-    del wq, wk, wv, wdo, wg, wsk, wcu
-    torch.cuda.empty_cache()
+            for _ in range(args.warmup):
+                wstep()
+            wevs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(DK)]
+            for e4 in wevs:
+                for e in e4:
+                    e.record()
+            barrier(world)
+            torch.cuda.synchronize()
+            w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            w0.record()
+            for i in range(DK):
+                wstep(wevs[i])
+            w1.record()
+            torch.cuda.synchronize()
+            barrier(world)
+            w_ms = max_over_ranks(world, w0.elapsed_time(w1)) / DK
+            w_tf = (w_fwd_fl + w_bwd_fl) * world / (w_ms * 1e-3) / 1e12
+            fk = statistics.mean(e[0].elapsed_time(e[1]) for e in wevs)
+            bk = statistics.mean(e[2].elapsed_time(e[3]) for e in wevs)
+            res[mode] = {"value": round(w_tf, 1), "pct_of_peak": round(w_tf / world / burst, 4),
+                         "ms_per_step": round(w_ms, 4), "fwd_kernel_ms": round(fk, 4), "bwd_kernel_ms": round(bk, 4),
+                         "fwd_kernel_tflops": round(w_fwd_fl / (fk * 1e-3) / 1e12, 1),
+                         "bwd_kernel_tflops": round(w_bwd_fl / (bk * 1e-3) / 1e12, 1)}
+        res["flops_per_step"] = w_fwd_fl + w_bwd_fl
+        if gcs.get_device_status() != 0:
+            raise RuntimeError("a wide-head kernel timed out")
+        del wq, wk, wv, wdo, wg, wsk, wcu
+        torch.cuda.empty_cache()
+        return res
+
+    wide = wide_leg(WIDE_WORKLOAD)
+    large = wide_leg(LARGE_WORKLOAD)
 
     # ------------------------------------------------ paged chunked prefill (fp8 cache)
     pc = decode_config(CHUNK_WORKLOAD)
@@ -574,12 +597,12 @@ def run_native(args):
     p_tf = p_fl * world / (p_ms * 1e-3) / 1e12
     pk_tf = p_fl / (pk_ms * 1e-3) / 1e12
     chunked = {"workload": CHUNK_WORKLOAD, "value": round(p_tf, 1), "unit": "TFLOP/s",
-               "pct_of_peak": round(p_tf / world / sustained, 4), "ms_per_call": round(p_ms, 4),
+               "pct_of_peak": round(p_tf / world / burst, 4), "ms_per_call": round(p_ms, 4),
                "flops_per_call": p_fl,
                "roofline": {"bound": "tensor", "kernel": "prefill_paged_kernel", "achieved": round(pk_tf, 1),
-                            "peak": sustained, "unit": "TFLOP/s", "frac": round(pk_tf / sustained, 4),
+                            "peak": burst, "unit": "TFLOP/s", "frac": round(pk_tf / burst, 4),
                             "traffic": NCU_TRAFFIC.get("prefill_paged"),
-                            "peak_source": f"{pk_kind} bf16_tflops_sustained (f16 runs at the bf16 rate)",
+                            "peak_source": f"{pk_kind} bf16_tflops burst (f16 runs at the bf16 rate)",
                             "kernel_ms": round(pk_ms, 4)}}
     del pd, pout
     torch.cuda.empty_cache()
@@ -621,7 +644,8 @@ def run_native(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "pct_of_peak": round(value / world / sustained, 4),
+        "pct_of_peak": round(value / world / burst, 4),
+        "pct_of_sustained_peak": round(value / world / sustained, 4),
         "config": {"workload": PREFILL_WORKLOAD, "seqlens": case.seqlens, "hq": case.hq, "hkv": case.hkv,
                    "dqk": case.dqk, "dv": case.dv, "gate": True, "sink": True, "window": case.window,
                    "flops_per_step": step_fl, "fwd_flops": fwd_fl, "bwd_flops": bwd_fl,
@@ -631,6 +655,7 @@ def run_native(args):
         "decode": decode,
         "chunked_prefill": chunked,
         "wide_prefill": wide,
+        "large_head_prefill": large,
         "cpu_baseline": cpu,
         "clocks": clocks,
         "e2e": e2e,

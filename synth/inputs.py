@@ -176,6 +176,10 @@ class DecodeCase:
     g_cache: Optional[torch.Tensor] = None  # fp32 [num_blocks, hq, block_size]: cumulative log gates G
     sink: Optional[torch.Tensor] = None  # fp32 [hq]
     window: int = 0
+    # the values before fp8 quantization (fp32, same layout as the caches, NaN where unused);
+    # kept only when make_decode is asked to (keep_unquantized), fp8 per-token only
+    k_unquant: Optional[torch.Tensor] = None
+    v_unquant: Optional[torch.Tensor] = None
 
     @property
     def num_reqs(self) -> int:
@@ -221,6 +225,7 @@ def make_decode(
     scale_mode: str = "per_token",
     features: bool = False,
     window: int = 0,
+    keep_unquantized: bool = False,
 ) -> DecodeCase:
     """Draw order: q N(0,1) -> bf16; a random permutation of the physical blocks (the page
     table); then per request: K scales, V scales (log-uniform over a 20x range), K normals,
@@ -241,6 +246,10 @@ def make_decode(
     (token, query head), G = their cumulative sum from the request's first token, stored
     in g_cache [num_blocks, hq, block_size] (NaN in unused slots); then sink ~ N(0, 1) [hq].
     window: the sliding window W (0 = none).
+
+    keep_unquantized (fp8 per-token only): also return the values before quantization,
+    (code input) x scale in fp32, i.e. z in reading A and 16 z x scale in reading B.  Nothing
+    extra is drawn, so the case is otherwise unchanged.
     """
     assert kv_format in ("fp8", "bf16") and scale_mode in ("per_token", "per_tensor")
     assert not (kv_format == "bf16" and scale_mode != "per_token")
@@ -277,6 +286,9 @@ def make_decode(
     v_cache = np.full((num_blocks, hkv, block_size, d), E4M3_NAN_CODE, dtype=np.uint8)
     k_sc = np.full((num_blocks, hkv, block_size), np.nan, dtype=np.float32)
     v_sc = np.full((num_blocks, hkv, block_size), np.nan, dtype=np.float32)
+    unq = {}
+    if keep_unquantized:
+        unq = {w: np.full((num_blocks, hkv, block_size, d), np.nan, dtype=np.float32) for w in "kv"}
     if scale_reading == "A":
         lo, hi, zmul = 1.0 / 64, 20.0 / 64, None
     elif scale_reading == "B":
@@ -300,6 +312,9 @@ def make_decode(
             scp = np.concatenate([sc, np.full((pad, hkv), np.nan, np.float32)], axis=0)
             cache[blocks] = codes.reshape(P, block_size, hkv, d).transpose(0, 2, 1, 3)
             scache[blocks] = scp.reshape(P, block_size, hkv).transpose(0, 2, 1)
+            if unq:
+                raw = np.concatenate([vals * sc[:, :, None], np.full((pad, hkv, d), np.nan, np.float32)], axis=0)
+                unq[which][blocks] = raw.reshape(P, block_size, hkv, d).transpose(0, 2, 1, 3)
     case = DecodeCase(
         name=name,
         q=q,
@@ -312,6 +327,8 @@ def make_decode(
         v_scale=torch.from_numpy(v_sc),
         scale=float(scale if scale is not None else 1.0 / math.sqrt(d)),
         segment_len=int(segment_len),
+        k_unquant=torch.from_numpy(unq["k"]) if unq else None,
+        v_unquant=torch.from_numpy(unq["v"]) if unq else None,
     )
     return _add_decode_features(rng, case, features, window)
 

@@ -34,6 +34,30 @@ def test_decode_parity(gcs_lib, name):
     assert abs(bias(out, ref)) <= DECODE_BIAS
 
 
+@pytest.mark.parametrize("reading", ["A", "B"])
+def test_decode_against_unquantized_reference(gcs_lib, reading):
+    """The [AIT] PR's test plan checks the decode against the dequantized reference, the
+    unquantized reference and the output bias.  Against the values before fp8 quantization
+    the error is the quantization's own: e4m3 keeps 3 mantissa bits (relative rounding error
+    at most 2^-4), which the fp64 oracle on the dequantized cache shows as about 3e-2 relative
+    RMS in reading A and 9e-2 in reading B (token magnitudes 20x apart sharpen the softmax,
+    so score errors weigh more).  The library must add nothing visible on top: its distance
+    from the unquantized reference may exceed the dequantized oracle's by at most 5 %, and it
+    stays within a fixed 5e-2 (A) / 1.5e-1 (B)."""
+    dc = make_decode([1, 17, 100, 2100, 4096, 65537], [1, 4, 2, 3, 1, 4], 16, 1, 128, seed=91,
+                     scale_reading=reading, keep_unquantized=True)
+    out = run_decode(gcs_lib, dc)
+    deq = oracle_decode(dc)
+    unq = oracle.decode_paged(f64(dc.q), dc.k_unquant.double().numpy(), dc.v_unquant.double().numpy(), None, None,
+                              dc.block_table.numpy(), dc.seq_lens.numpy(), dc.cu_q.numpy(), dc.scale)
+    assert_close("out vs dequantized", out, deq, DECODE_RTOL)
+    assert abs(bias(out, deq)) <= DECODE_BIAS
+    e_q = oracle.rel_rms(deq, unq)
+    e_lib = oracle.rel_rms(f64(out), unq)
+    assert e_lib <= {"A": 5e-2, "B": 1.5e-1}[reading], e_lib
+    assert e_lib <= 1.05 * e_q, (e_lib, e_q)
+
+
 def test_decode_rejects_prefill_shapes(gcs_lib):
     dc = make_decode([40], [5], 16, 1, 128, seed=3)
     with pytest.raises(NotImplementedError):

@@ -4,9 +4,12 @@ workspace entry point (attn_decode_paged), through the C ABI.
 The no-alloc call exists for callers that cannot allocate device memory (fixed memory
 plans, allocator-less C hosts, latency-critical loops where cudaMalloc's possible device
 synchronisation is not acceptable); it keeps the split-K partials in a fixed scratch
-inside the library.  Two calls in a row must both agree with the workspace path within
-the decode tolerance (the second call sees the first call's leftovers in the scratch),
-and a size whose partials exceed the scratch is rejected before any launch."""
+inside the library.  It runs the same kernels on the same inputs as the workspace call, so
+its output must be the same bits.  Before the calls under test, a call of the same shape
+with NaN queries fills every partial the scratch will hold with NaN: a partial that a later
+call read without first writing it would then show up as NaN or as a changed bit.  Two
+calls in a row must both match, and a size whose partials exceed the scratch is rejected
+before any launch."""
 import ctypes
 
 import pytest
@@ -14,14 +17,14 @@ import torch
 
 import oracle
 from synth import make_decode
-from helpers import DECODE_RTOL, decode_dev, f64
+from helpers import DECODE_RTOL, decode_dev, f64, oracle_decode
 
 pytestmark = pytest.mark.gpu
 
 
-def _args(gcs, dc, d):
-    return gcs.decode_args(d["q"], d["kc"], d["vc"], d["ks"], d["vs"], d["bt"], d["sl"], d["cq"], max(dc.q_lens),
-                           int(dc.seq_lens.max()), dc.scale, dc.segment_len)
+def _args(gcs, dc, d, q=None):
+    return gcs.decode_args(d["q"] if q is None else q, d["kc"], d["vc"], d["ks"], d["vs"], d["bt"], d["sl"],
+                           d["cq"], max(dc.q_lens), int(dc.seq_lens.max()), dc.scale, dc.segment_len)
 
 
 def test_noalloc_matches_workspace_entry_point_twice(gcs_lib):
@@ -38,13 +41,21 @@ def test_noalloc_matches_workspace_entry_point_twice(gcs_lib):
         ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
         ref = torch.empty_like(d["q"])
         assert L.attn_decode_paged(ctypes.byref(a), ref.data_ptr(), ws.data_ptr(), ws_bytes, stream) == 0
+        # poison: the same shape with NaN queries writes NaN into every partial of the scratch
+        q_nan = torch.full_like(d["q"], float("nan"))
+        poison = torch.empty_like(d["q"])
+        a_nan = _args(gcs_lib, dc, d, q=q_nan)
+        assert L.attn_decode_paged_noalloc(ctypes.byref(a_nan), poison.data_ptr(), stream) == 0
+        torch.cuda.synchronize()
+        assert torch.isnan(poison.float()).any()
+        expect = oracle_decode(dc)
         for _ in range(2):
             out = torch.full_like(d["q"], float("nan"))
             assert L.attn_decode_paged_noalloc(ctypes.byref(a), out.data_ptr(), stream) == 0
             torch.cuda.synchronize()
             assert gcs_lib.get_device_status() == 0
-            assert torch.isfinite(out.float()).all()
-            assert oracle.rel_rms(f64(out), f64(ref)) <= DECODE_RTOL
+            assert torch.equal(out, ref)
+            assert oracle.rel_rms(f64(out), expect) <= DECODE_RTOL
 
 
 def test_noalloc_rejects_partials_larger_than_its_scratch(gcs_lib):
