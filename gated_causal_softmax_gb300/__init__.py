@@ -50,6 +50,13 @@ STATUS = {
 }
 
 _c_int, _c_float, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_void_p
+_i64 = ctypes.c_int64
+
+
+class Strides(ctypes.Structure):
+    """gcs_strides: element strides (token, head) of a [tokens, heads, dim] tensor; (0, 0) =
+    contiguous."""
+    _fields_ = [("token", _i64), ("head", _i64)]
 
 
 class PrefillArgs(ctypes.Structure):
@@ -70,6 +77,14 @@ class PrefillArgs(ctypes.Structure):
         ("log_gate", _vp),
         ("sink", _vp),
         ("deterministic", _c_int),
+        ("q_stride", Strides),
+        ("k_stride", Strides),
+        ("v_stride", Strides),
+        ("o_stride", Strides),
+        ("do_stride", Strides),
+        ("dq_stride", Strides),
+        ("dk_stride", Strides),
+        ("dv_stride", Strides),
     ]
 
 
@@ -100,6 +115,11 @@ class DecodeArgs(ctypes.Structure):
         ("g_cache", _vp),
         ("sink", _vp),
         ("window", _c_int),
+        ("q_stride", Strides),
+        ("out_stride", Strides),
+        ("kv_stride_block", _i64),
+        ("kv_stride_head", _i64),
+        ("kv_stride_slot", _i64),
     ]
 
 
@@ -194,16 +214,30 @@ def _stream() -> int:
     return torch.cuda.current_stream().cuda_stream
 
 
-def _need(t: torch.Tensor, dtype, name: str) -> torch.Tensor:
+def _need(t: torch.Tensor, dtype, name: str, strided: bool = False) -> torch.Tensor:
+    """Checks device, dtype and layout: contiguous, or (strided=True) any layout whose last
+    dimension is contiguous (the library validates the other strides)."""
     if t is None:
         raise ValueError(f"{name} is required")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
     if t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
-    if not t.is_contiguous():
+    if strided:
+        if t.stride(-1) != 1:
+            raise ValueError(f"{name} must have a contiguous last dimension")
+    elif not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     return t
+
+
+def _st(t: Optional[torch.Tensor]) -> Strides:
+    """Token and head strides of a [tokens, heads, dim] tensor."""
+    if t is None:
+        return Strides(0, 0)
+    if t.dim() != 3:
+        raise ValueError("expected a [tokens, heads, dim] tensor")
+    return Strides(t.stride(0), t.stride(1))
 
 
 def set_kernel_events(before: Optional[torch.cuda.Event], after: Optional[torch.cuda.Event]) -> None:
@@ -257,9 +291,9 @@ def check_paged_inputs(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_l
 
 
 def prefill_args(q, k, v, cu_seqlens, max_seqlen, scale, window, log_gate, sink) -> PrefillArgs:
-    _need(q, torch.bfloat16, "q")
-    _need(k, torch.bfloat16, "k")
-    _need(v, torch.bfloat16, "v")
+    _need(q, torch.bfloat16, "q", strided=True)
+    _need(k, torch.bfloat16, "k", strided=True)
+    _need(v, torch.bfloat16, "v", strided=True)
     _need(cu_seqlens, torch.int32, "cu_seqlens")
     if log_gate is not None:
         _need(log_gate, torch.float32, "log_gate")
@@ -287,6 +321,9 @@ def prefill_args(q, k, v, cu_seqlens, max_seqlen, scale, window, log_gate, sink)
         v=v.data_ptr(),
         log_gate=_ptr(log_gate),
         sink=_ptr(sink),
+        q_stride=_st(q),
+        k_stride=_st(k),
+        v_stride=_st(v),
     )
 
 
@@ -300,6 +337,8 @@ def attn_fwd(q, k, v, cu_seqlens, max_seqlen=None, scale=None, window=0, log_gat
     tot, hq, _ = q.shape
     if out is None:
         out = torch.empty((tot, hq, v.shape[2]), dtype=torch.bfloat16, device=q.device)
+    _need(out, torch.bfloat16, "out", strided=True)
+    a.o_stride = _st(out)
     if lse is None:
         lse = torch.empty((hq, tot), dtype=torch.float32, device=q.device)
     ws_bytes = L.attn_fwd_workspace(ctypes.byref(a))
@@ -319,12 +358,15 @@ def attn_bwd(q, k, v, o, lse, dout, cu_seqlens, max_seqlen=None, scale=None, win
     L = load()
     a = prefill_args(q, k, v, cu_seqlens, max_seqlen, scale, window, log_gate, sink)
     a.deterministic = 1 if deterministic else 0
-    _need(o, torch.bfloat16, "o")
-    _need(dout, torch.bfloat16, "dout")
+    _need(o, torch.bfloat16, "o", strided=True)
+    _need(dout, torch.bfloat16, "dout", strided=True)
     _need(lse, torch.float32, "lse")
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
+    new = lambda t: torch.empty(t.shape, dtype=t.dtype, device=t.device)
+    dq = new(q) if dq is None else _need(dq, torch.bfloat16, "dq", strided=True)
+    dk = new(k) if dk is None else _need(dk, torch.bfloat16, "dk", strided=True)
+    dv = new(v) if dv is None else _need(dv, torch.bfloat16, "dv", strided=True)
+    a.o_stride, a.do_stride = _st(o), _st(dout)
+    a.dq_stride, a.dk_stride, a.dv_stride = _st(dq), _st(dk), _st(dv)
     if log_gate is not None and dlog_gate is None:
         dlog_gate = torch.empty_like(log_gate)
     if sink is not None and dsink is None:
@@ -343,8 +385,12 @@ def decode_args(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu
     """Marshals the decode arguments.  The cache format follows the cache dtype (fp8 e4m3 as
     uint8 or float8_e4m3fn, or bf16); fp8 scales are per token when they have the page shape
     [num_blocks, num_kv_heads, block_size] and per tensor when they hold one value; a bf16
-    cache takes no scales.  Any other scale shape raises NotImplementedError."""
-    _need(q, torch.bfloat16, "q")
+    cache takes no scales.  Any other scale shape raises NotImplementedError.
+
+    q may be strided (last dim contiguous).  The caches are [num_blocks, num_kv_heads,
+    block_size, d] views with any strides the library accepts, shared by K and V: a
+    [num_blocks, block_size, num_kv_heads, d] cache is passed as cache.permute(0, 2, 1, 3)."""
+    _need(q, torch.bfloat16, "q", strided=True)
     if k_cache.dtype == torch.float8_e4m3fn:
         k_cache = k_cache.view(torch.uint8)
     if v_cache.dtype == torch.float8_e4m3fn:
@@ -354,15 +400,18 @@ def decode_args(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu
     _need(cu_q, torch.int32, "cu_q")
     if tuple(v_cache.shape) != tuple(k_cache.shape):
         raise ValueError("k_cache and v_cache shapes differ")
+    if k_cache.stride() != v_cache.stride():
+        raise ValueError("k_cache and v_cache must share one layout")
     nb, hkv, bs, d = k_cache.shape
     if k_cache.dtype == torch.bfloat16:
-        _need(v_cache, torch.bfloat16, "v_cache")
+        _need(k_cache, torch.bfloat16, "k_cache", strided=True)
+        _need(v_cache, torch.bfloat16, "v_cache", strided=True)
         if k_scale is not None or v_scale is not None:
             raise ValueError("a bf16 KV cache takes no scales")
         kv_format, scale_mode, ks_ptr, vs_ptr = KV_BF16, SCALE_PER_TOKEN, None, None
     else:
-        _need(k_cache, torch.uint8, "k_cache")
-        _need(v_cache, torch.uint8, "v_cache")
+        _need(k_cache, torch.uint8, "k_cache", strided=True)
+        _need(v_cache, torch.uint8, "v_cache", strided=True)
         _need(k_scale, torch.float32, "k_scale")
         _need(v_scale, torch.float32, "v_scale")
         if tuple(k_scale.shape) == (nb, hkv, bs) and tuple(v_scale.shape) == (nb, hkv, bs):
@@ -407,6 +456,10 @@ def decode_args(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu
         g_cache=None if g_cache is None else g_cache.data_ptr(),
         sink=None if sink is None else sink.data_ptr(),
         window=int(window),
+        q_stride=_st(q),
+        kv_stride_block=k_cache.stride(0),
+        kv_stride_head=k_cache.stride(1),
+        kv_stride_slot=k_cache.stride(2),
     )
 
 
@@ -421,7 +474,8 @@ def attn_decode_paged(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_le
     a = decode_args(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu_q, max_q_len, max_seq_len,
                     scale, segment_len, g_cache, sink, window)
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+    a.out_stride = _st(_need(out, torch.bfloat16, "out", strided=True))
     ws_bytes = L.attn_decode_workspace(ctypes.byref(a))
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
@@ -440,7 +494,8 @@ def attn_prefill_paged(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_l
     a = decode_args(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu_q, max_q_len, max_seq_len,
                     scale, segment_len, g_cache, sink, window)
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+    a.out_stride = _st(_need(out, torch.bfloat16, "out", strided=True))
     ws_bytes = L.attn_prefill_paged_workspace(ctypes.byref(a))
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
@@ -458,7 +513,8 @@ def attn_decode_paged_noalloc(q, k_cache, v_cache, k_scale, v_scale, block_table
     a = decode_args(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, cu_q, max_q_len, max_seq_len,
                     scale, segment_len, g_cache, sink, window)
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+    a.out_stride = _st(_need(out, torch.bfloat16, "out", strided=True))
     _check(L.attn_decode_paged_noalloc(ctypes.byref(a), out.data_ptr(), _stream()), "attn_decode_paged_noalloc")
     return out
 

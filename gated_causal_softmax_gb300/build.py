@@ -15,7 +15,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libgcs_attn.so")
 SOURCES = ["api.cu", "prefill_fwd.cu", "prefill_fwd2.cu", "prefill_bwd.cu", "prefill_bwd_dq.cu", "prefill_bwd_wide.cu",
            "prefill_aux.cu", "decode.cu", "prefill_paged.cu", "prefill_bwd_wide_dq.cu",
-           "selftest.cu", "checks.cu"]
+           "selftest.cu", "checks.cu", "prefill_bwd_fused.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include")]
 

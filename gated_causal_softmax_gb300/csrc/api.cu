@@ -58,29 +58,43 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return g_encode;
 }
 
-// 2-D bf16 view [rows, width] with a 64 x box_rows box and 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, uint64_t width, uint64_t rows, uint32_t box_rows) {
+// Element strides (token, head) of a [tokens, heads, dim] tensor with dim contiguous.
+struct Layout {
+  long long ts, hs;
+};
+
+// 3-D bf16 map {dim, heads, tokens} with a 64 x 1 x box_rows box and 128-byte swizzle: one
+// box is 64 columns of one head for box_rows tokens, the same shared-memory tile as a 2-D box.
+bool make_map(CUtensorMap* m, const void* base, int dim, int heads, int tokens, const Layout& l, uint32_t box_rows) {
   auto enc = encode_fn();
   if (!enc) return false;
-  cuuint64_t dims[2] = {width, rows};
-  cuuint64_t strides[1] = {width * 2};
-  cuuint32_t box[2] = {64, box_rows};
-  cuuint32_t es[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+  cuuint64_t dims[3] = {(cuuint64_t)dim, (cuuint64_t)heads, (cuuint64_t)tokens};
+  cuuint64_t strides[2] = {(cuuint64_t)l.hs * 2, (cuuint64_t)l.ts * 2};
+  cuuint32_t box[3] = {64, 1, box_rows};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D byte view [rows, 128] of a paged fp8 cache, one page (16 rows x 128 B) per box, 128-byte
-// swizzle.
-bool make_page_map_u8(CUtensorMap* m, const void* base, uint64_t rows) {
+// Byte strides (block, kv head, slot) of a paged cache.
+struct CacheLayout {
+  long long bs, hs, ss;
+  bool head_inner() const { return hs < ss; }
+};
+
+// 4-D byte map of a paged fp8 cache, dims in increasing stride order: {128 B, slot, kv head,
+// block}, or {128 B, kv head, slot, block} when the kv head is the inner one.  One box is one
+// page of one kv head (16 slots x 128 B, 128-byte swizzle), the same tile either way.
+bool make_page_map_u8(CUtensorMap* m, const void* base, int num_blocks, int hkv, const CacheLayout& l) {
   auto enc = encode_fn();
   if (!enc) return false;
-  cuuint64_t dims[2] = {128, rows};
-  cuuint64_t strides[1] = {128};
-  cuuint32_t box[2] = {128, 16};
-  cuuint32_t es[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+  const bool hi = l.head_inner();
+  cuuint64_t dims[4] = {128, (cuuint64_t)(hi ? hkv : 16), (cuuint64_t)(hi ? 16 : hkv), (cuuint64_t)num_blocks};
+  cuuint64_t strides[3] = {(cuuint64_t)(hi ? l.hs : l.ss), (cuuint64_t)(hi ? l.ss : l.hs), (cuuint64_t)l.bs};
+  cuuint32_t box[4] = {128, hi ? 1u : 16u, hi ? 16u : 1u, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -97,12 +111,36 @@ Span span(const void* p, size_t bytes) {
   const uintptr_t a = reinterpret_cast<uintptr_t>(p);
   return Span{a, p ? a + bytes : a};
 }
-bool overlap(const Span& x, const Span& y) { return x.a < x.b && y.a < y.b && x.a < y.b && y.a < x.b; }
+// A strided token-major tensor: byte range plus the period (token stride in bytes) and the
+// bytes one token covers; period 0 = one dense range.
+struct TSpan {
+  uintptr_t a, b;
+  unsigned long long period, width;
+};
+TSpan tspan(const void* p, int tokens, int heads, int dim, const Layout& l, int elt) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  if (!p || tokens <= 0) return TSpan{a, a, 0, 0};
+  const unsigned long long w = ((unsigned long long)(heads - 1) * l.hs + dim) * elt;
+  return TSpan{a, a + (unsigned long long)(tokens - 1) * l.ts * elt + w, (unsigned long long)l.ts * elt, w};
+}
+TSpan tspan(const Span& s) { return TSpan{s.a, s.b, 0, 0}; }
+// True when two byte sets meet.  Two tensors with the same token period whose per-token ranges
+// sit side by side within every period (heads of one fused buffer) do not.
+bool overlap(const TSpan& x, const TSpan& y) {
+  if (!(x.a < x.b && y.a < y.b && x.a < y.b && y.a < x.b)) return false;
+  if (x.period != 0 && x.period == y.period && x.width <= x.period && y.width <= y.period) {
+    const unsigned long long P = x.period;
+    const unsigned long long d = (unsigned long long)((y.a >= x.a ? y.a - x.a : P - (x.a - y.a) % P) % P);
+    return !(d >= x.width && d + y.width <= P);
+  }
+  return true;
+}
+bool overlap(const Span& x, const Span& y) { return overlap(tspan(x), tspan(y)); }
 
 // True when an output range overlaps an input range or another output range (kernels read
 // their inputs and write their outputs concurrently, so any overlap is a race).
 template <size_t NO, size_t NI>
-bool outputs_overlap(const Span (&outs)[NO], const Span (&ins)[NI]) {
+bool outputs_overlap(const TSpan (&outs)[NO], const TSpan (&ins)[NI]) {
   for (size_t i = 0; i < NO; ++i) {
     for (size_t j = 0; j < NI; ++j)
       if (overlap(outs[i], ins[j])) return true;
@@ -124,6 +162,36 @@ struct Carver {
   }
 };
 
+// {0, 0} = contiguous; otherwise token-major without overlap, 16-byte granules.
+int resolve_layout(const gcs_strides& st, int heads, int dim, Layout* out) {
+  if (st.token == 0 && st.head == 0) {
+    *out = Layout{(long long)heads * dim, dim};
+    return GCS_OK;
+  }
+  if (st.token < 0 || st.head < 0) return GCS_ERR_INVALID_ARG;
+  if (st.head < dim || st.token < (long long)heads * st.head) return GCS_ERR_UNSUPPORTED;
+  if ((st.head % 8) != 0 || (st.token % 8) != 0) return GCS_ERR_UNSUPPORTED;
+  if (st.token > (1LL << 38)) return GCS_ERR_UNSUPPORTED;  // tensor-copy strides stay below 2^40 bytes
+  *out = Layout{st.token, st.head};
+  return GCS_OK;
+}
+
+struct PrefillLayouts {
+  Layout q, k, v, o, dout, dq, dk, dv;
+};
+
+int prefill_layouts(const gcs_prefill_args* a, PrefillLayouts* l) {
+  int st;
+  if ((st = resolve_layout(a->q_stride, a->hq, a->dqk, &l->q)) != GCS_OK) return st;
+  if ((st = resolve_layout(a->k_stride, a->hkv, a->dqk, &l->k)) != GCS_OK) return st;
+  if ((st = resolve_layout(a->v_stride, a->hkv, a->dv, &l->v)) != GCS_OK) return st;
+  if ((st = resolve_layout(a->o_stride, a->hq, a->dv, &l->o)) != GCS_OK) return st;
+  if ((st = resolve_layout(a->do_stride, a->hq, a->dv, &l->dout)) != GCS_OK) return st;
+  if ((st = resolve_layout(a->dq_stride, a->hq, a->dqk, &l->dq)) != GCS_OK) return st;
+  if ((st = resolve_layout(a->dk_stride, a->hkv, a->dqk, &l->dk)) != GCS_OK) return st;
+  return resolve_layout(a->dv_stride, a->hkv, a->dv, &l->dv);
+}
+
 bool supported_dims(int dqk, int dv) {
   return (dqk == 64 && dv == 64) || (dqk == 128 && dv == 128) || (dqk == 256 && dv == 256) ||
          (dqk == 256 && dv == 512) || (dqk == 512 && dv == 512);
@@ -142,21 +210,24 @@ int check_prefill(const gcs_prefill_args* a) {
   if ((a->log_gate && !aligned16(a->log_gate)) || (a->sink && (reinterpret_cast<uintptr_t>(a->sink) & 3u)))
     return GCS_ERR_INVALID_ARG;
   if (!supported_dims(a->dqk, a->dv)) return GCS_ERR_UNSUPPORTED;
-  // TMA coordinates and element offsets are 32-bit; keep every tensor below 2^31 elements
+  // 32-bit element counts of the contiguous fp32 workspaces and in-kernel indices: keep every
+  // tensor below 2^31 elements
   const double big = 2147483647.0;
   if ((double)a->total_tokens * a->hq * (a->dqk > a->dv ? a->dqk : a->dv) > big) return GCS_ERR_UNSUPPORTED;
-  return GCS_OK;
+  PrefillLayouts l;
+  return prefill_layouts(a, &l);
 }
 
 // Byte ranges of a prefill call's inputs: q, k, v, log_gate, sink, cu_seqlens.
 struct PrefillSpans {
-  Span q, k, v, g, s, cu;
+  TSpan q, k, v, g, s, cu;
 };
-PrefillSpans prefill_spans(const gcs_prefill_args* a) {
+PrefillSpans prefill_spans(const gcs_prefill_args* a, const PrefillLayouts& l) {
   const size_t t = (size_t)a->total_tokens;
-  return PrefillSpans{span(a->q, t * a->hq * a->dqk * 2),     span(a->k, t * a->hkv * a->dqk * 2),
-                      span(a->v, t * a->hkv * a->dv * 2),     span(a->log_gate, t * a->hq * 4),
-                      span(a->sink, (size_t)a->hq * 4),       span(a->cu_seqlens, ((size_t)a->num_seqs + 1) * 4)};
+  const int T = a->total_tokens;
+  return PrefillSpans{tspan(a->q, T, a->hq, a->dqk, l.q, 2),         tspan(a->k, T, a->hkv, a->dqk, l.k, 2),
+                      tspan(a->v, T, a->hkv, a->dv, l.v, 2),         tspan(span(a->log_gate, t * a->hq * 4)),
+                      tspan(span(a->sink, (size_t)a->hq * 4)), tspan(span(a->cu_seqlens, ((size_t)a->num_seqs + 1) * 4))};
 }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? GCS_OK : GCS_ERR_CUDA; }
@@ -181,9 +252,11 @@ size_t fwd_ws(const gcs_prefill_args* a, bool chk) {
   return c.off;
 }
 
-// Head dims <= 128 take the two-pass backward (dQ pass + dK/dV pass, no fp32 dQ buffer);
-// wider heads take the output-column roles with an fp32 dQ accumulator.
-bool two_pass(const gcs_prefill_args* a) { return a->dqk <= 128 && a->dv <= 128; }
+// Head dim 128 without `deterministic` takes the single-pass backward (dQ reduce-added into an
+// fp32 buffer); head dim 64, and 128 with `deterministic`, the two-pass backward (dQ pass +
+// dK/dV pass, no fp32 dQ buffer); wider heads the output-column roles below.
+bool fused(const gcs_prefill_args* a) { return a->dqk == 128 && a->dv == 128 && a->deterministic == 0; }
+bool two_pass(const gcs_prefill_args* a) { return a->dqk <= 128 && a->dv <= 128 && !fused(a); }
 
 // Head dims above 128 take the query-stationary dQ pass when asked for a deterministic result,
 // and where it is also the faster route (Dqk = 512, where the reduce-add role's 64-row steps
@@ -195,7 +268,8 @@ size_t bwd_ws(const gcs_prefill_args* a, bool chk) {
   const size_t ht = (size_t)a->hq * a->total_tokens;
   if (a->log_gate) c.take<float>(ht);                         // G^T
   c.take<float>(ht);                                           // delta
-  if (!two_pass(a) && !wide_two_pass(a)) c.take<float>((size_t)a->total_tokens * a->hq * a->dqk);  // dQ accumulator
+  if (fused(a) || (a->dqk > 128 && !wide_two_pass(a)))
+    c.take<float>((size_t)a->total_tokens * a->hq * a->dqk);  // dQ accumulator
   if (a->log_gate || a->sink) c.take<float>(ht);               // row sums of dS
   if (a->log_gate) c.take<float>(ht);                          // column sums of dS
   c.take<float>((size_t)a->hq * ((a->total_tokens + 63) / 64 + a->num_seqs) * 128);  // packed vectors
@@ -240,11 +314,13 @@ int attn_fwd(const gcs_prefill_args* a, void* o, float* lse, void* workspace, si
   int st = check_prefill(a);
   if (st != GCS_OK) return st;
   if (!o || !lse || !aligned16(o) || !aligned16(lse)) return GCS_ERR_INVALID_ARG;
+  PrefillLayouts lay;
+  prefill_layouts(a, &lay);
   {
     const size_t t = (size_t)a->total_tokens;
-    const PrefillSpans in = prefill_spans(a);
-    const Span outs[] = {span(o, t * a->hq * a->dv * 2), span(lse, t * a->hq * 4)};
-    const Span ins[] = {in.q, in.k, in.v, in.g, in.s, in.cu};
+    const PrefillSpans in = prefill_spans(a, lay);
+    const TSpan outs[] = {tspan(o, a->total_tokens, a->hq, a->dv, lay.o, 2), tspan(span(lse, t * a->hq * 4))};
+    const TSpan ins[] = {in.q, in.k, in.v, in.g, in.s, in.cu};
     if (outputs_overlap(outs, ins)) return GCS_ERR_INVALID_ARG;
   }
   const bool chk = device_checks_on();
@@ -260,9 +336,9 @@ int attn_fwd(const gcs_prefill_args* a, void* o, float* lse, void* workspace, si
   int32_t* cu_chk = chk ? c.take<int32_t>((size_t)a->num_seqs + 1) : nullptr;
 
   FwdMaps maps;
-  if (!make_map(&maps.q, a->q, (uint64_t)a->hq * a->dqk, a->total_tokens, 128) ||
-      !make_map(&maps.k, a->k, (uint64_t)a->hkv * a->dqk, a->total_tokens, 128) ||
-      !make_map(&maps.v, a->v, (uint64_t)a->hkv * a->dv, a->total_tokens, 128))
+  if (!make_map(&maps.q, a->q, a->dqk, a->hq, a->total_tokens, lay.q, 128) ||
+      !make_map(&maps.k, a->k, a->dqk, a->hkv, a->total_tokens, lay.k, 128) ||
+      !make_map(&maps.v, a->v, a->dv, a->hkv, a->total_tokens, lay.v, 128))
     return GCS_ERR_CUDA;
 
   // the kernels read the checked copy of cu_seqlens when device checks are on
@@ -290,6 +366,8 @@ int attn_fwd(const gcs_prefill_args* a, void* o, float* lse, void* workspace, si
   p.gT = gT;
   p.sink = a->sink;
   p.o = static_cast<uint16_t*>(o);
+  p.o_ts = lay.o.ts;
+  p.o_hs = lay.o.hs;
   p.lse = lse;
   p.status = status;
   KernelTimer timer(s);
@@ -314,14 +392,17 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
     return GCS_ERR_INVALID_ARG;
   if ((dlog_gate == nullptr) != (a->log_gate == nullptr)) return GCS_ERR_INVALID_ARG;
   if ((dsink == nullptr) != (a->sink == nullptr)) return GCS_ERR_INVALID_ARG;
+  PrefillLayouts lay;
+  prefill_layouts(a, &lay);
   {
     const size_t t = (size_t)a->total_tokens;
-    const PrefillSpans in = prefill_spans(a);
-    const Span outs[] = {span(dq, t * a->hq * a->dqk * 2), span(dk, t * a->hkv * a->dqk * 2),
-                         span(dv, t * a->hkv * a->dv * 2), span(dlog_gate, t * a->hq * 4),
-                         span(dsink, (size_t)a->hq * 4)};
-    const Span ins[] = {in.q,  in.k, in.v, in.g, in.s, in.cu, span(o, t * a->hq * a->dv * 2), span(lse, t * a->hq * 4),
-                        span(dout, t * a->hq * a->dv * 2)};
+    const int T = a->total_tokens;
+    const PrefillSpans in = prefill_spans(a, lay);
+    const TSpan outs[] = {tspan(dq, T, a->hq, a->dqk, lay.dq, 2), tspan(dk, T, a->hkv, a->dqk, lay.dk, 2),
+                          tspan(dv, T, a->hkv, a->dv, lay.dv, 2), tspan(span(dlog_gate, t * a->hq * 4)),
+                          tspan(span(dsink, (size_t)a->hq * 4))};
+    const TSpan ins[] = {in.q, in.k, in.v, in.g, in.s, in.cu, tspan(o, T, a->hq, a->dv, lay.o, 2),
+                         tspan(span(lse, t * a->hq * 4)), tspan(dout, T, a->hq, a->dv, lay.dout, 2)};
     if (outputs_overlap(outs, ins)) return GCS_ERR_INVALID_ARG;
   }
   const bool chk = device_checks_on();
@@ -336,9 +417,10 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
   Carver c{static_cast<uint8_t*>(workspace)};
   float* gT = a->log_gate ? c.take<float>(ht) : nullptr;
   float* delta = c.take<float>(ht);
+  const bool fu = fused(a);
   const bool tp = two_pass(a);
-  const bool wide_det = !tp && wide_two_pass(a);
-  // fp32 dQ accumulator: wide heads on the reduce-add route only
+  const bool wide_det = !tp && !fu && wide_two_pass(a);
+  // fp32 dQ accumulator: the single-pass route and wide heads on the reduce-add route
   float* dq_acc = (tp || wide_det) ? nullptr : c.take<float>((size_t)a->total_tokens * a->hq * a->dqk);
   float* dg_row = (a->log_gate || a->sink) ? c.take<float>(ht) : nullptr;
   float* dg_col = a->log_gate ? c.take<float>(ht) : nullptr;
@@ -347,12 +429,13 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
   int32_t* cu_chk = chk ? c.take<int32_t>((size_t)a->num_seqs + 1) : nullptr;
 
   BwdMaps maps;
-  if (!make_map(&maps.q, a->q, (uint64_t)a->hq * a->dqk, a->total_tokens, 64) ||
-      !make_map(&maps.k, a->k, (uint64_t)a->hkv * a->dqk, a->total_tokens, 128) ||
-      !make_map(&maps.v, a->v, (uint64_t)a->hkv * a->dv, a->total_tokens, 128) ||
-      !make_map(&maps.dout, dout, (uint64_t)a->hq * a->dv, a->total_tokens, 64) ||
-      !make_map(&maps.q128, a->q, (uint64_t)a->hq * a->dqk, a->total_tokens, 128) ||
-      !make_map(&maps.dout128, dout, (uint64_t)a->hq * a->dv, a->total_tokens, 128))
+  const int T = a->total_tokens;
+  if (!make_map(&maps.q, a->q, a->dqk, a->hq, T, lay.q, 64) ||
+      !make_map(&maps.k, a->k, a->dqk, a->hkv, T, lay.k, 128) ||
+      !make_map(&maps.v, a->v, a->dv, a->hkv, T, lay.v, 128) ||
+      !make_map(&maps.dout, dout, a->dv, a->hq, T, lay.dout, 64) ||
+      !make_map(&maps.q128, a->q, a->dqk, a->hq, T, lay.q, 128) ||
+      !make_map(&maps.dout128, dout, a->dv, a->hq, T, lay.dout, 128))
     return GCS_ERR_CUDA;
 
   const int32_t* cu = a->cu_seqlens;
@@ -366,7 +449,8 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
     if (st != GCS_OK) return st;
   }
   st = cuda_status(launch_bwd_pre(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout),
-                                  a->total_tokens, a->hq, a->dv, a->dqk, delta, dq_acc, dg_row, dg_col, s));
+                                  a->total_tokens, a->hq, a->dv, a->dqk, lay.o.ts, lay.o.hs, lay.dout.ts,
+                                  lay.dout.hs, delta, dq_acc, dg_row, dg_col, s));
   if (st != GCS_OK) return st;
 
   st = cuda_status(launch_bwd_pack(cu, a->num_seqs, a->total_tokens, a->hq, n_qtiles, lse, gT, delta,
@@ -390,6 +474,12 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
   p.grad_q = static_cast<uint16_t*>(dq);
   p.grad_k = static_cast<uint16_t*>(dk);
   p.grad_v = static_cast<uint16_t*>(dv);
+  p.dq_ts = lay.dq.ts;
+  p.dq_hs = lay.dq.hs;
+  p.dk_ts = lay.dk.ts;
+  p.dk_hs = lay.dk.hs;
+  p.dv_ts = lay.dv.ts;
+  p.dv_hs = lay.dv.hs;
   p.dq_acc = dq_acc;
   p.dg_row = dg_row;
   p.dg_col = dg_col;
@@ -398,7 +488,11 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
   p.status = status;
   const int num_tiles = (a->total_tokens + 127) / 128 + a->num_seqs;
   KernelTimer timer(s);
-  if (tp) {
+  if (fu) {
+    timer.before();
+    st = cuda_status(launch_prefill_bwd_fused(p, maps, num_tiles, s));
+    timer.after();
+  } else if (tp) {
     // dQ pass (query tiles of 128 rows), then the dK/dV pass; the timer brackets both
     BwdMaps dqmaps = maps;
     dqmaps.q = maps.q128;
@@ -422,8 +516,28 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
   }
   if (st != GCS_OK) return st;
   return cuda_status(launch_bwd_post(dq_acc, static_cast<uint16_t*>(dq), a->total_tokens, a->hq, a->dqk,
-                                     cu, a->num_seqs, dg_row, dg_col, dlog_gate, lse, delta, a->sink,
-                                     dsink, s));
+                                     lay.dq.ts, lay.dq.hs, cu, a->num_seqs, dg_row, dg_col, dlog_gate, lse,
+                                     delta, a->sink, dsink, s));
+}
+
+// Byte strides of the paged caches; all-zero element strides = contiguous
+// [num_blocks, hkv, block_size, d].
+static int cache_layout(const gcs_decode_args* a, CacheLayout* l) {
+  const long long elt = a->kv_format == GCS_KV_BF16 ? 2 : 1;
+  const long long row = (long long)a->d * elt;
+  if (a->kv_stride_block == 0 && a->kv_stride_head == 0 && a->kv_stride_slot == 0) {
+    *l = CacheLayout{(long long)a->hkv * a->block_size * row, (long long)a->block_size * row, row};
+    return GCS_OK;
+  }
+  if (a->kv_stride_block < 0 || a->kv_stride_head < 0 || a->kv_stride_slot < 0) return GCS_ERR_INVALID_ARG;
+  const long long b = a->kv_stride_block * elt, h = a->kv_stride_head * elt, sl = a->kv_stride_slot * elt;
+  if ((b % 16) || (h % 16) || (sl % 16) || b >= (1LL << 40)) return GCS_ERR_UNSUPPORTED;
+  const bool slot_inner = sl >= row && h >= (long long)a->block_size * sl;
+  const bool head_inner = h >= row && sl >= (long long)a->hkv * h;
+  if (!slot_inner && !head_inner) return GCS_ERR_UNSUPPORTED;
+  if (b < (long long)(a->hkv - 1) * h + (long long)(a->block_size - 1) * sl + row) return GCS_ERR_UNSUPPORTED;
+  *l = CacheLayout{b, h, sl};
+  return GCS_OK;
 }
 
 static int check_decode(const gcs_decode_args* a) {
@@ -460,10 +574,12 @@ static int check_decode(const gcs_decode_args* a) {
   if (a->g_cache && !aligned16(a->g_cache)) return GCS_ERR_INVALID_ARG;
   if (a->sink && (reinterpret_cast<uintptr_t>(a->sink) & 3u)) return GCS_ERR_INVALID_ARG;
   if ((double)a->num_blocks * a->hkv * a->block_size * a->d > 9.0e15) return GCS_ERR_UNSUPPORTED;
-  // the fp8 pages are fetched by tensor copies whose row coordinate is a 32-bit integer
-  if (a->kv_format == GCS_KV_FP8_E4M3 && (double)a->num_blocks * a->hkv * a->block_size > 2147483647.0)
-    return GCS_ERR_UNSUPPORTED;
-  return GCS_OK;
+  CacheLayout cl;
+  int st = cache_layout(a, &cl);
+  if (st != GCS_OK) return st;
+  Layout lq, lo;
+  if ((st = resolve_layout(a->q_stride, a->hq, a->d, &lq)) != GCS_OK) return st;
+  return resolve_layout(a->out_stride, a->hq, a->d, &lo);
 }
 
 // True when the output of a paged call overlaps one of its inputs.
@@ -471,17 +587,24 @@ static bool paged_out_overlaps(const gcs_decode_args* a, const void* out) {
   const size_t rows = (size_t)a->num_blocks * a->hkv * a->block_size;
   const size_t elt = a->kv_format == GCS_KV_BF16 ? 2 : 1;
   const size_t sc = a->scale_mode == GCS_SCALE_PER_TENSOR ? 4 : rows * 4;
-  const Span outs[] = {span(out, (size_t)a->total_q * a->hq * a->d * 2)};
-  const Span ins[] = {span(a->q, (size_t)a->total_q * a->hq * a->d * 2),
-                      span(a->k_cache, rows * a->d * elt),
-                      span(a->v_cache, rows * a->d * elt),
-                      span(a->k_scale, sc),
-                      span(a->v_scale, sc),
-                      span(a->block_table, (size_t)a->num_reqs * a->max_blocks_per_req * 4),
-                      span(a->seq_lens, (size_t)a->num_reqs * 4),
-                      span(a->cu_q, ((size_t)a->num_reqs + 1) * 4),
-                      span(a->g_cache, (size_t)a->num_blocks * a->hq * a->block_size * 4),
-                      span(a->sink, (size_t)a->hq * 4)};
+  CacheLayout cl;
+  Layout lq, lo;
+  cache_layout(a, &cl);
+  resolve_layout(a->q_stride, a->hq, a->d, &lq);
+  resolve_layout(a->out_stride, a->hq, a->d, &lo);
+  const size_t cache_bytes = (size_t)(a->num_blocks - 1) * cl.bs + (size_t)(a->hkv - 1) * cl.hs +
+                             (size_t)(a->block_size - 1) * cl.ss + (size_t)a->d * elt;
+  const TSpan outs[] = {tspan(out, a->total_q, a->hq, a->d, lo, 2)};
+  const TSpan ins[] = {tspan(a->q, a->total_q, a->hq, a->d, lq, 2),
+                       tspan(span(a->k_cache, cache_bytes)),
+                       tspan(span(a->v_cache, cache_bytes)),
+                       tspan(span(a->k_scale, sc)),
+                       tspan(span(a->v_scale, sc)),
+                       tspan(span(a->block_table, (size_t)a->num_reqs * a->max_blocks_per_req * 4)),
+                       tspan(span(a->seq_lens, (size_t)a->num_reqs * 4)),
+                       tspan(span(a->cu_q, ((size_t)a->num_reqs + 1) * 4)),
+                       tspan(span(a->g_cache, (size_t)a->num_blocks * a->hq * a->block_size * 4)),
+                       tspan(span(a->sink, (size_t)a->hq * 4))};
   return outputs_overlap(outs, ins);
 }
 
@@ -509,6 +632,19 @@ static void fill_paged_params(const gcs_decode_args* a, void* out, int* status, 
   p.scale = a->scale;
   p.q = static_cast<const uint16_t*>(a->q);
   p.out = static_cast<uint16_t*>(out);
+  CacheLayout cl;
+  Layout lq, lo;
+  cache_layout(a, &cl);
+  resolve_layout(a->q_stride, a->hq, a->d, &lq);
+  resolve_layout(a->out_stride, a->hq, a->d, &lo);
+  p.q_ts = lq.ts;
+  p.q_hs = lq.hs;
+  p.out_ts = lo.ts;
+  p.out_hs = lo.hs;
+  p.kv_bs = cl.bs;
+  p.kv_hs = cl.hs;
+  p.kv_ss = cl.ss;
+  p.kv_head_inner = cl.head_inner() ? 1 : 0;
   p.part_acc = nullptr;
   p.part_ml = nullptr;
   p.status = status;
@@ -534,11 +670,27 @@ static size_t decode_ws(const gcs_decode_args* a, bool chk, int* max_segs_out) {
 
 // Runs the device-content checks of a paged call when they are on: p.cu_q then points to the
 // checked copy at byte offset `off` of the workspace.
+static PagedOperandCheck operand_check(const gcs_decode_args* a) {
+  PagedOperandCheck c{};
+  if (a->kv_format != GCS_KV_FP8_E4M3) return c;  // hkv 0: nothing to check
+  Layout lq;
+  resolve_layout(a->q_stride, a->hq, a->d, &lq);
+  c.q = static_cast<const uint16_t*>(a->q);
+  c.q_ts = lq.ts;
+  c.q_hs = lq.hs;
+  c.hq = a->hq;
+  c.d = a->d;
+  c.hkv = a->hkv;
+  c.v_scale = a->v_scale;
+  c.per_tensor = a->scale_mode == GCS_SCALE_PER_TENSOR ? 1 : 0;
+  return c;
+}
+
 static int paged_checks(const gcs_decode_args* a, void* workspace, size_t off, DecodeParams& p, cudaStream_t s) {
   int32_t* cu_chk = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + off);
   const int st = cuda_status(launch_check_paged(a->cu_q, a->seq_lens, a->block_table, a->num_reqs, a->total_q,
                                                 a->max_q_len, a->max_seq_len, a->max_blocks_per_req, a->num_blocks,
-                                                a->block_size, a->window, cu_chk, p.status, s));
+                                                a->block_size, a->window, operand_check(a), cu_chk, p.status, s));
   if (st == GCS_OK) p.cu_q = cu_chk;
   return st;
 }
@@ -571,8 +723,10 @@ int attn_decode_paged(const gcs_decode_args* a, void* out, void* workspace, size
   DecodeMaps maps;
   std::memset(&maps, 0, sizeof(maps));
   if (a->kv_format == GCS_KV_FP8_E4M3) {
-    const uint64_t cache_rows = (uint64_t)a->num_blocks * a->hkv * a->block_size;
-    if (!make_page_map_u8(&maps.k, a->k_cache, cache_rows) || !make_page_map_u8(&maps.v, a->v_cache, cache_rows))
+    CacheLayout cl;
+    cache_layout(a, &cl);
+    if (!make_page_map_u8(&maps.k, a->k_cache, a->num_blocks, a->hkv, cl) ||
+        !make_page_map_u8(&maps.v, a->v_cache, a->num_blocks, a->hkv, cl))
       return GCS_ERR_CUDA;
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -672,8 +826,10 @@ int attn_prefill_paged(const gcs_decode_args* a, void* out, void* workspace, siz
         reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + round_up(units * rows * 128 * sizeof(float)));
   }
   DecodeMaps maps;
-  const uint64_t cache_rows = (uint64_t)a->num_blocks * a->hkv * a->block_size;
-  if (!make_page_map_u8(&maps.k, a->k_cache, cache_rows) || !make_page_map_u8(&maps.v, a->v_cache, cache_rows))
+  CacheLayout cl;
+  cache_layout(a, &cl);
+  if (!make_page_map_u8(&maps.k, a->k_cache, a->num_blocks, a->hkv, cl) ||
+      !make_page_map_u8(&maps.v, a->v_cache, a->num_blocks, a->hkv, cl))
     return GCS_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (chk) {
@@ -711,7 +867,8 @@ int gcs_check_paged_inputs(const gcs_decode_args* a, gcs_stream_t stream) {
   if (!status) return GCS_ERR_CUDA;
   return cuda_status(launch_check_paged(a->cu_q, a->seq_lens, a->block_table, a->num_reqs, a->total_q, a->max_q_len,
                                         a->max_seq_len, a->max_blocks_per_req, a->num_blocks, a->block_size,
-                                        a->window, nullptr, status, reinterpret_cast<cudaStream_t>(stream)));
+                                        a->window, operand_check(a), nullptr, status,
+                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int gcs_set_kernel_events(void* before, void* after) {

@@ -50,15 +50,35 @@ __global__ void __launch_bounds__(kCheckThreads) check_prefill_kernel(const int3
 // that holds the earliest key any of its query rows sees (key 0 without a window) to the
 // page of its last cached token; a request with no query rows reads none.  One warp per
 // request, one lane per page.
+//
+// With an fp8 cache (f16 operands, fp8.hkv > 0) it also checks the operand limits: every |q| at
+// most 65504 (q, strided, is read in 16-byte units) and every V scale of the slots below
+// seq_len in those pages below 255 in magnitude (per tensor: the one scale).
 __global__ void __launch_bounds__(kCheckThreads) check_paged_kernel(
     const int32_t* __restrict__ cu_q, const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ table,
     int num_reqs, int total_q, int max_q_len, int max_seq_len, int max_blocks, int num_blocks, int block_size,
-    int window, int32_t* __restrict__ cu_out, int* status) {
+    int window, PagedOperandCheck fp8, int32_t* __restrict__ cu_out, int* status) {
   __shared__ int bad_s;
   if (threadIdx.x == 0) bad_s = 0;
   __syncthreads();
   bool bad = false;
   if (threadIdx.x == 0) bad = __ldg(cu_q) != 0 || __ldg(cu_q + num_reqs) != total_q;
+  if (fp8.hkv > 0) {
+    // q: total_q x hq rows of d / 8 16-byte units
+    const int units = fp8.d / 8;
+    const long long n = (long long)total_q * fp8.hq * units;
+    for (long long i = threadIdx.x; i < n; i += blockDim.x) {
+      const long long row = i / units, t = row / fp8.hq, h = row % fp8.hq;
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(fp8.q + t * fp8.q_ts + h * fp8.q_hs) + i % units);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        // bf16 magnitude bits above 65504 (0x477fe0), NaN included
+        bad = bad || (w[k] & 0x7fffu) > 0x477fu || (w[k] >> 16 & 0x7fffu) > 0x477fu;
+      }
+    }
+    if (fp8.per_tensor && threadIdx.x == 0) bad = bad || !(fabsf(__ldg(fp8.v_scale)) < 255.f);
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   for (int r = warp; r < num_reqs; r += nwarps) {
     const long long ql = (long long)__ldg(cu_q + r + 1) - __ldg(cu_q + r);
@@ -74,6 +94,12 @@ __global__ void __launch_bounds__(kCheckThreads) check_paged_kernel(
     for (int pg = p0 + lane; pg < np; pg += 32) {
       const int blk = __ldg(table + (size_t)r * max_blocks + pg);
       bad = bad || blk < 0 || blk >= num_blocks;
+      if (fp8.hkv > 0 && !fp8.per_tensor && blk >= 0 && blk < num_blocks) {
+        const int nslot = min(block_size, L - pg * block_size);
+        for (int h = 0; h < fp8.hkv; ++h)
+          for (int sl = 0; sl < nslot; ++sl)
+            bad = bad || !(fabsf(__ldg(fp8.v_scale + ((size_t)blk * fp8.hkv + h) * block_size + sl)) < 255.f);
+      }
     }
   }
   finish_check(bad, &bad_s, cu_q, num_reqs + 1, cu_out, status);
@@ -89,9 +115,10 @@ cudaError_t launch_check_prefill(const int32_t* cu, int num_seqs, int total, int
 
 cudaError_t launch_check_paged(const int32_t* cu_q, const int32_t* seq_lens, const int32_t* table, int num_reqs,
                                int total_q, int max_q_len, int max_seq_len, int max_blocks, int num_blocks,
-                               int block_size, int window, int32_t* cu_out, int* status, cudaStream_t s) {
+                               int block_size, int window, const PagedOperandCheck& fp8, int32_t* cu_out,
+                               int* status, cudaStream_t s) {
   check_paged_kernel<<<1, kCheckThreads, 0, s>>>(cu_q, seq_lens, table, num_reqs, total_q, max_q_len, max_seq_len,
-                                                 max_blocks, num_blocks, block_size, window, cu_out, status);
+                                                 max_blocks, num_blocks, block_size, window, fp8, cu_out, status);
   return cudaGetLastError();
 }
 

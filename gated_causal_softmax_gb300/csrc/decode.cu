@@ -190,15 +190,24 @@ __global__ void __launch_bounds__(kThreads, 3)
         const int blk = __ldg(trow + i);
         const size_t slot0 = ((size_t)blk * p.hkv + kvh) * kPage;
         if (KVF == 0 && kind < 2) {
-          // fp8 K or V page: one 16-row x 128-B box of the cache viewed as [rows, 128 B]
-          tma_load_2d(kv + stage * C::KV + dst_off, kind ? &tmV : &tmK, &full[stage], 0, static_cast<int>(slot0));
+          // fp8 K or V page: one 16-slot x 128-B box of the cache's 4-D map (dims in stride order)
+          tma_load_4d(kv + stage * C::KV + dst_off, kind ? &tmV : &tmK, &full[stage], 0, p.kv_head_inner ? kvh : 0,
+                      p.kv_head_inner ? 0 : kvh, blk);
+        } else if (kind < 2) {
+          // bf16 K or V page: one 4 KB copy when its 16 rows are adjacent, else one per row
+          const uint8_t* src = (kind == 0 ? p.k_cache : p.v_cache) + (size_t)blk * p.kv_bs + (size_t)kvh * p.kv_hs;
+          uint8_t* dst = kv + stage * C::KV + dst_off;
+          if (p.kv_ss == C::KB / kPage) {
+            bulk_load(dst, src, bytes, &full[stage]);
+          } else {
+            for (int rr = 0; rr < kPage; ++rr)
+              bulk_load(dst + rr * (C::KB / kPage), src + rr * p.kv_ss, C::KB / kPage, &full[stage]);
+          }
         } else {
-          const void* src = kind == 0   ? static_cast<const void*>(p.k_cache + slot0 * (C::KB / kPage))
-                            : kind == 1 ? static_cast<const void*>(p.v_cache + slot0 * (C::KB / kPage))
-                            : is_g ? static_cast<const void*>(p.g_cache + ((size_t)blk * p.hq + kvh * kGroup) * kPage)
+          const void* src = is_g ? static_cast<const void*>(p.g_cache + ((size_t)blk * p.hq + kvh * kGroup) * kPage)
                             : kind == 2 ? static_cast<const void*>(p.k_scale + slot0)
                                         : static_cast<const void*>(p.v_scale + slot0);
-          bulk_load((kind < 2 ? kv + stage * C::KV : aux + stage * C::AUX) + dst_off, src, bytes, &full[stage]);
+          bulk_load(aux + stage * C::AUX + dst_off, src, bytes, &full[stage]);
         }
       }
     }
@@ -223,8 +232,8 @@ __global__ void __launch_bounds__(kThreads, 3)
   if (active && grp == 0) {
     uint32_t qa[8][4];
     {
-      const uint16_t* q0p = p.q + ((size_t)(q_begin + mt) * p.hq + kvh * kGroup + g) * kD + 32 * tq;
-      const uint16_t* q1p = q0p + 8 * kD;
+      const uint16_t* q0p = p.q + (size_t)(q_begin + mt) * p.q_ts + (size_t)(kvh * kGroup + g) * p.q_hs + 32 * tq;
+      const uint16_t* q1p = q0p + 8 * p.q_hs;
       uint32_t w0[16], w1[16];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -566,7 +575,8 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
   outv.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
   outv.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
   outv.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-  *reinterpret_cast<uint4*>(p.out + ((size_t)(q_begin + t) * p.hq + kvh * kGroup + hh) * kD + d0) = outv;
+  *reinterpret_cast<uint4*>(p.out + (size_t)(q_begin + t) * p.out_ts + (size_t)(kvh * kGroup + hh) * p.out_hs + d0) =
+      outv;
 }
 
 }  // namespace

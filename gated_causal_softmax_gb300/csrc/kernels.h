@@ -20,13 +20,14 @@ struct FwdParams {
   int window;            // 0 = none
   const float* gT;       // G^T [hq, total] in log2 units (gate cumsum * log2 e), or null
   const float* sink;     // [hq] natural-log sink logits, or null
-  uint16_t* o;           // bf16 [total, hq, dv]
+  uint16_t* o;           // bf16 [total, hq, dv] at token * o_ts + head * o_hs
+  long long o_ts, o_hs;  // element strides of o
   float* lse;            // [hq, total]
   int* status;
 };
 
 struct FwdMaps {
-  CUtensorMap q, k, v;  // 2-D bf16 maps, box 64 x 128, 128-B swizzle
+  CUtensorMap q, k, v;  // 3-D bf16 maps {dim, heads, tokens}, box 64 x 1 x 128, 128-B swizzle
 };
 
 cudaError_t launch_prefill_fwd(const FwdParams& p, const FwdMaps& maps, int num_tiles, cudaStream_t s);
@@ -47,6 +48,7 @@ struct BwdParams {
   uint16_t* grad_q;      // bf16 [total, hq, dqk] (written directly by the dQ pass)
   uint16_t* grad_k;      // bf16 [total, hkv, dqk]
   uint16_t* grad_v;      // bf16 [total, hkv, dv]
+  long long dq_ts, dq_hs, dk_ts, dk_hs, dv_ts, dv_hs;  // element strides (token, head) of the three
   float* dq_acc;         // fp32 [total, hq, dqk] (zeroed; wide heads, reduce-add route only)
   float* dg_row;         // fp32 [hq, total] sum_j dS_ij; null if not needed
   float* dg_col;         // fp32 [hq, total] sum_i dS_ij (zeroed); null if no gate
@@ -56,11 +58,14 @@ struct BwdParams {
 };
 
 struct BwdMaps {
-  CUtensorMap q, k, v, dout;   // 2-D bf16 maps, 128-B swizzle (q, dout: 64-row boxes)
+  CUtensorMap q, k, v, dout;   // 3-D bf16 maps {dim, heads, tokens}, 128-B swizzle (q, dout: 64-row boxes)
   CUtensorMap q128, dout128;   // q, dout with 128-row boxes (dQ pass)
 };
 
 cudaError_t launch_prefill_bwd(const BwdParams& p, const BwdMaps& maps, int num_kv_tiles, cudaStream_t s);
+// Single-pass backward at head dim 128: dK, dV written, dQ and the dS row sums reduce-added
+// into the zeroed fp32 buffers p.dq_acc and p.dg_row (q / dout maps with 128-row boxes).
+cudaError_t launch_prefill_bwd_fused(const BwdParams& p, const BwdMaps& maps, int num_kv_tiles, cudaStream_t s);
 // dQ pass of the two-pass backward (head dims <= 128): writes dQ (bf16) and dS row sums.
 cudaError_t launch_prefill_bwd_dq(const BwdParams& p, const BwdMaps& maps, int num_q_tiles, cudaStream_t s);
 // Head dims above 128, key-stationary output-column roles: dV chunks, and dK chunks that
@@ -74,14 +79,16 @@ cudaError_t launch_prefill_bwd_wide(const BwdParams& p, const BwdMaps& maps, int
 cudaError_t launch_gate_cumsum(const float* g, const int32_t* cu, int num_seqs, int total, int hq, float* gT,
                                cudaStream_t s);
 cudaError_t launch_bwd_pre(const uint16_t* o, const uint16_t* dout, int total, int hq, int dv, int dqk,
-                           float* delta, float* dq_acc, float* dg_row, float* dg_col, cudaStream_t s);
+                           long long o_ts, long long o_hs, long long do_ts, long long do_hs, float* delta,
+                           float* dq_acc, float* dg_row, float* dg_col, cudaStream_t s);
 // Packs (G_i - LSE_i) * log2 e and delta_i per (head, 64-row query tile): vecp
 // [hq][n_qtiles][128] with n_qtiles = ceil(total / 64) + num_seqs.
 cudaError_t launch_bwd_pack(const int32_t* cu, int num_seqs, int total, int hq, int n_qtiles, const float* lse,
                             const float* gT, const float* delta, float* vecp, cudaStream_t s);
-cudaError_t launch_bwd_post(const float* dq_acc, uint16_t* dq, int total, int hq, int dqk, const int32_t* cu,
-                            int num_seqs, const float* dg_row, const float* dg_col, float* dlog_gate,
-                            const float* lse, const float* delta, const float* sink, float* dsink, cudaStream_t s);
+cudaError_t launch_bwd_post(const float* dq_acc, uint16_t* dq, int total, int hq, int dqk, long long dq_ts,
+                            long long dq_hs, const int32_t* cu, int num_seqs, const float* dg_row,
+                            const float* dg_col, float* dlog_gate, const float* lse, const float* delta,
+                            const float* sink, float* dsink, cudaStream_t s);
 
 struct DecodeParams {
   const int32_t* cu_q;
@@ -102,15 +109,18 @@ struct DecodeParams {
   int max_segs;          // segments per request slot in the partial buffers
   int seg_pages;         // pages per segment
   float scale;
-  const uint16_t* q;     // bf16 [total_q, hq, 128]
-  uint16_t* out;         // bf16 [total_q, hq, 128]
+  const uint16_t* q;     // bf16 [total_q, hq, 128] at token * q_ts + head * q_hs
+  uint16_t* out;         // bf16 [total_q, hq, 128] at token * out_ts + head * out_hs
+  long long q_ts, q_hs, out_ts, out_hs;  // element strides
+  long long kv_bs, kv_hs, kv_ss;         // byte strides (block, kv head, slot) of both caches
+  int kv_head_inner;     // 1: the kv head stride is below the slot stride (fp8 maps order dims so)
   float* part_acc;       // [units, 4*16, 128]
   float* part_ml;        // [units, 4*16, 2]
   int* status;
 };
 
-// fp8 K and V caches viewed as 2-D [num_blocks * hkv * 16 rows, 128 B], box 128 B x 16 rows
-// (one page), 128-byte swizzle; unused for a bf16 cache.
+// fp8 K and V caches as 4-D maps {128 B, slot, kv head, block} (slot and kv head swapped when
+// kv_head_inner), box one page of 16 slots x 128 B, 128-byte swizzle; unused for a bf16 cache.
 struct DecodeMaps {
   CUtensorMap k, v;
 };
@@ -136,9 +146,18 @@ cudaError_t launch_bounded_wait_selftest(int* status, cudaStream_t s);
 // cu_seqlens / cu_q, or all zeros (an empty batch) on a failure.
 cudaError_t launch_check_prefill(const int32_t* cu, int num_seqs, int total, int max_seqlen, int32_t* cu_out,
                                  int* status, cudaStream_t s);
+// The f16 operand limits of an fp8 cache (hkv = 0: nothing to check, a bf16 cache).
+struct PagedOperandCheck {
+  const uint16_t* q;      // bf16 [total_q, hq, d] at token * q_ts + head * q_hs
+  long long q_ts, q_hs;
+  int hq, d, hkv;
+  const float* v_scale;   // per token [num_blocks, hkv, block_size] or per tensor [1]
+  int per_tensor;
+};
 cudaError_t launch_check_paged(const int32_t* cu_q, const int32_t* seq_lens, const int32_t* table, int num_reqs,
                                int total_q, int max_q_len, int max_seq_len, int max_blocks, int num_blocks,
-                               int block_size, int window, int32_t* cu_out, int* status, cudaStream_t s);
+                               int block_size, int window, const PagedOperandCheck& fp8, int32_t* cu_out,
+                               int* status, cudaStream_t s);
 
 // Size of the static scratch behind attn_decode_paged_noalloc (64 MiB).
 constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;

@@ -75,14 +75,14 @@ __global__ void __launch_bounds__(kScanThreads) gate_cumsum_kernel(const float* 
 }
 
 // L = min(32, dv / 8) lanes per (token, head) row, 8 elements (16 B of O and of dO) per lane
-// and chunk; rows are handed out grid-stride.
-// L = min(32, dv / 8) lanes per (token, head) row, 8 elements (16 B of O and of dO) per lane
 // and chunk; each warp takes 32 / L consecutive rows at a time, grid-stride.  The loop is
 // uniform across the warp (rows past the end load nothing), so the shuffles see every lane.
+// O and dO rows sit at token * ts + head * hs (element strides; dims contiguous).
 template <int L>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict__ o,
                                                       const uint16_t* __restrict__ dout, int total, int hq, int dv,
-                                                      float* __restrict__ delta) {
+                                                      long long o_ts, long long o_hs, long long do_ts,
+                                                      long long do_hs, float* __restrict__ delta) {
   constexpr int kRowsPerWarp = 32 / L;
   const int lane = threadIdx.x & (L - 1);
   const int group = (threadIdx.x & 31) / L;
@@ -95,8 +95,9 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
     const bool valid = row < rows;
     float acc0 = 0.f, acc1 = 0.f;
     if (valid) {
-      const uint4* po = reinterpret_cast<const uint4*>(o + (size_t)row * dv);
-      const uint4* pd = reinterpret_cast<const uint4*>(dout + (size_t)row * dv);
+      const long long t = row / hq, h = row % hq;
+      const uint4* po = reinterpret_cast<const uint4*>(o + t * o_ts + h * o_hs);
+      const uint4* pd = reinterpret_cast<const uint4*>(dout + t * do_ts + h * do_hs);
       for (int c = 0; c < chunks; ++c) {
         const uint4 a = __ldg(po + c * L + lane), b = __ldg(pd + c * L + lane);
         const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
@@ -117,11 +118,15 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
   }
 }
 
-__global__ void __launch_bounds__(256) dq_convert_kernel(const float4* __restrict__ src, uint2* __restrict__ dst,
-                                                         size_t n4) {
+// fp32 dQ accumulator [total, hq, dqk] (contiguous) -> bf16 dQ at token * ts + head * hs.
+__global__ void __launch_bounds__(256) dq_convert_kernel(const float4* __restrict__ src, uint16_t* __restrict__ dst,
+                                                         size_t n4, int hq, int dqk, long long ts, long long hs) {
+  const int q4 = dqk / 4;
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
     const float4 v = src[i];
-    dst[i] = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+    const size_t rh = i / q4;
+    const long long d = (long long)(i % q4) * 4, h = (long long)(rh % hq), t = (long long)(rh / hq);
+    *reinterpret_cast<uint2*>(dst + t * ts + h * hs + d) = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
   }
 }
 
@@ -244,15 +249,16 @@ cudaError_t launch_gate_cumsum(const float* g, const int32_t* cu, int num_seqs, 
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_pre(const uint16_t* o, const uint16_t* dout, int total, int hq, int dv, int dqk, float* delta,
+cudaError_t launch_bwd_pre(const uint16_t* o, const uint16_t* dout, int total, int hq, int dv, int dqk,
+                           long long o_ts, long long o_hs, long long do_ts, long long do_hs, float* delta,
                            float* dq_acc, float* dg_row, float* dg_col, cudaStream_t s) {
   // enough blocks to fill the GPU several times over; rows are grid-stride
   const int L = dv >= 256 ? 32 : dv / 8;
   const long long lanes = (long long)total * hq * L;
   const int blocks = (int)std::min<long long>((lanes + 255) / 256, 152 * 16);
-  if (L == 8) bwd_pre_kernel<8><<<blocks, 256, 0, s>>>(o, dout, total, hq, dv, delta);
-  else if (L == 16) bwd_pre_kernel<16><<<blocks, 256, 0, s>>>(o, dout, total, hq, dv, delta);
-  else bwd_pre_kernel<32><<<blocks, 256, 0, s>>>(o, dout, total, hq, dv, delta);
+  if (L == 8) bwd_pre_kernel<8><<<blocks, 256, 0, s>>>(o, dout, total, hq, dv, o_ts, o_hs, do_ts, do_hs, delta);
+  else if (L == 16) bwd_pre_kernel<16><<<blocks, 256, 0, s>>>(o, dout, total, hq, dv, o_ts, o_hs, do_ts, do_hs, delta);
+  else bwd_pre_kernel<32><<<blocks, 256, 0, s>>>(o, dout, total, hq, dv, o_ts, o_hs, do_ts, do_hs, delta);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (dq_acc) e = cudaMemsetAsync(dq_acc, 0, (size_t)total * hq * dqk * sizeof(float), s);
@@ -263,15 +269,16 @@ cudaError_t launch_bwd_pre(const uint16_t* o, const uint16_t* dout, int total, i
   return e;
 }
 
-cudaError_t launch_bwd_post(const float* dq_acc, uint16_t* dq, int total, int hq, int dqk, const int32_t* cu,
-                            int num_seqs, const float* dg_row, const float* dg_col, float* dlog_gate,
-                            const float* lse, const float* delta, const float* sink, float* dsink, cudaStream_t s) {
+cudaError_t launch_bwd_post(const float* dq_acc, uint16_t* dq, int total, int hq, int dqk, long long dq_ts,
+                            long long dq_hs, const int32_t* cu, int num_seqs, const float* dg_row,
+                            const float* dg_col, float* dlog_gate, const float* lse, const float* delta,
+                            const float* sink, float* dsink, cudaStream_t s) {
   cudaError_t e = cudaSuccess;
   if (dq_acc) {
     const size_t n4 = (size_t)total * hq * dqk / 4;
     const int blocks = (int)((n4 + 255) / 256 < 152 * 16 ? (n4 + 255) / 256 : 152 * 16);
-    dq_convert_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(dq_acc), reinterpret_cast<uint2*>(dq),
-                                             n4);
+    dq_convert_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(dq_acc), dq, n4, hq, dqk, dq_ts,
+                                             dq_hs);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

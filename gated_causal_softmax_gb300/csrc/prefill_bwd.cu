@@ -177,9 +177,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tmDO);
       mbar_expect_tx(kv_full, 2 * C::TILE);
       for (int c = 0; c < C::CH; ++c)
-        tma_load_2d(smem + C::OFF_K + c * kChunk, &tmK, kv_full, kvh * D + c * 64, seq_start + j0);
+        tma_load_3d(smem + C::OFF_K + c * kChunk, &tmK, kv_full, c * 64, kvh, seq_start + j0);
       for (int c = 0; c < C::CH; ++c)
-        tma_load_2d(smem + C::OFF_V + c * kChunk, &tmV, kv_full, kvh * D + c * 64, seq_start + j0);
+        tma_load_3d(smem + C::OFF_V + c * kChunk, &tmV, kv_full, c * 64, kvh, seq_start + j0);
       const uint64_t pol = l2_policy_evict_last();
       for (int s = 0; s < nsteps; ++s) {
         const int qb = s % kNQ, db = s % kNDO;
@@ -188,12 +188,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_bar(&q_empty[qb], ((s / kNQ) & 1) ^ 1, ab)) break;
         mbar_expect_tx(&q_full[qb], C::TILE);
         for (int c = 0; c < C::CH; ++c)
-          tma_load_2d_hint(smem + C::OFF_Q + qb * C::TILE + c * kChunk, &tmQ, &q_full[qb], h * D + c * 64,
+          tma_load_3d_hint(smem + C::OFF_Q + qb * C::TILE + c * kChunk, &tmQ, &q_full[qb], c * 64, h,
                            seq_start + it * kBM, pol);
         if (!wait_bar(&do_empty[db], ((s / kNDO) & 1) ^ 1, ab)) break;
         mbar_expect_tx(&do_full[db], C::TILE + kVecBytes);
         for (int c = 0; c < C::CH; ++c)
-          tma_load_2d_hint(smem + C::OFF_DO + db * C::TILE + c * kChunk, &tmDO, &do_full[db], h * D + c * 64,
+          tma_load_3d_hint(smem + C::OFF_DO + db * C::TILE + c * kChunk, &tmDO, &do_full[db], c * 64, h,
                            seq_start + it * kBM, pol);
         // per-column vectors of the two 64-row tiles: [(G_i - LSE_i) log2 e x 64, delta_i x 64] x 2
         bulk_load(smem + C::OFF_VEC + db * kVecBytes, p.vecp + ((size_t)h * p.n_qtiles + qoff + 2 * it) * 128,
@@ -391,8 +391,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) {
         tc_fence_after();
         const bool row_ok = jl < len;
-        const size_t row = (size_t)(seq_start + (row_ok ? jl : 0)) * p.hkv + kvh;
-        uint16_t* dst = wg == 0 ? p.grad_v + row * D : p.grad_k + row * D;
+        const size_t tok = (size_t)(seq_start + (row_ok ? jl : 0));
+        uint16_t* dst = wg == 0 ? p.grad_v + tok * p.dv_ts + (size_t)kvh * p.dv_hs
+                                : p.grad_k + tok * p.dk_ts + (size_t)kvh * p.dk_hs;
         const uint32_t col0 = wg == 0 ? C::T_DV : C::T_DK;
         const float sc = wg == 0 ? 1.f : p.scale;
 #pragma unroll 1

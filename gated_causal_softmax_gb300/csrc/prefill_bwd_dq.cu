@@ -145,8 +145,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_kv = l2_policy_evict_last();
       mbar_expect_tx(qd_full, 2 * C::TILE);
       for (int c = 0; c < C::CH; ++c) {
-        tma_load_2d(smem + C::OFF_Q + c * kChunk, &tmQ, qd_full, h * D + c * 64, seq_start + q0);
-        tma_load_2d(smem + C::OFF_DO + c * kChunk, &tmDO, qd_full, h * D + c * 64, seq_start + q0);
+        tma_load_3d(smem + C::OFF_Q + c * kChunk, &tmQ, qd_full, c * 64, h, seq_start + q0);
+        tma_load_3d(smem + C::OFF_DO + c * kChunk, &tmDO, qd_full, c * 64, h, seq_start + q0);
       }
       bool ok = true;
       for (int n = 0; n < nt && ok; ++n) {
@@ -156,13 +156,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         mbar_expect_tx(&k_full[kb], C::TILE);
         for (int c = 0; c < C::CH; ++c)
-          tma_load_2d_hint(smem + C::OFF_K + kb * C::TILE + c * kChunk, &tmK, &k_full[kb], kvh * D + c * 64, y,
+          tma_load_3d_hint(smem + C::OFF_K + kb * C::TILE + c * kChunk, &tmK, &k_full[kb], c * 64, kvh, y,
                            pol_kv);
         ok = wait_bar(&v_empty[kb], ((n >> 1) & 1) ^ 1, ab);
         if (!ok) break;
         mbar_expect_tx(&v_full[kb], C::TILE);
         for (int c = 0; c < C::CH; ++c)
-          tma_load_2d_hint(smem + C::OFF_V + kb * C::TILE + c * kChunk, &tmV, &v_full[kb], kvh * D + c * 64, y,
+          tma_load_3d_hint(smem + C::OFF_V + kb * C::TILE + c * kChunk, &tmV, &v_full[kb], c * 64, kvh, y,
                            pol_kv);
       }
     }
@@ -308,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) ok = wait_bar(dq_done, 0, ab);
     if (ok) {
       tc_fence_after();
-      uint16_t* dqrow = p.grad_q + ((size_t)(seq_start + (row_valid ? il : 0)) * p.hq + h) * D;
+      uint16_t* dqrow = p.grad_q + (size_t)(seq_start + (row_valid ? il : 0)) * p.dq_ts + (size_t)h * p.dq_hs;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];

@@ -133,10 +133,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     bool ok = true;
     uint32_t stage = 0, phase = 0;
-    auto issue = [&](const CUtensorMap* m, int x, int y, uint32_t bytes) -> bool {
+    // (x, hd, y) = (column within the head, head, token)
+    auto issue = [&](const CUtensorMap* m, int x, int hd, int y, uint32_t bytes) -> bool {
       if (!wait_bar(&empty[stage], phase ^ 1, ab)) return false;
       mbar_expect_tx(&full[stage], bytes);
-      tma_load_2d(smem + C::OFF_RING + stage * kStage, m, &full[stage], x, y);
+      tma_load_3d(smem + C::OFF_RING + stage * kStage, m, &full[stage], x, hd, y);
       if (++stage == C::NST) {
         stage = 0;
         phase ^= 1;
@@ -146,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       mbar_expect_tx(kv_full, C::NRES * kStage);
       for (int c = 0; c < C::NRES; ++c)
-        tma_load_2d(smem + C::OFF_KRES + c * kStage, &tmK, kv_full, kvh * DQK + (res0 + c) * 64, seq_start + j0);
+        tma_load_3d(smem + C::OFF_KRES + c * kStage, &tmK, kv_full, (res0 + c) * 64, kvh, seq_start + j0);
     }
     for (int s = 0; s < nsteps && ok; ++s) {
       const int h = kvh * group + s / n_it;
@@ -154,17 +155,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int yq = seq_start + i0, yk = seq_start + j0;
       if (lane == 0) {
         for (int c = 0; c < C::KCH && ok; ++c) {
-          if (c < res0 || c >= res0 + C::NRES) ok = issue(&tmK, kvh * DQK + c * 64, yk, kStage);
-          if (ok) ok = issue(&tmQ, h * DQK + c * 64, yq, BM * 128);
+          if (c < res0 || c >= res0 + C::NRES) ok = issue(&tmK, c * 64, kvh, yk, kStage);
+          if (ok) ok = issue(&tmQ, c * 64, h, yq, BM * 128);
         }
         if (KIND >= 1) {
           for (int c = 0; c < C::VCH && ok; ++c) {
-            ok = issue(&tmV, kvh * DV + c * 64, yk, kStage);
-            if (ok) ok = issue(&tmDO, h * DV + c * 64, yq, BM * 128);
+            ok = issue(&tmV, c * 64, kvh, yk, kStage);
+            if (ok) ok = issue(&tmDO, c * 64, h, yq, BM * 128);
           }
-          for (int c = 0; c < C::WCH && ok; ++c) ok = issue(&tmQ, h * DQK + w0 + c * 64, yq, BM * 128);
+          for (int c = 0; c < C::WCH && ok; ++c) ok = issue(&tmQ, w0 + c * 64, h, yq, BM * 128);
         } else {
-          for (int c = 0; c < C::WCH && ok; ++c) ok = issue(&tmDO, h * DV + w0 + c * 64, yq, BM * 128);
+          for (int c = 0; c < C::WCH && ok; ++c) ok = issue(&tmDO, w0 + c * 64, h, yq, BM * 128);
         }
         if (ok) ok = wait_bar(&vec_empty[s & 1], ((s >> 1) & 1) ^ 1, ab);
       }
@@ -426,9 +427,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && nsteps > 0) {
       tc_fence_after();
       const bool row_ok = jl < len;
-      uint16_t* dst = (KIND >= 1)
-                          ? p.grad_k + ((size_t)(seq_start + (row_ok ? jl : 0)) * p.hkv + kvh) * DQK + w0
-                          : p.grad_v + ((size_t)(seq_start + (row_ok ? jl : 0)) * p.hkv + kvh) * DV + w0;
+      const size_t tok = (size_t)(seq_start + (row_ok ? jl : 0));
+      uint16_t* dst = (KIND >= 1) ? p.grad_k + tok * p.dk_ts + (size_t)kvh * p.dk_hs + w0
+                                  : p.grad_v + tok * p.dv_ts + (size_t)kvh * p.dv_hs + w0;
       const float sc = (KIND >= 1) ? p.scale : 1.f;
 #pragma unroll 1
       for (int c = 0; c < kW / 32; ++c) {

@@ -120,9 +120,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int yq = seq_start + i0;
       mbar_expect_tx(q_full, (C::QCH + C::VCH) * (kStage / 2));
       for (int c = 0; c < C::QCH; ++c)
-        tma_load_2d(smem + C::OFF_Q + c * (kStage / 2), &tmQ, q_full, h * DQK + c * 64, yq);
+        tma_load_3d(smem + C::OFF_Q + c * (kStage / 2), &tmQ, q_full, c * 64, h, yq);
       for (int c = 0; c < C::VCH; ++c)
-        tma_load_2d(smem + C::OFF_DO + c * (kStage / 2), &tmDO, q_full, h * DV + c * 64, yq);
+        tma_load_3d(smem + C::OFF_DO + c * (kStage / 2), &tmDO, q_full, c * 64, h, yq);
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       // one 32 KB stage = columns x0 .. x0 + 127 of the tile's 128 key rows
@@ -130,8 +130,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_bar(&empty[stage], phase ^ 1, ab)) return false;
         mbar_expect_tx(&full[stage], C::PAIR);
         uint8_t* dst = smem + C::OFF_RING + stage * C::PAIR;
-        tma_load_2d(dst, m, &full[stage], x0, y);
-        tma_load_2d(dst + kStage, m, &full[stage], x0 + 64, y);
+        tma_load_3d(dst, m, &full[stage], x0, kvh, y);
+        tma_load_3d(dst + kStage, m, &full[stage], x0 + 64, kvh, y);
         if (++stage == C::NST) {
           stage = 0;
           phase ^= 1;
@@ -140,9 +140,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       for (int t = 0; t < nt && ok; ++t) {
         const int yk = seq_start + (jt_lo + t) * kBN;
-        for (int q = 0; q < C::KP && ok; ++q) ok = issue(&tmK, kvh * DQK + q * 128, yk);  // S^T
-        for (int q = 0; q < C::VP && ok; ++q) ok = issue(&tmV, kvh * DV + q * 128, yk);   // dP^T
-        for (int q = 0; q < C::KP && ok; ++q) ok = issue(&tmK, kvh * DQK + q * 128, yk);  // dQ^T
+        for (int q = 0; q < C::KP && ok; ++q) ok = issue(&tmK, q * 128, yk);  // S^T
+        for (int q = 0; q < C::VP && ok; ++q) ok = issue(&tmV, q * 128, yk);   // dP^T
+        for (int q = 0; q < C::KP && ok; ++q) ok = issue(&tmK, q * 128, yk);  // dQ^T
       }
     }
     __syncwarp();
@@ -324,14 +324,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       // dQ^T halves: lane r holds dims 128 q + r for the 64 queries
       const int nrows = min(kBM, len - i0);
-      const size_t row_stride = (size_t)p.hq * DQK;
+      const size_t row_stride = (size_t)p.dq_ts;
 #pragma unroll 1
       for (int q = 0; q < C::KP; ++q) {
         uint32_t dq[64];
         tmem_ld32(tmem + lane_off + C::T_DQ + 64 * q, dq);
         tmem_ld32(tmem + lane_off + C::T_DQ + 64 * q + 32, dq + 32);
         tmem_ld_wait();
-        uint16_t* base = p.grad_q + ((size_t)(seq_start + i0) * p.hq + h) * DQK + 128 * q + r;
+        uint16_t* base = p.grad_q + (size_t)(seq_start + i0) * p.dq_ts + (size_t)h * p.dq_hs + 128 * q + r;
 #pragma unroll
         for (int c = 0; c < kBM; ++c)
           if (c < nrows) {

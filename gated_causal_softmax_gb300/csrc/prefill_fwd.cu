@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_q = l2_policy_evict_first();
       mbar_expect_tx(q_full, C::QCH * kChunk);
       for (int c = 0; c < C::QCH; ++c)
-        tma_load_2d_hint(smem + C::OFF_Q + c * kChunk, &tmQ, q_full, h * DQK + c * 64, seq_start + q0, pol_q);
+        tma_load_3d_hint(smem + C::OFF_Q + c * kChunk, &tmQ, q_full, c * 64, h, seq_start + q0, pol_q);
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       for (int n = 0; n <= nt && ok; ++n) {
@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = wait_bar(&kv_empty[stage], phase ^ 1, ab);
             if (!ok) break;
             mbar_expect_tx(&kv_full[stage], kChunk);
-            tma_load_2d_hint(smem + C::OFF_RING + stage * kChunk, &tmK, &kv_full[stage], kvh * DQK + c * 64, y,
+            tma_load_3d_hint(smem + C::OFF_RING + stage * kChunk, &tmK, &kv_full[stage], c * 64, kvh, y,
                              pol_kv);
             if (++stage == C::NST) { stage = 0; phase ^= 1; }
           }
@@ -146,8 +146,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = wait_bar(&kv_empty[stage], phase ^ 1, ab);
             if (!ok) break;
             mbar_expect_tx(&kv_full[stage], kChunk);
-            tma_load_2d_hint(smem + C::OFF_RING + stage * kChunk, &tmV, &kv_full[stage],
-                             kvh * p.dv + dv0 + c * 64, y, pol_kv);
+            tma_load_3d_hint(smem + C::OFF_RING + stage * kChunk, &tmV, &kv_full[stage], dv0 + c * 64, kvh, y,
+                             pol_kv);
             if (++stage == C::NST) { stage = 0; phase ^= 1; }
           }
         }
@@ -329,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       tc_fence_after();
       const float inv_l = 1.f / l;
-      uint16_t* orow = p.o + ((size_t)(seq_start + (row_valid ? il : 0)) * p.hq + h) * p.dv + dv0;
+      uint16_t* orow = p.o + (size_t)(seq_start + (row_valid ? il : 0)) * p.o_ts + (size_t)h * p.o_hs + dv0;
 #pragma unroll 1
       for (int c = 0; c < DVC / 32; ++c) {
         uint32_t ov[32];

@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_expect_tx(q_full, 2 * C::CH * kChunk);
       for (int x = 0; x < 2; ++x)
         for (int c = 0; c < C::CH; ++c)
-          tma_load_2d_hint(smem + C::OFF_Q + (x * C::CH + c) * kChunk, &tmQ, q_full, h * D + c * 64,
+          tma_load_3d_hint(smem + C::OFF_Q + (x * C::CH + c) * kChunk, &tmQ, q_full, c * 64, h,
                            seq_start + q0 + x * kBM, pol_q);
       uint32_t stage = 0, phase = 0;
       bool ok = true;
@@ -141,8 +141,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           mbar_expect_tx(&full[stage], C::TILE);
           for (int c = 0; c < C::CH; ++c)
-            tma_load_2d_hint(smem + C::OFF_RING + stage * C::TILE + c * kChunk, kv ? &tmV : &tmK, &full[stage],
-                             kvh * D + c * 64, y, pol_kv);
+            tma_load_3d_hint(smem + C::OFF_RING + stage * C::TILE + c * kChunk, kv ? &tmV : &tmK, &full[stage],
+                             c * 64, kvh, y, pol_kv);
           if (++stage == C::NST) {
             stage = 0;
             phase ^= 1;
@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && kx > 0) {
       tc_fence_after();
       const float inv_l = 1.f / l;
-      uint16_t* orow = p.o + ((size_t)(seq_start + (row_valid ? il : 0)) * p.hq + h) * p.dv;
+      uint16_t* orow = p.o + (size_t)(seq_start + (row_valid ? il : 0)) * p.o_ts + (size_t)h * p.o_hs;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t ov[32];

@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const size_t slot0 = ((size_t)blk * p.hkv + kvh) * kPage;
         if (pl < nv) {
           if (kind == 0)
-            tma_load_2d(kraw + pl * 2048, &tmK, kr_full, 0, static_cast<int>(slot0));
+            tma_load_4d(kraw + pl * 2048, &tmK, kr_full, 0, p.kv_head_inner ? kvh : 0, p.kv_head_inner ? 0 : kvh, blk);
           else if (kind == 1 && per_token)
             bulk_load(kraw + C::KR_KS + pl * 64, p.k_scale + slot0, 64, kr_full);
           else if (kind == 2 && per_token)
@@ -250,7 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!__all_sync(0xffffffffu, okl)) break;
         if (lane == 0) mbar_expect_tx(vr_full, nv * 2048);
         __syncwarp();
-        if (kind == 0 && pl < nv) tma_load_2d(vraw + pl * 2048, &tmV, vr_full, 0, static_cast<int>(slot0));
+        if (kind == 0 && pl < nv)
+          tma_load_4d(vraw + pl * 2048, &tmV, vr_full, 0, p.kv_head_inner ? kvh : 0, p.kv_head_inner ? 0 : kvh, blk);
       }
     } else if (warp == 1) {
       if (lane == 0) {
@@ -480,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
       // this row of Q: bf16 -> f16 into the 128-B-swizzled K-major tile (two 64-dim chunks)
       const uint4* src =
-          reinterpret_cast<const uint4*>(p.q + ((size_t)(q_begin + posc) * p.hq + kvh * kGroup + head) * kD);
+          reinterpret_cast<const uint4*>(p.q + (size_t)(q_begin + posc) * p.q_ts + (size_t)(kvh * kGroup + head) * p.q_hs);
       uint8_t* qs = smem + C::OFF_Q + x * 2 * kStage;
 #pragma unroll 4
       for (int u = 0; u < 16; ++u) {
@@ -615,7 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (direct) {
         if (kx > 0) {
           const float inv = 1.f / (kPScale * l);
-          uint16_t* orow = p.out + ((size_t)(q_begin + posc) * p.hq + kvh * kGroup + head) * kD;
+          uint16_t* orow = p.out + (size_t)(q_begin + posc) * p.out_ts + (size_t)(kvh * kGroup + head) * p.out_hs;
 #pragma unroll 1
           for (int cc = 0; cc < kD / 32; ++cc) {
             uint32_t ov[32];

@@ -28,8 +28,12 @@
  *   - Every call is asynchronous on the given stream.  Arguments are validated on the
  *     host first; on any error the call returns a nonzero gcs_status and launches
  *     nothing, so outputs are untouched.
- *   - Tensors are contiguous, row-major, last dimension fastest; base addresses are
- *     16-byte aligned.
+ *   - Tensors are row-major with the last dimension contiguous and base addresses 16-byte
+ *     aligned.  The [tokens, heads, head_dim] tensors of the prefill and paged calls (q, k,
+ *     v, o, dout, the gradients, the paged q and out) take element strides (token, head)
+ *     given as gcs_strides, and the paged caches take element strides (block, kv head, slot);
+ *     all-zero strides mean contiguous.  Everything else (gates, sinks, LSE, scales, index
+ *     arrays) is contiguous.
  *   - No output may share a byte with an input or with another output (the kernels read
  *     and write concurrently); such a call returns GCS_ERR_INVALID_ARG.  Inputs may share
  *     memory with each other.
@@ -57,6 +61,18 @@ extern "C" {
 #endif
 
 typedef struct CUstream_st* gcs_stream_t; /* same type as cudaStream_t; NULL = legacy default stream */
+
+/* Element strides of a [tokens, heads, head_dim] tensor whose head_dim is contiguous: element
+ * (t, h, d) sits at base[t * token + h * head + d].  {0, 0} means the contiguous layout
+ * {heads * head_dim, head_dim}.  Otherwise the layout must be token-major without overlap,
+ * head >= head_dim and token >= heads * head, with both multiples of 8 elements (16 bytes, the
+ * granule of the tensor copies and vector stores); any other layout returns
+ * GCS_ERR_UNSUPPORTED.  A slice of a fused projection, e.g. q, k and v as views of one
+ * [tokens, (hq + 2 hkv) * d] buffer, is such a layout. */
+typedef struct {
+  int64_t token;
+  int64_t head;
+} gcs_strides;
 
 typedef enum {
   GCS_OK = 0,
@@ -99,13 +115,20 @@ typedef struct {
                                  order; 0 = the faster route for the shape: that same pass
                                  for dqk = 512, fp32 reduce-adds of dQ and the dS row sums
                                  otherwise.  Head dims <= 128 are deterministic either way. */
+  gcs_strides q_stride, k_stride, v_stride;  /* layouts of q, k, v ({0, 0} = contiguous)      */
+  gcs_strides o_stride;       /* attn_fwd's output o and attn_bwd's input o                    */
+  gcs_strides do_stride;      /* attn_bwd's dout                                               */
+  gcs_strides dq_stride, dk_stride, dv_stride;  /* attn_bwd's outputs dq, dk, dv              */
 } gcs_prefill_args;
 
 /* Workspace bytes attn_fwd needs (0 when there is no gate). */
 size_t attn_fwd_workspace(const gcs_prefill_args* a);
 
-/* Forward.  o: bf16 [total_tokens, hq, dv]; lse: fp32 [hq, total_tokens], natural-log
- * logsumexp of each row's scores including the sink term (needed by attn_bwd). */
+/* Forward.  o: bf16 [total_tokens, hq, dv] (layout a->o_stride); lse: fp32 [hq, total_tokens]
+ * contiguous, natural-log logsumexp of each row's scores including the sink term (needed by
+ * attn_bwd).  Outputs that share bytes with an input or with each other are rejected; two
+ * strided tensors with the same token stride whose per-token byte ranges interleave without
+ * meeting (e.g. heads of one fused buffer) do not share bytes. */
 int attn_fwd(const gcs_prefill_args* a, void* o, float* lse, void* workspace, size_t workspace_bytes,
              gcs_stream_t stream);
 
@@ -113,9 +136,10 @@ int attn_fwd(const gcs_prefill_args* a, void* o, float* lse, void* workspace, si
 size_t attn_bwd_workspace(const gcs_prefill_args* a);
 
 /* Backward of L = sum(O * dO) ([FLA] Description, the gradient list; Oct 3 / Oct 5 comments).
- * o, lse: the forward's outputs; dout: bf16 [total_tokens, hq, dv].
- * Outputs: dq bf16 [total_tokens, hq, dqk], dk bf16 [total_tokens, hkv, dqk],
- * dv bf16 [total_tokens, hkv, dv], dlog_gate fp32 [total_tokens, hq] (must be NULL iff
+ * o, lse: the forward's outputs (o in layout a->o_stride); dout: bf16 [total_tokens, hq, dv]
+ * (a->do_stride).  Outputs: dq bf16 [total_tokens, hq, dqk] (a->dq_stride), dk bf16
+ * [total_tokens, hkv, dqk] (a->dk_stride), dv bf16 [total_tokens, hkv, dv] (a->dv_stride),
+ * dlog_gate fp32 [total_tokens, hq] contiguous (must be NULL iff
  * log_gate is NULL), dsink fp32 [hq] (must be NULL iff sink is NULL).
  * The sink gradient is -sum_i p_sink,i * sum_j P_ij (dO_i . v_j), accumulated in fp32.
  * Head dims <= 128: dQ is accumulated per query tile in a separate pass and every gradient is
@@ -153,6 +177,12 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
  * e^sink_h to the softmax denominator (once, in the combine).
  * Supported: d == 128, block_size == 16, hq / hkv == 16, 1 <= q_len <= 4,
  * segment_len a positive multiple of block_size.
+ * Operand precision of an fp8 cache: the tensor cores see f16.  q is rounded from bf16 to f16,
+ * so no |q| may exceed 65504 (the f16 maximum); K and V codes convert to f16 exactly;
+ * P * vscale is rounded to nearest f16 after a 2^8 pre-scale (P <= 1), so every V scale of a
+ * slot below seq_len must stay below 255.  Outside these limits the output holds inf or NaN.
+ * The host cannot read device values; checked mode (gcs_set_device_checks) checks both on the
+ * device and records GCS_ERR_INVALID_ARG when one fails.
  */
 enum { GCS_KV_FP8_E4M3 = 0, GCS_KV_BF16 = 1 };
 enum { GCS_SCALE_PER_TOKEN = 0, GCS_SCALE_PER_TENSOR = 1 };
@@ -179,6 +209,17 @@ typedef struct {
   const float* g_cache;        /* fp32 [num_blocks, hq, block_size] cumulative log gates, or NULL */
   const float* sink;           /* fp32 [hq] sink logits, or NULL                          */
   int window;                  /* sliding window in keys, 0 = none                        */
+  gcs_strides q_stride;        /* layout of q ({0, 0} = contiguous)                       */
+  gcs_strides out_stride;      /* layout of out ({0, 0} = contiguous)                     */
+  int64_t kv_stride_block, kv_stride_head, kv_stride_slot;
+                               /* element strides of both caches (block, kv head, slot); all 0 =
+                                  contiguous [num_blocks, hkv, block_size, d].  The d elements of
+                                  a slot are contiguous; every stride is a multiple of 16 bytes;
+                                  the slots and kv heads of a block nest without overlap (slot
+                                  >= d and head >= block_size * slot, or head >= d and slot >=
+                                  hkv * head: the [num_blocks, block_size, hkv, d] cache layout of
+                                  vLLM-style engines) and block covers both.  Scales and gates
+                                  stay contiguous [num_blocks, ..., block_size]. */
 } gcs_decode_args;
 
 /* Workspace bytes attn_decode_paged needs (split-K partials). */
@@ -252,7 +293,9 @@ int gcs_selftest_bounded_wait(gcs_stream_t stream);
  *            0 <= q_len <= max_q_len and q_len <= seq_len <= max_seq_len; and, for a request
  *            with q_len >= 1, every block_table entry in [0, num_blocks) from the 128-key tile
  *            that holds the earliest key one of its query rows sees (key 0 without a window)
- *            up to the page of its last cached token (the pages the paged calls can read).
+ *            up to the page of its last cached token (the pages the paged calls can read);
+ *            with an fp8 cache, the f16 operand limits: every |q| <= 65504 and every V scale
+ *            of those pages' slots below seq_len (or the per-tensor V scale) < 255.
  * A failed check records GCS_ERR_INVALID_ARG in the current device's status word (first
  * writer wins, like a timeout); read it with gcs_get_device_status.
  *

@@ -96,6 +96,28 @@ int main(void) {
   EXPECT(attn_bwd(&a, OUT, (const float*)OUT2, FAKE, OUT, OUT2, OUT, NULL, NULL, NULL, 0, NULL) ==
          GCS_ERR_INVALID_ARG); /* gated backward without dlog_gate */
 
+  /* strides: a q slice of a fused [tokens, (hq + 2 hkv) * d] projection is accepted; heads
+   * that overlap, a token stride below the heads' span, or a stride off the 16-byte granule
+   * are refused before any launch */
+  b = a;
+  b.q_stride.token = (4 + 2 * 2) * 128;
+  b.q_stride.head = 128;
+  EXPECT(attn_fwd(&b, OUT, OUT2, NULL, 0, NULL) == GCS_ERR_WORKSPACE);
+  b.q_stride.head = 100;
+  EXPECT(attn_fwd(&b, OUT, OUT2, NULL, 0, NULL) == GCS_ERR_UNSUPPORTED);
+  b.q_stride.head = 128;
+  b.q_stride.token = 3 * 128;
+  EXPECT(attn_fwd(&b, OUT, OUT2, NULL, 0, NULL) == GCS_ERR_UNSUPPORTED);
+  b.q_stride.token = 4 * 128 + 4;
+  EXPECT(attn_fwd(&b, OUT, OUT2, NULL, 0, NULL) == GCS_ERR_UNSUPPORTED);
+  b = a;
+  b.o_stride.token = -8;
+  EXPECT(attn_fwd(&b, OUT, OUT2, NULL, 0, NULL) == GCS_ERR_INVALID_ARG);
+  b = a;
+  b.dk_stride.head = 64; /* the output store needs head >= dqk */
+  b.dk_stride.token = 256;
+  EXPECT(attn_bwd_workspace(&b) == 0);
+
   /* decode: split-K partials of 2 requests x 2 segments x 4 kv heads x 16 rows */
   {
     const size_t units = 2 * 2 * 4, rows = 16;
@@ -119,6 +141,19 @@ int main(void) {
   e.max_blocks_per_req = (1 << 20) / 16;
   EXPECT(attn_decode_workspace(&e) > ((size_t)64 << 20));
   EXPECT(attn_decode_paged_noalloc(&e, OUT, NULL) == GCS_ERR_WORKSPACE); /* partials exceed the scratch */
+
+  /* cache strides: the [num_blocks, block_size, hkv, d] layout is accepted, slots that
+   * overlap a kv head's rows are not */
+  e = d;
+  e.kv_stride_block = 16 * 4 * 128;
+  e.kv_stride_head = 128;
+  e.kv_stride_slot = 4 * 128;
+  EXPECT(attn_decode_workspace(&e) == attn_decode_workspace(&d));
+  EXPECT(attn_decode_paged(&e, OUT, NULL, 0, NULL) == GCS_ERR_WORKSPACE);
+  e.kv_stride_slot = 2 * 128;
+  EXPECT(attn_decode_paged(&e, OUT, NULL, 0, NULL) == GCS_ERR_UNSUPPORTED);
+  e.kv_stride_slot = 4 * 128 + 8;
+  EXPECT(attn_decode_paged(&e, OUT, NULL, 0, NULL) == GCS_ERR_UNSUPPORTED);
 
   /* paged prefill: any q_len, segments of whole 128-key tiles */
   e = d;

@@ -206,11 +206,9 @@ def test_size_limits_on_host(L):
     assert L.attn_bwd_workspace(b(prefill(total_tokens=(1 << 22) - 1, max_seqlen=1 << 20))) > 0
     # the larger of dqk and dv counts: dv = 512 with 2^20 tokens and hq = 4 is 2^31 elements
     assert fwd(prefill(total_tokens=1 << 20, max_seqlen=1 << 20, dqk=256, dv=512)) == 2
-    dec = lambda a: L.attn_decode_paged(b(a), FAKE, FAKE, 1 << 40, None)
-    # hkv x block_size = 64 rows per block: 2^25 blocks reach 2^31 rows
-    assert dec(decode(num_blocks=1 << 25)) == 2
-    assert L.attn_decode_workspace(b(decode(num_blocks=(1 << 25) - 1))) > 0
-    # a bf16 cache is read with plain 64-bit addressing and has no row limit
+    # the fp8 pages are fetched by 4-D tensor copies (block coordinate 32-bit), a bf16 cache with
+    # 64-bit addressing: 2^25 blocks (2^31 rows of 128 B) are accepted either way
+    assert L.attn_decode_workspace(b(decode(num_blocks=1 << 25))) > 0
     assert L.attn_decode_workspace(b(decode(num_blocks=1 << 25, kv_format=1, k_scale=None, v_scale=None))) > 0
     # the table-length check multiplies in 64 bits: (2^28 + 1) x 16 would wrap a 32-bit int to
     # 16 tokens, below max_seq_len, and the valid shape would be refused
@@ -268,3 +266,59 @@ def test_outputs_overlapping_inputs_are_rejected_on_host(L):
                                                   None)
     assert pp(OUT) == 3
     assert pp(OUT, k_scale=OUT + 512) == 1
+
+
+def test_strides_on_host(L):
+    """Element strides (token, head) of the [tokens, heads, dim] tensors and (block, kv head,
+    slot) of the paged caches: token-major layouts without overlap on the 16-byte granule are
+    accepted (the calls then stop at the missing workspace, 3); overlapping heads, a token
+    stride below the heads' span, strides off the granule and caches whose slots and heads
+    meet are refused (2), negative strides are invalid (1).  Outputs that interleave with each
+    other inside one fused buffer without sharing bytes are accepted; a shift that makes two
+    of them meet is refused."""
+    import gated_causal_softmax_gb300 as gcs
+
+    b = ctypes.byref
+    S = gcs.Strides
+    fused = (4 + 2 * 2) * 128  # [tokens, (hq + 2 hkv) * d] with hq 4, hkv 2, d 128
+    fwd = lambda a: L.attn_fwd(b(a), OUT, OUT2, None, 0, None)
+    g = dict(log_gate=FAKE)  # a gated forward needs a workspace, so accepted calls return 3
+    assert fwd(prefill(q_stride=S(fused, 128), k_stride=S(fused, 128), v_stride=S(fused, 128), **g)) == 3
+    assert fwd(prefill(q_stride=S(fused, 136), **g)) == 3  # padded heads
+    assert fwd(prefill(q_stride=S(fused, 120), **g)) == 2  # heads overlap
+    assert fwd(prefill(q_stride=S(3 * 128, 128), **g)) == 2  # token stride below 4 heads
+    assert fwd(prefill(q_stride=S(fused + 4, 128), **g)) == 2  # off the 16-byte granule
+    assert fwd(prefill(q_stride=S(-8, 128), **g)) == 1
+    assert fwd(prefill(o_stride=S(fused, 264), **g)) == 2  # 4 heads of 264 exceed the token stride
+    assert fwd(prefill(o_stride=S(8 * 128, 256), **g)) == 3  # every other head slot
+    # dq, dk, dv as interleaved views of one fused gradient buffer: accepted
+    a = prefill(log_gate=FAKE, sink=FAKE, dq_stride=S(fused, 128), dk_stride=S(fused, 128),
+                dv_stride=S(fused, 128))
+    base = OUT
+    dq, dk, dv = base, base + 4 * 128 * 2, base + 6 * 128 * 2
+    bwd = lambda dq, dk, dv: L.attn_bwd(b(a), at(3), at(4), at(5), dq, dk, dv, at(9), at(10), None, 0, None)
+    assert bwd(dq, dk, dv) == 3
+    assert bwd(dq, dk - 16, dv) == 1  # dk's first head meets dq's last
+    assert bwd(dq, dk, dv + 8 * 128 * 2 * 256) == 3  # dv in another buffer
+    assert bwd(dq, dq + fused * 2, dv) == 1  # dk one token later in dq's own slots
+    # o given to the backward as a strided input
+    a2 = prefill(log_gate=FAKE, sink=FAKE, o_stride=S(fused, 128), do_stride=S(fused, 136))
+    assert L.attn_bwd_workspace(b(a2)) == L.attn_bwd_workspace(b(prefill(log_gate=FAKE, sink=FAKE)))
+    # paged caches
+    dws = L.attn_decode_workspace(b(decode()))
+    vllm = dict(kv_stride_block=16 * 4 * 128, kv_stride_head=128, kv_stride_slot=4 * 128)
+    assert L.attn_decode_workspace(b(decode(**vllm))) == dws
+    assert L.attn_decode_workspace(b(decode(kv_format=1, k_scale=None, v_scale=None, **vllm))) == dws
+    assert L.attn_decode_paged(b(decode(**vllm)), OUT, None, 0, None) == 3
+    bad = [dict(vllm, kv_stride_slot=2 * 128),  # slots meet the other heads' rows
+           dict(vllm, kv_stride_block=16 * 4 * 128 - 16),  # blocks overlap
+           dict(vllm, kv_stride_slot=4 * 128 + 8),  # off the granule (fp8: bytes)
+           dict(kv_stride_block=16 * 4 * 128, kv_stride_head=16 * 64, kv_stride_slot=128)]  # heads meet
+    for over in bad:
+        assert L.attn_decode_paged(b(decode(**over)), OUT, None, 0, None) == 2, over
+    assert L.attn_decode_paged(b(decode(kv_stride_block=-1, kv_stride_head=128, kv_stride_slot=512)), OUT, None, 0,
+                               None) == 1
+    # q and out of the paged calls
+    assert L.attn_decode_paged(b(decode(q_stride=S(64 * 128 + 256, 128))), OUT, None, 0, None) == 3
+    assert L.attn_decode_paged(b(decode(out_stride=S(64 * 128, 64))), OUT, None, 0, None) == 2
+    assert L.attn_prefill_paged(b(decode(max_q_len=64, segment_len=256, **vllm)), OUT, None, 0, None) == 3

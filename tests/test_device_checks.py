@@ -217,3 +217,43 @@ def test_window_leaves_unread_pages_unchecked(checked, kind):
     got = run_paged_raw(gcs, a, kind, d["q"])
     assert gcs.get_device_status() == 0
     assert torch.equal(got, ref)
+
+
+@pytest.mark.parametrize("kind", ["decode", "prefill_paged"])
+@pytest.mark.parametrize("name", ["v_scale_at_255", "q_above_f16_max", "per_tensor_v_scale"])
+def test_fp8_operand_limits_are_caught(checked, kind, name):
+    """With an fp8 cache the tensor cores see f16: a |q| above 65504 or a V scale of 255 or more
+    in a slot below seq_len would overflow.  Checked mode refuses both (status
+    GCS_ERR_INVALID_ARG, output untouched); the same values where they are not read (slots past
+    seq_len hold NaN scales in every case here) pass."""
+    gcs = checked
+    ql = [1, 3] if kind == "decode" else [40, 100]
+    per_tensor = name == "per_tensor_v_scale"
+    dc = make_decode([600, 300], ql, 16, 1, 128, seed=750, scale_mode="per_tensor" if per_tensor else "per_token")
+    d = decode_dev(dc)
+    seg = 128 if kind == "decode" else 0
+    q = d["q"].clone()
+    vs = d["vs"].clone()
+    if name == "v_scale_at_255":
+        blk = int(dc.block_table[1, 18])  # request 1 (300 tokens): page 18 holds slots 288..299
+        vs[blk, 0, 11] = 255.0
+    elif name == "q_above_f16_max":
+        q[2, 5, 17] = 65536.0  # bf16-exact, above the f16 range
+    else:
+        vs.fill_(300.0)
+    a = gcs.decode_args(q, d["kc"], d["vc"], d["ks"], vs, d["bt"], d["sl"], d["cq"], max(ql), 600, dc.scale, seg)
+    out = run_paged_raw(gcs, a, kind, q)
+    assert gcs.get_device_status() == INVALID
+    assert bool((out == SENTINEL).all())
+    # the limits themselves pass: 254.9 in that slot, 65280 (the largest bf16 below 65504) in q
+    if name == "v_scale_at_255":
+        vs[blk, 0, 11] = 254.9
+    elif name == "q_above_f16_max":
+        q[2, 5, 17] = 65280.0
+    else:
+        vs.fill_(254.9)
+    a = gcs.decode_args(q, d["kc"], d["vc"], d["ks"], vs, d["bt"], d["sl"], d["cq"], max(ql), 600, dc.scale, seg)
+    L = gcs.load()
+    assert L.gcs_check_paged_inputs(ctypes.byref(a), torch.cuda.current_stream().cuda_stream) == 0
+    torch.cuda.synchronize()
+    assert gcs.get_device_status() == 0
