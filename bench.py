@@ -45,7 +45,7 @@ LAUNCHES_PER_DECODE = 2
 # workloads, from one ncu capture of the kernel as it stands; set back to None whenever the
 # kernel changes.
 NCU_TRAFFIC = {
-    "bwd": 217.9e6 + 277.0e6,  # prefill_bwd_dq_kernel<128> + prefill_bwd_kernel<128>
+    "bwd": None,               # prefill_bwd_fused_kernel: not captured yet
     "fwd": 119.8e6,            # prefill_fwd2_kernel<128>
     "decode_split": 1155.5e6 + 19.1e6,  # decode_split_kernel<0, 0, 0>
     "prefill_paged": 153.8e6 + 35.3e6,  # prefill_paged_kernel<0>
@@ -286,13 +286,34 @@ def run_native(args):
     if gcs.get_device_status() != 0:
         raise RuntimeError("a kernel timed out during the timed region")
 
-    # dominant kernel: the fused backward attention kernel
+    # the same step with the deterministic two-pass backward, timed the same way
+    def step_det():
+        o, lse = gcs.attn_fwd(q, k, v, cu, ms, case.scale, case.window, g, s)
+        return gcs.attn_bwd(q, k, v, o, lse, do, cu, ms, case.scale, case.window, g, s, deterministic=True)
+
+    for _ in range(args.warmup):
+        step_det()
+    barrier(world)
+    torch.cuda.synchronize()
+    t2, t3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t2.record()
+    for _ in range(K):
+        step_det()
+    t3.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    det_ms = max_over_ranks(world, t2.elapsed_time(t3)) / K
+    two_pass = {"ms_per_step": round(det_ms, 4),
+                "value": round(whole_job_rate(step_fl, world, det_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "note": "deterministic=True: dQ pass + dK/dV pass, no fp32 dQ buffer"}
+
+    # dominant kernel: the backward attention kernel(s)
     # The prefill kernels run in timed regions of tens of milliseconds at the maximum SM clock
     # (the clock record shows it), so the burst cuBLAS figure is their peak; the sustained one
     # was measured seconds into a power-capped loop at a lower clock and is reported beside it.
     burst = pk["bf16_tflops"]
     sustained = pk.get("bf16_tflops_sustained", burst)
-    dom = ("prefill_bwd_dq_kernel<128> + prefill_bwd_kernel<128> (two-pass backward)" if bwd_k >= fwd_k
+    dom = ("prefill_bwd_fused_kernel (single-pass backward, dQ reduce-added in fp32)" if bwd_k >= fwd_k
            else "prefill_fwd2_kernel<128>")
     dom_fl, dom_ms = (bwd_fl, bwd_k) if bwd_k >= fwd_k else (fwd_fl, fwd_k)
     achieved = dom_fl / (dom_ms * 1e-3) / 1e12
@@ -305,7 +326,8 @@ def run_native(args):
                 "kernel_ms_median_min": {"fwd": [round(statistics.median(fwd_all), 4), round(min(fwd_all), 4)],
                                          "bwd": [round(statistics.median(bwd_all), 4), round(min(bwd_all), 4)]},
                 "fwd_kernel_tflops": round(fwd_fl / (fwd_k * 1e-3) / 1e12, 1),
-                "bwd_kernel_tflops": round(bwd_fl / (bwd_k * 1e-3) / 1e12, 1)}
+                "bwd_kernel_tflops": round(bwd_fl / (bwd_k * 1e-3) / 1e12, 1),
+                "two_pass_route": two_pass}
 
     # ------------------------------------------------------------ end to end (host buffers)
     host = {n: t.pin_memory() for n, t in (("q", case.q), ("k", case.k), ("v", case.v), ("do", case.do),

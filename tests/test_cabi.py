@@ -94,18 +94,20 @@ def test_workspace_sizes_on_host(L):
     b = ctypes.byref
     assert L.attn_fwd_workspace(b(prefill())) == 0
     assert L.attn_fwd_workspace(b(prefill(log_gate=FAKE))) == 4 * 4 * 256
-    ws = L.attn_bwd_workspace(b(prefill(log_gate=FAKE, sink=FAKE)))
-    # G^T, delta, dS row sums, dS column sums, packed per-tile vectors; wider heads on the
-    # reduce-add route add the fp32 dQ accumulator, the deterministic route does not
+    ws = L.attn_bwd_workspace(b(prefill(log_gate=FAKE, sink=FAKE, deterministic=1)))
+    # G^T, delta, dS row sums, dS column sums, packed per-tile vectors; the single pass at head
+    # dim 128 and wider heads on the reduce-add route add the fp32 dQ accumulator, the
+    # deterministic routes do not
     n_qtiles = 256 // 64 + 1
     assert ws == 4 * (4 * 256) * 4 + 4 * n_qtiles * 128 * 4
+    assert L.attn_bwd_workspace(b(prefill(log_gate=FAKE, sink=FAKE))) == ws + 256 * 4 * 128 * 4
+    assert L.attn_bwd_workspace(b(prefill(log_gate=FAKE, sink=FAKE, dqk=64, dv=64))) == ws  # two passes at 64
     ws_wide = L.attn_bwd_workspace(b(prefill(log_gate=FAKE, sink=FAKE, dqk=256, dv=512)))
     assert ws_wide == 4 * (4 * 256) * 4 + 256 * 4 * 256 * 4 + 4 * n_qtiles * 128 * 4
     ws_det = L.attn_bwd_workspace(b(prefill(log_gate=FAKE, sink=FAKE, dqk=256, dv=512, deterministic=1)))
     assert ws_det == ws
     # (512, 512) takes the dQ pass either way: it is the faster route there
     assert L.attn_bwd_workspace(b(prefill(log_gate=FAKE, sink=FAKE, dqk=512, dv=512))) == ws
-    assert L.attn_bwd_workspace(b(prefill(log_gate=FAKE, sink=FAKE, deterministic=1))) == ws
     units, rows = 2 * 2 * 4, 16
     assert L.attn_decode_workspace(b(decode())) == units * rows * 128 * 4 + units * rows * 2 * 4
     assert L.attn_decode_workspace(b(decode(max_q_len=5))) == 0

@@ -12,6 +12,7 @@ import ctypes
 import pytest
 import torch
 
+import oracle
 from synth import make_decode, make_prefill
 from helpers import decode_dev, to_dev
 
@@ -40,7 +41,7 @@ def prefill_all(gcs, case, d, cu=None, deterministic=False):
     return [o, lse] + [t for t in g if t is not None]
 
 
-@pytest.mark.parametrize("dims,det", [((128, 128), False), ((64, 64), False), ((256, 512), True)])
+@pytest.mark.parametrize("dims,det", [((128, 128), True), ((128, 128), False), ((64, 64), False), ((256, 512), True)])
 def test_checked_mode_leaves_prefill_results_unchanged(gcs_lib, dims, det):
     case = make_prefill([300, 1, 129], 4, 2, dims[0], dims[1], seed=700 + dims[0], gate=True, sink=True, window=0)
     d = to_dev(case)
@@ -53,8 +54,14 @@ def test_checked_mode_leaves_prefill_results_unchanged(gcs_lib, dims, det):
         assert gcs_lib.get_device_status() == 0
     finally:
         gcs_lib.set_device_checks(False)
+    # o, lse, dq, dk, dv, dlog_gate, dsink: the single-pass route (128 without deterministic)
+    # reduce-adds dq and the dS row sums in fp32, whose low bits may vary from call to call
+    loose = {2, 5, 6} if (dims == (128, 128) and not det) else set()
     for i, (a, b) in enumerate(zip(ref, got)):
-        assert torch.equal(a, b), i
+        if i in loose:
+            assert oracle.rel_rms(a.double().cpu().numpy(), b.double().cpu().numpy()) <= 1e-4, i
+        else:
+            assert torch.equal(a, b), i
 
 
 def paged_calls(gcs, dc, d, segment_len):

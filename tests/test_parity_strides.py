@@ -44,8 +44,8 @@ def fused_views(x_list, pad=0):
 @pytest.mark.parametrize("deterministic", [False, True])
 def test_prefill_strided_layouts_match_contiguous(gcs_lib, name, deterministic):
     lens, hq, hkv, dqk, dv, gate, sink, window = PREFILL_CASES[name]
-    if deterministic and dqk <= 128:
-        pytest.skip("head dims <= 128 have one backward route")
+    if deterministic and dqk == 64:
+        pytest.skip("head dim 64 has one backward route")
     case = make_prefill(lens, hq, hkv, dqk, dv, seed=700 + dqk + dv, gate=gate, sink=sink, window=window)
     d = to_dev(case)
     ms = max(case.seqlens)
@@ -74,7 +74,8 @@ def test_prefill_strided_layouts_match_contiguous(gcs_lib, name, deterministic):
     assert torch.equal(lse, lse_ref)
     # the padding between heads is untouched
     assert torch.isnan(obuf[:, :, dv:].float()).all()
-    exact = deterministic or (dqk <= 128 and dv <= 128)
+    # fp32 reduce-adds of dQ and the dS row sums (single pass at 128, reduce-add route above)
+    exact = deterministic or dqk == 64
     for n, got, ref in zip(("dq", "dk", "dv", "dlog_gate", "dsink"), grads, g_ref):
         if ref is None:
             assert got is None
