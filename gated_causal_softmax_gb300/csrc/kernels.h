@@ -60,6 +60,8 @@ struct BwdParams {
 struct BwdMaps {
   CUtensorMap q, k, v, dout;   // 3-D bf16 maps {dim, heads, tokens}, 128-B swizzle (q, dout: 64-row boxes)
   CUtensorMap q128, dout128;   // q, dout with 128-row boxes (dQ pass)
+  CUtensorMap dq_acc;          // fp32 dQ accumulator {dqk, heads, tokens}, box 128 x 1 x 64, no swizzle
+                               // (single-pass route only)
 };
 
 cudaError_t launch_prefill_bwd(const BwdParams& p, const BwdMaps& maps, int num_kv_tiles, cudaStream_t s);

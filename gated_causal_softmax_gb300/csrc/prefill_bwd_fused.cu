@@ -10,8 +10,8 @@
 //     dV  += P^T dO      (A = P^T, bf16 over the consumed S^T in TMEM)
 //     dK  += dS^T Q      (A = dS^T, bf16 over the consumed dP^T in TMEM)
 //     dQ^T = K^T dS^T    (A = the resident K tile read MN-major, B = dS^T in shared memory)
-// and dQ^T is reduce-added in fp32 into the caller's zeroed buffer, plus the fp32 row and
-// column sums of dS (gate and sink gradients).
+// and dQ is reduce-added in fp32 into a zeroed buffer, plus the fp32 row and column sums of dS
+// (gate and sink gradients).
 //
 // TMEM (512 columns): S^T | dP^T, then dQ^T of the same step | dV | dK.  The issue order
 //     dV(s), S^T(s+1), dK(s), dQ^T(s), [dQ^T(s) read out], dP^T(s+1), dV(s+1), ...
@@ -21,10 +21,18 @@
 // loaded dQ^T(s).  dS^T reaches shared memory in the dO tile of its own step, which dV(s) and
 // dP^T(s) have finished reading by then (dv_done), so the kernel needs no extra tile.
 //
-// Warp roles (384 threads): warp 0 TMA producer, warp 1 tcgen05 issuer, warps 2-3 idle, warps
-// 4-7 and 8-11 the two halves (query columns 0-63, 64-127) of every step; they also read dQ^T
-// out (TMEM lane = head dim, one fp32 reduce-add per query column and lane, 128 contiguous bytes
-// per warp instruction).
+// dQ leaves through shared memory: once dQ^T(s) is in TMEM the two softmax warpgroups each load
+// their 64 query columns (TMEM lane = head dim) and write them as 64 rows x 128 dims of fp32
+// (32 KB) into a tile no MMA reads any more -- warpgroup 0 into the dO(s) tile, warpgroup 1
+// into the Q(s) tile -- and a tiled bulk reduce-add (fp32 add in L2) sends each block to the
+// dQ accumulator.  The bulk operations are issued and awaited by warps 2 and 3, which then
+// hand the tile back to the producer, so the softmax warps never wait for them.  Query rows of
+// a block that lie past the sequence hold exact zeros (their probabilities are 0), so adding
+// them to the next sequence's rows changes nothing; rows past the tensor are clipped.
+//
+// Warp roles (384 threads): warp 0 TMA producer, warp 1 tcgen05 issuer, warps 2-3 the dQ bulk
+// reduce-adds of warpgroups 0 and 1, warps 4-7 and 8-11 the two halves (query columns 0-63,
+// 64-127) of every step.
 #include "kernels.h"
 #include "sm103_ptx.cuh"
 #include "tiles.cuh"
@@ -103,7 +111,7 @@ __device__ __forceinline__ float warp_column_sums(float* v, int lane) {
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_bwd_fused_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                             const BwdParams p) {
+                             const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
 
   TileRef tr;
@@ -128,9 +136,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint64_t* kv_full = bars + 0;
   uint64_t* q_full = bars + 1;      // [kNQ] Q tile landed
-  uint64_t* q_empty = bars + 4;     // [kNQ] dK of its step retired
+  uint64_t* q_empty = bars + 4;     // [kNQ] dK of its step retired and the dQ block staged there sent
   uint64_t* do_full = bars + 7;     // [kNDO] dO tile and vectors landed
-  uint64_t* do_empty = bars + 9;    // [kNDO] dQ^T of its step retired (the buffer held dS^T)
+  uint64_t* do_empty = bars + 9;    // [kNDO] the dQ block staged in it sent (after dS^T and dO uses)
   uint64_t* s_full = bars + 11;     // S^T written
   uint64_t* dp_full = bars + 12;    // dP^T written
   uint64_t* p_ready = bars + 13;    // P^T stored in TMEM (8 warps)
@@ -141,6 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* dq_read = bars + 18;    // dQ^T loaded by the 8 softmax warps
   uint64_t* all_done = bars + 19;   // every MMA of the CTA retired (epilogue)
   uint64_t* drain = bars + 20;
+  uint64_t* stage_full = bars + 21;  // [2] a warpgroup's dQ block written to shared memory (4 warps)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
   const Abort ab{abort_flag, p.status};
@@ -166,6 +175,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(dq_read, 8);
     mbar_init(all_done, 1);
     mbar_init(drain, 1);
+    mbar_init(&stage_full[0], 4);
+    mbar_init(&stage_full[1], 4);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -279,8 +290,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < 8; ++k)
           mma_ss(tmem + T_DP, dKmn0 + 128 * k, dDOmn0 + db * kTile16 + 128 * k, idDQ, k > 0 ? 1u : 0u);
         mma_commit(dq_full);
-        mma_commit(&q_empty[qb]);
-        mma_commit(&do_empty[db]);
         if (more) {
           // dQ^T(s) loaded by the softmax warps, dO(s+1) landed
           ok = wait_bars(ab, dq_read, s & 1, &do_full[(s + 1) % kNDO], ((s + 1) / kNDO) & 1);
@@ -294,6 +303,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(drain);
         mbar_wait(drain, 0, nullptr);
       }
+    } else if (warp >= 2 && lane == 0) {
+      // ---------------------------------------------------------- dQ bulk reduce-adds
+      // warp 2: warpgroup 0's blocks (dO tiles), warp 3: warpgroup 1's blocks (Q tiles)
+      const int wg = warp - 2;
+      prefetch_tmap(&tmDQ);
+      for (int s = 0; s < nsteps; ++s) {
+        const int qb = s % kNQ, db = s % kNDO;
+        const int h = kvh * group + s / n_it;
+        const int cb = (it_lo + s % n_it) * kBM + 64 * wg;
+        if (!wait_bar(&stage_full[wg], s & 1, ab)) break;
+        const uint8_t* src = smem + (wg == 0 ? OFF_DO + db * kTile : OFF_Q + qb * kTile);
+        if (cb < len) tma_reduce_add_3d(&tmDQ, src, 0, h, seq_start + cb);
+        bulk_commit_group();
+        bulk_wait_group_read0();
+        mbar_arrive(wg == 0 ? &do_empty[db] : &q_empty[qb]);
+      }
+      bulk_wait_group0();
     }
     __syncwarp();
   } else {
@@ -416,7 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (i < len) red_add_f32(p.dg_row + (size_t)h * p.total + seq_start + i, sum);
         }
       }
-      // ---- dQ^T(s): lane r = head dim r, this warpgroup's 64 query columns
+      // ---- dQ^T(s): lane r = head dim r, this warpgroup's 64 query columns, staged as
+      // [64 query rows][128 dims] fp32 for the bulk reduce-add (warp 2 + wg sends it)
       ok = wait_bar(dq_full, s & 1, ab);
       if (!ok) break;
       tc_fence_after();
@@ -428,13 +455,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(dq_read);
       {
-        float* base = p.dq_acc + ((size_t)(seq_start + cb) * p.hq + h) * kD + r;
-        const size_t row_stride = (size_t)p.hq * kD;
-        const int nrows = min(64, len - cb);
+        float* stage = reinterpret_cast<float*>(smem + (wg == 0 ? OFF_DO + db * kTile : OFF_Q + (s % kNQ) * kTile));
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (c < nrows) red_add_f32(base + c * row_stride, __uint_as_float(dq[c]) * p.scale);
+        for (int c = 0; c < 64; ++c) stage[c * kD + r] = __uint_as_float(dq[c]) * p.scale;
       }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&stage_full[wg]);
     }
     if (ok && cur_h >= 0 && has_gate && jl < len)
       red_add_f32(p.dg_col + (size_t)cur_h * p.total + seq_start + jl, dgcol);
@@ -489,7 +516,7 @@ cudaError_t launch_prefill_bwd_fused(const BwdParams& p, const BwdMaps& maps, in
   auto kern = prefill_bwd_fused_kernel;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<dim3(p.hkv, num_kv_tiles), kThreads, SMEM, s>>>(maps.q128, maps.k, maps.v, maps.dout128, p);
+  kern<<<dim3(p.hkv, num_kv_tiles), kThreads, SMEM, s>>>(maps.q128, maps.k, maps.v, maps.dout128, maps.dq_acc, p);
   return cudaGetLastError();
 }
 

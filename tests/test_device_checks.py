@@ -128,15 +128,18 @@ def test_broken_cu_seqlens_is_caught(checked, name):
     torch.cuda.synchronize()
     assert gcs.get_device_status() == INVALID
     assert bool((o == SENTINEL).all()) and bool((lse == SENTINEL).all())
-    # a checked backward: dQ (two-pass route), dK, dV and d log_gate untouched
-    dq, dk, dv = (torch.full_like(t, SENTINEL) for t in (d["q"], d["k"], d["v"]))
-    dg = torch.full_like(d["g"], SENTINEL)
-    gcs.attn_bwd(d["q"], d["k"], d["v"], ok[0], ok[1], d["do"], bad, 200, case.scale, 0, d["g"], d["s"], dq=dq,
-                 dk=dk, dv=dv, dlog_gate=dg)
-    torch.cuda.synchronize()
-    assert gcs.get_device_status() == INVALID
-    for t in (dq, dk, dv, dg):
-        assert bool((t == SENTINEL).all())
+    # a checked backward: dQ (two-pass route), dK, dV and d log_gate untouched; the single
+    # pass converts its zeroed dQ accumulator, so there dQ holds zeros
+    for det in (True, False):
+        dq, dk, dv = (torch.full_like(t, SENTINEL) for t in (d["q"], d["k"], d["v"]))
+        dg = torch.full_like(d["g"], SENTINEL)
+        gcs.attn_bwd(d["q"], d["k"], d["v"], ok[0], ok[1], d["do"], bad, 200, case.scale, 0, d["g"], d["s"], dq=dq,
+                     dk=dk, dv=dv, dlog_gate=dg, deterministic=det)
+        torch.cuda.synchronize()
+        assert gcs.get_device_status() == INVALID
+        for t in (dk, dv, dg):
+            assert bool((t == SENTINEL).all())
+        assert bool((dq == SENTINEL).all()) if det else bool((dq == 0).all())
 
 
 def padded_paged(gcs, dc, d, max_q_len, max_seq_len, segment_len, bt=None, sl=None, cq=None):
