@@ -99,12 +99,14 @@ struct CacheLayout {
 
 // 4-D byte map of a paged fp8 cache, dims in increasing stride order: {128 B, slot, kv head,
 // block}, or {128 B, kv head, slot, block} when the kv head is the inner one.  One box is one
-// page of one kv head (16 slots x 128 B, 128-byte swizzle), the same tile either way.
-bool make_page_map_u8(CUtensorMap* m, const void* base, int num_blocks, int hkv, const CacheLayout& l) {
+// 16-slot page of one kv head (16 x 128 B, 128-byte swizzle), the same tile either way.
+bool make_page_map_u8(CUtensorMap* m, const void* base, int num_blocks, int hkv, int block_size,
+                      const CacheLayout& l) {
   auto enc = encode_fn();
   if (!enc) return false;
   const bool hi = l.head_inner();
-  cuuint64_t dims[4] = {128, (cuuint64_t)(hi ? hkv : 16), (cuuint64_t)(hi ? 16 : hkv), (cuuint64_t)num_blocks};
+  cuuint64_t dims[4] = {128, (cuuint64_t)(hi ? hkv : block_size), (cuuint64_t)(hi ? block_size : hkv),
+                        (cuuint64_t)num_blocks};
   cuuint64_t strides[3] = {(cuuint64_t)(hi ? l.hs : l.ss), (cuuint64_t)(hi ? l.ss : l.hs), (cuuint64_t)l.bs};
   cuuint32_t box[4] = {128, hi ? 1u : 16u, hi ? 16u : 1u, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
@@ -582,8 +584,12 @@ static int check_decode(const gcs_decode_args* a) {
   }
   // per-token scales are only read on decode / short-query shapes (a prefill shape is rejected)
   if (a->max_q_len > 4) return GCS_ERR_UNSUPPORTED;
-  if (a->d != 128 || a->block_size != 16 || a->hq != 16 * a->hkv) return GCS_ERR_UNSUPPORTED;
-  if (a->segment_len % a->block_size != 0) return GCS_ERR_UNSUPPORTED;
+  // head dim 128; GQA groups of 16 or 8 query heads; blocks of whole 16-token pages
+  if (a->d != 128 || (a->hq != 16 * a->hkv && a->hq != 8 * a->hkv)) return GCS_ERR_UNSUPPORTED;
+  // cache blocks of 16 x 2^k tokens (16, 32, 64, 128, ...)
+  if (a->block_size < 16 || a->block_size > 4096 || (a->block_size & (a->block_size - 1)) != 0)
+    return GCS_ERR_UNSUPPORTED;
+  if (a->segment_len % 16 != 0) return GCS_ERR_UNSUPPORTED;
   if ((long long)a->max_blocks_per_req * a->block_size < a->max_seq_len) return GCS_ERR_INVALID_ARG;
   if (!aligned16(a->k_cache) || !aligned16(a->v_cache) || !aligned16(a->q)) return GCS_ERR_INVALID_ARG;
   if (a->window < 0) return GCS_ERR_INVALID_ARG;
@@ -661,6 +667,10 @@ static void fill_paged_params(const gcs_decode_args* a, void* out, int* status, 
   p.kv_hs = cl.hs;
   p.kv_ss = cl.ss;
   p.kv_head_inner = cl.head_inner() ? 1 : 0;
+  p.block_size = a->block_size;
+  p.log2_block_pages = 0;
+  while ((16 << p.log2_block_pages) < a->block_size) ++p.log2_block_pages;
+  p.group = a->hq / a->hkv;
   p.part_acc = nullptr;
   p.part_ml = nullptr;
   p.status = status;
@@ -733,7 +743,7 @@ int attn_decode_paged(const gcs_decode_args* a, void* out, void* workspace, size
   DecodeParams p;
   fill_paged_params(a, out, status, p);
   p.max_segs = max_segs;
-  p.seg_pages = a->segment_len / a->block_size;
+  p.seg_pages = a->segment_len / 16;
   p.part_acc = static_cast<float*>(workspace);
   p.part_ml = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + round_up(units * rows * 128 * sizeof(float)));
   DecodeMaps maps;
@@ -741,8 +751,8 @@ int attn_decode_paged(const gcs_decode_args* a, void* out, void* workspace, size
   if (a->kv_format == GCS_KV_FP8_E4M3) {
     CacheLayout cl;
     cache_layout(a, &cl);
-    if (!make_page_map_u8(&maps.k, a->k_cache, a->num_blocks, a->hkv, cl) ||
-        !make_page_map_u8(&maps.v, a->v_cache, a->num_blocks, a->hkv, cl))
+    if (!make_page_map_u8(&maps.k, a->k_cache, a->num_blocks, a->hkv, a->block_size, cl) ||
+        !make_page_map_u8(&maps.v, a->v_cache, a->num_blocks, a->hkv, a->block_size, cl))
       return GCS_ERR_CUDA;
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -844,8 +854,8 @@ int attn_prefill_paged(const gcs_decode_args* a, void* out, void* workspace, siz
   DecodeMaps maps;
   CacheLayout cl;
   cache_layout(a, &cl);
-  if (!make_page_map_u8(&maps.k, a->k_cache, a->num_blocks, a->hkv, cl) ||
-      !make_page_map_u8(&maps.v, a->v_cache, a->num_blocks, a->hkv, cl))
+  if (!make_page_map_u8(&maps.k, a->k_cache, a->num_blocks, a->hkv, a->block_size, cl) ||
+      !make_page_map_u8(&maps.v, a->v_cache, a->num_blocks, a->hkv, a->block_size, cl))
     return GCS_ERR_CUDA;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (chk) {

@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(kCheckThreads) check_paged_kernel(
     }
     if (ql == 0) continue;
     const int first_key = window > 0 ? max(0, L - static_cast<int>(ql) - window + 1) : 0;
-    const int p0 = (first_key / 128) * (128 / block_size);
+    const int p0 = (first_key / 128) * 128 / block_size;  // block holding the first key of that tile
     const int np = (L + block_size - 1) / block_size;  // <= max_blocks: L <= max_seq_len
     for (int pg = p0 + lane; pg < np; pg += 32) {
       const int blk = __ldg(table + (size_t)r * max_blocks + pg);

@@ -10,11 +10,15 @@
 // decode_split_kernel: one CTA per (segment, kv head, request).  Warp 0 streams pages
 // (K 2 KB, V 2 KB, 16 K scales, 16 V scales) into a 16-stage shared-memory ring, eight pages
 // per round: each of its 32 lanes issues one of the round's 32 copies (a copy is a
-// per-thread instruction, and one lane issuing them all serially was the bottleneck).  The
+// per-thread instruction, and one lane issuing them all serially was the bottleneck).  A
+// "page" here is 16 tokens: a cache block of block_size = 16 k tokens holds k of them at
+// consecutive slots.  The
 // fp8 K and V pages come by tensor copy with the 128-byte swizzle, so the consumers' 16-B
 // reads of four rows at one column, or of two columns of two rows, hit eight different bank
-// groups; the scales (and gates) come by plain bulk copy.  Warps 1..4 each own one query position (16 query heads of the GQA
-// group = one m16 MMA tile) and a share of the pages (the query's MMA fragments are kept in
+// groups; the scales (and gates) come by plain bulk copy.  Warps 1..4 each own one m16 MMA
+// tile of query rows -- the 16 query heads of a GQA group of 16 at one query position, or the
+// 8 heads of a group of 8 at two consecutive positions (rows 0-7 and 8-15) -- and a share of
+// the pages (the query's MMA fragments are kept in
 // shared memory, one copy per query position, so the loop runs without register spills);
 // fp8 -> f16 conversion is exact,
 // QK^T and PV run on mma.sync m16n8k16 with fp32 accumulation, softmax in fp32 (log2
@@ -39,7 +43,7 @@ std::mutex g_noalloc_mu;
 
 constexpr int kPage = 16;
 constexpr int kD = 128;
-constexpr int kGroup = 16;
+constexpr int kRows = 16;  // rows of an m16 tile; partial rows per (unit, query position)
 // Ring layout: a K | V ring of NST pages (fp8: 2 KB + 2 KB, rows of 128 B stored with the
 // 128-byte swizzle of the tensor copy; bf16: 4 KB + 4 KB, linear) and, beside it, a ring of
 // the pages' small vectors: K and V scales (per-token fp8, 64 B each) and, with the decoding
@@ -117,8 +121,8 @@ __device__ __forceinline__ uint32_t bf16pair_to_f16x2(uint32_t w) {
 
 // KVF: 0 fp8 e4m3 codes, 1 bf16 values.  PT: one K and one V scale for the whole cache (fp8).
 // FEAT: the decoding features (gates from g_cache when given, the window; the sink is the
-// combine's).
-template <int KVF, bool PT, bool FEAT>
+// combine's).  G: query heads per kv head, 16 or 8.
+template <int KVF, bool PT, bool FEAT, int G>
 __global__ void __launch_bounds__(kThreads, 3)
     decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const DecodeParams p) {
@@ -138,6 +142,9 @@ __global__ void __launch_bounds__(kThreads, 3)
   const int npages = (L + kPage - 1) / kPage;
   int pb = seg * p.seg_pages;
   if (pb >= npages || ql < 1 || ql > 4) return;
+  constexpr int ppt = kRows / G;  // query positions per m16 tile: 1 or 2
+  const int ntile = (ql + ppt - 1) / ppt;
+  const int lbp = p.log2_block_pages;  // cache blocks hold 2^lbp 16-token pages
   const int pend = min(pb + p.seg_pages, npages);
   if (FEAT && p.window > 0) {
     // pages before the earliest key any query row of the request sees are skipped; a segment
@@ -148,13 +155,13 @@ __global__ void __launch_bounds__(kThreads, 3)
   }
   const int np = pend - pb;
   const bool has_gate = FEAT && p.g_cache != nullptr;
-  const int ng = 4 / ql;  // page groups
+  const int ng = 4 / ntile;  // page groups
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNST; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], ql);
+      mbar_init(&empty[i], ntile);
     }
     abort_flag_s = 0;
     fence_mbar_init();
@@ -166,17 +173,17 @@ __global__ void __launch_bounds__(kThreads, 3)
     // ------------------------------------------------------------ page producer
     // lane = kBatch * kind + page within the round; kind 0: K, 1: V, then (per-token fp8)
     // 2: K scales, 3: V scales, then (features) the gates of the group's query heads
-    const int32_t* trow = p.block_table + (size_t)r * p.max_blocks + pb;
+    const int32_t* trow = p.block_table + (size_t)r * p.max_blocks;
     const int pl = lane & (kBatch - 1), kind = lane / kBatch;
     const int g_kind = C::SCALES ? 4 : 2;
     const bool is_g = FEAT && kind == g_kind;
-    const uint32_t bytes = kind < 2 ? C::KB : is_g ? 1024 : kPage * 4;
+    const uint32_t bytes = kind < 2 ? C::KB : is_g ? G * kPage * 4 : kPage * 4;
     const uint32_t dst_off = kind < 2 ? kind * C::KB : is_g ? C::G_OFF : (kind - 2) * 64;
     if (KVF == 0 && lane == 0) {
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
     }
-    const uint32_t tx = 2 * C::KB + (C::SCALES ? 2 * kPage * 4 : 0) + (has_gate ? 1024 : 0);
+    const uint32_t tx = 2 * C::KB + (C::SCALES ? 2 * kPage * 4 : 0) + (has_gate ? G * kPage * 4 : 0);
     for (int base = 0; base < np; base += kBatch) {
       const int i = base + pl;
       const bool act = i < np && kind < kKinds && (!is_g || has_gate);
@@ -187,15 +194,17 @@ __global__ void __launch_bounds__(kThreads, 3)
       if (act && kind == 0) mbar_expect_tx(&full[stage], tx);
       __syncwarp();
       if (act) {
-        const int blk = __ldg(trow + i);
-        const size_t slot0 = ((size_t)blk * p.hkv + kvh) * kPage;
+        const int pg = pb + i;
+        const int blk = __ldg(trow + (pg >> lbp)), sub = (pg & ((1 << lbp) - 1)) * kPage;  // block, first slot
+        const size_t slot0 = ((size_t)blk * p.hkv + kvh) * p.block_size + sub;
         if (KVF == 0 && kind < 2) {
           // fp8 K or V page: one 16-slot x 128-B box of the cache's 4-D map (dims in stride order)
-          tma_load_4d(kv + stage * C::KV + dst_off, kind ? &tmV : &tmK, &full[stage], 0, p.kv_head_inner ? kvh : 0,
-                      p.kv_head_inner ? 0 : kvh, blk);
+          tma_load_4d(kv + stage * C::KV + dst_off, kind ? &tmV : &tmK, &full[stage], 0, p.kv_head_inner ? kvh : sub,
+                      p.kv_head_inner ? sub : kvh, blk);
         } else if (kind < 2) {
           // bf16 K or V page: one 4 KB copy when its 16 rows are adjacent, else one per row
-          const uint8_t* src = (kind == 0 ? p.k_cache : p.v_cache) + (size_t)blk * p.kv_bs + (size_t)kvh * p.kv_hs;
+          const uint8_t* src = (kind == 0 ? p.k_cache : p.v_cache) + (size_t)blk * p.kv_bs + (size_t)kvh * p.kv_hs +
+                               (size_t)sub * p.kv_ss;
           uint8_t* dst = kv + stage * C::KV + dst_off;
           if (p.kv_ss == C::KB / kPage) {
             bulk_load(dst, src, bytes, &full[stage]);
@@ -203,11 +212,18 @@ __global__ void __launch_bounds__(kThreads, 3)
             for (int rr = 0; rr < kPage; ++rr)
               bulk_load(dst + rr * (C::KB / kPage), src + rr * p.kv_ss, C::KB / kPage, &full[stage]);
           }
+        } else if (is_g) {
+          // the group's G heads x 16 slots of gates: adjacent when a block is one page
+          const float* src = p.g_cache + ((size_t)blk * p.hq + kvh * G) * p.block_size + sub;
+          if (lbp == 0) {
+            bulk_load(aux + stage * C::AUX + dst_off, src, bytes, &full[stage]);
+          } else {
+            for (int hh = 0; hh < G; ++hh)
+              bulk_load(aux + stage * C::AUX + dst_off + hh * kPage * 4, src + (size_t)hh * p.block_size, kPage * 4,
+                        &full[stage]);
+          }
         } else {
-          const void* src = is_g ? static_cast<const void*>(p.g_cache + ((size_t)blk * p.hq + kvh * kGroup) * kPage)
-                            : kind == 2 ? static_cast<const void*>(p.k_scale + slot0)
-                                        : static_cast<const void*>(p.v_scale + slot0);
-          bulk_load(aux + stage * C::AUX + dst_off, src, bytes, &full[stage]);
+          bulk_load(aux + stage * C::AUX + dst_off, (kind == 2 ? p.k_scale : p.v_scale) + slot0, bytes, &full[stage]);
         }
       }
     }
@@ -216,10 +232,16 @@ __global__ void __launch_bounds__(kThreads, 3)
 
   // -------------------------------------------------------------- consumers
   const int cw = warp - 1;
-  const int mt = cw % ql, grp = cw / ql;
+  const int mt = cw % ntile, grp = cw / ntile;
   const bool active = grp < ng;
   const int g = lane >> 2, tq = lane & 3;
-  const int lastk = L - ql + mt;  // last key visible to this query position
+  // tile rows g (A) and g + 8 (B): (query position, head of the group) = (mt, g) and (mt, g + 8)
+  // for a group of 16; (2 mt, g) and (2 mt + 1, g) for a group of 8 (row B unused past q_len)
+  const int posA = mt * ppt, posB = mt * ppt + ppt - 1;
+  const int headA = g, headB = ppt == 2 ? g : g + 8;
+  const bool validB = posB < ql;
+  const int lastkA = L - ql + posA;                  // last key visible to row A
+  const int lastkB = ppt == 1 ? lastkA : validB ? L - ql + posB : -1;  // and to row B (none past q_len)
   const float sl2 = p.scale * kLog2e;
   float o[16][4];
 #pragma unroll
@@ -232,13 +254,14 @@ __global__ void __launch_bounds__(kThreads, 3)
   if (active && grp == 0) {
     uint32_t qa[8][4];
     {
-      const uint16_t* q0p = p.q + (size_t)(q_begin + mt) * p.q_ts + (size_t)(kvh * kGroup + g) * p.q_hs + 32 * tq;
-      const uint16_t* q1p = q0p + 8 * p.q_hs;
+      const uint16_t* q0p = p.q + (size_t)(q_begin + posA) * p.q_ts + (size_t)(kvh * G + headA) * p.q_hs + 32 * tq;
+      const uint16_t* q1p =
+          p.q + (size_t)(q_begin + min(posB, ql - 1)) * p.q_ts + (size_t)(kvh * G + headB) * p.q_hs + 32 * tq;
       uint32_t w0[16], w1[16];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const uint4 a = __ldg(reinterpret_cast<const uint4*>(q0p) + j);
-        const uint4 b = __ldg(reinterpret_cast<const uint4*>(q1p) + j);
+        const uint4 b = validB ? __ldg(reinterpret_cast<const uint4*>(q1p) + j) : make_uint4(0u, 0u, 0u, 0u);
         w0[4 * j] = a.x; w0[4 * j + 1] = a.y; w0[4 * j + 2] = a.z; w0[4 * j + 3] = a.w;
         w1[4 * j] = b.x; w1[4 * j + 1] = b.y; w1[4 * j + 2] = b.z; w1[4 * j + 3] = b.w;
       }
@@ -259,13 +282,14 @@ __global__ void __launch_bounds__(kThreads, 3)
   if (active) {
     // one K and one V scale for the whole cache (fp8 per-tensor)
     const float kst = PT ? __ldg(p.k_scale) : 1.f, vst = PT ? __ldg(p.v_scale) : 1.f;
-    // the query row's own cumulative gate (log2 units) for heads g and g + 8 of the group
+    // each row's own cumulative gate (log2 units) at its position
     float gq0 = 0.f, gq1 = 0.f;
     if (has_gate) {
-      const int blk = __ldg(p.block_table + (size_t)r * p.max_blocks + lastk / kPage);
-      const float* gp = p.g_cache + ((size_t)blk * p.hq + kvh * kGroup) * kPage + lastk % kPage;
-      gq0 = __ldg(gp + g * kPage) * kLog2e;
-      gq1 = __ldg(gp + (g + 8) * kPage) * kLog2e;
+      const int32_t* trow = p.block_table + (size_t)r * p.max_blocks;
+      const int kB = validB ? lastkB : lastkA;  // row B past q_len reads row A's entry (unused)
+      const int bA = __ldg(trow + lastkA / p.block_size), bB = __ldg(trow + kB / p.block_size);
+      gq0 = __ldg(p.g_cache + ((size_t)bA * p.hq + kvh * G + headA) * p.block_size + lastkA % p.block_size) * kLog2e;
+      gq1 = __ldg(p.g_cache + ((size_t)bB * p.hq + kvh * G + headB) * p.block_size + kB % p.block_size) * kLog2e;
     }
     for (int i = grp; i < np; i += ng) {
       const int stage = i % kNST;
@@ -279,8 +303,9 @@ __global__ void __launch_bounds__(kThreads, 3)
         const float* gs = reinterpret_cast<const float*>(sa + C::G_OFF);
 #pragma unroll
         for (int rw2 = 0; rw2 < 2; ++rw2) {
-          const float2 a = *reinterpret_cast<const float2*>(gs + (g + 8 * rw2) * kPage + 2 * tq);
-          const float2 b = *reinterpret_cast<const float2*>(gs + (g + 8 * rw2) * kPage + 8 + 2 * tq);
+          const int hd = rw2 ? headB : headA;
+          const float2 a = *reinterpret_cast<const float2*>(gs + hd * kPage + 2 * tq);
+          const float2 b = *reinterpret_cast<const float2*>(gs + hd * kPage + 8 + 2 * tq);
           gk[rw2][0] = a.x; gk[rw2][1] = a.y; gk[rw2][2] = b.x; gk[rw2][3] = b.y;
         }
       }
@@ -346,16 +371,19 @@ __global__ void __launch_bounds__(kThreads, 3)
       float x[2][4];  // [row g / g+8][column]
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        bool vis = tk[c] <= lastk;
-        if (FEAT && p.window > 0) vis = vis && tk[c] > lastk - p.window;
+        bool visA = tk[c] <= lastkA, visB = tk[c] <= lastkB;
+        if (FEAT && p.window > 0) {
+          visA = visA && tk[c] > lastkA - p.window;
+          visB = visB && tk[c] > lastkB - p.window;
+        }
         const float sa = (c < 2) ? s0[c] : s1[c - 2];
         const float sb = (c < 2) ? s0[c + 2] : s1[c];
         if (FEAT) {  // + G_i - G_j
-          x[0][c] = vis ? fmaf(sa, sl2 * ks[c], fmaf(-gk[0][c], kLog2e, gq0)) : neg_inf();
-          x[1][c] = vis ? fmaf(sb, sl2 * ks[c], fmaf(-gk[1][c], kLog2e, gq1)) : neg_inf();
+          x[0][c] = visA ? fmaf(sa, sl2 * ks[c], fmaf(-gk[0][c], kLog2e, gq0)) : neg_inf();
+          x[1][c] = visB ? fmaf(sb, sl2 * ks[c], fmaf(-gk[1][c], kLog2e, gq1)) : neg_inf();
         } else {
-          x[0][c] = vis ? sa * sl2 * ks[c] : neg_inf();
-          x[1][c] = vis ? sb * sl2 * ks[c] : neg_inf();
+          x[0][c] = visA ? sa * sl2 * ks[c] : neg_inf();
+          x[1][c] = visB ? sb * sl2 * ks[c] : neg_inf();
         }
       }
       float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[0][2], x[0][3]));
@@ -488,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     named_bar_sync(1, 128);
     if (active && grp == 0) {
       for (int gg = 1; gg < ng; ++gg) {
-        const float* other = red + (gg * ql + mt) * (16 * 130);
+        const float* other = red + (gg * ntile + mt) * (16 * 130);
         const float om0 = other[g * 130 + 128], ol0 = other[g * 130 + 129];
         const float om1 = other[(g + 8) * 130 + 128], ol1 = other[(g + 8) * 130 + 129];
         const float n0 = fmaxf(m0, om0), n1 = fmaxf(m1, om1);
@@ -513,10 +541,13 @@ __global__ void __launch_bounds__(kThreads, 3)
   if (active && grp == 0) {
     constexpr float kOut = KVF == 0 ? kInvPScale : 1.f;  // the fp8 path carries P scaled by 2^8
     const size_t unit = ((size_t)r * p.max_segs + seg) * p.hkv + kvh;
-    const int rows = p.max_q_len * kGroup;
-    const size_t row0 = unit * rows + mt * kGroup + g;
+    const int rows = p.max_q_len * kRows;
+    const size_t row0 = unit * rows + posA * G + headA;
+    // row B past q_len (group of 8, odd q_len) writes its all-empty result into its own slot,
+    // which the combine never reads
+    const size_t row1 = unit * rows + posB * G + headB;
     float4* d0 = reinterpret_cast<float4*>(p.part_acc + row0 * kD + 32 * tq);
-    float4* d1 = reinterpret_cast<float4*>(p.part_acc + (row0 + 8) * kD + 32 * tq);
+    float4* d1 = reinterpret_cast<float4*>(p.part_acc + row1 * kD + 32 * tq);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       d0[k] = make_float4(o[4 * k][0] * kOut, o[4 * k + 1][0] * kOut, o[4 * k + 2][0] * kOut,
@@ -530,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     }
     if (tq == 0) {
       reinterpret_cast<float2*>(p.part_ml)[row0] = make_float2(m0, l0);
-      reinterpret_cast<float2*>(p.part_ml)[row0 + 8] = make_float2(m1, l1);
+      reinterpret_cast<float2*>(p.part_ml)[row1] = make_float2(m1, l1);
     }
   }
 }
@@ -546,9 +577,11 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
   const int L = __ldg(p.seq_lens + r);
   const int npages = (L + kPage - 1) / kPage;
   const int nseg = (npages + p.seg_pages - 1) / p.seg_pages;
+  const int G = p.group;
   const int hh = threadIdx.x >> 4, d0 = (threadIdx.x & 15) * 8;
-  const int rows = p.max_q_len * kGroup;
-  const int row = t * kGroup + hh;
+  if (hh >= G) return;
+  const int rows = p.max_q_len * kRows;
+  const int row = t * G + hh;
   auto unit_row = [&](int s) { return ((((size_t)r * p.max_segs + s) * p.hkv + kvh) * rows + row); };
   const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
   // segments wholly before every window of the request were not written (see the split kernel)
@@ -556,7 +589,7 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
   float M = neg_inf();
   for (int s = s_begin; s < nseg; ++s) M = fmaxf(M, ml[unit_row(s)].x);
   // the sink logit (log2 units) joins the max and, once, the denominator
-  const float sg = p.sink ? __ldg(p.sink + kvh * kGroup + hh) * kLog2e : neg_inf();
+  const float sg = p.sink ? __ldg(p.sink + kvh * G + hh) * kLog2e : neg_inf();
   M = fmaxf(M, sg);
   float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   float den = p.sink ? ex2(sg - M) : 0.f;
@@ -575,8 +608,7 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
   outv.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
   outv.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
   outv.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-  *reinterpret_cast<uint4*>(p.out + (size_t)(q_begin + t) * p.out_ts + (size_t)(kvh * kGroup + hh) * p.out_hs + d0) =
-      outv;
+  *reinterpret_cast<uint4*>(p.out + (size_t)(q_begin + t) * p.out_ts + (size_t)(kvh * G + hh) * p.out_hs + d0) = outv;
 }
 
 }  // namespace
@@ -595,7 +627,9 @@ cudaError_t launch_decode(const DecodeParams& p, const DecodeMaps& maps, cudaStr
   cudaError_t e;
   // the sink alone needs no change in the split kernel (it is the combine's)
   const bool feat = p.g_cache != nullptr || p.window > 0;
-#define GCS_RUN(KVF, PT, F) run(decode_split_kernel<KVF, PT, F>, DecCfg<KVF, PT, F>::SMEM)
+#define GCS_RUN(KVF, PT, F)                                                                         \
+  (p.group == 8 ? run(decode_split_kernel<KVF, PT, F, 8>, DecCfg<KVF, PT, F>::SMEM)                  \
+                : run(decode_split_kernel<KVF, PT, F, 16>, DecCfg<KVF, PT, F>::SMEM))
   if (p.kv_format == 1)
     e = feat ? GCS_RUN(1, false, true) : GCS_RUN(1, false, false);
   else if (p.scale_mode == 1)

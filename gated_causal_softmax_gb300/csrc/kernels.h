@@ -116,6 +116,9 @@ struct DecodeParams {
   long long q_ts, q_hs, out_ts, out_hs;  // element strides
   long long kv_bs, kv_hs, kv_ss;         // byte strides (block, kv head, slot) of both caches
   int kv_head_inner;     // 1: the kv head stride is below the slot stride (fp8 maps order dims so)
+  int block_size;        // tokens per cache block: 16-token pages times a power of two
+  int log2_block_pages;  // log2(block_size / 16)
+  int group;             // query heads per kv head: 16 or 8
   float* part_acc;       // [units, 4*16, 128]
   float* part_ml;        // [units, 4*16, 2]
   int* status;

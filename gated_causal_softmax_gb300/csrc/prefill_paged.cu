@@ -7,9 +7,10 @@
 // attention #1322 (Description: log gates, sliding windows, a sink) apply as in decode.
 //
 // Row t of a request sits at position L - q_len + t and sees keys 0 .. L - q_len + t
-// (bottom-right causal alignment).  A 128-row query tile is 8 positions x the 16 query heads
-// of one kv head (row = 16 * position + head); one CTA takes two tiles (16 positions) and one
-// segment of the context.  With one segment per request the CTA writes the bf16 output (the
+// (bottom-right causal alignment).  A 128-row query tile is 128 / G positions x the G query
+// heads of one kv head (G = 16 or 8; row = G * position + head); one CTA takes two tiles and one
+// segment of the context.  A "page" is 16 tokens; a cache block of block_size = 16 k tokens
+// holds k of them at consecutive slots.  With one segment per request the CTA writes the bf16 output (the
 // sink in its denominator); with several it writes split-K partials (unnormalised
 // accumulator, running max in log2 units and row sum) that the decode combine merges.
 //
@@ -34,9 +35,8 @@ namespace {
 
 constexpr int kPage = 16;
 constexpr int kD = 128;
-constexpr int kGroup = 16;        // query heads per kv head
+constexpr int kRows = 16;         // partial rows per (unit, query position), as in decode
 constexpr int kTileKeys = 128;    // 8 pages
-constexpr int kPosPerTile = 8;    // 8 positions x 16 heads = 128 rows
 constexpr int kThreads = 384;
 constexpr int kStage = 16384;     // one f16 operand stage: 128 rows x 64 dims or 64 keys x 128 dims
 constexpr float kLog2e = 1.4426950408889634f;
@@ -109,7 +109,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q_begin = __ldg(p.cu_q + r);
   const int ql = __ldg(p.cu_q + r + 1) - q_begin;
   const int L = __ldg(p.seq_lens + r);
-  const int pos0 = qp * 2 * kPosPerTile;
+  const int G = p.group, lgG = G == 16 ? 4 : 3;  // query heads per kv head (16 or 8)
+  const int pos_tile = 128 / G;                 // positions of a 128-row query tile
+  const int lbp = p.log2_block_pages;              // cache blocks hold 2^lbp 16-token pages
+  const int pos0 = qp * 2 * pos_tile;
   if (pos0 >= ql) return;
   const int npages = (L + kPage - 1) / kPage;
   const int pb = seg * p.seg_pages;
@@ -123,11 +126,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // key tiles of the segment (index jt, keys key_seg0 + 128 jt ..) that each query tile sees
   int lo[2], hi[2];
   for (int x = 0; x < 2; ++x) {
-    const int px = pos0 + x * kPosPerTile;
+    const int px = pos0 + x * pos_tile;
     lo[x] = 0;
     hi[x] = -1;
     if (px >= ql) continue;
-    const int lk_min = L - ql + px, lk_max = L - ql + min(px + kPosPerTile - 1, ql - 1);
+    const int lk_min = L - ql + px, lk_max = L - ql + min(px + pos_tile - 1, ql - 1);
     if (lk_max >= key_seg0) hi[x] = min(ntile_seg - 1, (lk_max - key_seg0) / kTileKeys);
     const int fk = W > 0 ? max(0, lk_min - W + 1) : 0;
     if (fk > key_seg0) lo[x] = (fk - key_seg0) / kTileKeys;
@@ -138,17 +141,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       hi_t = max(hi_t, hi[x]);
       lo_t = min(lo_t, lo[x]);
     }
-  const size_t rows_per_unit = (size_t)p.max_q_len * kGroup;
+  const size_t rows_per_unit = (size_t)p.max_q_len * kRows;
   const size_t unit = ((size_t)r * p.max_segs + seg) * p.hkv + kvh;
   if (hi_t < 0) {
     // nothing of this segment is visible to these 16 positions: empty partials (weight 0)
     if (!direct) {
-      const int npos = min(2 * kPosPerTile, ql - pos0);
-      const size_t row0 = unit * rows_per_unit + (size_t)pos0 * kGroup;
+      const int npos = min(2 * pos_tile, ql - pos0);
+      const size_t row0 = unit * rows_per_unit + (size_t)pos0 * G;
       float4* acc = reinterpret_cast<float4*>(p.part_acc + row0 * kD);
-      for (int i = threadIdx.x; i < npos * kGroup * (kD / 4); i += blockDim.x) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int i = threadIdx.x; i < npos * G * (kD / 4); i += blockDim.x) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
       float2* ml = reinterpret_cast<float2*>(p.part_ml) + row0;
-      for (int i = threadIdx.x; i < npos * kGroup; i += blockDim.x) ml[i] = make_float2(neg_inf(), 0.f);
+      for (int i = threadIdx.x; i < npos * G; i += blockDim.x) ml[i] = make_float2(neg_inf(), 0.f);
     }
     return;
   }
@@ -231,27 +234,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool okl = wait_bar(kr_empty, par, ab);
         if (!__all_sync(0xffffffffu, okl)) break;
         if (lane == 0)
-          mbar_expect_tx(kr_full, nv * (2048 + (per_token ? 128 : 0) + (has_gate ? 1024 : 0)));
+          mbar_expect_tx(kr_full, nv * (2048 + (per_token ? 128 : 0) + (has_gate ? G * kPage * 4 : 0)));
         __syncwarp();
-        const int blk = pl < nv ? __ldg(trow + pg0 + pl) : 0;
-        const size_t slot0 = ((size_t)blk * p.hkv + kvh) * kPage;
+        const int pg = pg0 + pl;
+        const int blk = pl < nv ? __ldg(trow + (pg >> lbp)) : 0;
+        const int sub = (pg & ((1 << lbp) - 1)) * kPage;  // first slot of the page in its block
+        const size_t slot0 = ((size_t)blk * p.hkv + kvh) * p.block_size + sub;
         if (pl < nv) {
-          if (kind == 0)
-            tma_load_4d(kraw + pl * 2048, &tmK, kr_full, 0, p.kv_head_inner ? kvh : 0, p.kv_head_inner ? 0 : kvh, blk);
-          else if (kind == 1 && per_token)
+          if (kind == 0) {
+            tma_load_4d(kraw + pl * 2048, &tmK, kr_full, 0, p.kv_head_inner ? kvh : sub, p.kv_head_inner ? sub : kvh,
+                        blk);
+          } else if (kind == 1 && per_token) {
             bulk_load(kraw + C::KR_KS + pl * 64, p.k_scale + slot0, 64, kr_full);
-          else if (kind == 2 && per_token)
+          } else if (kind == 2 && per_token) {
             bulk_load(kraw + C::KR_VS + pl * 64, p.v_scale + slot0, 64, kr_full);
-          else if (kind == 3 && has_gate)
-            bulk_load(kraw + C::KR_G + pl * 1024, p.g_cache + ((size_t)blk * p.hq + kvh * kGroup) * kPage, 1024,
-                      kr_full);
+          } else if (kind == 3 && has_gate) {
+            // the group's G heads x 16 slots: adjacent when a block is one page
+            const float* src = p.g_cache + ((size_t)blk * p.hq + kvh * G) * p.block_size + sub;
+            if (lbp == 0) {
+              bulk_load(kraw + C::KR_G + pl * 1024, src, G * kPage * 4, kr_full);
+            } else {
+              for (int hh = 0; hh < G; ++hh)
+                bulk_load(kraw + C::KR_G + pl * 1024 + hh * kPage * 4, src + (size_t)hh * p.block_size, kPage * 4,
+                          kr_full);
+            }
+          }
         }
         okl = wait_bar(vr_empty, par, ab);
         if (!__all_sync(0xffffffffu, okl)) break;
         if (lane == 0) mbar_expect_tx(vr_full, nv * 2048);
         __syncwarp();
         if (kind == 0 && pl < nv)
-          tma_load_4d(vraw + pl * 2048, &tmV, vr_full, 0, p.kv_head_inner ? kvh : 0, p.kv_head_inner ? 0 : kvh, blk);
+          tma_load_4d(vraw + pl * 2048, &tmV, vr_full, 0, p.kv_head_inner ? kvh : sub, p.kv_head_inner ? sub : kvh,
+                      blk);
       }
     } else if (warp == 1) {
       if (lane == 0) {
@@ -426,12 +441,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           ax[kTileKeys + k] = valid ? vs * kPScale : 0.f;
         }
         if (FEAT) {
-          // -G_j in log2 units for the group's 16 heads: raw pages hold [head][slot] per page
+          // -G_j in log2 units for the group's G heads: raw pages hold [head][slot], 1 KB apart
           const float* gr = reinterpret_cast<const float*>(kraw + C::KR_G);
-          for (int i = c; i < kGroup * kTileKeys; i += 64) {
+          for (int i = c; i < p.group * kTileKeys; i += 64) {
             const int h = i >> 7, k = i & 127;
             ax[2 * kTileKeys + i] =
-                (has_gate && key0 + k < L) ? -gr[(k >> 4) * (kGroup * kPage) + h * kPage + (k & 15)] * kLog2e : 0.f;
+                (has_gate && key0 + k < L) ? -gr[(k >> 4) * 256 + h * kPage + (k & 15)] * kLog2e : 0.f;
           }
         }
         __syncwarp();
@@ -471,8 +486,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int x = (warp - 4) >> 2;
     const int quarter = warp & 3;
     const int rr = quarter * 32 + lane;  // row of the tile
-    const int head = rr & (kGroup - 1);
-    const int pos = pos0 + x * kPosPerTile + (rr >> 4);
+    const int head = rr & (G - 1);
+    const int pos = pos0 + x * pos_tile + (rr >> lgG);
     const bool row_valid = pos < ql;
     const int posc = min(pos, ql - 1);
     const int lastk = L - ql + posc;  // last key this row sees
@@ -481,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
       // this row of Q: bf16 -> f16 into the 128-B-swizzled K-major tile (two 64-dim chunks)
       const uint4* src =
-          reinterpret_cast<const uint4*>(p.q + (size_t)(q_begin + posc) * p.q_ts + (size_t)(kvh * kGroup + head) * p.q_hs);
+          reinterpret_cast<const uint4*>(p.q + (size_t)(q_begin + posc) * p.q_ts + (size_t)(kvh * G + head) * p.q_hs);
       uint8_t* qs = smem + C::OFF_Q + x * 2 * kStage;
 #pragma unroll 4
       for (int u = 0; u < 16; ++u) {
@@ -497,15 +512,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool has_gate = FEAT && p.g_cache != nullptr;
     float gi = 0.f;  // the row's own G (log2 units)
     if (has_gate) {
-      const int blk = __ldg(p.block_table + (size_t)r * p.max_blocks + lastk / kPage);
-      gi = __ldg(p.g_cache + ((size_t)blk * p.hq + kvh * kGroup + head) * kPage + lastk % kPage) * kLog2e;
+      const int blk = __ldg(p.block_table + (size_t)r * p.max_blocks + lastk / p.block_size);
+      gi = __ldg(p.g_cache + ((size_t)blk * p.hq + kvh * G + head) * p.block_size + lastk % p.block_size) * kLog2e;
     }
     const bool sink_here = direct && p.sink != nullptr;
-    float m = sink_here ? __ldg(p.sink + kvh * kGroup + head) * kLog2e : neg_inf();
+    float m = sink_here ? __ldg(p.sink + kvh * G + head) * kLog2e : neg_inf();
     float l = sink_here ? 1.f : 0.f;
     const int my_first = x ? n_first[1] : n_first[0], my_last = x ? n_last[1] : n_last[0];
-    const int t_lk_min = L - ql + pos0 + x * kPosPerTile;
-    const int t_lk_max = L - ql + min(pos0 + x * kPosPerTile + kPosPerTile - 1, ql - 1);
+    const int t_lk_min = L - ql + pos0 + x * pos_tile;
+    const int t_lk_max = L - ql + min(pos0 + x * pos_tile + pos_tile - 1, ql - 1);
     bool ok = true;
     int kx = 0;  // key tiles processed by this query tile
     for (int n = 0; n < nt; ++n) {
@@ -616,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (direct) {
         if (kx > 0) {
           const float inv = 1.f / (kPScale * l);
-          uint16_t* orow = p.out + (size_t)(q_begin + posc) * p.out_ts + (size_t)(kvh * kGroup + head) * p.out_hs;
+          uint16_t* orow = p.out + (size_t)(q_begin + posc) * p.out_ts + (size_t)(kvh * G + head) * p.out_hs;
 #pragma unroll 1
           for (int cc = 0; cc < kD / 32; ++cc) {
             uint32_t ov[32];
@@ -634,7 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        const size_t row = unit * rows_per_unit + (size_t)posc * kGroup + head;
+        const size_t row = unit * rows_per_unit + (size_t)posc * G + head;
         float4* arow = reinterpret_cast<float4*>(p.part_acc + row * kD);
         if (kx > 0) {
           constexpr float kInv = 1.f / kPScale;
@@ -687,7 +702,8 @@ cudaError_t launch_t(const DecodeParams& p, const DecodeMaps& maps, int qpairs, 
 
 cudaError_t launch_prefill_paged(const DecodeParams& p, const DecodeMaps& maps, cudaStream_t s,
                                  const cudaEvent_t* ev_before, const cudaEvent_t* ev_after) {
-  const int qpairs = (p.max_q_len + 2 * kPosPerTile - 1) / (2 * kPosPerTile);
+  const int pos_pair = 2 * (128 / p.group);  // query positions of one CTA
+  const int qpairs = (p.max_q_len + pos_pair - 1) / pos_pair;
   if (ev_before && *ev_before) cudaEventRecord(*ev_before, s);
   const bool feat = p.g_cache != nullptr || p.window > 0;
   cudaError_t e = feat ? launch_t<true>(p, maps, qpairs, s) : launch_t<false>(p, maps, qpairs, s);

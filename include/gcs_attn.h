@@ -175,8 +175,9 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
  * (natural-log units); the score becomes scale*q.k_j + G_i - G_j with G_i the entry at the query row's
  * own position.  window W > 0 keeps keys with position_i - j < W.  sink fp32 [hq] adds
  * e^sink_h to the softmax denominator (once, in the combine).
- * Supported: d == 128, block_size == 16, hq / hkv == 16, 1 <= q_len <= 4,
- * segment_len a positive multiple of block_size.
+ * Supported: d == 128; hq / hkv == 16 or 8 (GQA groups of 16 or 8 query heads); block_size
+ * 16 x 2^k tokens (16, 32, 64, 128, ..., 4096); 1 <= q_len <= 4; segment_len a positive multiple
+ * of 16.
  * Operand precision of an fp8 cache: the tensor cores see f16.  q is rounded from bf16 to f16,
  * so no |q| may exceed 65504 (the f16 maximum); K and V codes convert to f16 exactly;
  * P * vscale is rounded to nearest f16 after a 2^8 pre-scale (P <= 1), so every V scale of a

@@ -118,9 +118,12 @@ def test_decode_validation_on_host(L):
     dec = lambda a: L.attn_decode_paged(b(a), FAKE, FAKE, 1 << 40, None)
     # per-token scales on a prefill shape are rejected
     assert dec(decode(max_q_len=5)) == 2
-    assert dec(decode(block_size=32)) == 2
+    assert dec(decode(block_size=24)) == 2  # not whole 16-token pages
+    assert dec(decode(block_size=48, max_blocks_per_req=128)) == 2  # 3 pages: not a power of two
+    assert L.attn_decode_workspace(b(decode(block_size=128, max_blocks_per_req=32))) > 0  # 128-token blocks
     assert dec(decode(d=64)) == 2
-    assert dec(decode(hq=32)) == 2  # GQA group must be 16
+    assert dec(decode(hq=48)) == 2  # GQA group must be 16 or 8
+    assert L.attn_decode_workspace(b(decode(hq=32))) > 0  # group of 8
     assert dec(decode(segment_len=2040)) == 2
     assert dec(decode(k_scale=None)) == 1
     assert dec(decode(max_blocks_per_req=10)) == 1  # table too short for max_seq_len
@@ -156,7 +159,7 @@ def test_prefill_paged_validation_and_workspace_on_host(L):
     assert pp(decode(max_q_len=64, kv_format=1, k_scale=None, v_scale=None)) == 2  # fp8 only
     assert pp(decode(max_q_len=5000)) == 1  # more query rows than cached tokens
     assert pp(decode(max_q_len=64, window=-1)) == 1
-    assert pp(decode(max_q_len=64, hq=32)) == 2
+    assert pp(decode(max_q_len=64, hq=48)) == 2
     assert pp(decode(max_q_len=64, segment_len=-128)) == 1
     assert L.attn_prefill_paged(b(decode(max_q_len=64)), FAKE + 8, FAKE, 1 << 40, None) == 1
 
@@ -192,7 +195,7 @@ def test_device_checks_mode_and_workspace_on_host(L):
     # the stand-alone checks validate their arguments on the host first
     assert L.gcs_check_prefill_inputs(b(prefill(hq=3, hkv=2)), None) == 1
     assert L.gcs_check_prefill_inputs(b(prefill(dqk=96, dv=96)), None) == 2
-    assert L.gcs_check_paged_inputs(b(decode(block_size=32)), None) == 2
+    assert L.gcs_check_paged_inputs(b(decode(block_size=24)), None) == 2
     assert L.gcs_check_paged_inputs(b(decode(cu_q=None)), None) == 1
 
 

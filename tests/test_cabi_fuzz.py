@@ -46,24 +46,27 @@ def test_prefill_workspace_queries_never_crash(L, num_seqs, total, max_seqlen, h
 
 @settings(max_examples=300, deadline=None)
 @given(num_reqs=ints, total_q=ints, max_q_len=st.integers(-1, 6), max_seq_len=ints, max_blocks=ints,
-       num_blocks=ints, hkv=st.sampled_from([-1, 0, 1, 2, 4]), group=st.sampled_from([8, 16]),
+       num_blocks=ints, hkv=st.sampled_from([-1, 0, 1, 2, 4]), group=st.sampled_from([4, 8, 16]),
+       block=st.sampled_from([8, 16, 24, 128]),
        seg=st.sampled_from([-16, 0, 16, 100, 2048]), fmt=st.sampled_from([(0, 0), (0, 1), (1, 0), (2, 0), (0, 2)]),
        window=ints)
 def test_decode_workspace_queries_never_crash(L, num_reqs, total_q, max_q_len, max_seq_len, max_blocks, num_blocks,
-                                              hkv, group, seg, fmt, window):
+                                              hkv, group, block, seg, fmt, window):
     import gated_causal_softmax_gb300 as gcs
 
     kvf, mode = fmt
     scales = None if kvf == 1 else FAKE
     a = gcs.DecodeArgs(num_reqs=num_reqs, cu_q=FAKE, total_q=total_q, max_q_len=max_q_len, seq_lens=FAKE,
                        max_seq_len=max_seq_len, block_table=FAKE, max_blocks_per_req=max_blocks, k_cache=FAKE,
-                       v_cache=FAKE, k_scale=scales, v_scale=scales, num_blocks=num_blocks, block_size=16,
+                       v_cache=FAKE, k_scale=scales, v_scale=scales, num_blocks=num_blocks, block_size=block,
                        hq=hkv * group, hkv=hkv, d=128, scale=0.1, segment_len=seg, q=FAKE, kv_format=kvf,
                        scale_mode=mode, window=window)
     dw = L.attn_decode_workspace(ctypes.byref(a))
     pw = L.attn_prefill_paged_workspace(ctypes.byref(a)) if seg != 0 else 0  # 0 asks the device for its SM count
     assert dw % 256 == 0 and pw % 256 == 0
     if min(num_reqs, total_q, max_q_len, max_seq_len, max_blocks, num_blocks, hkv) < 1 or window < 0:
+        assert dw == 0 and pw == 0
+    if group == 4 or block % 16 != 0:  # GQA groups of 16 or 8, whole 16-token pages
         assert dw == 0 and pw == 0
     if dw > 0 and num_reqs < (1 << 31) - 1:
         # one more request never needs less workspace

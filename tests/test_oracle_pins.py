@@ -553,3 +553,73 @@ def test_paged_chunk_splitk_equals_unsplit_and_rows_are_single_queries():
                               dc.v_scale.numpy(), np.stack(bt), np.array(seq), np.array(cu), dc.scale,
                               **_feature_kwargs(dc))
     np.testing.assert_allclose(one, ref, rtol=0, atol=1e-12)
+
+
+def _relayout_blocks(dc, block):
+    """The same logical cache with `block` tokens per cache block: every request's tokens are
+    copied, in order, into fresh blocks laid out [num_blocks, hkv, block, d] (and the scales and
+    gates likewise), with a reversed block order so that no index coincides by accident."""
+    bs = dc.k_cache.shape[2]
+    L = dc.seq_lens.tolist()
+    pages = [(x + block - 1) // block for x in L]
+    nb = sum(pages) + 1
+    order = list(range(nb))[::-1]
+    table = np.zeros((len(L), max(pages)), dtype=np.int32)
+
+    def tokens(arr, r, n):  # [n, heads, ...] token-major values of request r
+        old = dc.block_table[r].numpy()
+        out = [arr[old[j // bs], :, j % bs] for j in range(n)]
+        return np.stack(out)
+
+    def place(arr, fill):
+        new = np.full((nb, arr.shape[1], block) + arr.shape[3:], fill, dtype=arr.dtype)
+        pos = 0
+        for r, n in enumerate(L):
+            t = tokens(arr, r, n)
+            for j in range(n):
+                b = order[pos + j // block]
+                new[b, :, j % block] = t[j]
+            pos += pages[r]
+        return new
+
+    pos = 0
+    for r in range(len(L)):
+        table[r, : pages[r]] = [order[pos + i] for i in range(pages[r])]
+        pos += pages[r]
+    kc = place(dc.k_cache.numpy(), 0x7F)
+    vc = place(dc.v_cache.numpy(), 0x7F)
+    ks = place(dc.k_scale.numpy(), np.nan)
+    vs = place(dc.v_scale.numpy(), np.nan)
+    g = None if dc.g_cache is None else place(dc.g_cache.numpy(), np.nan)
+    return kc, vc, ks, vs, g, table
+
+
+@pytest.mark.parametrize("window", [0, 30])
+def test_decode_oracle_block_size_and_group_of_eight(window):
+    """Cache blocks of 128 tokens hold the same attention as blocks of 16 (the same logical
+    cache relaid by the test, not by the oracle), and a GQA group of 8 matches the last rows of
+    the prefill oracle on the dequantized cache, gates, window and sink included."""
+    dc = make_decode([1, 130, 300, 77], [1, 4, 3, 2], 16, 2, 16, seed=61, features=True, window=window)
+    kw = dict(sink=f64(dc.sink), window=dc.window)
+    args = lambda kc, vc, ks, vs, bt: (f64(dc.q), kc, vc, ks, vs, bt, dc.seq_lens.numpy(), dc.cu_q.numpy(), dc.scale)
+    ref = oracle.decode_paged(*args(dc.k_cache.numpy(), dc.v_cache.numpy(), dc.k_scale.numpy(), dc.v_scale.numpy(),
+                                    dc.block_table.numpy()), g_cache=dc.g_cache.numpy(), **kw)
+    kc, vc, ks, vs, g, bt = _relayout_blocks(dc, 128)
+    got = oracle.decode_paged(*args(kc, vc, ks, vs, bt), g_cache=g, **kw)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-13)
+    # group of 8 (hq 16 over hkv 2) against the prefill oracle's last q_len rows, request by request
+    cu = dc.cu_q.tolist()
+    for r, L in enumerate(dc.seq_lens.tolist()):
+        K = np.stack([oracle.gather_kv(dc.k_cache.numpy(), dc.k_scale.numpy(), dc.block_table[r].numpy(), L, h)
+                      for h in range(2)], axis=1)
+        V = np.stack([oracle.gather_kv(dc.v_cache.numpy(), dc.v_scale.numpy(), dc.block_table[r].numpy(), L, h)
+                      for h in range(2)], axis=1)
+        G = np.stack([oracle.attention._gate_of(dc.g_cache.numpy(), dc.block_table[r].numpy(), L, h)
+                      for h in range(16)], axis=1)
+        gates = np.diff(np.concatenate([np.zeros((1, 16)), G]), axis=0)  # per-token log gates
+        ql = cu[r + 1] - cu[r]
+        q = np.zeros((L, 16, dc.d))
+        q[L - ql:] = f64(dc.q)[cu[r]:cu[r + 1]]
+        o, _ = oracle.prefill_forward(q, K, V, np.array([0, L]), dc.scale, log_gate=gates, sink=f64(dc.sink),
+                                      window=dc.window)
+        np.testing.assert_allclose(ref[cu[r]:cu[r + 1]], o[L - ql:], rtol=0, atol=1e-12)

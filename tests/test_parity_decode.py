@@ -260,3 +260,52 @@ def test_decode_rn_bias_is_far_below_the_limit(gcs_lib, reading):
     got = f64(out)[[int(dc.cu_q[r]) for r in pick]]
     assert_close("out", got, ref, DECODE_RTOL)
     assert abs(bias(got, ref)) <= 2e-4
+
+
+# The aiter PR's test matrix: GQA groups of 16 and 8, head 128, pages of 16 and 128 tokens,
+# contexts from 1 to 4096 and 65537, tails that end 1 to 4 tokens into a page.
+MATRIX_LENS = [1, 2, 3, 4, 129, 130, 2051, 4096, 65537]
+MATRIX_QLENS = [1, 2, 3, 4, 1, 2, 3, 4, 4]
+
+
+@pytest.mark.parametrize("group", [16, 8])
+@pytest.mark.parametrize("block", [16, 128])
+@pytest.mark.parametrize("variant", ["A", "B", "bf16", "per_tensor", "features"])
+def test_decode_gqa_and_page_matrix(gcs_lib, group, block, variant):
+    kw = dict(scale_reading="B") if variant == "B" else dict(kv_format="bf16") if variant == "bf16" else \
+        dict(scale_mode="per_tensor") if variant == "per_tensor" else dict(features=True, window=300) \
+        if variant == "features" else {}
+    dc = make_decode(MATRIX_LENS, MATRIX_QLENS, 2 * group, 2, 128, seed=900 + group + block, block_size=block,
+                     segment_len=2048, **kw)
+    out = run_decode(gcs_lib, dc)
+    ref = oracle_decode(dc)
+    assert_close("out", out, ref, DECODE_RTOL)
+    assert abs(bias(out, ref)) <= DECODE_BIAS
+
+
+@pytest.mark.parametrize("group", [16, 8])
+def test_decode_gather_is_exact_with_128_token_blocks(gcs_lib, group):
+    """One dominant key per request at a chosen slot of a 128-token block; its value codes name
+    the block, so the output identifies the gathered (block, slot) exactly."""
+    sl = [37, 2050, 700]
+    dc = make_decode(sl, [1, 1, 1], group, 1, 128, seed=13, block_size=128)
+    kc, vc, ks, vs = dc.k_cache.clone(), dc.v_cache.clone(), dc.k_scale.clone(), dc.v_scale.clone()
+    q = torch.zeros_like(dc.q)
+    q[:, :, 0] = 1.0
+    kc.zero_()  # code 0 = +0
+    picks = [5, 2049, 333]
+    code = lambda x: int(torch.tensor(float(x)).to(torch.float8_e4m3fn).view(torch.uint8))
+    for r, slot in enumerate(picks):
+        blk = int(dc.block_table[r, slot // 128])
+        kc[blk, 0, slot % 128, 0] = 0x7E  # 448
+        ks[blk, 0, slot % 128] = 1.0
+        vc[blk, 0, slot % 128, 0] = code(blk % 8)
+        vc[blk, 0, slot % 128, 1] = code((blk // 8) % 8)
+        vs[blk, 0, slot % 128] = 1.0
+    dc.k_cache, dc.v_cache, dc.k_scale, dc.v_scale, dc.q = kc, vc, ks, vs, q
+    dc.scale = 1.0
+    out = run_decode(gcs_lib, dc).float().cpu()
+    for r, slot in enumerate(picks):
+        blk = int(dc.block_table[r, slot // 128])
+        assert out[r, :, 0].eq(float(blk % 8)).all(), (r, out[r, :, 0])
+        assert out[r, :, 1].eq(float((blk // 8) % 8)).all()

@@ -154,3 +154,20 @@ def test_prefill_paged_full_size_sampled(gcs_lib, seg):
     got = f64(out)[rows]
     assert_close("out", got, ref, DECODE_RTOL)
     assert abs(bias(got, ref)) <= DECODE_BIAS
+
+
+@pytest.mark.parametrize("group", [16, 8])
+@pytest.mark.parametrize("block", [16, 128])
+@pytest.mark.parametrize("features", [False, True])
+@pytest.mark.parametrize("seg", ["direct", "seg128"])
+def test_prefill_paged_gqa_and_page_matrix(gcs_lib, group, block, features, seg):
+    """GQA groups of 16 and 8 (a 128-row tile is 8 positions x 16 heads or 16 positions x 8
+    heads, so q_len 16, 17, 33 sit on and past the tile edges of both) over 16- and 128-token
+    cache blocks, with and without gates, window and sink."""
+    dc = make_decode([17, 300, 1025, 2049], [16, 17, 33, 130], 2 * group, 2, 128, seed=950 + group + block,
+                     block_size=block, features=features, window=200 if features else 0)
+    out = run_prefill_paged(gcs_lib, dc, SEGMENTS[seg])
+    ref = oracle_decode(dc)
+    assert np.isfinite(f64(out)).all()
+    assert_close("out", out, ref, DECODE_RTOL)
+    assert abs(bias(out, ref)) <= DECODE_BIAS
