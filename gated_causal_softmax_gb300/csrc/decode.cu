@@ -50,24 +50,30 @@ constexpr int kRows = 16;  // rows of an m16 tile; partial rows per (unit, query
 // features, the cumulative gates of the group's 16 query heads (16 x 16 fp32 = 1 KB).
 // Stages fill ~72 KB (three CTAs per SM); the producer issues BATCH pages per round, one
 // copy per lane.
-template <int KVF, bool PT, bool FEAT>
+template <int KVF, bool PT, bool FEAT, bool SQ>
 struct DecCfg {
   static constexpr int KB = KVF == 0 ? 2048 : 4096;  // bytes of one page of K (or V) for one kv head
   static constexpr bool SCALES = KVF == 0 && !PT;    // per-token scale copies
   static constexpr int KV = 2 * KB;                  // K | V of one page (a multiple of 1 KB)
   static constexpr int G_OFF = SCALES ? 128 : 0;     // gates inside a small-vector stage
   static constexpr int AUX = G_OFF + (FEAT ? 1024 : 0);
-  // NST is a multiple of 4: the page groups of a CTA are 4 / q_len warps (4, 2 or 1), so the
-  // previous page of every stage belongs to the warp that waits for the stage's next page.
-  // That warp has therefore seen the previous phase complete, and a full-barrier parity wait
-  // cannot match the phase before it (which a stage consumed by another warp could, while the
-  // previous page's copy is still in flight).
-  static constexpr int NST = ((72 * 1024 / (KV + AUX)) < 16 ? (72 * 1024 / (KV + AUX)) : 16) & ~3;
+  // Ring budget: ~72 KB, three CTAs per SM with the query fragments of one position (4 KB).
+  // SQ (3 or 4 query positions, 16 KB of fragments) trims the ring so that three CTAs still
+  // fit: short-query calls are latency-bound, and 12 consumer warps per SM beat 8 with a
+  // deeper ring.
+  static constexpr int BUDGET = SQ ? 57 * 1024 : 72 * 1024;
+  // NST is a multiple of 4: the page groups of a CTA are 4 / (query tiles) warps (4, 2 or 1),
+  // so the previous page of every stage belongs to the warp that waits for the stage's next
+  // page.  That warp has therefore seen the previous phase complete, and a full-barrier parity
+  // wait cannot match the phase before it (which a stage consumed by another warp could, while
+  // the previous page's copy is still in flight).
+  static constexpr int NST = ((BUDGET / (KV + AUX)) < 16 ? (BUDGET / (KV + AUX)) : 16) & ~3;
   static constexpr int OFF_AUX = NST * KV;
   static constexpr int SMEM = OFF_AUX + NST * AUX + 1024;  // + alignment of the base to 1 KB
   static constexpr int KINDS = 2 + (SCALES ? 2 : 0) + (FEAT ? 1 : 0);  // K, V (, K/V scales) (, gates)
-  static constexpr int BATCH = (KINDS * 8 <= 32 && NST >= 16) ? 8 : 4;
-  static_assert(NST % 4 == 0, "stages per page-group warp");
+  // pages per producer round: a power of two, one copy per lane, at most half the ring
+  static constexpr int BATCH = (KINDS * 8 <= 32 && NST >= 16) ? 8 : (NST >= 8 ? 4 : 2);
+  static_assert(NST % 4 == 0 && NST >= 4, "stages per page-group warp");
   static_assert(KINDS * BATCH <= 32 && NST >= 2 * BATCH, "producer round");
 };
 constexpr int kThreads = 160;
@@ -122,11 +128,11 @@ __device__ __forceinline__ uint32_t bf16pair_to_f16x2(uint32_t w) {
 // KVF: 0 fp8 e4m3 codes, 1 bf16 values.  PT: one K and one V scale for the whole cache (fp8).
 // FEAT: the decoding features (gates from g_cache when given, the window; the sink is the
 // combine's).  G: query heads per kv head, 16 or 8.
-template <int KVF, bool PT, bool FEAT, int G>
+template <int KVF, bool PT, bool FEAT, int G, bool SQ>
 __global__ void __launch_bounds__(kThreads, 3)
     decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const DecodeParams p) {
-  using C = DecCfg<KVF, PT, FEAT>;
+  using C = DecCfg<KVF, PT, FEAT, SQ>;
   constexpr int kNST = C::NST, kBatch = C::BATCH;
   constexpr int kKinds = C::KINDS;
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -627,9 +633,10 @@ cudaError_t launch_decode(const DecodeParams& p, const DecodeMaps& maps, cudaStr
   cudaError_t e;
   // the sink alone needs no change in the split kernel (it is the combine's)
   const bool feat = p.g_cache != nullptr || p.window > 0;
-#define GCS_RUN(KVF, PT, F)                                                                         \
-  (p.group == 8 ? run(decode_split_kernel<KVF, PT, F, 8>, DecCfg<KVF, PT, F>::SMEM)                  \
-                : run(decode_split_kernel<KVF, PT, F, 16>, DecCfg<KVF, PT, F>::SMEM))
+#define GCS_RUN2(KVF, PT, F, SQ)                                                                    \
+  (p.group == 8 ? run(decode_split_kernel<KVF, PT, F, 8, SQ>, DecCfg<KVF, PT, F, SQ>::SMEM)          \
+                : run(decode_split_kernel<KVF, PT, F, 16, SQ>, DecCfg<KVF, PT, F, SQ>::SMEM))
+#define GCS_RUN(KVF, PT, F) (p.max_q_len > 2 ? GCS_RUN2(KVF, PT, F, true) : GCS_RUN2(KVF, PT, F, false))
   if (p.kv_format == 1)
     e = feat ? GCS_RUN(1, false, true) : GCS_RUN(1, false, false);
   else if (p.scale_mode == 1)
@@ -637,6 +644,7 @@ cudaError_t launch_decode(const DecodeParams& p, const DecodeMaps& maps, cudaStr
   else
     e = feat ? GCS_RUN(0, false, true) : GCS_RUN(0, false, false);
 #undef GCS_RUN
+#undef GCS_RUN2
   if (ev_after && *ev_after) cudaEventRecord(*ev_after, s);
   if (e != cudaSuccess) return e;
   return launch_decode_combine(p, s);
