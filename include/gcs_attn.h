@@ -110,11 +110,12 @@ typedef struct {
   const void* v;              /* bf16 [total_tokens, hkv, dv]                            */
   const float* log_gate;      /* fp32 [total_tokens, hq] per-token log forget gates, or NULL */
   const float* sink;          /* fp32 [hq] sink logits, or NULL                          */
-  int deterministic;          /* attn_bwd with dqk or dv > 128: 1 = a separate query-stationary
-                                 dQ pass, every gradient written once or summed in a fixed
-                                 order; 0 = the faster route for the shape: that same pass
-                                 for dqk = 512, fp32 reduce-adds of dQ and the dS row sums
-                                 otherwise.  Head dims <= 128 are deterministic either way. */
+  int deterministic;          /* attn_bwd: 1 = a separate query-stationary dQ pass, every
+                                 gradient written once or summed in a fixed order; 0 = the
+                                 faster route for the shape: a single pass with fp32
+                                 reduce-adds of dQ and the dS row sums at head dim 128 and at
+                                 dqk = 256, the separate dQ pass at 64 (the only route there)
+                                 and at dqk = 512. */
   gcs_strides q_stride, k_stride, v_stride;  /* layouts of q, k, v ({0, 0} = contiguous)      */
   gcs_strides o_stride;       /* attn_fwd's output o and attn_bwd's input o                    */
   gcs_strides do_stride;      /* attn_bwd's dout                                               */
@@ -142,11 +143,11 @@ size_t attn_bwd_workspace(const gcs_prefill_args* a);
  * dlog_gate fp32 [total_tokens, hq] contiguous (must be NULL iff
  * log_gate is NULL), dsink fp32 [hq] (must be NULL iff sink is NULL).
  * The sink gradient is -sum_i p_sink,i * sum_j P_ij (dO_i . v_j), accumulated in fp32.
- * Head dims <= 128: dQ is accumulated per query tile in a separate pass and every gradient is
- * written once or summed in a fixed order, so repeated calls give the same bits.  Wider heads
- * do the same with a->deterministic = 1, and with 0 when dqk = 512; otherwise (dqk = 256 with
- * deterministic = 0) dQ and d log_gate are accumulated by fp32 reduce-adds into a
- * zero-initialised buffer, and their low bits may vary from run to run. */
+ * With a->deterministic = 1 (and always at head dim 64, and at dqk = 512) dQ is accumulated per
+ * query tile in a separate pass and every gradient is written once or summed in a fixed order,
+ * so repeated calls give the same bits.  Otherwise (head dim 128, dqk = 256) dQ, d log_gate and
+ * d sink come from fp32 reduce-adds into zero-initialised buffers (the [FLA] comment of Oct 5),
+ * and their low bits may vary from run to run. */
 int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const void* dout, void* dq, void* dk,
              void* dv, float* dlog_gate, float* dsink, void* workspace, size_t workspace_bytes,
              gcs_stream_t stream);
