@@ -20,8 +20,11 @@ namespace gcs {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kScanThreads = 256;
-constexpr int kScanPer = 4;
+// One block per (sequence, head) scans 8192 tokens per pass: sequences up to that length take
+// one pass of independent loads (the scans are latency-bound), longer ones carry the running
+// total between passes.
+constexpr int kScanThreads = 1024;
+constexpr int kScanPer = 8;
 
 // Block-wide inclusive scan of one value per thread; returns the inclusive prefix and
 // writes the block total into *total.
