@@ -34,6 +34,13 @@ constexpr float kRescale = 8.0f;
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
+// Three-input maximum (one instruction on this architecture).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 template <int DQK, int DVC>
 struct FwdCfg {
   static constexpr int QCH = DQK / 64;
@@ -224,8 +231,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool row_valid = il < len;
     const int tok = seq_start + (row_valid ? il : len - 1);
     const bool has_gate = p.gT != nullptr;
-    const float gi = has_gate ? __ldg(p.gT + (size_t)h * p.total + tok) : 0.f;
-    float m = p.sink ? __ldg(p.sink + h) * kLog2e : neg_inf();
+    // G_i is the same for every key of the row: the scores are kept without it (the softmax
+    // does not change), the sink logit is shifted by -G_i, and G_i returns in the LSE
+    float m = p.sink ? __ldg(p.sink + h) * kLog2e - (has_gate ? __ldg(p.gT + (size_t)h * p.total + tok) : 0.f)
+                     : neg_inf();
     float l = p.sink ? 1.f : 0.f;
     bool ok = true;
     if (!has_gate) {
@@ -265,22 +274,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int e = 0; e < 8; ++e) mxp[e] = neg_inf();
       if (need_mask) {
 #pragma unroll
-        for (int j = 0; j < 128; ++j) {
-          float t = fmaf(__uint_as_float(sv[j]), p.scale_log2, gi) + gj[j];
-          t = (j >= jmin && j <= jmax) ? t : neg_inf();
-          sv[j] = __float_as_uint(t);
-          mxp[j & 7] = fmaxf(mxp[j & 7], t);
+        for (int j = 0; j < 128; j += 2) {
+          float t0 = fmaf(__uint_as_float(sv[j]), p.scale_log2, gj[j]);
+          float t1 = fmaf(__uint_as_float(sv[j + 1]), p.scale_log2, gj[j + 1]);
+          t0 = (j >= jmin && j <= jmax) ? t0 : neg_inf();
+          t1 = (j + 1 >= jmin && j + 1 <= jmax) ? t1 : neg_inf();
+          sv[j] = __float_as_uint(t0);
+          sv[j + 1] = __float_as_uint(t1);
+          mxp[(j >> 1) & 7] = fmax3(mxp[(j >> 1) & 7], t0, t1);
         }
       } else {
 #pragma unroll
-        for (int j = 0; j < 128; ++j) {
-          const float t = fmaf(__uint_as_float(sv[j]), p.scale_log2, gi) + gj[j];
-          sv[j] = __float_as_uint(t);
-          mxp[j & 7] = fmaxf(mxp[j & 7], t);
+        for (int j = 0; j < 128; j += 2) {
+          const float t0 = fmaf(__uint_as_float(sv[j]), p.scale_log2, gj[j]);
+          const float t1 = fmaf(__uint_as_float(sv[j + 1]), p.scale_log2, gj[j + 1]);
+          sv[j] = __float_as_uint(t0);
+          sv[j + 1] = __float_as_uint(t1);
+          mxp[(j >> 1) & 7] = fmax3(mxp[(j >> 1) & 7], t0, t1);
         }
       }
-      const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
-                             fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
+      const float mx = fmax3(fmax3(mxp[0], mxp[1], mxp[2]), fmax3(mxp[3], mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7]));
       const float m_new = fmaxf(m, mx);
       const bool need = m_new > m + kRescale;
       if (__any_sync(0xffffffffu, need)) {
@@ -345,7 +358,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
         }
       }
-      if (row_valid && blockIdx.z == 0) p.lse[(size_t)h * p.total + seq_start + il] = (m + log2f(l)) * kLn2;
+      if (row_valid && blockIdx.z == 0) {
+        const float gi = has_gate ? __ldg(p.gT + (size_t)h * p.total + tok) : 0.f;
+        p.lse[(size_t)h * p.total + seq_start + il] = (m + gi + log2f(l)) * kLn2;
+      }
     }
   }
 

@@ -31,6 +31,13 @@ constexpr float kRescale = 8.0f;
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
+// Three-input maximum (one instruction on this architecture).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 template <int D>
 struct Fwd2Cfg {
   static constexpr int CH = D / 64;
@@ -248,8 +255,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool row_valid = il < len;
     const int tok = seq_start + (row_valid ? il : len - 1);
     const bool has_gate = p.gT != nullptr;
-    const float gi = has_gate ? __ldg(p.gT + (size_t)h * p.total + tok) : 0.f;
-    float m = p.sink ? __ldg(p.sink + h) * kLog2e : neg_inf();
+    // The row's own G_i is the same for every key, so the scores are kept without it (the
+    // softmax does not change) and it returns in the LSE; the sink logit, which carries no
+    // G_i, is shifted by -G_i instead.
+    float m = p.sink ? __ldg(p.sink + h) * kLog2e - (has_gate ? __ldg(p.gT + (size_t)h * p.total + tok) : 0.f)
+                     : neg_inf();
     float l = p.sink ? 1.f : 0.f;
     float* sG = reinterpret_cast<float*>(smem + C::OFF_G) + (x * 4 + quarter) * 2 * kBN;
     if (!has_gate) {
@@ -285,39 +295,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       float mxp[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) mxp[e] = neg_inf();
-      // -G_j read as 16-B broadcast loads: shared-memory loads compete with the operand reads
-      // of running MMAs, so fewer, wider ones
+      // t = s scale log2e - G_j (one FMA), maxima three at a time; -G_j read as 16-B broadcast
+      // loads: shared-memory loads compete with the operand reads of running MMAs, so fewer,
+      // wider ones
       const float4* gj4 = reinterpret_cast<const float4*>(gj);
       if (need_mask) {
 #pragma unroll
         for (int j4 = 0; j4 < 32; ++j4) {
           const float4 g4 = gj4[j4];
           const float gs[4] = {g4.x, g4.y, g4.z, g4.w};
+          float t[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int j = 4 * j4 + e;
-            float t = fmaf(__uint_as_float(sv[j]), p.scale_log2, gi) + gs[e];
-            t = (j >= jmin && j <= jmax) ? t : neg_inf();
-            sv[j] = __float_as_uint(t);
-            mxp[j & 7] = fmaxf(mxp[j & 7], t);
+            t[e] = fmaf(__uint_as_float(sv[j]), p.scale_log2, gs[e]);
+            t[e] = (j >= jmin && j <= jmax) ? t[e] : neg_inf();
+            sv[j] = __float_as_uint(t[e]);
           }
+          mxp[(2 * j4) & 7] = fmax3(mxp[(2 * j4) & 7], t[0], t[1]);
+          mxp[(2 * j4 + 1) & 7] = fmax3(mxp[(2 * j4 + 1) & 7], t[2], t[3]);
         }
       } else {
 #pragma unroll
         for (int j4 = 0; j4 < 32; ++j4) {
           const float4 g4 = gj4[j4];
           const float gs[4] = {g4.x, g4.y, g4.z, g4.w};
+          float t[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int j = 4 * j4 + e;
-            const float t = fmaf(__uint_as_float(sv[j]), p.scale_log2, gi) + gs[e];
-            sv[j] = __float_as_uint(t);
-            mxp[j & 7] = fmaxf(mxp[j & 7], t);
+            t[e] = fmaf(__uint_as_float(sv[j]), p.scale_log2, gs[e]);
+            sv[j] = __float_as_uint(t[e]);
           }
+          mxp[(2 * j4) & 7] = fmax3(mxp[(2 * j4) & 7], t[0], t[1]);
+          mxp[(2 * j4 + 1) & 7] = fmax3(mxp[(2 * j4 + 1) & 7], t[2], t[3]);
         }
       }
-      const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
-                             fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
+      const float mx = fmax3(fmax3(mxp[0], mxp[1], mxp[2]), fmax3(mxp[3], mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7]));
       const float m_new = fmaxf(m, mx);
       const bool need = m_new > m + kRescale;
       if (__any_sync(0xffffffffu, need)) {
@@ -384,7 +398,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 4; ++j) dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
         }
       }
-      if (row_valid) p.lse[(size_t)h * p.total + seq_start + il] = (m + log2f(l)) * kLn2;
+      // G_i read again here rather than kept live through the loop
+      const float gi = has_gate ? __ldg(p.gT + (size_t)h * p.total + tok) : 0.f;
+      if (row_valid) p.lse[(size_t)h * p.total + seq_start + il] = (m + gi + log2f(l)) * kLn2;
     }
   }
 

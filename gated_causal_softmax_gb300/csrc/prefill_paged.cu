@@ -45,6 +45,13 @@ constexpr float kRescale = 4.f;   // lazy rescale threshold (log2 units): P <= 2
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
+// Three-input maximum (one instruction on this architecture).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 template <bool FEAT>
 struct PpCfg {
   static constexpr int NST = FEAT ? 6 : 7;                 // f16 operand stages
@@ -560,17 +567,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             gs[2] += g.z;
             gs[3] += g.w;
           }
+          float t[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int j = 4 * j4 + e;
-            float t = FEAT ? fmaf(__uint_as_float(sv[j]), ks[e], gs[e]) : __uint_as_float(sv[j]) * ks[e];
-            if (need_mask) t = (j >= jmin && j <= jmax) ? t : neg_inf();
-            sv[j] = __float_as_uint(t);
-            mxp[j & 7] = fmaxf(mxp[j & 7], t);
+            t[e] = FEAT ? fmaf(__uint_as_float(sv[j]), ks[e], gs[e]) : __uint_as_float(sv[j]) * ks[e];
+            if (need_mask) t[e] = (j >= jmin && j <= jmax) ? t[e] : neg_inf();
+            sv[j] = __float_as_uint(t[e]);
           }
+          mxp[(2 * j4) & 7] = fmax3(mxp[(2 * j4) & 7], t[0], t[1]);
+          mxp[(2 * j4 + 1) & 7] = fmax3(mxp[(2 * j4 + 1) & 7], t[2], t[3]);
         }
-        const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
-                               fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
+        const float mx = fmax3(fmax3(mxp[0], mxp[1], mxp[2]), fmax3(mxp[3], mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7]));
         const float m_new = fmaxf(m, mx);
         const bool need = m_new > m + kRescale;
         if (__any_sync(0xffffffffu, need)) {
