@@ -127,8 +127,10 @@ __device__ __forceinline__ uint32_t bf16pair_to_f16x2(uint32_t w) {
 
 // KVF: 0 fp8 e4m3 codes, 1 bf16 values.  PT: one K and one V scale for the whole cache (fp8).
 // FEAT: the decoding features (gates from g_cache when given, the window; the sink is the
-// combine's).  G: query heads per kv head, 16 or 8.
-template <int KVF, bool PT, bool FEAT, int G, bool SQ>
+// combine's).  G: query heads per kv head, 16 or 8.  SQ: 3 or 4 query positions (a smaller
+// ring).  PG1: cache blocks of one 16-token page (the page index is the block-table index,
+// which keeps the producer's first copies of a CTA a few instructions shorter).
+template <int KVF, bool PT, bool FEAT, int G, bool SQ, bool PG1>
 __global__ void __launch_bounds__(kThreads, 3)
     decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const DecodeParams p) {
@@ -201,7 +203,8 @@ __global__ void __launch_bounds__(kThreads, 3)
       __syncwarp();
       if (act) {
         const int pg = pb + i;
-        const int blk = __ldg(trow + (pg >> lbp)), sub = (pg & ((1 << lbp) - 1)) * kPage;  // block, first slot
+        const int blk = PG1 ? __ldg(trow + pg) : __ldg(trow + (pg >> lbp));  // block
+        const int sub = PG1 ? 0 : (pg & ((1 << lbp) - 1)) * kPage;           // first slot of the page
         const size_t slot0 = ((size_t)blk * p.hkv + kvh) * p.block_size + sub;
         if (KVF == 0 && kind < 2) {
           // fp8 K or V page: one 16-slot x 128-B box of the cache's 4-D map (dims in stride order)
@@ -633,9 +636,11 @@ cudaError_t launch_decode(const DecodeParams& p, const DecodeMaps& maps, cudaStr
   cudaError_t e;
   // the sink alone needs no change in the split kernel (it is the combine's)
   const bool feat = p.g_cache != nullptr || p.window > 0;
-#define GCS_RUN2(KVF, PT, F, SQ)                                                                    \
-  (p.group == 8 ? run(decode_split_kernel<KVF, PT, F, 8, SQ>, DecCfg<KVF, PT, F, SQ>::SMEM)          \
-                : run(decode_split_kernel<KVF, PT, F, 16, SQ>, DecCfg<KVF, PT, F, SQ>::SMEM))
+#define GCS_RUN3(KVF, PT, F, SQ, P1)                                                                 \
+  (p.group == 8 ? run(decode_split_kernel<KVF, PT, F, 8, SQ, P1>, DecCfg<KVF, PT, F, SQ>::SMEM)       \
+                : run(decode_split_kernel<KVF, PT, F, 16, SQ, P1>, DecCfg<KVF, PT, F, SQ>::SMEM))
+#define GCS_RUN2(KVF, PT, F, SQ) \
+  (p.log2_block_pages == 0 ? GCS_RUN3(KVF, PT, F, SQ, true) : GCS_RUN3(KVF, PT, F, SQ, false))
 #define GCS_RUN(KVF, PT, F) (p.max_q_len > 2 ? GCS_RUN2(KVF, PT, F, true) : GCS_RUN2(KVF, PT, F, false))
   if (p.kv_format == 1)
     e = feat ? GCS_RUN(1, false, true) : GCS_RUN(1, false, false);
@@ -645,6 +650,7 @@ cudaError_t launch_decode(const DecodeParams& p, const DecodeMaps& maps, cudaStr
     e = feat ? GCS_RUN(0, false, true) : GCS_RUN(0, false, false);
 #undef GCS_RUN
 #undef GCS_RUN2
+#undef GCS_RUN3
   if (ev_after && *ev_after) cudaEventRecord(*ev_after, s);
   if (e != cudaSuccess) return e;
   return launch_decode_combine(p, s);
