@@ -46,9 +46,9 @@ LAUNCHES_PER_DECODE = 2
 # kernel changes.
 NCU_TRAFFIC = {
     "bwd": 549.2e6 + 247.0e6,  # prefill_bwd_fused_kernel
-    "fwd": 119.8e6,            # prefill_fwd2_kernel<128>
-    "decode_split": 1155.5e6 + 19.1e6,  # decode_split_kernel<0, 0, 0>
-    "prefill_paged": 153.8e6 + 35.3e6,  # prefill_paged_kernel<0>
+    "fwd": 102.6e6 + 16.7e6,   # prefill_fwd2_kernel<128>
+    "decode_split": 1155.8e6 + 20.1e6,  # decode_split_kernel<0, 0, 0, 16, 0, 1>
+    "prefill_paged": 154.0e6 + 35.3e6,  # prefill_paged_kernel<0>
 }
 
 
@@ -172,10 +172,11 @@ def barrier(world):
         dist.barrier()
 
 
-def time_decode_graph(world, step, nbytes, calls=10, replays=5):
-    """The same decode calls captured once into a CUDA graph (the split kernel and the combine of
-    `calls` back-to-back calls) and replayed: per-call time and GB/s without host launch work.
-    A capture the runtime refuses is reported, not raised (every rank still joins the max)."""
+def time_graph(world, step, calls=10, replays=5):
+    """`calls` back-to-back calls of `step` captured once into a CUDA graph and replayed:
+    the time per call without host launch work (max over ranks).  Returns (ms, None), or
+    (None, reason) when the runtime refused the capture (reported, not raised; every rank
+    still joins the max)."""
     import torch
 
     err, g_ms = None, -1.0
@@ -204,7 +205,16 @@ def time_decode_graph(world, step, nbytes, calls=10, replays=5):
         err = f"{type(e).__name__}: {e}"[:200]
     g_ms = max_over_ranks(world, g_ms)
     if err is not None or g_ms <= 0:
-        return {"error": err or "capture failed on another rank"}
+        return None, err or "capture failed on another rank"
+    return g_ms, None
+
+
+def time_decode_graph(world, step, nbytes, calls=10, replays=5):
+    """The same decode calls captured once into a CUDA graph (the split kernel and the combine of
+    `calls` back-to-back calls) and replayed: per-call time and GB/s without host launch work."""
+    g_ms, err = time_graph(world, step, calls, replays)
+    if err is not None:
+        return {"error": err}
     return {"ms_per_call": round(g_ms, 4), "value": round(nbytes * world / (g_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
             "calls_per_graph": calls, "replays": replays}
 
@@ -645,6 +655,28 @@ def run_native(args):
     del gd, gout
     torch.cuda.empty_cache()
 
+    # ------------------------------------------------ the prefill step replayed from a CUDA graph
+    # (the same forward + backward calls as the timed steps, into buffers allocated once)
+    po = torch.empty((case.total, case.hq, case.dv), dtype=torch.bfloat16, device=dev)
+    plse = torch.empty((case.hq, case.total), dtype=torch.float32, device=dev)
+    pgrad = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v), dlog_gate=torch.empty_like(g),
+                 dsink=torch.empty_like(s))
+
+    def gstep_prefill():
+        gcs.attn_fwd(q, k, v, cu, ms, case.scale, case.window, g, s, out=po, lse=plse)
+        gcs.attn_bwd(q, k, v, po, plse, do, cu, ms, case.scale, case.window, g, s, **pgrad)
+
+    pg_ms, pg_err = time_graph(world, gstep_prefill)
+    if pg_err is None and gcs.get_device_status() != 0:
+        raise RuntimeError("a prefill kernel timed out")
+    prefill_graph = ({"error": pg_err} if pg_err is not None else
+                     {"ms_per_step": round(pg_ms, 4),
+                      "value": round(whole_job_rate(step_fl, world, pg_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                      "steps_per_graph": 10, "replays": 5,
+                      "note": "the timed step's calls captured into one CUDA graph: no host launch work between kernels"})
+    del po, plse, pgrad
+    torch.cuda.empty_cache()
+
     # ------------------------------------------------------------ CPU oracle baseline
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -674,6 +706,7 @@ def run_native(args):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "inputs and fp32 dQ buffer (~0.5 GB) larger than L2; no flush"},
         "roofline": roofline,
+        "graph": prefill_graph,
         "decode": decode,
         "chunked_prefill": chunked,
         "wide_prefill": wide,
@@ -835,6 +868,54 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def profile_case(args):
+    """Runs warmup + steps calls of one named workload through the library and nothing else:
+    a prefill config takes forward + backward steps, a decode config decode calls, the chunked
+    prefill config paged prefill calls.  A short, focused command for profiler captures; it
+    prints one line with the workload and the device status, and no bench line."""
+    import torch
+
+    import gated_causal_softmax_gb300 as gcs
+    from synth import DECODE_CONFIGS, PREFILL_CONFIGS, decode_config, prefill_config
+
+    name = args.profile_case
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    if name in PREFILL_CONFIGS:
+        case = prefill_config(name)
+        q, k, v, do = (t.to(dev) for t in (case.q, case.k, case.v, case.do))
+        g = case.log_gate.to(dev) if case.log_gate is not None else None
+        s = case.sink.to(dev) if case.sink is not None else None
+        cu = case.cu_seqlens.to(dev)
+        ms = max(case.seqlens)
+
+        def call():
+            o, lse = gcs.attn_fwd(q, k, v, cu, ms, case.scale, case.window, g, s)
+            gcs.attn_bwd(q, k, v, o, lse, do, cu, ms, case.scale, case.window, g, s)
+    elif name in DECODE_CONFIGS:
+        dc = decode_config(name)
+        d = dict(q=dc.q.to(dev), kc=dc.k_cache.to(dev), vc=dc.v_cache.to(dev), ks=dc.k_scale.to(dev),
+                 vs=dc.v_scale.to(dev), bt=dc.block_table.to(dev), sl=dc.seq_lens.to(dev), cq=dc.cu_q.to(dev))
+        out = torch.empty_like(d["q"])
+        maxq, maxl = max(dc.q_lens), int(dc.seq_lens.max())
+        paged_prefill = name == CHUNK_WORKLOAD
+        fn = gcs.attn_prefill_paged if paged_prefill else gcs.attn_decode_paged
+        seg = 0 if paged_prefill else dc.segment_len
+
+        def call():
+            fn(d["q"], d["kc"], d["vc"], d["ks"], d["vs"], d["bt"], d["sl"], d["cq"], maxq, maxl, dc.scale, seg,
+               out=out)
+    else:
+        raise SystemExit(f"unknown workload {name}")
+    for _ in range(args.warmup + args.steps):
+        call()
+    torch.cuda.synchronize()
+    status = gcs.get_device_status()
+    print(json.dumps({"profile_case": name, "calls": args.warmup + args.steps, "device_status": status}))
+    if status != 0:
+        raise SystemExit(1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -845,9 +926,13 @@ def main():
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the dominant kernel from an ncu capture")
     ap.add_argument("--decode-traffic", type=float, default=None)
+    ap.add_argument("--profile-case", default=None,
+                    help="run only this workload's calls (warmup + steps of them) for a profiler capture")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps
-    if args.impl == "reference":
+    if args.profile_case:
+        profile_case(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_native(args)

@@ -124,13 +124,15 @@ def test_decode_full_size_64x1_sampled(gcs_lib):
 
 
 def test_decode_full_size_verify_3x4_227k(gcs_lib):
+    """Three requests of 4 query positions at ~227K tokens of context: every row of every
+    request against the oracle."""
     dc = decode_config("paged_fp8_verify_3x4_227k")
     out = run_decode(gcs_lib, dc)
-    sub = make_sub(dc, [1])
-    ref = oracle_decode(sub)
-    got = f64(out)[int(dc.cu_q[1]) : int(dc.cu_q[2])]
-    assert_close("out", got, ref, DECODE_RTOL)
-    assert abs(bias(got, ref)) <= DECODE_BIAS
+    for r in range(len(dc.seq_lens)):
+        ref = oracle_decode(make_sub(dc, [r]))
+        got = f64(out)[int(dc.cu_q[r]) : int(dc.cu_q[r + 1])]
+        assert_close(f"out[request {r}]", got, ref, DECODE_RTOL)
+        assert abs(bias(got, ref)) <= DECODE_BIAS
 
 
 def make_sub(dc, reqs):

@@ -145,17 +145,20 @@ def _sampled_full_size(gcs_lib, name, kv_group=1, backward=True, seqs=None, dete
     return case, grads
 
 
-@pytest.mark.parametrize("deterministic", [False, True])
-def test_full_size_varlen_gqa_d128_sampled(gcs_lib, deterministic):
-    """Packed 1000/3000/4192, Hq=32, Hkv=8, D=128, gate + sink: every sequence of kv-head
-    group 5 against the oracle; the sink gradient of those heads over the whole batch.  Both
-    backward routes: the single pass (the bench's launch configuration) and the two passes."""
-    case, grads = _sampled_full_size(gcs_lib, "varlen_gqa_8192_d128", kv_group=5, deterministic=deterministic)
-    heads = list(range(20, 24))
+@pytest.mark.parametrize("deterministic,kv_group", [(False, 0), (False, 5), (False, 7), (True, 5)])
+def test_full_size_varlen_gqa_d128_sampled(gcs_lib, deterministic, kv_group):
+    """Packed 1000/3000/4192, Hq=32, Hkv=8, D=128, gate + sink: every sequence of one kv-head
+    group against the oracle; the sink gradient of those heads over the whole batch.  Both
+    backward routes: the single pass (the bench's launch configuration: the first, a middle
+    and the last group) and the two passes."""
+    case, grads = _sampled_full_size(gcs_lib, "varlen_gqa_8192_d128", kv_group=kv_group,
+                                     deterministic=deterministic)
+    group = case.hq // case.hkv
+    heads = list(range(kv_group * group, (kv_group + 1) * group))
     cu = case.cu_seqlens.numpy()
     _, _, _, _, rds = oracle.prefill_backward(
-        f64(case.q)[:, heads], f64(case.k)[:, [5]], f64(case.v)[:, [5]], f64(case.do)[:, heads], cu, case.scale,
-        log_gate=f64(case.log_gate)[:, heads], sink=f64(case.sink)[heads])
+        f64(case.q)[:, heads], f64(case.k)[:, [kv_group]], f64(case.v)[:, [kv_group]], f64(case.do)[:, heads], cu,
+        case.scale, log_gate=f64(case.log_gate)[:, heads], sink=f64(case.sink)[heads])
     assert_close("dsink", f64(grads[4])[heads], rds, PREFILL_RTOL)
 
 
