@@ -22,8 +22,9 @@
 // shared memory, one copy per query position, so the loop runs without register spills);
 // fp8 -> f16 conversion is exact,
 // QK^T and PV run on mma.sync m16n8k16 with fp32 accumulation, softmax in fp32 (log2
-// units).  P * vscale is scaled by 2^8 before the f16 rounding (round-to-nearest, no
-// truncation bias) and the factor is removed in fp32 afterwards.
+// units).  A row's reference max moves only when its max grows by more than 2^3, so P <= 8
+// and most pages skip the accumulator rescale; P * vscale is scaled by 2^5 before the f16
+// rounding (round-to-nearest, no truncation bias) and the factor is removed in fp32 afterwards.
 // decode_combine_kernel: LSE-weighted merge of the segments of each (query row, head).
 #include <mutex>
 
@@ -78,8 +79,12 @@ struct DecCfg {
 };
 constexpr int kThreads = 160;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kPScale = 256.f;
-constexpr float kInvPScale = 1.f / 256.f;
+// Each row's reference max moves only when the row max grows by more than 2^kLazy (log2 units),
+// so P <= 2^3; the fp8 path rounds P * vscale to f16 after a 2^5 pre-scale, which keeps
+// 2^3 * 255 * 2^5 = 65280 below the f16 maximum for every V scale below 255.
+constexpr float kLazy = 3.f;
+constexpr float kPScale = 32.f;
+constexpr float kInvPScale = 1.f / 32.f;
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
@@ -401,13 +406,16 @@ __global__ void __launch_bounds__(kThreads, 3)
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      // a row's reference max moves (and its accumulators are rescaled) only when the row max
+      // grows by more than 2^kLazy; a first finite max always moves it (-inf + kLazy = -inf)
       const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-      const float a0 = (n0 == neg_inf()) ? 1.f : ex2(m0 - n0);
-      const float a1 = (n1 == neg_inf()) ? 1.f : ex2(m1 - n1);
-      const float u0 = (n0 == neg_inf()) ? 0.f : n0;
-      const float u1 = (n1 == neg_inf()) ? 0.f : n1;
-      m0 = n0;
-      m1 = n1;
+      const bool up0 = n0 > m0 + kLazy, up1 = n1 > m1 + kLazy;
+      const float a0 = up0 ? ex2(m0 - n0) : 1.f;
+      const float a1 = up1 ? ex2(m1 - n1) : 1.f;
+      if (up0) m0 = n0;
+      if (up1) m1 = n1;
+      const float u0 = (m0 == neg_inf()) ? 0.f : m0;
+      const float u1 = (m1 == neg_inf()) ? 0.f : m1;
       float pr[2][4];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -416,8 +424,8 @@ __global__ void __launch_bounds__(kThreads, 3)
       }
       l0 = l0 * a0 + (pr[0][0] + pr[0][1]) + (pr[0][2] + pr[0][3]);
       l1 = l1 * a1 + (pr[1][0] + pr[1][1]) + (pr[1][2] + pr[1][3]);
-      // the accumulators change only where a row's max moved (the factor is 1 elsewhere)
-      if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
+      // the accumulators change only where a row's reference moved (the factor is 1 elsewhere)
+      if (__any_sync(0xffffffffu, up0 || up1)) {
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
           o[u][0] *= a0;
@@ -548,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     }
   }
   if (active && grp == 0) {
-    constexpr float kOut = KVF == 0 ? kInvPScale : 1.f;  // the fp8 path carries P scaled by 2^8
+    constexpr float kOut = KVF == 0 ? kInvPScale : 1.f;  // the fp8 path carries P scaled by 2^5
     const size_t unit = ((size_t)r * p.max_segs + seg) * p.hkv + kvh;
     const int rows = p.max_q_len * kRows;
     const size_t row0 = unit * rows + posA * G + headA;

@@ -181,8 +181,9 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
  * of 16.
  * Operand precision of an fp8 cache: the tensor cores see f16.  q is rounded from bf16 to f16,
  * so no |q| may exceed 65504 (the f16 maximum); K and V codes convert to f16 exactly;
- * P * vscale is rounded to nearest f16 after a 2^8 pre-scale (P <= 1), so every V scale of a
- * slot below seq_len must stay below 255.  Outside these limits the output holds inf or NaN.
+ * P * vscale is rounded to nearest f16 after a 2^5 pre-scale (P <= 2^3: a row's reference max
+ * moves only when the row max grows by more than 2^3), so every V scale of a slot below
+ * seq_len must stay below 255.  Outside these limits the output holds inf or NaN.
  * The host cannot read device values; checked mode (gcs_set_device_checks) checks both on the
  * device and records GCS_ERR_INVALID_ARG when one fails.
  */
