@@ -38,8 +38,9 @@ LARGE_WORKLOAD = "varlen_16384_d512"
 VERIFY_WORKLOAD = "paged_fp8_verify_3x4_227k"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # my kernels per prefill step with gates and sink: fwd (gate cumsum, attention) and bwd
-# (gate cumsum, delta, vector pack, dQ pass, dK/dV pass, d gate scan, d sink reduce)
-LAUNCHES_PER_PREFILL_STEP = 9
+# (gate cumsum + delta + zeroing, vector pack, single-pass attention, dQ conversion + d gate
+# scan + d sink reduce)
+LAUNCHES_PER_PREFILL_STEP = 6
 LAUNCHES_PER_DECODE = 2
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of each kernel on these
 # workloads, from one ncu capture of the kernel as it stands; set back to None whenever the

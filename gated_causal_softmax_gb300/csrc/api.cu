@@ -462,13 +462,26 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
     if (st != GCS_OK) return st;
     cu = cu_chk;
   }
-  if (gT) {
-    st = cuda_status(launch_gate_cumsum(a->log_gate, cu, a->num_seqs, a->total_tokens, a->hq, gT, s));
-    if (st != GCS_OK) return st;
-  }
-  st = cuda_status(launch_bwd_pre(static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dout),
-                                  a->total_tokens, a->hq, a->dv, a->dqk, lay.o.ts, lay.o.hs, lay.dout.ts,
-                                  lay.dout.hs, delta, dq_acc, dg_row, dg_col, s));
+  PreArgs pre{};
+  pre.o = static_cast<const uint16_t*>(o);
+  pre.dout = static_cast<const uint16_t*>(dout);
+  pre.total = a->total_tokens;
+  pre.hq = a->hq;
+  pre.dv = a->dv;
+  pre.dqk = a->dqk;
+  pre.o_ts = lay.o.ts;
+  pre.o_hs = lay.o.hs;
+  pre.do_ts = lay.dout.ts;
+  pre.do_hs = lay.dout.hs;
+  pre.delta = delta;
+  pre.dq_acc = dq_acc;
+  pre.dg_row = dg_row;
+  pre.dg_col = dg_col;
+  pre.g = a->log_gate;
+  pre.cu = cu;
+  pre.num_seqs = a->num_seqs;
+  pre.gT = gT;
+  st = cuda_status(launch_bwd_pre(pre, s));
   if (st != GCS_OK) return st;
 
   st = cuda_status(launch_bwd_pack(cu, a->num_seqs, a->total_tokens, a->hq, n_qtiles, lse, gT, delta,
@@ -533,9 +546,24 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
     timer.after();
   }
   if (st != GCS_OK) return st;
-  return cuda_status(launch_bwd_post(dq_acc, static_cast<uint16_t*>(dq), a->total_tokens, a->hq, a->dqk,
-                                     lay.dq.ts, lay.dq.hs, cu, a->num_seqs, dg_row, dg_col, dlog_gate, lse,
-                                     delta, a->sink, dsink, s));
+  PostArgs post{};
+  post.dq_acc = dq_acc;
+  post.dq = static_cast<uint16_t*>(dq);
+  post.total = a->total_tokens;
+  post.hq = a->hq;
+  post.dqk = a->dqk;
+  post.dq_ts = lay.dq.ts;
+  post.dq_hs = lay.dq.hs;
+  post.cu = cu;
+  post.num_seqs = a->num_seqs;
+  post.dg_row = dg_row;
+  post.dg_col = dg_col;
+  post.dlog_gate = dlog_gate;
+  post.lse = lse;
+  post.delta = delta;
+  post.sink = a->sink;
+  post.dsink = dsink;
+  return cuda_status(launch_bwd_post(post, s));
 }
 
 // Byte strides of the paged caches; all-zero element strides = contiguous

@@ -80,17 +80,50 @@ cudaError_t launch_prefill_bwd_wide(const BwdParams& p, const BwdMaps& maps, int
 // Small HBM-bound helpers.
 cudaError_t launch_gate_cumsum(const float* g, const int32_t* cu, int num_seqs, int total, int hq, float* gT,
                                cudaStream_t s);
-cudaError_t launch_bwd_pre(const uint16_t* o, const uint16_t* dout, int total, int hq, int dv, int dqk,
-                           long long o_ts, long long o_hs, long long do_ts, long long do_hs, float* delta,
-                           float* dq_acc, float* dg_row, float* dg_col, cudaStream_t s);
+// Before the backward attention kernels, one launch: G (when gT is set; the gate cumsum of
+// the log gates g) beside delta_i = dO_i . O_i and the zeroing of the fp32 dQ accumulator and
+// the dS row / column sums (each where set).  n_scan is set by the launcher.
+struct PreArgs {
+  const uint16_t* o;
+  const uint16_t* dout;
+  int total, hq, dv, dqk;
+  long long o_ts, o_hs, do_ts, do_hs;  // element strides (token, head)
+  float* delta;                        // [hq, total]
+  float* dq_acc;                       // [total, hq, dqk] or null
+  float* dg_row;                       // [hq, total] or null
+  float* dg_col;                       // [hq, total] or null
+  const float* g;                      // log gates [total, hq] (with gT)
+  const int32_t* cu;
+  int num_seqs;
+  float* gT;                           // [hq, total] or null
+  int n_scan;
+};
+cudaError_t launch_bwd_pre(const PreArgs& a, cudaStream_t s);
 // Packs (G_i - LSE_i) * log2 e and delta_i per (head, 64-row query tile): vecp
 // [hq][n_qtiles][128] with n_qtiles = ceil(total / 64) + num_seqs.
 cudaError_t launch_bwd_pack(const int32_t* cu, int num_seqs, int total, int hq, int n_qtiles, const float* lse,
                             const float* gT, const float* delta, float* vecp, cudaStream_t s);
-cudaError_t launch_bwd_post(const float* dq_acc, uint16_t* dq, int total, int hq, int dqk, long long dq_ts,
-                            long long dq_hs, const int32_t* cu, int num_seqs, const float* dg_row,
-                            const float* dg_col, float* dlog_gate, const float* lse, const float* delta,
-                            const float* sink, float* dsink, cudaStream_t s);
+// After the backward attention kernels, one launch: the dQ conversion (when dq_acc is set),
+// d log_gate (when dlog_gate is set) and d sink (when dsink is set).  n4, n_gate and n_sink are
+// set by the launcher.
+struct PostArgs {
+  const float* dq_acc;  // [total, hq, dqk] fp32 or null
+  uint16_t* dq;
+  int total, hq, dqk;
+  long long dq_ts, dq_hs;
+  const int32_t* cu;
+  int num_seqs;
+  const float* dg_row;  // [hq, total]
+  const float* dg_col;  // [hq, total]
+  float* dlog_gate;     // [total, hq] or null
+  const float* lse;     // [hq, total]
+  const float* delta;   // [hq, total]
+  const float* sink;    // [hq]
+  float* dsink;         // [hq] or null
+  size_t n4;
+  int n_gate, n_sink;
+};
+cudaError_t launch_bwd_post(const PostArgs& a, cudaStream_t s);
 
 struct DecodeParams {
   const int32_t* cu_q;

@@ -48,12 +48,10 @@ __device__ __forceinline__ float block_scan(float x, float* warp_sums, float* to
   return x + before;
 }
 
-// grid (num_seqs, hq)
-__global__ void __launch_bounds__(kScanThreads) gate_cumsum_kernel(const float* __restrict__ g,
-                                                                   const int32_t* __restrict__ cu, int total, int hq,
-                                                                   float* __restrict__ gT) {
-  __shared__ float warp_sums[kScanThreads / 32];
-  const int s = blockIdx.x, h = blockIdx.y;
+// G of sequence s, head h by one kScanThreads-thread block.
+__device__ __forceinline__ void gate_cumsum_block(const float* __restrict__ g, const int32_t* __restrict__ cu,
+                                                  int total, int hq, float* __restrict__ gT, int s, int h,
+                                                  float* warp_sums) {
   const int a = __ldg(cu + s), b = __ldg(cu + s + 1);
   float carry = 0.f;
   for (int base = a; base < b; base += kScanThreads * kScanPer) {
@@ -77,82 +75,105 @@ __global__ void __launch_bounds__(kScanThreads) gate_cumsum_kernel(const float* 
   }
 }
 
+// grid (num_seqs, hq)
+__global__ void __launch_bounds__(kScanThreads) gate_cumsum_kernel(const float* __restrict__ g,
+                                                                   const int32_t* __restrict__ cu, int total, int hq,
+                                                                   float* __restrict__ gT) {
+  __shared__ float warp_sums[kScanThreads / 32];
+  gate_cumsum_block(g, cu, total, hq, gT, blockIdx.x, blockIdx.y, warp_sums);
+}
+
 // L = min(32, dv / 8) lanes per (token, head) row, 8 elements (16 B of O and of dO) per lane
-// and chunk; each warp takes 32 / L consecutive rows at a time, grid-stride.  The loop is
-// uniform across the warp (rows past the end load nothing), so the shuffles see every lane.
-// O and dO rows sit at token * ts + head * hs (element strides; dims contiguous).
+// and chunk; each warp takes 32 / L consecutive rows at a time, grid-stride over the role's
+// blocks.  The loop is uniform across the warp (rows past the end load nothing), so the
+// shuffles see every lane.  O and dO rows sit at token * ts + head * hs (element strides;
+// dims contiguous).  The same lanes zero the row's fp32 dQ accumulator ([total, hq, dqk],
+// contiguous) and its entries of the dS row and column sums ([hq, total]).
 template <int L>
-__global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict__ o,
-                                                      const uint16_t* __restrict__ dout, int total, int hq, int dv,
-                                                      long long o_ts, long long o_hs, long long do_ts,
-                                                      long long do_hs, float* __restrict__ delta) {
+__device__ __forceinline__ void pre_rows(const PreArgs& a, int blk, int nblk) {
   constexpr int kRowsPerWarp = 32 / L;
   const int lane = threadIdx.x & (L - 1);
   const int group = (threadIdx.x & 31) / L;
-  const int rows = total * hq;
-  const int chunks = dv / (8 * L);
-  const int warps = gridDim.x * (blockDim.x >> 5);
-  for (int row0 = (blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * kRowsPerWarp; row0 < rows;
+  const int rows = a.total * a.hq;
+  const int chunks = a.dv / (8 * L);
+  const int warps = nblk * (blockDim.x >> 5);
+  for (int row0 = (blk * (blockDim.x >> 5) + (threadIdx.x >> 5)) * kRowsPerWarp; row0 < rows;
        row0 += warps * kRowsPerWarp) {
     const int row = row0 + group;
     const bool valid = row < rows;
+    const int t = valid ? row / a.hq : 0, h = valid ? row % a.hq : 0;
     float acc0 = 0.f, acc1 = 0.f;
     if (valid) {
-      const long long t = row / hq, h = row % hq;
-      const uint4* po = reinterpret_cast<const uint4*>(o + t * o_ts + h * o_hs);
-      const uint4* pd = reinterpret_cast<const uint4*>(dout + t * do_ts + h * do_hs);
+      const uint4* po = reinterpret_cast<const uint4*>(a.o + (long long)t * a.o_ts + (long long)h * a.o_hs);
+      const uint4* pd = reinterpret_cast<const uint4*>(a.dout + (long long)t * a.do_ts + (long long)h * a.do_hs);
       for (int c = 0; c < chunks; ++c) {
-        const uint4 a = __ldg(po + c * L + lane), b = __ldg(pd + c * L + lane);
-        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+        const uint4 x = __ldg(po + c * L + lane), y = __ldg(pd + c * L + lane);
+        const uint32_t aw[4] = {x.x, x.y, x.z, x.w}, bw[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           acc0 = fmaf(__uint_as_float(aw[k] << 16), __uint_as_float(bw[k] << 16), acc0);
           acc1 = fmaf(__uint_as_float(aw[k] & 0xffff0000u), __uint_as_float(bw[k] & 0xffff0000u), acc1);
         }
       }
+      if (a.dq_acc) {
+        float4* z = reinterpret_cast<float4*>(a.dq_acc + (size_t)row * a.dqk);
+        for (int c = lane; c < a.dqk / 4; c += L) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
     float acc = acc0 + acc1;
 #pragma unroll
     for (int off = L / 2; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, L);
     if (valid && lane == 0) {
-      const int t = row / hq, h = row % hq;
-      delta[(size_t)h * total + t] = acc;
+      const size_t idx = (size_t)h * a.total + t;
+      a.delta[idx] = acc;
+      if (a.dg_row) a.dg_row[idx] = 0.f;
+      if (a.dg_col) a.dg_col[idx] = 0.f;
     }
   }
 }
 
-// fp32 dQ accumulator [total, hq, dqk] (contiguous) -> bf16 dQ at token * ts + head * hs.
-__global__ void __launch_bounds__(256) dq_convert_kernel(const float4* __restrict__ src, uint16_t* __restrict__ dst,
-                                                         size_t n4, int hq, int dqk, long long ts, long long hs) {
-  const int q4 = dqk / 4;
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+// Blocks [0, n_scan): the gate cumsum of (sequence b / hq, head b % hq); the rest: delta and
+// the zeroing above.  The two roles touch disjoint data, so one launch runs them side by side.
+template <int L>
+__global__ void __launch_bounds__(kScanThreads) bwd_pre_kernel(const PreArgs a) {
+  __shared__ float warp_sums[kScanThreads / 32];
+  if ((int)blockIdx.x < a.n_scan) {
+    gate_cumsum_block(a.g, a.cu, a.total, a.hq, a.gT, blockIdx.x / a.hq, blockIdx.x % a.hq, warp_sums);
+    return;
+  }
+  pre_rows<L>(a, blockIdx.x - a.n_scan, gridDim.x - a.n_scan);
+}
+
+// fp32 dQ accumulator [total, hq, dqk] (contiguous) -> bf16 dQ at token * ts + head * hs,
+// grid-stride over the role's blocks.
+__device__ __forceinline__ void dq_convert_range(const PostArgs& a, int blk, int nblk) {
+  const float4* src = reinterpret_cast<const float4*>(a.dq_acc);
+  const int q4 = a.dqk / 4;
+  for (size_t i = blk * (size_t)blockDim.x + threadIdx.x; i < a.n4; i += (size_t)nblk * blockDim.x) {
     const float4 v = src[i];
     const size_t rh = i / q4;
-    const long long d = (long long)(i % q4) * 4, h = (long long)(rh % hq), t = (long long)(rh / hq);
-    *reinterpret_cast<uint2*>(dst + t * ts + h * hs + d) = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+    const long long d = (long long)(i % q4) * 4, h = (long long)(rh % a.hq), t = (long long)(rh / a.hq);
+    *reinterpret_cast<uint2*>(a.dq + t * a.dq_ts + h * a.dq_hs + d) =
+        make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
   }
 }
 
-// grid (num_seqs, hq): dg_t = sum_{u >= t} (row_u - col_u), scanned from the sequence end.
-__global__ void __launch_bounds__(kScanThreads) dgate_kernel(const float* __restrict__ row,
-                                                             const float* __restrict__ col,
-                                                             const int32_t* __restrict__ cu, int total, int hq,
-                                                             float* __restrict__ dg) {
-  __shared__ float warp_sums[kScanThreads / 32];
-  const int s = blockIdx.x, h = blockIdx.y;
-  const int a = __ldg(cu + s), b = __ldg(cu + s + 1);
-  const float* rr = row + (size_t)h * total;
-  const float* cc = col + (size_t)h * total;
+// d log_gate of sequence s, head h: dg_t = sum_{u >= t} (row_u - col_u), scanned from the
+// sequence end by one kScanThreads-thread block.
+__device__ __forceinline__ void dgate_block(const PostArgs& a, int s, int h, float* warp_sums) {
+  const int lo = __ldg(a.cu + s), hi = __ldg(a.cu + s + 1);
+  const float* rr = a.dg_row + (size_t)h * a.total;
+  const float* cc = a.dg_col + (size_t)h * a.total;
   float carry = 0.f;
-  // walk backwards: element k of the reversed sequence is token b - 1 - k
-  for (int base = 0; base < b - a; base += kScanThreads * kScanPer) {
+  // walk backwards: element k of the reversed sequence is token hi - 1 - k
+  for (int base = 0; base < hi - lo; base += kScanThreads * kScanPer) {
     float v[kScanPer];
     float local = 0.f;
 #pragma unroll
     for (int u = 0; u < kScanPer; ++u) {
       const int k = base + threadIdx.x * kScanPer + u;
-      const int t = b - 1 - k;
-      local += (t >= a) ? (rr[t] - cc[t]) : 0.f;
+      const int t = hi - 1 - k;
+      local += (t >= lo) ? (rr[t] - cc[t]) : 0.f;
       v[u] = local;
     }
     float chunk_total;
@@ -161,47 +182,61 @@ __global__ void __launch_bounds__(kScanThreads) dgate_kernel(const float* __rest
 #pragma unroll
     for (int u = 0; u < kScanPer; ++u) {
       const int k = base + threadIdx.x * kScanPer + u;
-      const int t = b - 1 - k;
-      if (t >= a) dg[(size_t)t * hq + h] = excl + v[u];
+      const int t = hi - 1 - k;
+      if (t >= lo) a.dlog_gate[(size_t)t * a.hq + h] = excl + v[u];
     }
     carry += chunk_total;
   }
 }
 
-// grid (hq), 1024 threads: dsink_h = -sum_i p_i (rowsum_i + delta_i (1 - p_i)), p_i = e^{sigma_h - lse_i};
-// four independent rows per thread and iteration keep loads in flight.  One block per head
-// sums in a fixed order, so the result does not depend on scheduling.
-__global__ void __launch_bounds__(1024) dsink_kernel(const float* __restrict__ row, const float* __restrict__ lse,
-                                                     const float* __restrict__ delta, const float* __restrict__ sink,
-                                                     int total, float* __restrict__ dsink) {
-  __shared__ float red[32];
-  const int h = blockIdx.x;
-  const float sig = __ldg(sink + h);
-  const float* rr = row + (size_t)h * total;
-  const float* ll = lse + (size_t)h * total;
-  const float* dd = delta + (size_t)h * total;
+// dsink_h = -sum_i p_i (rowsum_i + delta_i (1 - p_i)), p_i = e^{sigma_h - lse_i}, by one
+// 1024-thread block; four independent rows per thread and iteration keep loads in flight.
+// One block per head sums in a fixed order, so the result does not depend on scheduling.
+__device__ __forceinline__ void dsink_block(const PostArgs& a, int h, float* red) {
+  const float sig = __ldg(a.sink + h);
+  const float* rr = a.dg_row + (size_t)h * a.total;
+  const float* ll = a.lse + (size_t)h * a.total;
+  const float* dd = a.delta + (size_t)h * a.total;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int base = 0; base < total; base += 4 * 1024) {
+  for (int base = 0; base < a.total; base += 4 * 1024) {
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int t = base + u * 1024 + threadIdx.x;
-      if (t < total) {
+      if (t < a.total) {
         const float ps = __expf(sig - __ldg(ll + t));
         acc[u] += ps * (__ldg(rr + t) + __ldg(dd + t) * (1.f - ps));
       }
     }
   }
-  float a = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+  float x = (acc[0] + acc[1]) + (acc[2] + acc[3]);
 #pragma unroll
-  for (int off = 16; off; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = a;
+  for (int off = 16; off; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = x;
   __syncthreads();
   if (threadIdx.x < 32) {
-    a = red[threadIdx.x];
+    x = red[threadIdx.x];
 #pragma unroll
-    for (int off = 16; off; off >>= 1) a += __shfl_xor_sync(0xffffffffu, a, off);
-    if (threadIdx.x == 0) dsink[h] = -a;
+    for (int off = 16; off; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    if (threadIdx.x == 0) a.dsink[h] = -x;
   }
+}
+
+// Blocks [0, n_gate): d log_gate of (sequence b / hq, head b % hq); [n_gate, n_gate + n_sink):
+// d sink of head b - n_gate; the rest: the dQ conversion.  The roles write disjoint outputs, so
+// one launch runs the latency-bound scans beside the bandwidth-bound conversion.
+__global__ void __launch_bounds__(1024) bwd_post_kernel(const PostArgs a) {
+  __shared__ float sm[32];
+  int b = blockIdx.x;
+  if (b < a.n_gate) {
+    dgate_block(a, b / a.hq, b % a.hq, sm);
+    return;
+  }
+  b -= a.n_gate;
+  if (b < a.n_sink) {
+    dsink_block(a, b, sm);
+    return;
+  }
+  dq_convert_range(a, b - a.n_sink, gridDim.x - a.n_gate - a.n_sink);
 }
 
 // grid (query tiles of 64 rows over all sequences, hq), 64 threads: packs the per-column
@@ -252,49 +287,29 @@ cudaError_t launch_gate_cumsum(const float* g, const int32_t* cu, int num_seqs, 
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_pre(const uint16_t* o, const uint16_t* dout, int total, int hq, int dv, int dqk,
-                           long long o_ts, long long o_hs, long long do_ts, long long do_hs, float* delta,
-                           float* dq_acc, float* dg_row, float* dg_col, cudaStream_t s) {
-  // enough blocks to fill the GPU several times over; rows are grid-stride
-  const int L = dv >= 256 ? 32 : dv / 8;
-  const long long lanes = (long long)total * hq * L;
-  const int blocks = (int)std::min<long long>((lanes + 255) / 256, 152 * 16);
-  if (L == 8) bwd_pre_kernel<8><<<blocks, 256, 0, s>>>(o, dout, total, hq, dv, o_ts, o_hs, do_ts, do_hs, delta);
-  else if (L == 16) bwd_pre_kernel<16><<<blocks, 256, 0, s>>>(o, dout, total, hq, dv, o_ts, o_hs, do_ts, do_hs, delta);
-  else bwd_pre_kernel<32><<<blocks, 256, 0, s>>>(o, dout, total, hq, dv, o_ts, o_hs, do_ts, do_hs, delta);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  if (dq_acc) e = cudaMemsetAsync(dq_acc, 0, (size_t)total * hq * dqk * sizeof(float), s);
-  if (e != cudaSuccess) return e;
-  if (dg_row) e = cudaMemsetAsync(dg_row, 0, (size_t)total * hq * sizeof(float), s);
-  if (e != cudaSuccess) return e;
-  if (dg_col) e = cudaMemsetAsync(dg_col, 0, (size_t)total * hq * sizeof(float), s);
-  return e;
+cudaError_t launch_bwd_pre(const PreArgs& args, cudaStream_t s) {
+  PreArgs a = args;
+  a.n_scan = a.gT ? a.num_seqs * a.hq : 0;
+  // enough row blocks to fill the GPU several times over; rows are grid-stride
+  const int L = a.dv >= 256 ? 32 : a.dv / 8;
+  const long long lanes = (long long)a.total * a.hq * L;
+  const int blocks = a.n_scan + (int)std::min<long long>((lanes + kScanThreads - 1) / kScanThreads, 152 * 4);
+  if (L == 8) bwd_pre_kernel<8><<<blocks, kScanThreads, 0, s>>>(a);
+  else if (L == 16) bwd_pre_kernel<16><<<blocks, kScanThreads, 0, s>>>(a);
+  else bwd_pre_kernel<32><<<blocks, kScanThreads, 0, s>>>(a);
+  return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_post(const float* dq_acc, uint16_t* dq, int total, int hq, int dqk, long long dq_ts,
-                            long long dq_hs, const int32_t* cu, int num_seqs, const float* dg_row,
-                            const float* dg_col, float* dlog_gate, const float* lse, const float* delta,
-                            const float* sink, float* dsink, cudaStream_t s) {
-  cudaError_t e = cudaSuccess;
-  if (dq_acc) {
-    const size_t n4 = (size_t)total * hq * dqk / 4;
-    const int blocks = (int)((n4 + 255) / 256 < 152 * 16 ? (n4 + 255) / 256 : 152 * 16);
-    dq_convert_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(dq_acc), dq, n4, hq, dqk, dq_ts,
-                                             dq_hs);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  if (dlog_gate) {
-    dgate_kernel<<<dim3(num_seqs, hq), kScanThreads, 0, s>>>(dg_row, dg_col, cu, total, hq, dlog_gate);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  if (dsink) {
-    dsink_kernel<<<hq, 1024, 0, s>>>(dg_row, lse, delta, sink, total, dsink);
-    e = cudaGetLastError();
-  }
-  return e;
+cudaError_t launch_bwd_post(const PostArgs& args, cudaStream_t s) {
+  PostArgs a = args;
+  a.n4 = a.dq_acc ? (size_t)a.total * a.hq * a.dqk / 4 : 0;
+  a.n_gate = a.dlog_gate ? a.num_seqs * a.hq : 0;
+  a.n_sink = a.dsink ? a.hq : 0;
+  const int n_conv = (int)std::min<size_t>((a.n4 + 1023) / 1024, 152 * 4);
+  const int blocks = a.n_gate + a.n_sink + n_conv;
+  if (blocks == 0) return cudaSuccess;
+  bwd_post_kernel<<<blocks, 1024, 0, s>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace gcs
