@@ -193,7 +193,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idS = idesc_bf16(128, BM, false, false);  // S^T, dP^T
-      const uint32_t idAcc = idesc_bf16(128, 64, false, true);  // dV / dK, one 64-column chunk
+      const uint32_t idAcc = idesc_bf16(128, 64, false, true);   // dV / dK, one 64-column chunk
+      const uint32_t idAcc2 = idesc_bf16(128, 128, false, true); // two chunks in adjacent stages
       const uint32_t idDQ = idesc_bf16(128, BM, true, true);    // dQ^T half
       const uint32_t sRes = smem_u32(smem + C::OFF_KRES), sRing = smem_u32(smem + C::OFF_RING);
       const uint32_t sDS = smem_u32(smem + C::OFF_DS);
@@ -261,17 +262,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = wait_bar(p_full, s & 1, ab);
         if (!ok) break;
         tc_fence_after();
-        // accumulator += (P^T or dS^T) x (dO or Q) chunk by chunk (N = 64 each)
+        // accumulator += (P^T or dS^T) x (dO or Q): a pair of 64-column chunks in adjacent ring
+        // stages as one N = 128 MMA (LBO = one stage; an N = 64 MMA costs nearly as much as an
+        // N = 128 one), a lone chunk with N = 64
         const uint32_t aT = tmem + (KIND >= 1 ? C::T_DP : C::T_S);
-        for (int c = 0; c < C::WCH && ok; ++c) {
+        for (int c = 0; c < C::WCH && ok;) {
+          const bool pair = c + 1 < C::WCH && stage + 1 < C::NST;
           uint32_t bq = 0;
           ok = take(bq);
+          if (ok && pair) ok = wait_bar(&full[stage + 1], phase, ab);
           if (!ok) break;
+          tc_fence_after();
 #pragma unroll
           for (int k = 0; k < BM / 16; ++k)
-            mma_ts(tmem + C::T_ACC + c * 64, aT + k * 8, sdesc_sw128(bq + k * 2048, kStage, 1024), idAcc,
-                   (s > 0 || k > 0) ? 1u : 0u);
+            mma_ts(tmem + C::T_ACC + c * 64, aT + k * 8, sdesc_sw128(bq + k * 2048, kStage, 1024),
+                   pair ? idAcc2 : idAcc, (s > 0 || k > 0) ? 1u : 0u);
           give();
+          if (pair) give();
+          c += pair ? 2 : 1;
         }
         if (!ok) break;
         if (KIND == 1) {

@@ -165,7 +165,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idS = idesc_bf16(128, kBN, false, false);
+      // P V per pair of 64-column value chunks in adjacent ring stages as one N = 128 MMA (LBO =
+      // one stage; an N = 64 MMA costs nearly as much as an N = 128 one), a lone chunk with N = 64
       const uint32_t idPV = idesc_bf16(128, 64, false, true);
+      const uint32_t idPV2 = idesc_bf16(128, 128, false, true);
       const uint32_t sQ = smem_u32(smem + C::OFF_Q);
       const uint32_t sRing = smem_u32(smem + C::OFF_RING);
       uint32_t stage = 0, phase = 0;
@@ -199,17 +202,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           tc_fence_after();
           const uint32_t aP = tmem + bm * 128;
-          for (int c = 0; c < C::VCH && ok; ++c) {
+          for (int c = 0; c < C::VCH && ok;) {
+            const bool pair = c + 1 < C::VCH && stage + 1 < C::NST;
             ok = wait_bar(&kv_full[stage], phase, ab);
+            if (ok && pair) ok = wait_bar(&kv_full[stage + 1], phase, ab);
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
               const uint64_t bd = sdesc_sw128(sRing + stage * kChunk + k * 2048, kChunk, 1024);
-              mma_ts(tO + c * 64, aP + k * 8, bd, idPV, (m > 0 || k > 0) ? 1u : 0u);
+              mma_ts(tO + c * 64, aP + k * 8, bd, pair ? idPV2 : idPV, (m > 0 || k > 0) ? 1u : 0u);
             }
-            mma_commit(&kv_empty[stage]);
-            if (++stage == C::NST) { stage = 0; phase ^= 1; }
+            for (int u = 0; u < (pair ? 2 : 1); ++u) {
+              mma_commit(&kv_empty[stage]);
+              if (++stage == C::NST) { stage = 0; phase ^= 1; }
+            }
+            c += pair ? 2 : 1;
           }
           if (!ok) break;
           mma_commit(&pv_done[bm]);
