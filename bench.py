@@ -48,7 +48,7 @@ LAUNCHES_PER_DECODE = 2
 NCU_TRAFFIC = {
     "bwd": 549.2e6 + 247.0e6,  # prefill_bwd_fused_kernel
     "fwd": 102.6e6 + 16.7e6,   # prefill_fwd2_kernel<128>
-    "decode_split": 1155.8e6 + 20.1e6,  # decode_split_kernel<0, 0, 0, 16, 0, 1>
+    "decode_split": 1155.7e6 + 19.7e6,  # decode_split_kernel<0, 0, 0, 16, 0, 1>
     "prefill_paged": 154.0e6 + 35.3e6,  # prefill_paged_kernel<0>
 }
 
@@ -657,7 +657,10 @@ def run_native(args):
     torch.cuda.empty_cache()
 
     # ------------------------------------------------ the prefill step replayed from a CUDA graph
-    # (the same forward + backward calls as the timed steps, into buffers allocated once)
+    # (the same forward + backward calls as the timed steps, on inputs copied in again and into
+    # buffers allocated once)
+    q, k, v, do = (t.to(dev) for t in (case.q, case.k, case.v, case.do))
+    g, s, cu = case.log_gate.to(dev), case.sink.to(dev), case.cu_seqlens.to(dev)
     po = torch.empty((case.total, case.hq, case.dv), dtype=torch.bfloat16, device=dev)
     plse = torch.empty((case.hq, case.total), dtype=torch.float32, device=dev)
     pgrad = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v), dlog_gate=torch.empty_like(g),
@@ -675,7 +678,7 @@ def run_native(args):
                       "value": round(whole_job_rate(step_fl, world, pg_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                       "steps_per_graph": 10, "replays": 5,
                       "note": "the timed step's calls captured into one CUDA graph: no host launch work between kernels"})
-    del po, plse, pgrad
+    del po, plse, pgrad, q, k, v, do, g, s, cu
     torch.cuda.empty_cache()
 
     # ------------------------------------------------------------ CPU oracle baseline
