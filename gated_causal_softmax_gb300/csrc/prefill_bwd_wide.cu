@@ -10,7 +10,7 @@
 //   role K   (kind 2):  dK[:, k0 : k0+256) only, for the deterministic backward, whose dQ and
 //                       dS row sums come from the query-stationary pass (prefill_bwd_wide_dq.cu)
 // Every role recomputes the full-width contractions it needs; the extra work is the price
-// of fitting the accumulators in TMEM.  Operands stream through a ring of 16 KB stages
+// of fitting the accumulators in TMEM.  The K-side and dV roles of a call run in one launch.  Operands stream through a ring of 16 KB stages
 // (128 x 64 or 64 x 64 bf16 chunks, 128-B swizzle); the K columns a role keeps using
 // (its own 256 dims) stay resident.  One softmax warpgroup, one thread per key row.
 // Per query step of BM rows (s = step; the pipeline is sequential per step):
@@ -62,11 +62,11 @@ struct WideCfg {
   static_assert(T_ACC + 256 <= 512, "TMEM columns");
 };
 
+// One role of one (128-key tile, kv head): role index `role` of its kind (output columns
+// 256 role ..), tile blockIdx.y, kv head blockIdx.x.
 template <int DQK, int DV, int KIND, int BM>
-__global__ void __launch_bounds__(kThreads, 1)
-    prefill_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                            const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                            const BwdParams p) {
+__device__ __forceinline__ void wide_role(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                          const CUtensorMap& tmDO, const BwdParams& p, int role) {
   using C = WideCfg<DQK, DV, KIND, BM>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!lpt_tile(p.cu_seqlens, p.num_seqs, kBN, blockIdx.y, tr)) return;
   const int seq_start = tr.start, len = tr.len, jt = tr.n - 1 - tr.u;
   const int kvh = blockIdx.x;
-  const int w0 = blockIdx.z * kW;         // v0 (role V) or k0 (roles KQ, K)
+  const int w0 = role * kW;               // v0 (role V) or k0 (roles KQ, K)
   const int res0 = (KIND >= 1) ? w0 / 64 : 0;  // first resident K chunk
   const int group = p.hq / p.hkv;
   const int j0 = jt * kBN;
@@ -470,26 +470,41 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int DQK, int DV, int KIND>
-cudaError_t launch_t(const BwdParams& p, const BwdMaps& maps, int num_tiles, cudaStream_t s) {
-  constexpr int BM = KIND == 1 ? 64 : 128;
-  using C = WideCfg<DQK, DV, KIND, BM>;
-  auto kern = prefill_bwd_wide_kernel<DQK, DV, KIND, BM>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+// Both kinds of role in one launch, so that the dV roles fill the SMs the heavier dK roles'
+// last wave leaves idle: blockIdx.z < DQK / 256 selects a dK role (KQ_KIND: 1 with dQ, 2 without),
+// the rest the dV roles.  The K-side roles come first (they are dispatched first).
+template <int DQK, int DV, int KQ_KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_bwd_wide_kernel(const __grid_constant__ CUtensorMap tmQ64, const __grid_constant__ CUtensorMap tmQ128,
+                            const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                            const __grid_constant__ CUtensorMap tmDO64, const __grid_constant__ CUtensorMap tmDO128,
+                            const BwdParams p) {
+  constexpr int nk = DQK / kW;
+  constexpr int bk = KQ_KIND == 1 ? 64 : 128;  // query rows per step of the K-side role
+  if ((int)blockIdx.z < nk)
+    wide_role<DQK, DV, KQ_KIND, bk>(bk == 64 ? tmQ64 : tmQ128, tmK, tmV, bk == 64 ? tmDO64 : tmDO128, p, blockIdx.z);
+  else
+    wide_role<DQK, DV, 0, 128>(tmQ128, tmK, tmV, tmDO128, p, blockIdx.z - nk);
+}
+
+template <int DQK, int DV, int KQ_KIND>
+cudaError_t launch_roles(const BwdParams& p, const BwdMaps& maps, int num_tiles, cudaStream_t s) {
+  constexpr int bk = KQ_KIND == 1 ? 64 : 128;
+  constexpr int smem = WideCfg<DQK, DV, KQ_KIND, bk>::SMEM > WideCfg<DQK, DV, 0, 128>::SMEM
+                           ? WideCfg<DQK, DV, KQ_KIND, bk>::SMEM
+                           : WideCfg<DQK, DV, 0, 128>::SMEM;
+  auto kern = prefill_bwd_wide_kernel<DQK, DV, KQ_KIND>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const int roles = (KIND >= 1 ? DQK : DV) / kW;
-  // query and dO boxes of BM rows
-  const CUtensorMap& mq = BM == 128 ? maps.q128 : maps.q;
-  const CUtensorMap& mdo = BM == 128 ? maps.dout128 : maps.dout;
-  kern<<<dim3(p.hkv, num_tiles, roles), kThreads, C::SMEM, s>>>(mq, maps.k, maps.v, mdo, p);
+  const int roles = DQK / kW + DV / kW;
+  kern<<<dim3(p.hkv, num_tiles, roles), kThreads, smem, s>>>(maps.q, maps.q128, maps.k, maps.v, maps.dout,
+                                                             maps.dout128, p);
   return cudaGetLastError();
 }
 
 template <int DQK, int DV>
 cudaError_t launch_both(const BwdParams& p, const BwdMaps& maps, int num_tiles, bool with_dq, cudaStream_t s) {
-  cudaError_t e = with_dq ? launch_t<DQK, DV, 1>(p, maps, num_tiles, s) : launch_t<DQK, DV, 2>(p, maps, num_tiles, s);
-  if (e != cudaSuccess) return e;
-  return launch_t<DQK, DV, 0>(p, maps, num_tiles, s);
+  return with_dq ? launch_roles<DQK, DV, 1>(p, maps, num_tiles, s) : launch_roles<DQK, DV, 2>(p, maps, num_tiles, s);
 }
 
 }  // namespace
