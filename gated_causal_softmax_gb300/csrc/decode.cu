@@ -583,8 +583,23 @@ __global__ void __launch_bounds__(kThreads, 3)
   }
 }
 
-// One CTA per (request, query position) x kv head; 256 threads = 16 heads x 16 threads,
-// 8 value dims per thread.
+// Online merge of a partial (m2, l2, a2) into (m, l, a): both are relative to their own
+// reference max (log2 units); an empty partial has m = -inf and weighs 0.
+__device__ __forceinline__ void merge_partial(float& m, float& l, float (&a)[8], float m2, float l2,
+                                              const float (&a2)[8]) {
+  const float M = fmaxf(m, m2);
+  const float w1 = (m == neg_inf()) ? 0.f : ex2(m - M);
+  const float w2 = (m2 == neg_inf()) ? 0.f : ex2(m2 - M);
+  l = w1 * l + w2 * l2;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) a[j] = w1 * a[j] + w2 * a2[j];
+  m = M;
+}
+
+// One CTA per (request x query position, kv head, 4 query heads); 256 threads = 4 heads x
+// 16 groups of 8 value dims x 4 segment lanes.  The four lanes of a (head, dims) pair are
+// adjacent: each merges every fourth segment online (their loads are independent), then two
+// shuffle rounds merge the four.
 __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams p) {
   const int r = blockIdx.x / p.max_q_len, t = blockIdx.x % p.max_q_len;
   const int kvh = blockIdx.y;
@@ -595,29 +610,44 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
   const int npages = (L + kPage - 1) / kPage;
   const int nseg = (npages + p.seg_pages - 1) / p.seg_pages;
   const int G = p.group;
-  const int hh = threadIdx.x >> 4, d0 = (threadIdx.x & 15) * 8;
-  if (hh >= G) return;
+  const int sl = threadIdx.x & 3, dg = (threadIdx.x >> 2) & 15;
+  const int hh = blockIdx.z * 4 + (threadIdx.x >> 6);
+  const int d0 = dg * 8;
   const int rows = p.max_q_len * kRows;
   const int row = t * G + hh;
   auto unit_row = [&](int s) { return ((((size_t)r * p.max_segs + s) * p.hkv + kvh) * rows + row); };
   const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
   // segments wholly before every window of the request were not written (see the split kernel)
   const int s_begin = p.window > 0 ? (max(0, L - ql - p.window + 1) / kPage) / p.seg_pages : 0;
-  float M = neg_inf();
-  for (int s = s_begin; s < nseg; ++s) M = fmaxf(M, ml[unit_row(s)].x);
-  // the sink logit (log2 units) joins the max and, once, the denominator
-  const float sg = p.sink ? __ldg(p.sink + kvh * G + hh) * kLog2e : neg_inf();
-  M = fmaxf(M, sg);
+  float m = neg_inf(), l = 0.f;
   float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  float den = p.sink ? ex2(sg - M) : 0.f;
-  for (int s = s_begin; s < nseg; ++s) {
+#pragma unroll 2
+  for (int s = s_begin + sl; s < nseg; s += 4) {
     const float2 v = ml[unit_row(s)];
-    const float w = (v.x == neg_inf()) ? 0.f : ex2(v.x - M);  // empty partial weighs 0
-    den += w * v.y;
     const float4* a = reinterpret_cast<const float4*>(p.part_acc + unit_row(s) * kD + d0);
     const float4 x0 = a[0], x1 = a[1];
-    acc[0] += w * x0.x; acc[1] += w * x0.y; acc[2] += w * x0.z; acc[3] += w * x0.w;
-    acc[4] += w * x1.x; acc[5] += w * x1.y; acc[6] += w * x1.z; acc[7] += w * x1.w;
+    const float a2[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+    merge_partial(m, l, acc, v.x, v.y, a2);
+  }
+#pragma unroll
+  for (int off = 1; off <= 2; off <<= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+    const float l2 = __shfl_xor_sync(0xffffffffu, l, off);
+    float a2[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) a2[j] = __shfl_xor_sync(0xffffffffu, acc[j], off);
+    merge_partial(m, l, acc, m2, l2, a2);
+  }
+  if (sl != 0 || hh >= G) return;
+  // the sink logit (log2 units) joins the max and, once, the denominator
+  float den = l;
+  if (p.sink) {
+    const float sg = __ldg(p.sink + kvh * G + hh) * kLog2e;
+    const float M = fmaxf(m, sg);
+    const float w = (m == neg_inf()) ? 0.f : ex2(m - M);
+    den = w * l + ex2(sg - M);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] *= w;
   }
   const float inv = den > 0.f ? 1.f / den : 0.f;
   uint4 outv;
@@ -665,7 +695,7 @@ cudaError_t launch_decode(const DecodeParams& p, const DecodeMaps& maps, cudaStr
 }
 
 cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t s) {
-  dim3 g2(p.num_reqs * p.max_q_len, p.hkv);
+  dim3 g2(p.num_reqs * p.max_q_len, p.hkv, (p.group + 3) / 4);
   decode_combine_kernel<<<g2, 256, 0, s>>>(p);
   return cudaGetLastError();
 }
