@@ -256,6 +256,9 @@ __global__ void __launch_bounds__(kThreads, 3)
   const bool validB = posB < ql;
   const int lastkA = L - ql + posA;                  // last key visible to row A
   const int lastkB = ppt == 1 ? lastkA : validB ? L - ql + posB : -1;  // and to row B (none past q_len)
+  // a page whose slots all lie at or below both rows' last keys (and, with a window, above
+  // both windows' starts) needs no per-slot masks; with row B past q_len no page qualifies
+  const int lastk_min = min(lastkA, lastkB), lastk_max = max(lastkA, lastkB);
   const float sl2 = p.scale * kLog2e;
   float o[16][4];
 #pragma unroll
@@ -382,22 +385,32 @@ __global__ void __launch_bounds__(kThreads, 3)
       // this thread's columns: slots 2tq, 2tq+1 (n-tile 0) and 8+2tq, 9+2tq (n-tile 1)
       const int tok0 = (pb + i) * kPage + 2 * tq;
       const int tk[4] = {tok0, tok0 + 1, tok0 + 8, tok0 + 9};
+      const int pfirst = (pb + i) * kPage;
+      const bool inner = pfirst + kPage - 1 <= lastk_min &&
+                         !(FEAT && p.window > 0 && pfirst <= lastk_max - p.window);  // uniform per warp
       float x[2][4];  // [row g / g+8][column]
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        bool visA = tk[c] <= lastkA, visB = tk[c] <= lastkB;
-        if (FEAT && p.window > 0) {
-          visA = visA && tk[c] > lastkA - p.window;
-          visB = visB && tk[c] > lastkB - p.window;
-        }
         const float sa = (c < 2) ? s0[c] : s1[c - 2];
         const float sb = (c < 2) ? s0[c + 2] : s1[c];
         if (FEAT) {  // + G_i - G_j
-          x[0][c] = visA ? fmaf(sa, sl2 * ks[c], fmaf(-gk[0][c], kLog2e, gq0)) : neg_inf();
-          x[1][c] = visB ? fmaf(sb, sl2 * ks[c], fmaf(-gk[1][c], kLog2e, gq1)) : neg_inf();
+          x[0][c] = fmaf(sa, sl2 * ks[c], fmaf(-gk[0][c], kLog2e, gq0));
+          x[1][c] = fmaf(sb, sl2 * ks[c], fmaf(-gk[1][c], kLog2e, gq1));
         } else {
-          x[0][c] = visA ? sa * sl2 * ks[c] : neg_inf();
-          x[1][c] = visB ? sb * sl2 * ks[c] : neg_inf();
+          x[0][c] = sa * sl2 * ks[c];
+          x[1][c] = sb * sl2 * ks[c];
+        }
+      }
+      if (!inner) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          bool visA = tk[c] <= lastkA, visB = tk[c] <= lastkB;
+          if (FEAT && p.window > 0) {
+            visA = visA && tk[c] > lastkA - p.window;
+            visB = visB && tk[c] > lastkB - p.window;
+          }
+          if (!visA) x[0][c] = neg_inf();
+          if (!visB) x[1][c] = neg_inf();
         }
       }
       float mx0 = fmaxf(fmaxf(x[0][0], x[0][1]), fmaxf(x[0][2], x[0][3]));
@@ -437,7 +450,12 @@ __global__ void __launch_bounds__(kThreads, 3)
       // V scales multiply the probabilities after the row sum; slots >= L get scale 0, and
       // their value bytes are never multiplied (NaN allowed there)
 #pragma unroll
-      for (int c = 0; c < 4; ++c) vs[c] = (tk[c] < L) ? vs[c] * (KVF == 0 ? kPScale : 1.f) : 0.f;
+      for (int c = 0; c < 4; ++c) vs[c] *= KVF == 0 ? kPScale : 1.f;
+      if (!inner) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          if (tk[c] >= L) vs[c] = 0.f;
+      }
       if constexpr (KVF == 0) {
         uint32_t pa[4];
         pa[0] = pack_f16x2(pr[0][0] * vs[0], pr[0][1] * vs[1]);
@@ -451,7 +469,11 @@ __global__ void __launch_bounds__(kThreads, 3)
         for (int c = 0; c < 4; ++c) {
           const int row = 2 * tq + (c & 1) + 8 * (c >> 1);
           vr[c] = lds128(st + C::KB + row * kD + ((g ^ (row & 7)) << 4));
-          if (tk[c] >= L) vr[c] = make_uint4(0, 0, 0, 0);
+        }
+        if (!inner) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            if (tk[c] >= L) vr[c] = make_uint4(0, 0, 0, 0);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[stage]);
@@ -488,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 3)
         for (int rr = 0; rr < 4; ++rr) {
           const int row = 2 * tq + (rr & 1) + 8 * (rr >> 1);
           uint4 a = lds128(st + C::KB + row * 256 + 32 * g), b = lds128(st + C::KB + row * 256 + 32 * g + 16);
-          if (tk[rr] >= L) a = b = make_uint4(0, 0, 0, 0);
+          if (!inner && tk[rr] >= L) a = b = make_uint4(0, 0, 0, 0);
           rw[rr][0] = a.x; rw[rr][1] = a.y; rw[rr][2] = a.z; rw[rr][3] = a.w;
           rw[rr][4] = b.x; rw[rr][5] = b.y; rw[rr][6] = b.z; rw[rr][7] = b.w;
         }
