@@ -78,16 +78,16 @@ bool make_map(CUtensorMap* m, const void* base, int dim, int heads, int tokens, 
 }
 
 // 3-D fp32 map {dim, heads, tokens} of a contiguous [tokens, heads, dim] accumulator with a
-// dim x 1 x box_rows box, no swizzle: the target of tiled reduce-adds.
+// 32 x 1 x box_rows box and the 128-byte swizzle: the target of tiled reduce-adds.
 bool make_map_f32(CUtensorMap* m, void* base, int dim, int heads, int tokens, uint32_t box_rows) {
   auto enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[3] = {(cuuint64_t)dim, (cuuint64_t)heads, (cuuint64_t)tokens};
   cuuint64_t strides[2] = {(cuuint64_t)dim * 4, (cuuint64_t)dim * heads * 4};
-  cuuint32_t box[3] = {(cuuint32_t)dim, 1, box_rows};
+  cuuint32_t box[3] = {32, 1, box_rows};  // 32 fp32 = one 128-byte swizzle row
   cuuint32_t es[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -454,7 +454,7 @@ int attn_bwd(const gcs_prefill_args* a, const void* o, const float* lse, const v
       !make_map(&maps.dout128, dout, a->dv, a->hq, T, lay.dout, 128))
     return GCS_ERR_CUDA;
   std::memset(&maps.dq_acc, 0, sizeof(maps.dq_acc));
-  if (fu && !make_map_f32(&maps.dq_acc, dq_acc, a->dqk, a->hq, T, 64)) return GCS_ERR_CUDA;
+  if (fu && !make_map_f32(&maps.dq_acc, dq_acc, a->dqk, a->hq, T, 128)) return GCS_ERR_CUDA;
 
   const int32_t* cu = a->cu_seqlens;
   if (cu_chk) {

@@ -49,7 +49,7 @@ struct BwdParams {
   uint16_t* grad_k;      // bf16 [total, hkv, dqk]
   uint16_t* grad_v;      // bf16 [total, hkv, dv]
   long long dq_ts, dq_hs, dk_ts, dk_hs, dv_ts, dv_hs;  // element strides (token, head) of the three
-  float* dq_acc;         // fp32 [total, hq, dqk] (zeroed; wide heads, reduce-add route only)
+  float* dq_acc;         // fp32 [total, hq, dqk] (zeroed; single pass and wide reduce-add route)
   float* dg_row;         // fp32 [hq, total] sum_j dS_ij; null if not needed
   float* dg_col;         // fp32 [hq, total] sum_i dS_ij (zeroed); null if no gate
   const float* vecp;     // packed per-(head, 64-row query tile) vectors (see launch_bwd_pack)
@@ -60,7 +60,7 @@ struct BwdParams {
 struct BwdMaps {
   CUtensorMap q, k, v, dout;   // 3-D bf16 maps {dim, heads, tokens}, 128-B swizzle (q, dout: 64-row boxes)
   CUtensorMap q128, dout128;   // q, dout with 128-row boxes (dQ pass)
-  CUtensorMap dq_acc;          // fp32 dQ accumulator {dqk, heads, tokens}, box 128 x 1 x 64, no swizzle
+  CUtensorMap dq_acc;          // fp32 dQ accumulator {dqk, heads, tokens}, box 32 x 1 x 128, 128-B swizzle
                                // (single-pass route only)
 };
 

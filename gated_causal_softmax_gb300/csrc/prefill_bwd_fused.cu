@@ -9,23 +9,23 @@
 //     dP^T = V dO^T      (TMEM, fp32)     dS^T = P^T o (dP^T - delta_i)
 //     dV  += P^T dO      (A = P^T, bf16 over the consumed S^T in TMEM)
 //     dK  += dS^T Q      (A = dS^T, bf16 over the consumed dP^T in TMEM)
-//     dQ^T = K^T dS^T    (A = the resident K tile read MN-major, B = dS^T in shared memory)
+//     dQ   = dS K        (A = dS^T in shared memory read MN-major, B = the resident K tile MN-major)
 // and dQ is reduce-added in fp32 into a zeroed buffer, plus the fp32 row and column sums of dS
 // (gate and sink gradients).
 //
-// TMEM (512 columns): S^T | dP^T, then dQ^T of the same step | dV | dK.  The issue order
-//     dV(s), S^T(s+1), dK(s), dQ^T(s), [dQ^T(s) read out], dP^T(s+1), dV(s+1), ...
+// TMEM (512 columns): S^T | dP^T, then dQ of the same step | dV | dK.  The issue order
+//     dV(s), S^T(s+1), dK(s), dQ(s), [dQ(s) read out], dP^T(s+1), dV(s+1), ...
 // keeps every overwrite behind the MMA that reads the old contents: tcgen05.mma operations
 // issued by one thread execute in issue order, so S^T(s+1) may replace the P^T that dV(s)
-// reads and dQ^T(s) the dS^T that dK(s) reads; dP^T(s+1) waits until the softmax warps have
-// loaded dQ^T(s).  dS^T reaches shared memory in the dO tile of its own step, which dV(s) and
+// reads and dQ(s) the dS^T that dK(s) reads; dP^T(s+1) waits until the softmax warps have
+// loaded dQ(s).  dS^T reaches shared memory in the dO tile of its own step, which dV(s) and
 // dP^T(s) have finished reading by then (dv_done), so the kernel needs no extra tile.
 //
-// dQ leaves through shared memory: once dQ^T(s) is in TMEM the two softmax warpgroups each load
-// their 64 query columns (TMEM lane = head dim) and write them as 64 rows x 128 dims of fp32
-// (32 KB) into a tile no MMA reads any more -- warpgroup 0 into the dO(s) tile, warpgroup 1
-// into the Q(s) tile -- and a tiled bulk reduce-add (fp32 add in L2) sends each block to the
-// dQ accumulator.  The bulk operations are issued and awaited by warps 2 and 3, which then
+// dQ leaves through shared memory: once dQ(s) is in TMEM (lane = query row) the two softmax
+// warpgroups each load their 64 head dims and write them as two 128-row x 32-dim fp32 boxes
+// with the 128-byte swizzle (16-byte stores, 32 KB) into a tile no MMA reads any more --
+// warpgroup 0 into the dO(s) tile, warpgroup 1 into the Q(s) tile -- and tiled bulk
+// reduce-adds (fp32 add in L2) send the boxes to the dQ accumulator.  The bulk operations are issued and awaited by warps 2 and 3, which then
 // hand the tile back to the producer, so the softmax warps never wait for them.  Query rows of
 // a block that lie past the sequence hold exact zeros (their probabilities are 0), so adding
 // them to the next sequence's rows changes nothing; rows past the tensor are clipped.
@@ -62,7 +62,7 @@ constexpr int NBAR = 24;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int SMEM = OFF_MISC + 16;
 static_assert(SMEM <= kSmemOptinMax, "shared memory budget");
-constexpr int T_S = 0, T_DP = 128, T_DV = 256, T_DK = 384;  // T_DP also holds dQ^T
+constexpr int T_S = 0, T_DP = 128, T_DV = 256, T_DK = 384;  // T_DP also holds dQ
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
@@ -145,8 +145,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* ds_ready = bars + 14;   // dS^T stored in TMEM (8 warps)
   uint64_t* ds_smem = bars + 15;    // dS^T stored in shared memory (8 warps)
   uint64_t* dv_done = bars + 16;    // dV of the step retired: its dO tile may take dS^T
-  uint64_t* dq_full = bars + 17;    // dQ^T written
-  uint64_t* dq_read = bars + 18;    // dQ^T loaded by the 8 softmax warps
+  uint64_t* dq_full = bars + 17;    // dQ written
+  uint64_t* dq_read = bars + 18;    // dQ loaded by the 8 softmax warps
   uint64_t* all_done = bars + 19;   // every MMA of the CTA retired (epilogue)
   uint64_t* drain = bars + 20;
   uint64_t* stage_full = bars + 21;  // [2] a warpgroup's dQ block written to shared memory (4 warps)
@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------------------------------------------------- MMA issuer
       const uint32_t idS = idesc_bf16(128, kBM, false, false);  // S^T, dP^T: N = 128 query rows
       const uint32_t idAcc = idesc_bf16(128, kD, false, true);  // dV, dK: B = dO / Q, MN-major
-      const uint32_t idDQ = idesc_bf16(128, kBM, true, true);   // dQ^T: A = K^T, B = dS^T, both MN-major
+      const uint32_t idDQ = idesc_bf16(kBM, kD, true, true);    // dQ: A = dS (the dS^T tile), B = K, both MN-major
       const uint64_t dK0 = sdesc_sw128(smem_u32(smem + OFF_K), 16, 1024);
       const uint64_t dV0 = sdesc_sw128(smem_u32(smem + OFF_V), 16, 1024);
       const uint64_t dQ0 = sdesc_sw128(smem_u32(smem + OFF_Q), 16, 1024);
@@ -282,16 +282,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < 8; ++k)
           mma_ts(tmem + T_DK, tmem + T_DP + (k >> 2) * 64 + 8 * (k & 3), dQmn0 + qb * kTile16 + 128 * k, idAcc,
                  (s > 0 || k > 0) ? 1u : 0u);
-        // dS^T(s) in shared memory (the dO(s) tile): dQ^T = K^T dS^T over the dP^T columns
+        // dS^T(s) in shared memory (the dO(s) tile): dQ = dS K over the dP^T columns (TMEM lane =
+        // query row, column = head dim)
         ok = wait_bar(ds_smem, s & 1, ab);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          mma_ss(tmem + T_DP, dKmn0 + 128 * k, dDOmn0 + db * kTile16 + 128 * k, idDQ, k > 0 ? 1u : 0u);
+          mma_ss(tmem + T_DP, dDOmn0 + db * kTile16 + 128 * k, dKmn0 + 128 * k, idDQ, k > 0 ? 1u : 0u);
         mma_commit(dq_full);
         if (more) {
-          // dQ^T(s) loaded by the softmax warps, dO(s+1) landed
+          // dQ(s) loaded by the softmax warps, dO(s+1) landed
           ok = wait_bars(ab, dq_read, s & 1, &do_full[(s + 1) % kNDO], ((s + 1) / kNDO) & 1);
           if (!ok) break;
           tc_fence_after();
@@ -311,10 +312,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < nsteps; ++s) {
         const int qb = s % kNQ, db = s % kNDO;
         const int h = kvh * group + s / n_it;
-        const int cb = (it_lo + s % n_it) * kBM + 64 * wg;
+        const int i0 = (it_lo + s % n_it) * kBM;
         if (!wait_bar(&stage_full[wg], s & 1, ab)) break;
         const uint8_t* src = smem + (wg == 0 ? OFF_DO + db * kTile : OFF_Q + qb * kTile);
-        if (cb < len) tma_reduce_add_3d(&tmDQ, src, 0, h, seq_start + cb);
+        // this warpgroup's head dims 64 wg .. 64 wg + 63 as two 32-dim x 128-row boxes
+        for (int b = 0; b < 2; ++b) tma_reduce_add_3d(&tmDQ, src + b * kChunk, 64 * wg + 32 * b, h, seq_start + i0);
         bulk_commit_group();
         bulk_wait_group_read0();
         mbar_arrive(wg == 0 ? &do_empty[db] : &q_empty[qb]);
@@ -327,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ key rows, 64 query columns
     const int wg = (warp - 4) >> 2;     // query columns 64 wg .. 64 wg + 63 of every step
     const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;  // key row within the tile = TMEM lane (dQ^T: head dim)
+    const int r = quarter * 32 + lane;  // key row within the tile = TMEM lane (dQ: query row)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_off + T_S + 64 * wg;
     const uint32_t tDP = tmem + lane_off + T_DP + 64 * wg;
@@ -442,8 +444,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (i < len) red_add_f32(p.dg_row + (size_t)h * p.total + seq_start + i, sum);
         }
       }
-      // ---- dQ^T(s): lane r = head dim r, this warpgroup's 64 query columns, staged as
-      // [64 query rows][128 dims] fp32 for the bulk reduce-add (warp 2 + wg sends it)
+      // ---- dQ(s): lane r = query row i0 + r, this warpgroup's 64 head dims, staged as two
+      // [128 query rows][32 dims] fp32 boxes with the 128-byte swizzle for the bulk
+      // reduce-adds (warp 2 + wg sends them)
       ok = wait_bar(dq_full, s & 1, ab);
       if (!ok) break;
       tc_fence_after();
@@ -455,9 +458,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(dq_read);
       {
-        float* stage = reinterpret_cast<float*>(smem + (wg == 0 ? OFF_DO + db * kTile : OFF_Q + (s % kNQ) * kTile));
+        uint8_t* stage = smem + (wg == 0 ? OFF_DO + db * kTile : OFF_Q + (s % kNQ) * kTile);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) stage[c * kD + r] = __uint_as_float(dq[c]) * p.scale;
+        for (int u = 0; u < 16; ++u) {
+          const float4 v = make_float4(__uint_as_float(dq[4 * u]) * p.scale, __uint_as_float(dq[4 * u + 1]) * p.scale,
+                                       __uint_as_float(dq[4 * u + 2]) * p.scale,
+                                       __uint_as_float(dq[4 * u + 3]) * p.scale);
+          *reinterpret_cast<float4*>(stage + (u >> 3) * kChunk + sw128_offset(r, u & 7)) = v;
+        }
       }
       fence_proxy_async_smem();
       __syncwarp();
