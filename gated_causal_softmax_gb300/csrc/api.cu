@@ -389,8 +389,7 @@ int attn_fwd(const gcs_prefill_args* a, void* o, float* lse, void* workspace, si
   KernelTimer timer(s);
   timer.before();
   if (a->dqk == a->dv && a->dqk <= 128) {
-    const int num_pairs = (a->total_tokens + 255) / 256 + a->num_seqs;
-    st = cuda_status(launch_prefill_fwd2(p, maps, num_pairs, s));
+    st = cuda_status(launch_prefill_fwd2(p, maps, s));
   } else {
     const int num_tiles = (a->total_tokens + 127) / 128 + a->num_seqs;
     st = cuda_status(launch_prefill_fwd(p, maps, num_tiles, s));

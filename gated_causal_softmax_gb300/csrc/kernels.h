@@ -31,8 +31,9 @@ struct FwdMaps {
 };
 
 cudaError_t launch_prefill_fwd(const FwdParams& p, const FwdMaps& maps, int num_tiles, cudaStream_t s);
-// Head dims 64 / 128: two 128-row query tiles per CTA (num_pairs = 256-row query tiles).
-cudaError_t launch_prefill_fwd2(const FwdParams& p, const FwdMaps& maps, int num_pairs, cudaStream_t s);
+// Head dims 64 / 128: two 128-row query tiles per CTA (two query heads of a GQA group over the
+// same rows when the group size is even, else 256 rows of one head).
+cudaError_t launch_prefill_fwd2(const FwdParams& p, const FwdMaps& maps, cudaStream_t s);
 
 struct BwdParams {
   const int32_t* cu_seqlens;

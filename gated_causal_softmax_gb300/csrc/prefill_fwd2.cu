@@ -2,8 +2,10 @@
 // flash-linear-attention #1322 "Gluon attention backend with large head dimensions",
 // Description: causal attention with log gates, sliding windows and a sink bias).
 //
-// Same arithmetic as prefill_fwd.cu; the difference is the schedule.  One CTA takes 256
-// query rows of one head as tiles A (rows q0..q0+127) and B (q0+128..q0+255).  Each tile has
+// Same arithmetic as prefill_fwd.cu; the difference is the schedule.  One CTA takes two
+// 128-row query tiles A and B: with a GQA group of even size, the same rows of two query heads
+// of the group (same causal range, so both tiles take part in every key tile); otherwise 256
+// query rows of one head (rows q0..q0+127 and q0+128..q0+255).  Each tile has
 // its own TMEM score buffer and accumulator (S_A, S_B, O_A, O_B: 4 x 128 columns) and its
 // own softmax warpgroup, and the MMA issuer interleaves them
 //     PV_A(n), S_A(n+1), PV_B(n), S_B(n+1), ...
@@ -52,12 +54,16 @@ struct Fwd2Cfg {
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
 
-// Register split (per thread): warpgroup 0 (producer, MMA, 2 idle warps) 88, the two softmax
-// warpgroups 208 each: 128 x 88 + 256 x 208 = 64512 = 384 threads x 168 at launch.
-__device__ __forceinline__ void reg_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 88;\n" ::: "memory"); }
-__device__ __forceinline__ void reg_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 208;\n" ::: "memory"); }
+// Register split (per thread): warpgroup 0 (producer, MMA, 2 idle warps) 120, the two softmax
+// warpgroups 184 each: 128 x 120 + 256 x 184 = 62464 <= 384 threads x 168 at launch (both
+// tile pairings compile without spills at this split).
+__device__ __forceinline__ void reg_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 120;\n" ::: "memory"); }
+__device__ __forceinline__ void reg_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 184;\n" ::: "memory"); }
 
-template <int D>
+// HP (head pairs, GQA groups of even size): tiles A and B are the same 128 query rows of two
+// query heads of one group, so they share every key tile over the same causal range.
+// Otherwise they are 256 consecutive query rows of one head.
+template <int D, bool HP>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -65,15 +71,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-  // heaviest 256-row query pairs first
+  // heaviest query tiles (or 256-row pairs) first
   TileRef tr;
-  if (!lpt_tile(p.cu_seqlens, p.num_seqs, 2 * kBM, blockIdx.y, tr)) return;
+  if (!lpt_tile(p.cu_seqlens, p.num_seqs, HP ? kBM : 2 * kBM, blockIdx.y, tr)) return;
   const int seq_start = tr.start, len = tr.len;
-  const int h = blockIdx.x;
-  const int kvh = h / (p.hq / p.hkv);
-  const int q0 = tr.u * 2 * kBM;
-  const int qt[2] = {q0 / kBM, q0 / kBM + 1};
-  const bool valid_b = q0 + kBM < len;
+  // tile x: query head h0 + (HP ? x : 0), first query row q0 + (HP ? 0 : 128 x)
+  const int h0 = HP ? 2 * (int)blockIdx.x : (int)blockIdx.x;
+  const int kvh = h0 / (p.hq / p.hkv);
+  const int q0 = HP ? tr.u * kBM : tr.u * 2 * kBM;
+  const int qt[2] = {q0 / kBM, HP ? q0 / kBM : q0 / kBM + 1};
+  const bool valid_b = HP || q0 + kBM < len;
   int lo[2];
   for (int x = 0; x < 2; ++x) {
     const int lo_j = qt[x] * kBM - p.window + 1;
@@ -137,8 +144,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_expect_tx(q_full, 2 * C::CH * kChunk);
       for (int x = 0; x < 2; ++x)
         for (int c = 0; c < C::CH; ++c)
-          tma_load_3d_hint(smem + C::OFF_Q + (x * C::CH + c) * kChunk, &tmQ, q_full, c * 64, h,
-                           seq_start + q0 + x * kBM, pol_q);
+          tma_load_3d_hint(smem + C::OFF_Q + (x * C::CH + c) * kChunk, &tmQ, q_full, c * 64, HP ? h0 + x : h0,
+                           seq_start + q0 + (HP ? 0 : x * kBM), pol_q);
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       for (int n = 0; n < nt && ok; ++n) {
@@ -250,7 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_off + 128 * x, tO = tmem + lane_off + 256 + 128 * x;
-    const int xq0 = q0 + x * kBM;
+    const int h = HP ? h0 + x : h0;
+    const int xq0 = q0 + (HP ? 0 : x * kBM);
     const int il = xq0 + r;
     const bool row_valid = il < len;
     const int tok = seq_start + (row_valid ? il : len - 1);
@@ -417,21 +425,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
-cudaError_t launch_t(const FwdParams& p, const FwdMaps& maps, int num_pairs, cudaStream_t s) {
+template <int D, bool HP>
+cudaError_t launch_t(const FwdParams& p, const FwdMaps& maps, int num_units, cudaStream_t s) {
   using C = Fwd2Cfg<D>;
-  auto kern = prefill_fwd2_kernel<D>;
+  auto kern = prefill_fwd2_kernel<D, HP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  kern<<<dim3(p.hq, num_pairs), kThreads, C::SMEM, s>>>(maps.q, maps.k, maps.v, p);
+  kern<<<dim3(HP ? p.hq / 2 : p.hq, num_units), kThreads, C::SMEM, s>>>(maps.q, maps.k, maps.v, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_prefill_fwd2(const FwdParams& p, const FwdMaps& maps, int num_pairs, cudaStream_t s) {
-  if (p.dqk == 64 && p.dv == 64) return launch_t<64>(p, maps, num_pairs, s);
-  if (p.dqk == 128 && p.dv == 128) return launch_t<128>(p, maps, num_pairs, s);
+cudaError_t launch_prefill_fwd2(const FwdParams& p, const FwdMaps& maps, cudaStream_t s) {
+  // GQA groups of even size pair two query heads per CTA over 128-row tiles; otherwise two
+  // consecutive 128-row tiles of one head (an upper bound on the tiles of the packed batch:
+  // the CTAs past the last tile return at once)
+  const bool hp = (p.hq / p.hkv) % 2 == 0;
+  const int units = hp ? (p.total + kBM - 1) / kBM + p.num_seqs : (p.total + 2 * kBM - 1) / (2 * kBM) + p.num_seqs;
+  if (p.dqk == 64 && p.dv == 64) return hp ? launch_t<64, true>(p, maps, units, s) : launch_t<64, false>(p, maps, units, s);
+  if (p.dqk == 128 && p.dv == 128)
+    return hp ? launch_t<128, true>(p, maps, units, s) : launch_t<128, false>(p, maps, units, s);
   return cudaErrorInvalidValue;
 }
 
