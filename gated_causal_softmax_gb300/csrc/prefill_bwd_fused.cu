@@ -66,10 +66,11 @@ constexpr int T_S = 0, T_DP = 128, T_DV = 256, T_DK = 384;  // T_DP also holds d
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
-// Register split: warpgroup 0 (producer, MMA issuer with its extra descriptors, 2 idle warps)
-// 112, the softmax warpgroups 192: 128 x 112 + 256 x 192 = 63488 <= 384 threads x 168 at launch.
-__device__ __forceinline__ void reg_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 112;\n" ::: "memory"); }
-__device__ __forceinline__ void reg_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 192;\n" ::: "memory"); }
+// Register split: warpgroup 0 (producer, MMA issuer with its extra descriptors, the two
+// reduce-add warps) 104, the softmax warpgroups 200: 128 x 104 + 256 x 200 = 64512 = 384 threads
+// x 168 at launch.
+__device__ __forceinline__ void reg_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 104;\n" ::: "memory"); }
+__device__ __forceinline__ void reg_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 200;\n" ::: "memory"); }
 
 __device__ __forceinline__ void red_add_f32(float* addr, float v) {
   asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
