@@ -197,10 +197,20 @@ __global__ void __launch_bounds__(kThreads, 3)
       prefetch_tmap(&tmV);
     }
     const uint32_t tx = 2 * C::KB + (C::SCALES ? 2 * kPage * 4 : 0) + (has_gate ? G * kPage * 4 : 0);
+    // each lane's block-table entry for its page of the next round is read one round ahead, so
+    // the read's latency overlaps this round's waits and copies
+    const bool lane_kind = kind < kKinds && (!is_g || has_gate);
+    auto table_entry = [&](int i) -> int {
+      const int pg = pb + i;
+      return (lane_kind && i < np) ? (PG1 ? __ldg(trow + pg) : __ldg(trow + (pg >> lbp))) : 0;
+    };
+    int blk_next = table_entry(pl);
     for (int base = 0; base < np; base += kBatch) {
       const int i = base + pl;
-      const bool act = i < np && kind < kKinds && (!is_g || has_gate);
+      const bool act = i < np && lane_kind;
       const int stage = i % kNST;
+      const int blk = blk_next;  // block of this lane's page
+      blk_next = table_entry(i + kBatch);
       bool okl = true;
       if (act) okl = wait_bar(&empty[stage], ((i / kNST) & 1) ^ 1, ab);
       if (!__all_sync(0xffffffffu, okl)) break;
@@ -208,7 +218,6 @@ __global__ void __launch_bounds__(kThreads, 3)
       __syncwarp();
       if (act) {
         const int pg = pb + i;
-        const int blk = PG1 ? __ldg(trow + pg) : __ldg(trow + (pg >> lbp));  // block
         const int sub = PG1 ? 0 : (pg & ((1 << lbp) - 1)) * kPage;           // first slot of the page
         const size_t slot0 = ((size_t)blk * p.hkv + kvh) * p.block_size + sub;
         if (KVF == 0 && kind < 2) {
