@@ -48,7 +48,7 @@ LAUNCHES_PER_DECODE = 2
 NCU_TRAFFIC = {
     "bwd": 551.3e6 + 250.6e6,  # prefill_bwd_fused_kernel
     "fwd": 102.6e6 + 16.2e6,   # prefill_fwd2_kernel<128, 1>
-    "decode_split": 1155.6e6 + 20.0e6,  # decode_split_kernel<0, 0, 0, 16, 0, 1>
+    "decode_split": 1155.6e6 + 19.5e6,  # decode_split_kernel<0, 0, 0, 16, 0, 1>
     "prefill_paged": 154.0e6 + 35.3e6,  # prefill_paged_kernel<0>
 }
 
