@@ -151,7 +151,6 @@ bool overlap(const TSpan& x, const TSpan& y) {
   }
   return true;
 }
-bool overlap(const Span& x, const Span& y) { return overlap(tspan(x), tspan(y)); }
 
 // True when an output range overlaps an input range or another output range (kernels read
 // their inputs and write their outputs concurrently, so any overlap is a race).

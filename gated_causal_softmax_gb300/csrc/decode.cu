@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, 3)
   constexpr int kKinds = C::KINDS;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   // the swizzled tensor copies want 1 KB-aligned pages
-  uint8_t* kv = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* kv = smem_align_1k(smem_raw);
   uint8_t* aux = kv + C::OFF_AUX;
   __shared__ uint64_t full[kNST], empty[kNST];
   __shared__ int abort_flag_s;

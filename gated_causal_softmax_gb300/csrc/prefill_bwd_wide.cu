@@ -69,7 +69,7 @@ __device__ __forceinline__ void wide_role(const CUtensorMap& tmQ, const CUtensor
                                           const CUtensorMap& tmDO, const BwdParams& p, int role) {
   using C = WideCfg<DQK, DV, KIND, BM>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_align_1k(smem_raw);
 
   TileRef tr;
   if (!lpt_tile(p.cu_seqlens, p.num_seqs, kBN, blockIdx.y, tr)) return;

@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                const BwdParams p) {
   using C = WdqCfg<DQK, DV>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_align_1k(smem_raw);
 
   TileRef tr;
   if (!lpt_tile(p.cu_seqlens, p.num_seqs, kBM, blockIdx.y, tr)) return;

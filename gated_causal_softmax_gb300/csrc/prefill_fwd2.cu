@@ -69,7 +69,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using C = Fwd2Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_align_1k(smem_raw);
 
   // heaviest query tiles (or 256-row pairs) first
   TileRef tr;

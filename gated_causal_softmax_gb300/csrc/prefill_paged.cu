@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const DecodeParams p) {
   using C = PpCfg<FEAT>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_align_1k(smem_raw);
 
   const int nseg = p.max_segs;
   const int seg = blockIdx.x % nseg, qp = blockIdx.x / nseg;

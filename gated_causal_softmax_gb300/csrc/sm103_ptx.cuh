@@ -27,6 +27,14 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// The dynamic shared-memory base rounded up to a 1 KB boundary (the 128-byte swizzle atoms
+// want it).  The offset is added to the shared array itself: a round trip through an integer
+// would hide the address space from the compiler, and every access through the result would
+// then be a generic load or store instead of a shared one.
+__device__ __forceinline__ uint8_t* smem_align_1k(uint8_t* base) {
+  return base + ((1024u - (smem_u32(base) & 1023u)) & 1023u);
+}
+
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
