@@ -54,11 +54,11 @@ struct Fwd2Cfg {
   static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
 
-// Register split (per thread): warpgroup 0 (producer, MMA, 2 idle warps) 120, the two softmax
-// warpgroups 184 each: 128 x 120 + 256 x 184 = 62464 <= 384 threads x 168 at launch (both
-// tile pairings compile without spills at this split).
-__device__ __forceinline__ void reg_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 120;\n" ::: "memory"); }
-__device__ __forceinline__ void reg_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 184;\n" ::: "memory"); }
+// Register split (per thread): warpgroup 0 (producer, MMA, 2 idle warps) 112, the two softmax
+// warpgroups 192 each: 128 x 112 + 256 x 192 = 63488 <= 384 threads x 168 at launch (both
+// tile pairings compile without spills at this split; at 120 / 184 the softmax spills).
+__device__ __forceinline__ void reg_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 112;\n" ::: "memory"); }
+__device__ __forceinline__ void reg_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 192;\n" ::: "memory"); }
 
 // HP (head pairs, GQA groups of even size): tiles A and B are the same 128 query rows of two
 // query heads of one group, so they share every key tile over the same causal range.

@@ -70,7 +70,8 @@ struct PpCfg {
 };
 
 // Register split: warpgroup 0 (producer, MMA, converters) 88, the softmax warpgroups 208:
-// 128 x 88 + 256 x 208 = 64512 = 384 threads x 168 at launch.
+// 128 x 88 + 256 x 208 = 64512 = 384 threads x 168 at launch.  The converters spill a few
+// words at 88; 96 / 200 removes that but measured slower (the softmax wants the registers).
 __device__ __forceinline__ void reg_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 88;\n" ::: "memory"); }
 __device__ __forceinline__ void reg_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 208;\n" ::: "memory"); }
 
