@@ -46,10 +46,10 @@ LAUNCHES_PER_DECODE = 2
 # workloads, from one ncu capture of the kernel as it stands; set back to None whenever the
 # kernel changes.
 NCU_TRAFFIC = {
-    "bwd": 551.3e6 + 250.6e6,  # prefill_bwd_fused_kernel
+    "bwd": 583.2e6 + 256.7e6,  # prefill_bwd_fused_kernel
     "fwd": 102.6e6 + 16.2e6,   # prefill_fwd2_kernel<128, 1>
-    "decode_split": 1155.6e6 + 19.5e6,  # decode_split_kernel<0, 0, 0, 16, 0, 1>
-    "prefill_paged": 154.0e6 + 35.3e6,  # prefill_paged_kernel<0>
+    "decode_split": 1155.4e6 + 18.8e6,  # decode_split_kernel<0, 0, 0, 16, 0, 1>
+    "prefill_paged": 154.7e6 + 34.7e6,  # prefill_paged_kernel<0>
 }
 
 
