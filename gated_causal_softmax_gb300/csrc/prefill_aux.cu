@@ -145,15 +145,19 @@ __global__ void __launch_bounds__(kScanThreads) bwd_pre_kernel(const PreArgs a) 
 }
 
 // fp32 dQ accumulator [total, hq, dqk] (contiguous) -> bf16 dQ at token * ts + head * hs,
-// grid-stride over the role's blocks.
+// grid-stride over the role's blocks.  Every prefill tensor holds fewer than 2^31 elements (a
+// host check), so the element index fits 32 bits; head dims are powers of two, so the head-dim
+// offset is a mask and one 32-bit division per float4 splits the row into (token, head).
 __device__ __forceinline__ void dq_convert_range(const PostArgs& a, int blk, int nblk) {
   const float4* src = reinterpret_cast<const float4*>(a.dq_acc);
-  const int q4 = a.dqk / 4;
-  for (size_t i = blk * (size_t)blockDim.x + threadIdx.x; i < a.n4; i += (size_t)nblk * blockDim.x) {
+  const int lq4 = __ffs(a.dqk >> 2) - 1;  // log2(dqk / 4)
+  const int n4 = static_cast<int>(a.n4);
+  for (int i = blk * blockDim.x + threadIdx.x; i < n4; i += nblk * blockDim.x) {
     const float4 v = src[i];
-    const size_t rh = i / q4;
-    const long long d = (long long)(i % q4) * 4, h = (long long)(rh % a.hq), t = (long long)(rh / a.hq);
-    *reinterpret_cast<uint2*>(a.dq + t * a.dq_ts + h * a.dq_hs + d) =
+    const int rh = i >> lq4;
+    const int t = rh / a.hq, h = rh - t * a.hq;
+    const int d = (i & ((1 << lq4) - 1)) * 4;
+    *reinterpret_cast<uint2*>(a.dq + (long long)t * a.dq_ts + (long long)h * a.dq_hs + d) =
         make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
   }
 }
