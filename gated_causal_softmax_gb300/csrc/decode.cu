@@ -627,11 +627,15 @@ __device__ __forceinline__ void merge_partial(float& m, float& l, float (&a)[8],
   m = M;
 }
 
-// One CTA per (request x query position, kv head, 4 query heads); 256 threads = 4 heads x
-// 16 groups of 8 value dims x 4 segment lanes.  The four lanes of a (head, dims) pair are
-// adjacent: each merges every fourth segment online (their loads are independent), then two
-// shuffle rounds merge the four.
+// One CTA per (request x query position, kv head, 16 / SL query heads); 256 threads = 16 / SL
+// heads x 16 groups of 8 value dims x SL segment lanes.  The SL lanes of a (head, dims) pair are
+// adjacent: each merges every SL-th segment online (their loads are independent), then log2 SL
+// shuffle rounds merge them.  SL = 4 for short contexts, 8 from 32 segments on (fewer serial
+// merges per lane: 3 x 4 queries at 227K, 114 segments, 20.1 -> 17.5 us per combine; 16 lanes
+// measured no better than 4 there, and 16 lanes on 16 segments cost the 64 x 1 call 8 us).
+template <int SL>
 __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams p) {
+  constexpr int kHeads = 16 / SL;  // query heads per CTA
   const int r = blockIdx.x / p.max_q_len, t = blockIdx.x % p.max_q_len;
   const int kvh = blockIdx.y;
   const int q_begin = __ldg(p.cu_q + r);
@@ -641,8 +645,8 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
   const int npages = (L + kPage - 1) / kPage;
   const int nseg = (npages + p.seg_pages - 1) / p.seg_pages;
   const int G = p.group;
-  const int sl = threadIdx.x & 3, dg = (threadIdx.x >> 2) & 15;
-  const int hh = blockIdx.z * 4 + (threadIdx.x >> 6);
+  const int sl = threadIdx.x & (SL - 1), dg = (threadIdx.x / SL) & 15;
+  const int hh = blockIdx.z * kHeads + threadIdx.x / (16 * SL);
   const int d0 = dg * 8;
   const int rows = p.max_q_len * kRows;
   const int row = t * G + hh;
@@ -652,16 +656,18 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeParams 
   const int s_begin = p.window > 0 ? (max(0, L - ql - p.window + 1) / kPage) / p.seg_pages : 0;
   float m = neg_inf(), l = 0.f;
   float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  if (hh < G) {
 #pragma unroll 2
-  for (int s = s_begin + sl; s < nseg; s += 4) {
-    const float2 v = ml[unit_row(s)];
-    const float4* a = reinterpret_cast<const float4*>(p.part_acc + unit_row(s) * kD + d0);
-    const float4 x0 = a[0], x1 = a[1];
-    const float a2[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-    merge_partial(m, l, acc, v.x, v.y, a2);
+    for (int s = s_begin + sl; s < nseg; s += SL) {
+      const float2 v = ml[unit_row(s)];
+      const float4* a = reinterpret_cast<const float4*>(p.part_acc + unit_row(s) * kD + d0);
+      const float4 x0 = a[0], x1 = a[1];
+      const float a2[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+      merge_partial(m, l, acc, v.x, v.y, a2);
+    }
   }
 #pragma unroll
-  for (int off = 1; off <= 2; off <<= 1) {
+  for (int off = 1; off < SL; off <<= 1) {
     const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
     const float l2 = __shfl_xor_sync(0xffffffffu, l, off);
     float a2[8];
@@ -726,8 +732,13 @@ cudaError_t launch_decode(const DecodeParams& p, const DecodeMaps& maps, cudaStr
 }
 
 cudaError_t launch_decode_combine(const DecodeParams& p, cudaStream_t s) {
-  dim3 g2(p.num_reqs * p.max_q_len, p.hkv, (p.group + 3) / 4);
-  decode_combine_kernel<<<g2, 256, 0, s>>>(p);
+  if (p.max_segs >= 32) {
+    dim3 g2(p.num_reqs * p.max_q_len, p.hkv, p.group / 2);
+    decode_combine_kernel<8><<<g2, 256, 0, s>>>(p);
+  } else {
+    dim3 g2(p.num_reqs * p.max_q_len, p.hkv, (p.group + 3) / 4);
+    decode_combine_kernel<4><<<g2, 256, 0, s>>>(p);
+  }
   return cudaGetLastError();
 }
 
