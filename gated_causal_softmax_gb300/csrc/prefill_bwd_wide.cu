@@ -85,6 +85,12 @@ __device__ __forceinline__ void wide_role(const CUtensorMap& tmQ, const CUtensor
   const int n_it = i_hi / BM - it_lo + 1;
   const int nsteps = n_it * group;
   const bool sums = (KIND >= 1) && (w0 == 0);  // this role takes the dS column (and row) sums
+  // Role V double-buffers S^T (its dP^T columns are free) when the next step's score operands and
+  // this step's dO chunks fit in the ring together (Dqk = 256: K resident, 4 + 4 chunks of 8), so
+  // that the producer can stage this step's dO while the next scores stream.  At Dqk = 512 the 12
+  // score chunks would push the dO loads behind them and expose their latency (measured 1.6 %
+  // slower there), so that shape keeps the single buffer.
+  constexpr bool DB = KIND == 0 && (2 * C::KCH - C::NRES) + C::WCH <= C::NST;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* full = bars;                 // [NST]
@@ -97,6 +103,12 @@ __device__ __forceinline__ void wide_role(const CUtensorMap& tmQ, const CUtensor
   uint64_t* mma_done = kv_full + 7;
   uint64_t* dq_free = kv_full + 8;
   uint64_t* drain = kv_full + 9;
+  // role V with DB (below): S^T is double-buffered, so the scores of step s + 1
+  // are computed while the key-row warps turn step s into P^T; per buffer b = s & 1 a scores-ready
+  // and a P^T-ready barrier, and one barrier for the accumulator after the last step
+  uint64_t* s_full2 = kv_full + 10;  // [2]
+  uint64_t* p_full2 = kv_full + 12;  // [2]
+  uint64_t* acc_done = kv_full + 14;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   const Abort ab{abort_flag, p.status};
@@ -117,6 +129,11 @@ __device__ __forceinline__ void wide_role(const CUtensorMap& tmQ, const CUtensor
     mbar_init(mma_done, 1);
     mbar_init(dq_free, 4);
     mbar_init(drain, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full2[b], 1);
+      mbar_init(&p_full2[b], 4);
+    }
+    mbar_init(acc_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -149,45 +166,99 @@ __device__ __forceinline__ void wide_role(const CUtensorMap& tmQ, const CUtensor
       for (int c = 0; c < C::NRES; ++c)
         tma_load_3d(smem + C::OFF_KRES + c * kStage, &tmK, kv_full, (res0 + c) * 64, kvh, seq_start + j0);
     }
-    for (int s = 0; s < nsteps && ok; ++s) {
-      const int h = kvh * group + s / n_it;
-      const int i0 = (it_lo + s % n_it) * BM;
-      const int yq = seq_start + i0, yk = seq_start + j0;
-      if (lane == 0) {
-        for (int c = 0; c < C::KCH && ok; ++c) {
-          if (c < res0 || c >= res0 + C::NRES) ok = issue(&tmK, c * 64, kvh, yk, kStage);
-          if (ok) ok = issue(&tmQ, c * 64, h, yq, BM * 128);
-        }
-        if (KIND >= 1) {
-          for (int c = 0; c < C::VCH && ok; ++c) {
-            ok = issue(&tmV, c * 64, kvh, yk, kStage);
-            if (ok) ok = issue(&tmDO, c * 64, h, yq, BM * 128);
+    if constexpr (DB) {
+      // the per-column vectors of step s: (G_i - LSE_i) log2 e and delta_i, into buffer s & 1
+      auto put_vectors = [&](int s) -> bool {
+        const int h = kvh * group + s / n_it;
+        const int i0 = (it_lo + s % n_it) * BM;
+        bool okv = true;
+        if (lane == 0) okv = wait_bar(&vec_empty[s & 1], ((s >> 1) & 1) ^ 1, ab);
+        okv = __shfl_sync(0xffffffffu, okv ? 1 : 0, 0) != 0;
+        if (!okv) return false;
+        float* vec = reinterpret_cast<float*>(smem + C::OFF_VEC) + (s & 1) * 2 * BM;
+  #pragma unroll
+        for (int u = 0; u < BM / 32; ++u) {
+          const int c = lane * (BM / 32) + u;
+          const int i = i0 + c;
+          float colterm = 0.f, dl = 0.f;
+          if (i < len) {
+            const size_t idx = (size_t)h * p.total + seq_start + i;
+            colterm = -__ldg(p.lse + idx) * kLog2e;
+            if (p.gT) colterm += __ldg(p.gT + idx);
+            dl = __ldg(p.delta + idx);
           }
-          for (int c = 0; c < C::WCH && ok; ++c) ok = issue(&tmQ, w0 + c * 64, h, yq, BM * 128);
-        } else {
+          vec[c] = colterm;
+          vec[BM + c] = dl;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&vec_full[s & 1]);
+        return true;
+      };
+      // operands of step s's score MMAs: streamed K chunks and the Q chunks (lane 0)
+      auto put_score_operands = [&](int s) -> bool {
+        const int h = kvh * group + s / n_it;
+        const int yq = seq_start + (it_lo + s % n_it) * BM, yk = seq_start + j0;
+        bool okl = true;
+        if (lane == 0) {
+          for (int c = 0; c < C::KCH && okl; ++c) {
+            if (c < res0 || c >= res0 + C::NRES) okl = issue(&tmK, c * 64, kvh, yk, kStage);
+            if (okl) okl = issue(&tmQ, c * 64, h, yq, BM * 128);
+          }
+        }
+        return __shfl_sync(0xffffffffu, okl ? 1 : 0, 0) != 0;
+      };
+      // consumption order of the MMA warp: S(0), then per step s: S(s + 1), dV(s)
+      if (nsteps > 0) ok = put_score_operands(0) && put_vectors(0);
+      for (int s = 0; s < nsteps && ok; ++s) {
+        if (s + 1 < nsteps) ok = put_score_operands(s + 1) && put_vectors(s + 1);
+        if (!ok) break;
+        const int h = kvh * group + s / n_it;
+        const int yq = seq_start + (it_lo + s % n_it) * BM;
+        if (lane == 0)
           for (int c = 0; c < C::WCH && ok; ++c) ok = issue(&tmDO, w0 + c * 64, h, yq, BM * 128);
-        }
-        if (ok) ok = wait_bar(&vec_empty[s & 1], ((s >> 1) & 1) ^ 1, ab);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       }
-      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-      if (!ok) break;
-      float* vec = reinterpret_cast<float*>(smem + C::OFF_VEC) + (s & 1) * 2 * BM;
-#pragma unroll
-      for (int u = 0; u < BM / 32; ++u) {
-        const int c = lane * (BM / 32) + u;
-        const int i = i0 + c;
-        float colterm = 0.f, dl = 0.f;
-        if (i < len) {
-          const size_t idx = (size_t)h * p.total + seq_start + i;
-          colterm = -__ldg(p.lse + idx) * kLog2e;
-          if (p.gT) colterm += __ldg(p.gT + idx);
-          dl = __ldg(p.delta + idx);
+    } else {
+      for (int s = 0; s < nsteps && ok; ++s) {
+        const int h = kvh * group + s / n_it;
+        const int i0 = (it_lo + s % n_it) * BM;
+        const int yq = seq_start + i0, yk = seq_start + j0;
+        if (lane == 0) {
+          for (int c = 0; c < C::KCH && ok; ++c) {
+            if (c < res0 || c >= res0 + C::NRES) ok = issue(&tmK, c * 64, kvh, yk, kStage);
+            if (ok) ok = issue(&tmQ, c * 64, h, yq, BM * 128);
+          }
+          if (KIND >= 1) {
+            for (int c = 0; c < C::VCH && ok; ++c) {
+              ok = issue(&tmV, c * 64, kvh, yk, kStage);
+              if (ok) ok = issue(&tmDO, c * 64, h, yq, BM * 128);
+            }
+            for (int c = 0; c < C::WCH && ok; ++c) ok = issue(&tmQ, w0 + c * 64, h, yq, BM * 128);
+          } else {
+            for (int c = 0; c < C::WCH && ok; ++c) ok = issue(&tmDO, w0 + c * 64, h, yq, BM * 128);
+          }
+          if (ok) ok = wait_bar(&vec_empty[s & 1], ((s >> 1) & 1) ^ 1, ab);
         }
-        vec[c] = colterm;
-        vec[BM + c] = dl;
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        float* vec = reinterpret_cast<float*>(smem + C::OFF_VEC) + (s & 1) * 2 * BM;
+  #pragma unroll
+        for (int u = 0; u < BM / 32; ++u) {
+          const int c = lane * (BM / 32) + u;
+          const int i = i0 + c;
+          float colterm = 0.f, dl = 0.f;
+          if (i < len) {
+            const size_t idx = (size_t)h * p.total + seq_start + i;
+            colterm = -__ldg(p.lse + idx) * kLog2e;
+            if (p.gT) colterm += __ldg(p.gT + idx);
+            dl = __ldg(p.delta + idx);
+          }
+          vec[c] = colterm;
+          vec[BM + c] = dl;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&vec_full[s & 1]);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&vec_full[s & 1]);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -216,87 +287,152 @@ __device__ __forceinline__ void wide_role(const CUtensorMap& tmQ, const CUtensor
         advance();
       };
       bool ok = wait_bar(kv_full, 0, ab);
-      for (int s = 0; s < nsteps && ok; ++s) {
-        // S^T = K Q^T over all of DQK (K chunk resident or streamed, Q chunk streamed)
-        for (int c = 0; c < C::KCH && ok; ++c) {
-          uint32_t a = 0, bq = 0;
-          int kst = -1;
-          if (c >= res0 && c < res0 + C::NRES) {
-            a = sRes + (c - res0) * kStage;
-          } else {
-            ok = take(a);
-            if (!ok) break;
-            kst = stage;
-            advance();
-          }
-          ok = take(bq);
-          if (!ok) break;
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mma_ss(tmem + C::T_S, sdesc_sw128(a + k * 32, 16, 1024), sdesc_sw128(bq + k * 32, 16, 1024), idS,
-                   (c | k) != 0);
-          if (kst >= 0) mma_commit(&empty[kst]);
-          give();
-        }
-        if (!ok) break;
-        if (KIND >= 1) {
-          // dP^T = V dO^T over all of DV
-          for (int c = 0; c < C::VCH && ok; ++c) {
+      if constexpr (DB) {
+        // S^T = K Q^T over all of DQK (K chunk resident or streamed, Q chunk streamed) into the
+        // columns at t_s
+        auto scores = [&](uint32_t t_s) -> bool {
+          for (int c = 0; c < C::KCH; ++c) {
             uint32_t a = 0, bq = 0;
-            ok = take(a);
+            int kst = -1;
+            if (c >= res0 && c < res0 + C::NRES) {
+              a = sRes + (c - res0) * kStage;
+            } else {
+              if (!take(a)) return false;
+              kst = stage;
+              advance();
+            }
+            if (!take(bq)) return false;
+  #pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_ss(tmem + t_s, sdesc_sw128(a + k * 32, 16, 1024), sdesc_sw128(bq + k * 32, 16, 1024), idS,
+                     (c | k) != 0);
+            if (kst >= 0) mma_commit(&empty[kst]);
+            give();
+          }
+          return true;
+        };
+        // accumulator += A x (dO or Q chunks): a pair of 64-column chunks in adjacent ring stages as
+        // one N = 128 MMA (LBO = one stage; an N = 64 MMA costs nearly as much as an N = 128 one), a
+        // lone chunk with N = 64
+        auto accumulate = [&](uint32_t aT, bool first) -> bool {
+          for (int c = 0; c < C::WCH;) {
+            const bool pair = c + 1 < C::WCH && stage + 1 < C::NST;
+            uint32_t bq = 0;
+            if (!take(bq)) return false;
+            if (pair && !wait_bar(&full[stage + 1], phase, ab)) return false;
+            tc_fence_after();
+  #pragma unroll
+            for (int k = 0; k < BM / 16; ++k)
+              mma_ts(tmem + C::T_ACC + c * 64, aT + k * 8, sdesc_sw128(bq + k * 2048, kStage, 1024),
+                     pair ? idAcc2 : idAcc, (!first || k > 0) ? 1u : 0u);
+            give();
+            if (pair) give();
+            c += pair ? 2 : 1;
+          }
+          return true;
+        };
+        // S(0); then per step s: S(s + 1) into the other buffer, wait for P^T(s), dV(s).  MMAs run
+        // in issue order, so S(s + 2) (issued after dV(s)) overwrites buffer s & 1 only after dV(s)
+        // has read P^T(s) there.
+        if (ok && nsteps > 0) {
+          ok = scores(C::T_S);
+          if (ok) mma_commit(&s_full2[0]);
+        }
+        for (int s = 0; s < nsteps && ok; ++s) {
+          if (s + 1 < nsteps) {
+            ok = scores(C::T_S + ((s + 1) & 1) * BM);
             if (!ok) break;
-            const int vst = stage;
-            advance();
+            mma_commit(&s_full2[(s + 1) & 1]);
+          }
+          ok = wait_bar(&p_full2[s & 1], (s >> 1) & 1, ab);
+          if (!ok) break;
+          tc_fence_after();
+          ok = accumulate(tmem + C::T_S + (s & 1) * BM, s == 0);
+        }
+        if (ok && nsteps > 0) mma_commit(acc_done);
+      } else {
+        for (int s = 0; s < nsteps && ok; ++s) {
+          // S^T = K Q^T over all of DQK (K chunk resident or streamed, Q chunk streamed)
+          for (int c = 0; c < C::KCH && ok; ++c) {
+            uint32_t a = 0, bq = 0;
+            int kst = -1;
+            if (c >= res0 && c < res0 + C::NRES) {
+              a = sRes + (c - res0) * kStage;
+            } else {
+              ok = take(a);
+              if (!ok) break;
+              kst = stage;
+              advance();
+            }
             ok = take(bq);
             if (!ok) break;
-#pragma unroll
+  #pragma unroll
             for (int k = 0; k < 4; ++k)
-              mma_ss(tmem + C::T_DP, sdesc_sw128(a + k * 32, 16, 1024), sdesc_sw128(bq + k * 32, 16, 1024), idS,
+              mma_ss(tmem + C::T_S, sdesc_sw128(a + k * 32, 16, 1024), sdesc_sw128(bq + k * 32, 16, 1024), idS,
                      (c | k) != 0);
-            mma_commit(&empty[vst]);
+            if (kst >= 0) mma_commit(&empty[kst]);
             give();
           }
           if (!ok) break;
-        }
-        mma_commit(s_full);
-        ok = wait_bar(p_full, s & 1, ab);
-        if (!ok) break;
-        tc_fence_after();
-        // accumulator += (P^T or dS^T) x (dO or Q): a pair of 64-column chunks in adjacent ring
-        // stages as one N = 128 MMA (LBO = one stage; an N = 64 MMA costs nearly as much as an
-        // N = 128 one), a lone chunk with N = 64
-        const uint32_t aT = tmem + (KIND >= 1 ? C::T_DP : C::T_S);
-        for (int c = 0; c < C::WCH && ok;) {
-          const bool pair = c + 1 < C::WCH && stage + 1 < C::NST;
-          uint32_t bq = 0;
-          ok = take(bq);
-          if (ok && pair) ok = wait_bar(&full[stage + 1], phase, ab);
+          if (KIND >= 1) {
+            // dP^T = V dO^T over all of DV
+            for (int c = 0; c < C::VCH && ok; ++c) {
+              uint32_t a = 0, bq = 0;
+              ok = take(a);
+              if (!ok) break;
+              const int vst = stage;
+              advance();
+              ok = take(bq);
+              if (!ok) break;
+  #pragma unroll
+              for (int k = 0; k < 4; ++k)
+                mma_ss(tmem + C::T_DP, sdesc_sw128(a + k * 32, 16, 1024), sdesc_sw128(bq + k * 32, 16, 1024), idS,
+                       (c | k) != 0);
+              mma_commit(&empty[vst]);
+              give();
+            }
+            if (!ok) break;
+          }
+          mma_commit(s_full);
+          ok = wait_bar(p_full, s & 1, ab);
           if (!ok) break;
           tc_fence_after();
-#pragma unroll
-          for (int k = 0; k < BM / 16; ++k)
-            mma_ts(tmem + C::T_ACC + c * 64, aT + k * 8, sdesc_sw128(bq + k * 2048, kStage, 1024),
-                   pair ? idAcc2 : idAcc, (s > 0 || k > 0) ? 1u : 0u);
-          give();
-          if (pair) give();
-          c += pair ? 2 : 1;
-        }
-        if (!ok) break;
-        if (KIND == 1) {
-          if (s > 0) {
-            ok = wait_bar(dq_free, (s - 1) & 1, ab);
+          // accumulator += (P^T or dS^T) x (dO or Q): a pair of 64-column chunks in adjacent ring
+          // stages as one N = 128 MMA (LBO = one stage; an N = 64 MMA costs nearly as much as an
+          // N = 128 one), a lone chunk with N = 64
+          const uint32_t aT = tmem + (KIND >= 1 ? C::T_DP : C::T_S);
+          for (int c = 0; c < C::WCH && ok;) {
+            const bool pair = c + 1 < C::WCH && stage + 1 < C::NST;
+            uint32_t bq = 0;
+            ok = take(bq);
+            if (ok && pair) ok = wait_bar(&full[stage + 1], phase, ab);
             if (!ok) break;
             tc_fence_after();
+  #pragma unroll
+            for (int k = 0; k < BM / 16; ++k)
+              mma_ts(tmem + C::T_ACC + c * 64, aT + k * 8, sdesc_sw128(bq + k * 2048, kStage, 1024),
+                     pair ? idAcc2 : idAcc, (s > 0 || k > 0) ? 1u : 0u);
+            give();
+            if (pair) give();
+            c += pair ? 2 : 1;
           }
-          // dQ^T for dims w0 .. w0+255: two M=128 halves from the resident K chunks
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              mma_ss(tmem + C::T_DQ + hf * 64, sdesc_sw128(sRes + 2 * hf * kStage + k * 2048, kStage, 1024),
-                     sdesc_sw128(sDS + k * 2048, kStage, 1024), idDQ, k > 0);
+          if (!ok) break;
+          if (KIND == 1) {
+            if (s > 0) {
+              ok = wait_bar(dq_free, (s - 1) & 1, ab);
+              if (!ok) break;
+              tc_fence_after();
+            }
+            // dQ^T for dims w0 .. w0+255: two M=128 halves from the resident K chunks
+  #pragma unroll
+            for (int hf = 0; hf < 2; ++hf)
+  #pragma unroll
+              for (int k = 0; k < 8; ++k)
+                mma_ss(tmem + C::T_DQ + hf * 64, sdesc_sw128(sRes + 2 * hf * kStage + k * 2048, kStage, 1024),
+                       sdesc_sw128(sDS + k * 2048, kStage, 1024), idDQ, k > 0);
+          }
+          mma_commit(mma_done);
         }
-        mma_commit(mma_done);
       }
       if (!ok) {
         mma_commit(drain);
@@ -329,16 +465,18 @@ __device__ __forceinline__ void wide_role(const CUtensorMap& tmQ, const CUtensor
       }
       ok = wait_bar(&vec_full[s & 1], (s >> 1) & 1, ab);
       if (!ok) break;
-      ok = wait_bar(s_full, s & 1, ab);
+      ok = DB ? wait_bar(&s_full2[s & 1], (s >> 1) & 1, ab) : wait_bar(s_full, s & 1, ab);
       if (!ok) break;
       tc_fence_after();
+      // role V with DB: this step's score buffer
+      const uint32_t tSs = tS + (DB ? (s & 1) * BM : 0);
       const float* vec = reinterpret_cast<const float*>(smem + C::OFF_VEC) + (s & 1) * 2 * BM;
       const bool need_mask = (i0 < j0 + kBN - 1) || (p.window > 0 && i0 + BM - 1 - j0 >= p.window) ||
                              (i0 + BM > len);
 #pragma unroll
       for (int ch = 0; ch < BM / 32; ++ch) {
         uint32_t sv[32], dp[32];
-        tmem_ld32(tS + 32 * ch, sv);
+        tmem_ld32(tSs + 32 * ch, sv);
         if (KIND >= 1) tmem_ld32(tDP + 32 * ch, dp);
         tmem_ld_wait();
 #pragma unroll
@@ -359,7 +497,7 @@ __device__ __forceinline__ void wide_role(const CUtensorMap& tmQ, const CUtensor
 #pragma unroll
           for (int c = 0; c < 16; ++c)
             pk[c] = pack_bf16x2(__uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1]));
-          tmem_st16(tS + 16 * ch, pk);
+          tmem_st16(tSs + 16 * ch, pk);
         } else {
 #pragma unroll
           for (int c = 0; c < 16; ++c)
@@ -402,8 +540,9 @@ __device__ __forceinline__ void wide_role(const CUtensorMap& tmQ, const CUtensor
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&vec_empty[s & 1]);
-        mbar_arrive(p_full);
+        mbar_arrive(DB ? &p_full2[s & 1] : p_full);
       }
+      if (DB) continue;  // the next step's scores are already under way
       ok = wait_bar(mma_done, s & 1, ab);
       if (!ok) break;
       if (KIND == 1) {
@@ -432,6 +571,7 @@ __device__ __forceinline__ void wide_role(const CUtensorMap& tmQ, const CUtensor
     if (ok && sums && cur_h >= 0 && has_gate && jl < len)
       red_add_f32(p.dg_col + (size_t)cur_h * p.total + seq_start + jl, dgcol);
     // ---- epilogue: dV (role V) or scale * dK (role KQ), columns w0 .. w0+255
+    if (ok && nsteps > 0 && DB) ok = wait_bar(acc_done, 0, ab);
     if (ok && nsteps > 0) {
       tc_fence_after();
       const bool row_ok = jl < len;
