@@ -13,7 +13,8 @@
 // of fitting the accumulators in TMEM.  The K-side and dV roles of a call run in one launch.  Operands stream through a ring of 16 KB stages
 // (128 x 64 or 64 x 64 bf16 chunks, 128-B swizzle); the K columns a role keeps using
 // (its own 256 dims) stay resident.  One softmax warpgroup, one thread per key row.
-// Per query step of BM rows (s = step; the pipeline is sequential per step):
+// Per query step of BM rows (s = step; the pipeline is sequential per step, except that role V at
+// Dqk = 256 computes step s + 1's S^T into a second TMEM buffer while step s's P^T is formed):
 //     S^T = K Q^T (TMEM)   [dP^T = V dO^T (TMEM)]   P^T / dS^T in fp32, bf16 operands
 //     role V:  dV  += P^T dO[:, v0..]
 //     role KQ: dK  += dS^T Q[:, k0..];  dQ^T[k0..] = K[:, k0..]^T dS^T -> fp32 reduce-adds
@@ -88,8 +89,8 @@ __device__ __forceinline__ void wide_role(const CUtensorMap& tmQ, const CUtensor
   // Role V double-buffers S^T (its dP^T columns are free) when the next step's score operands and
   // this step's dO chunks fit in the ring together (Dqk = 256: K resident, 4 + 4 chunks of 8), so
   // that the producer can stage this step's dO while the next scores stream.  At Dqk = 512 the 12
-  // score chunks would push the dO loads behind them and expose their latency (measured 1.6 %
-  // slower there), so that shape keeps the single buffer.
+  // score chunks would push the dO loads behind them and expose their latency (a double buffer
+  // there measured slower), so that shape keeps the single buffer.
   constexpr bool DB = KIND == 0 && (2 * C::KCH - C::NRES) + C::WCH <= C::NST;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
