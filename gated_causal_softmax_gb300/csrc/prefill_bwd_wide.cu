@@ -92,6 +92,7 @@ __device__ __forceinline__ void wide_role(const CUtensorMap& tmQ, const CUtensor
   // score chunks would push the dO loads behind them and expose their latency (a double buffer
   // there measured slower), so that shape keeps the single buffer.
   constexpr bool DB = KIND == 0 && (2 * C::KCH - C::NRES) + C::WCH <= C::NST;
+  static_assert(C::KCH > 0 && C::VCH > 0 && C::WCH > 0, "head-dim chunks");
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* full = bars;                 // [NST]
